@@ -1,0 +1,505 @@
+/*
+ * echo_oracle.cpp -- plain CPU oracle for the ECHO per-layer decode hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  The tests, the smoke check and the bench's CPU
+ * baseline leg are the only code that loads this library.  The CUDA library
+ * never includes, links or calls it, and it shares no header, helper, table or
+ * constant with the CUDA sources.  It is written for a reader who checks it
+ * against the sources below by eye: every step is the definition, in fp64
+ * where the step is arithmetic, with no blocking, fusion or reordering.
+ *
+ * Sources (page title, then section):
+ *   [EXPL] "ECHO: Lossless KV Cache Offloading for Sparse Attention LLMs"
+ *          (interactive explainer page), section 2 "The top-k dependency",
+ *          sub-panels "Five fixed-size integer tensors on the GPU",
+ *          "One layer, one step: free -> allocate -> recall",
+ *          "Decode: fetch above a predicted threshold",
+ *          "Prefill: one-round histogram".
+ *   [AE]   "OSDI'26 Artifact Evaluation for ECHO: Efficient KV Cache Offloading
+ *          with Lossless Prefetching for Serving Native Sparse Attention LLMs",
+ *          sections "Download the model" (DeepSeek-V3.2) and "Baselines under
+ *          evaluation" (bounded GPU cache NSA_DEV_CACHE_SIZE).
+ *   [OCP]  OCP 8-bit Floating Point Specification (OFP8), format E4M3.
+ *   [IDX]  The DeepSeek-V3.2 lightning-indexer score this library computes:
+ *          I[s] = sum_h w[h] * ReLU(q[h] . k[s]), 64 heads x 128 dims, FP8
+ *          keys with one fp32 scale per token.
+ *
+ * Readings where the sources are silent are marked READING and listed with
+ * their reasons in the design notes of the repository.
+ *
+ * Return codes of the int-valued functions: 0 ok, 1 bad argument, 2 capacity
+ * (k > C or cache full), 3 NaN/Inf met.
+ *
+ * Build: g++ -O2 -std=c++17 -shared -fPIC -ffp-contract=off -pthread.
+ * -ffp-contract=off matters: the fp32 EMA below must round every product
+ * and sum separately, as written.
+ */
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <set>
+#include <thread>
+#include <vector>
+
+namespace {
+
+constexpr int ORC_OK = 0;
+constexpr int ORC_EINVAL = 1;
+constexpr int ORC_ECAPACITY = 2;
+constexpr int ORC_ENAN = 3;
+
+// ---------------------------------------------------------------------------
+// [OCP] E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits.
+// Exponent field 0 encodes subnormals m/8 * 2^-6; S.1111.111 is NaN; there is
+// no infinity, so the largest finite magnitude is 1.75 * 2^8 = 448.
+// ---------------------------------------------------------------------------
+double e4m3_value(uint8_t code) {
+    const int sign = code >> 7;
+    const int e = (code >> 3) & 0xF;
+    const int m = code & 0x7;
+    if (e == 15 && m == 7) return std::nan("");
+    double mag;
+    if (e == 0)
+        mag = std::ldexp(m / 8.0, -6);
+    else
+        mag = std::ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+// Round-to-nearest-even onto the E4M3 grid, saturating to +-448 (the
+// behaviour of a "satfinite" conversion).  Plain search: the positive codes
+// 0..126 are in ascending order of value, so a binary search finds the two
+// neighbours of |x|; the nearer wins, and an exact tie goes to the even code
+// (the code whose mantissa LSB is 0).
+uint8_t e4m3_round(double x) {
+    if (std::isnan(x)) return 0x7F;
+    const uint8_t sign = std::signbit(x) ? 0x80 : 0x00;
+    const double a = std::fabs(x);
+    if (a >= 448.0) return sign | 0x7E;
+    int lo = 0, hi = 126;  // invariant: value(lo) <= a
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) / 2;
+        if (e4m3_value((uint8_t)mid) <= a)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const double vlo = e4m3_value((uint8_t)lo);
+    if (vlo == a) return sign | (uint8_t)lo;
+    const double vhi = e4m3_value((uint8_t)(lo + 1));
+    const double dlo = a - vlo, dhi = vhi - a;
+    int c;
+    if (dlo < dhi)
+        c = lo;
+    else if (dhi < dlo)
+        c = lo + 1;
+    else
+        c = (lo % 2 == 0) ? lo : lo + 1;
+    return sign | (uint8_t)c;
+}
+
+bool finite_f(float x) { return std::isfinite(x); }
+
+uint32_t f32_bits(float x) {
+    uint32_t u;
+    std::memcpy(&u, &x, 4);
+    return u;
+}
+
+float bits_f32(uint32_t u) {
+    float x;
+    std::memcpy(&x, &u, 4);
+    return x;
+}
+
+// A key on which unsigned comparison orders floats: larger float, larger key.
+// -0 is first made +0 so that the two zeros compare equal (READING: the pages
+// do not say how signed zeros rank; they are equal scores).
+uint32_t order_key(float x) {
+    if (x == 0.0f) x = 0.0f;
+    const uint32_t u = f32_bits(x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ---------------------------------------------------------------------------
+// Query quantisation (READING; the sources say only that the score GEMM runs
+// in FP8): one power-of-two scale per (request, head), the smallest 2^e with
+// amax <= 448 * 2^e, with e held at or above -126 so that 2^e is a normal
+// float; amax == 0 gives scale 1.  Dividing by a power of two is exact, so
+// q / scale is rounded once, onto the E4M3 grid, without saturating.
+// ---------------------------------------------------------------------------
+int q_scale_exponent(float amax) {
+    if (amax == 0.0f) return 0;
+    int e = -126;
+    while ((double)amax > std::ldexp(448.0, e)) ++e;
+    return e;
+}
+
+// ---------------------------------------------------------------------------
+// Exact top-k of one score vector [EXPL "guarantees an exact top-k"]:
+// stable sort of indices by score, descending, so equal scores keep the lower
+// index first; take min(k, n); report them in ascending index order
+// (READING: the output order is not stated), padded with -1.
+// kth = the score of the k-th element of the sorted order, or of the last
+// selected one when n < k (READING).  -INFINITY when n == 0.
+// ---------------------------------------------------------------------------
+int topk_one(const float* scores, int64_t n, int k, int32_t* idx, float* kth) {
+    std::vector<int32_t> order((size_t)n);
+    for (int64_t i = 0; i < n; ++i) {
+        if (std::isnan(scores[i])) return ORC_ENAN;
+        order[(size_t)i] = (int32_t)i;
+    }
+    std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
+        return order_key(scores[a]) > order_key(scores[b]);
+    });
+    const int64_t take = std::min<int64_t>(k, n);
+    std::vector<int32_t> chosen(order.begin(), order.begin() + take);
+    std::sort(chosen.begin(), chosen.end());
+    for (int i = 0; i < k; ++i) idx[i] = (i < take) ? chosen[(size_t)i] : -1;
+    if (take == 0) {
+        *kth = -INFINITY;
+    } else {
+        float v = scores[order[(size_t)(take - 1)]];
+        if (v == 0.0f) v = 0.0f;
+        *kth = v;
+    }
+    return ORC_OK;
+}
+
+// [EXPL "Decode: fetch above a predicted threshold"]: the predicted threshold
+// is an EMA, weight alpha = 0.5, of the previous step's k-th score.
+// theta_next = alpha * kth + (1 - alpha) * theta, each operation rounded in
+// fp32.  READING: the first step has no prediction (theta = +inf, so nothing
+// is fetched early) and the first k-th score replaces it instead of being
+// averaged with +inf.  A request with no tokens (kth = -inf) keeps theta.
+float ema(float theta, float kth, float alpha) {
+    if (std::isinf(kth) && kth < 0) return theta;
+    if (std::isinf(theta)) return kth;
+    const float one_minus = 1.0f - alpha;
+    const float a = alpha * kth;
+    const float b = one_minus * theta;
+    return a + b;
+}
+
+// ---------------------------------------------------------------------------
+// One segment's GPU cache, held as the ordered containers the definition
+// talks about: a token -> slot map and the set of free slots.
+// ---------------------------------------------------------------------------
+struct Cache {
+    std::map<int32_t, int32_t> resident;  // token -> slot
+    std::set<int32_t> free_slots;         // ascending
+};
+
+Cache load_cache(int64_t n, int C, const int32_t* tok2slot, const int32_t* slot2tok) {
+    Cache c;
+    for (int64_t s = 0; s < n; ++s)
+        if (tok2slot[s] >= 0) c.resident[(int32_t)s] = tok2slot[s];
+    for (int j = 0; j < C; ++j)
+        if (slot2tok[j] < 0) c.free_slots.insert(j);
+    return c;
+}
+
+void store_cache(const Cache& c, int64_t n, int C, int32_t* tok2slot, int32_t* slot2tok) {
+    for (int64_t s = 0; s < n; ++s) tok2slot[s] = -1;
+    for (int j = 0; j < C; ++j) slot2tok[j] = -1;
+    for (const auto& kv : c.resident) {
+        tok2slot[kv.first] = kv.second;
+        slot2tok[kv.second] = kv.first;
+    }
+}
+
+// Slot tables must be mutual inverses; anything else is a bad argument.
+bool cache_consistent(int64_t n, int C, const int32_t* tok2slot, const int32_t* slot2tok) {
+    for (int64_t s = 0; s < n; ++s) {
+        const int32_t j = tok2slot[s];
+        if (j < -1 || j >= C) return false;
+        if (j >= 0 && slot2tok[j] != s) return false;
+    }
+    for (int j = 0; j < C; ++j) {
+        const int32_t s = slot2tok[j];
+        if (s < -1 || s >= n) return false;
+        if (s >= 0 && tok2slot[s] != j) return false;
+    }
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+// ---- [OCP] E4M3 codec -----------------------------------------------------
+double orc_e4m3_decode(uint8_t code) { return e4m3_value(code); }
+uint8_t orc_e4m3_encode(double x) { return e4m3_round(x); }
+
+void orc_e4m3_encode_f32(const float* x, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_round((double)x[i]);
+}
+
+uint32_t orc_order_key(float x) { return order_key(x); }
+
+// ---- query quantisation (READING above) -----------------------------------
+// q [B,H,D] f32, w [B,H] f32 -> q8 [B,H,D] E4M3 bytes, qscale [B,H] f32 (the
+// power of two), wfold [B,H] f32 = w * qscale rounded in fp32 (what a scaled
+// kernel multiplies by; the oracle's score below does not use it).
+int orc_quantize_q(const float* q, const float* w, int B, int H, int D, uint8_t* q8,
+                   float* qscale, float* wfold) {
+    if (B < 0 || H <= 0 || D <= 0) return ORC_EINVAL;
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h) {
+            const float* row = q + ((int64_t)b * H + h) * D;
+            float amax = 0.0f;
+            for (int d = 0; d < D; ++d) {
+                if (!finite_f(row[d])) return ORC_ENAN;
+                amax = std::max(amax, std::fabs(row[d]));
+            }
+            if (!finite_f(w[(int64_t)b * H + h])) return ORC_ENAN;
+            const int e = q_scale_exponent(amax);
+            const double scale = std::ldexp(1.0, e);
+            for (int d = 0; d < D; ++d)
+                q8[((int64_t)b * H + h) * D + d] = e4m3_round((double)row[d] / scale);
+            qscale[(int64_t)b * H + h] = (float)scale;
+            wfold[(int64_t)b * H + h] = (float)((double)w[(int64_t)b * H + h] * scale);
+        }
+    return ORC_OK;
+}
+
+// ---- [IDX] indexer score, fp64, direct form ------------------------------
+// out[s] = sum_h w[h] * max(0, sum_d (dec(q8[h,d]) * qscale[h]) * (dec(k8[s,d]) * ks[s]))
+// absb[s] = sum_h |w[h]| * sum_d |dec(q8[h,d]) * qscale[h] * dec(k8[s,d]) * ks[s]|,
+// the size of the terms, which bounds the rounding a reordered sum may make.
+// Tokens are the rows tok[0..n) of k8 [*,D] and ks; tok == NULL means 0..n-1.
+void orc_scores(const uint8_t* q8, const float* qscale, const float* w, int H, int D,
+                const uint8_t* k8, const float* ks, const int64_t* tok, int64_t n,
+                double* out, double* absb) {
+    std::vector<double> qv((size_t)H * D);
+    for (int h = 0; h < H; ++h)
+        for (int d = 0; d < D; ++d)
+            qv[(size_t)h * D + d] = e4m3_value(q8[(int64_t)h * D + d]) * (double)qscale[h];
+    std::vector<double> kv((size_t)D);
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t s = tok ? tok[i] : i;
+        for (int d = 0; d < D; ++d) kv[(size_t)d] = e4m3_value(k8[s * D + d]) * (double)ks[s];
+        double total = 0.0, bound = 0.0;
+        for (int h = 0; h < H; ++h) {
+            double dot = 0.0, dabs = 0.0;
+            for (int d = 0; d < D; ++d) {
+                const double p = qv[(size_t)h * D + d] * kv[(size_t)d];
+                dot += p;
+                dabs += std::fabs(p);
+            }
+            total += (double)w[h] * std::max(0.0, dot);
+            bound += std::fabs((double)w[h]) * dabs;
+        }
+        out[i] = total;
+        if (absb) absb[i] = bound;
+    }
+}
+
+// ---- [EXPL "Prefill: one-round histogram"] --------------------------------
+// 256 bins over the top 8 bits of each score shifted by the predicted
+// threshold: bin = order_key(fp32(score - shift)) >> 24, one fp32 subtraction
+// rounded to nearest.  shift is the threshold when it is finite, else 0
+// (READING: with no prediction yet the scores are binned unshifted).
+void orc_hist256(const float* scores, int64_t n, float theta, uint32_t* hist) {
+    const float shift = std::isfinite(theta) ? theta : 0.0f;
+    for (int i = 0; i < 256; ++i) hist[i] = 0;
+    for (int64_t s = 0; s < n; ++s) {
+        float x = scores[s];
+        if (x == 0.0f) x = 0.0f;
+        const float d = x - shift;
+        hist[order_key(d) >> 24] += 1;
+    }
+}
+
+// ---- exact top-k ----------------------------------------------------------
+int orc_topk(const float* scores, int64_t n, int k, int32_t* idx, float* kth) {
+    if (n < 0 || k <= 0) return ORC_EINVAL;
+    return topk_one(scores, n, k, idx, kth);
+}
+
+float orc_ema(float theta, float kth, float alpha) { return ema(theta, kth, alpha); }
+
+// ---- [EXPL "Decode: fetch above a predicted threshold"] -------------------
+// Before top-k is known, tokens that score strictly above the predicted
+// threshold and are not resident are fetched early (READING: strict ">").
+// They are taken in ascending token order, at most min(cap, F) of them, F the
+// number of free slots when the step starts (READING: the page's early-fetch
+// cap value did not survive; cap < 0 means "no cap beyond F").  They get the
+// lowest free slots, in ascending order, and become resident at once.
+// Outputs: early_tok / early_slot [count], *count.
+int orc_early_fetch(int64_t n, int C, const float* scores, float theta, int cap,
+                    int32_t* tok2slot, int32_t* slot2tok, int32_t* early_tok,
+                    int32_t* early_slot, int32_t* count) {
+    if (!cache_consistent(n, C, tok2slot, slot2tok)) return ORC_EINVAL;
+    Cache c = load_cache(n, C, tok2slot, slot2tok);
+    const int64_t F = (int64_t)c.free_slots.size();
+    const int64_t limit = (cap < 0) ? F : std::min<int64_t>(cap, F);
+    int32_t got = 0;
+    for (int64_t s = 0; s < n && got < limit; ++s) {
+        if (!(scores[s] > theta)) continue;
+        if (c.resident.count((int32_t)s)) continue;
+        const int32_t slot = *c.free_slots.begin();
+        c.free_slots.erase(c.free_slots.begin());
+        c.resident[(int32_t)s] = slot;
+        early_tok[got] = (int32_t)s;
+        early_slot[got] = slot;
+        ++got;
+    }
+    *count = got;
+    store_cache(c, n, C, tok2slot, slot2tok);
+    return ORC_OK;
+}
+
+// ---- [EXPL "One layer, one step: free -> allocate -> recall"] -------------
+// sel [m] is the step's selection in ascending token order, -1 padded.
+// 1. Free every resident token that is not selected: both table entries go
+//    to -1; the KV bytes stay where they are and nothing is written back to
+//    the host, which holds every token.
+// 2. The selected tokens that are not resident are the misses; in ascending
+//    token order each takes the lowest free slot, in ascending order.
+// 3. sel_slot[i] = slot of sel[i] (-1 for padding).
+// Outputs: miss_tok / miss_slot [*nmiss], *nfreed.  Capacity: the number of
+// selected tokens must not exceed C (return 2, state untouched).
+int orc_cache_step(int64_t n, int C, int32_t* tok2slot, int32_t* slot2tok, const int32_t* sel,
+                   int m, int32_t* sel_slot, int32_t* miss_tok, int32_t* miss_slot,
+                   int32_t* nmiss, int32_t* nfreed) {
+    if (!cache_consistent(n, C, tok2slot, slot2tok)) return ORC_EINVAL;
+    std::set<int32_t> selected;
+    for (int i = 0; i < m; ++i) {
+        if (sel[i] < 0) continue;
+        if (sel[i] >= n) return ORC_EINVAL;
+        selected.insert(sel[i]);
+    }
+    if ((int64_t)selected.size() > C) return ORC_ECAPACITY;
+    Cache c = load_cache(n, C, tok2slot, slot2tok);
+    // 1. free
+    int32_t freed = 0;
+    for (auto it = c.resident.begin(); it != c.resident.end();) {
+        if (!selected.count(it->first)) {
+            c.free_slots.insert(it->second);
+            it = c.resident.erase(it);
+            ++freed;
+        } else {
+            ++it;
+        }
+    }
+    // 2. allocate, misses in ascending token order (std::set is ordered)
+    int32_t got = 0;
+    for (int32_t s : selected) {
+        if (c.resident.count(s)) continue;
+        const int32_t slot = *c.free_slots.begin();
+        c.free_slots.erase(c.free_slots.begin());
+        c.resident[s] = slot;
+        miss_tok[got] = s;
+        miss_slot[got] = slot;
+        ++got;
+    }
+    // 3. slot of every selected entry
+    for (int i = 0; i < m; ++i) sel_slot[i] = (sel[i] < 0) ? -1 : c.resident.at(sel[i]);
+    *nmiss = got;
+    *nfreed = freed;
+    store_cache(c, n, C, tok2slot, slot2tok);
+    return ORC_OK;
+}
+
+// ---- recall: the device copy of a row is the host row, byte for byte ------
+void orc_recall(const uint8_t* host_rows, int64_t row_bytes, const int32_t* tok,
+                const int32_t* slot, int32_t count, uint8_t* dev_rows) {
+    for (int32_t i = 0; i < count; ++i)
+        std::memcpy(dev_rows + (int64_t)slot[i] * row_bytes, host_rows + (int64_t)tok[i] * row_bytes,
+                    (size_t)row_bytes);
+}
+
+// ---- [EXPL "Prefill: one-round histogram"] chunked-prefill block ----------
+// Rows r = 0..R-1 of one query block sit at absolute positions p = row0 + r
+// and see the causal prefix [0, p] (READING: the row's own token included).
+// scores [R, W] (row stride W >= row0 + R) are the per-row scores; only
+// entries [0, p] of row r are read.  Per row: exact top-k over [0, p]
+// (everything when p + 1 <= k), ascending, -1 padded into sel [R, k], kth[r].
+// hist [R, 256] (optional) is the per-row histogram of the shifted scores.
+// union_mask [row0 + R] is set to 1 for every token selected by some row.
+int orc_prefill_rows(const float* scores, int64_t W, int R, int64_t row0, int k, float theta,
+                     int32_t* sel, float* kth, uint32_t* hist, uint8_t* union_mask) {
+    if (R < 0 || row0 < 0 || k <= 0 || W < row0 + R) return ORC_EINVAL;
+    std::memset(union_mask, 0, (size_t)(row0 + R));
+    for (int r = 0; r < R; ++r) {
+        const int64_t p = row0 + r;
+        const float* row = scores + (int64_t)r * W;
+        const int rc = topk_one(row, p + 1, k, sel + (int64_t)r * k, kth + r);
+        if (rc) return rc;
+        if (hist) orc_hist256(row, p + 1, theta, hist + (int64_t)r * 256);
+        for (int i = 0; i < k; ++i)
+            if (sel[(int64_t)r * k + i] >= 0) union_mask[sel[(int64_t)r * k + i]] = 1;
+    }
+    return ORC_OK;
+}
+
+// ---- one whole decode step of one layer, for the CPU baseline ------------
+// Everything the GPU path does for B requests of one layer, in order, with
+// the oracle's own fp64 scores rounded to fp32 feeding selection:
+// quantise q, score, early fetch above theta (if predictor), exact top-k,
+// EMA, cache step, recall of early and late misses.  Requests are split over
+// nthreads std::threads.  State arrays are updated in place.
+// tok_off [B+1]; q [B,H,D]; w [B,H]; k8 [tok_off[B], D]; ks; theta [B];
+// tok2slot [tok_off[B]] (request-local slot); slot2tok [B*C] (request-local
+// token); host_rows [tok_off[B], row_bytes]; dev_rows [B*C, row_bytes];
+// sel_idx / sel_slot [B,k]; kth [B]; nmiss [B]; scores_out [tok_off[B]] or NULL.
+int orc_decode_step(int B, const int64_t* tok_off, const float* q, const float* w, int H, int D,
+                    const uint8_t* k8, const float* ks, int k, float alpha, int predictor, int cap,
+                    float* theta, int C, int32_t* tok2slot, int32_t* slot2tok,
+                    const uint8_t* host_rows, int64_t row_bytes, uint8_t* dev_rows,
+                    int32_t* sel_idx, int32_t* sel_slot, float* kth, int32_t* nmiss,
+                    float* scores_out, int nthreads) {
+    if (B <= 0 || H <= 0 || D <= 0 || k <= 0 || k > C) return B <= 0 ? ORC_EINVAL : ORC_ECAPACITY;
+    std::vector<int> rcs((size_t)B, ORC_OK);
+    auto one = [&](int b) {
+        const int64_t off = tok_off[b];
+        const int64_t n = tok_off[b + 1] - off;
+        std::vector<uint8_t> q8((size_t)H * D);
+        std::vector<float> qs((size_t)H), wf((size_t)H);
+        int rc = orc_quantize_q(q + (int64_t)b * H * D, w + (int64_t)b * H, 1, H, D, q8.data(),
+                                qs.data(), wf.data());
+        if (rc) { rcs[(size_t)b] = rc; return; }
+        std::vector<double> sd((size_t)n);
+        orc_scores(q8.data(), qs.data(), w + (int64_t)b * H, H, D, k8 + off * D, ks + off, nullptr,
+                   n, sd.data(), nullptr);
+        std::vector<float> sf((size_t)n);
+        for (int64_t s = 0; s < n; ++s) sf[(size_t)s] = (float)sd[(size_t)s];
+        if (scores_out) std::memcpy(scores_out + off, sf.data(), (size_t)n * 4);
+        int32_t* t2s = tok2slot + off;
+        int32_t* s2t = slot2tok + (int64_t)b * C;
+        uint8_t* drows = dev_rows + (int64_t)b * C * row_bytes;
+        const uint8_t* hrows = host_rows + off * row_bytes;
+        std::vector<int32_t> et((size_t)C), es((size_t)C);
+        int32_t ne = 0;
+        if (predictor) {
+            rc = orc_early_fetch(n, C, sf.data(), theta[b], cap, t2s, s2t, et.data(), es.data(), &ne);
+            if (rc) { rcs[(size_t)b] = rc; return; }
+            orc_recall(hrows, row_bytes, et.data(), es.data(), ne, drows);
+        }
+        rc = topk_one(sf.data(), n, k, sel_idx + (int64_t)b * k, kth + b);
+        if (rc) { rcs[(size_t)b] = rc; return; }
+        theta[b] = ema(theta[b], kth[b], alpha);
+        std::vector<int32_t> mt((size_t)k), ms((size_t)k);
+        int32_t nm = 0, nf = 0;
+        rc = orc_cache_step(n, C, t2s, s2t, sel_idx + (int64_t)b * k, k, sel_slot + (int64_t)b * k,
+                            mt.data(), ms.data(), &nm, &nf);
+        if (rc) { rcs[(size_t)b] = rc; return; }
+        orc_recall(hrows, row_bytes, mt.data(), ms.data(), nm, drows);
+        nmiss[b] = nm;
+    };
+    const int T = std::max(1, std::min(nthreads, B));
+    std::vector<std::thread> pool;
+    for (int t = 0; t < T; ++t)
+        pool.emplace_back([&, t]() {
+            for (int b = t; b < B; b += T) one(b);
+        });
+    for (auto& th : pool) th.join();
+    for (int b = 0; b < B; ++b)
+        if (rcs[(size_t)b]) return rcs[(size_t)b];
+    return ORC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,166 @@
+"""Seeded synthetic inputs shaped like the ECHO evaluation workloads.
+
+This module only draws random numbers and lays them out; it holds none of the
+method's arithmetic.  Both the CUDA path and the CPU oracle consume the bytes
+it produces.  Keys are stored the way a DeepSeek-V3.2 index cache stores them
+(E4M3 bytes with one fp32 scale per token); the cast to E4M3 is torch's own
+``float8_e4m3fn`` conversion, a library routine shared with neither side.
+
+Workloads (all seeded, seed 0 unless stated):
+  tiny     1 request x 8192 tokens, 1 layer, k=256, 1024 slots, 16 steps
+  batch    8 x 32768, 1 layer, k=2048, 4096 slots/request, 64 steps
+  v32      32 x 131072, 4 layers (independent keys and pools), k=2048,
+           8192 slots/request/layer, 5% hot tokens (+2.0 before quantising), 128 steps
+  prefill  1 x 102400-token prompt, 2048-row query blocks, k=2048 per row, 260000 slots
+  skewed   64 requests, lengths log-uniform in [4096, 262144], 2 layers, k=2048,
+           2560 slots/request, queries re-drawn every 8 steps, 96 steps
+Queries q ~ N(0,1) [64,128] fp32 drift as q_t = 0.9 q_{t-1} + 0.44 eps_t; head
+weights w ~ U(0,1); host KV rows are 576 bf16 values ~ N(0,1) (1152 bytes).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+H = 64          # index heads
+D = 128         # index head dim
+KV_DIM = 576    # bf16 values per KV row
+ROW_BYTES = KV_DIM * 2
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int                      # requests
+    L: int                      # layers (independent keys, pools and caches)
+    lengths: tuple              # tokens per request
+    k: int
+    C: int                      # GPU slots per request per layer
+    steps: int
+    drift: str = "ar"           # "ar": AR(0.9) every step; "redraw8": i.i.d. redraw every 8 steps
+    hot_frac: float = 0.0
+    hot_offset: float = 0.0
+    predictor: bool = True
+    prefill_block: int = 0      # > 0: chunked prefill with this many rows per block
+    seed: int = 0
+
+    @property
+    def total_tokens(self) -> int:
+        return int(sum(self.lengths))
+
+
+def _skewed_lengths(B: int, seed: int) -> tuple:
+    rng = np.random.default_rng(seed * 1000003 + 4)
+    u = rng.uniform(math.log(4096), math.log(262144), size=B)
+    return tuple(int(round(math.exp(x))) for x in u)
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 1, 1, (8192,), 256, 1024, 16),
+    "batch": Workload("batch", 8, 1, (32768,) * 8, 2048, 4096, 64),
+    "v32": Workload("v32", 32, 4, (131072,) * 32, 2048, 8192, 128, hot_frac=0.05, hot_offset=2.0),
+    "prefill": Workload("prefill", 1, 1, (102400,), 2048, 260000, 50, prefill_block=2048),
+    "skewed": Workload("skewed", 64, 2, _skewed_lengths(64, 0), 2048, 2560, 96, drift="redraw8"),
+}
+
+
+def scaled(w: Workload, name: str, **kw) -> Workload:
+    """A copy of a workload with some fields replaced (smaller parity cases)."""
+    d = dict(w.__dict__)
+    d.update(kw)
+    d["name"] = name
+    return Workload(**d)
+
+
+def _gen(device, seed: int, stream: int) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed * 1000003 + stream)
+    return g
+
+
+def tok_offsets(lengths) -> np.ndarray:
+    off = np.zeros(len(lengths) + 1, np.int64)
+    off[1:] = np.cumsum(np.asarray(lengths, np.int64))
+    return off
+
+
+def make_keys(w: Workload, layer: int, device="cpu"):
+    """E4M3 index keys [sum N, 128] (uint8) and per-token fp32 scales [sum N] of one layer.
+
+    Each key row ~ N(0,1) (plus hot_offset on a hot subset of hot_frac of each
+    request's tokens, drawn uniformly without replacement), then stored as
+    E4M3 bytes with scale amax/448 per token."""
+    rows = []
+    scales = []
+    for b, n in enumerate(w.lengths):
+        g = _gen(device, w.seed, 10_000 + 1000 * layer + b)
+        kf = torch.randn((n, D), generator=g, device=device, dtype=torch.float32)
+        if w.hot_frac > 0:
+            nh = int(round(w.hot_frac * n))
+            perm = torch.randperm(n, generator=g, device=device)[:nh]
+            kf[perm] += w.hot_offset
+        amax = kf.abs().amax(dim=1)
+        amax = torch.where(amax > 0, amax, torch.ones_like(amax))
+        s = amax / 448.0
+        k8 = (kf / s[:, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+        rows.append(k8)
+        scales.append(s)
+    return torch.cat(rows, 0).contiguous(), torch.cat(scales, 0).contiguous()
+
+
+def make_weights(w: Workload, layer: int, device="cpu") -> torch.Tensor:
+    """Per-head weights w ~ U(0,1), [B, 64] fp32."""
+    g = _gen(device, w.seed, 20_000 + layer)
+    return torch.rand((w.B, H), generator=g, device=device, dtype=torch.float32)
+
+
+class QueryStream:
+    """Index queries [B, 64, 128] fp32 of one layer, step after step."""
+
+    def __init__(self, w: Workload, layer: int, device="cpu"):
+        self.w = w
+        self.g = _gen(device, w.seed, 30_000 + layer)
+        self.device = device
+        self.t = 0
+        self.q = torch.randn((w.B, H, D), generator=self.g, device=device, dtype=torch.float32)
+
+    def next(self) -> torch.Tensor:
+        """The query of the current step; advances the stream."""
+        out = self.q.clone()
+        self.t += 1
+        eps = torch.randn(self.q.shape, generator=self.g, device=self.device, dtype=torch.float32)
+        if self.w.drift == "redraw8" and self.t % 8 == 0:
+            self.q = eps
+        else:
+            self.q = 0.9 * self.q + 0.44 * eps
+        return out
+
+
+def make_host_pool(w: Workload, layer: int, device="cpu", pin: bool = False) -> torch.Tensor:
+    """Host KV pool [sum N, 576] bf16 ~ N(0,1) of one layer (pinned when pin=True).
+
+    With device='cuda' the values are drawn on the GPU and copied to host memory."""
+    g = _gen(device, w.seed, 40_000 + layer)
+    n = w.total_tokens
+    if pin:
+        out = torch.empty((n, KV_DIM), dtype=torch.bfloat16, pin_memory=True)
+    else:
+        out = torch.empty((n, KV_DIM), dtype=torch.bfloat16)
+    chunk = 1 << 16
+    for r0 in range(0, n, chunk):
+        r1 = min(n, r0 + chunk)
+        out[r0:r1].copy_(torch.randn((r1 - r0, KV_DIM), generator=g, device=device,
+                                     dtype=torch.float32).to(torch.bfloat16))
+    return out
+
+
+def make_prefill_queries(w: Workload, block: int, device="cpu"):
+    """Queries [R, 64, 128] fp32 (i.i.d. N(0,1) per row) and weights [R, 64] U(0,1) of one block."""
+    R = min(w.prefill_block, w.total_tokens - block * w.prefill_block)
+    g = _gen(device, w.seed, 50_000 + block)
+    q = torch.randn((R, H, D), generator=g, device=device, dtype=torch.float32)
+    wt = torch.rand((R, H), generator=g, device=device, dtype=torch.float32)
+    return q, wt
