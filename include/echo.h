@@ -1,0 +1,214 @@
+/*
+ * echo.h -- C ABI of libecho, the GB300 (sm_103a) decode hot path of ECHO,
+ * lossless KV-cache offloading for sparse-attention LLMs.
+ *
+ * Per layer and decode step the path computes, for a batch of B requests:
+ *   1. the indexer score of every context token (echo_quantize_q,
+ *      echo_index_scores),
+ *   2. the exact top-k tokens and the EMA threshold prediction
+ *      (echo_topk_select), with tokens above the prediction fetched early,
+ *   3. the GPU-cache step: free unselected slots, allocate slots for the
+ *      misses, recall the missing KV rows from the host pool (echo_cache_step).
+ *
+ * Sources (page title, then section):
+ *   [EXPL] "ECHO: Lossless KV Cache Offloading for Sparse Attention LLMs",
+ *          section 2 "The top-k dependency" and its panels.
+ *   [AE]   "OSDI'26 Artifact Evaluation for ECHO: Efficient KV Cache Offloading
+ *          with Lossless Prefetching for Serving Native Sparse Attention LLMs",
+ *          sections "Download the model", "Baselines under evaluation",
+ *          "Fused Prefetch Kernels (ECHO only)".
+ *   [IDX]  The DeepSeek-V3.2 lightning-indexer score computed here:
+ *          I[s] = sum_h w[h] * ReLU(q[h] . k[s]), 64 heads x 128 dims, keys
+ *          stored as E4M3 bytes with one fp32 scale per token.
+ *
+ * Conventions shared by every call
+ *   - Pointers are DEVICE pointers owned by the caller unless stated.  The
+ *     library allocates nothing, keeps no state between calls, never
+ *     synchronises the device and never reads device memory from the host;
+ *     every call only enqueues work on the given stream(s), so a whole decode
+ *     step can be captured into one CUDA graph.
+ *   - Requests are ragged (CSR): tok_off[B+1] (int64, device, non-decreasing,
+ *     tok_off[0] = 0, tok_off[B] <= n_tokens) gives request b the token rows
+ *     [tok_off[b], tok_off[b+1]) of every per-token array.  Token indices in
+ *     selections and slot tables are request-local (0 .. N_b - 1).
+ *     n_tokens is the number of rows allocated in the per-token arrays; it
+ *     is a host value and fixed for a captured graph, the lengths are data.
+ *   - Return value: ECHO_OK or a negative ECHO_E* code from host-side
+ *     argument checks (nothing is enqueued then).  Conditions found on the
+ *     device are OR-ed as ECHO_ST_* bits into *status (int32, device), which
+ *     the caller clears and reads when it likes; the kernels never trap.
+ *   - stats (optional, may be NULL): uint32 device counters [ECHO_STATS_N],
+ *     accumulated (never cleared by the library).
+ *   - Every wait inside a kernel is bounded; a wait that runs out sets
+ *     ECHO_ST_TIMEOUT and the kernel returns.
+ */
+#ifndef ECHO_H
+#define ECHO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* echo_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+/* host-side return codes */
+#define ECHO_OK 0
+#define ECHO_EINVAL (-1)        /* NULL pointer, negative size, misaligned pointer */
+#define ECHO_ECAPACITY (-2)     /* k > C, workspace too small, C not a multiple of 32 */
+#define ECHO_EUNSUPPORTED (-3)  /* B above ECHO_MAX_REQUESTS, row size not a multiple of 16 */
+#define ECHO_ECUDA (-4)         /* a CUDA launch or driver call failed */
+
+/* device status bits (OR-ed into *status) */
+#define ECHO_ST_TIMEOUT 0x1     /* a bounded wait ran out; outputs of that call are invalid */
+#define ECHO_ST_NAN 0x2         /* NaN/Inf in q or w, or a NaN score */
+#define ECHO_ST_NOSLOT 0x4      /* a miss found no free slot (cannot happen when k <= C) */
+#define ECHO_ST_BADDATA 0x8     /* tok_off/tables/selection/histogram inconsistent with the sizes given */
+
+/* stats counters (uint32 each) */
+#define ECHO_STAT_TOPK_FALLBACK 0   /* top-k boundary bins too large for shared memory */
+#define ECHO_STAT_BOUNDARY_MAX 1    /* largest boundary-bin population seen */
+#define ECHO_STAT_EARLY 2           /* tokens fetched early (above the prediction) */
+#define ECHO_STAT_MISSES 3          /* tokens recalled after top-k */
+#define ECHO_STAT_EARLY_USED 4      /* early-fetched tokens that top-k then selected */
+#define ECHO_STATS_N 8
+
+#define ECHO_HEADS 64           /* index heads */
+#define ECHO_DIM 128            /* index head dimension (bytes per E4M3 key row) */
+#define ECHO_MAX_REQUESTS 4096  /* requests per call */
+
+/*
+ * GPU cache of one layer for B requests [EXPL panels "Five fixed-size integer
+ * tensors on the GPU" and "One layer, one step: free -> allocate -> recall"].
+ * Every array has a fixed size, so nothing changes length from step to step.
+ * Initial state: tok2slot and slot2tok all -1, freebits all ones, counts 0.
+ *   tok2slot  [n_tokens] int32   slot of each token in its request's slot range, -1 = not resident
+ *   slot2tok  [B*C]      int32   request-local token held by each slot, -1 = free
+ *   freebits  [B*C/32]   uint32  bit (j%32) of word j/32 set <=> slot j of that request is free
+ *   miss_tok  [B*C]      int32   this step's late misses per request (ascending tokens)
+ *   miss_slot [B*C]      int32   the slot each late miss was given
+ *   miss_cnt  [B]        int32
+ *   early_tok [B*C]      int32   this step's early fetches per request (ascending tokens)
+ *   early_slot[B*C]      int32   the slot each early fetch was given
+ *   early_cnt [B]        int32
+ *   host_kv   device-accessible address of the pinned host KV pool [n_tokens, row_bytes]
+ *             (cudaHostAlloc'd or registered; the address the device uses for it)
+ *   dev_kv    [B*C, row_bytes] device cache rows; request b owns rows [b*C, (b+1)*C)
+ * C is a multiple of 32; row_bytes a multiple of 16 (1152 for 576 bf16 values).
+ * Recall copies run on a copy stream and read only the (token, slot) lists,
+ * never the tables, so the next table update may overlap them; a consumer of
+ * dev_kv must wait for the copy stream.
+ */
+typedef struct echo_cache {
+    int32_t* tok2slot;
+    int32_t* slot2tok;
+    uint32_t* freebits;
+    int32_t* miss_tok;
+    int32_t* miss_slot;
+    int32_t* miss_cnt;
+    int32_t* early_tok;
+    int32_t* early_slot;
+    int32_t* early_cnt;
+    const void* host_kv;
+    void* dev_kv;
+    int64_t row_bytes;
+    int32_t C;
+    int32_t reserved;
+} echo_cache;
+
+/* Bytes of device workspace the calls below need for B requests.  One
+ * workspace may be shared by consecutive calls on the same stream. */
+size_t echo_workspace_size(int B);
+
+/*
+ * Query quantisation [IDX; the sources only say the score GEMM runs in FP8].
+ * Per (request, head): scale = the smallest power of two 2^e with
+ * max_d |q[b,h,d]| <= 448 * 2^e (e >= -126; 1 for an all-zero row),
+ * q8[b,h,d] = E4M3 round-to-nearest-even(q / scale), and
+ * wfold[b,h] = w[b,h] * scale (fp32).
+ *   q [B,64,128] f32, w [B,64] f32 -> q8 [B,64,128] u8, qscale [B,64] f32, wfold [B,64] f32
+ * NaN/Inf in q or w -> ECHO_ST_NAN.
+ */
+int echo_quantize_q(int B, const float* q, const float* w, uint8_t* q8, float* qscale,
+                    float* wfold, int32_t* status, echo_stream_t stream);
+
+/*
+ * Indexer score of every token [IDX]; 256-bin histogram [EXPL panel
+ * "Prefill: one-round histogram"]; early fetch [EXPL panel "Decode: fetch
+ * above a predicted threshold"].
+ *   scores[t] = ks[t] * sum_h wfold[b,h] * max(0, sum_d q8[b,h,d] * k8[t,d])
+ *   for every token row t of request b, which equals the definition
+ *   sum_h w[h] * ReLU(q[h] . k[t]) over the dequantised E4M3 values.
+ *   Inputs: q [B,64,128] f32, w [B,64] f32 (quantised inside, into ws),
+ *   k8 [n_tokens,128] E4M3 bytes (16-byte aligned), ks [n_tokens] f32.
+ *   Outputs: scores [n_tokens] f32 (rows outside every request untouched);
+ *   hist [B,256] u32 (may be NULL; overwritten): per request, counts of
+ *   bin = top 8 bits of orderkey(fp32(score - shift)), shift = theta_hat[b]
+ *   when finite, else 0; orderkey maps a float to a uint32 in the same order
+ *   (-0 counted as +0).  theta_hat [B] f32 (may be NULL = no shift) is read
+ *   only here.
+ *   early (may be NULL = predictor off): tokens with score > theta_hat[b]
+ *   that are not resident, in ascending order, at most min(early_cap, free
+ *   slots) of them (early_cap < 0: no cap but the free slots), take the
+ *   lowest free slots in ascending order and become resident; the lists go
+ *   to early->early_tok / early_slot / early_cnt and their rows are recalled
+ *   into dev_kv on copy_stream (may equal stream), overlapping what follows.
+ *   ws: echo_workspace_size(B) bytes, 256-byte aligned.
+ */
+int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens, const float* q,
+                      const float* w, const uint8_t* k8, const float* ks, float* scores,
+                      const float* theta_hat, uint32_t* hist, const echo_cache* early,
+                      int early_cap, void* ws, size_t ws_bytes, int32_t* status, uint32_t* stats,
+                      echo_stream_t stream, echo_stream_t copy_stream);
+
+/*
+ * Exact top-k per request [EXPL section 2: "guarantees an exact top-k"] and
+ * the EMA threshold update [EXPL panel "Decode: fetch above a predicted
+ * threshold": EMA with alpha = 0.5 of the previous k-th score].
+ *   sel_idx [B,k] int32: the min(k, N_b) highest scores of request b, equal
+ *   scores resolved towards the lower index, written in ascending index
+ *   order and padded with -1.  kth [B] f32: the k-th highest score (the
+ *   smallest selected one when N_b < k; -inf when N_b = 0).
+ *   theta_hat [B] in/out (may be NULL): +inf -> kth; else
+ *   alpha*kth + (1-alpha)*theta_hat, each operation rounded in fp32;
+ *   unchanged when N_b = 0.
+ *   hist [B,256] as written by echo_index_scores with the same theta_hat, or
+ *   NULL (then it is computed here).  The selection never depends on the
+ *   histogram or the prediction; they only decide how much work it takes (a
+ *   histogram that does not describe the scores is rebuilt and flagged
+ *   ECHO_ST_BADDATA).
+ */
+int echo_topk_select(int B, const int64_t* tok_off, int64_t n_tokens, const float* scores, int k,
+                     const uint32_t* hist, float* theta_hat, float alpha, int32_t* sel_idx,
+                     float* kth, int32_t* status, uint32_t* stats, echo_stream_t stream);
+
+/*
+ * GPU-cache step [EXPL panel "One layer, one step: free -> allocate ->
+ * recall"]: with sel [B,m] (ascending request-local tokens, -1 padded):
+ *   1. every resident token that is not selected is freed (both table
+ *      entries -1, its free bit set); its bytes stay, nothing is written back;
+ *   2. the selected tokens that are not resident (the misses), in ascending
+ *      order, take the lowest free slots in ascending order;
+ *   3. sel_slot [B,m] = slot of each selected token (-1 for padding);
+ *   4. the miss rows are copied host_kv[tok_off[b] + t] -> dev_kv[b*C + slot],
+ *      on copy_stream (which may equal stream; an event orders it after 1-3).
+ * Needs m <= C.
+ */
+int echo_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
+                    const echo_cache* cache, int32_t* sel_slot, int32_t* status, uint32_t* stats,
+                    echo_stream_t stream, echo_stream_t copy_stream);
+
+/* Device-accessible address of a pinned host buffer (for echo_cache.host_kv).
+ * Returns ECHO_ECUDA when the pointer is not pinned/mapped host memory. */
+int echo_host_device_alias(const void* host_ptr, const void** device_ptr);
+
+/* Number of SMs of the current device (for sizing); negative on error. */
+int echo_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ECHO_H */

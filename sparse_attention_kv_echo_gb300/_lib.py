@@ -1,0 +1,194 @@
+"""ctypes binding of libecho -- argument marshalling only.
+
+Every call takes torch CUDA tensors (or None where the C ABI allows NULL),
+passes their device addresses and the current CUDA stream to the library and
+returns.  Nothing here computes: all work runs in the library's kernels.  The
+library must be built (``build()``); there is no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+ECHO_OK, ECHO_EINVAL, ECHO_ECAPACITY, ECHO_EUNSUPPORTED, ECHO_ECUDA = 0, -1, -2, -3, -4
+ST_TIMEOUT, ST_NAN, ST_NOSLOT, ST_BADDATA = 0x1, 0x2, 0x4, 0x8
+STAT_TOPK_FALLBACK, STAT_BOUNDARY_MAX, STAT_EARLY, STAT_MISSES, STAT_EARLY_USED = 0, 1, 2, 3, 4
+STATS_N = 8
+HEADS, DIM, MAX_REQUESTS = 64, 128, 4096
+
+EXPORTS = ("echo_cache_step", "echo_device_sm_count", "echo_host_device_alias", "echo_index_scores",
+           "echo_quantize_q", "echo_topk_select", "echo_workspace_size")
+
+_vp = ctypes.c_void_p
+
+
+class EchoCacheStruct(ctypes.Structure):
+    _fields_ = [("tok2slot", _vp), ("slot2tok", _vp), ("freebits", _vp), ("miss_tok", _vp),
+                ("miss_slot", _vp), ("miss_cnt", _vp), ("early_tok", _vp), ("early_slot", _vp),
+                ("early_cnt", _vp), ("host_kv", _vp), ("dev_kv", _vp), ("row_bytes", ctypes.c_int64),
+                ("C", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class EchoError(RuntimeError):
+    def __init__(self, call, rc):
+        super().__init__(f"{call} returned {rc}")
+        self.rc = rc
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libecho.so (raises when it is missing and not built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_build.LIB):
+            if not build_if_missing:
+                raise RuntimeError(f"libecho is not built ({_build.LIB}); run "
+                                   "python -m sparse_attention_kv_echo_gb300.build")
+            _build.build()
+        L = ctypes.CDLL(_build.LIB)
+        i32, i64, f32, sz = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+        L.echo_workspace_size.restype = sz
+        L.echo_workspace_size.argtypes = [i32]
+        L.echo_quantize_q.restype = i32
+        L.echo_quantize_q.argtypes = [i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+        L.echo_index_scores.restype = i32
+        L.echo_index_scores.argtypes = [i32, _vp, i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                        ctypes.POINTER(EchoCacheStruct), i32, _vp, sz, _vp, _vp, _vp, _vp]
+        L.echo_topk_select.restype = i32
+        L.echo_topk_select.argtypes = [i32, _vp, i64, _vp, i32, _vp, _vp, f32, _vp, _vp, _vp, _vp, _vp]
+        L.echo_cache_step.restype = i32
+        L.echo_cache_step.argtypes = [i32, _vp, i64, _vp, i32, ctypes.POINTER(EchoCacheStruct), _vp,
+                                      _vp, _vp, _vp, _vp]
+        L.echo_host_device_alias.restype = i32
+        L.echo_host_device_alias.argtypes = [_vp, ctypes.POINTER(_vp)]
+        L.echo_device_sm_count.restype = i32
+        L.echo_device_sm_count.argtypes = []
+        _lib = L
+        return L
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(call, rc):
+    if rc != ECHO_OK:
+        raise EchoError(call, rc)
+
+
+def workspace_size(B: int) -> int:
+    return load().echo_workspace_size(int(B))
+
+
+def host_device_alias(host_tensor: torch.Tensor) -> int:
+    out = _vp()
+    _check("echo_host_device_alias", load().echo_host_device_alias(host_tensor.data_ptr(), ctypes.byref(out)))
+    return out.value
+
+
+def sm_count() -> int:
+    return load().echo_device_sm_count()
+
+
+def quantize_q(q, w, q8, qscale, wfold, status, stream=None):
+    B = q.shape[0]
+    _check("echo_quantize_q", load().echo_quantize_q(B, _ptr(q), _ptr(w), _ptr(q8), _ptr(qscale),
+                                                    _ptr(wfold), _ptr(status), _stream(stream)))
+
+
+def index_scores(tok_off, n_tokens, q, w, k8, ks, scores, theta_hat, hist, ws, status, cache=None,
+                 early_cap=-1, stats=None, stream=None, copy_stream=None):
+    B = q.shape[0]
+    cs = ctypes.byref(cache.struct) if cache is not None else None
+    st = _stream(stream)
+    cst = _stream(copy_stream) if copy_stream is not None else st
+    _check("echo_index_scores", load().echo_index_scores(
+        B, _ptr(tok_off), int(n_tokens), _ptr(q), _ptr(w), _ptr(k8), _ptr(ks), _ptr(scores),
+        _ptr(theta_hat), _ptr(hist), cs, int(early_cap), _ptr(ws), ws.numel() * ws.element_size(),
+        _ptr(status), _ptr(stats), st, cst))
+
+
+def topk_select(tok_off, n_tokens, scores, k, hist, theta_hat, alpha, sel_idx, kth, status, stats=None,
+                stream=None):
+    B = tok_off.shape[0] - 1
+    _check("echo_topk_select", load().echo_topk_select(
+        B, _ptr(tok_off), int(n_tokens), _ptr(scores), int(k), _ptr(hist), _ptr(theta_hat), float(alpha),
+        _ptr(sel_idx), _ptr(kth), _ptr(status), _ptr(stats), _stream(stream)))
+
+
+def cache_step(tok_off, n_tokens, sel, cache, sel_slot, status, stats=None, stream=None, copy_stream=None):
+    B = tok_off.shape[0] - 1
+    m = sel.shape[-1]
+    st = _stream(stream)
+    cst = _stream(copy_stream) if copy_stream is not None else st
+    _check("echo_cache_step", load().echo_cache_step(
+        B, _ptr(tok_off), int(n_tokens), _ptr(sel), int(m), ctypes.byref(cache.struct), _ptr(sel_slot),
+        _ptr(status), _ptr(stats), st, cst))
+
+
+class LayerCache:
+    """The fixed-size GPU cache tensors of one layer for B requests (torch-owned).
+
+    host_pool: pinned host tensor [n_tokens, row_bytes/2] bf16 (the per-layer
+    host copy of every token's KV row)."""
+
+    def __init__(self, B: int, n_tokens: int, C: int, host_pool: torch.Tensor, device="cuda"):
+        if C % 32:
+            raise ValueError("C must be a multiple of 32")
+        assert host_pool.is_pinned()
+        self.B, self.C, self.n_tokens = B, C, n_tokens
+        self.row_bytes = host_pool.shape[1] * host_pool.element_size()
+        i32 = dict(dtype=torch.int32, device=device)
+        self.tok2slot = torch.full((max(n_tokens, 1),), -1, **i32)
+        self.slot2tok = torch.full((B * C,), -1, **i32)
+        self.freebits = torch.full((B * C // 32,), -1, **i32)   # all bits set: every slot free
+        self.miss_tok = torch.zeros((B * C,), **i32)
+        self.miss_slot = torch.zeros((B * C,), **i32)
+        self.miss_cnt = torch.zeros((B,), **i32)
+        self.early_tok = torch.zeros((B * C,), **i32)
+        self.early_slot = torch.zeros((B * C,), **i32)
+        self.early_cnt = torch.zeros((B,), **i32)
+        self.dev_kv = torch.zeros((B * C, host_pool.shape[1]), dtype=host_pool.dtype, device=device)
+        self.host_pool = host_pool
+        self.host_alias = host_device_alias(host_pool)
+        s = EchoCacheStruct()
+        s.tok2slot, s.slot2tok, s.freebits = _ptr(self.tok2slot), _ptr(self.slot2tok), _ptr(self.freebits)
+        s.miss_tok, s.miss_slot, s.miss_cnt = _ptr(self.miss_tok), _ptr(self.miss_slot), _ptr(self.miss_cnt)
+        s.early_tok, s.early_slot, s.early_cnt = (_ptr(self.early_tok), _ptr(self.early_slot),
+                                                  _ptr(self.early_cnt))
+        s.host_kv, s.dev_kv = self.host_alias, _ptr(self.dev_kv)
+        s.row_bytes, s.C, s.reserved = self.row_bytes, C, 0
+        self.struct = s
+
+    def reset(self):
+        self.tok2slot.fill_(-1)
+        self.slot2tok.fill_(-1)
+        self.freebits.fill_(-1)
+        self.miss_cnt.zero_()
+        self.early_cnt.zero_()

@@ -1,0 +1,340 @@
+// echo_cache.cu -- the per-layer GPU cache step, early fetch and recall.
+//
+// "ECHO: Lossless KV Cache Offloading for Sparse Attention LLMs", section 2:
+//   panel "Five fixed-size integer tensors on the GPU": nothing changes
+//     length, so a decode step stays inside one CUDA graph;
+//   panel "One layer, one step: free -> allocate -> recall": unselected slots
+//     are freed (no write-back: the host holds every token), misses get
+//     slots, their rows are recalled from the host pool;
+//   panel "Decode: fetch above a predicted threshold": tokens scoring above
+//     the predicted threshold are fetched before top-k completes, up to a cap.
+//
+// Kernels (one CTA of 1024 threads per request for the table work):
+//   early_select_kernel  ordered scan of score > theta over non-resident tokens
+//                        (block prefix sums), the first min(cap, free) of them
+//                        take the lowest free slots.
+//   cache_step_kernel    marks the slots of selected residents in a shared
+//                        bitmap, frees the rest one warp per 32-slot word
+//                        (ballot -> free-bit word), compacts the misses in
+//                        ascending order, hands them the lowest free slots by a
+//                        prefix sum of popcounts over the free-bit words.
+//   recall_kernel        one warp per row, 16-byte loads from the pinned host
+//                        pool through its device alias (zero-copy over the
+//                        host link), 16-byte stores into the device cache.
+#include "echo_common.cuh"
+#include "echo_internal.h"
+
+namespace echo {
+namespace {
+
+constexpr int kCT = 1024;
+constexpr int kMaxSlotsSmem = 1 << 20;   // slot bitmap of up to 2^20 slots (128 KB)
+
+struct CacheArgs {
+    int32_t* tok2slot;
+    int32_t* slot2tok;
+    uint32_t* freebits;
+    int32_t* miss_tok;
+    int32_t* miss_slot;
+    int32_t* miss_cnt;
+    int32_t* early_tok;
+    int32_t* early_slot;
+    int32_t* early_cnt;
+    int32_t C;
+};
+
+CacheArgs cache_args(const echo_cache& c) {
+    return CacheArgs{c.tok2slot, c.slot2tok, c.freebits, c.miss_tok, c.miss_slot, c.miss_cnt,
+                     c.early_tok, c.early_slot, c.early_cnt, c.C};
+}
+
+__device__ __forceinline__ bool request_range(const int64_t* tok_off, int64_t n_tokens, int b, int64_t* base,
+                                              int64_t* n) {
+    const int64_t lo = tok_off[b], hi = tok_off[b + 1];
+    if (lo < 0 || hi < lo || hi > n_tokens) {
+        *base = 0;
+        *n = 0;
+        return false;
+    }
+    *base = lo;
+    *n = hi - lo;
+    return true;
+}
+
+// Give the first M tokens of tok_list the M lowest free slots of one
+// request, in ascending order.  Block-wide; returns the number assigned.
+__device__ uint32_t assign_lowest_free(uint32_t* fb, int words, uint32_t M, const int32_t* tok_list,
+                                       int32_t* slot_list, int32_t* t2s, int32_t* s2t, int64_t n, int C,
+                                       uint32_t* scan, int32_t* status) {
+    uint32_t done = 0;
+    for (int w0 = 0; w0 < words && done < M; w0 += kCT) {
+        const int w = w0 + threadIdx.x;
+        const uint32_t f = (w < words) ? fb[w] : 0u;
+        uint32_t tot;
+        uint32_t rank = done + block_exclusive_scan<kCT>(__popc(f), scan, &tot);
+        if (f && rank < M) {
+            uint32_t x = f, taken = 0;
+            while (x && rank < M) {
+                const int bit = __ffs(x) - 1;
+                x &= x - 1;
+                const int slot = w * 32 + bit;
+                const int32_t tok = tok_list[rank];
+                if (tok >= 0 && tok < n && slot < C) {
+                    t2s[tok] = slot;
+                    s2t[slot] = tok;
+                    slot_list[rank] = slot;
+                    taken |= 1u << bit;
+                } else {
+                    set_status(status, ECHO_ST_BADDATA);
+                }
+                ++rank;
+            }
+            fb[w] = f & ~taken;
+        }
+        done += tot;
+    }
+    if (done < M && threadIdx.x == 0) set_status(status, ECHO_ST_NOSLOT);
+    return done < M ? done : M;
+}
+
+__global__ void __launch_bounds__(kCT) early_select_kernel(const int64_t* __restrict__ tok_off, int64_t n_tokens,
+                                                           const float* __restrict__ scores,
+                                                           const float* __restrict__ theta_hat, int cap, CacheArgs c,
+                                                           int32_t* status, uint32_t* stats) {
+    __shared__ uint32_t scan[40];
+    const int b = blockIdx.x, tid = threadIdx.x;
+    int64_t base, n;
+    if (!request_range(tok_off, n_tokens, b, &base, &n) && tid == 0) set_status(status, ECHO_ST_BADDATA);
+    const int C = c.C, words = C / 32;
+    int32_t* t2s = c.tok2slot + base;
+    int32_t* s2t = c.slot2tok + static_cast<int64_t>(b) * C;
+    uint32_t* fb = c.freebits + static_cast<int64_t>(b) * words;
+    int32_t* etok = c.early_tok + static_cast<int64_t>(b) * C;
+    int32_t* eslot = c.early_slot + static_cast<int64_t>(b) * C;
+    const float th = theta_hat[b];
+    if (!isfinite(th) || n == 0 || cap == 0) {
+        if (tid == 0) c.early_cnt[b] = 0;
+        return;
+    }
+    uint32_t F = 0;
+    for (int w0 = 0; w0 < words; w0 += kCT) {
+        const int w = w0 + tid;
+        uint32_t tot;
+        block_exclusive_scan<kCT>(w < words ? __popc(fb[w]) : 0u, scan, &tot);
+        F += tot;
+    }
+    const uint32_t limit = (cap < 0) ? F : min(F, static_cast<uint32_t>(cap));
+    uint32_t found = 0;
+    for (int64_t c0 = 0; c0 < n && found < limit; c0 += 4 * kCT) {
+        const int64_t s0 = c0 + 4 * tid;
+        uint32_t f = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int64_t s = s0 + j;
+            if (s < n && scores[base + s] > th && t2s[s] < 0) f |= 1u << j;
+        }
+        uint32_t tot;
+        uint32_t rank = found + block_exclusive_scan<kCT>(__popc(f), scan, &tot);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (f & (1u << j)) {
+                if (rank < limit) etok[rank] = static_cast<int32_t>(s0 + j);
+                ++rank;
+            }
+        found += tot;
+    }
+    const uint32_t E = min(found, limit);
+    __syncthreads();
+    const uint32_t got = assign_lowest_free(fb, words, E, etok, eslot, t2s, s2t, n, C, scan, status);
+    if (tid == 0) {
+        c.early_cnt[b] = static_cast<int32_t>(got);
+        if (stats && got) atomicAdd(stats + ECHO_STAT_EARLY, got);
+    }
+}
+
+__global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restrict__ tok_off, int64_t n_tokens,
+                                                         const int32_t* __restrict__ sel, int m, CacheArgs c,
+                                                         int32_t* __restrict__ sel_slot, int32_t* status,
+                                                         uint32_t* stats) {
+    extern __shared__ uint32_t keep[];  // one bit per slot: a selected token lives there
+    __shared__ uint32_t scan[40];
+    __shared__ uint32_t s_flags;
+    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int64_t base, n;
+    if (!request_range(tok_off, n_tokens, b, &base, &n) && tid == 0) set_status(status, ECHO_ST_BADDATA);
+    const int C = c.C, words = C / 32;
+    int32_t* t2s = c.tok2slot + base;
+    int32_t* s2t = c.slot2tok + static_cast<int64_t>(b) * C;
+    uint32_t* fb = c.freebits + static_cast<int64_t>(b) * words;
+    const int32_t* sl = sel + static_cast<int64_t>(b) * m;
+    int32_t* mtok = c.miss_tok + static_cast<int64_t>(b) * C;
+    int32_t* mslot = c.miss_slot + static_cast<int64_t>(b) * C;
+
+    for (int w = tid; w < words; w += kCT) keep[w] = 0u;
+    if (tid == 0) s_flags = 0;
+    __syncthreads();
+    // 1a. slots that hold a selected token are kept
+    for (int i = tid; i < m; i += kCT) {
+        const int32_t s = sl[i];
+        if (s < 0) continue;
+        if (s >= n) {
+            atomicOr(&s_flags, static_cast<uint32_t>(ECHO_ST_BADDATA));
+            continue;
+        }
+        const int32_t j = t2s[s];
+        if (j >= 0 && j < C) atomicOr(&keep[j >> 5], 1u << (j & 31));
+    }
+    __syncthreads();
+    // 1b. every other occupied slot is freed; bytes stay, nothing is written back
+    for (int w = warp; w < words; w += kCT / 32) {
+        const int slot = w * 32 + lane;
+        const int32_t s = s2t[slot];
+        const bool kept = (keep[w] >> lane) & 1u;
+        const bool freeing = s >= 0 && !kept;
+        if (freeing) {
+            s2t[slot] = -1;
+            if (s < n) t2s[s] = -1;
+        }
+        const unsigned fm = __ballot_sync(0xffffffffu, freeing);
+        if (lane == 0 && fm) fb[w] |= fm;
+    }
+    __syncthreads();
+    // 2. misses, ascending; the selection must be ascending with -1 padding last
+    uint32_t M = 0, early_used = 0;
+    for (int c0 = 0; c0 < m; c0 += 4 * kCT) {
+        const int i0 = c0 + 4 * tid;
+        uint32_t f = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = i0 + j;
+            if (i < m) {
+                const int32_t s = sl[i];
+                if (s >= 0 && s < n) {
+                    if (i + 1 < m && sl[i + 1] >= 0 && sl[i + 1] <= s)
+                        atomicOr(&s_flags, static_cast<uint32_t>(ECHO_ST_BADDATA));
+                    if (t2s[s] < 0) f |= 1u << j;
+                } else if (s >= 0 || (i + 1 < m && sl[i + 1] >= 0)) {
+                    atomicOr(&s_flags, static_cast<uint32_t>(ECHO_ST_BADDATA));
+                }
+            }
+        }
+        uint32_t tot;
+        uint32_t rank = M + block_exclusive_scan<kCT>(__popc(f), scan, &tot);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (f & (1u << j)) {
+                if (rank < static_cast<uint32_t>(C)) mtok[rank] = sl[i0 + j];
+                ++rank;
+            }
+        M += tot;
+    }
+    if (M > static_cast<uint32_t>(C)) M = C;
+    // early fetches of this step that the selection kept
+    const int ecnt = min(c.early_cnt[b], C);
+    for (int i = tid; i < ecnt; i += kCT) {
+        const int32_t s = c.early_tok[static_cast<int64_t>(b) * C + i];
+        if (s >= 0 && s < n && t2s[s] >= 0) ++early_used;
+    }
+    __syncthreads();
+    // 3. the misses take the lowest free slots
+    const uint32_t got = assign_lowest_free(fb, words, M, mtok, mslot, t2s, s2t, n, C, scan, status);
+    __syncthreads();
+    // 4. slot of every selected entry
+    for (int i = tid; i < m; i += kCT) {
+        const int32_t s = sl[i];
+        sel_slot[static_cast<int64_t>(b) * m + i] = (s >= 0 && s < n) ? t2s[s] : -1;
+    }
+    if (early_used && stats) atomicAdd(stats + ECHO_STAT_EARLY_USED, early_used);
+    __syncthreads();
+    if (tid == 0) {
+        c.miss_cnt[b] = static_cast<int32_t>(got);
+        if (stats && got) atomicAdd(stats + ECHO_STAT_MISSES, got);
+        if (s_flags) set_status(status, static_cast<int>(s_flags));
+    }
+}
+
+__global__ void __launch_bounds__(256) recall_kernel(const int64_t* __restrict__ tok_off, int64_t n_tokens, int C,
+                                                     const int32_t* __restrict__ tok_list,
+                                                     const int32_t* __restrict__ slot_list,
+                                                     const int32_t* __restrict__ cnt, const uint8_t* host,
+                                                     uint8_t* __restrict__ dev, int64_t row_bytes, int32_t* status) {
+    const int b = blockIdx.y;
+    const int lane = threadIdx.x & 31;
+    const int warps = blockDim.x >> 5;
+    int64_t base, n;
+    if (!request_range(tok_off, n_tokens, b, &base, &n)) return;
+    int count = cnt[b];
+    if (count > C) count = C;
+    const int chunks = static_cast<int>(row_bytes / 16);
+    for (int i = blockIdx.x * warps + (threadIdx.x >> 5); i < count; i += gridDim.x * warps) {
+        const int32_t tok = tok_list[static_cast<int64_t>(b) * C + i];
+        const int32_t slot = slot_list[static_cast<int64_t>(b) * C + i];
+        if (tok < 0 || tok >= n || slot < 0 || slot >= C) {
+            if (lane == 0) set_status(status, ECHO_ST_BADDATA);
+            continue;
+        }
+        const int4* src = reinterpret_cast<const int4*>(host + (base + tok) * row_bytes);
+        int4* dst = reinterpret_cast<int4*>(dev + (static_cast<int64_t>(b) * C + slot) * row_bytes);
+        for (int c0 = 0; c0 < chunks; c0 += 96) {
+            int4 v0 = make_int4(0, 0, 0, 0), v1 = v0, v2 = v0;
+            const int a0 = c0 + lane, a1 = a0 + 32, a2 = a0 + 64;
+            if (a0 < chunks) v0 = __ldcs(src + a0);
+            if (a1 < chunks) v1 = __ldcs(src + a1);
+            if (a2 < chunks) v2 = __ldcs(src + a2);
+            if (a0 < chunks) dst[a0] = v0;
+            if (a1 < chunks) dst[a1] = v1;
+            if (a2 < chunks) dst[a2] = v2;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_early_select(int B, const int64_t* tok_off, int64_t n_tokens, const float* scores,
+                                const float* theta_hat, int cap, const echo_cache& c, int32_t* status,
+                                uint32_t* stats, cudaStream_t s) {
+    early_select_kernel<<<B, kCT, 0, s>>>(tok_off, n_tokens, scores, theta_hat, cap, cache_args(c), status, stats);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_recall(int B, const int64_t* tok_off, int64_t n_tokens, int C, const int32_t* tok_list,
+                          const int32_t* slot_list, const int32_t* cnt, const void* host_kv, void* dev_kv,
+                          int64_t row_bytes, int32_t* status, cudaStream_t s) {
+    const int sms = sm_count();
+    if (sms <= 0) return cudaErrorInvalidDevice;
+    int gx = (4 * sms + B - 1) / B;
+    const int rows_per_block = 8;
+    const int gx_max = (C + rows_per_block - 1) / rows_per_block;
+    if (gx > gx_max) gx = gx_max;
+    if (gx < 1) gx = 1;
+    recall_kernel<<<dim3(gx, B), 256, 0, s>>>(tok_off, n_tokens, C, tok_list, slot_list, cnt,
+                                              static_cast<const uint8_t*>(host_kv), static_cast<uint8_t*>(dev_kv),
+                                              row_bytes, status);
+    return cudaGetLastError();
+}
+
+}  // namespace echo
+
+extern "C" int echo_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
+                               const echo_cache* cache, int32_t* sel_slot, int32_t* status, uint32_t* stats,
+                               echo_stream_t stream, echo_stream_t copy_stream) {
+    using namespace echo;
+    if (B <= 0 || n_tokens < 0 || m < 0) return ECHO_EINVAL;
+    if (B > ECHO_MAX_REQUESTS) return ECHO_EUNSUPPORTED;
+    if (!tok_off || !status || (m > 0 && (!sel || !sel_slot))) return ECHO_EINVAL;
+    if (n_tokens >= (1ll << 31)) return ECHO_EUNSUPPORTED;
+    int rc = check_cache(cache, B, m);
+    if (rc) return rc;
+    if (cache->C > kMaxSlotsSmem) return ECHO_EUNSUPPORTED;
+    const size_t smem = static_cast<size_t>(cache->C / 32) * sizeof(uint32_t);
+    ECHO_CUDA_OK(cudaFuncSetAttribute(cache_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(smem)));
+    cache_step_kernel<<<B, kCT, smem, stream>>>(tok_off, n_tokens, sel, m, cache_args(*cache), sel_slot, status,
+                                                stats);
+    ECHO_CUDA_OK(cudaGetLastError());
+    rc = stream_wait(copy_stream, stream);
+    if (rc) return rc;
+    ECHO_CUDA_OK(launch_recall(B, tok_off, n_tokens, cache->C, cache->miss_tok, cache->miss_slot, cache->miss_cnt,
+                               cache->host_kv, cache->dev_kv, cache->row_bytes, status, copy_stream));
+    return ECHO_OK;
+}

@@ -1,0 +1,55 @@
+// echo_internal.h -- host-side helpers shared by the libecho translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "echo.h"
+
+namespace echo {
+
+inline bool is_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace layout for B requests: q8 [B,64,128] u8 | qscale [B,64] f32 | wfold [B,64] f32.
+struct Workspace {
+    uint8_t* q8;
+    float* qscale;
+    float* wfold;
+};
+size_t workspace_bytes(int B);
+Workspace carve_workspace(void* ws, int B);
+
+// SM count of the current device.
+int sm_count();
+
+// 2-D tensor map over a row-major byte matrix [rows, inner_bytes] with a box
+// of [box_rows, box_inner] bytes and the 128-byte swizzle.  0 on success.
+int encode_tmap_bytes_2d(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,
+                         uint32_t box_inner, uint32_t box_rows);
+
+// Make `to` wait for everything enqueued so far on `from` (no-op when equal).
+int stream_wait(cudaStream_t to, cudaStream_t from);
+
+// Host-side checks of an echo_cache for B requests and selections of up to m tokens.
+int check_cache(const echo_cache* c, int B, int m);
+
+// Launchers shared across translation units.
+cudaError_t launch_quantize(int B, const float* q, const float* w, uint8_t* q8, float* qscale, float* wfold,
+                            uint32_t* hist_to_zero, int32_t* status, cudaStream_t s);
+cudaError_t launch_early_select(int B, const int64_t* tok_off, int64_t n_tokens, const float* scores,
+                                const float* theta_hat, int cap, const echo_cache& c, int32_t* status,
+                                uint32_t* stats, cudaStream_t s);
+cudaError_t launch_recall(int B, const int64_t* tok_off, int64_t n_tokens, int C, const int32_t* tok_list,
+                          const int32_t* slot_list, const int32_t* cnt, const void* host_kv, void* dev_kv,
+                          int64_t row_bytes, int32_t* status, cudaStream_t s);
+
+}  // namespace echo
+
+#define ECHO_CUDA_OK(expr)                               \
+    do {                                                 \
+        if ((expr) != cudaSuccess) return ECHO_ECUDA;    \
+    } while (0)

@@ -1,0 +1,412 @@
+// echo_scores.cu -- indexer score of every context token on the tcgen05 tensor cores.
+//
+// I[t] = ks[t] * sum_h wfold[b,h] * max(0, sum_d q8[b,h,d] * k8[t,d])
+// (the DeepSeek-V3.2 lightning-indexer score over E4M3 keys, with the query
+// scales folded into the head weights), plus the per-request 256-bin
+// histogram of the threshold-shifted scores that top-k selection starts from
+// ("ECHO: Lossless KV Cache Offloading for Sparse Attention LLMs", section 2,
+// panel "Prefill: one-round histogram").
+//
+// Design (one persistent CTA per SM, 320 threads, warp-specialised):
+//   warp 0      TMA producer: 128-token x 128-byte key tiles (16 KB, 128-byte
+//               swizzle) into an 8-stage shared-memory ring; the request's
+//               q8 [64 x 128] into one of two q buffers when the request changes.
+//   warp 1      TMEM owner + single-thread MMA issuer: per tile, four
+//               tcgen05.mma kind::f8f6f4 (M=128 tokens, N=64 heads, K=32)
+//               into one of four fp32 accumulators of 64 TMEM columns.
+//   warps 2-9   two epilogue groups of four warps; group g drains the tiles
+//               with local index = g (mod 2).  Each thread owns one token:
+//               tcgen05.ld of its 64 head sums, ReLU, weighted sum, times the
+//               token scale, store, and a warp-private histogram in shared
+//               memory flushed with global atomics when the request changes.
+// Tiles of all requests form one list; CTA c takes a contiguous share of it.
+// The scan of the keys is the HBM-bound part: 132 bytes per token (128 key
+// bytes + 4 scale bytes) against 16384 FP8 MAC-flops.
+#include "echo_common.cuh"
+#include "echo_internal.h"
+
+namespace echo {
+namespace {
+
+constexpr int kStages = 8;
+constexpr int kTileM = 128;                            // tokens per tile (MMA M)
+constexpr int kKeyBytes = kTileM * ECHO_DIM;           // 16 KB per key tile
+constexpr int kQBytes = ECHO_HEADS * ECHO_DIM;         // 8 KB q8 per request
+constexpr int kAccBufs = 4;                            // TMEM accumulators
+constexpr int kTmemCols = kAccBufs * ECHO_HEADS;       // 256 columns
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + kEpiWarps * 32;          // 320
+constexpr uint32_t kIdesc = idesc_e4m3_f32(kTileM, ECHO_HEADS);
+
+struct ScoreArgs {
+    int B;
+    const int64_t* tok_off;
+    int64_t n_tokens;
+    const float* wfold;
+    const float* ks;
+    float* scores;
+    const float* theta_hat;
+    uint32_t* hist;
+    int32_t* status;
+};
+
+struct __align__(16) ScoreCtl {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t qfull[2];
+    uint64_t qempty[2];
+    uint64_t accfull[kAccBufs];
+    uint64_t accempty[kAccBufs];
+    uint64_t done;
+    uint32_t tmem_base;
+    int abort;
+    uint32_t scan[16];
+    uint32_t hist[kEpiWarps][256];
+};
+
+__host__ __device__ constexpr size_t smem_bytes(int B) {
+    return 1024 + static_cast<size_t>(kStages) * kKeyBytes + 2 * kQBytes + sizeof(ScoreCtl) +
+           4 * static_cast<size_t>(B + 1);
+}
+
+// Largest request b in [0, B) whose first tile is <= t.
+__device__ __forceinline__ int find_request(const int32_t* tstart, int B, uint32_t t) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (static_cast<uint32_t>(tstart[mid]) <= t)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ int64_t request_len(const ScoreArgs& a, int b, bool* bad) {
+    const int64_t lo = a.tok_off[b], hi = a.tok_off[b + 1];
+    if (lo < 0 || hi < lo || hi > a.n_tokens) {
+        *bad = true;
+        return 0;
+    }
+    return hi - lo;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    score_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                 const ScoreArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* keys = smem;
+    uint8_t* qbuf = smem + kStages * kKeyBytes;
+    ScoreCtl* ctl = reinterpret_cast<ScoreCtl*>(qbuf + 2 * kQBytes);
+    int32_t* tstart = reinterpret_cast<int32_t*>(ctl + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int B = a.B;
+
+    // ---- first tile of every request (ceil(N_b / 128) tiles each)
+    {
+        const int per = (B + kThreads - 1) / kThreads;
+        const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+        bool bad = false;
+        uint32_t local = 0;
+        for (int b = b0; b < b1; ++b) local += static_cast<uint32_t>((request_len(a, b, &bad) + kTileM - 1) / kTileM);
+        uint32_t total;
+        uint32_t run = block_exclusive_scan<kThreads>(local, ctl->scan, &total);
+        for (int b = b0; b < b1; ++b) {
+            tstart[b] = static_cast<int32_t>(run);
+            run += static_cast<uint32_t>((request_len(a, b, &bad) + kTileM - 1) / kTileM);
+        }
+        if (tid == 0) tstart[B] = static_cast<int32_t>(total);
+        if (bad) set_status(a.status, ECHO_ST_BADDATA);
+    }
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_addr(&ctl->full[s]), 1);
+            mbar_init(smem_addr(&ctl->empty[s]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_addr(&ctl->qfull[i]), 1);
+            mbar_init(smem_addr(&ctl->qempty[i]), 1);
+        }
+        for (int i = 0; i < kAccBufs; ++i) {
+            mbar_init(smem_addr(&ctl->accfull[i]), 1);
+            mbar_init(smem_addr(&ctl->accempty[i]), 4);
+        }
+        mbar_init(smem_addr(&ctl->done), 1);
+        ctl->abort = 0;
+        fence_barrier_init();
+    }
+    for (int i = tid; i < kEpiWarps * 256; i += kThreads) (&ctl->hist[0][0])[i] = 0u;
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&kmap);
+        prefetch_tmap(&qmap);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem_base = ctl->tmem_base;
+    const uint32_t T = static_cast<uint32_t>(tstart[B]);
+    const uint32_t G = gridDim.x, c = blockIdx.x;
+    const uint32_t t_begin = static_cast<uint32_t>((static_cast<uint64_t>(T) * c) / G);
+    const uint32_t t_end = static_cast<uint32_t>((static_cast<uint64_t>(T) * (c + 1)) / G);
+    const uint32_t ntiles = t_end - t_begin;
+    volatile int* abort = &ctl->abort;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && ntiles > 0) {
+            const uint64_t pol = policy_evict_first();
+            int b = find_request(tstart, B, t_begin), cur_b = -1;
+            uint32_t qn = 0, it = 0;
+            int64_t row_base = 0;
+            bool ok = true;
+            for (; it < ntiles; ++it) {
+                const uint32_t t = t_begin + it;
+                while (t >= static_cast<uint32_t>(tstart[b + 1])) ++b;
+                if (b != cur_b) {
+                    const uint32_t qi = qn & 1;
+                    if (!mbar_wait(smem_addr(&ctl->qempty[qi]), ((qn >> 1) & 1) ^ 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(smem_addr(&ctl->qfull[qi]), kQBytes);
+                    tma_load_2d(smem_addr(qbuf + qi * kQBytes), &qmap, smem_addr(&ctl->qfull[qi]), 0,
+                                b * ECHO_HEADS);
+                    cur_b = b;
+                    ++qn;
+                    row_base = a.tok_off[b];
+                }
+                const uint32_t s = it % kStages;
+                if (!mbar_wait(smem_addr(&ctl->empty[s]), ((it / kStages) & 1) ^ 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(smem_addr(&ctl->full[s]), kKeyBytes);
+                const int64_t row0 = row_base + static_cast<int64_t>(t - tstart[b]) * kTileM;
+                tma_load_2d_hint(smem_addr(keys + s * kKeyBytes), &kmap, smem_addr(&ctl->full[s]), 0,
+                                 static_cast<int32_t>(row0), pol);
+            }
+            if (!ok) {
+                set_status(a.status, ECHO_ST_TIMEOUT);
+                *abort = 1;
+            }
+            // Let every copy this thread started land before the CTA exits.
+            for (uint32_t j = (it > kStages ? it - kStages : 0); j < it; ++j)
+                mbar_wait(smem_addr(&ctl->full[j % kStages]), (j / kStages) & 1, nullptr);
+            for (uint32_t j = (qn > 2 ? qn - 2 : 0); j < qn; ++j)
+                mbar_wait(smem_addr(&ctl->qfull[j & 1]), (j >> 1) & 1, nullptr);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && ntiles > 0) {
+            const uint32_t keys_s = smem_addr(keys), q_s = smem_addr(qbuf);
+            int b = find_request(tstart, B, t_begin), cur_b = -1;
+            uint32_t qn = 0;
+            bool ok = true;
+            for (uint32_t it = 0; it < ntiles; ++it) {
+                const uint32_t t = t_begin + it;
+                while (t >= static_cast<uint32_t>(tstart[b + 1])) ++b;
+                if (b != cur_b) {
+                    if (cur_b >= 0) mma_commit(smem_addr(&ctl->qempty[(qn - 1) & 1]));
+                    const uint32_t qi = qn & 1;
+                    if (!mbar_wait(smem_addr(&ctl->qfull[qi]), (qn >> 1) & 1, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    cur_b = b;
+                    ++qn;
+                }
+                const uint32_t acc = it % kAccBufs;
+                if (!mbar_wait(smem_addr(&ctl->accempty[acc]), ((it / kAccBufs) & 1) ^ 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t s = it % kStages;
+                if (!mbar_wait(smem_addr(&ctl->full[s]), (it / kStages) & 1, abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t ad = sw128_kmajor_desc(keys_s + s * kKeyBytes);
+                const uint64_t bd = sw128_kmajor_desc(q_s + ((qn - 1) & 1) * kQBytes);
+                const uint32_t d = tmem_base + acc * ECHO_HEADS;
+#pragma unroll
+                for (int kk = 0; kk < ECHO_DIM / 32; ++kk)
+                    mma_f8f6f4(d, ad + 2 * kk, bd + 2 * kk, kIdesc, kk > 0 ? 1u : 0u);
+                mma_commit(smem_addr(&ctl->empty[s]));
+                mma_commit(smem_addr(&ctl->accfull[acc]));
+            }
+            if (!ok) {
+                set_status(a.status, ECHO_ST_TIMEOUT);
+                *abort = 1;
+            }
+            // All MMAs of this thread complete before TMEM is released.
+            mma_commit(smem_addr(&ctl->done));
+            mbar_wait(smem_addr(&ctl->done), 0, nullptr);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int ew = warp - 2;               // 0..7
+        const int group = ew >> 2;             // tiles with local index = group (mod 2)
+        const int quarter = warp & 3;          // TMEM lanes this warp may access
+        const int row = quarter * 32 + lane;   // token row within the tile
+        uint32_t* whist = ctl->hist[ew];
+        int b = (ntiles > 0) ? find_request(tstart, B, t_begin) : 0;
+        int cur_b = -1;
+        float wv[ECHO_HEADS];
+        float shift = 0.f;
+        int64_t base = 0, nb = 0;
+        bool ok = true;
+        for (uint32_t it = group; it < ntiles; it += 2) {
+            const uint32_t t = t_begin + it;
+            while (t >= static_cast<uint32_t>(tstart[b + 1])) ++b;
+            if (b != cur_b) {
+                if (cur_b >= 0 && a.hist) {
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t v = whist[lane + 32 * j];
+                        if (v) {
+                            atomicAdd(a.hist + static_cast<size_t>(cur_b) * 256 + lane + 32 * j, v);
+                            whist[lane + 32 * j] = 0u;
+                        }
+                    }
+                    __syncwarp();
+                }
+                cur_b = b;
+                const float4* wp = reinterpret_cast<const float4*>(a.wfold + static_cast<size_t>(b) * ECHO_HEADS);
+#pragma unroll
+                for (int i = 0; i < ECHO_HEADS / 4; ++i) {
+                    const float4 x = wp[i];
+                    wv[4 * i + 0] = x.x;
+                    wv[4 * i + 1] = x.y;
+                    wv[4 * i + 2] = x.z;
+                    wv[4 * i + 3] = x.w;
+                }
+                const float th = a.theta_hat ? a.theta_hat[b] : __int_as_float(0x7f800000);
+                shift = isfinite(th) ? th : 0.f;
+                base = a.tok_off[b];
+                nb = a.tok_off[b + 1] - base;
+            }
+            const int64_t tok = static_cast<int64_t>(t - tstart[b]) * kTileM + row;
+            const bool valid = tok < nb;
+            const float ksv = valid ? __ldg(a.ks + base + tok) : 0.f;
+            const uint32_t acc = it % kAccBufs;
+            if (!mbar_wait(smem_addr(&ctl->accfull[acc]), (it / kAccBufs) & 1, abort)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t r0[16], r1[16], r2[16], r3[16];
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * ECHO_HEADS;
+            tmem_ld_x16(taddr + 0, r0);
+            tmem_ld_x16(taddr + 16, r1);
+            tmem_ld_x16(taddr + 32, r2);
+            tmem_ld_x16(taddr + 48, r3);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(r0[i]), "+r"(r1[i]), "+r"(r2[i]), "+r"(r3[i]));
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&ctl->accempty[acc]));
+            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                s0 = fmaf(wv[i], fmaxf(__uint_as_float(r0[i]), 0.f), s0);
+                s1 = fmaf(wv[16 + i], fmaxf(__uint_as_float(r1[i]), 0.f), s1);
+                s2 = fmaf(wv[32 + i], fmaxf(__uint_as_float(r2[i]), 0.f), s2);
+                s3 = fmaf(wv[48 + i], fmaxf(__uint_as_float(r3[i]), 0.f), s3);
+            }
+            const float score = __fmul_rn(__fadd_rn(__fadd_rn(s0, s1), __fadd_rn(s2, s3)), ksv);
+            const unsigned vm = __ballot_sync(0xffffffffu, valid);
+            if (valid) {
+                a.scores[base + tok] = score;
+                if (a.hist) {
+                    const uint32_t bin = shifted_bin(score, shift);
+                    const unsigned grp = __match_any_sync(vm, bin);
+                    if (lane == __ffs(grp) - 1) whist[bin] += __popc(grp);
+                }
+            }
+        }
+        if (!ok) {
+            set_status(a.status, ECHO_ST_TIMEOUT);
+            *abort = 1;
+        }
+        if (cur_b >= 0 && a.hist) {
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t v = whist[lane + 32 * j];
+                if (v) atomicAdd(a.hist + static_cast<size_t>(cur_b) * 256 + lane + 32 * j, v);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace
+}  // namespace echo
+
+extern "C" int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens, const float* q, const float* w,
+                                 const uint8_t* k8, const float* ks, float* scores, const float* theta_hat,
+                                 uint32_t* hist, const echo_cache* early, int early_cap, void* ws, size_t ws_bytes,
+                                 int32_t* status, uint32_t* stats, echo_stream_t stream,
+                                 echo_stream_t copy_stream) {
+    using namespace echo;
+    if (B <= 0 || n_tokens < 0) return ECHO_EINVAL;
+    if (B > ECHO_MAX_REQUESTS) return ECHO_EUNSUPPORTED;
+    if (!tok_off || !q || !w || !ws || !status) return ECHO_EINVAL;
+    if (n_tokens > 0 && (!k8 || !ks || !scores)) return ECHO_EINVAL;
+    if (n_tokens >= (1ll << 31)) return ECHO_EUNSUPPORTED;
+    if (!is_aligned(q, 16) || !is_aligned(ws, 256) || !is_aligned(k8, 16)) return ECHO_EINVAL;
+    if (ws_bytes < workspace_bytes(B)) return ECHO_ECAPACITY;
+    if (early) {
+        const int rc = check_cache(early, B, 0);
+        if (rc) return rc;
+        if (!theta_hat) return ECHO_EINVAL;
+    }
+    const Workspace wsp = carve_workspace(ws, B);
+    if (launch_quantize(B, q, w, wsp.q8, wsp.qscale, wsp.wfold, hist, status, stream) != cudaSuccess)
+        return ECHO_ECUDA;
+    if (n_tokens > 0) {
+        CUtensorMap kmap, qmap;
+        int rc = encode_tmap_bytes_2d(&kmap, k8, ECHO_DIM, static_cast<uint64_t>(n_tokens), ECHO_DIM, kTileM);
+        if (rc) return rc;
+        rc = encode_tmap_bytes_2d(&qmap, wsp.q8, ECHO_DIM, static_cast<uint64_t>(B) * ECHO_HEADS, ECHO_DIM,
+                                  ECHO_HEADS);
+        if (rc) return rc;
+        const int sms = sm_count();
+        if (sms <= 0) return ECHO_ECUDA;
+        const int64_t tiles_ub = n_tokens / kTileM + B;
+        const int grid = static_cast<int>(tiles_ub < sms ? tiles_ub : sms);
+        const size_t smem = smem_bytes(B);
+        ECHO_CUDA_OK(cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(smem)));
+        ScoreArgs args{B, tok_off, n_tokens, wsp.wfold, ks, scores, theta_hat, hist, status};
+        score_kernel<<<grid, kThreads, smem, stream>>>(kmap, qmap, args);
+        ECHO_CUDA_OK(cudaGetLastError());
+    }
+    if (early) {
+        ECHO_CUDA_OK(launch_early_select(B, tok_off, n_tokens, scores, theta_hat, early_cap, *early, status, stats,
+                                         stream));
+        const int rc = stream_wait(copy_stream, stream);
+        if (rc) return rc;
+        ECHO_CUDA_OK(launch_recall(B, tok_off, n_tokens, early->C, early->early_tok, early->early_slot,
+                                   early->early_cnt, early->host_kv, early->dev_kv, early->row_bytes, status,
+                                   copy_stream));
+    }
+    return ECHO_OK;
+}

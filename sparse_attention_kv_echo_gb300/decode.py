@@ -1,0 +1,68 @@
+"""One layer's decode step through the libecho C ABI, on fixed-size buffers.
+
+A DecodeLayer owns the torch tensors one layer needs for B requests (scores,
+histogram, threshold state, selection, the GPU cache and its lists, the
+workspace) and issues the three calls of a step:
+    echo_index_scores  -> scores, shifted-score histogram, early fetch (+recall)
+    echo_topk_select   -> exact top-k indices, k-th score, EMA threshold
+    echo_cache_step    -> free / allocate / recall, slot of every selection
+Every buffer keeps its address and size, so ``step`` can be captured into a
+CUDA graph and replayed; ``q_in``/``w_in`` are the inputs a graph reads.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _lib as L
+
+
+class DecodeLayer:
+    def __init__(self, tok_off, k8: torch.Tensor, ks: torch.Tensor, k: int, C: int,
+                 host_pool: torch.Tensor, alpha: float = 0.5, predictor: bool = True,
+                 early_cap: int = -1, device="cuda"):
+        tok_off = torch.as_tensor(tok_off, dtype=torch.int64)
+        self.B = int(tok_off.numel() - 1)
+        self.n_tokens = int(k8.shape[0])
+        self.k, self.C, self.alpha = int(k), int(C), float(alpha)
+        self.predictor, self.early_cap = bool(predictor), int(early_cap)
+        self.tok_off = tok_off.to(device)
+        self.k8, self.ks = k8, ks
+        f32 = dict(dtype=torch.float32, device=device)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.scores = torch.zeros(max(self.n_tokens, 1), **f32)
+        self.hist = torch.zeros((self.B, 256), **i32)
+        self.theta = torch.full((self.B,), math.inf, **f32)
+        self.sel_idx = torch.full((self.B, self.k), -1, **i32)
+        self.sel_slot = torch.full((self.B, self.k), -1, **i32)
+        self.kth = torch.zeros((self.B,), **f32)
+        self.ws = torch.zeros(L.workspace_size(self.B), dtype=torch.uint8, device=device)
+        self.status = torch.zeros(1, **i32)
+        self.stats = torch.zeros(L.STATS_N, **i32)
+        self.q_in = torch.zeros((self.B, L.HEADS, L.DIM), **f32)
+        self.w_in = torch.zeros((self.B, L.HEADS), **f32)
+        self.cache = L.LayerCache(self.B, self.n_tokens, self.C, host_pool, device=device)
+
+    def reset(self):
+        self.cache.reset()
+        self.theta.fill_(math.inf)
+        self.status.zero_()
+        self.stats.zero_()
+
+    def step(self, q: torch.Tensor | None = None, w: torch.Tensor | None = None, stream=None,
+             copy_stream=None):
+        """Enqueue one decode step (q [B,64,128] f32, w [B,64] f32; defaults q_in / w_in)."""
+        q = self.q_in if q is None else q
+        w = self.w_in if w is None else w
+        L.index_scores(self.tok_off, self.n_tokens, q, w, self.k8, self.ks, self.scores, self.theta,
+                       self.hist, self.ws, self.status, cache=self.cache if self.predictor else None,
+                       early_cap=self.early_cap, stats=self.stats, stream=stream, copy_stream=copy_stream)
+        L.topk_select(self.tok_off, self.n_tokens, self.scores, self.k, self.hist, self.theta, self.alpha,
+                      self.sel_idx, self.kth, self.status, stats=self.stats, stream=stream)
+        L.cache_step(self.tok_off, self.n_tokens, self.sel_idx, self.cache, self.sel_slot, self.status,
+                     stats=self.stats, stream=stream, copy_stream=copy_stream)
+
+    def kernel_launches_per_step(self) -> int:
+        # quantize + score (+ early select + early recall) + top-k + cache step + recall
+        return 2 + (2 if self.predictor else 0) + 1 + 2

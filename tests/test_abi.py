@@ -1,0 +1,102 @@
+"""The C-ABI library builds, loads and exports every entry point its header
+declares; host-side argument checks answer without touching a GPU (CPU only)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "echo.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:[\w\s\*]+?)\b(echo_\w+)\s*\(", src, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from sparse_attention_kv_echo_gb300 import build, lib
+    build.build()
+    return lib.load()
+
+
+def test_header_declares_the_calls():
+    names = _declared()
+    for want in ("echo_index_scores", "echo_topk_select", "echo_cache_step", "echo_quantize_q",
+                 "echo_workspace_size"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    from sparse_attention_kv_echo_gb300 import build
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (echo_\w+)", out))
+    for name in _declared():
+        assert name in exported, name
+        assert hasattr(L, name)
+
+
+def test_binding_lists_every_export(L):
+    from sparse_attention_kv_echo_gb300 import lib
+    assert sorted(lib.EXPORTS) == _declared()
+
+
+def test_workspace_size(L):
+    from sparse_attention_kv_echo_gb300 import lib
+    assert lib.workspace_size(1) >= 64 * 128 + 2 * 64 * 4
+    assert lib.workspace_size(8) >= 8 * (64 * 128 + 2 * 64 * 4)
+    assert lib.workspace_size(0) == 0
+
+
+def test_host_checks_reject_bad_arguments(L):
+    """These return before any CUDA call, so they run without a GPU."""
+    from sparse_attention_kv_echo_gb300 import lib
+    v = ctypes.c_void_p
+    dummy = v(0x1000)
+    # B <= 0, B too large, negative sizes
+    assert L.echo_index_scores(0, dummy, 10, dummy, dummy, dummy, dummy, dummy, None, None, None, -1,
+                               dummy, 1 << 20, dummy, None, None, None) == lib.ECHO_EINVAL
+    assert L.echo_index_scores(lib.MAX_REQUESTS + 1, dummy, 10, dummy, dummy, dummy, dummy, dummy, None,
+                               None, None, -1, dummy, 1 << 30, dummy, None, None, None) == lib.ECHO_EUNSUPPORTED
+    # missing q
+    assert L.echo_index_scores(1, dummy, 10, None, dummy, dummy, dummy, dummy, None, None, None, -1,
+                               dummy, 1 << 20, dummy, None, None, None) == lib.ECHO_EINVAL
+    # misaligned keys (must be 16-byte aligned)
+    assert L.echo_index_scores(1, dummy, 10, dummy, dummy, v(0x1001), dummy, dummy, None, None, None, -1,
+                               dummy, 1 << 20, dummy, None, None, None) == lib.ECHO_EINVAL
+    # workspace too small
+    assert L.echo_index_scores(2, dummy, 10, dummy, dummy, dummy, dummy, dummy, None, None, None, -1,
+                               dummy, 16, dummy, None, None, None) == lib.ECHO_ECAPACITY
+    assert L.echo_topk_select(1, dummy, 10, dummy, 0, None, None, 0.5, dummy, dummy, dummy, None,
+                              None) == lib.ECHO_EINVAL
+    assert L.echo_topk_select(-3, dummy, 10, dummy, 4, None, None, 0.5, dummy, dummy, dummy, None,
+                              None) == lib.ECHO_EINVAL
+    assert L.echo_quantize_q(-1, dummy, dummy, dummy, dummy, dummy, dummy, None) == lib.ECHO_EINVAL
+    assert L.echo_quantize_q(0, None, None, None, None, None, None, None) == lib.ECHO_OK
+
+
+def test_cache_checks(L):
+    from sparse_attention_kv_echo_gb300 import lib
+    v = ctypes.c_void_p
+    s = lib.EchoCacheStruct()
+    for f, _ in lib.EchoCacheStruct._fields_[:11]:
+        setattr(s, f, 0x2000)
+    s.row_bytes, s.C = 1152, 64
+    dummy = v(0x1000)
+    # k (m) larger than C
+    assert L.echo_cache_step(1, dummy, 100, dummy, 65, ctypes.byref(s), dummy, dummy, None, None,
+                             None) == lib.ECHO_ECAPACITY
+    s.C = 48   # not a multiple of 32
+    assert L.echo_cache_step(1, dummy, 100, dummy, 16, ctypes.byref(s), dummy, dummy, None, None,
+                             None) == lib.ECHO_ECAPACITY
+    s.C, s.row_bytes = 64, 1000  # row not a multiple of 16 bytes
+    assert L.echo_cache_step(1, dummy, 100, dummy, 16, ctypes.byref(s), dummy, dummy, None, None,
+                             None) == lib.ECHO_EUNSUPPORTED
+    s.row_bytes, s.dev_kv = 1152, None
+    assert L.echo_cache_step(1, dummy, 100, dummy, 16, ctypes.byref(s), dummy, dummy, None, None,
+                             None) == lib.ECHO_EINVAL

@@ -1,0 +1,113 @@
+"""GPU parity of whole decode steps (scores -> early fetch -> top-k -> cache step
+-> recall) over many steps against the oracle's own state machine, on the
+workloads' shapes: every step bit-exact on histograms, selections, thresholds,
+tables, slots and recalled bytes; scores within the fp64 tolerance."""
+import numpy as np
+import pytest
+import torch
+
+from sparse_attention_kv_echo_gb300 import DecodeLayer
+from sparse_attention_kv_echo_gb300 import _lib as L
+from sparse_attention_kv_echo_gb300 import workloads as wl
+from tests._parity import run_decode
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    L.load(build_if_missing=True)
+
+
+def test_tiny_workload_all_steps():
+    w = wl.WORKLOADS["tiny"]
+    rep = run_decode(w, w.steps, predictor=True)
+    assert sum(rep["early"]) > 0                       # the predictor fetched something early
+    assert rep["misses"][0] == w.k                     # first step: everything misses
+
+
+def test_tiny_predictor_off():
+    w = wl.WORKLOADS["tiny"]
+    rep = run_decode(w, 6, predictor=False)
+    assert rep["early"] == []
+
+
+@pytest.mark.parametrize("cap", [0, 16])
+def test_early_cap(cap):
+    w = wl.scaled(wl.WORKLOADS["tiny"], "cap", lengths=(6000,))
+    run_decode(w, 5, predictor=True, cap=cap)
+
+
+def test_ragged_batch_edge_cases():
+    # a request shorter than k, an empty one, a 1-token one, ragged tile tails
+    w = wl.scaled(wl.WORKLOADS["tiny"], "ragged", B=6, lengths=(3000, 200, 0, 1, 4173, 129), k=256, C=320)
+    run_decode(w, 6, predictor=True)
+
+
+def test_c_equals_k():
+    w = wl.scaled(wl.WORKLOADS["tiny"], "ck", B=2, lengths=(5000, 2500), k=256, C=256)
+    run_decode(w, 5, predictor=True)
+
+
+def test_redraw_bursts():
+    w = wl.scaled(wl.WORKLOADS["skewed"], "burst", B=4, lengths=(9000, 4096, 20000, 5000), C=2560)
+    run_decode(w, 10, predictor=True)
+
+
+def test_batch_workload_full_size():
+    """8 x 32768, k=2048, C=4096: every table/selection bit-exact, scores sampled."""
+    w = wl.WORKLOADS["batch"]
+    rep = run_decode(w, 6, predictor=True, score_sample=1024)
+    assert rep["fallbacks"] >= 1            # the unshifted first step overflows the boundary bin
+
+
+def test_hot_set_workload_one_layer():
+    """The DeepSeek-V3.2-shaped workload (32 x 131072, hot set), one layer, a few steps."""
+    w = wl.WORKLOADS["v32"]
+    rep = run_decode(w, 3, predictor=True, score_sample=256, keys_device="cuda")
+    assert rep["misses"][0] == w.B * w.k
+
+
+def test_skewed_workload_both_predictor_modes():
+    w = wl.WORKLOADS["skewed"]
+    a = run_decode(w, 3, predictor=True, score_sample=256, check_every_score_step=False, keys_device="cuda")
+    b = run_decode(w, 3, predictor=False, score_sample=256, check_every_score_step=False, keys_device="cuda")
+    assert a["misses"][0] == b["misses"][0]
+
+
+def test_graph_replay_equals_eager():
+    """One captured decode step, replayed, gives the same bytes as eager steps."""
+    w = wl.scaled(wl.WORKLOADS["batch"], "graph", B=3, lengths=(9000, 20000, 4000), k=512, C=1024)
+    dev = "cuda"
+    off = wl.tok_offsets(w.lengths)
+    k8, ks = wl.make_keys(w, 0)
+    wt = wl.make_weights(w, 0)
+    host = wl.make_host_pool(w, 0, pin=True)
+    eager = DecodeLayer(off, k8.to(dev), ks.to(dev), w.k, w.C, host)
+    graph = DecodeLayer(off, k8.to(dev), ks.to(dev), w.k, w.C, host)
+    qs = wl.QueryStream(w, 0)
+    queries = [qs.next() for _ in range(6)]
+    for lay in (eager, graph):
+        lay.q_in.copy_(queries[0].to(dev))
+        lay.w_in.copy_(wt.to(dev))
+        lay.step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            graph.step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for t in range(1, 6):
+        eager.q_in.copy_(queries[t].to(dev))
+        eager.step()
+        graph.q_in.copy_(queries[t].to(dev))
+        g.replay()
+        torch.cuda.synchronize()
+        for name in ("scores", "hist", "theta", "sel_idx", "sel_slot", "kth"):
+            assert torch.equal(getattr(eager, name), getattr(graph, name)), (t, name)
+        for name in ("tok2slot", "slot2tok", "freebits", "dev_kv"):
+            assert torch.equal(getattr(eager.cache, name), getattr(graph.cache, name)), (t, name)
+        assert eager.status.item() == 0 and graph.status.item() == 0
