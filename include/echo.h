@@ -5,8 +5,9 @@
  * Per layer and decode step the path computes, for a batch of B requests:
  *   1. the indexer score of every context token (echo_quantize_q,
  *      echo_index_scores),
- *   2. the exact top-k tokens and the EMA threshold prediction
- *      (echo_topk_select), with tokens above the prediction fetched early,
+ *   2. the tokens above the predicted threshold, fetched early
+ *      (echo_early_fetch), then the exact top-k tokens and the EMA threshold
+ *      prediction (echo_topk_select),
  *   3. the GPU-cache step: free unselected slots, allocate slots for the
  *      misses, recall the missing KV rows from the host pool (echo_cache_step).
  *
@@ -57,7 +58,7 @@ typedef struct CUstream_st* echo_stream_t; /* a cudaStream_t; NULL = legacy defa
 /* host-side return codes */
 #define ECHO_OK 0
 #define ECHO_EINVAL (-1)        /* NULL pointer, negative size, misaligned pointer */
-#define ECHO_ECAPACITY (-2)     /* k > C, workspace too small, C not a multiple of 32 */
+#define ECHO_ECAPACITY (-2)     /* k > C, C not a multiple of 32 */
 #define ECHO_EUNSUPPORTED (-3)  /* B above ECHO_MAX_REQUESTS, row size not a multiple of 16 */
 #define ECHO_ECUDA (-4)         /* a CUDA launch or driver call failed */
 
@@ -118,50 +119,53 @@ typedef struct echo_cache {
     int32_t reserved;
 } echo_cache;
 
-/* Bytes of device workspace the calls below need for B requests.  One
- * workspace may be shared by consecutive calls on the same stream. */
-size_t echo_workspace_size(int B);
-
 /*
  * Query quantisation [IDX; the sources only say the score GEMM runs in FP8].
  * Per (request, head): scale = the smallest power of two 2^e with
  * max_d |q[b,h,d]| <= 448 * 2^e (e >= -126; 1 for an all-zero row),
  * q8[b,h,d] = E4M3 round-to-nearest-even(q / scale), and
  * wfold[b,h] = w[b,h] * scale (fp32).
- *   q [B,64,128] f32, w [B,64] f32 -> q8 [B,64,128] u8, qscale [B,64] f32, wfold [B,64] f32
+ *   q [B,64,128] f32 (16-byte aligned), w [B,64] f32
+ *   -> q8 [B,64,128] u8, qscale [B,64] f32, wfold [B,64] f32 (16-byte aligned).
+ *   hist [B,256] u32 (may be NULL) is set to zero, ready for echo_index_scores.
  * NaN/Inf in q or w -> ECHO_ST_NAN.
  */
 int echo_quantize_q(int B, const float* q, const float* w, uint8_t* q8, float* qscale,
-                    float* wfold, int32_t* status, echo_stream_t stream);
+                    float* wfold, uint32_t* hist, int32_t* status, echo_stream_t stream);
 
 /*
- * Indexer score of every token [IDX]; 256-bin histogram [EXPL panel
- * "Prefill: one-round histogram"]; early fetch [EXPL panel "Decode: fetch
- * above a predicted threshold"].
+ * Indexer score of every token [IDX] and the 256-bin histogram of the
+ * threshold-shifted scores [EXPL panel "Prefill: one-round histogram"].
  *   scores[t] = ks[t] * sum_h wfold[b,h] * max(0, sum_d q8[b,h,d] * k8[t,d])
  *   for every token row t of request b, which equals the definition
  *   sum_h w[h] * ReLU(q[h] . k[t]) over the dequantised E4M3 values.
- *   Inputs: q [B,64,128] f32, w [B,64] f32 (quantised inside, into ws),
- *   k8 [n_tokens,128] E4M3 bytes (16-byte aligned), ks [n_tokens] f32.
+ *   Inputs: q8 [B,64,128] u8 and wfold [B,64] f32 from echo_quantize_q,
+ *   k8 [n_tokens,128] E4M3 bytes, ks [n_tokens] f32 (q8 and k8 16-byte aligned).
  *   Outputs: scores [n_tokens] f32 (rows outside every request untouched);
- *   hist [B,256] u32 (may be NULL; overwritten): per request, counts of
+ *   hist [B,256] u32 (may be NULL): ADDS, per request, the counts of
  *   bin = top 8 bits of orderkey(fp32(score - shift)), shift = theta_hat[b]
- *   when finite, else 0; orderkey maps a float to a uint32 in the same order
- *   (-0 counted as +0).  theta_hat [B] f32 (may be NULL = no shift) is read
- *   only here.
- *   early (may be NULL = predictor off): tokens with score > theta_hat[b]
- *   that are not resident, in ascending order, at most min(early_cap, free
- *   slots) of them (early_cap < 0: no cap but the free slots), take the
- *   lowest free slots in ascending order and become resident; the lists go
- *   to early->early_tok / early_slot / early_cnt and their rows are recalled
- *   into dev_kv on copy_stream (may equal stream), overlapping what follows.
- *   ws: echo_workspace_size(B) bytes, 256-byte aligned.
+ *   when finite, else 0, so it must hold zeros on entry (echo_quantize_q
+ *   clears it); orderkey maps a float to a uint32 in the same order (-0
+ *   counted as +0).  theta_hat [B] f32 may be NULL (no shift).
  */
-int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens, const float* q,
-                      const float* w, const uint8_t* k8, const float* ks, float* scores,
-                      const float* theta_hat, uint32_t* hist, const echo_cache* early,
-                      int early_cap, void* ws, size_t ws_bytes, int32_t* status, uint32_t* stats,
-                      echo_stream_t stream, echo_stream_t copy_stream);
+int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens, const uint8_t* q8,
+                      const float* wfold, const uint8_t* k8, const float* ks, float* scores,
+                      const float* theta_hat, uint32_t* hist, int32_t* status,
+                      echo_stream_t stream);
+
+/*
+ * Early fetch [EXPL panel "Decode: fetch above a predicted threshold"]: before
+ * top-k is known, the tokens with score > theta_hat[b] that are not resident,
+ * in ascending order, at most min(early_cap, free slots) of them (early_cap
+ * < 0: no cap but the free slots), take the lowest free slots in ascending
+ * order and become resident.  The lists go to cache->early_tok / early_slot /
+ * early_cnt and the rows are recalled into dev_kv on copy_stream (may equal
+ * stream), overlapping the top-k that follows.  theta_hat = +inf (no
+ * prediction yet) fetches nothing.
+ */
+int echo_early_fetch(int B, const int64_t* tok_off, int64_t n_tokens, const float* scores,
+                     const float* theta_hat, int early_cap, const echo_cache* cache, int32_t* status,
+                     uint32_t* stats, echo_stream_t stream, echo_stream_t copy_stream);
 
 /*
  * Exact top-k per request [EXPL section 2: "guarantees an exact top-k"] and

@@ -21,8 +21,8 @@ STAT_TOPK_FALLBACK, STAT_BOUNDARY_MAX, STAT_EARLY, STAT_MISSES, STAT_EARLY_USED 
 STATS_N = 8
 HEADS, DIM, MAX_REQUESTS = 64, 128, 4096
 
-EXPORTS = ("echo_cache_step", "echo_device_sm_count", "echo_host_device_alias", "echo_index_scores",
-           "echo_quantize_q", "echo_topk_select", "echo_workspace_size")
+EXPORTS = ("echo_cache_step", "echo_device_sm_count", "echo_early_fetch", "echo_host_device_alias",
+           "echo_index_scores", "echo_quantize_q", "echo_topk_select")
 
 _vp = ctypes.c_void_p
 
@@ -60,14 +60,14 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
                                    "python -m sparse_attention_kv_echo_gb300.build")
             _build.build()
         L = ctypes.CDLL(_build.LIB)
-        i32, i64, f32, sz = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
-        L.echo_workspace_size.restype = sz
-        L.echo_workspace_size.argtypes = [i32]
+        i32, i64, f32 = ctypes.c_int, ctypes.c_int64, ctypes.c_float
         L.echo_quantize_q.restype = i32
-        L.echo_quantize_q.argtypes = [i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+        L.echo_quantize_q.argtypes = [i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
         L.echo_index_scores.restype = i32
-        L.echo_index_scores.argtypes = [i32, _vp, i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
-                                        ctypes.POINTER(EchoCacheStruct), i32, _vp, sz, _vp, _vp, _vp, _vp]
+        L.echo_index_scores.argtypes = [i32, _vp, i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+        L.echo_early_fetch.restype = i32
+        L.echo_early_fetch.argtypes = [i32, _vp, i64, _vp, _vp, i32, ctypes.POINTER(EchoCacheStruct), _vp,
+                                       _vp, _vp, _vp]
         L.echo_topk_select.restype = i32
         L.echo_topk_select.argtypes = [i32, _vp, i64, _vp, i32, _vp, _vp, f32, _vp, _vp, _vp, _vp, _vp]
         L.echo_cache_step.restype = i32
@@ -102,10 +102,6 @@ def _check(call, rc):
         raise EchoError(call, rc)
 
 
-def workspace_size(B: int) -> int:
-    return load().echo_workspace_size(int(B))
-
-
 def host_device_alias(host_tensor: torch.Tensor) -> int:
     out = _vp()
     _check("echo_host_device_alias", load().echo_host_device_alias(host_tensor.data_ptr(), ctypes.byref(out)))
@@ -116,22 +112,27 @@ def sm_count() -> int:
     return load().echo_device_sm_count()
 
 
-def quantize_q(q, w, q8, qscale, wfold, status, stream=None):
+def quantize_q(q, w, q8, qscale, wfold, status, hist=None, stream=None):
     B = q.shape[0]
     _check("echo_quantize_q", load().echo_quantize_q(B, _ptr(q), _ptr(w), _ptr(q8), _ptr(qscale),
-                                                    _ptr(wfold), _ptr(status), _stream(stream)))
+                                                    _ptr(wfold), _ptr(hist), _ptr(status), _stream(stream)))
 
 
-def index_scores(tok_off, n_tokens, q, w, k8, ks, scores, theta_hat, hist, ws, status, cache=None,
-                 early_cap=-1, stats=None, stream=None, copy_stream=None):
-    B = q.shape[0]
-    cs = ctypes.byref(cache.struct) if cache is not None else None
+def index_scores(tok_off, n_tokens, q8, wfold, k8, ks, scores, theta_hat, hist, status, stream=None):
+    B = q8.shape[0]
+    _check("echo_index_scores", load().echo_index_scores(
+        B, _ptr(tok_off), int(n_tokens), _ptr(q8), _ptr(wfold), _ptr(k8), _ptr(ks), _ptr(scores),
+        _ptr(theta_hat), _ptr(hist), _ptr(status), _stream(stream)))
+
+
+def early_fetch(tok_off, n_tokens, scores, theta_hat, early_cap, cache, status, stats=None, stream=None,
+                copy_stream=None):
+    B = tok_off.shape[0] - 1
     st = _stream(stream)
     cst = _stream(copy_stream) if copy_stream is not None else st
-    _check("echo_index_scores", load().echo_index_scores(
-        B, _ptr(tok_off), int(n_tokens), _ptr(q), _ptr(w), _ptr(k8), _ptr(ks), _ptr(scores),
-        _ptr(theta_hat), _ptr(hist), cs, int(early_cap), _ptr(ws), ws.numel() * ws.element_size(),
-        _ptr(status), _ptr(stats), st, cst))
+    _check("echo_early_fetch", load().echo_early_fetch(
+        B, _ptr(tok_off), int(n_tokens), _ptr(scores), _ptr(theta_hat), int(early_cap),
+        ctypes.byref(cache.struct), _ptr(status), _ptr(stats), st, cst))
 
 
 def topk_select(tok_off, n_tokens, scores, k, hist, theta_hat, alpha, sel_idx, kth, status, stats=None,

@@ -1,27 +1,11 @@
-// echo_abi.cu -- host-side plumbing of the libecho C ABI: workspace sizing,
-// TMA descriptor encoding through the driver entry point, stream ordering,
-// argument checks and small queries.
+// echo_abi.cu -- host-side plumbing of the libecho C ABI: TMA descriptor
+// encoding through the driver entry point, stream ordering, argument checks
+// and small queries.
 #include <string.h>
 
 #include "echo_internal.h"
 
 namespace echo {
-
-size_t workspace_bytes(int B) {
-    const size_t b = B > 0 ? static_cast<size_t>(B) : 0;
-    return round_up(b * ECHO_HEADS * ECHO_DIM, 256) + 2 * round_up(b * ECHO_HEADS * sizeof(float), 256);
-}
-
-Workspace carve_workspace(void* ws, int B) {
-    uint8_t* p = static_cast<uint8_t*>(ws);
-    Workspace w;
-    w.q8 = p;
-    p += round_up(static_cast<size_t>(B) * ECHO_HEADS * ECHO_DIM, 256);
-    w.qscale = reinterpret_cast<float*>(p);
-    p += round_up(static_cast<size_t>(B) * ECHO_HEADS * sizeof(float), 256);
-    w.wfold = reinterpret_cast<float*>(p);
-    return w;
-}
 
 int sm_count() {
     int dev = 0, n = 0;
@@ -89,8 +73,6 @@ int check_cache(const echo_cache* c, int B, int m) {
 }  // namespace echo
 
 extern "C" {
-
-size_t echo_workspace_size(int B) { return echo::workspace_bytes(B); }
 
 int echo_host_device_alias(const void* host_ptr, const void** device_ptr) {
     if (!host_ptr || !device_ptr) return ECHO_EINVAL;

@@ -338,3 +338,23 @@ extern "C" int echo_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, 
                                cache->host_kv, cache->dev_kv, cache->row_bytes, status, copy_stream));
     return ECHO_OK;
 }
+
+extern "C" int echo_early_fetch(int B, const int64_t* tok_off, int64_t n_tokens, const float* scores,
+                                const float* theta_hat, int early_cap, const echo_cache* cache, int32_t* status,
+                                uint32_t* stats, echo_stream_t stream, echo_stream_t copy_stream) {
+    using namespace echo;
+    if (B <= 0 || n_tokens < 0) return ECHO_EINVAL;
+    if (B > ECHO_MAX_REQUESTS) return ECHO_EUNSUPPORTED;
+    if (!tok_off || !theta_hat || !status || (n_tokens > 0 && !scores)) return ECHO_EINVAL;
+    if (n_tokens >= (1ll << 31)) return ECHO_EUNSUPPORTED;
+    int rc = check_cache(cache, B, 0);
+    if (rc) return rc;
+    ECHO_CUDA_OK(launch_early_select(B, tok_off, n_tokens, scores, theta_hat, early_cap, *cache, status, stats,
+                                     stream));
+    rc = stream_wait(copy_stream, stream);
+    if (rc) return rc;
+    ECHO_CUDA_OK(launch_recall(B, tok_off, n_tokens, cache->C, cache->early_tok, cache->early_slot,
+                               cache->early_cnt, cache->host_kv, cache->dev_kv, cache->row_bytes, status,
+                               copy_stream));
+    return ECHO_OK;
+}

@@ -14,15 +14,6 @@ inline bool is_aligned(const void* p, size_t a) { return (reinterpret_cast<uintp
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace layout for B requests: q8 [B,64,128] u8 | qscale [B,64] f32 | wfold [B,64] f32.
-struct Workspace {
-    uint8_t* q8;
-    float* qscale;
-    float* wfold;
-};
-size_t workspace_bytes(int B);
-Workspace carve_workspace(void* ws, int B);
-
 // SM count of the current device.
 int sm_count();
 

@@ -79,11 +79,13 @@ cudaError_t launch_quantize(int B, const float* q, const float* w, uint8_t* q8, 
 }  // namespace echo
 
 extern "C" int echo_quantize_q(int B, const float* q, const float* w, uint8_t* q8, float* qscale, float* wfold,
-                               int32_t* status, echo_stream_t stream) {
+                               uint32_t* hist, int32_t* status, echo_stream_t stream) {
     if (B < 0 || B > ECHO_MAX_REQUESTS) return B < 0 ? ECHO_EINVAL : ECHO_EUNSUPPORTED;
     if (B == 0) return ECHO_OK;
     if (!q || !w || !q8 || !qscale || !wfold) return ECHO_EINVAL;
-    if (!echo::is_aligned(q, 16) || !echo::is_aligned(q8, 4) || !echo::is_aligned(w, 4)) return ECHO_EINVAL;
-    return echo::launch_quantize(B, q, w, q8, qscale, wfold, nullptr, status, stream) == cudaSuccess ? ECHO_OK
-                                                                                                    : ECHO_ECUDA;
+    if (!echo::is_aligned(q, 16) || !echo::is_aligned(q8, 16) || !echo::is_aligned(w, 4) ||
+        !echo::is_aligned(wfold, 16) || !echo::is_aligned(qscale, 4) || !echo::is_aligned(hist, 4))
+        return ECHO_EINVAL;
+    return echo::launch_quantize(B, q, w, q8, qscale, wfold, hist, status, stream) == cudaSuccess ? ECHO_OK
+                                                                                                 : ECHO_ECUDA;
 }

@@ -360,53 +360,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 }  // namespace echo
 
-extern "C" int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens, const float* q, const float* w,
-                                 const uint8_t* k8, const float* ks, float* scores, const float* theta_hat,
-                                 uint32_t* hist, const echo_cache* early, int early_cap, void* ws, size_t ws_bytes,
-                                 int32_t* status, uint32_t* stats, echo_stream_t stream,
-                                 echo_stream_t copy_stream) {
+extern "C" int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens, const uint8_t* q8,
+                                 const float* wfold, const uint8_t* k8, const float* ks, float* scores,
+                                 const float* theta_hat, uint32_t* hist, int32_t* status, echo_stream_t stream) {
     using namespace echo;
     if (B <= 0 || n_tokens < 0) return ECHO_EINVAL;
     if (B > ECHO_MAX_REQUESTS) return ECHO_EUNSUPPORTED;
-    if (!tok_off || !q || !w || !ws || !status) return ECHO_EINVAL;
+    if (!tok_off || !q8 || !wfold || !status) return ECHO_EINVAL;
     if (n_tokens > 0 && (!k8 || !ks || !scores)) return ECHO_EINVAL;
     if (n_tokens >= (1ll << 31)) return ECHO_EUNSUPPORTED;
-    if (!is_aligned(q, 16) || !is_aligned(ws, 256) || !is_aligned(k8, 16)) return ECHO_EINVAL;
-    if (ws_bytes < workspace_bytes(B)) return ECHO_ECAPACITY;
-    if (early) {
-        const int rc = check_cache(early, B, 0);
-        if (rc) return rc;
-        if (!theta_hat) return ECHO_EINVAL;
-    }
-    const Workspace wsp = carve_workspace(ws, B);
-    if (launch_quantize(B, q, w, wsp.q8, wsp.qscale, wsp.wfold, hist, status, stream) != cudaSuccess)
-        return ECHO_ECUDA;
-    if (n_tokens > 0) {
-        CUtensorMap kmap, qmap;
-        int rc = encode_tmap_bytes_2d(&kmap, k8, ECHO_DIM, static_cast<uint64_t>(n_tokens), ECHO_DIM, kTileM);
-        if (rc) return rc;
-        rc = encode_tmap_bytes_2d(&qmap, wsp.q8, ECHO_DIM, static_cast<uint64_t>(B) * ECHO_HEADS, ECHO_DIM,
-                                  ECHO_HEADS);
-        if (rc) return rc;
-        const int sms = sm_count();
-        if (sms <= 0) return ECHO_ECUDA;
-        const int64_t tiles_ub = n_tokens / kTileM + B;
-        const int grid = static_cast<int>(tiles_ub < sms ? tiles_ub : sms);
-        const size_t smem = smem_bytes(B);
-        ECHO_CUDA_OK(cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          static_cast<int>(smem)));
-        ScoreArgs args{B, tok_off, n_tokens, wsp.wfold, ks, scores, theta_hat, hist, status};
-        score_kernel<<<grid, kThreads, smem, stream>>>(kmap, qmap, args);
-        ECHO_CUDA_OK(cudaGetLastError());
-    }
-    if (early) {
-        ECHO_CUDA_OK(launch_early_select(B, tok_off, n_tokens, scores, theta_hat, early_cap, *early, status, stats,
-                                         stream));
-        const int rc = stream_wait(copy_stream, stream);
-        if (rc) return rc;
-        ECHO_CUDA_OK(launch_recall(B, tok_off, n_tokens, early->C, early->early_tok, early->early_slot,
-                                   early->early_cnt, early->host_kv, early->dev_kv, early->row_bytes, status,
-                                   copy_stream));
-    }
+    if (!is_aligned(q8, 16) || !is_aligned(wfold, 16) || !is_aligned(k8, 16)) return ECHO_EINVAL;
+    if (n_tokens == 0) return ECHO_OK;
+    CUtensorMap kmap, qmap;
+    int rc = encode_tmap_bytes_2d(&kmap, k8, ECHO_DIM, static_cast<uint64_t>(n_tokens), ECHO_DIM, kTileM);
+    if (rc) return rc;
+    rc = encode_tmap_bytes_2d(&qmap, q8, ECHO_DIM, static_cast<uint64_t>(B) * ECHO_HEADS, ECHO_DIM, ECHO_HEADS);
+    if (rc) return rc;
+    const int sms = sm_count();
+    if (sms <= 0) return ECHO_ECUDA;
+    const int64_t tiles_ub = n_tokens / kTileM + B;
+    const int grid = static_cast<int>(tiles_ub < sms ? tiles_ub : sms);
+    const size_t smem = smem_bytes(B);
+    ECHO_CUDA_OK(cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(smem)));
+    ScoreArgs args{B, tok_off, n_tokens, wfold, ks, scores, theta_hat, hist, status};
+    score_kernel<<<grid, kThreads, smem, stream>>>(kmap, qmap, args);
+    ECHO_CUDA_OK(cudaGetLastError());
     return ECHO_OK;
 }

@@ -2,8 +2,10 @@
 
 A DecodeLayer owns the torch tensors one layer needs for B requests (scores,
 histogram, threshold state, selection, the GPU cache and its lists, the
-workspace) and issues the three calls of a step:
-    echo_index_scores  -> scores, shifted-score histogram, early fetch (+recall)
+quantised query) and issues the calls of a step:
+    echo_quantize_q    -> E4M3 query, folded head weights, cleared histogram
+    echo_index_scores  -> scores, shifted-score histogram
+    echo_early_fetch   -> tokens above the predicted threshold (+ recall)
     echo_topk_select   -> exact top-k indices, k-th score, EMA threshold
     echo_cache_step    -> free / allocate / recall, slot of every selection
 Every buffer keeps its address and size, so ``step`` can be captured into a
@@ -37,7 +39,9 @@ class DecodeLayer:
         self.sel_idx = torch.full((self.B, self.k), -1, **i32)
         self.sel_slot = torch.full((self.B, self.k), -1, **i32)
         self.kth = torch.zeros((self.B,), **f32)
-        self.ws = torch.zeros(L.workspace_size(self.B), dtype=torch.uint8, device=device)
+        self.q8 = torch.zeros((self.B, L.HEADS, L.DIM), dtype=torch.uint8, device=device)
+        self.qscale = torch.zeros((self.B, L.HEADS), **f32)
+        self.wfold = torch.zeros((self.B, L.HEADS), **f32)
         self.status = torch.zeros(1, **i32)
         self.stats = torch.zeros(L.STATS_N, **i32)
         self.q_in = torch.zeros((self.B, L.HEADS, L.DIM), **f32)
@@ -55,9 +59,12 @@ class DecodeLayer:
         """Enqueue one decode step (q [B,64,128] f32, w [B,64] f32; defaults q_in / w_in)."""
         q = self.q_in if q is None else q
         w = self.w_in if w is None else w
-        L.index_scores(self.tok_off, self.n_tokens, q, w, self.k8, self.ks, self.scores, self.theta,
-                       self.hist, self.ws, self.status, cache=self.cache if self.predictor else None,
-                       early_cap=self.early_cap, stats=self.stats, stream=stream, copy_stream=copy_stream)
+        L.quantize_q(q, w, self.q8, self.qscale, self.wfold, self.status, hist=self.hist, stream=stream)
+        L.index_scores(self.tok_off, self.n_tokens, self.q8, self.wfold, self.k8, self.ks, self.scores,
+                       self.theta, self.hist, self.status, stream=stream)
+        if self.predictor:
+            L.early_fetch(self.tok_off, self.n_tokens, self.scores, self.theta, self.early_cap, self.cache,
+                          self.status, stats=self.stats, stream=stream, copy_stream=copy_stream)
         L.topk_select(self.tok_off, self.n_tokens, self.scores, self.k, self.hist, self.theta, self.alpha,
                       self.sel_idx, self.kth, self.status, stats=self.stats, stream=stream)
         L.cache_step(self.tok_off, self.n_tokens, self.sel_idx, self.cache, self.sel_slot, self.status,

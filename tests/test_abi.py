@@ -27,7 +27,7 @@ def L():
 def test_header_declares_the_calls():
     names = _declared()
     for want in ("echo_index_scores", "echo_topk_select", "echo_cache_step", "echo_quantize_q",
-                 "echo_workspace_size"):
+                 "echo_early_fetch"):
         assert want in names
 
 
@@ -46,38 +46,37 @@ def test_binding_lists_every_export(L):
     assert sorted(lib.EXPORTS) == _declared()
 
 
-def test_workspace_size(L):
-    from sparse_attention_kv_echo_gb300 import lib
-    assert lib.workspace_size(1) >= 64 * 128 + 2 * 64 * 4
-    assert lib.workspace_size(8) >= 8 * (64 * 128 + 2 * 64 * 4)
-    assert lib.workspace_size(0) == 0
-
-
 def test_host_checks_reject_bad_arguments(L):
     """These return before any CUDA call, so they run without a GPU."""
     from sparse_attention_kv_echo_gb300 import lib
     v = ctypes.c_void_p
     dummy = v(0x1000)
-    # B <= 0, B too large, negative sizes
-    assert L.echo_index_scores(0, dummy, 10, dummy, dummy, dummy, dummy, dummy, None, None, None, -1,
-                               dummy, 1 << 20, dummy, None, None, None) == lib.ECHO_EINVAL
+    # index_scores(B, tok_off, n_tokens, q8, wfold, k8, ks, scores, theta, hist, status, stream)
+    assert L.echo_index_scores(0, dummy, 10, dummy, dummy, dummy, dummy, dummy, None, None, dummy,
+                               None) == lib.ECHO_EINVAL
     assert L.echo_index_scores(lib.MAX_REQUESTS + 1, dummy, 10, dummy, dummy, dummy, dummy, dummy, None,
-                               None, None, -1, dummy, 1 << 30, dummy, None, None, None) == lib.ECHO_EUNSUPPORTED
-    # missing q
-    assert L.echo_index_scores(1, dummy, 10, None, dummy, dummy, dummy, dummy, None, None, None, -1,
-                               dummy, 1 << 20, dummy, None, None, None) == lib.ECHO_EINVAL
+                               None, dummy, None) == lib.ECHO_EUNSUPPORTED
+    # missing q8
+    assert L.echo_index_scores(1, dummy, 10, None, dummy, dummy, dummy, dummy, None, None, dummy,
+                               None) == lib.ECHO_EINVAL
     # misaligned keys (must be 16-byte aligned)
-    assert L.echo_index_scores(1, dummy, 10, dummy, dummy, v(0x1001), dummy, dummy, None, None, None, -1,
-                               dummy, 1 << 20, dummy, None, None, None) == lib.ECHO_EINVAL
-    # workspace too small
-    assert L.echo_index_scores(2, dummy, 10, dummy, dummy, dummy, dummy, dummy, None, None, None, -1,
-                               dummy, 16, dummy, None, None, None) == lib.ECHO_ECAPACITY
+    assert L.echo_index_scores(1, dummy, 10, dummy, dummy, v(0x1001), dummy, dummy, None, None, dummy,
+                               None) == lib.ECHO_EINVAL
+    # negative token count
+    assert L.echo_index_scores(1, dummy, -5, dummy, dummy, dummy, dummy, dummy, None, None, dummy,
+                               None) == lib.ECHO_EINVAL
+    # no tokens: nothing to do, nothing enqueued
+    assert L.echo_index_scores(1, dummy, 0, dummy, dummy, None, None, None, None, None, dummy,
+                               None) == lib.ECHO_OK
+    # early fetch needs the threshold
+    assert L.echo_early_fetch(1, dummy, 10, dummy, None, -1, None, dummy, None, None, None) == lib.ECHO_EINVAL
     assert L.echo_topk_select(1, dummy, 10, dummy, 0, None, None, 0.5, dummy, dummy, dummy, None,
                               None) == lib.ECHO_EINVAL
     assert L.echo_topk_select(-3, dummy, 10, dummy, 4, None, None, 0.5, dummy, dummy, dummy, None,
                               None) == lib.ECHO_EINVAL
-    assert L.echo_quantize_q(-1, dummy, dummy, dummy, dummy, dummy, dummy, None) == lib.ECHO_EINVAL
-    assert L.echo_quantize_q(0, None, None, None, None, None, None, None) == lib.ECHO_OK
+    assert L.echo_quantize_q(-1, dummy, dummy, dummy, dummy, dummy, None, dummy, None) == lib.ECHO_EINVAL
+    assert L.echo_quantize_q(1, dummy, dummy, dummy, dummy, v(0x1004), None, dummy, None) == lib.ECHO_EINVAL
+    assert L.echo_quantize_q(0, None, None, None, None, None, None, None, None) == lib.ECHO_OK
 
 
 def test_cache_checks(L):

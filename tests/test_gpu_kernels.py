@@ -82,6 +82,16 @@ def test_e4m3_conversion_sweep():
     assert bad.size == 0, (x[bad[:5]], got[bad[:5]], ref[bad[:5]])
 
 
+def _scores_gpu(off, n, q, w, k8, ks, scores, theta, hist, status):
+    """quantize_q (clears hist) then index_scores, as a step issues them."""
+    B = q.shape[0]
+    q8 = torch.empty((B, 64, 128), dtype=torch.uint8, device=dev)
+    qs = torch.empty((B, 64), dtype=torch.float32, device=dev)
+    wf = torch.empty((B, 64), dtype=torch.float32, device=dev)
+    L.quantize_q(q, w, q8, qs, wf, status, hist=hist)
+    L.index_scores(off, n, q8, wf, k8, ks, scores, theta, hist, status)
+
+
 def _score_call(w, layer=0, theta=None, device_keys="cpu"):
     off = wl.tok_offsets(w.lengths)
     k8, ks = wl.make_keys(w, layer, device=device_keys)
@@ -91,10 +101,10 @@ def _score_call(w, layer=0, theta=None, device_keys="cpu"):
     scores = torch.full((max(n, 1) + 64,), float("nan"), device=dev)
     hist = torch.zeros((w.B, 256), dtype=torch.int32, device=dev)
     th = torch.full((w.B,), math.inf if theta is None else theta, device=dev)
-    ws = torch.zeros(L.workspace_size(w.B), dtype=torch.uint8, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    L.index_scores(torch.from_numpy(off).to(dev), n, q.to(dev), wt.to(dev), k8.to(dev), ks.to(dev), scores,
-                   th, hist, ws, st)
+    hist.fill_(12345)                                 # stale contents: quantize_q must clear them
+    _scores_gpu(torch.from_numpy(off).to(dev), n, q.to(dev), wt.to(dev), k8.to(dev), ks.to(dev), scores,
+                th, hist, st)
     torch.cuda.synchronize()
     return off, k8.cpu().numpy(), ks.cpu().numpy(), q.cpu().numpy(), wt.cpu().numpy(), scores.cpu().numpy(), \
         hist.cpu().numpy().view(np.uint32), int(st.item()), th.cpu().numpy()
@@ -134,10 +144,9 @@ def test_scores_integer_exact():
     scores = torch.zeros(n, device=dev)
     hist = torch.zeros((1, 256), dtype=torch.int32, device=dev)
     th = torch.full((1,), math.inf, device=dev)
-    ws = torch.zeros(L.workspace_size(1), dtype=torch.uint8, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    L.index_scores(torch.from_numpy(off).to(dev), n, torch.from_numpy(q).to(dev), torch.from_numpy(w).to(dev),
-                   torch.from_numpy(k8).to(dev), torch.from_numpy(ks).to(dev), scores, th, hist, ws, st)
+    _scores_gpu(torch.from_numpy(off).to(dev), n, torch.from_numpy(q).to(dev), torch.from_numpy(w).to(dev),
+                torch.from_numpy(k8).to(dev), torch.from_numpy(ks).to(dev), scores, th, hist, st)
     torch.cuda.synchronize()
     q8, qs, _ = orc.quantize_q(q, w)
     ref, _ = orc.scores(q8[0], qs[0], w[0], k8, ks)
@@ -267,10 +276,9 @@ def test_nan_query_sets_status():
     scores = torch.zeros(1024, device=dev)
     hist = torch.zeros((1, 256), dtype=torch.int32, device=dev)
     th = torch.full((1,), math.inf, device=dev)
-    ws = torch.zeros(L.workspace_size(1), dtype=torch.uint8, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    L.index_scores(torch.from_numpy(off).to(dev), 1024, q.to(dev), wt.to(dev), k8.to(dev), ks.to(dev), scores,
-                   th, hist, ws, st)
+    _scores_gpu(torch.from_numpy(off).to(dev), 1024, q.to(dev), wt.to(dev), k8.to(dev), ks.to(dev), scores,
+                th, hist, st)
     torch.cuda.synchronize()
     assert int(st.item()) & L.ST_NAN
 
@@ -283,10 +291,9 @@ def test_bad_offsets_set_status_not_fault():
     ks = torch.ones(n, device=dev)
     scores = torch.zeros(n, device=dev)
     hist = torch.zeros((1, 256), dtype=torch.int32, device=dev)
-    ws = torch.zeros(L.workspace_size(1), dtype=torch.uint8, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    L.index_scores(off, n, torch.randn((1, 64, 128), device=dev), torch.rand((1, 64), device=dev), k8, ks,
-                   scores, None, hist, ws, st)
+    _scores_gpu(off, n, torch.randn((1, 64, 128), device=dev), torch.rand((1, 64), device=dev), k8, ks,
+                scores, None, hist, st)
     sel = torch.empty((1, 16), dtype=torch.int32, device=dev)
     kth = torch.empty(1, device=dev)
     L.topk_select(off, n, scores, 16, hist, None, 0.5, sel, kth, st)
