@@ -1,0 +1,452 @@
+#!/usr/bin/env python3
+"""Benchmark of the ECHO per-layer decode hot path on GB300.
+
+One step = one decode step of one layer for the whole batch: E4M3 query
+quantisation, FP8 indexer scores of every context token, early fetch above
+the predicted threshold (with recall), exact top-k with the EMA threshold,
+and the GPU-cache step (free -> allocate -> recall from the pinned host
+pool), captured as one CUDA graph with the recall on a second stream.
+
+Workload: 8 requests x 32768 context tokens, 1 layer, 64 index heads x 128,
+E4M3 keys with fp32 scales, k = 2048, 4096 GPU slots per request, 576-dim
+bf16 KV rows in a pinned host pool, AR(0.9) query drift, predictor on.
+
+Prints ONE JSON line (rank 0).  Timing: W warm-up graph replays, then K
+timed steps, each bracketed by CUDA events on the launching stream, with a
+256 MB write flushing L2 before every timed step (outside the events).
+Under torchrun each rank runs an independent replica (its own requests):
+barrier, max over ranks, value = total steps of all ranks / slowest time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode steps/s (indexer+top-k+recall per layer) & GB/s vs HBM/PCIe roofline"
+UNIT = "steps/s"
+SCORE_BYTES_PER_TOKEN = 132      # 128 E4M3 key bytes + 4-byte fp32 scale
+FLUSH_BYTES = 256 << 20          # > 129 MB L2
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=64)
+    p.add_argument("--warmup", type=int, default=8)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--cpu-budget-s", type=float, default=10.0,
+                   help="seconds of oracle work for the CPU baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+def workload_config(w):
+    return {"workload": (f"decode batch: {w.B} requests x {w.lengths[0]} tokens, {w.L} layer, "
+                         f"64x128 index heads, E4M3 keys, k={w.k}, {w.C} GPU slots/request, "
+                         f"576-dim bf16 host KV rows, AR(0.9) query drift, EMA predictor on"),
+            "requests": w.B, "tokens_per_request": w.lengths[0], "layers": w.L, "k": w.k,
+            "gpu_slots_per_request": w.C, "predictor": True, "alpha": 0.5,
+            "l2": "flushed by a 256 MB write before every timed step", "cuda_graph": True}
+
+
+# ----------------------------------------------------------------------------- multi-rank plumbing
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
+        int(os.environ.get("LOCAL_RANK", 0))
+
+
+def combine_over_ranks(elapsed_s: float, steps: int, world: int, reduce_max) -> tuple[float, float]:
+    """Whole-job throughput of independent replicas: every rank ran `steps` steps;
+    the job took as long as the slowest rank.  reduce_max(x) returns the max over ranks."""
+    slowest = reduce_max(elapsed_s)
+    return world * steps / slowest, slowest
+
+
+# ----------------------------------------------------------------------------- peaks, clocks, profile
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def score_kernel_traffic():
+    """DRAM bytes per launch of the score kernel from the committed ncu summary,
+    or None when the kernel source changed since those counters were taken."""
+    path = os.path.join(ROOT, "profiles", "score_kernel_batch8x32768.txt")
+    src = os.path.join(ROOT, "sparse_attention_kv_echo_gb300", "csrc", "echo_scores.cu")
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+        m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+        if m_sha and m_tr and m_sha.group(1) == sha:
+            return int(m_tr.group(1))
+    except OSError:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of the GPU's clocks and throttle reasons while running."""
+
+    FIELDS = ("pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.bus_id = (bus_id or "").lower()
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                                          "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.flush()
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                if self.bus_id and not parts[0].lower().endswith(self.bus_id[-12:]):
+                    continue
+                rows.append(parts)
+        os.unlink(self.out.name)
+        if not rows:
+            return None
+        mhz = [float(r[1].split()[0]) for r in rows if r[1].split()[0].replace(".", "").isdigit()]
+        mx = [float(r[2].split()[0]) for r in rows if r[2].split()[0].replace(".", "").isdigit()]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                                 r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) leg
+def oracle_steps(w, inputs, max_steps: int, budget_s: float, warmup: int = 0):
+    """Runs the CPU oracle's decode steps on the workload (state carried across
+    steps); returns (timed steps, seconds, threads)."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    off, k8, ks, wt, host_u8, q_all = inputs
+    threads = max(1, min(w.B, len(os.sched_getaffinity(0))))
+    theta = np.full(w.B, np.inf, np.float32)
+    t2s = np.full(w.total_tokens, -1, np.int32)
+    s2t = np.full(w.B * w.C, -1, np.int32)
+    dev_rows = np.zeros((w.B * w.C, host_u8.shape[1]), np.uint8)
+
+    def one(t):
+        oracle.decode_step(off, q_all[t % len(q_all)], wt, k8, ks, w.k, 0.5, True, -1, theta, w.C, t2s, s2t,
+                           host_u8, dev_rows, nthreads=threads)
+
+    for t in range(warmup):
+        one(t)
+    t0 = time.perf_counter()
+    n = 0
+    while n < max_steps:
+        one(warmup + n)
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    return n, time.perf_counter() - t0, threads
+
+
+def cpu_inputs(w, k8, ks, wt, host, q_all):
+    import numpy as np
+    import torch
+    from sparse_attention_kv_echo_gb300 import workloads as wl
+    return (wl.tok_offsets(w.lengths), k8.cpu().numpy(), ks.cpu().numpy(), wt.cpu().numpy(),
+            host.view(torch.uint8).numpy().reshape(w.total_tokens, -1), q_all.cpu().numpy())
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from sparse_attention_kv_echo_gb300 import DecodeLayer
+    from sparse_attention_kv_echo_gb300 import _lib as L
+    from sparse_attention_kv_echo_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device(dev))
+    L.load(build_if_missing=True)
+
+    w = wl.WORKLOADS["batch"]
+    if rank:
+        w = wl.scaled(w, w.name, seed=rank)                 # each replica serves its own requests
+    off = wl.tok_offsets(w.lengths)
+    k8, ks = wl.make_keys(w, 0, device=dev)
+    wt = wl.make_weights(w, 0, device=dev)
+    host = wl.make_host_pool(w, 0, device=dev, pin=True)
+    qsrc = wl.QueryStream(w, 0, device=dev)
+    q_all = torch.stack([qsrc.next() for _ in range(w.steps)])
+    S = q_all.shape[0]
+    lay = DecodeLayer(off, k8, ks, w.k, w.C, host, device=dev)
+    main, copy = torch.cuda.Stream(), torch.cuda.Stream()
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def eager_step(t):
+        with torch.cuda.stream(main):
+            lay.q_in.copy_(q_all[t % S])
+            lay.step(stream=main, copy_stream=copy)
+            main.wait_stream(copy)
+
+    with torch.cuda.stream(main):
+        lay.w_in.copy_(wt)
+    eager_step(0)
+    torch.cuda.synchronize()
+    lay.reset()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=main):
+        lay.step(stream=main, copy_stream=copy)
+        main.wait_stream(copy)
+    torch.cuda.synchronize()
+
+    def replay(t):
+        with torch.cuda.stream(main):
+            lay.q_in.copy_(q_all[t % S])
+            g.replay()
+
+    # ---------------- timed region: graph replays, L2 flushed before each step
+    props = torch.cuda.get_device_properties(local)
+    try:
+        bus = f"{int(props.pci_domain_id):08x}:{int(props.pci_bus_id):02x}:{int(props.pci_device_id):02x}.0"
+    except Exception:
+        bus = None
+    sampler = ClockSampler(bus)
+    for t in range(args.warmup):
+        replay(t)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stats0 = lay.stats.clone()
+    sampler.start()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        with torch.cuda.stream(main):
+            flush.zero_()
+            starts[i].record(main)
+        replay(args.warmup + i)
+        ends[i].record(main)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    elapsed_s = sum(step_ms) / 1e3
+    status = int(lay.status.item())
+    stats = (lay.stats - stats0).cpu().numpy().astype(np.int64)
+
+    def reduce_max(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    value, slowest = combine_over_ranks(elapsed_s, args.steps, world, reduce_max)
+
+    # ---------------- per-call pass: each call timed alone with events (L2 flushed)
+    reps = max(4, min(args.steps, 32))
+    names = ("quantize", "scores", "early_fetch", "topk", "cache_step")
+    kt = {n: [] for n in names}
+    recall_ms = []
+    recall_rows = []
+    for r in range(reps):
+        t = args.warmup + args.steps + r
+        with torch.cuda.stream(main):
+            lay.q_in.copy_(q_all[t % S])
+            flush.zero_()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+            ev_copy_end = torch.cuda.Event(enable_timing=True)
+            ev[0].record(main)
+            L.quantize_q(lay.q_in, lay.w_in, lay.q8, lay.qscale, lay.wfold, lay.status, hist=lay.hist, stream=main)
+            ev[1].record(main)
+            L.index_scores(lay.tok_off, lay.n_tokens, lay.q8, lay.wfold, lay.k8, lay.ks, lay.scores, lay.theta,
+                           lay.hist, lay.status, stream=main)
+            ev[2].record(main)
+            L.early_fetch(lay.tok_off, lay.n_tokens, lay.scores, lay.theta, -1, lay.cache, lay.status,
+                          stream=main, copy_stream=main)
+            ev[3].record(main)
+            L.topk_select(lay.tok_off, lay.n_tokens, lay.scores, lay.k, lay.hist, lay.theta, lay.alpha,
+                          lay.sel_idx, lay.kth, lay.status, stream=main)
+            ev[4].record(main)
+            L.cache_step(lay.tok_off, lay.n_tokens, lay.sel_idx, lay.cache, lay.sel_slot, lay.status,
+                         stream=main, copy_stream=copy)
+            ev[5].record(main)          # cache-step kernel done; recall runs on `copy` after it
+            ev_copy_end.record(copy)
+            main.wait_stream(copy)
+        torch.cuda.synchronize()
+        for i, n in enumerate(names):
+            kt[n].append(ev[i].elapsed_time(ev[i + 1]))
+        recall_ms.append(ev[5].elapsed_time(ev_copy_end))
+        recall_rows.append(int(lay.cache.miss_cnt.sum().item()))
+    misses_per_step = float(stats[L.STAT_MISSES]) / args.steps
+    early_per_step = float(stats[L.STAT_EARLY]) / args.steps
+    kern_us = {n: 1e3 * statistics.mean(v) for n, v in kt.items()}
+    t_score = statistics.mean(kt["scores"]) / 1e3
+    score_bytes = SCORE_BYTES_PER_TOKEN * w.total_tokens
+    peak, peak_kind = measured_peaks()
+    achieved = score_bytes / t_score / 1e9
+    traffic = score_kernel_traffic()
+    topk_bytes = 4 * w.total_tokens                  # one read of the fp32 scores (algorithmic)
+    scoring_topk_gbs = (score_bytes + topk_bytes) / ((statistics.mean(kt["scores"]) +
+                                                      statistics.mean(kt["topk"])) / 1e3) / 1e9
+    # host link: pinned host -> device copy, best of 5
+    hbuf = torch.empty(256 << 20, dtype=torch.uint8, pin_memory=True)
+    dbuf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    h2d = []
+    for _ in range(5):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        dbuf.copy_(hbuf, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        h2d.append(hbuf.numel() / (a.elapsed_time(b) / 1e3) / 1e9)
+    h2d_gbs = max(h2d)
+    recall_gbs = (sum(recall_rows) * lay.cache.row_bytes) / (sum(recall_ms) / 1e3) / 1e9
+
+    # ---------------- end to end through the public API with host buffers
+    q_host = q_all.cpu().pin_memory()
+    w_host = wt.cpu().pin_memory()
+    slot_host = torch.empty_like(lay.sel_slot, device="cpu").pin_memory()
+    kth_host = torch.empty_like(lay.kth, device="cpu").pin_memory()
+    e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        with torch.cuda.stream(main):
+            flush.zero_()
+            e_starts[i].record(main)
+            lay.q_in.copy_(q_host[i % S], non_blocking=True)
+            lay.w_in.copy_(w_host, non_blocking=True)
+            g.replay()
+            slot_host.copy_(lay.sel_slot, non_blocking=True)
+            kth_host.copy_(lay.kth, non_blocking=True)
+            e_ends[i].record(main)
+    torch.cuda.synchronize()
+    e2e_s = sum(s.elapsed_time(e) for s, e in zip(e_starts, e_ends)) / 1e3
+    e2e_value, _ = combine_over_ranks(e2e_s, args.steps, world, reduce_max)
+    h2d_bytes = q_host[0].numel() * 4 + w_host.numel() * 4
+    d2h_bytes = slot_host.numel() * 4 + kth_host.numel() * 4
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * slowest / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 MMA, fp32 accumulate/epilogue, int32 tables",
+        "data": "synthetic (seeded; shapes of the evaluation workloads)", "config": workload_config(w),
+        "roofline": {"kernel": "score_kernel (echo_index_scores)", "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"hbm_gbs, {peak_kind}", "algorithmic_bytes": score_bytes,
+                     "bytes_per_token": SCORE_BYTES_PER_TOKEN, "launch_us": round(1e6 * t_score, 2)},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d_bytes,
+                "d2h_bytes_per_step": d2h_bytes},
+        "gpu_launches": lay.kernel_launches_per_step() * args.steps,
+        "clocks": clocks,
+        "status": status,
+        "detail": {"kernel_us": {k: round(v, 2) for k, v in kern_us.items()},
+                   "recall_us": round(1e3 * statistics.mean(recall_ms), 2),
+                   "scoring_topk_gbs": round(scoring_topk_gbs, 1),
+                   "scoring_topk_frac_of_8tbs": round(scoring_topk_gbs / 8000.0, 4),
+                   "misses_per_step": round(misses_per_step, 1), "early_per_step": round(early_per_step, 1),
+                   "recall_rows_per_step_kernel_pass": round(statistics.mean(recall_rows), 1),
+                   "recall_gbs": round(recall_gbs, 1), "h2d_copy_gbs": round(h2d_gbs, 1),
+                   "recall_frac_of_h2d": round(recall_gbs / h2d_gbs, 4) if h2d_gbs else None,
+                   "step_ms_min": round(min(step_ms), 4), "step_ms_median": round(statistics.median(step_ms), 4)},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n, secs, threads = oracle_steps(w, cpu_inputs(w, k8, ks, wt, host, q_all), max_steps=args.steps,
+                                        budget_s=args.cpu_budget_s)
+        result["cpu_baseline"] = {"value": round(n / secs, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+                                  "sample": f"first {n} decode steps of the same workload (all {w.B} requests, "
+                                            f"fp64 scores, stable-sort top-k, map/set cache), ~{secs:.1f} s"}
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+# ----------------------------------------------------------------------------- reference arm (the oracle)
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+    from sparse_attention_kv_echo_gb300 import workloads as wl
+    w = wl.WORKLOADS["batch"]
+    gen = "cuda" if torch.cuda.is_available() else "cpu"   # same draws as our arm when a GPU is present
+    k8, ks = wl.make_keys(w, 0, device=gen)
+    wt = wl.make_weights(w, 0, device=gen)
+    host = wl.make_host_pool(w, 0, device=gen)
+    qsrc = wl.QueryStream(w, 0, device=gen)
+    q_all = torch.stack([qsrc.next() for _ in range(w.steps)])
+    n, secs, threads = oracle_steps(w, cpu_inputs(w, k8, ks, wt, host, q_all), max_steps=args.steps,
+                                    budget_s=float("inf"), warmup=args.warmup)
+    value = n / secs
+    sample = f"{n} timed decode steps (after {args.warmup} untimed) of the whole workload on the CPU oracle"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": n, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / max(n, 1), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp64 scores, fp32 selection", "data": "synthetic", "config": workload_config(w),
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
