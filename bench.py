@@ -300,6 +300,9 @@ def run_ours(args):
     for r in range(reps):
         t = args.warmup + args.steps + r
         with torch.cuda.stream(main):
+            # park the GPU while the host enqueues everything, so the events time
+            # GPU work only and not the host's launch latency between calls
+            torch.cuda._sleep(4_000_000)
             lay.q_in.copy_(q_all[t % S])
             flush.zero_()
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
