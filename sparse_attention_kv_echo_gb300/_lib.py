@@ -21,8 +21,8 @@ STAT_TOPK_FALLBACK, STAT_BOUNDARY_MAX, STAT_EARLY, STAT_MISSES, STAT_EARLY_USED 
 STATS_N = 8
 HEADS, DIM, MAX_REQUESTS = 64, 128, 4096
 
-EXPORTS = ("echo_cache_step", "echo_device_sm_count", "echo_early_fetch", "echo_host_device_alias",
-           "echo_index_scores", "echo_quantize_q", "echo_topk_select")
+EXPORTS = ("echo_above_words", "echo_cache_step", "echo_device_sm_count", "echo_early_fetch",
+           "echo_host_device_alias", "echo_index_scores", "echo_quantize_q", "echo_topk_select")
 
 _vp = ctypes.c_void_p
 
@@ -63,10 +63,12 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         i32, i64, f32 = ctypes.c_int, ctypes.c_int64, ctypes.c_float
         L.echo_quantize_q.restype = i32
         L.echo_quantize_q.argtypes = [i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+        L.echo_above_words.restype = ctypes.c_size_t
+        L.echo_above_words.argtypes = [i32, i64]
         L.echo_index_scores.restype = i32
-        L.echo_index_scores.argtypes = [i32, _vp, i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+        L.echo_index_scores.argtypes = [i32, _vp, i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
         L.echo_early_fetch.restype = i32
-        L.echo_early_fetch.argtypes = [i32, _vp, i64, _vp, _vp, i32, ctypes.POINTER(EchoCacheStruct), _vp,
+        L.echo_early_fetch.argtypes = [i32, _vp, i64, _vp, i32, ctypes.POINTER(EchoCacheStruct), _vp,
                                        _vp, _vp, _vp]
         L.echo_topk_select.restype = i32
         L.echo_topk_select.argtypes = [i32, _vp, i64, _vp, i32, _vp, _vp, f32, _vp, _vp, _vp, _vp, _vp]
@@ -118,21 +120,25 @@ def quantize_q(q, w, q8, qscale, wfold, status, hist=None, stream=None):
                                                     _ptr(wfold), _ptr(hist), _ptr(status), _stream(stream)))
 
 
-def index_scores(tok_off, n_tokens, q8, wfold, k8, ks, scores, theta_hat, hist, status, stream=None):
+def above_words(B: int, n_tokens: int) -> int:
+    return int(load().echo_above_words(int(B), int(n_tokens)))
+
+
+def index_scores(tok_off, n_tokens, q8, wfold, k8, ks, scores, theta_hat, hist, status, above=None,
+                 stream=None):
     B = q8.shape[0]
     _check("echo_index_scores", load().echo_index_scores(
         B, _ptr(tok_off), int(n_tokens), _ptr(q8), _ptr(wfold), _ptr(k8), _ptr(ks), _ptr(scores),
-        _ptr(theta_hat), _ptr(hist), _ptr(status), _stream(stream)))
+        _ptr(theta_hat), _ptr(hist), _ptr(above), _ptr(status), _stream(stream)))
 
 
-def early_fetch(tok_off, n_tokens, scores, theta_hat, early_cap, cache, status, stats=None, stream=None,
-                copy_stream=None):
+def early_fetch(tok_off, n_tokens, above, early_cap, cache, status, stats=None, stream=None, copy_stream=None):
     B = tok_off.shape[0] - 1
     st = _stream(stream)
     cst = _stream(copy_stream) if copy_stream is not None else st
     _check("echo_early_fetch", load().echo_early_fetch(
-        B, _ptr(tok_off), int(n_tokens), _ptr(scores), _ptr(theta_hat), int(early_cap),
-        ctypes.byref(cache.struct), _ptr(status), _ptr(stats), st, cst))
+        B, _ptr(tok_off), int(n_tokens), _ptr(above), int(early_cap), ctypes.byref(cache.struct),
+        _ptr(status), _ptr(stats), st, cst))
 
 
 def topk_select(tok_off, n_tokens, scores, k, hist, theta_hat, alpha, sel_idx, kth, status, stats=None,

@@ -10,8 +10,9 @@
 //     the predicted threshold are fetched before top-k completes, up to a cap.
 //
 // Kernels (one CTA of 1024 threads per request for the table work):
-//   early_select_kernel  ordered scan of score > theta over non-resident tokens
-//                        (block prefix sums), the first min(cap, free) of them
+//   early_select_kernel  ordered scan of the score kernel's above-threshold bits
+//                        (one word per 32 tokens), keeping non-resident tokens
+//                        (block prefix sums); the first min(cap, free) of them
 //                        take the lowest free slots.
 //   cache_step_kernel    marks the slots of selected residents in a shared
 //                        bitmap, frees the rest one warp per 32-slot word
@@ -97,9 +98,21 @@ __device__ uint32_t assign_lowest_free(uint32_t* fb, int words, uint32_t M, cons
     return done < M ? done : M;
 }
 
+// Tiles of 128 tokens of request b, and the first tile of b in the list of all
+// requests' tiles (the order the score kernel writes its above-threshold words in).
+__device__ uint32_t first_tile_of(const int64_t* tok_off, int64_t n_tokens, int b, uint32_t* scan) {
+    uint32_t part = 0;
+    for (int bb = threadIdx.x; bb < b; bb += kCT) {
+        const int64_t lo = tok_off[bb], hi = tok_off[bb + 1];
+        if (lo >= 0 && hi >= lo && hi <= n_tokens) part += static_cast<uint32_t>((hi - lo + 127) / 128);
+    }
+    uint32_t total;
+    block_exclusive_scan<kCT>(part, scan, &total);
+    return total;
+}
+
 __global__ void __launch_bounds__(kCT) early_select_kernel(const int64_t* __restrict__ tok_off, int64_t n_tokens,
-                                                           const float* __restrict__ scores,
-                                                           const float* __restrict__ theta_hat, int cap, CacheArgs c,
+                                                           const uint32_t* __restrict__ above, int cap, CacheArgs c,
                                                            int32_t* status, uint32_t* stats) {
     __shared__ uint32_t scan[40];
     const int b = blockIdx.x, tid = threadIdx.x;
@@ -111,11 +124,13 @@ __global__ void __launch_bounds__(kCT) early_select_kernel(const int64_t* __rest
     uint32_t* fb = c.freebits + static_cast<int64_t>(b) * words;
     int32_t* etok = c.early_tok + static_cast<int64_t>(b) * C;
     int32_t* eslot = c.early_slot + static_cast<int64_t>(b) * C;
-    const float th = theta_hat[b];
-    if (!isfinite(th) || n == 0 || cap == 0) {
+    if (n == 0 || cap == 0) {
         if (tid == 0) c.early_cnt[b] = 0;
         return;
     }
+    const uint32_t t0 = first_tile_of(tok_off, n_tokens, b, scan);
+    const uint32_t* ab = above + 4 * static_cast<size_t>(t0);
+    const int awords = static_cast<int>(4 * ((n + 127) / 128));
     uint32_t F = 0;
     for (int w0 = 0; w0 < words; w0 += kCT) {
         const int w = w0 + tid;
@@ -125,22 +140,24 @@ __global__ void __launch_bounds__(kCT) early_select_kernel(const int64_t* __rest
     }
     const uint32_t limit = (cap < 0) ? F : min(F, static_cast<uint32_t>(cap));
     uint32_t found = 0;
-    for (int64_t c0 = 0; c0 < n && found < limit; c0 += 4 * kCT) {
-        const int64_t s0 = c0 + 4 * tid;
-        uint32_t f = 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int64_t s = s0 + j;
-            if (s < n && scores[base + s] > th && t2s[s] < 0) f |= 1u << j;
+    // word w covers tokens 32*w .. 32*w+31 of the request: ascending word, ascending bit
+    for (int w0 = 0; w0 < awords && found < limit; w0 += kCT) {
+        const int w = w0 + tid;
+        uint32_t cand = (w < awords) ? ab[w] : 0u, nonres = 0;
+        while (cand) {
+            const int bit = __ffs(cand) - 1;
+            cand &= cand - 1;
+            const int64_t s = 32 * static_cast<int64_t>(w) + bit;
+            if (s < n && t2s[s] < 0) nonres |= 1u << bit;
         }
         uint32_t tot;
-        uint32_t rank = found + block_exclusive_scan<kCT>(__popc(f), scan, &tot);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (f & (1u << j)) {
-                if (rank < limit) etok[rank] = static_cast<int32_t>(s0 + j);
-                ++rank;
-            }
+        uint32_t rank = found + block_exclusive_scan<kCT>(__popc(nonres), scan, &tot);
+        while (nonres) {
+            const int bit = __ffs(nonres) - 1;
+            nonres &= nonres - 1;
+            if (rank < limit) etok[rank] = 32 * w + bit;
+            ++rank;
+        }
         found += tot;
     }
     const uint32_t E = min(found, limit);
@@ -290,10 +307,9 @@ __global__ void __launch_bounds__(256) recall_kernel(const int64_t* __restrict__
 
 }  // namespace
 
-cudaError_t launch_early_select(int B, const int64_t* tok_off, int64_t n_tokens, const float* scores,
-                                const float* theta_hat, int cap, const echo_cache& c, int32_t* status,
-                                uint32_t* stats, cudaStream_t s) {
-    early_select_kernel<<<B, kCT, 0, s>>>(tok_off, n_tokens, scores, theta_hat, cap, cache_args(c), status, stats);
+cudaError_t launch_early_select(int B, const int64_t* tok_off, int64_t n_tokens, const uint32_t* above, int cap,
+                                const echo_cache& c, int32_t* status, uint32_t* stats, cudaStream_t s) {
+    early_select_kernel<<<B, kCT, 0, s>>>(tok_off, n_tokens, above, cap, cache_args(c), status, stats);
     return cudaGetLastError();
 }
 
@@ -339,18 +355,17 @@ extern "C" int echo_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, 
     return ECHO_OK;
 }
 
-extern "C" int echo_early_fetch(int B, const int64_t* tok_off, int64_t n_tokens, const float* scores,
-                                const float* theta_hat, int early_cap, const echo_cache* cache, int32_t* status,
-                                uint32_t* stats, echo_stream_t stream, echo_stream_t copy_stream) {
+extern "C" int echo_early_fetch(int B, const int64_t* tok_off, int64_t n_tokens, const uint32_t* above,
+                                int early_cap, const echo_cache* cache, int32_t* status, uint32_t* stats,
+                                echo_stream_t stream, echo_stream_t copy_stream) {
     using namespace echo;
     if (B <= 0 || n_tokens < 0) return ECHO_EINVAL;
     if (B > ECHO_MAX_REQUESTS) return ECHO_EUNSUPPORTED;
-    if (!tok_off || !theta_hat || !status || (n_tokens > 0 && !scores)) return ECHO_EINVAL;
+    if (!tok_off || !status || (n_tokens > 0 && !above)) return ECHO_EINVAL;
     if (n_tokens >= (1ll << 31)) return ECHO_EUNSUPPORTED;
     int rc = check_cache(cache, B, 0);
     if (rc) return rc;
-    ECHO_CUDA_OK(launch_early_select(B, tok_off, n_tokens, scores, theta_hat, early_cap, *cache, status, stats,
-                                     stream));
+    ECHO_CUDA_OK(launch_early_select(B, tok_off, n_tokens, above, early_cap, *cache, status, stats, stream));
     rc = stream_wait(copy_stream, stream);
     if (rc) return rc;
     ECHO_CUDA_OK(launch_recall(B, tok_off, n_tokens, cache->C, cache->early_tok, cache->early_slot,

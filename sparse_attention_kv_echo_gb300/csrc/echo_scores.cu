@@ -47,6 +47,7 @@ struct ScoreArgs {
     float* scores;
     const float* theta_hat;
     uint32_t* hist;
+    uint32_t* above;
     int32_t* status;
 };
 
@@ -262,7 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int b = (ntiles > 0) ? find_request(tstart, B, t_begin) : 0;
         int cur_b = -1;
         float wv[ECHO_HEADS];
-        float shift = 0.f;
+        float shift = 0.f, theta = 0.f;
+        bool theta_ok = false;
         int64_t base = 0, nb = 0;
         bool ok = true;
         for (uint32_t it = group; it < ntiles; it += 2) {
@@ -292,7 +294,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     wv[4 * i + 3] = x.w;
                 }
                 const float th = a.theta_hat ? a.theta_hat[b] : __int_as_float(0x7f800000);
-                shift = isfinite(th) ? th : 0.f;
+                theta_ok = isfinite(th);
+                theta = th;
+                shift = theta_ok ? th : 0.f;
                 base = a.tok_off[b];
                 nb = a.tok_off[b + 1] - base;
             }
@@ -327,6 +331,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float score = __fmul_rn(__fadd_rn(__fadd_rn(s0, s1), __fadd_rn(s2, s3)), ksv);
             const unsigned vm = __ballot_sync(0xffffffffu, valid);
+            if (a.above) {
+                // tokens above the predicted threshold: one word per 32 rows of the tile
+                const unsigned am = __ballot_sync(0xffffffffu, valid && theta_ok && score > theta);
+                if (lane == 0) a.above[4 * static_cast<size_t>(t) + quarter] = am;
+            }
             if (valid) {
                 a.scores[base + tok] = score;
                 if (a.hist) {
@@ -360,9 +369,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 }  // namespace echo
 
+extern "C" size_t echo_above_words(int B, int64_t n_tokens) {
+    if (B <= 0 || n_tokens < 0) return 0;
+    return 4 * static_cast<size_t>(n_tokens / echo::kTileM + B);
+}
+
 extern "C" int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens, const uint8_t* q8,
                                  const float* wfold, const uint8_t* k8, const float* ks, float* scores,
-                                 const float* theta_hat, uint32_t* hist, int32_t* status, echo_stream_t stream) {
+                                 const float* theta_hat, uint32_t* hist, uint32_t* above, int32_t* status,
+                                 echo_stream_t stream) {
     using namespace echo;
     if (B <= 0 || n_tokens < 0) return ECHO_EINVAL;
     if (B > ECHO_MAX_REQUESTS) return ECHO_EUNSUPPORTED;
@@ -383,7 +398,7 @@ extern "C" int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens
     const size_t smem = smem_bytes(B);
     ECHO_CUDA_OK(cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(smem)));
-    ScoreArgs args{B, tok_off, n_tokens, wfold, ks, scores, theta_hat, hist, status};
+    ScoreArgs args{B, tok_off, n_tokens, wfold, ks, scores, theta_hat, hist, above, status};
     score_kernel<<<grid, kThreads, smem, stream>>>(kmap, qmap, args);
     ECHO_CUDA_OK(cudaGetLastError());
     return ECHO_OK;

@@ -6,41 +6,54 @@
 // real kernel bins scores by the top 8 bits of each score shifted by the
 // predicted threshold (panel "Prefill: one-round histogram").
 //
-// One CTA of 1024 threads per request:
+// One thread-block cluster of kCS CTAs (1024 threads each) per request; CTA r
+// of the cluster owns the r-th contiguous slice of the request's tokens.
 //   1. boundary bin: from the 256-bin histogram of the shifted scores (made by
-//      the score kernel, or here), the bin b* where the count from the top
-//      reaches k.  Shifting is monotone, so every token in a bin above b*
+//      the score kernel, or rebuilt here), the bin b* where the count from the
+//      top reaches k.  Shifting is monotone, so every token in a bin above b*
 //      outranks every token at or below it.
-//   2. one pass collects the tokens of bin b* into shared memory; a radix
-//      select (four 8-bit digits of the order key) finds K*, the key of the
-//      k-th score, and a second radix select on ~index resolves equal keys
-//      towards the lower index.  When bin b* does not fit in shared memory the
-//      same selects run as passes over the scores in global memory.
-//   3. one ordered pass writes the selected indices in ascending order with
-//      block-wide prefix sums; the k-th score updates the EMA.
+//   2. every CTA scans its slice once and appends the tokens of bin b* to the
+//      leader CTA's shared memory through distributed shared memory (one
+//      atomic per warp); the leader runs a radix select (four 8-bit digits of
+//      the order key) for K*, the key of the k-th score, and a second one on
+//      ~index to resolve equal keys towards the lower index.  When bin b*
+//      does not fit in shared memory the leader runs the same selects as
+//      passes over the scores in global memory.
+//   3. every CTA counts its selected tokens; a cluster-wide prefix of those
+//      counts (read over DSMEM) places each slice, and one ordered pass per
+//      slice writes the indices in ascending order with block-wide scans.
 // A good prediction puts the k-th score near 0 after the shift, where the
 // exponent bins are narrow, so the boundary bin holds few tokens.
+#include <cooperative_groups.h>
+
 #include "echo_common.cuh"
 #include "echo_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace echo {
 namespace {
 
 constexpr int kTT = 1024;
-constexpr int kCandMax = 12288;
+constexpr int kCS = 8;           // CTAs per request (one cluster)
+constexpr int kCandMax = 12288;  // boundary-bin entries the leader keeps in shared memory
 
 struct TopkShared {
     uint32_t hist[256];
+    uint32_t hist_acc[256];      // leader: cluster-wide rebuild of the histogram
     uint32_t scan[40];
     uint32_t cand_key[kCandMax];
     uint32_t cand_idx[kCandMax];
-    uint32_t cnt;
+    uint32_t cnt;                // leader: boundary-bin entries appended
+    uint32_t chk_above;          // leader: tokens above b*, summed over the cluster
+    uint32_t chk_eq;             // leader: tokens in b*, summed over the cluster
     uint32_t digit;
     uint32_t above;
     uint32_t minkey;
     uint32_t flag;
-    uint32_t chk_above;
-    uint32_t chk_eq;
+    uint32_t K;                  // leader -> all: key of the k-th score
+    uint32_t idx_cut;            // leader -> all: last index taken among keys == K
+    uint32_t selected;           // this CTA's number of selected tokens
 };
 
 // Warp 0: the largest digit d with (count of digits >= d) >= target, and the
@@ -124,8 +137,8 @@ struct GlobalCands {
     }
 };
 
-// The r-th largest value (1-based) among the elements; *rem = r minus the
-// number of elements strictly larger (>= 1), *eq = number equal to it.
+// The r-th largest value (1-based) among the elements (block-wide); *rem = r
+// minus the number of elements strictly larger (>= 1), *eq = number equal to it.
 template <class Src>
 __device__ uint32_t radix_select(const Src& src, uint32_t r, TopkShared& sh, uint32_t* rem, uint32_t* eq) {
     uint32_t prefix = 0, mask = 0;
@@ -158,17 +171,27 @@ __device__ __forceinline__ float ema_update(float theta, float kth, float alpha)
     return __fadd_rn(a, b);
 }
 
-__global__ void __launch_bounds__(kTT, 1)
+__device__ __forceinline__ bool takes(float x, float shift, uint32_t bstar, uint32_t K, uint32_t cut, int64_t s) {
+    const uint32_t bin = shifted_bin(x, shift);
+    const uint32_t key = order_key(x);
+    return bin > bstar || (bin == bstar && (key > K || (key == K && static_cast<uint32_t>(s) <= cut)));
+}
+
+__global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTT, 1)
     topk_kernel(const int64_t* __restrict__ tok_off, int64_t n_tokens, const float* __restrict__ scores, int k,
                 const uint32_t* __restrict__ hist, float* theta_hat, float alpha, int32_t* __restrict__ sel,
                 float* kth_out, int32_t* status, uint32_t* stats) {
     extern __shared__ uint8_t smem_raw[];
     TopkShared& sh = *reinterpret_cast<TopkShared*>(smem_raw);
-    const int b = blockIdx.x, tid = threadIdx.x;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = static_cast<int>(cluster.block_rank());
+    const bool leader = rank == 0;
+    TopkShared& lsh = *cluster.map_shared_rank(&sh, 0);     // the leader's shared memory
+    const int b = blockIdx.x / kCS, tid = threadIdx.x;
     const int64_t lo = tok_off[b], hi = tok_off[b + 1];
     int64_t n = hi - lo;
     if (lo < 0 || hi < lo || hi > n_tokens) {
-        if (tid == 0) set_status(status, ECHO_ST_BADDATA);
+        if (leader && tid == 0) set_status(status, ECHO_ST_BADDATA);
         n = 0;
     }
     const float* sc = scores + (n > 0 ? lo : 0);
@@ -176,12 +199,15 @@ __global__ void __launch_bounds__(kTT, 1)
     const float th_old = theta_hat ? theta_hat[b] : __int_as_float(0x7f800000);
     const float shift = isfinite(th_old) ? th_old : 0.f;
 
+    // ---- trivial requests: the leader alone, no cluster traffic
     if (n == 0) {
+        if (!leader) return;
         for (int i = tid; i < k; i += kTT) out[i] = -1;
         if (tid == 0) kth_out[b] = __int_as_float(0xff800000);
         return;
     }
     if (n <= k) {
+        if (!leader) return;
         if (tid == 0) {
             sh.minkey = 0xFFFFFFFFu;
             sh.flag = 0;
@@ -207,26 +233,37 @@ __global__ void __launch_bounds__(kTT, 1)
         return;
     }
 
-    // ---- 1. histogram of shifted bins, boundary bin
+    // this CTA's slice of the request
+    const int64_t s_lo = n * rank / kCS, s_hi = n * (rank + 1) / kCS;
+
+    // ---- 1-2. boundary bin, its tokens gathered in the leader
     bool have = hist != nullptr;
-    uint32_t bstar = 0, above = 0, eq_total = 0;
+    uint32_t bstar = 0, above = 0;
     for (int attempt = 0; attempt < 2; ++attempt) {
         if (have) {
             for (int i = tid; i < 256; i += kTT) sh.hist[i] = hist[static_cast<int64_t>(b) * 256 + i];
         } else {
+            // rebuild: slice histograms summed into the leader over DSMEM
+            if (leader)
+                for (int i = tid; i < 256; i += kTT) sh.hist_acc[i] = 0u;
             for (int i = tid; i < 256; i += kTT) sh.hist[i] = 0u;
-            __syncthreads();
-            for (int64_t s0 = 0; s0 < n; s0 += kTT) {
+            cluster.sync();
+            for (int64_t s0 = s_lo; s0 < s_hi; s0 += kTT) {
                 const int64_t s = s0 + tid;
-                const bool v = s < n;
+                const bool v = s < s_hi;
                 const uint32_t bin = v ? shifted_bin(sc[s], shift) : 256u;
                 const unsigned grp = __match_any_sync(0xffffffffu, bin);
                 if (v && (tid & 31) == __ffs(grp) - 1) atomicAdd(&sh.hist[bin], __popc(grp));
             }
+            __syncthreads();
+            for (int i = tid; i < 256; i += kTT)
+                if (sh.hist[i]) atomicAdd(&lsh.hist_acc[i], sh.hist[i]);
+            cluster.sync();
+            for (int i = tid; i < 256; i += kTT) sh.hist[i] = lsh.hist_acc[i];
         }
         __syncthreads();
         if (tid < 32) find_digit(sh.hist, static_cast<uint32_t>(k), &sh.digit, &sh.above);
-        if (tid == 0) {
+        if (leader && tid == 0) {
             sh.cnt = 0;
             sh.chk_above = 0;
             sh.chk_eq = 0;
@@ -234,12 +271,12 @@ __global__ void __launch_bounds__(kTT, 1)
         __syncthreads();
         bstar = sh.digit;
         above = sh.above;
-        eq_total = sh.hist[bstar];
-        // ---- 2. collect the boundary bin; count what lies above it
+        const uint32_t eq_total = sh.hist[bstar];
+        cluster.sync();  // the leader's counters are reset before anyone appends
         uint32_t my_above = 0, my_eq = 0;
-        for (int64_t s0 = 0; s0 < n; s0 += kTT) {
+        for (int64_t s0 = s_lo; s0 < s_hi; s0 += kTT) {
             const int64_t s = s0 + tid;
-            const bool v = s < n;
+            const bool v = s < s_hi;
             const float x = v ? sc[s] : 0.f;
             const uint32_t bin = shifted_bin(x, shift);
             my_above += v && bin > bstar;
@@ -247,74 +284,102 @@ __global__ void __launch_bounds__(kTT, 1)
             my_eq += in;
             const unsigned m = __ballot_sync(0xffffffffu, in);
             if (in) {
-                const int leader = __ffs(m) - 1;
+                const int leader_lane = __ffs(m) - 1;
                 uint32_t basepos = 0;
-                if ((tid & 31) == leader) basepos = atomicAdd(&sh.cnt, __popc(m));
-                basepos = __shfl_sync(m, basepos, leader);
+                if ((tid & 31) == leader_lane) basepos = atomicAdd(&lsh.cnt, __popc(m));
+                basepos = __shfl_sync(m, basepos, leader_lane);
                 const uint32_t pos = basepos + __popc(m & ((1u << (tid & 31)) - 1u));
                 if (pos < kCandMax) {
-                    sh.cand_key[pos] = order_key(x);
-                    sh.cand_idx[pos] = static_cast<uint32_t>(s);
+                    lsh.cand_key[pos] = order_key(x);
+                    lsh.cand_idx[pos] = static_cast<uint32_t>(s);
                 }
             }
         }
-        atomicAdd(&sh.chk_above, my_above);
-        atomicAdd(&sh.chk_eq, my_eq);
-        __syncthreads();
-        if (sh.chk_above == above && sh.chk_eq == eq_total) break;
+        // warp-reduce the checks before the remote atomics
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            my_above += __shfl_xor_sync(0xffffffffu, my_above, o);
+            my_eq += __shfl_xor_sync(0xffffffffu, my_eq, o);
+        }
+        if ((tid & 31) == 0) {
+            if (my_above) atomicAdd(&lsh.chk_above, my_above);
+            if (my_eq) atomicAdd(&lsh.chk_eq, my_eq);
+        }
+        cluster.sync();
+        const bool consistent = lsh.chk_above == above && lsh.chk_eq == eq_total;
+        cluster.sync();  // everyone has read the leader's checks before they may be reset
+        if (consistent) break;
         // The histogram given does not describe these scores: rebuild it here.
-        if (tid == 0) set_status(status, ECHO_ST_BADDATA);
+        if (leader && tid == 0) set_status(status, ECHO_ST_BADDATA);
         have = false;
-        __syncthreads();
-    }
-    const uint32_t need = static_cast<uint32_t>(k) - above;  // >= 1
-    const uint32_t cnt = sh.cnt;
-    if (tid == 0 && stats) {
-        atomicMax(stats + ECHO_STAT_BOUNDARY_MAX, cnt);
-        if (cnt > kCandMax) atomicAdd(stats + ECHO_STAT_TOPK_FALLBACK, 1u);
-    }
-    __syncthreads();
-
-    // ---- 3. K*, the key of the k-th score, and the index cut among equal keys
-    uint32_t rem = 0, eqn = 0, K = 0, idx_cut = 0xFFFFFFFFu;
-    if (cnt <= kCandMax) {
-        SmemCands src{sh.cand_key, sh.cand_idx, cnt, false, 0};
-        K = radix_select(src, need, sh, &rem, &eqn);
-        if (rem < eqn) {
-            SmemCands src2{sh.cand_key, sh.cand_idx, cnt, true, K};
-            uint32_t r2, e2;
-            idx_cut = ~radix_select(src2, rem, sh, &r2, &e2);
-        }
-    } else {
-        GlobalCands src{sc, n, shift, bstar, false, 0};
-        K = radix_select(src, need, sh, &rem, &eqn);
-        if (rem < eqn) {
-            GlobalCands src2{sc, n, shift, bstar, true, K};
-            uint32_t r2, e2;
-            idx_cut = ~radix_select(src2, rem, sh, &r2, &e2);
-        }
     }
 
-    // ---- 4. ordered compaction
-    if (tid == 0) sh.flag = 0;
-    __syncthreads();
-    uint32_t written = 0;
+    // ---- 3. K*, the key of the k-th score, and the index cut among equal keys (leader)
+    if (leader) {
+        const uint32_t need = static_cast<uint32_t>(k) - above;  // >= 1
+        const uint32_t cnt = sh.cnt;
+        if (tid == 0 && stats) {
+            atomicMax(stats + ECHO_STAT_BOUNDARY_MAX, cnt);
+            if (cnt > kCandMax) atomicAdd(stats + ECHO_STAT_TOPK_FALLBACK, 1u);
+        }
+        uint32_t rem = 0, eqn = 0, K = 0, idx_cut = 0xFFFFFFFFu;
+        if (cnt <= kCandMax) {
+            SmemCands src{sh.cand_key, sh.cand_idx, cnt, false, 0};
+            K = radix_select(src, need, sh, &rem, &eqn);
+            if (rem < eqn) {
+                SmemCands src2{sh.cand_key, sh.cand_idx, cnt, true, K};
+                uint32_t r2, e2;
+                idx_cut = ~radix_select(src2, rem, sh, &r2, &e2);
+            }
+        } else {
+            GlobalCands src{sc, n, shift, bstar, false, 0};
+            K = radix_select(src, need, sh, &rem, &eqn);
+            if (rem < eqn) {
+                GlobalCands src2{sc, n, shift, bstar, true, K};
+                uint32_t r2, e2;
+                idx_cut = ~radix_select(src2, rem, sh, &r2, &e2);
+            }
+        }
+        if (tid == 0) {
+            sh.K = K;
+            sh.idx_cut = idx_cut;
+        }
+    }
+    cluster.sync();
+    const uint32_t K = lsh.K, idx_cut = lsh.idx_cut;
+
+    // ---- 4. ordered compaction: count, cluster prefix, write
+    uint32_t mine = 0;
     bool nan = false;
-    for (int64_t c0 = 0; c0 < n; c0 += 4 * kTT) {
+    for (int64_t s = s_lo + tid; s < s_hi; s += kTT) {
+        const float x = sc[s];
+        nan |= isnan(x);
+        mine += takes(x, shift, bstar, K, idx_cut, s);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+    if (tid == 0) {
+        sh.selected = 0;
+        sh.flag = 0;
+    }
+    __syncthreads();
+    if ((tid & 31) == 0 && mine) atomicAdd(&sh.selected, mine);
+    if (nan) sh.flag = 1;
+    cluster.sync();
+    uint32_t offset = 0, total = 0;
+    for (int r = 0; r < kCS; ++r) {
+        const uint32_t c = cluster.map_shared_rank(&sh, r)->selected;
+        if (r < rank) offset += c;
+        total += c;
+    }
+    uint32_t written = offset;
+    for (int64_t c0 = s_lo; c0 < s_hi; c0 += 4 * kTT) {
         const int64_t s0 = c0 + 4 * tid;
         uint32_t f = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int64_t s = s0 + j;
-            if (s < n) {
-                const float x = sc[s];
-                nan |= isnan(x);
-                const uint32_t bin = shifted_bin(x, shift);
-                const uint32_t key = order_key(x);
-                const bool take = bin > bstar ||
-                                  (bin == bstar && (key > K || (key == K && static_cast<uint32_t>(s) <= idx_cut)));
-                f |= static_cast<uint32_t>(take) << j;
-            }
+            if (s < s_hi && takes(sc[s], shift, bstar, K, idx_cut, s)) f |= 1u << j;
         }
         uint32_t tot;
         uint32_t pos = written + block_exclusive_scan<kTT>(__popc(f), sh.scan, &tot);
@@ -326,16 +391,17 @@ __global__ void __launch_bounds__(kTT, 1)
             }
         written += tot;
     }
-    if (nan) sh.flag = 1;
-    for (int i = static_cast<int>(written) + tid; i < k; i += kTT) out[i] = -1;
-    __syncthreads();
-    if (tid == 0) {
-        if (sh.flag) set_status(status, ECHO_ST_NAN);
-        if (written != static_cast<uint32_t>(k)) set_status(status, ECHO_ST_BADDATA);
-        const float kth = key_to_float(K);
-        kth_out[b] = kth;
-        if (theta_hat) theta_hat[b] = ema_update(th_old, kth, alpha);
+    if (leader) {
+        for (int i = static_cast<int>(total) + tid; i < k; i += kTT) out[i] = -1;
+        if (tid == 0) {
+            if (total != static_cast<uint32_t>(k)) set_status(status, ECHO_ST_BADDATA);
+            const float kth = key_to_float(K);
+            kth_out[b] = kth;
+            if (theta_hat) theta_hat[b] = ema_update(th_old, kth, alpha);
+        }
     }
+    if (tid == 0 && sh.flag) set_status(status, ECHO_ST_NAN);
+    cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
 }  // namespace
@@ -352,8 +418,8 @@ extern "C" int echo_topk_select(int B, const int64_t* tok_off, int64_t n_tokens,
     const size_t smem = sizeof(TopkShared);
     ECHO_CUDA_OK(cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(smem)));
-    topk_kernel<<<B, kTT, smem, stream>>>(tok_off, n_tokens, scores, k, hist, theta_hat, alpha, sel_idx, kth, status,
-                                          stats);
+    topk_kernel<<<B * kCS, kTT, smem, stream>>>(tok_off, n_tokens, scores, k, hist, theta_hat, alpha, sel_idx, kth,
+                                                status, stats);
     ECHO_CUDA_OK(cudaGetLastError());
     return ECHO_OK;
 }

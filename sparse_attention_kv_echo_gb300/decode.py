@@ -4,8 +4,9 @@ A DecodeLayer owns the torch tensors one layer needs for B requests (scores,
 histogram, threshold state, selection, the GPU cache and its lists, the
 quantised query) and issues the calls of a step:
     echo_quantize_q    -> E4M3 query, folded head weights, cleared histogram
-    echo_index_scores  -> scores, shifted-score histogram
-    echo_early_fetch   -> tokens above the predicted threshold (+ recall)
+    echo_index_scores  -> scores, shifted-score histogram, above-threshold bits
+    echo_early_fetch   -> tokens above the predicted threshold (+ recall); on a
+                          side stream, concurrently with top-k
     echo_topk_select   -> exact top-k indices, k-th score, EMA threshold
     echo_cache_step    -> free / allocate / recall, slot of every selection
 Every buffer keeps its address and size, so ``step`` can be captured into a
@@ -39,6 +40,7 @@ class DecodeLayer:
         self.sel_idx = torch.full((self.B, self.k), -1, **i32)
         self.sel_slot = torch.full((self.B, self.k), -1, **i32)
         self.kth = torch.zeros((self.B,), **f32)
+        self.above = torch.zeros(max(L.above_words(self.B, self.n_tokens), 1), **i32)
         self.q8 = torch.zeros((self.B, L.HEADS, L.DIM), dtype=torch.uint8, device=device)
         self.qscale = torch.zeros((self.B, L.HEADS), **f32)
         self.wfold = torch.zeros((self.B, L.HEADS), **f32)
@@ -47,6 +49,7 @@ class DecodeLayer:
         self.q_in = torch.zeros((self.B, L.HEADS, L.DIM), **f32)
         self.w_in = torch.zeros((self.B, L.HEADS), **f32)
         self.cache = L.LayerCache(self.B, self.n_tokens, self.C, host_pool, device=device)
+        self.side = torch.cuda.Stream(device=device)
 
     def reset(self):
         self.cache.reset()
@@ -56,19 +59,28 @@ class DecodeLayer:
 
     def step(self, q: torch.Tensor | None = None, w: torch.Tensor | None = None, stream=None,
              copy_stream=None):
-        """Enqueue one decode step (q [B,64,128] f32, w [B,64] f32; defaults q_in / w_in)."""
+        """Enqueue one decode step (q [B,64,128] f32, w [B,64] f32; defaults q_in / w_in).
+
+        stream: the step's stream (default: current); copy_stream: recalls (default: stream).
+        The early fetch's selection runs on the layer's side stream while top-k runs."""
         q = self.q_in if q is None else q
         w = self.w_in if w is None else w
-        L.quantize_q(q, w, self.q8, self.qscale, self.wfold, self.status, hist=self.hist, stream=stream)
+        main = torch.cuda.current_stream() if stream is None else stream
+        L.quantize_q(q, w, self.q8, self.qscale, self.wfold, self.status, hist=self.hist, stream=main)
         L.index_scores(self.tok_off, self.n_tokens, self.q8, self.wfold, self.k8, self.ks, self.scores,
-                       self.theta, self.hist, self.status, stream=stream)
+                       self.theta, self.hist, self.status, above=self.above if self.predictor else None,
+                       stream=main)
         if self.predictor:
-            L.early_fetch(self.tok_off, self.n_tokens, self.scores, self.theta, self.early_cap, self.cache,
-                          self.status, stats=self.stats, stream=stream, copy_stream=copy_stream)
+            self.side.wait_stream(main)
+            L.early_fetch(self.tok_off, self.n_tokens, self.above, self.early_cap, self.cache, self.status,
+                          stats=self.stats, stream=self.side,
+                          copy_stream=copy_stream if copy_stream is not None else self.side)
         L.topk_select(self.tok_off, self.n_tokens, self.scores, self.k, self.hist, self.theta, self.alpha,
-                      self.sel_idx, self.kth, self.status, stats=self.stats, stream=stream)
+                      self.sel_idx, self.kth, self.status, stats=self.stats, stream=main)
+        if self.predictor:
+            main.wait_stream(self.side)
         L.cache_step(self.tok_off, self.n_tokens, self.sel_idx, self.cache, self.sel_slot, self.status,
-                     stats=self.stats, stream=stream, copy_stream=copy_stream)
+                     stats=self.stats, stream=main, copy_stream=copy_stream)
 
     def kernel_launches_per_step(self) -> int:
         # quantize + score (+ early select + early recall) + top-k + cache step + recall

@@ -82,14 +82,14 @@ def test_e4m3_conversion_sweep():
     assert bad.size == 0, (x[bad[:5]], got[bad[:5]], ref[bad[:5]])
 
 
-def _scores_gpu(off, n, q, w, k8, ks, scores, theta, hist, status):
+def _scores_gpu(off, n, q, w, k8, ks, scores, theta, hist, status, above=None):
     """quantize_q (clears hist) then index_scores, as a step issues them."""
     B = q.shape[0]
     q8 = torch.empty((B, 64, 128), dtype=torch.uint8, device=dev)
     qs = torch.empty((B, 64), dtype=torch.float32, device=dev)
     wf = torch.empty((B, 64), dtype=torch.float32, device=dev)
     L.quantize_q(q, w, q8, qs, wf, status, hist=hist)
-    L.index_scores(off, n, q8, wf, k8, ks, scores, theta, hist, status)
+    L.index_scores(off, n, q8, wf, k8, ks, scores, theta, hist, status, above=above)
 
 
 def _score_call(w, layer=0, theta=None, device_keys="cpu"):
@@ -103,11 +103,12 @@ def _score_call(w, layer=0, theta=None, device_keys="cpu"):
     th = torch.full((w.B,), math.inf if theta is None else theta, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     hist.fill_(12345)                                 # stale contents: quantize_q must clear them
+    above = torch.full((L.above_words(w.B, n),), -1, dtype=torch.int32, device=dev)
     _scores_gpu(torch.from_numpy(off).to(dev), n, q.to(dev), wt.to(dev), k8.to(dev), ks.to(dev), scores,
-                th, hist, st)
+                th, hist, st, above=above)
     torch.cuda.synchronize()
     return off, k8.cpu().numpy(), ks.cpu().numpy(), q.cpu().numpy(), wt.cpu().numpy(), scores.cpu().numpy(), \
-        hist.cpu().numpy().view(np.uint32), int(st.item()), th.cpu().numpy()
+        hist.cpu().numpy().view(np.uint32), int(st.item()), th.cpu().numpy(), above.cpu().numpy().view(np.uint32)
 
 
 @pytest.mark.parametrize("lengths,theta", [
@@ -118,11 +119,24 @@ def _score_call(w, layer=0, theta=None, device_keys="cpu"):
 def test_scores_and_hist(lengths, theta):
     from tests._parity import check_scores
     w = wl.scaled(wl.WORKLOADS["tiny"], "s", B=len(lengths), lengths=tuple(lengths))
-    off, k8, ks, q, wt, gs, gh, st, th = _score_call(w, theta=theta)
+    off, k8, ks, q, wt, gs, gh, st, th, ab = _score_call(w, theta=theta)
     assert st == 0
     check_scores((off, k8, ks), q, wt, gs)
+    t0 = 0
     for b in range(w.B):
-        assert np.array_equal(gh[b], orc.hist256(gs[off[b]:off[b + 1]], th[b]))
+        sc = gs[off[b]:off[b + 1]]
+        assert np.array_equal(gh[b], orc.hist256(sc, th[b]))
+        # above-threshold bits: request b's words start at 4 * (tiles of the requests before it)
+        nb = sc.size
+        words = 4 * ((nb + 127) // 128)
+        bits = np.unpackbits(ab[t0:t0 + words].view(np.uint8), bitorder="little")[:nb].astype(bool) \
+            if words else np.zeros(0, bool)
+        want = (sc > th[b]) if np.isfinite(th[b]) else np.zeros(nb, bool)
+        assert np.array_equal(bits, want), b
+        if words:
+            pad = np.unpackbits(ab[t0:t0 + words].view(np.uint8), bitorder="little")[nb:]
+            assert not pad.any()
+        t0 += words
     assert np.all(np.isnan(gs[w.total_tokens:]))      # rows outside every request untouched
 
 
