@@ -9,7 +9,8 @@
  *      (echo_early_fetch), then the exact top-k tokens and the EMA threshold
  *      prediction (echo_topk_select),
  *   3. the GPU-cache step: free unselected slots, allocate slots for the
- *      misses, recall the missing KV rows from the host pool (echo_cache_step).
+ *      misses, recall the missing KV rows from the host pool (echo_cache_step);
+ * and, for chunked prefill, a block of query rows at once (echo_prefill_block).
  *
  * Sources (page title, then section):
  *   [EXPL] "ECHO: Lossless KV Cache Offloading for Sparse Attention LLMs",
@@ -209,6 +210,49 @@ int echo_topk_select(int B, const int64_t* tok_off, int64_t n_tokens, const floa
 int echo_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
                     const echo_cache* cache, int32_t* sel_slot, int32_t* status, uint32_t* stats,
                     echo_stream_t stream, echo_stream_t copy_stream);
+
+/*
+ * Chunked prefill [EXPL panel "Prefill: one-round histogram"; AE section
+ * "Fused Prefetch Kernels (ECHO only)", inter-query prefetch].
+ *
+ * echo_prefill_scores: scores of one block of R query rows against the
+ * prompt's keys, causal.  Row r sits at position row0 + r and sees keys
+ * [0, row0 + r] (itself included); its scores go to scores[r*W + s] for
+ * s <= row0 + r (the rest of the row is untouched), with
+ * scores = ks[s] * sum_h wfold[r,h] * max(0, sum_d q8[r,h,d] * k8[s,d]).
+ * hist [R,256] (may be NULL) ADDS the per-row counts of the 256 bins of
+ * orderkey(fp32(score - theta)) >> 24, theta = *theta_hat when finite else 0
+ * (one scalar for the block).  Needs row0 + R <= n_keys and W >= row0 + R.
+ */
+int echo_prefill_scores(int R, int64_t row0, int64_t n_keys, const uint8_t* q8, const float* wfold,
+                        const uint8_t* k8, const float* ks, float* scores, int64_t W,
+                        const float* theta_hat, uint32_t* hist, int32_t* status, echo_stream_t stream);
+
+/* Bytes of device workspace echo_prefill_block needs for R rows and row stride W. */
+size_t echo_prefill_workspace_size(int R, int64_t W);
+
+/*
+ * One prefill block: on `stream`, quantise the R rows q [R,64,128] / w [R,64]
+ * (echo_quantize_q), score them (echo_prefill_scores into scores [R,W] and
+ * hist [R,256]), select each row's exact top-k over its causal prefix into
+ * sel_idx [R,k] (ascending, -1 padded; every token when row0 + r + 1 <= k)
+ * with its k-th score in kth [R], then the union of the rows' selections:
+ * union_list [W] (ascending, -1 padded), *union_count, union_bits
+ * [ceil(W/32)] (may be NULL), and the block threshold update
+ * *theta_hat <- EMA(alpha) with the last row's k-th score (+inf: replaced).
+ * With a cache (B = 1 over the whole prompt, C >= W): the cache step on the
+ * union (free the rest, misses -> lowest free slots; sel_slot [W]) after the
+ * previous block's recall has read its lists, and the recall of the misses on
+ * copy_stream, which overlaps the next block's scoring on `stream`.
+ * ws: echo_prefill_workspace_size(R, W) bytes, 256-byte aligned.
+ */
+int echo_prefill_block(int R, int64_t row0, int64_t n_keys, const float* q, const float* w,
+                       const uint8_t* k8, const float* ks, int k, float* theta_hat, float alpha,
+                       float* scores, int64_t W, uint32_t* hist, int32_t* sel_idx, float* kth,
+                       int32_t* union_list, int32_t* union_count, uint32_t* union_bits,
+                       const echo_cache* cache, int32_t* sel_slot, void* ws, size_t ws_bytes,
+                       int32_t* status, uint32_t* stats, echo_stream_t stream,
+                       echo_stream_t copy_stream);
 
 /* Device-accessible address of a pinned host buffer (for echo_cache.host_kv).
  * Returns ECHO_ECUDA when the pointer is not pinned/mapped host memory. */

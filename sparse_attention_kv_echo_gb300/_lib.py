@@ -22,7 +22,8 @@ STATS_N = 8
 HEADS, DIM, MAX_REQUESTS = 64, 128, 4096
 
 EXPORTS = ("echo_above_words", "echo_cache_step", "echo_device_sm_count", "echo_early_fetch",
-           "echo_host_device_alias", "echo_index_scores", "echo_quantize_q", "echo_topk_select")
+           "echo_host_device_alias", "echo_index_scores", "echo_prefill_block", "echo_prefill_scores",
+           "echo_prefill_workspace_size", "echo_quantize_q", "echo_topk_select")
 
 _vp = ctypes.c_void_p
 
@@ -75,6 +76,14 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         L.echo_cache_step.restype = i32
         L.echo_cache_step.argtypes = [i32, _vp, i64, _vp, i32, ctypes.POINTER(EchoCacheStruct), _vp,
                                       _vp, _vp, _vp, _vp]
+        L.echo_prefill_scores.restype = i32
+        L.echo_prefill_scores.argtypes = [i32, i64, i64, _vp, _vp, _vp, _vp, _vp, i64, _vp, _vp, _vp, _vp]
+        L.echo_prefill_workspace_size.restype = ctypes.c_size_t
+        L.echo_prefill_workspace_size.argtypes = [i32, i64]
+        L.echo_prefill_block.restype = i32
+        L.echo_prefill_block.argtypes = [i32, i64, i64, _vp, _vp, _vp, _vp, i32, _vp, f32, _vp, i64, _vp, _vp,
+                                         _vp, _vp, _vp, _vp, ctypes.POINTER(EchoCacheStruct), _vp, _vp,
+                                         ctypes.c_size_t, _vp, _vp, _vp, _vp]
         L.echo_host_device_alias.restype = i32
         L.echo_host_device_alias.argtypes = [_vp, ctypes.POINTER(_vp)]
         L.echo_device_sm_count.restype = i32
@@ -157,6 +166,28 @@ def cache_step(tok_off, n_tokens, sel, cache, sel_slot, status, stats=None, stre
     _check("echo_cache_step", load().echo_cache_step(
         B, _ptr(tok_off), int(n_tokens), _ptr(sel), int(m), ctypes.byref(cache.struct), _ptr(sel_slot),
         _ptr(status), _ptr(stats), st, cst))
+
+
+def prefill_scores(R, row0, n_keys, q8, wfold, k8, ks, scores, W, theta_hat, hist, status, stream=None):
+    _check("echo_prefill_scores", load().echo_prefill_scores(
+        int(R), int(row0), int(n_keys), _ptr(q8), _ptr(wfold), _ptr(k8), _ptr(ks), _ptr(scores), int(W),
+        _ptr(theta_hat), _ptr(hist), _ptr(status), _stream(stream)))
+
+
+def prefill_workspace_size(R: int, W: int) -> int:
+    return int(load().echo_prefill_workspace_size(int(R), int(W)))
+
+
+def prefill_block(R, row0, n_keys, q, w, k8, ks, k, theta_hat, alpha, scores, W, hist, sel_idx, kth,
+                  union_list, union_count, union_bits, cache, sel_slot, ws, status, stats=None, stream=None,
+                  copy_stream=None):
+    st = _stream(stream)
+    cst = _stream(copy_stream) if copy_stream is not None else st
+    _check("echo_prefill_block", load().echo_prefill_block(
+        int(R), int(row0), int(n_keys), _ptr(q), _ptr(w), _ptr(k8), _ptr(ks), int(k), _ptr(theta_hat),
+        float(alpha), _ptr(scores), int(W), _ptr(hist), _ptr(sel_idx), _ptr(kth), _ptr(union_list),
+        _ptr(union_count), _ptr(union_bits), ctypes.byref(cache.struct) if cache is not None else None,
+        _ptr(sel_slot), _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _ptr(stats), st, cst))
 
 
 class LayerCache:

@@ -331,28 +331,46 @@ cudaError_t launch_recall(int B, const int64_t* tok_off, int64_t n_tokens, int C
 
 }  // namespace echo
 
-extern "C" int echo_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
-                               const echo_cache* cache, int32_t* sel_slot, int32_t* status, uint32_t* stats,
-                               echo_stream_t stream, echo_stream_t copy_stream) {
-    using namespace echo;
-    if (B <= 0 || n_tokens < 0 || m < 0) return ECHO_EINVAL;
-    if (B > ECHO_MAX_REQUESTS) return ECHO_EUNSUPPORTED;
-    if (!tok_off || !status || (m > 0 && (!sel || !sel_slot))) return ECHO_EINVAL;
-    if (n_tokens >= (1ll << 31)) return ECHO_EUNSUPPORTED;
-    int rc = check_cache(cache, B, m);
-    if (rc) return rc;
-    if (cache->C > kMaxSlotsSmem) return ECHO_EUNSUPPORTED;
+namespace echo {
+
+int enqueue_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
+                       const echo_cache* cache, int32_t* sel_slot, int32_t* status, uint32_t* stats,
+                       cudaStream_t stream, cudaStream_t copy_stream) {
     const size_t smem = static_cast<size_t>(cache->C / 32) * sizeof(uint32_t);
     ECHO_CUDA_OK(cudaFuncSetAttribute(cache_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(smem)));
     cache_step_kernel<<<B, kCT, smem, stream>>>(tok_off, n_tokens, sel, m, cache_args(*cache), sel_slot, status,
                                                 stats);
     ECHO_CUDA_OK(cudaGetLastError());
-    rc = stream_wait(copy_stream, stream);
+    const int rc = stream_wait(copy_stream, stream);
     if (rc) return rc;
     ECHO_CUDA_OK(launch_recall(B, tok_off, n_tokens, cache->C, cache->miss_tok, cache->miss_slot, cache->miss_cnt,
                                cache->host_kv, cache->dev_kv, cache->row_bytes, status, copy_stream));
     return ECHO_OK;
+}
+
+int check_cache_step_args(int B, int64_t n_tokens, const int32_t* sel, int m, const echo_cache* cache,
+                          const int32_t* sel_slot) {
+    if (B <= 0 || n_tokens < 0 || m < 0) return ECHO_EINVAL;
+    if (B > ECHO_MAX_REQUESTS) return ECHO_EUNSUPPORTED;
+    if (m > 0 && (!sel || !sel_slot)) return ECHO_EINVAL;
+    if (n_tokens >= (1ll << 31)) return ECHO_EUNSUPPORTED;
+    const int rc = check_cache(cache, B, m);
+    if (rc) return rc;
+    if (cache->C > kMaxSlotsSmem) return ECHO_EUNSUPPORTED;
+    return ECHO_OK;
+}
+
+}  // namespace echo
+
+extern "C" int echo_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
+                               const echo_cache* cache, int32_t* sel_slot, int32_t* status, uint32_t* stats,
+                               echo_stream_t stream, echo_stream_t copy_stream) {
+    using namespace echo;
+    if (!tok_off || !status) return ECHO_EINVAL;
+    const int rc = check_cache_step_args(B, n_tokens, sel, m, cache, sel_slot);
+    if (rc) return rc;
+    return enqueue_cache_step(B, tok_off, n_tokens, sel, m, cache, sel_slot, status, stats, stream, copy_stream);
 }
 
 extern "C" int echo_early_fetch(int B, const int64_t* tok_off, int64_t n_tokens, const uint32_t* above,

@@ -8,6 +8,7 @@
 
 #include "echo.h"
 
+
 namespace echo {
 
 inline bool is_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -36,6 +37,16 @@ cudaError_t launch_early_select(int B, const int64_t* tok_off, int64_t n_tokens,
 cudaError_t launch_recall(int B, const int64_t* tok_off, int64_t n_tokens, int C, const int32_t* tok_list,
                           const int32_t* slot_list, const int32_t* cnt, const void* host_kv, void* dev_kv,
                           int64_t row_bytes, int32_t* status, cudaStream_t s);
+
+// Enqueue helpers shared by the decode calls and the prefill block call.
+int launch_topk(int B, const int64_t* tok_off, int64_t n_tokens, int64_t row0, int64_t W, const float* scores, int k,
+                const uint32_t* hist, float* theta_hat, float alpha, int32_t* sel_idx, float* kth, int32_t* status,
+                uint32_t* stats, cudaStream_t stream);
+int check_cache_step_args(int B, int64_t n_tokens, const int32_t* sel, int m, const echo_cache* cache,
+                          const int32_t* sel_slot);
+int enqueue_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
+                       const echo_cache* cache, int32_t* sel_slot, int32_t* status, uint32_t* stats,
+                       cudaStream_t stream, cudaStream_t copy_stream);
 
 }  // namespace echo
 

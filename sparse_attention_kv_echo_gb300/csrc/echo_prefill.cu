@@ -1,0 +1,165 @@
+// echo_prefill.cu -- chunked prefill, one block of query rows at a time.
+//
+// "ECHO: Lossless KV Cache Offloading for Sparse Attention LLMs", section 2,
+// panel "Prefill: one-round histogram": while the indexer scores query block
+// i+1, the tokens of block i are fetched; the real kernel bins scores into
+// 256 bins over the top 8 bits of each score shifted by the predicted
+// threshold.
+//
+// echo_prefill_block enqueues, on `stream`:
+//   quantize_kernel      the block's R query rows (each row is its own "request")
+//   score_kernel         prefill mode: row r at position row0 + r scores keys
+//                        [0, row0 + r] (causal, itself included) into scores[r*W + s],
+//                        with the per-row histogram shifted by the block's threshold
+//   topk_kernel          one 8-CTA cluster per row: exact top-k of the row
+//   union_mark_kernel    marks every token some row selected
+//   union_compact_kernel ascending list of the marked tokens (the block's
+//                        selection for the cache), its bit words, and the
+//                        block threshold update: EMA (alpha) of the last row's
+//                        k-th score
+//   cache_step_kernel    free / allocate for the union (after the previous
+//                        block's recall has read its lists),
+// and the recall of the misses on `copy_stream`, so that the next block's
+// scoring on `stream` overlaps it.
+#include "echo_common.cuh"
+#include "echo_internal.h"
+
+namespace echo {
+namespace {
+
+constexpr int kPT = 1024;
+
+__global__ void union_mark_kernel(const int32_t* __restrict__ sel, int64_t total, uint8_t* __restrict__ mark,
+                                  int64_t n) {
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int32_t s = sel[i];
+        if (s >= 0 && s < n) mark[s] = 1;
+    }
+}
+
+__device__ __forceinline__ float block_ema(float theta, float kth, float alpha) {
+    if (isinf(kth) && kth < 0) return theta;
+    if (isinf(theta)) return kth;
+    return __fadd_rn(__fmul_rn(alpha, kth), __fmul_rn(__fsub_rn(1.0f, alpha), theta));
+}
+
+__global__ void __launch_bounds__(kPT) union_compact_kernel(const uint8_t* __restrict__ mark, int64_t n, int64_t m,
+                                                            int32_t* __restrict__ list, uint32_t* union_bits,
+                                                            int32_t* count, int64_t* tok_off2, int64_t n_keys,
+                                                            const float* kth, int R, float* theta, float alpha) {
+    __shared__ uint32_t scan[40];
+    uint32_t done = 0;
+    const int64_t words = (n + 31) / 32;
+    for (int64_t w0 = 0; w0 < words; w0 += kPT) {
+        const int64_t w = w0 + threadIdx.x;
+        uint32_t bits = 0;
+        if (w < words) {
+            for (int j = 0; j < 32; ++j) {
+                const int64_t s = 32 * w + j;
+                if (s < n && mark[s]) bits |= 1u << j;
+            }
+            if (union_bits) union_bits[w] = bits;
+        }
+        uint32_t tot;
+        uint32_t pos = done + block_exclusive_scan<kPT>(__popc(bits), scan, &tot);
+        while (bits) {
+            const int j = __ffs(bits) - 1;
+            bits &= bits - 1;
+            if (pos < m) list[pos] = static_cast<int32_t>(32 * w + j);
+            ++pos;
+        }
+        done += tot;
+    }
+    for (int64_t i = done + threadIdx.x; i < m; i += kPT) list[i] = -1;
+    if (threadIdx.x == 0) {
+        *count = static_cast<int32_t>(done);
+        tok_off2[0] = 0;
+        tok_off2[1] = n_keys;
+        if (theta) *theta = block_ema(*theta, kth[R - 1], alpha);
+    }
+}
+
+struct PrefillWs {
+    uint8_t* q8;
+    float* qscale;
+    float* wfold;
+    uint8_t* mark;
+    int64_t* tok_off2;
+};
+
+size_t prefill_ws_bytes(int R, int64_t W) {
+    const size_t r = static_cast<size_t>(R);
+    return round_up(r * ECHO_HEADS * ECHO_DIM, 256) + 2 * round_up(r * ECHO_HEADS * 4, 256) +
+           round_up(static_cast<size_t>(W), 256) + 256;
+}
+
+PrefillWs carve(void* ws, int R, int64_t W) {
+    uint8_t* p = static_cast<uint8_t*>(ws);
+    const size_t r = static_cast<size_t>(R);
+    PrefillWs o;
+    o.q8 = p;
+    p += round_up(r * ECHO_HEADS * ECHO_DIM, 256);
+    o.qscale = reinterpret_cast<float*>(p);
+    p += round_up(r * ECHO_HEADS * 4, 256);
+    o.wfold = reinterpret_cast<float*>(p);
+    p += round_up(r * ECHO_HEADS * 4, 256);
+    o.mark = p;
+    p += round_up(static_cast<size_t>(W), 256);
+    o.tok_off2 = reinterpret_cast<int64_t*>(p);
+    return o;
+}
+
+}  // namespace
+}  // namespace echo
+
+extern "C" size_t echo_prefill_workspace_size(int R, int64_t W) {
+    if (R <= 0 || W <= 0) return 0;
+    return echo::prefill_ws_bytes(R, W);
+}
+
+extern "C" int echo_prefill_block(int R, int64_t row0, int64_t n_keys, const float* q, const float* w,
+                                  const uint8_t* k8, const float* ks, int k, float* theta_hat, float alpha,
+                                  float* scores, int64_t W, uint32_t* hist, int32_t* sel_idx, float* kth,
+                                  int32_t* union_list, int32_t* union_count, uint32_t* union_bits,
+                                  const echo_cache* cache, int32_t* sel_slot, void* ws, size_t ws_bytes,
+                                  int32_t* status, uint32_t* stats, echo_stream_t stream, echo_stream_t copy_stream) {
+    using namespace echo;
+    if (R <= 0 || row0 < 0 || n_keys <= 0 || k <= 0 || W <= 0) return ECHO_EINVAL;
+    if (R > ECHO_MAX_REQUESTS) return ECHO_EUNSUPPORTED;
+    if (!q || !w || !k8 || !ks || !theta_hat || !scores || !hist || !sel_idx || !kth || !union_list ||
+        !union_count || !ws || !status)
+        return ECHO_EINVAL;
+    if (row0 + R > n_keys || W < row0 + R) return ECHO_EINVAL;
+    if (W > (1ll << 31) || n_keys >= (1ll << 31)) return ECHO_EUNSUPPORTED;
+    if (!is_aligned(q, 16) || !is_aligned(k8, 16) || !is_aligned(ws, 256)) return ECHO_EINVAL;
+    if (ws_bytes < prefill_ws_bytes(R, W)) return ECHO_ECAPACITY;
+    if (cache) {
+        const int rc = check_cache_step_args(1, n_keys, union_list, static_cast<int>(W), cache, sel_slot);
+        if (rc) return rc;
+    }
+    const PrefillWs p = carve(ws, R, W);
+    if (launch_quantize(R, q, w, p.q8, p.qscale, p.wfold, hist, status, stream) != cudaSuccess) return ECHO_ECUDA;
+    int rc = echo_prefill_scores(R, row0, n_keys, p.q8, p.wfold, k8, ks, scores, W, theta_hat, hist, status, stream);
+    if (rc) return rc;
+    rc = launch_topk(R, nullptr, 0, row0, W, scores, k, hist, theta_hat, alpha, sel_idx, kth, status, stats, stream);
+    if (rc) return rc;
+    const int64_t n = row0 + R;
+    ECHO_CUDA_OK(cudaMemsetAsync(p.mark, 0, static_cast<size_t>(n), stream));
+    const int64_t total = static_cast<int64_t>(R) * k;
+    const int sms = sm_count();
+    if (sms <= 0) return ECHO_ECUDA;
+    int64_t grid = (total + 255) / 256;
+    if (grid > 8 * sms) grid = 8 * sms;
+    union_mark_kernel<<<static_cast<int>(grid), 256, 0, stream>>>(sel_idx, total, p.mark, n);
+    ECHO_CUDA_OK(cudaGetLastError());
+    union_compact_kernel<<<1, kPT, 0, stream>>>(p.mark, n, W, union_list, union_bits, union_count, p.tok_off2,
+                                                n_keys, kth, R, theta_hat, alpha);
+    ECHO_CUDA_OK(cudaGetLastError());
+    if (!cache) return ECHO_OK;
+    // the previous block's recall reads the miss lists this step rewrites
+    rc = stream_wait(stream, copy_stream);
+    if (rc) return rc;
+    return enqueue_cache_step(1, p.tok_off2, n_keys, union_list, static_cast<int>(W), cache, sel_slot, status, stats,
+                              stream, copy_stream);
+}

@@ -38,10 +38,16 @@ constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + kEpiWarps * 32;          // 320
 constexpr uint32_t kIdesc = idesc_e4m3_f32(kTileM, ECHO_HEADS);
 
+// Segments: decode requests (CSR tok_off: keys and scores at rows
+// [tok_off[b], tok_off[b+1])) or prefill rows (W > 0: row b at position
+// row0 + b sees keys [0, row0 + b] and writes its scores at b * W).
 struct ScoreArgs {
     int B;
     const int64_t* tok_off;
     int64_t n_tokens;
+    int64_t row0;
+    int64_t W;
+    int theta_stride;
     const float* wfold;
     const float* ks;
     float* scores;
@@ -83,13 +89,27 @@ __device__ __forceinline__ int find_request(const int32_t* tstart, int B, uint32
     return lo;
 }
 
-__device__ __forceinline__ int64_t request_len(const ScoreArgs& a, int b, bool* bad) {
+struct Seg {
+    int64_t key_lo;   // first key row
+    int64_t len;      // keys (= scores) of the segment
+    int64_t out;      // index of its first score
+};
+
+__device__ __forceinline__ Seg segment(const ScoreArgs& a, int b, bool* bad) {
+    if (a.W > 0) {
+        const int64_t len = a.row0 + b + 1;
+        if (len > a.n_tokens || len > a.W) {
+            *bad = true;
+            return Seg{0, 0, 0};
+        }
+        return Seg{0, len, static_cast<int64_t>(b) * a.W};
+    }
     const int64_t lo = a.tok_off[b], hi = a.tok_off[b + 1];
     if (lo < 0 || hi < lo || hi > a.n_tokens) {
         *bad = true;
-        return 0;
+        return Seg{0, 0, 0};
     }
-    return hi - lo;
+    return Seg{lo, hi - lo, lo};
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -111,12 +131,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
         bool bad = false;
         uint32_t local = 0;
-        for (int b = b0; b < b1; ++b) local += static_cast<uint32_t>((request_len(a, b, &bad) + kTileM - 1) / kTileM);
+        for (int b = b0; b < b1; ++b) local += static_cast<uint32_t>((segment(a, b, &bad).len + kTileM - 1) / kTileM);
         uint32_t total;
         uint32_t run = block_exclusive_scan<kThreads>(local, ctl->scan, &total);
         for (int b = b0; b < b1; ++b) {
             tstart[b] = static_cast<int32_t>(run);
-            run += static_cast<uint32_t>((request_len(a, b, &bad) + kTileM - 1) / kTileM);
+            run += static_cast<uint32_t>((segment(a, b, &bad).len + kTileM - 1) / kTileM);
         }
         if (tid == 0) tstart[B] = static_cast<int32_t>(total);
         if (bad) set_status(a.status, ECHO_ST_BADDATA);
@@ -181,7 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 b * ECHO_HEADS);
                     cur_b = b;
                     ++qn;
-                    row_base = a.tok_off[b];
+                    bool bad = false;
+                    row_base = segment(a, b, &bad).key_lo;
                 }
                 const uint32_t s = it % kStages;
                 if (!mbar_wait(smem_addr(&ctl->empty[s]), ((it / kStages) & 1) ^ 1, abort)) {
@@ -265,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float wv[ECHO_HEADS];
         float shift = 0.f, theta = 0.f;
         bool theta_ok = false;
-        int64_t base = 0, nb = 0;
+        int64_t base = 0, nb = 0, obase = 0;
         bool ok = true;
         for (uint32_t it = group; it < ntiles; it += 2) {
             const uint32_t t = t_begin + it;
@@ -293,12 +314,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     wv[4 * i + 2] = x.z;
                     wv[4 * i + 3] = x.w;
                 }
-                const float th = a.theta_hat ? a.theta_hat[b] : __int_as_float(0x7f800000);
+                const float th =
+                    a.theta_hat ? a.theta_hat[static_cast<int64_t>(b) * a.theta_stride] : __int_as_float(0x7f800000);
                 theta_ok = isfinite(th);
                 theta = th;
                 shift = theta_ok ? th : 0.f;
-                base = a.tok_off[b];
-                nb = a.tok_off[b + 1] - base;
+                bool bad = false;
+                const Seg sg = segment(a, b, &bad);
+                base = sg.key_lo;
+                nb = sg.len;
+                obase = sg.out;
             }
             const int64_t tok = static_cast<int64_t>(t - tstart[b]) * kTileM + row;
             const bool valid = tok < nb;
@@ -337,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) a.above[4 * static_cast<size_t>(t) + quarter] = am;
             }
             if (valid) {
-                a.scores[base + tok] = score;
+                a.scores[obase + tok] = score;
                 if (a.hist) {
                     const uint32_t bin = shifted_bin(score, shift);
                     const unsigned grp = __match_any_sync(vm, bin);
@@ -367,12 +392,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 }  // namespace
-}  // namespace echo
 
-extern "C" size_t echo_above_words(int B, int64_t n_tokens) {
-    if (B <= 0 || n_tokens < 0) return 0;
-    return 4 * static_cast<size_t>(n_tokens / echo::kTileM + B);
+static int launch_scores(const ScoreArgs& args, const uint8_t* q8, const uint8_t* k8, int64_t key_rows,
+                         int64_t tiles_ub, cudaStream_t stream) {
+    CUtensorMap kmap, qmap;
+    int rc = encode_tmap_bytes_2d(&kmap, k8, ECHO_DIM, static_cast<uint64_t>(key_rows), ECHO_DIM, kTileM);
+    if (rc) return rc;
+    rc = encode_tmap_bytes_2d(&qmap, q8, ECHO_DIM, static_cast<uint64_t>(args.B) * ECHO_HEADS, ECHO_DIM,
+                              ECHO_HEADS);
+    if (rc) return rc;
+    const int sms = sm_count();
+    if (sms <= 0) return ECHO_ECUDA;
+    const int grid = static_cast<int>(tiles_ub < sms ? tiles_ub : sms);
+    const size_t smem = smem_bytes(args.B);
+    ECHO_CUDA_OK(cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(smem)));
+    score_kernel<<<grid, kThreads, smem, stream>>>(kmap, qmap, args);
+    ECHO_CUDA_OK(cudaGetLastError());
+    return ECHO_OK;
 }
+
+}  // namespace echo
 
 extern "C" int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens, const uint8_t* q8,
                                  const float* wfold, const uint8_t* k8, const float* ks, float* scores,
@@ -386,20 +426,26 @@ extern "C" int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens
     if (n_tokens >= (1ll << 31)) return ECHO_EUNSUPPORTED;
     if (!is_aligned(q8, 16) || !is_aligned(wfold, 16) || !is_aligned(k8, 16)) return ECHO_EINVAL;
     if (n_tokens == 0) return ECHO_OK;
-    CUtensorMap kmap, qmap;
-    int rc = encode_tmap_bytes_2d(&kmap, k8, ECHO_DIM, static_cast<uint64_t>(n_tokens), ECHO_DIM, kTileM);
-    if (rc) return rc;
-    rc = encode_tmap_bytes_2d(&qmap, q8, ECHO_DIM, static_cast<uint64_t>(B) * ECHO_HEADS, ECHO_DIM, ECHO_HEADS);
-    if (rc) return rc;
-    const int sms = sm_count();
-    if (sms <= 0) return ECHO_ECUDA;
-    const int64_t tiles_ub = n_tokens / kTileM + B;
-    const int grid = static_cast<int>(tiles_ub < sms ? tiles_ub : sms);
-    const size_t smem = smem_bytes(B);
-    ECHO_CUDA_OK(cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(smem)));
-    ScoreArgs args{B, tok_off, n_tokens, wfold, ks, scores, theta_hat, hist, above, status};
-    score_kernel<<<grid, kThreads, smem, stream>>>(kmap, qmap, args);
-    ECHO_CUDA_OK(cudaGetLastError());
-    return ECHO_OK;
+    ScoreArgs args{B, tok_off, n_tokens, 0, 0, 1, wfold, ks, scores, theta_hat, hist, above, status};
+    return launch_scores(args, q8, k8, n_tokens, n_tokens / kTileM + B, stream);
+}
+
+extern "C" int echo_prefill_scores(int R, int64_t row0, int64_t n_keys, const uint8_t* q8, const float* wfold,
+                                   const uint8_t* k8, const float* ks, float* scores, int64_t W,
+                                   const float* theta_hat, uint32_t* hist, int32_t* status, echo_stream_t stream) {
+    using namespace echo;
+    if (R <= 0 || row0 < 0 || n_keys <= 0) return ECHO_EINVAL;
+    if (R > ECHO_MAX_REQUESTS) return ECHO_EUNSUPPORTED;
+    if (!q8 || !wfold || !k8 || !ks || !scores || !status) return ECHO_EINVAL;
+    if (row0 + R > n_keys || W < row0 + R) return ECHO_EINVAL;
+    if (n_keys >= (1ll << 31) || static_cast<int64_t>(R) * W >= (1ll << 40)) return ECHO_EUNSUPPORTED;
+    if (!is_aligned(q8, 16) || !is_aligned(wfold, 16) || !is_aligned(k8, 16)) return ECHO_EINVAL;
+    ScoreArgs args{R, nullptr, n_keys, row0, W, 0, wfold, ks, scores, theta_hat, hist, nullptr, status};
+    const int64_t tiles_ub = static_cast<int64_t>(R) * ((row0 + R + kTileM - 1) / kTileM);
+    return launch_scores(args, q8, k8, n_keys, tiles_ub, stream);
+}
+
+extern "C" size_t echo_above_words(int B, int64_t n_tokens) {
+    if (B <= 0 || n_tokens < 0) return 0;
+    return 4 * static_cast<size_t>(n_tokens / 128 + B);
 }

@@ -177,10 +177,20 @@ __device__ __forceinline__ bool takes(float x, float shift, uint32_t bstar, uint
     return bin > bstar || (bin == bstar && (key > K || (key == K && static_cast<uint32_t>(s) <= cut)));
 }
 
+// Segments: decode requests (CSR tok_off over the scores) or prefill rows
+// (W > 0: row b holds row0 + b + 1 scores starting at b * W).  In prefill the
+// threshold is one scalar for every row and is not updated here.
+struct TopkSegs {
+    const int64_t* tok_off;
+    int64_t n_tokens;
+    int64_t row0;
+    int64_t W;
+};
+
 __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTT, 1)
-    topk_kernel(const int64_t* __restrict__ tok_off, int64_t n_tokens, const float* __restrict__ scores, int k,
-                const uint32_t* __restrict__ hist, float* theta_hat, float alpha, int32_t* __restrict__ sel,
-                float* kth_out, int32_t* status, uint32_t* stats) {
+    topk_kernel(TopkSegs segs, const float* __restrict__ scores, int k, const uint32_t* __restrict__ hist,
+                float* theta_hat, float alpha, int32_t* __restrict__ sel, float* kth_out, int32_t* status,
+                uint32_t* stats) {
     extern __shared__ uint8_t smem_raw[];
     TopkShared& sh = *reinterpret_cast<TopkShared*>(smem_raw);
     cg::cluster_group cluster = cg::this_cluster();
@@ -188,15 +198,28 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTT, 1)
     const bool leader = rank == 0;
     TopkShared& lsh = *cluster.map_shared_rank(&sh, 0);     // the leader's shared memory
     const int b = blockIdx.x / kCS, tid = threadIdx.x;
-    const int64_t lo = tok_off[b], hi = tok_off[b + 1];
-    int64_t n = hi - lo;
-    if (lo < 0 || hi < lo || hi > n_tokens) {
-        if (leader && tid == 0) set_status(status, ECHO_ST_BADDATA);
-        n = 0;
+    const bool prefill = segs.W > 0;
+    int64_t lo, n;
+    if (prefill) {
+        lo = static_cast<int64_t>(b) * segs.W;
+        n = segs.row0 + b + 1;
+        if (n > segs.W) {
+            if (leader && tid == 0) set_status(status, ECHO_ST_BADDATA);
+            n = 0;
+        }
+    } else {
+        lo = segs.tok_off[b];
+        const int64_t hi = segs.tok_off[b + 1];
+        n = hi - lo;
+        if (lo < 0 || hi < lo || hi > segs.n_tokens) {
+            if (leader && tid == 0) set_status(status, ECHO_ST_BADDATA);
+            n = 0;
+        }
     }
     const float* sc = scores + (n > 0 ? lo : 0);
     int32_t* out = sel + static_cast<int64_t>(b) * k;
-    const float th_old = theta_hat ? theta_hat[b] : __int_as_float(0x7f800000);
+    float* const theta_upd = prefill ? nullptr : theta_hat;   // prefill: one scalar, updated per block
+    const float th_old = theta_hat ? theta_hat[prefill ? 0 : b] : __int_as_float(0x7f800000);
     const float shift = isfinite(th_old) ? th_old : 0.f;
 
     // ---- trivial requests: the leader alone, no cluster traffic
@@ -228,7 +251,7 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTT, 1)
             if (sh.flag) set_status(status, ECHO_ST_NAN);
             const float kth = key_to_float(sh.minkey);
             kth_out[b] = kth;
-            if (theta_hat) theta_hat[b] = ema_update(th_old, kth, alpha);
+            if (theta_upd) theta_upd[b] = ema_update(th_old, kth, alpha);
         }
         return;
     }
@@ -397,7 +420,7 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTT, 1)
             if (total != static_cast<uint32_t>(k)) set_status(status, ECHO_ST_BADDATA);
             const float kth = key_to_float(K);
             kth_out[b] = kth;
-            if (theta_hat) theta_hat[b] = ema_update(th_old, kth, alpha);
+            if (theta_upd) theta_upd[b] = ema_update(th_old, kth, alpha);
         }
     }
     if (tid == 0 && sh.flag) set_status(status, ECHO_ST_NAN);
@@ -405,6 +428,22 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTT, 1)
 }
 
 }  // namespace
+}  // namespace echo
+
+namespace echo {
+
+int launch_topk(int B, const int64_t* tok_off, int64_t n_tokens, int64_t row0, int64_t W, const float* scores, int k,
+                const uint32_t* hist, float* theta_hat, float alpha, int32_t* sel_idx, float* kth, int32_t* status,
+                uint32_t* stats, cudaStream_t stream) {
+    const size_t smem = sizeof(TopkShared);
+    ECHO_CUDA_OK(cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(smem)));
+    TopkSegs segs{tok_off, n_tokens, row0, W};
+    topk_kernel<<<B * kCS, kTT, smem, stream>>>(segs, scores, k, hist, theta_hat, alpha, sel_idx, kth, status, stats);
+    ECHO_CUDA_OK(cudaGetLastError());
+    return ECHO_OK;
+}
+
 }  // namespace echo
 
 extern "C" int echo_topk_select(int B, const int64_t* tok_off, int64_t n_tokens, const float* scores, int k,
@@ -415,11 +454,6 @@ extern "C" int echo_topk_select(int B, const int64_t* tok_off, int64_t n_tokens,
     if (B > ECHO_MAX_REQUESTS) return ECHO_EUNSUPPORTED;
     if (!tok_off || !sel_idx || !kth || !status || (n_tokens > 0 && !scores)) return ECHO_EINVAL;
     if (n_tokens >= (1ll << 31)) return ECHO_EUNSUPPORTED;
-    const size_t smem = sizeof(TopkShared);
-    ECHO_CUDA_OK(cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(smem)));
-    topk_kernel<<<B * kCS, kTT, smem, stream>>>(tok_off, n_tokens, scores, k, hist, theta_hat, alpha, sel_idx, kth,
-                                                status, stats);
-    ECHO_CUDA_OK(cudaGetLastError());
-    return ECHO_OK;
+    return launch_topk(B, tok_off, n_tokens, 0, 0, scores, k, hist, theta_hat, alpha, sel_idx, kth, status, stats,
+                       stream);
 }
