@@ -62,6 +62,7 @@ typedef struct CUstream_st* echo_stream_t; /* a cudaStream_t; NULL = legacy defa
 #define ECHO_ECAPACITY (-2)     /* k > C, C not a multiple of 32 */
 #define ECHO_EUNSUPPORTED (-3)  /* B above ECHO_MAX_REQUESTS, row size not a multiple of 16 */
 #define ECHO_ECUDA (-4)         /* a CUDA launch or driver call failed */
+#define ECHO_ETOOLARGE (-5)     /* the call needs more than its fixed device scratch holds */
 
 /* device status bits (OR-ed into *status) */
 #define ECHO_ST_TIMEOUT 0x1     /* a bounded wait ran out; outputs of that call are invalid */
@@ -253,6 +254,36 @@ int echo_prefill_block(int R, int64_t row0, int64_t n_keys, const float* q, cons
                        const echo_cache* cache, int32_t* sel_slot, void* ws, size_t ws_bytes,
                        int32_t* status, uint32_t* stats, echo_stream_t stream,
                        echo_stream_t copy_stream);
+
+/*
+ * Allocation-free variant of echo_prefill_block (the pages have no
+ * counterpart: this is a library service, not part of the method).
+ *
+ * For callers that cannot provide device workspace: a runtime that reserves
+ * all of its device memory up front and may not allocate again, an embedder
+ * without an allocator of its own, or a latency-critical thread that cannot
+ * afford the device synchronisation cudaMalloc may imply.  It runs the same
+ * block as echo_prefill_block, with the same arguments minus ws / ws_bytes;
+ * the workspace lives in a fixed device array inside the library, of
+ * ECHO_PREFILL_STATIC_SCRATCH_BYTES, which every GPU that loads the library
+ * keeps until the process exits.  It allocates nothing.
+ *   - Limit: blocks whose workspace (echo_prefill_workspace_size(R, W)) is
+ *     larger than the array return ECHO_ETOOLARGE and enqueue nothing; a
+ *     2048-row block of a 102400-token prompt needs about 18 MB.
+ *   - The first call on each device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls on a device share the one array and it keeps the previous
+ *     call's contents; the block clears what must start at zero itself.
+ *     Calls whose work overlaps on the GPU (other streams, other threads)
+ *     race on the array: order them on one stream or serialise them.
+ */
+#define ECHO_PREFILL_STATIC_SCRATCH_BYTES (32u << 20)
+int echo_prefill_block_static(int R, int64_t row0, int64_t n_keys, const float* q, const float* w,
+                              const uint8_t* k8, const float* ks, int k, float* theta_hat, float alpha,
+                              float* scores, int64_t W, uint32_t* hist, int32_t* sel_idx, float* kth,
+                              int32_t* union_list, int32_t* union_count, uint32_t* union_bits,
+                              const echo_cache* cache, int32_t* sel_slot, int32_t* status, uint32_t* stats,
+                              echo_stream_t stream, echo_stream_t copy_stream);
 
 /* Device-accessible address of a pinned host buffer (for echo_cache.host_kv).
  * Returns ECHO_ECUDA when the pointer is not pinned/mapped host memory. */

@@ -15,14 +15,16 @@ import torch
 
 from . import build as _build
 
-ECHO_OK, ECHO_EINVAL, ECHO_ECAPACITY, ECHO_EUNSUPPORTED, ECHO_ECUDA = 0, -1, -2, -3, -4
+ECHO_OK, ECHO_EINVAL, ECHO_ECAPACITY, ECHO_EUNSUPPORTED, ECHO_ECUDA, ECHO_ETOOLARGE = 0, -1, -2, -3, -4, -5
+PREFILL_STATIC_SCRATCH_BYTES = 32 << 20
 ST_TIMEOUT, ST_NAN, ST_NOSLOT, ST_BADDATA = 0x1, 0x2, 0x4, 0x8
 STAT_TOPK_FALLBACK, STAT_BOUNDARY_MAX, STAT_EARLY, STAT_MISSES, STAT_EARLY_USED = 0, 1, 2, 3, 4
 STATS_N = 8
 HEADS, DIM, MAX_REQUESTS = 64, 128, 4096
 
 EXPORTS = ("echo_above_words", "echo_cache_step", "echo_device_sm_count", "echo_early_fetch",
-           "echo_host_device_alias", "echo_index_scores", "echo_prefill_block", "echo_prefill_scores",
+           "echo_host_device_alias", "echo_index_scores", "echo_prefill_block", "echo_prefill_block_static",
+           "echo_prefill_scores",
            "echo_prefill_workspace_size", "echo_quantize_q", "echo_topk_select")
 
 _vp = ctypes.c_void_p
@@ -84,6 +86,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         L.echo_prefill_block.argtypes = [i32, i64, i64, _vp, _vp, _vp, _vp, i32, _vp, f32, _vp, i64, _vp, _vp,
                                          _vp, _vp, _vp, _vp, ctypes.POINTER(EchoCacheStruct), _vp, _vp,
                                          ctypes.c_size_t, _vp, _vp, _vp, _vp]
+        L.echo_prefill_block_static.restype = i32
+        L.echo_prefill_block_static.argtypes = [i32, i64, i64, _vp, _vp, _vp, _vp, i32, _vp, f32, _vp, i64, _vp,
+                                                _vp, _vp, _vp, _vp, _vp, ctypes.POINTER(EchoCacheStruct), _vp, _vp,
+                                                _vp, _vp, _vp]
         L.echo_host_device_alias.restype = i32
         L.echo_host_device_alias.argtypes = [_vp, ctypes.POINTER(_vp)]
         L.echo_device_sm_count.restype = i32
@@ -188,6 +194,19 @@ def prefill_block(R, row0, n_keys, q, w, k8, ks, k, theta_hat, alpha, scores, W,
         float(alpha), _ptr(scores), int(W), _ptr(hist), _ptr(sel_idx), _ptr(kth), _ptr(union_list),
         _ptr(union_count), _ptr(union_bits), ctypes.byref(cache.struct) if cache is not None else None,
         _ptr(sel_slot), _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _ptr(stats), st, cst))
+
+
+def prefill_block_static(R, row0, n_keys, q, w, k8, ks, k, theta_hat, alpha, scores, W, hist, sel_idx, kth,
+                         union_list, union_count, union_bits, cache, sel_slot, status, stats=None, stream=None,
+                         copy_stream=None):
+    """echo_prefill_block with the library's fixed device scratch instead of a workspace."""
+    st = _stream(stream)
+    cst = _stream(copy_stream) if copy_stream is not None else st
+    _check("echo_prefill_block_static", load().echo_prefill_block_static(
+        int(R), int(row0), int(n_keys), _ptr(q), _ptr(w), _ptr(k8), _ptr(ks), int(k), _ptr(theta_hat),
+        float(alpha), _ptr(scores), int(W), _ptr(hist), _ptr(sel_idx), _ptr(kth), _ptr(union_list),
+        _ptr(union_count), _ptr(union_bits), ctypes.byref(cache.struct) if cache is not None else None,
+        _ptr(sel_slot), _ptr(status), _ptr(stats), st, cst))
 
 
 class LayerCache:

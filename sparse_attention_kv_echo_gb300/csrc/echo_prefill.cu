@@ -21,6 +21,8 @@
 //                        block's recall has read its lists),
 // and the recall of the misses on `copy_stream`, so that the next block's
 // scoring on `stream` overlaps it.
+#include <mutex>
+
 #include "echo_common.cuh"
 #include "echo_internal.h"
 
@@ -162,4 +164,68 @@ extern "C" int echo_prefill_block(int R, int64_t row0, int64_t n_keys, const flo
     if (rc) return rc;
     return enqueue_cache_step(1, p.tok_off2, n_keys, union_list, static_cast<int>(W), cache, sel_slot, status, stats,
                               stream, copy_stream);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free prefill block.
+//
+// Some callers cannot hand this library a workspace: a serving runtime whose
+// device memory is carved up once at start-up and forbids new allocations
+// afterwards, an embedder that has no allocator of its own to call, or a
+// latency-critical thread where cudaMalloc's implicit device synchronisation
+// is not acceptable.  For them, echo_prefill_block_static runs the same
+// prefill block as echo_prefill_block, with its workspace in the fixed device
+// array below instead of caller memory.  The array is part of the library
+// image: every GPU that loads the library holds ECHO_PREFILL_STATIC_SCRATCH_BYTES
+// of device memory for it until the process exits.
+// ---------------------------------------------------------------------------
+namespace echo {
+namespace {
+
+static __device__ __align__(256) uint8_t g_prefill_scratch[ECHO_PREFILL_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (with that device current) and remembered.
+int static_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ECHO_ECUDA;
+    if (dev < 0 || dev >= kMaxDevices) return ECHO_EUNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_prefill_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return ECHO_ECUDA;
+        }
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return ECHO_OK;
+}
+
+}  // namespace
+}  // namespace echo
+
+extern "C" int echo_prefill_block_static(int R, int64_t row0, int64_t n_keys, const float* q, const float* w,
+                                         const uint8_t* k8, const float* ks, int k, float* theta_hat, float alpha,
+                                         float* scores, int64_t W, uint32_t* hist, int32_t* sel_idx, float* kth,
+                                         int32_t* union_list, int32_t* union_count, uint32_t* union_bits,
+                                         const echo_cache* cache, int32_t* sel_slot, int32_t* status,
+                                         uint32_t* stats, echo_stream_t stream, echo_stream_t copy_stream) {
+    using namespace echo;
+    if (R <= 0 || W <= 0) return ECHO_EINVAL;
+    if (prefill_ws_bytes(R, W) > static_cast<size_t>(ECHO_PREFILL_STATIC_SCRATCH_BYTES)) return ECHO_ETOOLARGE;
+    void* scratch = nullptr;
+    const int rc = static_scratch(&scratch);
+    if (rc) return rc;
+    // Everything the block needs zeroed (the union marks) it clears itself on
+    // the stream; the rest of the scratch is written before it is read.
+    return echo_prefill_block(R, row0, n_keys, q, w, k8, ks, k, theta_hat, alpha, scores, W, hist, sel_idx, kth,
+                              union_list, union_count, union_bits, cache, sel_slot, scratch,
+                              static_cast<size_t>(ECHO_PREFILL_STATIC_SCRATCH_BYTES), status, stats, stream,
+                              copy_stream);
 }
