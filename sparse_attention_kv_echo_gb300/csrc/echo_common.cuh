@@ -123,6 +123,28 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+// 4-byte asynchronous copy global -> shared; src_bytes 0 writes zeros without reading.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+// The barrier's current phase also waits for this thread's cp.async copies
+// (no change to its expected arrival count).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// Wait until the grid this one depends on has completed and its writes are
+// visible (a no-op for a normal launch).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next grid of the stream start its prologue now.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),

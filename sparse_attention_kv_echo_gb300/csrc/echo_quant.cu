@@ -35,6 +35,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) quantize_kernel(int B, co
                                                                        float* __restrict__ wfold,
                                                                        uint32_t* __restrict__ hist,
                                                                        int32_t* status) {
+    pdl_launch_dependents();  // the score kernel may start its prologue and key loads
     const int lane = threadIdx.x & 31;
     const int gw = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);  // (request, head) row
     if (gw >= B * ECHO_HEADS) return;

@@ -58,6 +58,7 @@ struct ScoreArgs {
 };
 
 struct __align__(16) ScoreCtl {
+    float ks[kStages][kTileM];  // per-token key scales of each stage's tile
     uint64_t full[kStages];
     uint64_t empty[kStages];
     uint64_t qfull[2];
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_addr(&ctl->full[s]), 1);
-            mbar_init(smem_addr(&ctl->empty[s]), 1);
+            mbar_init(smem_addr(&ctl->empty[s]), 1 + 4);  // MMA done + the tile's 4 epilogue warps read ks
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_addr(&ctl->qfull[i]), 1);
@@ -181,48 +182,97 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0 && ntiles > 0) {
+        // Lane 0 issues the TMA copies; all 32 lanes copy the tile's 128 key
+        // scales with cp.async, tracked by the same stage barrier.  The first
+        // stages' key loads go out before waiting for the quantiser (their
+        // inputs do not depend on it); q8 loads come after that wait.
+        if (ntiles > 0) {
             const uint64_t pol = policy_evict_first();
-            int b = find_request(tstart, B, t_begin), cur_b = -1;
-            uint32_t qn = 0, it = 0;
-            int64_t row_base = 0;
+            const uint32_t prefill = ntiles < static_cast<uint32_t>(kStages) ? ntiles : kStages;
+            int kb = find_request(tstart, B, t_begin);   // request of the next key load
+            int64_t key_lo = 0, klen = 0;
+            int kcur = -1;
+            uint32_t issued = 0, qn = 0;
             bool ok = true;
-            for (; it < ntiles; ++it) {
+            auto issue_keys = [&](uint32_t it) -> bool {
+                const uint32_t t = t_begin + it;
+                while (t >= static_cast<uint32_t>(tstart[kb + 1])) ++kb;
+                if (kb != kcur) {
+                    bool bad = false;
+                    const Seg sg = segment(a, kb, &bad);
+                    key_lo = sg.key_lo;
+                    klen = sg.len;
+                    kcur = kb;
+                }
+                const uint32_t s = it % kStages;
+                bool got = true;
+                if (lane == 0) got = mbar_wait(smem_addr(&ctl->empty[s]), ((it / kStages) & 1) ^ 1, abort);
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (!got) return false;
+                const int64_t tok0 = static_cast<int64_t>(t - tstart[kb]) * kTileM;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int r = 4 * lane + j;
+                    const bool in = tok0 + r < klen;
+                    cp_async_4(smem_addr(&ctl->ks[s][r]), in ? a.ks + key_lo + tok0 + r : a.ks, in ? 4u : 0u);
+                }
+                cp_async_mbar_arrive(smem_addr(&ctl->full[s]));
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(smem_addr(&ctl->full[s]), kKeyBytes);
+                    tma_load_2d_hint(smem_addr(keys + s * kKeyBytes), &kmap, smem_addr(&ctl->full[s]), 0,
+                                     static_cast<int32_t>(key_lo + tok0), pol);
+                }
+                return true;
+            };
+            for (; issued < prefill; ++issued)
+                if (!issue_keys(issued)) {
+                    ok = false;
+                    break;
+                }
+            pdl_wait();  // q8 comes from the quantiser
+            int cur_b = -1, b = find_request(tstart, B, t_begin);
+            for (uint32_t it = 0; it < ntiles && ok; ++it) {
                 const uint32_t t = t_begin + it;
                 while (t >= static_cast<uint32_t>(tstart[b + 1])) ++b;
                 if (b != cur_b) {
                     const uint32_t qi = qn & 1;
-                    if (!mbar_wait(smem_addr(&ctl->qempty[qi]), ((qn >> 1) & 1) ^ 1, abort)) {
+                    bool got = true;
+                    if (lane == 0) {
+                        got = mbar_wait(smem_addr(&ctl->qempty[qi]), ((qn >> 1) & 1) ^ 1, abort);
+                        if (got) {
+                            mbar_arrive_expect_tx(smem_addr(&ctl->qfull[qi]), kQBytes);
+                            tma_load_2d(smem_addr(qbuf + qi * kQBytes), &qmap, smem_addr(&ctl->qfull[qi]), 0,
+                                        b * ECHO_HEADS);
+                        }
+                    }
+                    got = __shfl_sync(0xffffffffu, got, 0);
+                    if (!got) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(smem_addr(&ctl->qfull[qi]), kQBytes);
-                    tma_load_2d(smem_addr(qbuf + qi * kQBytes), &qmap, smem_addr(&ctl->qfull[qi]), 0,
-                                b * ECHO_HEADS);
                     cur_b = b;
                     ++qn;
-                    bool bad = false;
-                    row_base = segment(a, b, &bad).key_lo;
                 }
-                const uint32_t s = it % kStages;
-                if (!mbar_wait(smem_addr(&ctl->empty[s]), ((it / kStages) & 1) ^ 1, abort)) {
-                    ok = false;
-                    break;
+                if (it >= issued) {
+                    if (!issue_keys(it)) {
+                        ok = false;
+                        break;
+                    }
+                    ++issued;
                 }
-                mbar_arrive_expect_tx(smem_addr(&ctl->full[s]), kKeyBytes);
-                const int64_t row0 = row_base + static_cast<int64_t>(t - tstart[b]) * kTileM;
-                tma_load_2d_hint(smem_addr(keys + s * kKeyBytes), &kmap, smem_addr(&ctl->full[s]), 0,
-                                 static_cast<int32_t>(row0), pol);
             }
-            if (!ok) {
+            if (!ok && lane == 0) {
                 set_status(a.status, ECHO_ST_TIMEOUT);
                 *abort = 1;
             }
-            // Let every copy this thread started land before the CTA exits.
-            for (uint32_t j = (it > kStages ? it - kStages : 0); j < it; ++j)
-                mbar_wait(smem_addr(&ctl->full[j % kStages]), (j / kStages) & 1, nullptr);
-            for (uint32_t j = (qn > 2 ? qn - 2 : 0); j < qn; ++j)
-                mbar_wait(smem_addr(&ctl->qfull[j & 1]), (j >> 1) & 1, nullptr);
+            // Let every copy this warp started land before the CTA exits.
+            if (lane == 0) {
+                for (uint32_t j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
+                    mbar_wait(smem_addr(&ctl->full[j % kStages]), (j / kStages) & 1, nullptr);
+                for (uint32_t j = (qn > 2 ? qn - 2 : 0); j < qn; ++j)
+                    mbar_wait(smem_addr(&ctl->qfull[j & 1]), (j >> 1) & 1, nullptr);
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -276,6 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
+        pdl_wait();                            // wfold and the cleared histogram come from the quantiser
         const int ew = warp - 2;               // 0..7
         const int group = ew >> 2;             // tiles with local index = group (mod 2)
         const int quarter = warp & 3;          // TMEM lanes this warp may access
@@ -286,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float wv[ECHO_HEADS];
         float shift = 0.f, theta = 0.f;
         bool theta_ok = false;
-        int64_t base = 0, nb = 0, obase = 0;
+        int64_t nb = 0, obase = 0;
         bool ok = true;
         for (uint32_t it = group; it < ntiles; it += 2) {
             const uint32_t t = t_begin + it;
@@ -316,24 +367,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const float th =
                     a.theta_hat ? a.theta_hat[static_cast<int64_t>(b) * a.theta_stride] : __int_as_float(0x7f800000);
+
                 theta_ok = isfinite(th);
                 theta = th;
                 shift = theta_ok ? th : 0.f;
                 bool bad = false;
                 const Seg sg = segment(a, b, &bad);
-                base = sg.key_lo;
                 nb = sg.len;
                 obase = sg.out;
             }
             const int64_t tok = static_cast<int64_t>(t - tstart[b]) * kTileM + row;
             const bool valid = tok < nb;
-            const float ksv = valid ? __ldg(a.ks + base + tok) : 0.f;
             const uint32_t acc = it % kAccBufs;
             if (!mbar_wait(smem_addr(&ctl->accfull[acc]), (it / kAccBufs) & 1, abort)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            // the MMA has consumed the stage's keys; read its scales and release it
+            // (waiting on the stage's own barrier orders the cp.async writes before the read)
+            if (!mbar_wait(smem_addr(&ctl->full[it % kStages]), (it / kStages) & 1, abort)) {
+                ok = false;
+                break;
+            }
+            const float ksv = ctl->ks[it % kStages][row];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&ctl->empty[it % kStages]));
             uint32_t r0[16], r1[16], r2[16], r3[16];
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * ECHO_HEADS;
             tmem_ld_x16(taddr + 0, r0);
@@ -407,8 +466,19 @@ static int launch_scores(const ScoreArgs& args, const uint8_t* q8, const uint8_t
     const size_t smem = smem_bytes(args.B);
     ECHO_CUDA_OK(cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(smem)));
-    score_kernel<<<grid, kThreads, smem, stream>>>(kmap, qmap, args);
-    ECHO_CUDA_OK(cudaGetLastError());
+    // Programmatic dependent launch: the prologue and first key loads overlap
+    // the quantiser; the kernel waits for it before touching q8, wfold, hist.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, score_kernel, kmap, qmap, args));
     return ECHO_OK;
 }
 
