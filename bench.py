@@ -311,7 +311,7 @@ def run_ours(args):
             L.quantize_q(lay.q_in, lay.w_in, lay.q8, lay.qscale, lay.wfold, lay.status, hist=lay.hist, stream=main)
             ev[1].record(main)
             L.index_scores(lay.tok_off, lay.n_tokens, lay.q8, lay.wfold, lay.k8, lay.ks, lay.scores, lay.theta,
-                           lay.hist, lay.status, above=lay.above, stream=main)
+                           lay.hist, lay.status, above=lay.above, tok2slot=lay.cache.tok2slot, stream=main)
             ev[2].record(main)
             L.early_fetch(lay.tok_off, lay.n_tokens, lay.above, -1, lay.cache, lay.status,
                           stream=main, copy_stream=main)

@@ -150,20 +150,24 @@ int echo_quantize_q(int B, const float* q, const float* w, uint8_t* q8, float* q
  *   clears it); orderkey maps a float to a uint32 in the same order (-0
  *   counted as +0).  theta_hat [B] f32 may be NULL (no shift).
  *   above (may be NULL): [echo_above_words(B, n_tokens)] u32, the tokens with
- *   score > theta_hat[b] (none when theta_hat[b] is not finite) for
- *   echo_early_fetch.  Request b's words start at 4 * (sum over b' < b of
- *   ceil(N_b'/128)); bit j of its word w is its token 32*w + j.
+ *   score > theta_hat[b] (none when theta_hat[b] is not finite) that are not
+ *   resident in the cache whose tok2slot [n_tokens] is given (tok2slot NULL:
+ *   residency not considered), for echo_early_fetch.  Request b's words start
+ *   at 4 * (sum over b' < b of ceil(N_b'/128)); bit j of its word w is its
+ *   token 32*w + j.
  */
 size_t echo_above_words(int B, int64_t n_tokens);
 int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens, const uint8_t* q8,
                       const float* wfold, const uint8_t* k8, const float* ks, float* scores,
-                      const float* theta_hat, uint32_t* hist, uint32_t* above, int32_t* status,
-                      echo_stream_t stream);
+                      const float* theta_hat, uint32_t* hist, uint32_t* above,
+                      const int32_t* tok2slot, int32_t* status, echo_stream_t stream);
 
 /*
  * Early fetch [EXPL panel "Decode: fetch above a predicted threshold"]: before
  * top-k is known, the tokens marked in `above` by echo_index_scores (score >
- * the predicted threshold) that are not resident, in ascending order, at most
+ * the predicted threshold, not resident: pass the same cache's tok2slot there;
+ * a marked token that is resident is skipped and flagged ECHO_ST_BADDATA),
+ * in ascending order, at most
  * min(early_cap, free slots) of them (early_cap < 0: no cap but the free
  * slots), take the lowest free slots in ascending order and become resident.
  * The lists go to cache->early_tok / early_slot / early_cnt and the rows are

@@ -69,7 +69,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         L.echo_above_words.restype = ctypes.c_size_t
         L.echo_above_words.argtypes = [i32, i64]
         L.echo_index_scores.restype = i32
-        L.echo_index_scores.argtypes = [i32, _vp, i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+        L.echo_index_scores.argtypes = [i32, _vp, i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
         L.echo_early_fetch.restype = i32
         L.echo_early_fetch.argtypes = [i32, _vp, i64, _vp, i32, ctypes.POINTER(EchoCacheStruct), _vp,
                                        _vp, _vp, _vp]
@@ -140,11 +140,11 @@ def above_words(B: int, n_tokens: int) -> int:
 
 
 def index_scores(tok_off, n_tokens, q8, wfold, k8, ks, scores, theta_hat, hist, status, above=None,
-                 stream=None):
+                 tok2slot=None, stream=None):
     B = q8.shape[0]
     _check("echo_index_scores", load().echo_index_scores(
         B, _ptr(tok_off), int(n_tokens), _ptr(q8), _ptr(wfold), _ptr(k8), _ptr(ks), _ptr(scores),
-        _ptr(theta_hat), _ptr(hist), _ptr(above), _ptr(status), _stream(stream)))
+        _ptr(theta_hat), _ptr(hist), _ptr(above), _ptr(tok2slot), _ptr(status), _stream(stream)))
 
 
 def early_fetch(tok_off, n_tokens, above, early_cap, cache, status, stats=None, stream=None, copy_stream=None):

@@ -80,7 +80,7 @@ __device__ uint32_t assign_lowest_free(uint32_t* fb, int words, uint32_t M, cons
                 x &= x - 1;
                 const int slot = w * 32 + bit;
                 const int32_t tok = tok_list[rank];
-                if (tok >= 0 && tok < n && slot < C) {
+                if (tok >= 0 && tok < n && slot < C && t2s[tok] < 0) {
                     t2s[tok] = slot;
                     s2t[slot] = tok;
                     slot_list[rank] = slot;
@@ -140,21 +140,17 @@ __global__ void __launch_bounds__(kCT) early_select_kernel(const int64_t* __rest
     }
     const uint32_t limit = (cap < 0) ? F : min(F, static_cast<uint32_t>(cap));
     uint32_t found = 0;
-    // word w covers tokens 32*w .. 32*w+31 of the request: ascending word, ascending bit
+    // word w covers tokens 32*w .. 32*w+31 of the request: ascending word, ascending bit;
+    // the marked tokens are the non-resident ones above the threshold
     for (int w0 = 0; w0 < awords && found < limit; w0 += kCT) {
         const int w = w0 + tid;
-        uint32_t cand = (w < awords) ? ab[w] : 0u, nonres = 0;
+        uint32_t cand = (w < awords) ? ab[w] : 0u;
+        if (w == awords - 1 && (n & 31)) cand &= (1u << (n & 31)) - 1u;   // no token past the request end
+        uint32_t tot;
+        uint32_t rank = found + block_exclusive_scan<kCT>(__popc(cand), scan, &tot);
         while (cand) {
             const int bit = __ffs(cand) - 1;
             cand &= cand - 1;
-            const int64_t s = 32 * static_cast<int64_t>(w) + bit;
-            if (s < n && t2s[s] < 0) nonres |= 1u << bit;
-        }
-        uint32_t tot;
-        uint32_t rank = found + block_exclusive_scan<kCT>(__popc(nonres), scan, &tot);
-        while (nonres) {
-            const int bit = __ffs(nonres) - 1;
-            nonres &= nonres - 1;
             if (rank < limit) etok[rank] = 32 * w + bit;
             ++rank;
         }
@@ -283,24 +279,44 @@ __global__ void __launch_bounds__(256) recall_kernel(const int64_t* __restrict__
     int count = cnt[b];
     if (count > C) count = C;
     const int chunks = static_cast<int>(row_bytes / 16);
-    for (int i = blockIdx.x * warps + (threadIdx.x >> 5); i < count; i += gridDim.x * warps) {
-        const int32_t tok = tok_list[static_cast<int64_t>(b) * C + i];
-        const int32_t slot = slot_list[static_cast<int64_t>(b) * C + i];
-        if (tok < 0 || tok >= n || slot < 0 || slot >= C) {
-            if (lane == 0) set_status(status, ECHO_ST_BADDATA);
-            continue;
+    constexpr int kRows = 2;  // rows per warp in flight
+    for (int i0 = (blockIdx.x * warps + (threadIdx.x >> 5)) * kRows; i0 < count;
+         i0 += gridDim.x * warps * kRows) {
+        const int4* src[kRows];
+        int4* dst[kRows];
+        bool ok[kRows];
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            const int i = i0 + r;
+            ok[r] = false;
+            if (i < count) {
+                const int32_t tok = tok_list[static_cast<int64_t>(b) * C + i];
+                const int32_t slot = slot_list[static_cast<int64_t>(b) * C + i];
+                if (tok >= 0 && tok < n && slot >= 0 && slot < C) {
+                    ok[r] = true;
+                    src[r] = reinterpret_cast<const int4*>(host + (base + tok) * row_bytes);
+                    dst[r] = reinterpret_cast<int4*>(dev + (static_cast<int64_t>(b) * C + slot) * row_bytes);
+                } else if (lane == 0) {
+                    set_status(status, ECHO_ST_BADDATA);
+                }
+            }
         }
-        const int4* src = reinterpret_cast<const int4*>(host + (base + tok) * row_bytes);
-        int4* dst = reinterpret_cast<int4*>(dev + (static_cast<int64_t>(b) * C + slot) * row_bytes);
         for (int c0 = 0; c0 < chunks; c0 += 96) {
-            int4 v0 = make_int4(0, 0, 0, 0), v1 = v0, v2 = v0;
-            const int a0 = c0 + lane, a1 = a0 + 32, a2 = a0 + 64;
-            if (a0 < chunks) v0 = __ldcs(src + a0);
-            if (a1 < chunks) v1 = __ldcs(src + a1);
-            if (a2 < chunks) v2 = __ldcs(src + a2);
-            if (a0 < chunks) dst[a0] = v0;
-            if (a1 < chunks) dst[a1] = v1;
-            if (a2 < chunks) dst[a2] = v2;
+            int4 v[kRows][3];
+#pragma unroll
+            for (int r = 0; r < kRows; ++r)
+#pragma unroll
+                for (int j = 0; j < 3; ++j) {
+                    const int c = c0 + lane + 32 * j;
+                    v[r][j] = (ok[r] && c < chunks) ? __ldcs(src[r] + c) : make_int4(0, 0, 0, 0);
+                }
+#pragma unroll
+            for (int r = 0; r < kRows; ++r)
+#pragma unroll
+                for (int j = 0; j < 3; ++j) {
+                    const int c = c0 + lane + 32 * j;
+                    if (ok[r] && c < chunks) dst[r][c] = v[r][j];
+                }
         }
     }
 }
@@ -318,8 +334,10 @@ cudaError_t launch_recall(int B, const int64_t* tok_off, int64_t n_tokens, int C
                           int64_t row_bytes, int32_t* status, cudaStream_t s) {
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    int gx = (4 * sms + B - 1) / B;
-    const int rows_per_block = 8;
+    // About one block per SM in all: the host link, not the SMs, bounds the copy,
+    // and a small footprint lets the step's other kernels run alongside.
+    int gx = (sms + B - 1) / B;
+    const int rows_per_block = 16;
     const int gx_max = (C + rows_per_block - 1) / rows_per_block;
     if (gx > gx_max) gx = gx_max;
     if (gx < 1) gx = 1;

@@ -54,11 +54,13 @@ struct ScoreArgs {
     const float* theta_hat;
     uint32_t* hist;
     uint32_t* above;
+    const int32_t* tok2slot;   // with above: mark only tokens that are not resident (NULL: all)
     int32_t* status;
 };
 
 struct __align__(16) ScoreCtl {
     float ks[kStages][kTileM];  // per-token key scales of each stage's tile
+    int32_t res[kStages][kTileM];  // per-token cache slot (>= 0: resident) when above is filtered
     uint64_t full[kStages];
     uint64_t empty[kStages];
     uint64_t qfull[2];
@@ -215,6 +217,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int r = 4 * lane + j;
                     const bool in = tok0 + r < klen;
                     cp_async_4(smem_addr(&ctl->ks[s][r]), in ? a.ks + key_lo + tok0 + r : a.ks, in ? 4u : 0u);
+                    if (a.tok2slot)
+                        cp_async_4(smem_addr(&ctl->res[s][r]), in ? a.tok2slot + key_lo + tok0 + r : a.tok2slot,
+                                   in ? 4u : 0u);
                 }
                 cp_async_mbar_arrive(smem_addr(&ctl->full[s]));
                 __syncwarp();
@@ -391,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             const float ksv = ctl->ks[it % kStages][row];
+            const bool resident = a.tok2slot && ctl->res[it % kStages][row] >= 0;
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&ctl->empty[it % kStages]));
             uint32_t r0[16], r1[16], r2[16], r3[16];
@@ -417,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const unsigned vm = __ballot_sync(0xffffffffu, valid);
             if (a.above) {
                 // tokens above the predicted threshold: one word per 32 rows of the tile
-                const unsigned am = __ballot_sync(0xffffffffu, valid && theta_ok && score > theta);
+                const unsigned am = __ballot_sync(0xffffffffu, valid && theta_ok && score > theta && !resident);
                 if (lane == 0) a.above[4 * static_cast<size_t>(t) + quarter] = am;
             }
             if (valid) {
@@ -486,8 +492,8 @@ static int launch_scores(const ScoreArgs& args, const uint8_t* q8, const uint8_t
 
 extern "C" int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens, const uint8_t* q8,
                                  const float* wfold, const uint8_t* k8, const float* ks, float* scores,
-                                 const float* theta_hat, uint32_t* hist, uint32_t* above, int32_t* status,
-                                 echo_stream_t stream) {
+                                 const float* theta_hat, uint32_t* hist, uint32_t* above, const int32_t* tok2slot,
+                                 int32_t* status, echo_stream_t stream) {
     using namespace echo;
     if (B <= 0 || n_tokens < 0) return ECHO_EINVAL;
     if (B > ECHO_MAX_REQUESTS) return ECHO_EUNSUPPORTED;
@@ -496,7 +502,8 @@ extern "C" int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens
     if (n_tokens >= (1ll << 31)) return ECHO_EUNSUPPORTED;
     if (!is_aligned(q8, 16) || !is_aligned(wfold, 16) || !is_aligned(k8, 16)) return ECHO_EINVAL;
     if (n_tokens == 0) return ECHO_OK;
-    ScoreArgs args{B, tok_off, n_tokens, 0, 0, 1, wfold, ks, scores, theta_hat, hist, above, status};
+    ScoreArgs args{B, tok_off, n_tokens, 0, 0, 1, wfold, ks, scores, theta_hat, hist, above,
+                   above ? tok2slot : nullptr, status};
     return launch_scores(args, q8, k8, n_tokens, n_tokens / kTileM + B, stream);
 }
 
@@ -510,7 +517,7 @@ extern "C" int echo_prefill_scores(int R, int64_t row0, int64_t n_keys, const ui
     if (row0 + R > n_keys || W < row0 + R) return ECHO_EINVAL;
     if (n_keys >= (1ll << 31) || static_cast<int64_t>(R) * W >= (1ll << 40)) return ECHO_EUNSUPPORTED;
     if (!is_aligned(q8, 16) || !is_aligned(wfold, 16) || !is_aligned(k8, 16)) return ECHO_EINVAL;
-    ScoreArgs args{R, nullptr, n_keys, row0, W, 0, wfold, ks, scores, theta_hat, hist, nullptr, status};
+    ScoreArgs args{R, nullptr, n_keys, row0, W, 0, wfold, ks, scores, theta_hat, hist, nullptr, nullptr, status};
     const int64_t tiles_ub = static_cast<int64_t>(R) * ((row0 + R + kTileM - 1) / kTileM);
     return launch_scores(args, q8, k8, n_keys, tiles_ub, stream);
 }

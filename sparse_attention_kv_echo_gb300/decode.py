@@ -69,7 +69,7 @@ class DecodeLayer:
         L.quantize_q(q, w, self.q8, self.qscale, self.wfold, self.status, hist=self.hist, stream=main)
         L.index_scores(self.tok_off, self.n_tokens, self.q8, self.wfold, self.k8, self.ks, self.scores,
                        self.theta, self.hist, self.status, above=self.above if self.predictor else None,
-                       stream=main)
+                       tok2slot=self.cache.tok2slot, stream=main)
         if self.predictor:
             self.side.wait_stream(main)
             L.early_fetch(self.tok_off, self.n_tokens, self.above, self.early_cap, self.cache, self.status,

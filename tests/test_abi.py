@@ -51,22 +51,22 @@ def test_host_checks_reject_bad_arguments(L):
     from sparse_attention_kv_echo_gb300 import lib
     v = ctypes.c_void_p
     dummy = v(0x1000)
-    # index_scores(B, tok_off, n_tokens, q8, wfold, k8, ks, scores, theta, hist, above, status, stream)
-    assert L.echo_index_scores(0, dummy, 10, dummy, dummy, dummy, dummy, dummy, None, None, None, dummy,
+    # index_scores(B, tok_off, n_tokens, q8, wfold, k8, ks, scores, theta, hist, above, tok2slot, status, stream)
+    assert L.echo_index_scores(0, dummy, 10, dummy, dummy, dummy, dummy, dummy, None, None, None, None, dummy,
                                None) == lib.ECHO_EINVAL
     assert L.echo_index_scores(lib.MAX_REQUESTS + 1, dummy, 10, dummy, dummy, dummy, dummy, dummy, None,
-                               None, None, dummy, None) == lib.ECHO_EUNSUPPORTED
+                               None, None, None, dummy, None) == lib.ECHO_EUNSUPPORTED
     # missing q8
-    assert L.echo_index_scores(1, dummy, 10, None, dummy, dummy, dummy, dummy, None, None, None, dummy,
+    assert L.echo_index_scores(1, dummy, 10, None, dummy, dummy, dummy, dummy, None, None, None, None, dummy,
                                None) == lib.ECHO_EINVAL
     # misaligned keys (must be 16-byte aligned)
-    assert L.echo_index_scores(1, dummy, 10, dummy, dummy, v(0x1001), dummy, dummy, None, None, None, dummy,
+    assert L.echo_index_scores(1, dummy, 10, dummy, dummy, v(0x1001), dummy, dummy, None, None, None, None, dummy,
                                None) == lib.ECHO_EINVAL
     # negative token count
-    assert L.echo_index_scores(1, dummy, -5, dummy, dummy, dummy, dummy, dummy, None, None, None, dummy,
+    assert L.echo_index_scores(1, dummy, -5, dummy, dummy, dummy, dummy, dummy, None, None, None, None, dummy,
                                None) == lib.ECHO_EINVAL
     # no tokens: nothing to do, nothing enqueued
-    assert L.echo_index_scores(1, dummy, 0, dummy, dummy, None, None, None, None, None, None, dummy,
+    assert L.echo_index_scores(1, dummy, 0, dummy, dummy, None, None, None, None, None, None, None, dummy,
                                None) == lib.ECHO_OK
     # early fetch needs the above-threshold words and a cache
     assert L.echo_early_fetch(1, dummy, 10, None, -1, None, dummy, None, None, None) == lib.ECHO_EINVAL
