@@ -99,7 +99,8 @@ typedef struct CUstream_st* echo_stream_t; /* a cudaStream_t; NULL = legacy defa
  *   host_kv   device-accessible address of the pinned host KV pool [n_tokens, row_bytes]
  *             (cudaHostAlloc'd or registered; the address the device uses for it)
  *   dev_kv    [B*C, row_bytes] device cache rows; request b owns rows [b*C, (b+1)*C)
- * C is a multiple of 32; row_bytes a multiple of 16 (1152 for 576 bf16 values).
+ * C is a multiple of 32 and at most 524288 (2^19; ECHO_EUNSUPPORTED above);
+ * row_bytes a multiple of 16 (1152 for 576 bf16 values).
  * Recall copies run on a copy stream and read only the (token, slot) lists,
  * never the tables, so the next table update may overlap them; a consumer of
  * dev_kv must wait for the copy stream.

@@ -29,7 +29,7 @@ namespace echo {
 namespace {
 
 constexpr int kCT = 1024;
-constexpr int kMaxSlotsSmem = 1 << 20;   // slot bitmap of up to 2^20 slots (128 KB)
+constexpr int kMaxSlotsSmem = 1 << 19;   // per-slot-word tables in shared memory: 3 x 2^14 words (192 KB)
 
 struct CacheArgs {
     int32_t* tok2slot;
@@ -63,39 +63,65 @@ __device__ __forceinline__ bool request_range(const int64_t* tok_off, int64_t n_
 }
 
 // Give the first M tokens of tok_list the M lowest free slots of one
-// request, in ascending order.  Block-wide; returns the number assigned.
+// request, in ascending order.  Block-wide and parallel over ranks: a prefix
+// of the free-slot counts of the bit words (wpre, shared memory) maps rank r to
+// its word by binary search and to its bit as the (r - wpre[w])-th set bit.
+// wpre: words + 1 entries, fbs: words entries of shared memory.  Returns the
+// number assigned.
 __device__ uint32_t assign_lowest_free(uint32_t* fb, int words, uint32_t M, const int32_t* tok_list,
                                        int32_t* slot_list, int32_t* t2s, int32_t* s2t, int64_t n, int C,
-                                       uint32_t* scan, int32_t* status) {
-    uint32_t done = 0;
-    for (int w0 = 0; w0 < words && done < M; w0 += kCT) {
+                                       uint32_t* scan, uint32_t* wpre, uint32_t* fbs, int32_t* status) {
+    uint32_t run = 0;
+    for (int w0 = 0; w0 < words; w0 += kCT) {
         const int w = w0 + threadIdx.x;
         const uint32_t f = (w < words) ? fb[w] : 0u;
+        if (w < words) fbs[w] = f;
         uint32_t tot;
-        uint32_t rank = done + block_exclusive_scan<kCT>(__popc(f), scan, &tot);
-        if (f && rank < M) {
-            uint32_t x = f, taken = 0;
-            while (x && rank < M) {
-                const int bit = __ffs(x) - 1;
-                x &= x - 1;
-                const int slot = w * 32 + bit;
-                const int32_t tok = tok_list[rank];
-                if (tok >= 0 && tok < n && slot < C && t2s[tok] < 0) {
-                    t2s[tok] = slot;
-                    s2t[slot] = tok;
-                    slot_list[rank] = slot;
-                    taken |= 1u << bit;
-                } else {
-                    set_status(status, ECHO_ST_BADDATA);
-                }
-                ++rank;
-            }
-            fb[w] = f & ~taken;
-        }
-        done += tot;
+        const uint32_t ex = block_exclusive_scan<kCT>(__popc(f), scan, &tot);
+        if (w < words) wpre[w] = run + ex;
+        run += tot;
     }
-    if (done < M && threadIdx.x == 0) set_status(status, ECHO_ST_NOSLOT);
-    return done < M ? done : M;
+    if (threadIdx.x == 0) wpre[words] = run;
+    __syncthreads();
+    const uint32_t take = M < run ? M : run;
+    for (uint32_t r = threadIdx.x; r < take; r += kCT) {
+        int lo = 0, hi = words - 1;   // largest w with wpre[w] <= r
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (wpre[mid] <= r)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        uint32_t f = fbs[lo];
+        for (uint32_t i = r - wpre[lo]; i > 0; --i) f &= f - 1;
+        const int slot = lo * 32 + (__ffs(f) - 1);
+        const int32_t tok = tok_list[r];
+        if (tok >= 0 && tok < n && slot < C && t2s[tok] < 0) {
+            t2s[tok] = slot;
+            s2t[slot] = tok;
+            slot_list[r] = slot;
+        } else {
+            set_status(status, ECHO_ST_BADDATA);
+        }
+    }
+    // the taken slots are the lowest `take` free ones: clear them word by word
+    for (int w = threadIdx.x; w < words; w += kCT) {
+        if (wpre[w] >= take) continue;
+        uint32_t f = fbs[w];
+        uint32_t k = take - wpre[w];
+        uint32_t taken = 0;
+        while (f && k) {
+            const uint32_t low = f & (0u - f);
+            taken |= low;
+            f ^= low;
+            --k;
+        }
+        if (taken) fb[w] = fbs[w] & ~taken;
+    }
+    if (take < M && threadIdx.x == 0) set_status(status, ECHO_ST_NOSLOT);
+    __syncthreads();
+    return take;
 }
 
 // Tiles of 128 tokens of request b, and the first tile of b in the list of all
@@ -115,10 +141,13 @@ __global__ void __launch_bounds__(kCT) early_select_kernel(const int64_t* __rest
                                                            const uint32_t* __restrict__ above, int cap, CacheArgs c,
                                                            int32_t* status, uint32_t* stats) {
     __shared__ uint32_t scan[40];
+    extern __shared__ uint32_t dyn[];   // wpre [words + 1], fbs [words]
     const int b = blockIdx.x, tid = threadIdx.x;
     int64_t base, n;
     if (!request_range(tok_off, n_tokens, b, &base, &n) && tid == 0) set_status(status, ECHO_ST_BADDATA);
     const int C = c.C, words = C / 32;
+    uint32_t* wpre = dyn;
+    uint32_t* fbs = dyn + words + 1;
     int32_t* t2s = c.tok2slot + base;
     int32_t* s2t = c.slot2tok + static_cast<int64_t>(b) * C;
     uint32_t* fb = c.freebits + static_cast<int64_t>(b) * words;
@@ -158,7 +187,7 @@ __global__ void __launch_bounds__(kCT) early_select_kernel(const int64_t* __rest
     }
     const uint32_t E = min(found, limit);
     __syncthreads();
-    const uint32_t got = assign_lowest_free(fb, words, E, etok, eslot, t2s, s2t, n, C, scan, status);
+    const uint32_t got = assign_lowest_free(fb, words, E, etok, eslot, t2s, s2t, n, C, scan, wpre, fbs, status);
     if (tid == 0) {
         c.early_cnt[b] = static_cast<int32_t>(got);
         if (stats && got) atomicAdd(stats + ECHO_STAT_EARLY, got);
@@ -169,7 +198,7 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
                                                          const int32_t* __restrict__ sel, int m, CacheArgs c,
                                                          int32_t* __restrict__ sel_slot, int32_t* status,
                                                          uint32_t* stats) {
-    extern __shared__ uint32_t keep[];  // one bit per slot: a selected token lives there
+    extern __shared__ uint32_t keep[];  // keep [words]: a selected token lives in the slot; then wpre, fbs
     __shared__ uint32_t scan[40];
     __shared__ uint32_t s_flags;
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -182,6 +211,8 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
     const int32_t* sl = sel + static_cast<int64_t>(b) * m;
     int32_t* mtok = c.miss_tok + static_cast<int64_t>(b) * C;
     int32_t* mslot = c.miss_slot + static_cast<int64_t>(b) * C;
+    uint32_t* wpre = keep + words;
+    uint32_t* fbs = wpre + words + 1;
 
     for (int w = tid; w < words; w += kCT) keep[w] = 0u;
     if (tid == 0) s_flags = 0;
@@ -250,7 +281,7 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
     }
     __syncthreads();
     // 3. the misses take the lowest free slots
-    const uint32_t got = assign_lowest_free(fb, words, M, mtok, mslot, t2s, s2t, n, C, scan, status);
+    const uint32_t got = assign_lowest_free(fb, words, M, mtok, mslot, t2s, s2t, n, C, scan, wpre, fbs, status);
     __syncthreads();
     // 4. slot of every selected entry
     for (int i = tid; i < m; i += kCT) {
@@ -325,7 +356,11 @@ __global__ void __launch_bounds__(256) recall_kernel(const int64_t* __restrict__
 
 cudaError_t launch_early_select(int B, const int64_t* tok_off, int64_t n_tokens, const uint32_t* above, int cap,
                                 const echo_cache& c, int32_t* status, uint32_t* stats, cudaStream_t s) {
-    early_select_kernel<<<B, kCT, 0, s>>>(tok_off, n_tokens, above, cap, cache_args(c), status, stats);
+    const size_t smem = (2 * static_cast<size_t>(c.C / 32) + 1) * sizeof(uint32_t);
+    cudaError_t e = cudaFuncSetAttribute(early_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    early_select_kernel<<<B, kCT, smem, s>>>(tok_off, n_tokens, above, cap, cache_args(c), status, stats);
     return cudaGetLastError();
 }
 
@@ -354,7 +389,7 @@ namespace echo {
 int enqueue_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
                        const echo_cache* cache, int32_t* sel_slot, int32_t* status, uint32_t* stats,
                        cudaStream_t stream, cudaStream_t copy_stream) {
-    const size_t smem = static_cast<size_t>(cache->C / 32) * sizeof(uint32_t);
+    const size_t smem = (3 * static_cast<size_t>(cache->C / 32) + 1) * sizeof(uint32_t);
     ECHO_CUDA_OK(cudaFuncSetAttribute(cache_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(smem)));
     cache_step_kernel<<<B, kCT, smem, stream>>>(tok_off, n_tokens, sel, m, cache_args(*cache), sel_slot, status,
@@ -401,6 +436,7 @@ extern "C" int echo_early_fetch(int B, const int64_t* tok_off, int64_t n_tokens,
     if (n_tokens >= (1ll << 31)) return ECHO_EUNSUPPORTED;
     int rc = check_cache(cache, B, 0);
     if (rc) return rc;
+    if (cache->C > kMaxSlotsSmem) return ECHO_EUNSUPPORTED;
     ECHO_CUDA_OK(launch_early_select(B, tok_off, n_tokens, above, early_cap, *cache, status, stats, stream));
     rc = stream_wait(copy_stream, stream);
     if (rc) return rc;
