@@ -39,7 +39,7 @@ if ROOT not in sys.path:
 
 METRIC = "decode steps/s (indexer+top-k+recall per layer) & GB/s vs HBM/PCIe roofline"
 UNIT = "steps/s"
-SCORE_BYTES_PER_TOKEN = 132      # 128 E4M3 key bytes + 4-byte fp32 scale
+SCORE_BYTES_PER_TOKEN = 136      # 128 E4M3 key bytes + 4-byte fp32 scale + 4-byte residency (early fetch)
 FLUSH_BYTES = 256 << 20          # > 129 MB L2
 FALLBACK_HBM_GBS = 6800.0
 
