@@ -4,10 +4,10 @@
  *
  * Per layer and decode step the path computes, for a batch of B requests:
  *   1. the indexer score of every context token (echo_quantize_q,
- *      echo_index_scores),
- *   2. the tokens above the predicted threshold, fetched early
- *      (echo_early_fetch), then the exact top-k tokens and the EMA threshold
- *      prediction (echo_topk_select),
+ *      echo_index_scores), then the rows of the tokens above the predicted
+ *      threshold fetched early (echo_early_fetch) while
+ *   2. the exact top-k tokens and the EMA threshold prediction
+ *      (echo_topk_select),
  *   3. the GPU-cache step: free unselected slots, allocate slots for the
  *      misses, recall the missing KV rows from the host pool (echo_cache_step);
  * and, for chunked prefill, a block of query rows at once (echo_prefill_block).
@@ -96,13 +96,15 @@ typedef struct CUstream_st* echo_stream_t; /* a cudaStream_t; NULL = legacy defa
  *   early_tok [B*C]      int32   this step's early fetches per request (ascending tokens)
  *   early_slot[B*C]      int32   the slot each early fetch was given
  *   early_cnt [B]        int32
+ *   free_snap [B*C/32]   uint32  freebits as echo_index_scores found them (echo_early_fetch
+ *                                reads this copy while echo_cache_step updates freebits)
  *   host_kv   device-accessible address of the pinned host KV pool [n_tokens, row_bytes]
  *             (cudaHostAlloc'd or registered; the address the device uses for it)
  *   dev_kv    [B*C, row_bytes] device cache rows; request b owns rows [b*C, (b+1)*C)
  * C is a multiple of 32 and at most 524288 (2^19; ECHO_EUNSUPPORTED above);
  * row_bytes a multiple of 16 (1152 for 576 bf16 values).
- * Recall copies run on a copy stream and read only the (token, slot) lists,
- * never the tables, so the next table update may overlap them; a consumer of
+ * Row copies read the (token, slot) lists of the late misses or free_snap
+ * (early fetch), never the live tables, so a table update may overlap them; a consumer of
  * dev_kv must wait for the copy stream.
  */
 typedef struct echo_cache {
@@ -115,6 +117,7 @@ typedef struct echo_cache {
     int32_t* early_tok;
     int32_t* early_slot;
     int32_t* early_cnt;
+    uint32_t* free_snap;
     const void* host_kv;
     void* dev_kv;
     int64_t row_bytes;
@@ -152,33 +155,37 @@ int echo_quantize_q(int B, const float* q, const float* w, uint8_t* q8, float* q
  *   counted as +0).  theta_hat [B] f32 may be NULL (no shift).
  *   above (may be NULL): [echo_above_words(B, n_tokens)] u32, the tokens with
  *   score > theta_hat[b] (none when theta_hat[b] is not finite) that are not
- *   resident in the cache whose tok2slot [n_tokens] is given (tok2slot NULL:
- *   residency not considered), for echo_early_fetch.  Request b's words start
- *   at 4 * (sum over b' < b of ceil(N_b'/128)); bit j of its word w is its
- *   token 32*w + j.
+ *   resident in `cache` (NULL: residency not considered), for echo_early_fetch.
+ *   Request b's words start at 4 * (floor(tok_off[b] / 128) + b); bit j of
+ *   its word w is its token 32*w + j; words past its last token hold zeros.
+ *   cache (may be NULL; needs above): the layer's cache; its freebits are
+ *   also copied to free_snap for echo_early_fetch.
  */
 size_t echo_above_words(int B, int64_t n_tokens);
 int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens, const uint8_t* q8,
                       const float* wfold, const uint8_t* k8, const float* ks, float* scores,
                       const float* theta_hat, uint32_t* hist, uint32_t* above,
-                      const int32_t* tok2slot, int32_t* status, echo_stream_t stream);
+                      const echo_cache* cache, int32_t* status, echo_stream_t stream);
 
 /*
- * Early fetch [EXPL panel "Decode: fetch above a predicted threshold"]: before
- * top-k is known, the tokens marked in `above` by echo_index_scores (score >
- * the predicted threshold, not resident: pass the same cache's tok2slot there;
- * a marked token that is resident is skipped and flagged ECHO_ST_BADDATA),
- * in ascending order, at most
- * min(early_cap, free slots) of them (early_cap < 0: no cap but the free
- * slots), take the lowest free slots in ascending order and become resident.
- * The lists go to cache->early_tok / early_slot / early_cnt and the rows are
- * recalled into dev_kv on copy_stream (may equal stream).  It reads neither
- * the scores nor the threshold, so it may run on a side stream while
- * echo_topk_select runs; echo_cache_step must come after it.
+ * Early fetch [EXPL panel "Decode: fetch above a predicted threshold"], the
+ * copy half.  Before top-k is known, the early set of request b is the tokens
+ * marked in `above` by echo_index_scores (score > the predicted threshold,
+ * not resident), in ascending order, at most min(early_cap, free slots) of
+ * them (early_cap < 0: no cap but the free slots); they take the lowest free
+ * slots in ascending order (free as in cache->free_snap).  This call copies
+ * their rows host_kv[tok_off[b] + t] -> dev_kv[b*C + slot] and writes nothing
+ * else: the tables learn the early set in echo_cache_step (given the same
+ * above and early_cap), which may therefore run concurrently with this copy.
+ * Enqueue it on the stream of echo_index_scores right after it: it is
+ * launched as a programmatic dependent of the score kernel.  It reads neither
+ * the scores nor the threshold, so echo_topk_select may run on another stream
+ * meanwhile; the late-miss recall of echo_cache_step must be ordered after it
+ * (its copy_stream = this stream), since a slot fetched early and then freed
+ * may be handed to a miss.
  */
-int echo_early_fetch(int B, const int64_t* tok_off, int64_t n_tokens, const uint32_t* above,
-                     int early_cap, const echo_cache* cache, int32_t* status, uint32_t* stats,
-                     echo_stream_t stream, echo_stream_t copy_stream);
+int echo_early_fetch(int B, const int64_t* tok_off, int64_t n_tokens, const uint32_t* above, int early_cap,
+                     const echo_cache* cache, int32_t* status, echo_stream_t stream);
 
 /*
  * Exact top-k per request [EXPL section 2: "guarantees an exact top-k"] and
@@ -203,19 +210,24 @@ int echo_topk_select(int B, const int64_t* tok_off, int64_t n_tokens, const floa
 
 /*
  * GPU-cache step [EXPL panel "One layer, one step: free -> allocate ->
- * recall"]: with sel [B,m] (ascending request-local tokens, -1 padded):
+ * recall"; panel "Decode: fetch above a predicted threshold"]: with sel [B,m]
+ * (ascending request-local tokens, -1 padded):
+ *   0. with above (may be NULL: no early fetch this step), the early set of
+ *      echo_early_fetch (same above and early_cap) becomes resident in the
+ *      slots that call copied it to; early_tok / early_slot / early_cnt list
+ *      it (early_cnt = 0 without above);
  *   1. every resident token that is not selected is freed (both table
  *      entries -1, its free bit set); its bytes stay, nothing is written back;
  *   2. the selected tokens that are not resident (the misses), in ascending
  *      order, take the lowest free slots in ascending order;
  *   3. sel_slot [B,m] = slot of each selected token (-1 for padding);
  *   4. the miss rows are copied host_kv[tok_off[b] + t] -> dev_kv[b*C + slot],
- *      on copy_stream (which may equal stream; an event orders it after 1-3).
+ *      on copy_stream (which may equal stream; an event orders it after 0-3).
  * Needs m <= C.
  */
 int echo_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
-                    const echo_cache* cache, int32_t* sel_slot, int32_t* status, uint32_t* stats,
-                    echo_stream_t stream, echo_stream_t copy_stream);
+                    const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,
+                    int32_t* status, uint32_t* stats, echo_stream_t stream, echo_stream_t copy_stream);
 
 /*
  * Chunked prefill [EXPL panel "Prefill: one-round histogram"; AE section

@@ -33,7 +33,7 @@ _vp = ctypes.c_void_p
 class EchoCacheStruct(ctypes.Structure):
     _fields_ = [("tok2slot", _vp), ("slot2tok", _vp), ("freebits", _vp), ("miss_tok", _vp),
                 ("miss_slot", _vp), ("miss_cnt", _vp), ("early_tok", _vp), ("early_slot", _vp),
-                ("early_cnt", _vp), ("host_kv", _vp), ("dev_kv", _vp), ("row_bytes", ctypes.c_int64),
+                ("early_cnt", _vp), ("free_snap", _vp), ("host_kv", _vp), ("dev_kv", _vp), ("row_bytes", ctypes.c_int64),
                 ("C", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
@@ -69,14 +69,14 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         L.echo_above_words.restype = ctypes.c_size_t
         L.echo_above_words.argtypes = [i32, i64]
         L.echo_index_scores.restype = i32
-        L.echo_index_scores.argtypes = [i32, _vp, i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+        L.echo_index_scores.argtypes = [i32, _vp, i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                        ctypes.POINTER(EchoCacheStruct), _vp, _vp]
         L.echo_early_fetch.restype = i32
-        L.echo_early_fetch.argtypes = [i32, _vp, i64, _vp, i32, ctypes.POINTER(EchoCacheStruct), _vp,
-                                       _vp, _vp, _vp]
+        L.echo_early_fetch.argtypes = [i32, _vp, i64, _vp, i32, ctypes.POINTER(EchoCacheStruct), _vp, _vp]
         L.echo_topk_select.restype = i32
         L.echo_topk_select.argtypes = [i32, _vp, i64, _vp, i32, _vp, _vp, f32, _vp, _vp, _vp, _vp, _vp]
         L.echo_cache_step.restype = i32
-        L.echo_cache_step.argtypes = [i32, _vp, i64, _vp, i32, ctypes.POINTER(EchoCacheStruct), _vp,
+        L.echo_cache_step.argtypes = [i32, _vp, i64, _vp, i32, _vp, i32, ctypes.POINTER(EchoCacheStruct), _vp,
                                       _vp, _vp, _vp, _vp]
         L.echo_prefill_scores.restype = i32
         L.echo_prefill_scores.argtypes = [i32, i64, i64, _vp, _vp, _vp, _vp, _vp, i64, _vp, _vp, _vp, _vp]
@@ -140,20 +140,22 @@ def above_words(B: int, n_tokens: int) -> int:
 
 
 def index_scores(tok_off, n_tokens, q8, wfold, k8, ks, scores, theta_hat, hist, status, above=None,
-                 tok2slot=None, stream=None):
+                 cache=None, stream=None):
+    """echo_index_scores; cache: a LayerCache whose residents `above` leaves out (and whose free bits
+    are snapshotted for early_fetch)."""
     B = q8.shape[0]
     _check("echo_index_scores", load().echo_index_scores(
         B, _ptr(tok_off), int(n_tokens), _ptr(q8), _ptr(wfold), _ptr(k8), _ptr(ks), _ptr(scores),
-        _ptr(theta_hat), _ptr(hist), _ptr(above), _ptr(tok2slot), _ptr(status), _stream(stream)))
+        _ptr(theta_hat), _ptr(hist), _ptr(above), ctypes.byref(cache.struct) if cache is not None else None,
+        _ptr(status), _stream(stream)))
 
 
-def early_fetch(tok_off, n_tokens, above, early_cap, cache, status, stats=None, stream=None, copy_stream=None):
+def early_fetch(tok_off, n_tokens, above, early_cap, cache, status, stream=None):
+    """echo_early_fetch: copy the rows of the early set (the tables learn it in cache_step)."""
     B = tok_off.shape[0] - 1
-    st = _stream(stream)
-    cst = _stream(copy_stream) if copy_stream is not None else st
     _check("echo_early_fetch", load().echo_early_fetch(
-        B, _ptr(tok_off), int(n_tokens), _ptr(above), int(early_cap), ctypes.byref(cache.struct),
-        _ptr(status), _ptr(stats), st, cst))
+        B, _ptr(tok_off), int(n_tokens), _ptr(above), int(early_cap), ctypes.byref(cache.struct), _ptr(status),
+        _stream(stream)))
 
 
 def topk_select(tok_off, n_tokens, scores, k, hist, theta_hat, alpha, sel_idx, kth, status, stats=None,
@@ -164,14 +166,16 @@ def topk_select(tok_off, n_tokens, scores, k, hist, theta_hat, alpha, sel_idx, k
         _ptr(sel_idx), _ptr(kth), _ptr(status), _ptr(stats), _stream(stream)))
 
 
-def cache_step(tok_off, n_tokens, sel, cache, sel_slot, status, stats=None, stream=None, copy_stream=None):
+def cache_step(tok_off, n_tokens, sel, cache, sel_slot, status, stats=None, stream=None, copy_stream=None,
+               above=None, early_cap=-1):
+    """echo_cache_step; above/early_cap: the early set of this step (as given to early_fetch)."""
     B = tok_off.shape[0] - 1
     m = sel.shape[-1]
     st = _stream(stream)
     cst = _stream(copy_stream) if copy_stream is not None else st
     _check("echo_cache_step", load().echo_cache_step(
-        B, _ptr(tok_off), int(n_tokens), _ptr(sel), int(m), ctypes.byref(cache.struct), _ptr(sel_slot),
-        _ptr(status), _ptr(stats), st, cst))
+        B, _ptr(tok_off), int(n_tokens), _ptr(sel), int(m), _ptr(above), int(early_cap),
+        ctypes.byref(cache.struct), _ptr(sel_slot), _ptr(status), _ptr(stats), st, cst))
 
 
 def prefill_scores(R, row0, n_keys, q8, wfold, k8, ks, scores, W, theta_hat, hist, status, stream=None):
@@ -231,6 +235,7 @@ class LayerCache:
         self.early_tok = torch.zeros((B * C,), **i32)
         self.early_slot = torch.zeros((B * C,), **i32)
         self.early_cnt = torch.zeros((B,), **i32)
+        self.free_snap = torch.zeros((B * C // 32,), **i32)
         self.dev_kv = torch.zeros((B * C, host_pool.shape[1]), dtype=host_pool.dtype, device=device)
         self.host_pool = host_pool
         self.host_alias = host_device_alias(host_pool)
@@ -239,6 +244,7 @@ class LayerCache:
         s.miss_tok, s.miss_slot, s.miss_cnt = _ptr(self.miss_tok), _ptr(self.miss_slot), _ptr(self.miss_cnt)
         s.early_tok, s.early_slot, s.early_cnt = (_ptr(self.early_tok), _ptr(self.early_slot),
                                                   _ptr(self.early_cnt))
+        s.free_snap = _ptr(self.free_snap)
         s.host_kv, s.dev_kv = self.host_alias, _ptr(self.dev_kv)
         s.row_bytes, s.C, s.reserved = self.row_bytes, C, 0
         self.struct = s

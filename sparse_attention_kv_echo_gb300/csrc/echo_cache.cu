@@ -6,48 +6,33 @@
 //   panel "One layer, one step: free -> allocate -> recall": unselected slots
 //     are freed (no write-back: the host holds every token), misses get
 //     slots, their rows are recalled from the host pool;
-//   panel "Decode: fetch above a predicted threshold": tokens scoring above
-//     the predicted threshold are fetched before top-k completes, up to a cap.
 //
-// Kernels (one CTA of 1024 threads per request for the table work):
-//   early_select_kernel  ordered scan of the score kernel's above-threshold bits
-//                        (one word per 32 tokens), keeping non-resident tokens
-//                        (block prefix sums); the first min(cap, free) of them
-//                        take the lowest free slots.
+// Kernels (one CTA of 1024 threads per request for the table work; the early
+// selection runs at the end of the score kernel, echo_scores.cu):
 //   cache_step_kernel    marks the slots of selected residents in a shared
 //                        bitmap, frees the rest one warp per 32-slot word
-//                        (ballot -> free-bit word), compacts the misses in
-//                        ascending order, hands them the lowest free slots by a
-//                        prefix sum of popcounts over the free-bit words.
-//   recall_kernel        one warp per row, 16-byte loads from the pinned host
-//                        pool through its device alias (zero-copy over the
-//                        host link), 16-byte stores into the device cache.
+//                        (ballot -> free-bit word), then a prefix sum of
+//                        popcounts over the free-bit words hands the misses,
+//                        in ascending order, the lowest free slots: each
+//                        thread owns 4 consecutive selection entries, so its
+//                        misses take consecutive free slots (one binary search,
+//                        then a walk over the free bits).  Independent loads go
+//                        out together at the start: two rounds of global
+//                        latency for a 2048-entry selection and 4096 slots.
+//   recall_kernel        one warp per row (two in flight), 16-byte loads from
+//                        the pinned host pool through its device alias
+//                        (zero-copy over the host link), 16-byte stores into
+//                        the device cache; the rows of all requests form one
+//                        list spread over a few large blocks.
 #include "echo_common.cuh"
 #include "echo_internal.h"
+#include "echo_slots.cuh"
 
 namespace echo {
 namespace {
 
 constexpr int kCT = 1024;
-constexpr int kMaxSlotsSmem = 1 << 19;   // per-slot-word tables in shared memory: 3 x 2^14 words (192 KB)
 
-struct CacheArgs {
-    int32_t* tok2slot;
-    int32_t* slot2tok;
-    uint32_t* freebits;
-    int32_t* miss_tok;
-    int32_t* miss_slot;
-    int32_t* miss_cnt;
-    int32_t* early_tok;
-    int32_t* early_slot;
-    int32_t* early_cnt;
-    int32_t C;
-};
-
-CacheArgs cache_args(const echo_cache& c) {
-    return CacheArgs{c.tok2slot, c.slot2tok, c.freebits, c.miss_tok, c.miss_slot, c.miss_cnt,
-                     c.early_tok, c.early_slot, c.early_cnt, c.C};
-}
 
 __device__ __forceinline__ bool request_range(const int64_t* tok_off, int64_t n_tokens, int b, int64_t* base,
                                               int64_t* n) {
@@ -62,145 +47,17 @@ __device__ __forceinline__ bool request_range(const int64_t* tok_off, int64_t n_
     return true;
 }
 
-// Give the first M tokens of tok_list the M lowest free slots of one
-// request, in ascending order.  Block-wide and parallel over ranks: a prefix
-// of the free-slot counts of the bit words (wpre, shared memory) maps rank r to
-// its word by binary search and to its bit as the (r - wpre[w])-th set bit.
-// wpre: words + 1 entries, fbs: words entries of shared memory.  Returns the
-// number assigned.
-__device__ uint32_t assign_lowest_free(uint32_t* fb, int words, uint32_t M, const int32_t* tok_list,
-                                       int32_t* slot_list, int32_t* t2s, int32_t* s2t, int64_t n, int C,
-                                       uint32_t* scan, uint32_t* wpre, uint32_t* fbs, int32_t* status) {
-    uint32_t run = 0;
-    for (int w0 = 0; w0 < words; w0 += kCT) {
-        const int w = w0 + threadIdx.x;
-        const uint32_t f = (w < words) ? fb[w] : 0u;
-        if (w < words) fbs[w] = f;
-        uint32_t tot;
-        const uint32_t ex = block_exclusive_scan<kCT>(__popc(f), scan, &tot);
-        if (w < words) wpre[w] = run + ex;
-        run += tot;
-    }
-    if (threadIdx.x == 0) wpre[words] = run;
-    __syncthreads();
-    const uint32_t take = M < run ? M : run;
-    for (uint32_t r = threadIdx.x; r < take; r += kCT) {
-        int lo = 0, hi = words - 1;   // largest w with wpre[w] <= r
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (wpre[mid] <= r)
-                lo = mid;
-            else
-                hi = mid - 1;
-        }
-        uint32_t f = fbs[lo];
-        for (uint32_t i = r - wpre[lo]; i > 0; --i) f &= f - 1;
-        const int slot = lo * 32 + (__ffs(f) - 1);
-        const int32_t tok = tok_list[r];
-        if (tok >= 0 && tok < n && slot < C && t2s[tok] < 0) {
-            t2s[tok] = slot;
-            s2t[slot] = tok;
-            slot_list[r] = slot;
-        } else {
-            set_status(status, ECHO_ST_BADDATA);
-        }
-    }
-    // the taken slots are the lowest `take` free ones: clear them word by word
-    for (int w = threadIdx.x; w < words; w += kCT) {
-        if (wpre[w] >= take) continue;
-        uint32_t f = fbs[w];
-        uint32_t k = take - wpre[w];
-        uint32_t taken = 0;
-        while (f && k) {
-            const uint32_t low = f & (0u - f);
-            taken |= low;
-            f ^= low;
-            --k;
-        }
-        if (taken) fb[w] = fbs[w] & ~taken;
-    }
-    if (take < M && threadIdx.x == 0) set_status(status, ECHO_ST_NOSLOT);
-    __syncthreads();
-    return take;
-}
-
-// Tiles of 128 tokens of request b, and the first tile of b in the list of all
-// requests' tiles (the order the score kernel writes its above-threshold words in).
-__device__ uint32_t first_tile_of(const int64_t* tok_off, int64_t n_tokens, int b, uint32_t* scan) {
-    uint32_t part = 0;
-    for (int bb = threadIdx.x; bb < b; bb += kCT) {
-        const int64_t lo = tok_off[bb], hi = tok_off[bb + 1];
-        if (lo >= 0 && hi >= lo && hi <= n_tokens) part += static_cast<uint32_t>((hi - lo + 127) / 128);
-    }
-    uint32_t total;
-    block_exclusive_scan<kCT>(part, scan, &total);
-    return total;
-}
-
-__global__ void __launch_bounds__(kCT) early_select_kernel(const int64_t* __restrict__ tok_off, int64_t n_tokens,
-                                                           const uint32_t* __restrict__ above, int cap, CacheArgs c,
-                                                           int32_t* status, uint32_t* stats) {
-    __shared__ uint32_t scan[40];
-    extern __shared__ uint32_t dyn[];   // wpre [words + 1], fbs [words]
-    const int b = blockIdx.x, tid = threadIdx.x;
-    int64_t base, n;
-    if (!request_range(tok_off, n_tokens, b, &base, &n) && tid == 0) set_status(status, ECHO_ST_BADDATA);
-    const int C = c.C, words = C / 32;
-    uint32_t* wpre = dyn;
-    uint32_t* fbs = dyn + words + 1;
-    int32_t* t2s = c.tok2slot + base;
-    int32_t* s2t = c.slot2tok + static_cast<int64_t>(b) * C;
-    uint32_t* fb = c.freebits + static_cast<int64_t>(b) * words;
-    int32_t* etok = c.early_tok + static_cast<int64_t>(b) * C;
-    int32_t* eslot = c.early_slot + static_cast<int64_t>(b) * C;
-    if (n == 0 || cap == 0) {
-        if (tid == 0) c.early_cnt[b] = 0;
-        return;
-    }
-    const uint32_t t0 = first_tile_of(tok_off, n_tokens, b, scan);
-    const uint32_t* ab = above + 4 * static_cast<size_t>(t0);
-    const int awords = static_cast<int>(4 * ((n + 127) / 128));
-    uint32_t F = 0;
-    for (int w0 = 0; w0 < words; w0 += kCT) {
-        const int w = w0 + tid;
-        uint32_t tot;
-        block_exclusive_scan<kCT>(w < words ? __popc(fb[w]) : 0u, scan, &tot);
-        F += tot;
-    }
-    const uint32_t limit = (cap < 0) ? F : min(F, static_cast<uint32_t>(cap));
-    uint32_t found = 0;
-    // word w covers tokens 32*w .. 32*w+31 of the request: ascending word, ascending bit;
-    // the marked tokens are the non-resident ones above the threshold
-    for (int w0 = 0; w0 < awords && found < limit; w0 += kCT) {
-        const int w = w0 + tid;
-        uint32_t cand = (w < awords) ? ab[w] : 0u;
-        if (w == awords - 1 && (n & 31)) cand &= (1u << (n & 31)) - 1u;   // no token past the request end
-        uint32_t tot;
-        uint32_t rank = found + block_exclusive_scan<kCT>(__popc(cand), scan, &tot);
-        while (cand) {
-            const int bit = __ffs(cand) - 1;
-            cand &= cand - 1;
-            if (rank < limit) etok[rank] = 32 * w + bit;
-            ++rank;
-        }
-        found += tot;
-    }
-    const uint32_t E = min(found, limit);
-    __syncthreads();
-    const uint32_t got = assign_lowest_free(fb, words, E, etok, eslot, t2s, s2t, n, C, scan, wpre, fbs, status);
-    if (tid == 0) {
-        c.early_cnt[b] = static_cast<int32_t>(got);
-        if (stats && got) atomicAdd(stats + ECHO_STAT_EARLY, got);
-    }
-}
+constexpr int kPer = 4;        // selection entries per thread per chunk
+constexpr int kEarlyWords = 4;  // above-threshold words per thread per chunk
 
 __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restrict__ tok_off, int64_t n_tokens,
-                                                         const int32_t* __restrict__ sel, int m, CacheArgs c,
-                                                         int32_t* __restrict__ sel_slot, int32_t* status,
+                                                         const int32_t* __restrict__ sel, int m,
+                                                         const uint32_t* __restrict__ above, int early_cap,
+                                                         CacheArgs c, int32_t* __restrict__ sel_slot, int32_t* status,
                                                          uint32_t* stats) {
     extern __shared__ uint32_t keep[];  // keep [words]: a selected token lives in the slot; then wpre, fbs
     __shared__ uint32_t scan[40];
-    __shared__ uint32_t s_flags;
+    __shared__ uint32_t s_flags, s_early_used;
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int64_t base, n;
     if (!request_range(tok_off, n_tokens, b, &base, &n) && tid == 0) set_status(status, ECHO_ST_BADDATA);
@@ -209,109 +66,230 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
     int32_t* s2t = c.slot2tok + static_cast<int64_t>(b) * C;
     uint32_t* fb = c.freebits + static_cast<int64_t>(b) * words;
     const int32_t* sl = sel + static_cast<int64_t>(b) * m;
+    int32_t* out = sel_slot + static_cast<int64_t>(b) * m;
     int32_t* mtok = c.miss_tok + static_cast<int64_t>(b) * C;
     int32_t* mslot = c.miss_slot + static_cast<int64_t>(b) * C;
+    int32_t* etok = c.early_tok + static_cast<int64_t>(b) * C;
+    int32_t* eslot = c.early_slot + static_cast<int64_t>(b) * C;
     uint32_t* wpre = keep + words;
     uint32_t* fbs = wpre + words + 1;
+    constexpr int kChunk = kCT * kPer;
+    const int chunks = (m + kChunk - 1) / kChunk;
+    const bool early = above != nullptr && early_cap != 0 && n > 0;
 
-    for (int w = tid; w < words; w += kCT) keep[w] = 0u;
-    if (tid == 0) s_flags = 0;
-    __syncthreads();
-    // 1a. slots that hold a selected token are kept
-    for (int i = tid; i < m; i += kCT) {
-        const int32_t s = sl[i];
-        if (s < 0) continue;
-        if (s >= n) {
-            atomicOr(&s_flags, static_cast<uint32_t>(ECHO_ST_BADDATA));
-            continue;
+    // Loads that depend on nothing else go out together: this thread's
+    // selection entries (kPer consecutive ones, so its misses have consecutive
+    // ranks), the free-bit words, and its first above-threshold words.
+    int32_t s[kPer], j[kPer];
+    auto load_sel = [&](int c0) {
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int i = c0 + kPer * tid + q;
+            s[q] = (i < m) ? sl[i] : -1;
         }
-        const int32_t j = t2s[s];
-        if (j >= 0 && j < C) atomicOr(&keep[j >> 5], 1u << (j & 31));
+    };
+    load_sel(0);
+    const uint32_t* ab = early ? above + 4 * (base / 128 + b) : nullptr;
+    const int nw = static_cast<int>((n + 31) >> 5);
+    const uint32_t tail_mask = (n & 31) ? (1u << (n & 31)) - 1u : ~0u;
+    uint32_t v[kEarlyWords];
+    if (early) early_words<kEarlyWords>(ab, nw, tail_mask, kEarlyWords * tid, v);
+    for (int w = tid; w < words; w += kCT) {
+        fbs[w] = fb[w];
+        keep[w] = 0u;
+    }
+    if (tid == 0) {
+        s_flags = 0;
+        s_early_used = 0;
     }
     __syncthreads();
-    // 1b. every other occupied slot is freed; bytes stay, nothing is written back
+
+    // 0. the early set (the tokens echo_early_fetch copied) becomes resident
+    uint32_t E = 0;
+    if (early) {
+        const uint32_t F = free_prefix<kCT>(fbs, words, scan, wpre, fbs);
+        const uint32_t limit = (early_cap < 0) ? F : min(F, static_cast<uint32_t>(early_cap));
+        const uint32_t found = early_assign<kCT, kEarlyWords>(
+            ab, nw, tail_mask, limit, 0u, limit, wpre, fbs, words, scan, v, [&](uint32_t r, int tok, int slot) {
+                if (slot < 0 || t2s[tok] >= 0) {  // no free slot left, or not the non-resident token it should be
+                    set_status(status, ECHO_ST_BADDATA);
+                    return;
+                }
+                etok[r] = tok;
+                eslot[r] = slot;
+                t2s[tok] = slot;
+                s2t[slot] = tok;
+            });
+        E = min(found, limit);
+        __syncthreads();  // every walk over fbs is done before its bits change
+        take_lowest_free<kCT>(fbs, words, E, wpre);
+        __syncthreads();
+    }
+
+    // 1a. slots that hold a selected token are kept; the selection must be
+    // ascending with -1 padding last
+    auto resident_slots = [&](int c0) -> uint32_t {
+        const int inext = c0 + kPer * tid + kPer;
+        const int32_t after = (inext < m) ? sl[inext] : -1;
+        uint32_t flags = 0;
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int32_t nxt = (q + 1 < kPer) ? s[q + 1] : after;
+            if (s[q] >= 0 && s[q] < n) {
+                if (nxt >= 0 && nxt <= s[q]) flags |= ECHO_ST_BADDATA;
+                j[q] = t2s[s[q]];
+            } else {
+                j[q] = -1;
+                if (s[q] >= 0 || nxt >= 0) flags |= ECHO_ST_BADDATA;
+            }
+        }
+        return flags;
+    };
+    for (int ch = 0; ch < chunks; ++ch) {
+        if (ch > 0) load_sel(ch * kChunk);
+        const uint32_t flags = resident_slots(ch * kChunk);
+        if (flags) atomicOr(&s_flags, flags);
+#pragma unroll
+        for (int q = 0; q < kPer; ++q)
+            if (j[q] >= 0 && j[q] < C) atomicOr(&keep[j[q] >> 5], 1u << (j[q] & 31));
+    }
+    __syncthreads();
+
+    // 1b. every other occupied slot is freed (bytes stay, nothing is written
+    // back), one warp per 32-slot word
     for (int w = warp; w < words; w += kCT / 32) {
         const int slot = w * 32 + lane;
-        const int32_t s = s2t[slot];
+        const int32_t st = s2t[slot];
         const bool kept = (keep[w] >> lane) & 1u;
-        const bool freeing = s >= 0 && !kept;
+        const bool freeing = st >= 0 && !kept;
         if (freeing) {
             s2t[slot] = -1;
-            if (s < n) t2s[s] = -1;
+            if (st < n) t2s[st] = -1;
         }
         const unsigned fm = __ballot_sync(0xffffffffu, freeing);
-        if (lane == 0 && fm) fb[w] |= fm;
+        if (lane == 0) fbs[w] |= fm;
     }
+    // early fetches of this step that the selection kept (their slot is kept)
+    uint32_t used = 0;
+    for (uint32_t e = tid; e < E; e += kCT) {
+        const int32_t es = eslot[e];
+        if (es >= 0 && es < C && ((keep[es >> 5] >> (es & 31)) & 1u)) ++used;
+    }
+    if (used) atomicAdd(&s_early_used, used);
     __syncthreads();
-    // 2. misses, ascending; the selection must be ascending with -1 padding last
-    uint32_t M = 0, early_used = 0;
-    for (int c0 = 0; c0 < m; c0 += 4 * kCT) {
-        const int i0 = c0 + 4 * tid;
-        uint32_t f = 0;
+
+    // 2. free-slot prefix over the new free-bit words
+    const uint32_t F = free_prefix<kCT>(fbs, words, scan, wpre, fbs);
+
+    // 3. the misses, in ascending token order, take the lowest free slots; the
+    // slot of every selected entry is written on the way
+    uint32_t found = 0;
+    for (int ch = 0; ch < chunks; ++ch) {
+        const int c0 = ch * kChunk;
+        if (chunks > 1) {  // the registers hold the last chunk only: reload
+            load_sel(c0);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int i = i0 + j;
-            if (i < m) {
-                const int32_t s = sl[i];
-                if (s >= 0 && s < n) {
-                    if (i + 1 < m && sl[i + 1] >= 0 && sl[i + 1] <= s)
-                        atomicOr(&s_flags, static_cast<uint32_t>(ECHO_ST_BADDATA));
-                    if (t2s[s] < 0) f |= 1u << j;
-                } else if (s >= 0 || (i + 1 < m && sl[i + 1] >= 0)) {
-                    atomicOr(&s_flags, static_cast<uint32_t>(ECHO_ST_BADDATA));
-                }
-            }
+            for (int q = 0; q < kPer; ++q) j[q] = (s[q] >= 0 && s[q] < n) ? t2s[s[q]] : -1;
         }
-        uint32_t tot;
-        uint32_t rank = M + block_exclusive_scan<kCT>(__popc(f), scan, &tot);
+        uint32_t missing = 0;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (f & (1u << j)) {
-                if (rank < static_cast<uint32_t>(C)) mtok[rank] = sl[i0 + j];
+        for (int q = 0; q < kPer; ++q)
+            if (s[q] >= 0 && s[q] < n && j[q] < 0) missing |= 1u << q;
+        uint32_t tot;
+        uint32_t rank = found + block_exclusive_scan<kCT>(__popc(missing), scan, &tot);
+        FreeWalk walk(wpre, fbs, words, rank < F ? rank : 0u);
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int i = c0 + kPer * tid + q;
+            if (i >= m) break;
+            int32_t slot = j[q];
+            if (missing & (1u << q)) {
+                slot = (rank < F) ? walk.next() : -1;
+                if (slot >= 0) {
+                    if (rank < static_cast<uint32_t>(C)) {
+                        mtok[rank] = s[q];
+                        mslot[rank] = slot;
+                    }
+                    t2s[s[q]] = slot;
+                    s2t[slot] = s[q];
+                }
                 ++rank;
+            } else if (s[q] < 0 || s[q] >= n) {
+                slot = -1;
             }
-        M += tot;
+            out[i] = slot;
+        }
+        found += tot;
     }
-    if (M > static_cast<uint32_t>(C)) M = C;
-    // early fetches of this step that the selection kept
-    const int ecnt = min(c.early_cnt[b], C);
-    for (int i = tid; i < ecnt; i += kCT) {
-        const int32_t s = c.early_tok[static_cast<int64_t>(b) * C + i];
-        if (s >= 0 && s < n && t2s[s] >= 0) ++early_used;
-    }
+    const uint32_t got = min(found, F);
+    __syncthreads();  // every walk over fbs is done before its bits change
+    take_lowest_free<kCT>(fbs, words, got, wpre);
     __syncthreads();
-    // 3. the misses take the lowest free slots
-    const uint32_t got = assign_lowest_free(fb, words, M, mtok, mslot, t2s, s2t, n, C, scan, wpre, fbs, status);
-    __syncthreads();
-    // 4. slot of every selected entry
-    for (int i = tid; i < m; i += kCT) {
-        const int32_t s = sl[i];
-        sel_slot[static_cast<int64_t>(b) * m + i] = (s >= 0 && s < n) ? t2s[s] : -1;
-    }
-    if (early_used && stats) atomicAdd(stats + ECHO_STAT_EARLY_USED, early_used);
-    __syncthreads();
+    for (int w = tid; w < words; w += kCT) fb[w] = fbs[w];
     if (tid == 0) {
         c.miss_cnt[b] = static_cast<int32_t>(got);
+        c.early_cnt[b] = static_cast<int32_t>(E);
         if (stats && got) atomicAdd(stats + ECHO_STAT_MISSES, got);
-        if (s_flags) set_status(status, static_cast<int>(s_flags));
+        if (stats && E) atomicAdd(stats + ECHO_STAT_EARLY, E);
+        if (stats && s_early_used) atomicAdd(stats + ECHO_STAT_EARLY_USED, s_early_used);
+        uint32_t flags = s_flags;
+        if (found > F) flags |= ECHO_ST_NOSLOT;
+        if (flags) set_status(status, static_cast<int>(flags));
     }
 }
 
-__global__ void __launch_bounds__(256) recall_kernel(const int64_t* __restrict__ tok_off, int64_t n_tokens, int C,
-                                                     const int32_t* __restrict__ tok_list,
-                                                     const int32_t* __restrict__ slot_list,
-                                                     const int32_t* __restrict__ cnt, const uint8_t* host,
-                                                     uint8_t* __restrict__ dev, int64_t row_bytes, int32_t* status) {
-    const int b = blockIdx.y;
+constexpr int kRecallThreads = 512;
+constexpr int kRecallBlocks = 32;
+constexpr int kRows = 2;        // rows per warp in flight
+constexpr int kStage = 4096;    // early (token, slot) pairs staged in shared memory per round
+
+// One warp copies kRows rows (those with ok[r]) of `chunks` 16-byte pieces.
+__device__ __forceinline__ void copy_rows(const int4* const (&src)[kRows], int4* const (&dst)[kRows],
+                                          const bool (&ok)[kRows], int chunks, int lane) {
+    for (int c0 = 0; c0 < chunks; c0 += 96) {
+        int4 v[kRows][3];
+#pragma unroll
+        for (int r = 0; r < kRows; ++r)
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {
+                const int c = c0 + lane + 32 * j;
+                v[r][j] = (ok[r] && c < chunks) ? __ldcs(src[r] + c) : make_int4(0, 0, 0, 0);
+            }
+#pragma unroll
+        for (int r = 0; r < kRows; ++r)
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {
+                const int c = c0 + lane + 32 * j;
+                if (ok[r] && c < chunks) dst[r][c] = v[r][j];
+            }
+    }
+}
+
+// Rows of all requests form one list (request b's rows at pre[b] .. pre[b+1]);
+// warp w of the grid copies rows w*2, w*2+1, then strides by the grid's warps.
+__global__ void __launch_bounds__(kRecallThreads)
+    recall_kernel(int B, const int64_t* __restrict__ tok_off, int64_t n_tokens, int C,
+                  const int32_t* __restrict__ tok_list, const int32_t* __restrict__ slot_list,
+                  const int32_t* __restrict__ cnt, const uint8_t* host, uint8_t* __restrict__ dev, int64_t row_bytes,
+                  int32_t* status) {
+    extern __shared__ int32_t pre[];  // [B + 1]
+    __shared__ uint32_t scan[kRecallThreads / 32 + 1];
     const int lane = threadIdx.x & 31;
     const int warps = blockDim.x >> 5;
-    int64_t base, n;
-    if (!request_range(tok_off, n_tokens, b, &base, &n)) return;
-    int count = cnt[b];
-    if (count > C) count = C;
+    uint32_t run = 0;
+    for (int b0 = 0; b0 < B; b0 += kRecallThreads) {
+        const int b = b0 + static_cast<int>(threadIdx.x);
+        const uint32_t v = (b < B) ? static_cast<uint32_t>(min(max(cnt[b], 0), C)) : 0u;
+        uint32_t tot;
+        const uint32_t ex = block_exclusive_scan<kRecallThreads>(v, scan, &tot);
+        if (b < B) pre[b] = static_cast<int32_t>(run + ex);
+        run += tot;
+    }
+    if (threadIdx.x == 0) pre[B] = static_cast<int32_t>(run);
+    __syncthreads();
+    const int total = static_cast<int>(run);
     const int chunks = static_cast<int>(row_bytes / 16);
-    constexpr int kRows = 2;  // rows per warp in flight
-    for (int i0 = (blockIdx.x * warps + (threadIdx.x >> 5)) * kRows; i0 < count;
+    for (int i0 = (blockIdx.x * warps + (threadIdx.x >> 5)) * kRows; i0 < total;
          i0 += gridDim.x * warps * kRows) {
         const int4* src[kRows];
         int4* dst[kRows];
@@ -320,10 +298,24 @@ __global__ void __launch_bounds__(256) recall_kernel(const int64_t* __restrict__
         for (int r = 0; r < kRows; ++r) {
             const int i = i0 + r;
             ok[r] = false;
-            if (i < count) {
-                const int32_t tok = tok_list[static_cast<int64_t>(b) * C + i];
-                const int32_t slot = slot_list[static_cast<int64_t>(b) * C + i];
-                if (tok >= 0 && tok < n && slot >= 0 && slot < C) {
+            src[r] = nullptr;
+            dst[r] = nullptr;
+            if (i < total) {
+                int lo = 0, hi = B - 1;  // request of row i: largest b with pre[b] <= i
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (pre[mid] <= i)
+                        lo = mid;
+                    else
+                        hi = mid - 1;
+                }
+                const int b = lo;
+                int64_t base, n;
+                const bool range_ok = request_range(tok_off, n_tokens, b, &base, &n);
+                const int64_t e = static_cast<int64_t>(b) * C + (i - pre[b]);
+                const int32_t tok = tok_list[e];
+                const int32_t slot = slot_list[e];
+                if (range_ok && tok >= 0 && tok < n && slot >= 0 && slot < C) {
                     ok[r] = true;
                     src[r] = reinterpret_cast<const int4*>(host + (base + tok) * row_bytes);
                     dst[r] = reinterpret_cast<int4*>(dev + (static_cast<int64_t>(b) * C + slot) * row_bytes);
@@ -332,53 +324,112 @@ __global__ void __launch_bounds__(256) recall_kernel(const int64_t* __restrict__
                 }
             }
         }
-        for (int c0 = 0; c0 < chunks; c0 += 96) {
-            int4 v[kRows][3];
+        copy_rows(src, dst, ok, chunks, lane);
+    }
+}
+
+// The early fetch: G = gridDim.x / B blocks per request (at least one; blocks
+// beyond a multiple of G idle).  Every block of a request computes the early
+// set from the above-threshold words and the free-bit snapshot (the tables
+// are not touched), stages (token, slot) pairs in shared memory, and copies
+// the staged rows whose index is g (mod G), g its place in the request's group.
+__global__ void __launch_bounds__(kRecallThreads)
+    early_fetch_kernel(int B, const int64_t* __restrict__ tok_off, int64_t n_tokens,
+                       const uint32_t* __restrict__ above, int cap, const uint32_t* __restrict__ snap, int C,
+                       const uint8_t* host, uint8_t* __restrict__ dev, int64_t row_bytes, int32_t* status) {
+    extern __shared__ uint32_t esm[];  // wpre [words + 1], fbs [words], stage tokens, stage slots
+    __shared__ uint32_t scan[kRecallThreads / 32 + 1];
+    const int words = C / 32;
+    uint32_t* wpre = esm;
+    uint32_t* fbs = wpre + words + 1;
+    int32_t* stok = reinterpret_cast<int32_t*>(fbs + words);
+    int32_t* sslot = stok + kStage;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int kWarps = kRecallThreads / 32;
+    const int G = max(1, static_cast<int>(gridDim.x) / B);
+    const int groups = static_cast<int>(gridDim.x) / G;
+    const int g = static_cast<int>(blockIdx.x) % G;
+    const int chunks = static_cast<int>(row_bytes / 16);
+    pdl_wait();  // the above-threshold words and the snapshot come from the score kernel
+    for (int b = static_cast<int>(blockIdx.x) / G; b < B && static_cast<int>(blockIdx.x) < groups * G;
+         b += groups) {
+        int64_t base, n;
+        if (!request_range(tok_off, n_tokens, b, &base, &n)) {
+            if (threadIdx.x == 0) set_status(status, ECHO_ST_BADDATA);
+            continue;
+        }
+        if (n == 0 || cap == 0) continue;
+        const uint32_t* ab = above + 4 * (base / 128 + b);
+        const int nw = static_cast<int>((n + 31) >> 5);
+        const uint32_t tail_mask = (n & 31) ? (1u << (n & 31)) - 1u : ~0u;
+        uint32_t v[kEarlyWords];
+        early_words<kEarlyWords>(ab, nw, tail_mask, kEarlyWords * threadIdx.x, v);
+        const uint32_t F = free_prefix<kRecallThreads>(snap + static_cast<int64_t>(b) * words, words, scan, wpre, fbs);
+        const uint32_t limit = (cap < 0) ? F : min(F, static_cast<uint32_t>(cap));
+        for (uint32_t r_lo = 0; r_lo < limit; r_lo += kStage) {
+            if (r_lo > 0) early_words<kEarlyWords>(ab, nw, tail_mask, kEarlyWords * threadIdx.x, v);
+            const uint32_t r_hi = min(limit, r_lo + kStage);
+            const uint32_t found = early_assign<kRecallThreads, kEarlyWords>(
+                ab, nw, tail_mask, limit, r_lo, r_hi, wpre, fbs, words, scan, v, [&](uint32_t r, int tok, int slot) {
+                    stok[r - r_lo] = tok;
+                    sslot[r - r_lo] = slot;
+                });
+            const uint32_t E = min(found, limit);
+            __syncthreads();
+            const int staged = static_cast<int>(min(E, r_hi) - min(E, r_lo));
+            const int share = staged > g ? (staged - g + G - 1) / G : 0;
+            for (int k0 = warp * kRows; k0 < share; k0 += kWarps * kRows) {
+                const int4* src[kRows];
+                int4* dst[kRows];
+                bool ok[kRows];
 #pragma unroll
-            for (int r = 0; r < kRows; ++r)
-#pragma unroll
-                for (int j = 0; j < 3; ++j) {
-                    const int c = c0 + lane + 32 * j;
-                    v[r][j] = (ok[r] && c < chunks) ? __ldcs(src[r] + c) : make_int4(0, 0, 0, 0);
+                for (int r = 0; r < kRows; ++r) {
+                    const int k = k0 + r;
+                    ok[r] = false;
+                    src[r] = nullptr;
+                    dst[r] = nullptr;
+                    if (k < share) {
+                        const int i = g + G * k;
+                        const int32_t tok = stok[i], slot = sslot[i];
+                        if (tok >= 0 && tok < n && slot >= 0 && slot < C) {
+                            ok[r] = true;
+                            src[r] = reinterpret_cast<const int4*>(host + (base + tok) * row_bytes);
+                            dst[r] = reinterpret_cast<int4*>(dev + (static_cast<int64_t>(b) * C + slot) * row_bytes);
+                        } else if (lane == 0) {
+                            set_status(status, ECHO_ST_BADDATA);
+                        }
+                    }
                 }
-#pragma unroll
-            for (int r = 0; r < kRows; ++r)
-#pragma unroll
-                for (int j = 0; j < 3; ++j) {
-                    const int c = c0 + lane + 32 * j;
-                    if (ok[r] && c < chunks) dst[r][c] = v[r][j];
-                }
+                copy_rows(src, dst, ok, chunks, lane);
+            }
+            __syncthreads();  // the stage is reused by the next round / request
+            if (found < r_hi) break;  // every marked token was counted
         }
     }
 }
 
 }  // namespace
 
-cudaError_t launch_early_select(int B, const int64_t* tok_off, int64_t n_tokens, const uint32_t* above, int cap,
-                                const echo_cache& c, int32_t* status, uint32_t* stats, cudaStream_t s) {
-    const size_t smem = (2 * static_cast<size_t>(c.C / 32) + 1) * sizeof(uint32_t);
-    cudaError_t e = cudaFuncSetAttribute(early_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    early_select_kernel<<<B, kCT, smem, s>>>(tok_off, n_tokens, above, cap, cache_args(c), status, stats);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_recall(int B, const int64_t* tok_off, int64_t n_tokens, int C, const int32_t* tok_list,
                           const int32_t* slot_list, const int32_t* cnt, const void* host_kv, void* dev_kv,
                           int64_t row_bytes, int32_t* status, cudaStream_t s) {
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    // About one block per SM in all: the host link, not the SMs, bounds the copy,
-    // and a small footprint lets the step's other kernels run alongside.
-    int gx = (sms + B - 1) / B;
-    const int rows_per_block = 16;
-    const int gx_max = (C + rows_per_block - 1) / rows_per_block;
-    if (gx > gx_max) gx = gx_max;
-    if (gx < 1) gx = 1;
-    recall_kernel<<<dim3(gx, B), 256, 0, s>>>(tok_off, n_tokens, C, tok_list, slot_list, cnt,
-                                              static_cast<const uint8_t*>(host_kv), static_cast<uint8_t*>(dev_kv),
-                                              row_bytes, status);
+    // A few large blocks: the host link, not the SMs, bounds the copy (32 x 16
+    // warps x 2 rows keep ~1.2 MB of host reads in flight).  Loads that wait on
+    // the host link slow every other kernel that shares an SM with them, so the
+    // copy stays on few SMs, and a block this size (512 threads x ~50 registers)
+    // cannot share an SM with a 1024-thread top-k CTA, which then runs elsewhere.
+    int blocks = kRecallBlocks < sms / 2 ? kRecallBlocks : sms / 2;
+    if (blocks < 1) blocks = 1;
+    const size_t smem = (static_cast<size_t>(B) + 1) * sizeof(int32_t);
+    cudaError_t e = prefer_max_shared(recall_kernel);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(recall_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    recall_kernel<<<blocks, kRecallThreads, smem, s>>>(B, tok_off, n_tokens, C, tok_list, slot_list, cnt,
+                                                      static_cast<const uint8_t*>(host_kv),
+                                                      static_cast<uint8_t*>(dev_kv), row_bytes, status);
     return cudaGetLastError();
 }
 
@@ -387,13 +438,14 @@ cudaError_t launch_recall(int B, const int64_t* tok_off, int64_t n_tokens, int C
 namespace echo {
 
 int enqueue_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
-                       const echo_cache* cache, int32_t* sel_slot, int32_t* status, uint32_t* stats,
-                       cudaStream_t stream, cudaStream_t copy_stream) {
+                       const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,
+                       int32_t* status, uint32_t* stats, cudaStream_t stream, cudaStream_t copy_stream) {
     const size_t smem = (3 * static_cast<size_t>(cache->C / 32) + 1) * sizeof(uint32_t);
+    ECHO_CUDA_OK(prefer_max_shared(cache_step_kernel));
     ECHO_CUDA_OK(cudaFuncSetAttribute(cache_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(smem)));
-    cache_step_kernel<<<B, kCT, smem, stream>>>(tok_off, n_tokens, sel, m, cache_args(*cache), sel_slot, status,
-                                                stats);
+    cache_step_kernel<<<B, kCT, smem, stream>>>(tok_off, n_tokens, sel, m, above, early_cap, cache_args(*cache),
+                                                sel_slot, status, stats);
     ECHO_CUDA_OK(cudaGetLastError());
     const int rc = stream_wait(copy_stream, stream);
     if (rc) return rc;
@@ -410,38 +462,58 @@ int check_cache_step_args(int B, int64_t n_tokens, const int32_t* sel, int m, co
     if (n_tokens >= (1ll << 31)) return ECHO_EUNSUPPORTED;
     const int rc = check_cache(cache, B, m);
     if (rc) return rc;
-    if (cache->C > kMaxSlotsSmem) return ECHO_EUNSUPPORTED;
+    if (cache->C > kMaxSlots) return ECHO_EUNSUPPORTED;
     return ECHO_OK;
 }
 
 }  // namespace echo
 
 extern "C" int echo_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
-                               const echo_cache* cache, int32_t* sel_slot, int32_t* status, uint32_t* stats,
-                               echo_stream_t stream, echo_stream_t copy_stream) {
+                               const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,
+                               int32_t* status, uint32_t* stats, echo_stream_t stream, echo_stream_t copy_stream) {
     using namespace echo;
     if (!tok_off || !status) return ECHO_EINVAL;
     const int rc = check_cache_step_args(B, n_tokens, sel, m, cache, sel_slot);
     if (rc) return rc;
-    return enqueue_cache_step(B, tok_off, n_tokens, sel, m, cache, sel_slot, status, stats, stream, copy_stream);
+    return enqueue_cache_step(B, tok_off, n_tokens, sel, m, above, early_cap, cache, sel_slot, status, stats, stream,
+                              copy_stream);
 }
 
 extern "C" int echo_early_fetch(int B, const int64_t* tok_off, int64_t n_tokens, const uint32_t* above,
-                                int early_cap, const echo_cache* cache, int32_t* status, uint32_t* stats,
-                                echo_stream_t stream, echo_stream_t copy_stream) {
+                                int early_cap, const echo_cache* cache, int32_t* status, echo_stream_t stream) {
     using namespace echo;
     if (B <= 0 || n_tokens < 0) return ECHO_EINVAL;
     if (B > ECHO_MAX_REQUESTS) return ECHO_EUNSUPPORTED;
-    if (!tok_off || !status || (n_tokens > 0 && !above)) return ECHO_EINVAL;
+    if (!tok_off || !above || !status) return ECHO_EINVAL;
     if (n_tokens >= (1ll << 31)) return ECHO_EUNSUPPORTED;
     int rc = check_cache(cache, B, 0);
     if (rc) return rc;
-    if (cache->C > kMaxSlotsSmem) return ECHO_EUNSUPPORTED;
-    ECHO_CUDA_OK(launch_early_select(B, tok_off, n_tokens, above, early_cap, *cache, status, stats, stream));
-    rc = stream_wait(copy_stream, stream);
-    if (rc) return rc;
-    ECHO_CUDA_OK(launch_recall(B, tok_off, n_tokens, cache->C, cache->early_tok, cache->early_slot,
-                               cache->early_cnt, cache->host_kv, cache->dev_kv, cache->row_bytes, status,
-                               copy_stream));
+    if (!cache->free_snap) return ECHO_EINVAL;
+    if (cache->C > kMaxSlots) return ECHO_EUNSUPPORTED;
+    if (n_tokens == 0 || early_cap == 0) return ECHO_OK;
+    const int sms = sm_count();
+    if (sms <= 0) return ECHO_ECUDA;
+    int blocks = kRecallBlocks < sms / 2 ? kRecallBlocks : sms / 2;
+    if (blocks < 1) blocks = 1;
+    const size_t smem = (2 * static_cast<size_t>(cache->C / 32) + 1 + 2 * kStage) * sizeof(uint32_t);
+    ECHO_CUDA_OK(prefer_max_shared(early_fetch_kernel));
+    ECHO_CUDA_OK(cudaFuncSetAttribute(early_fetch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(smem)));
+    // Programmatic dependent launch: the blocks are scheduled as the score
+    // kernel's CTAs retire and wait (griddepcontrol.wait) for its results.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(kRecallThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, early_fetch_kernel, B, tok_off, n_tokens, above, early_cap,
+                                    static_cast<const uint32_t*>(cache->free_snap), static_cast<int>(cache->C),
+                                    static_cast<const uint8_t*>(cache->host_kv), static_cast<uint8_t*>(cache->dev_kv),
+                                    cache->row_bytes, status));
     return ECHO_OK;
 }

@@ -153,6 +153,8 @@ extern "C" int echo_prefill_block(int R, int64_t row0, int64_t n_keys, const flo
     if (sms <= 0) return ECHO_ECUDA;
     int64_t grid = (total + 255) / 256;
     if (grid > 8 * sms) grid = 8 * sms;
+    ECHO_CUDA_OK(prefer_max_shared(union_mark_kernel));
+    ECHO_CUDA_OK(prefer_max_shared(union_compact_kernel));
     union_mark_kernel<<<static_cast<int>(grid), 256, 0, stream>>>(sel_idx, total, p.mark, n);
     ECHO_CUDA_OK(cudaGetLastError());
     union_compact_kernel<<<1, kPT, 0, stream>>>(p.mark, n, W, union_list, union_bits, union_count, p.tok_off2,
@@ -162,8 +164,8 @@ extern "C" int echo_prefill_block(int R, int64_t row0, int64_t n_keys, const flo
     // the previous block's recall reads the miss lists this step rewrites
     rc = stream_wait(stream, copy_stream);
     if (rc) return rc;
-    return enqueue_cache_step(1, p.tok_off2, n_keys, union_list, static_cast<int>(W), cache, sel_slot, status, stats,
-                              stream, copy_stream);
+    return enqueue_cache_step(1, p.tok_off2, n_keys, union_list, static_cast<int>(W), nullptr, 0, cache, sel_slot,
+                              status, stats, stream, copy_stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -73,6 +73,8 @@ cudaError_t launch_quantize(int B, const float* q, const float* w, uint8_t* q8, 
                             uint32_t* hist_to_zero, int32_t* status, cudaStream_t s) {
     const int rows = B * ECHO_HEADS;
     const int blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    const cudaError_t e = prefer_max_shared(quantize_kernel);
+    if (e != cudaSuccess) return e;
     quantize_kernel<<<blocks, kWarpsPerBlock * 32, 0, s>>>(B, q, w, q8, qscale, wfold, hist_to_zero, status);
     return cudaGetLastError();
 }

@@ -56,6 +56,9 @@ struct ScoreArgs {
     uint32_t* above;
     const int32_t* tok2slot;   // with above: mark only tokens that are not resident (NULL: all)
     int32_t* status;
+    const uint32_t* freebits;  // copied to free_snap (fb_words words) for the early fetch
+    uint32_t* free_snap;
+    int64_t fb_words;
 };
 
 struct __align__(16) ScoreCtl {
@@ -162,6 +165,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_barrier_init();
     }
     for (int i = tid; i < kEpiWarps * 256; i += kThreads) (&ctl->hist[0][0])[i] = 0u;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + tid; i < a.fb_words;
+         i += static_cast<int64_t>(gridDim.x) * kThreads)
+        a.free_snap[i] = a.freebits[i];
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&kmap);
         prefetch_tmap(&qmap);
@@ -342,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float wv[ECHO_HEADS];
         float shift = 0.f, theta = 0.f;
         bool theta_ok = false;
-        int64_t nb = 0, obase = 0;
+        int64_t nb = 0, obase = 0, abase = 0;
         bool ok = true;
         for (uint32_t it = group; it < ntiles; it += 2) {
             const uint32_t t = t_begin + it;
@@ -380,6 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Seg sg = segment(a, b, &bad);
                 nb = sg.len;
                 obase = sg.out;
+                // the request's above-threshold words start at 4 * (floor(first row / 128) + b)
+                abase = 4 * (sg.key_lo / kTileM + b - static_cast<int64_t>(tstart[b]));
             }
             const int64_t tok = static_cast<int64_t>(t - tstart[b]) * kTileM + row;
             const bool valid = tok < nb;
@@ -424,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (a.above) {
                 // tokens above the predicted threshold: one word per 32 rows of the tile
                 const unsigned am = __ballot_sync(0xffffffffu, valid && theta_ok && score > theta && !resident);
-                if (lane == 0) a.above[4 * static_cast<size_t>(t) + quarter] = am;
+                if (lane == 0) a.above[abase + 4 * static_cast<int64_t>(t) + quarter] = am;
             }
             if (valid) {
                 a.scores[obase + tok] = score;
@@ -470,6 +478,7 @@ static int launch_scores(const ScoreArgs& args, const uint8_t* q8, const uint8_t
     if (sms <= 0) return ECHO_ECUDA;
     const int grid = static_cast<int>(tiles_ub < sms ? tiles_ub : sms);
     const size_t smem = smem_bytes(args.B);
+    ECHO_CUDA_OK(prefer_max_shared(score_kernel));
     ECHO_CUDA_OK(cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(smem)));
     // Programmatic dependent launch: the prologue and first key loads overlap
@@ -492,7 +501,7 @@ static int launch_scores(const ScoreArgs& args, const uint8_t* q8, const uint8_t
 
 extern "C" int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens, const uint8_t* q8,
                                  const float* wfold, const uint8_t* k8, const float* ks, float* scores,
-                                 const float* theta_hat, uint32_t* hist, uint32_t* above, const int32_t* tok2slot,
+                                 const float* theta_hat, uint32_t* hist, uint32_t* above, const echo_cache* cache,
                                  int32_t* status, echo_stream_t stream) {
     using namespace echo;
     if (B <= 0 || n_tokens < 0) return ECHO_EINVAL;
@@ -501,9 +510,17 @@ extern "C" int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens
     if (n_tokens > 0 && (!k8 || !ks || !scores)) return ECHO_EINVAL;
     if (n_tokens >= (1ll << 31)) return ECHO_EUNSUPPORTED;
     if (!is_aligned(q8, 16) || !is_aligned(wfold, 16) || !is_aligned(k8, 16)) return ECHO_EINVAL;
+    if (cache) {
+        if (!above) return ECHO_EINVAL;
+        const int rc = check_cache(cache, B, 0);
+        if (rc) return rc;
+        if (!cache->free_snap) return ECHO_EINVAL;
+    }
     if (n_tokens == 0) return ECHO_OK;
     ScoreArgs args{B, tok_off, n_tokens, 0, 0, 1, wfold, ks, scores, theta_hat, hist, above,
-                   above ? tok2slot : nullptr, status};
+                   cache ? cache->tok2slot : nullptr, status, cache ? cache->freebits : nullptr,
+                   cache ? cache->free_snap : nullptr,
+                   cache ? static_cast<int64_t>(B) * (cache->C / 32) : 0};
     return launch_scores(args, q8, k8, n_tokens, n_tokens / kTileM + B, stream);
 }
 
@@ -517,7 +534,8 @@ extern "C" int echo_prefill_scores(int R, int64_t row0, int64_t n_keys, const ui
     if (row0 + R > n_keys || W < row0 + R) return ECHO_EINVAL;
     if (n_keys >= (1ll << 31) || static_cast<int64_t>(R) * W >= (1ll << 40)) return ECHO_EUNSUPPORTED;
     if (!is_aligned(q8, 16) || !is_aligned(wfold, 16) || !is_aligned(k8, 16)) return ECHO_EINVAL;
-    ScoreArgs args{R, nullptr, n_keys, row0, W, 0, wfold, ks, scores, theta_hat, hist, nullptr, nullptr, status};
+    ScoreArgs args{R, nullptr, n_keys, row0, W, 0, wfold, ks, scores, theta_hat, hist, nullptr, nullptr, status,
+                   nullptr, nullptr, 0};
     const int64_t tiles_ub = static_cast<int64_t>(R) * ((row0 + R + kTileM - 1) / kTileM);
     return launch_scores(args, q8, k8, n_keys, tiles_ub, stream);
 }

@@ -436,6 +436,7 @@ int launch_topk(int B, const int64_t* tok_off, int64_t n_tokens, int64_t row0, i
                 const uint32_t* hist, float* theta_hat, float alpha, int32_t* sel_idx, float* kth, int32_t* status,
                 uint32_t* stats, cudaStream_t stream) {
     const size_t smem = sizeof(TopkShared);
+    ECHO_CUDA_OK(prefer_max_shared(topk_kernel));
     ECHO_CUDA_OK(cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(smem)));
     TopkSegs segs{tok_off, n_tokens, row0, W};

@@ -4,11 +4,15 @@ A DecodeLayer owns the torch tensors one layer needs for B requests (scores,
 histogram, threshold state, selection, the GPU cache and its lists, the
 quantised query) and issues the calls of a step:
     echo_quantize_q    -> E4M3 query, folded head weights, cleared histogram
-    echo_index_scores  -> scores, shifted-score histogram, above-threshold bits
-    echo_early_fetch   -> tokens above the predicted threshold (+ recall); on a
-                          side stream, concurrently with top-k
-    echo_topk_select   -> exact top-k indices, k-th score, EMA threshold
-    echo_cache_step    -> free / allocate / recall, slot of every selection
+    echo_index_scores  -> scores, shifted-score histogram, above-threshold bits,
+                          free-bit snapshot
+    echo_early_fetch   -> rows of the tokens above the predicted threshold,
+                          copied from the host pool on the step's stream
+                          (programmatic dependent of the score kernel) while
+    echo_topk_select   -> exact top-k indices, k-th score, EMA threshold, and
+    echo_cache_step    -> early set into the tables, free / allocate, slot of
+                          every selection run on a side stream; the late-miss
+                          recall joins the step's stream after both.
 Every buffer keeps its address and size, so ``step`` can be captured into a
 CUDA graph and replayed; ``q_in``/``w_in`` are the inputs a graph reads.
 """
@@ -57,31 +61,33 @@ class DecodeLayer:
         self.status.zero_()
         self.stats.zero_()
 
-    def step(self, q: torch.Tensor | None = None, w: torch.Tensor | None = None, stream=None,
-             copy_stream=None):
+    def step(self, q: torch.Tensor | None = None, w: torch.Tensor | None = None, stream=None):
         """Enqueue one decode step (q [B,64,128] f32, w [B,64] f32; defaults q_in / w_in).
 
-        stream: the step's stream (default: current); copy_stream: recalls (default: stream).
-        The early fetch's selection runs on the layer's side stream while top-k runs."""
+        stream: the step's stream (default: current).  Everything, the row copies
+        included, is ordered before whatever is enqueued on `stream` next."""
         q = self.q_in if q is None else q
         w = self.w_in if w is None else w
         main = torch.cuda.current_stream() if stream is None else stream
+        above = self.above if self.predictor else None
         L.quantize_q(q, w, self.q8, self.qscale, self.wfold, self.status, hist=self.hist, stream=main)
         L.index_scores(self.tok_off, self.n_tokens, self.q8, self.wfold, self.k8, self.ks, self.scores,
-                       self.theta, self.hist, self.status, above=self.above if self.predictor else None,
-                       tok2slot=self.cache.tok2slot, stream=main)
+                       self.theta, self.hist, self.status, above=above,
+                       cache=self.cache if self.predictor else None, stream=main)
         if self.predictor:
+            # the early rows stream over the host link on `main` while top-k and
+            # the table update run on the side stream
             self.side.wait_stream(main)
             L.early_fetch(self.tok_off, self.n_tokens, self.above, self.early_cap, self.cache, self.status,
-                          stats=self.stats, stream=self.side,
-                          copy_stream=copy_stream if copy_stream is not None else self.side)
+                          stream=main)
+            work = self.side
+        else:
+            work = main
         L.topk_select(self.tok_off, self.n_tokens, self.scores, self.k, self.hist, self.theta, self.alpha,
-                      self.sel_idx, self.kth, self.status, stats=self.stats, stream=main)
-        if self.predictor:
-            main.wait_stream(self.side)
+                      self.sel_idx, self.kth, self.status, stats=self.stats, stream=work)
         L.cache_step(self.tok_off, self.n_tokens, self.sel_idx, self.cache, self.sel_slot, self.status,
-                     stats=self.stats, stream=main, copy_stream=copy_stream)
+                     stats=self.stats, stream=work, copy_stream=main, above=above, early_cap=self.early_cap)
 
     def kernel_launches_per_step(self) -> int:
-        # quantize + score (+ early select + early recall) + top-k + cache step + recall
-        return 2 + (2 if self.predictor else 0) + 1 + 2
+        # quantize + score (+ early fetch) + top-k + cache step + late recall
+        return 2 + (1 if self.predictor else 0) + 1 + 2

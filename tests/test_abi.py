@@ -27,7 +27,7 @@ def L():
 def test_header_declares_the_calls():
     names = _declared()
     for want in ("echo_index_scores", "echo_topk_select", "echo_cache_step", "echo_quantize_q",
-                 "echo_early_fetch"):
+                 "echo_early_fetch", "echo_prefill_block"):
         assert want in names
 
 
@@ -51,26 +51,36 @@ def test_host_checks_reject_bad_arguments(L):
     from sparse_attention_kv_echo_gb300 import lib
     v = ctypes.c_void_p
     dummy = v(0x1000)
-    # index_scores(B, tok_off, n_tokens, q8, wfold, k8, ks, scores, theta, hist, above, tok2slot, status, stream)
-    assert L.echo_index_scores(0, dummy, 10, dummy, dummy, dummy, dummy, dummy, None, None, None, None, dummy,
-                               None) == lib.ECHO_EINVAL
-    assert L.echo_index_scores(lib.MAX_REQUESTS + 1, dummy, 10, dummy, dummy, dummy, dummy, dummy, None,
-                               None, None, None, dummy, None) == lib.ECHO_EUNSUPPORTED
-    # missing q8
-    assert L.echo_index_scores(1, dummy, 10, None, dummy, dummy, dummy, dummy, None, None, None, None, dummy,
-                               None) == lib.ECHO_EINVAL
-    # misaligned keys (must be 16-byte aligned)
-    assert L.echo_index_scores(1, dummy, 10, dummy, dummy, v(0x1001), dummy, dummy, None, None, None, None, dummy,
-                               None) == lib.ECHO_EINVAL
-    # negative token count
-    assert L.echo_index_scores(1, dummy, -5, dummy, dummy, dummy, dummy, dummy, None, None, None, None, dummy,
-                               None) == lib.ECHO_EINVAL
-    # no tokens: nothing to do, nothing enqueued
-    assert L.echo_index_scores(1, dummy, 0, dummy, dummy, None, None, None, None, None, None, None, dummy,
-                               None) == lib.ECHO_OK
-    # early fetch needs the above-threshold words and a cache
-    assert L.echo_early_fetch(1, dummy, 10, None, -1, None, dummy, None, None, None) == lib.ECHO_EINVAL
-    assert L.echo_early_fetch(1, dummy, 10, dummy, -1, None, dummy, None, None, None) == lib.ECHO_EINVAL
+    # index_scores(B, tok_off, n_tokens, q8, wfold, k8, ks, scores, theta, hist, above, cache, status, stream)
+    def scores_call(B=1, n=10, q8=dummy, k8=dummy, above=None, cache=None):
+        return L.echo_index_scores(B, dummy, n, q8, dummy, k8, dummy, dummy, None, None, above, cache, dummy, None)
+    assert scores_call(B=0) == lib.ECHO_EINVAL
+    assert scores_call(B=lib.MAX_REQUESTS + 1) == lib.ECHO_EUNSUPPORTED
+    assert scores_call(q8=None) == lib.ECHO_EINVAL                     # missing q8
+    assert scores_call(k8=v(0x1001)) == lib.ECHO_EINVAL                # keys must be 16-byte aligned
+    assert scores_call(n=-5) == lib.ECHO_EINVAL                        # negative token count
+    assert scores_call(n=0) == lib.ECHO_OK                             # no tokens: nothing enqueued
+    # a cache needs the above-threshold words, a complete struct and the snapshot
+    c = lib.EchoCacheStruct()
+    for f, _ in lib.EchoCacheStruct._fields_:
+        if f not in ("row_bytes", "C", "reserved"):
+            setattr(c, f, 0x1000)
+    c.row_bytes, c.C = 1152, 64
+    cache = ctypes.byref(c)
+    assert scores_call(above=None, cache=cache) == lib.ECHO_EINVAL
+    c.free_snap = None
+    assert scores_call(above=dummy, cache=cache) == lib.ECHO_EINVAL
+    # early_fetch(B, tok_off, n_tokens, above, early_cap, cache, status, stream)
+    assert L.echo_early_fetch(1, dummy, 10, dummy, -1, cache, dummy, None) == lib.ECHO_EINVAL   # no snapshot
+    c.free_snap = 0x1000
+    assert L.echo_early_fetch(1, dummy, 10, None, -1, cache, dummy, None) == lib.ECHO_EINVAL    # no above words
+    assert L.echo_early_fetch(1, dummy, 10, dummy, -1, None, dummy, None) == lib.ECHO_EINVAL    # no cache
+    assert L.echo_early_fetch(0, dummy, 10, dummy, -1, cache, dummy, None) == lib.ECHO_EINVAL
+    assert L.echo_early_fetch(1, dummy, 0, dummy, -1, cache, dummy, None) == lib.ECHO_OK        # nothing to do
+    assert L.echo_early_fetch(1, dummy, 10, dummy, 0, cache, dummy, None) == lib.ECHO_OK        # cap 0: nothing
+    c.C = 48                                                           # not a multiple of 32
+    assert L.echo_early_fetch(1, dummy, 10, dummy, -1, cache, dummy, None) == lib.ECHO_ECAPACITY
+    assert scores_call(above=dummy, cache=cache) == lib.ECHO_ECAPACITY
     # the bitmask size: four words per 128-token tile of each request, at most
     assert lib.above_words(8, 32768) == 4 * (256 + 8)
     assert lib.above_words(0, 10) == 0
@@ -87,19 +97,19 @@ def test_cache_checks(L):
     from sparse_attention_kv_echo_gb300 import lib
     v = ctypes.c_void_p
     s = lib.EchoCacheStruct()
-    for f, _ in lib.EchoCacheStruct._fields_[:11]:
+    for f, _ in lib.EchoCacheStruct._fields_[:12]:
         setattr(s, f, 0x2000)
     s.row_bytes, s.C = 1152, 64
     dummy = v(0x1000)
     # k (m) larger than C
-    assert L.echo_cache_step(1, dummy, 100, dummy, 65, ctypes.byref(s), dummy, dummy, None, None,
+    assert L.echo_cache_step(1, dummy, 100, dummy, 65, None, 0, ctypes.byref(s), dummy, dummy, None, None,
                              None) == lib.ECHO_ECAPACITY
     s.C = 48   # not a multiple of 32
-    assert L.echo_cache_step(1, dummy, 100, dummy, 16, ctypes.byref(s), dummy, dummy, None, None,
+    assert L.echo_cache_step(1, dummy, 100, dummy, 16, None, 0, ctypes.byref(s), dummy, dummy, None, None,
                              None) == lib.ECHO_ECAPACITY
     s.C, s.row_bytes = 64, 1000  # row not a multiple of 16 bytes
-    assert L.echo_cache_step(1, dummy, 100, dummy, 16, ctypes.byref(s), dummy, dummy, None, None,
+    assert L.echo_cache_step(1, dummy, 100, dummy, 16, None, 0, ctypes.byref(s), dummy, dummy, None, None,
                              None) == lib.ECHO_EUNSUPPORTED
     s.row_bytes, s.dev_kv = 1152, None
-    assert L.echo_cache_step(1, dummy, 100, dummy, 16, ctypes.byref(s), dummy, dummy, None, None,
+    assert L.echo_cache_step(1, dummy, 100, dummy, 16, None, 0, ctypes.byref(s), dummy, dummy, None, None,
                              None) == lib.ECHO_EINVAL

@@ -122,11 +122,11 @@ def test_scores_and_hist(lengths, theta):
     off, k8, ks, q, wt, gs, gh, st, th, ab = _score_call(w, theta=theta)
     assert st == 0
     check_scores((off, k8, ks), q, wt, gs)
-    t0 = 0
     for b in range(w.B):
         sc = gs[off[b]:off[b + 1]]
         assert np.array_equal(gh[b], orc.hist256(sc, th[b]))
-        # above-threshold bits: request b's words start at 4 * (tiles of the requests before it)
+        # above-threshold bits: request b's words start at 4 * (floor(first row / 128) + b)
+        t0 = 4 * (int(off[b]) // 128 + b)
         nb = sc.size
         words = 4 * ((nb + 127) // 128)
         bits = np.unpackbits(ab[t0:t0 + words].view(np.uint8), bitorder="little")[:nb].astype(bool) \
@@ -136,7 +136,6 @@ def test_scores_and_hist(lengths, theta):
         if words:
             pad = np.unpackbits(ab[t0:t0 + words].view(np.uint8), bitorder="little")[nb:]
             assert not pad.any()
-        t0 += words
     assert np.all(np.isnan(gs[w.total_tokens:]))      # rows outside every request untouched
 
 
