@@ -146,7 +146,8 @@ int echo_quantize_q(int B, const float* q, const float* w, uint8_t* q8, float* q
  *   for every token row t of request b, which equals the definition
  *   sum_h w[h] * ReLU(q[h] . k[t]) over the dequantised E4M3 values.
  *   Inputs: q8 [B,64,128] u8 and wfold [B,64] f32 from echo_quantize_q,
- *   k8 [n_tokens,128] E4M3 bytes, ks [n_tokens] f32 (q8 and k8 16-byte aligned).
+ *   k8 [n_tokens,128] E4M3 bytes, ks [n_tokens] f32 (q8, k8 and ks 16-byte
+ *   aligned; with a cache, its tok2slot too).
  *   Outputs: scores [n_tokens] f32 (rows outside every request untouched);
  *   hist [B,256] u32 (may be NULL): ADDS, per request, the counts of
  *   bin = top 8 bits of orderkey(fp32(score - shift)), shift = theta_hat[b]

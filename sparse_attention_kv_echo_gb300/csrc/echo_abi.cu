@@ -47,6 +47,22 @@ int encode_tmap_bytes_2d(CUtensorMap* map, const void* base, uint64_t inner_byte
     return r == CUDA_SUCCESS ? ECHO_OK : ECHO_ECUDA;
 }
 
+int encode_tmap_1d(CUtensorMap* map, const void* base, bool is_float, uint64_t n, uint32_t box) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return ECHO_ECUDA;
+    if (!is_aligned(base, 16) || n == 0 || n > (1ull << 31) || (box * 4u) % 16u != 0) return ECHO_EINVAL;
+    const cuuint64_t dims[1] = {n};
+    const cuuint64_t strides[1] = {n * 4};  // not read for rank 1, but the encoder wants the array
+    const cuuint32_t boxd[1] = {box};
+    const cuuint32_t estr[1] = {1};
+    memset(map, 0, sizeof(*map));
+    const CUresult r = fn(map, is_float ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_INT32, 1,
+                          const_cast<void*>(base), dims, strides, boxd, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ECHO_OK : ECHO_ECUDA;
+}
+
 int stream_wait(cudaStream_t to, cudaStream_t from) {
     if (to == from) return ECHO_OK;
     cudaEvent_t ev;

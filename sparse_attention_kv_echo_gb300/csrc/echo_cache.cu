@@ -48,7 +48,12 @@ __device__ __forceinline__ bool request_range(const int64_t* tok_off, int64_t n_
 }
 
 constexpr int kPer = 4;        // selection entries per thread per chunk
-constexpr int kEarlyWords = 4;  // above-threshold words per thread per chunk
+// Above-threshold words per thread per chunk: the early set's ranks do not
+// depend on it, so each kernel picks what keeps its threads' walks short
+// (1024 words = 32768 tokens per request: one word per thread of the cache
+// step, two per thread of the early fetch).
+constexpr int kEarlyWordsStep = 1;
+constexpr int kEarlyWordsFetch = 2;
 
 __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restrict__ tok_off, int64_t n_tokens,
                                                          const int32_t* __restrict__ sel, int m,
@@ -92,8 +97,8 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
     const uint32_t* ab = early ? above + 4 * (base / 128 + b) : nullptr;
     const int nw = static_cast<int>((n + 31) >> 5);
     const uint32_t tail_mask = (n & 31) ? (1u << (n & 31)) - 1u : ~0u;
-    uint32_t v[kEarlyWords];
-    if (early) early_words<kEarlyWords>(ab, nw, tail_mask, kEarlyWords * tid, v);
+    uint32_t v[kEarlyWordsStep];
+    if (early) early_words<kEarlyWordsStep>(ab, nw, tail_mask, kEarlyWordsStep * tid, v);
     for (int w = tid; w < words; w += kCT) {
         fbs[w] = fb[w];
         keep[w] = 0u;
@@ -109,9 +114,11 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
     if (early) {
         const uint32_t F = free_prefix<kCT>(fbs, words, scan, wpre, fbs);
         const uint32_t limit = (early_cap < 0) ? F : min(F, static_cast<uint32_t>(early_cap));
-        const uint32_t found = early_assign<kCT, kEarlyWords>(
+        const uint32_t found = early_assign<kCT, kEarlyWordsStep>(
             ab, nw, tail_mask, limit, 0u, limit, wpre, fbs, words, scan, v, [&](uint32_t r, int tok, int slot) {
-                if (slot < 0 || t2s[tok] >= 0) {  // no free slot left, or not the non-resident token it should be
+                // the marked tokens are not resident (the score kernel filtered them against these
+                // tables), so the tables are only written here, never read: no load on this path
+                if (slot < 0) {
                     set_status(status, ECHO_ST_BADDATA);
                     return;
                 }
@@ -350,11 +357,15 @@ __global__ void __launch_bounds__(kRecallThreads)
     const int groups = static_cast<int>(gridDim.x) / G;
     const int g = static_cast<int>(blockIdx.x) % G;
     const int chunks = static_cast<int>(row_bytes / 16);
+    // the request's rows come from the caller, not the score kernel: read them
+    // before waiting for it
+    int b = static_cast<int>(blockIdx.x) / G;
+    int64_t base = 0, n = 0;
+    bool range_ok = b < B && request_range(tok_off, n_tokens, b, &base, &n);
     pdl_wait();  // the above-threshold words and the snapshot come from the score kernel
-    for (int b = static_cast<int>(blockIdx.x) / G; b < B && static_cast<int>(blockIdx.x) < groups * G;
-         b += groups) {
-        int64_t base, n;
-        if (!request_range(tok_off, n_tokens, b, &base, &n)) {
+    for (; b < B && static_cast<int>(blockIdx.x) < groups * G; b += groups) {
+        if (b != static_cast<int>(blockIdx.x) / G) range_ok = request_range(tok_off, n_tokens, b, &base, &n);
+        if (!range_ok) {
             if (threadIdx.x == 0) set_status(status, ECHO_ST_BADDATA);
             continue;
         }
@@ -362,14 +373,14 @@ __global__ void __launch_bounds__(kRecallThreads)
         const uint32_t* ab = above + 4 * (base / 128 + b);
         const int nw = static_cast<int>((n + 31) >> 5);
         const uint32_t tail_mask = (n & 31) ? (1u << (n & 31)) - 1u : ~0u;
-        uint32_t v[kEarlyWords];
-        early_words<kEarlyWords>(ab, nw, tail_mask, kEarlyWords * threadIdx.x, v);
+        uint32_t v[kEarlyWordsFetch];
+        early_words<kEarlyWordsFetch>(ab, nw, tail_mask, kEarlyWordsFetch * threadIdx.x, v);
         const uint32_t F = free_prefix<kRecallThreads>(snap + static_cast<int64_t>(b) * words, words, scan, wpre, fbs);
         const uint32_t limit = (cap < 0) ? F : min(F, static_cast<uint32_t>(cap));
         for (uint32_t r_lo = 0; r_lo < limit; r_lo += kStage) {
-            if (r_lo > 0) early_words<kEarlyWords>(ab, nw, tail_mask, kEarlyWords * threadIdx.x, v);
+            if (r_lo > 0) early_words<kEarlyWordsFetch>(ab, nw, tail_mask, kEarlyWordsFetch * threadIdx.x, v);
             const uint32_t r_hi = min(limit, r_lo + kStage);
-            const uint32_t found = early_assign<kRecallThreads, kEarlyWords>(
+            const uint32_t found = early_assign<kRecallThreads, kEarlyWordsFetch>(
                 ab, nw, tail_mask, limit, r_lo, r_hi, wpre, fbs, words, scan, v, [&](uint32_t r, int tok, int slot) {
                     stok[r - r_lo] = tok;
                     sslot[r - r_lo] = slot;

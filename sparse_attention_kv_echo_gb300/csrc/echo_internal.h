@@ -23,6 +23,10 @@ int sm_count();
 int encode_tmap_bytes_2d(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,
                          uint32_t box_inner, uint32_t box_rows);
 
+// 1-D tensor map over n 4-byte elements (float32 or int32), box of `box`
+// elements (box * 4 a multiple of 16), no swizzle, zero fill out of range.
+int encode_tmap_1d(CUtensorMap* map, const void* base, bool is_float, uint64_t n, uint32_t box);
+
 // Make `to` wait for everything enqueued so far on `from` (no-op when equal).
 int stream_wait(cudaStream_t to, cudaStream_t from);
 

@@ -36,6 +36,13 @@ constexpr int kAccBufs = 4;                            // TMEM accumulators
 constexpr int kTmemCols = kAccBufs * ECHO_HEADS;       // 256 columns
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + kEpiWarps * 32;          // 320
+// Per-token side loads (key scale; cache slot for the residency filter) are
+// 1-D TMA boxes of 132 elements starting at the tile's first token rounded
+// down to a multiple of 4 (16 bytes), so that the box start is aligned; the
+// tile's 128 values sit at offset (first token & 3) inside the box.
+constexpr int kSideBox = 132;
+constexpr int kSidePitch = 160;                        // 640-byte smem rows (128-byte multiple)
+constexpr uint32_t kSideBytes = kSideBox * 4;
 constexpr uint32_t kIdesc = idesc_e4m3_f32(kTileM, ECHO_HEADS);
 
 // Segments: decode requests (CSR tok_off: keys and scores at rows
@@ -49,21 +56,20 @@ struct ScoreArgs {
     int64_t W;
     int theta_stride;
     const float* wfold;
-    const float* ks;
     float* scores;
     const float* theta_hat;
     uint32_t* hist;
     uint32_t* above;
-    const int32_t* tok2slot;   // with above: mark only tokens that are not resident (NULL: all)
+    int has_res;               // with above: mark only tokens that are not resident (slots from rmap)
     int32_t* status;
     const uint32_t* freebits;  // copied to free_snap (fb_words words) for the early fetch
     uint32_t* free_snap;
     int64_t fb_words;
 };
 
-struct __align__(16) ScoreCtl {
-    float ks[kStages][kTileM];  // per-token key scales of each stage's tile
-    int32_t res[kStages][kTileM];  // per-token cache slot (>= 0: resident) when above is filtered
+struct __align__(128) ScoreCtl {
+    float ks[kStages][kSidePitch];    // per-token key scales of each stage's tile (side box)
+    int32_t res[kStages][kSidePitch]; // per-token cache slot (>= 0: resident) when above is filtered
     uint64_t full[kStages];
     uint64_t empty[kStages];
     uint64_t qfull[2];
@@ -77,9 +83,10 @@ struct __align__(16) ScoreCtl {
     uint32_t hist[kEpiWarps][256];
 };
 
+// keys | q8 x 2 | ScoreCtl | tstart[B+1] | seg_lo[B] | seg_len[B]  (int32)
 __host__ __device__ constexpr size_t smem_bytes(int B) {
     return 1024 + static_cast<size_t>(kStages) * kKeyBytes + 2 * kQBytes + sizeof(ScoreCtl) +
-           4 * static_cast<size_t>(B + 1);
+           4 * static_cast<size_t>(3 * B + 1);
 }
 
 // Largest request b in [0, B) whose first tile is <= t.
@@ -101,6 +108,7 @@ struct Seg {
     int64_t out;      // index of its first score
 };
 
+// Segment of request (row) b from the arguments; bad segments are empty.
 __device__ __forceinline__ Seg segment(const ScoreArgs& a, int b, bool* bad) {
     if (a.W > 0) {
         const int64_t len = a.row0 + b + 1;
@@ -118,8 +126,16 @@ __device__ __forceinline__ Seg segment(const ScoreArgs& a, int b, bool* bad) {
     return Seg{lo, hi - lo, lo};
 }
 
+// The same, from the copy the prologue keeps in shared memory.
+__device__ __forceinline__ Seg cached_segment(const ScoreArgs& a, const int32_t* seg_lo, const int32_t* seg_len,
+                                              int b) {
+    const int64_t lo = seg_lo[b], len = seg_len[b];
+    return Seg{lo, len, a.W > 0 ? static_cast<int64_t>(b) * a.W : lo};
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     score_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+                 const __grid_constant__ CUtensorMap smap, const __grid_constant__ CUtensorMap rmap,
                  const ScoreArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -127,9 +143,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* qbuf = smem + kStages * kKeyBytes;
     ScoreCtl* ctl = reinterpret_cast<ScoreCtl*>(qbuf + 2 * kQBytes);
     int32_t* tstart = reinterpret_cast<int32_t*>(ctl + 1);
+    int32_t* seg_lo = tstart + (a.B + 1);
+    int32_t* seg_len = seg_lo + a.B;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int B = a.B;
+    // The next kernel of the stream (the early fetch) may be scheduled as this
+    // grid's CTAs retire; it waits for the whole grid before reading anything.
+    pdl_launch_dependents();
 
     // ---- first tile of every request (ceil(N_b / 128) tiles each)
     {
@@ -137,12 +158,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
         bool bad = false;
         uint32_t local = 0;
-        for (int b = b0; b < b1; ++b) local += static_cast<uint32_t>((segment(a, b, &bad).len + kTileM - 1) / kTileM);
+        for (int b = b0; b < b1; ++b) {
+            const Seg sg = segment(a, b, &bad);
+            seg_lo[b] = static_cast<int32_t>(sg.key_lo);
+            seg_len[b] = static_cast<int32_t>(sg.len);
+            local += static_cast<uint32_t>((sg.len + kTileM - 1) / kTileM);
+        }
         uint32_t total;
         uint32_t run = block_exclusive_scan<kThreads>(local, ctl->scan, &total);
         for (int b = b0; b < b1; ++b) {
             tstart[b] = static_cast<int32_t>(run);
-            run += static_cast<uint32_t>((segment(a, b, &bad).len + kTileM - 1) / kTileM);
+            run += static_cast<uint32_t>((seg_len[b] + kTileM - 1) / kTileM);
         }
         if (tid == 0) tstart[B] = static_cast<int32_t>(total);
         if (bad) set_status(a.status, ECHO_ST_BADDATA);
@@ -170,8 +196,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         a.free_snap[i] = a.freebits[i];
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&kmap);
-        prefetch_tmap(&qmap);
+        prefetch_tmap(&smap);
+        if (a.has_res) prefetch_tmap(&rmap);
     }
+    if (warp == 1 && lane == 0) prefetch_tmap(&qmap);
     if (warp == 1) {
         tmem_alloc(smem_addr(&ctl->tmem_base), kTmemCols);
         tmem_relinquish();
@@ -190,15 +218,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        // Lane 0 issues the TMA copies; all 32 lanes copy the tile's 128 key
-        // scales with cp.async, tracked by the same stage barrier.  The first
-        // stages' key loads go out before waiting for the quantiser (their
-        // inputs do not depend on it); q8 loads come after that wait.
-        if (ntiles > 0) {
+        // Lane 0 issues, per tile, the TMA copies of the 128 keys and of the
+        // side boxes (scales; slots), all on the stage barrier.  The first
+        // stages' loads go out before waiting for the quantiser (their inputs
+        // do not depend on it); the q8 of every request after the first (which
+        // the MMA warp loads) come after that wait.
+        if (ntiles > 0 && lane == 0) {
             const uint64_t pol = policy_evict_first();
             const uint32_t prefill = ntiles < static_cast<uint32_t>(kStages) ? ntiles : kStages;
+            const uint32_t stage_tx = kKeyBytes + kSideBytes * (a.has_res ? 2u : 1u);
             int kb = find_request(tstart, B, t_begin);   // request of the next key load
-            int64_t key_lo = 0, klen = 0;
+            int64_t key_lo = 0;
             int kcur = -1;
             uint32_t issued = 0, qn = 0;
             bool ok = true;
@@ -206,34 +236,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t t = t_begin + it;
                 while (t >= static_cast<uint32_t>(tstart[kb + 1])) ++kb;
                 if (kb != kcur) {
-                    bool bad = false;
-                    const Seg sg = segment(a, kb, &bad);
-                    key_lo = sg.key_lo;
-                    klen = sg.len;
+                    key_lo = seg_lo[kb];
                     kcur = kb;
                 }
                 const uint32_t s = it % kStages;
-                bool got = true;
-                if (lane == 0) got = mbar_wait(smem_addr(&ctl->empty[s]), ((it / kStages) & 1) ^ 1, abort);
-                got = __shfl_sync(0xffffffffu, got, 0);
-                if (!got) return false;
-                const int64_t tok0 = static_cast<int64_t>(t - tstart[kb]) * kTileM;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int r = 4 * lane + j;
-                    const bool in = tok0 + r < klen;
-                    cp_async_4(smem_addr(&ctl->ks[s][r]), in ? a.ks + key_lo + tok0 + r : a.ks, in ? 4u : 0u);
-                    if (a.tok2slot)
-                        cp_async_4(smem_addr(&ctl->res[s][r]), in ? a.tok2slot + key_lo + tok0 + r : a.tok2slot,
-                                   in ? 4u : 0u);
-                }
-                cp_async_mbar_arrive(smem_addr(&ctl->full[s]));
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(smem_addr(&ctl->full[s]), kKeyBytes);
-                    tma_load_2d_hint(smem_addr(keys + s * kKeyBytes), &kmap, smem_addr(&ctl->full[s]), 0,
-                                     static_cast<int32_t>(key_lo + tok0), pol);
-                }
+                if (!mbar_wait(smem_addr(&ctl->empty[s]), ((it / kStages) & 1) ^ 1, abort)) return false;
+                const int64_t tok0 = key_lo + static_cast<int64_t>(t - tstart[kb]) * kTileM;
+                const int32_t x0 = static_cast<int32_t>(tok0 & ~int64_t(3));   // 16-byte aligned box start
+                const uint32_t full = smem_addr(&ctl->full[s]);
+                mbar_arrive_expect_tx(full, stage_tx);
+                tma_load_2d_hint(smem_addr(keys + s * kKeyBytes), &kmap, full, 0, static_cast<int32_t>(tok0), pol);
+                tma_load_1d_hint(smem_addr(&ctl->ks[s][0]), &smap, full, x0, pol);
+                if (a.has_res) tma_load_1d_hint(smem_addr(&ctl->res[s][0]), &rmap, full, x0, pol);
                 return true;
             };
             for (; issued < prefill; ++issued)
@@ -247,20 +261,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t t = t_begin + it;
                 while (t >= static_cast<uint32_t>(tstart[b + 1])) ++b;
                 if (b != cur_b) {
-                    const uint32_t qi = qn & 1;
-                    bool got = true;
-                    if (lane == 0) {
-                        got = mbar_wait(smem_addr(&ctl->qempty[qi]), ((qn >> 1) & 1) ^ 1, abort);
-                        if (got) {
-                            mbar_arrive_expect_tx(smem_addr(&ctl->qfull[qi]), kQBytes);
-                            tma_load_2d(smem_addr(qbuf + qi * kQBytes), &qmap, smem_addr(&ctl->qfull[qi]), 0,
-                                        b * ECHO_HEADS);
+                    if (qn > 0) {  // the first request's q8 is loaded by the MMA warp
+                        const uint32_t qi = qn & 1;
+                        if (!mbar_wait(smem_addr(&ctl->qempty[qi]), ((qn >> 1) & 1) ^ 1, abort)) {
+                            ok = false;
+                            break;
                         }
-                    }
-                    got = __shfl_sync(0xffffffffu, got, 0);
-                    if (!got) {
-                        ok = false;
-                        break;
+                        mbar_arrive_expect_tx(smem_addr(&ctl->qfull[qi]), kQBytes);
+                        tma_load_2d(smem_addr(qbuf + qi * kQBytes), &qmap, smem_addr(&ctl->qfull[qi]), 0,
+                                    b * ECHO_HEADS);
                     }
                     cur_b = b;
                     ++qn;
@@ -273,17 +282,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++issued;
                 }
             }
-            if (!ok && lane == 0) {
+            if (!ok) {
                 set_status(a.status, ECHO_ST_TIMEOUT);
                 *abort = 1;
             }
-            // Let every copy this warp started land before the CTA exits.
-            if (lane == 0) {
-                for (uint32_t j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
-                    mbar_wait(smem_addr(&ctl->full[j % kStages]), (j / kStages) & 1, nullptr);
-                for (uint32_t j = (qn > 2 ? qn - 2 : 0); j < qn; ++j)
-                    mbar_wait(smem_addr(&ctl->qfull[j & 1]), (j >> 1) & 1, nullptr);
-            }
+            // Let every copy this thread started land before the CTA exits.
+            for (uint32_t j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
+                mbar_wait(smem_addr(&ctl->full[j % kStages]), (j / kStages) & 1, nullptr);
+            for (uint32_t j = (qn > 2 ? qn - 2 : 1); j < qn; ++j)
+                mbar_wait(smem_addr(&ctl->qfull[j & 1]), (j >> 1) & 1, nullptr);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -291,6 +298,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && ntiles > 0) {
             const uint32_t keys_s = smem_addr(keys), q_s = smem_addr(qbuf);
             int b = find_request(tstart, B, t_begin), cur_b = -1;
+            // q8 of the first request, as soon as the quantiser is done (the
+            // producer is busy with the first key loads meanwhile)
+            pdl_wait();
+            mbar_arrive_expect_tx(smem_addr(&ctl->qfull[0]), kQBytes);
+            tma_load_2d(q_s, &qmap, smem_addr(&ctl->qfull[0]), 0, b * ECHO_HEADS);
+            bool q0_landed = false;
             uint32_t qn = 0;
             bool ok = true;
             for (uint32_t it = 0; it < ntiles; ++it) {
@@ -303,6 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
+                    if (qn == 0) q0_landed = true;
                     cur_b = b;
                     ++qn;
                 }
@@ -330,6 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 set_status(a.status, ECHO_ST_TIMEOUT);
                 *abort = 1;
             }
+            if (!q0_landed) mbar_wait(smem_addr(&ctl->qfull[0]), 0, nullptr);  // its copy lands before exit
             // All MMAs of this thread complete before TMEM is released.
             mma_commit(smem_addr(&ctl->done));
             mbar_wait(smem_addr(&ctl->done), 0, nullptr);
@@ -349,6 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float shift = 0.f, theta = 0.f;
         bool theta_ok = false;
         int64_t nb = 0, obase = 0, abase = 0;
+        int side = 0;   // offset of the tile's first token in its side boxes
         bool ok = true;
         for (uint32_t it = group; it < ntiles; it += 2) {
             const uint32_t t = t_begin + it;
@@ -382,8 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 theta_ok = isfinite(th);
                 theta = th;
                 shift = theta_ok ? th : 0.f;
-                bool bad = false;
-                const Seg sg = segment(a, b, &bad);
+                const Seg sg = cached_segment(a, seg_lo, seg_len, b);
+                side = static_cast<int>(sg.key_lo & 3);
                 nb = sg.len;
                 obase = sg.out;
                 // the request's above-threshold words start at 4 * (floor(first row / 128) + b)
@@ -403,8 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
             }
-            const float ksv = ctl->ks[it % kStages][row];
-            const bool resident = a.tok2slot && ctl->res[it % kStages][row] >= 0;
+            const float ksv = ctl->ks[it % kStages][row + side];
+            const bool resident = a.has_res && ctl->res[it % kStages][row + side] >= 0;
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&ctl->empty[it % kStages]));
             uint32_t r0[16], r1[16], r2[16], r3[16];
@@ -466,13 +482,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-static int launch_scores(const ScoreArgs& args, const uint8_t* q8, const uint8_t* k8, int64_t key_rows,
-                         int64_t tiles_ub, cudaStream_t stream) {
-    CUtensorMap kmap, qmap;
+static int launch_scores(const ScoreArgs& args, const uint8_t* q8, const uint8_t* k8, const float* ks,
+                  const int32_t* tok2slot, int64_t key_rows, int64_t tiles_ub, cudaStream_t stream) {
+    CUtensorMap kmap, qmap, smap, rmap;
     int rc = encode_tmap_bytes_2d(&kmap, k8, ECHO_DIM, static_cast<uint64_t>(key_rows), ECHO_DIM, kTileM);
     if (rc) return rc;
     rc = encode_tmap_bytes_2d(&qmap, q8, ECHO_DIM, static_cast<uint64_t>(args.B) * ECHO_HEADS, ECHO_DIM,
                               ECHO_HEADS);
+    if (rc) return rc;
+    rc = encode_tmap_1d(&smap, ks, true, static_cast<uint64_t>(key_rows), kSideBox);
+    if (rc) return rc;
+    rc = encode_tmap_1d(&rmap, tok2slot ? static_cast<const void*>(tok2slot) : static_cast<const void*>(ks),
+                        tok2slot == nullptr, static_cast<uint64_t>(key_rows), kSideBox);
     if (rc) return rc;
     const int sms = sm_count();
     if (sms <= 0) return ECHO_ECUDA;
@@ -493,7 +514,7 @@ static int launch_scores(const ScoreArgs& args, const uint8_t* q8, const uint8_t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, score_kernel, kmap, qmap, args));
+    ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, score_kernel, kmap, qmap, smap, rmap, args));
     return ECHO_OK;
 }
 
@@ -509,19 +530,21 @@ extern "C" int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens
     if (!tok_off || !q8 || !wfold || !status) return ECHO_EINVAL;
     if (n_tokens > 0 && (!k8 || !ks || !scores)) return ECHO_EINVAL;
     if (n_tokens >= (1ll << 31)) return ECHO_EUNSUPPORTED;
-    if (!is_aligned(q8, 16) || !is_aligned(wfold, 16) || !is_aligned(k8, 16)) return ECHO_EINVAL;
+    if (!is_aligned(q8, 16) || !is_aligned(wfold, 16) || !is_aligned(k8, 16) || !is_aligned(ks, 16))
+        return ECHO_EINVAL;
     if (cache) {
         if (!above) return ECHO_EINVAL;
         const int rc = check_cache(cache, B, 0);
         if (rc) return rc;
-        if (!cache->free_snap) return ECHO_EINVAL;
+        if (!cache->free_snap || !is_aligned(cache->tok2slot, 16)) return ECHO_EINVAL;
     }
     if (n_tokens == 0) return ECHO_OK;
-    ScoreArgs args{B, tok_off, n_tokens, 0, 0, 1, wfold, ks, scores, theta_hat, hist, above,
-                   cache ? cache->tok2slot : nullptr, status, cache ? cache->freebits : nullptr,
+    ScoreArgs args{B, tok_off, n_tokens, 0, 0, 1, wfold, scores, theta_hat, hist, above,
+                   cache ? 1 : 0, status, cache ? cache->freebits : nullptr,
                    cache ? cache->free_snap : nullptr,
                    cache ? static_cast<int64_t>(B) * (cache->C / 32) : 0};
-    return launch_scores(args, q8, k8, n_tokens, n_tokens / kTileM + B, stream);
+    return launch_scores(args, q8, k8, ks, cache ? cache->tok2slot : nullptr, n_tokens, n_tokens / kTileM + B,
+                         stream);
 }
 
 extern "C" int echo_prefill_scores(int R, int64_t row0, int64_t n_keys, const uint8_t* q8, const float* wfold,
@@ -533,11 +556,12 @@ extern "C" int echo_prefill_scores(int R, int64_t row0, int64_t n_keys, const ui
     if (!q8 || !wfold || !k8 || !ks || !scores || !status) return ECHO_EINVAL;
     if (row0 + R > n_keys || W < row0 + R) return ECHO_EINVAL;
     if (n_keys >= (1ll << 31) || static_cast<int64_t>(R) * W >= (1ll << 40)) return ECHO_EUNSUPPORTED;
-    if (!is_aligned(q8, 16) || !is_aligned(wfold, 16) || !is_aligned(k8, 16)) return ECHO_EINVAL;
-    ScoreArgs args{R, nullptr, n_keys, row0, W, 0, wfold, ks, scores, theta_hat, hist, nullptr, nullptr, status,
-                   nullptr, nullptr, 0};
+    if (!is_aligned(q8, 16) || !is_aligned(wfold, 16) || !is_aligned(k8, 16) || !is_aligned(ks, 16))
+        return ECHO_EINVAL;
+    ScoreArgs args{R, nullptr, n_keys, row0, W, 0, wfold, scores, theta_hat, hist, nullptr, 0, status, nullptr,
+                   nullptr, 0};
     const int64_t tiles_ub = static_cast<int64_t>(R) * ((row0 + R + kTileM - 1) / kTileM);
-    return launch_scores(args, q8, k8, n_keys, tiles_ub, stream);
+    return launch_scores(args, q8, k8, ks, nullptr, n_keys, tiles_ub, stream);
 }
 
 extern "C" size_t echo_above_words(int B, int64_t n_tokens) {
