@@ -28,7 +28,8 @@
 namespace echo {
 namespace {
 
-constexpr int kStages = 8;
+constexpr int kStages = 8;                             // key ring (released when the MMA is done)
+constexpr int kSideStages = 12;                        // side ring (released when the epilogue read it)
 constexpr int kTileM = 128;                            // tokens per tile (MMA M)
 constexpr int kKeyBytes = kTileM * ECHO_DIM;           // 16 KB per key tile
 constexpr int kQBytes = ECHO_HEADS * ECHO_DIM;         // 8 KB q8 per request
@@ -68,10 +69,12 @@ struct ScoreArgs {
 };
 
 struct __align__(128) ScoreCtl {
-    float ks[kStages][kSidePitch];    // per-token key scales of each stage's tile (side box)
-    int32_t res[kStages][kSidePitch]; // per-token cache slot (>= 0: resident) when above is filtered
+    float ks[kSideStages][kSidePitch];    // per-token key scales of each side stage's tile
+    int32_t res[kSideStages][kSidePitch]; // per-token cache slot (>= 0: resident) when above is filtered
     uint64_t full[kStages];
     uint64_t empty[kStages];
+    uint64_t sfull[kSideStages];
+    uint64_t sempty[kSideStages];
     uint64_t qfull[2];
     uint64_t qempty[2];
     uint64_t accfull[kAccBufs];
@@ -176,7 +179,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_addr(&ctl->full[s]), 1);
-            mbar_init(smem_addr(&ctl->empty[s]), 1 + 4);  // MMA done + the tile's 4 epilogue warps read ks
+            mbar_init(smem_addr(&ctl->empty[s]), 1);      // the MMA is done with the keys
+        }
+        for (int s = 0; s < kSideStages; ++s) {
+            mbar_init(smem_addr(&ctl->sfull[s]), 1);
+            mbar_init(smem_addr(&ctl->sempty[s]), 4);     // the tile's 4 epilogue warps read the side boxes
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_addr(&ctl->qfull[i]), 1);
@@ -226,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ntiles > 0 && lane == 0) {
             const uint64_t pol = policy_evict_first();
             const uint32_t prefill = ntiles < static_cast<uint32_t>(kStages) ? ntiles : kStages;
-            const uint32_t stage_tx = kKeyBytes + kSideBytes * (a.has_res ? 2u : 1u);
+            const uint32_t side_tx = kSideBytes * (a.has_res ? 2u : 1u);
             int kb = find_request(tstart, B, t_begin);   // request of the next key load
             int64_t key_lo = 0;
             int kcur = -1;
@@ -239,15 +246,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     key_lo = seg_lo[kb];
                     kcur = kb;
                 }
-                const uint32_t s = it % kStages;
+                const uint32_t s = it % kStages, ss = it % kSideStages;
                 if (!mbar_wait(smem_addr(&ctl->empty[s]), ((it / kStages) & 1) ^ 1, abort)) return false;
+                if (!mbar_wait(smem_addr(&ctl->sempty[ss]), ((it / kSideStages) & 1) ^ 1, abort)) return false;
                 const int64_t tok0 = key_lo + static_cast<int64_t>(t - tstart[kb]) * kTileM;
                 const int32_t x0 = static_cast<int32_t>(tok0 & ~int64_t(3));   // 16-byte aligned box start
-                const uint32_t full = smem_addr(&ctl->full[s]);
-                mbar_arrive_expect_tx(full, stage_tx);
+                const uint32_t full = smem_addr(&ctl->full[s]), sfull = smem_addr(&ctl->sfull[ss]);
+                mbar_arrive_expect_tx(full, kKeyBytes);
                 tma_load_2d_hint(smem_addr(keys + s * kKeyBytes), &kmap, full, 0, static_cast<int32_t>(tok0), pol);
-                tma_load_1d_hint(smem_addr(&ctl->ks[s][0]), &smap, full, x0, pol);
-                if (a.has_res) tma_load_1d_hint(smem_addr(&ctl->res[s][0]), &rmap, full, x0, pol);
+                mbar_arrive_expect_tx(sfull, side_tx);
+                tma_load_1d_hint(smem_addr(&ctl->ks[ss][0]), &smap, sfull, x0, pol);
+                if (a.has_res) tma_load_1d_hint(smem_addr(&ctl->res[ss][0]), &rmap, sfull, x0, pol);
                 return true;
             };
             for (; issued < prefill; ++issued)
@@ -289,6 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Let every copy this thread started land before the CTA exits.
             for (uint32_t j = (issued > kStages ? issued - kStages : 0); j < issued; ++j)
                 mbar_wait(smem_addr(&ctl->full[j % kStages]), (j / kStages) & 1, nullptr);
+            for (uint32_t j = (issued > kSideStages ? issued - kSideStages : 0); j < issued; ++j)
+                mbar_wait(smem_addr(&ctl->sfull[j % kSideStages]), (j / kSideStages) & 1, nullptr);
             for (uint32_t j = (qn > 2 ? qn - 2 : 1); j < qn; ++j)
                 mbar_wait(smem_addr(&ctl->qfull[j & 1]), (j >> 1) & 1, nullptr);
         }
@@ -413,16 +424,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            // the MMA has consumed the stage's keys; read its scales and release it
-            // (waiting on the stage's own barrier orders the cp.async writes before the read)
-            if (!mbar_wait(smem_addr(&ctl->full[it % kStages]), (it / kStages) & 1, abort)) {
+            // the tile's side boxes: read the scales (and slots), then release them
+            const uint32_t ss = it % kSideStages;
+            if (!mbar_wait(smem_addr(&ctl->sfull[ss]), (it / kSideStages) & 1, abort)) {
                 ok = false;
                 break;
             }
-            const float ksv = ctl->ks[it % kStages][row + side];
-            const bool resident = a.has_res && ctl->res[it % kStages][row + side] >= 0;
+            const float ksv = ctl->ks[ss][row + side];
+            const bool resident = a.has_res && ctl->res[ss][row + side] >= 0;
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&ctl->empty[it % kStages]));
+            if (lane == 0) mbar_arrive(smem_addr(&ctl->sempty[ss]));
             uint32_t r0[16], r1[16], r2[16], r3[16];
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * ECHO_HEADS;
             tmem_ld_x16(taddr + 0, r0);

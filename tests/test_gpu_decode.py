@@ -54,6 +54,14 @@ def test_redraw_bursts():
     run_decode(w, 10, predictor=True)
 
 
+def test_early_set_larger_than_one_staging_round():
+    """A query redraw with a large k and cache: one request fetches more than 4096 rows early, so the
+    early fetch stages its (token, slot) pairs in several rounds."""
+    w = wl.scaled(wl.WORKLOADS["skewed"], "rounds", B=2, lengths=(32768, 3000), k=6144, C=16384)
+    rep = run_decode(w, 10, predictor=True, score_sample=2048)
+    assert max(rep["early"]) > 4096, rep["early"]
+
+
 def test_batch_workload_full_size():
     """8 x 32768, k=2048, C=4096: every table/selection bit-exact, scores sampled."""
     w = wl.WORKLOADS["batch"]
