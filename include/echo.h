@@ -161,12 +161,16 @@ int echo_quantize_q(int B, const float* q, const float* w, uint8_t* q8, float* q
  *   its word w is its token 32*w + j; words past its last token hold zeros.
  *   cache (may be NULL; needs above): the layer's cache; its freebits are
  *   also copied to free_snap for echo_early_fetch.
+ *   ctas: CTAs of the score kernel, one per SM at most (<= 0: one per SM).
+ *   Pass fewer when other kernels will hold SMs while this one runs (e.g. the
+ *   early fetch of another group of requests), so that none of its CTAs
+ *   waits for an SM.
  */
 size_t echo_above_words(int B, int64_t n_tokens);
 int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens, const uint8_t* q8,
                       const float* wfold, const uint8_t* k8, const float* ks, float* scores,
                       const float* theta_hat, uint32_t* hist, uint32_t* above,
-                      const echo_cache* cache, int32_t* status, echo_stream_t stream);
+                      const echo_cache* cache, int ctas, int32_t* status, echo_stream_t stream);
 
 /*
  * Early fetch [EXPL panel "Decode: fetch above a predicted threshold"], the

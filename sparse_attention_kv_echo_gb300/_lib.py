@@ -21,6 +21,7 @@ ST_TIMEOUT, ST_NAN, ST_NOSLOT, ST_BADDATA = 0x1, 0x2, 0x4, 0x8
 STAT_TOPK_FALLBACK, STAT_BOUNDARY_MAX, STAT_EARLY, STAT_MISSES, STAT_EARLY_USED = 0, 1, 2, 3, 4
 STATS_N = 8
 HEADS, DIM, MAX_REQUESTS = 64, 128, 4096
+EARLY_FETCH_BLOCKS = 32      # CTAs of the early-fetch and late-recall kernels
 
 EXPORTS = ("echo_above_words", "echo_cache_step", "echo_device_sm_count", "echo_early_fetch",
            "echo_host_device_alias", "echo_index_scores", "echo_prefill_block", "echo_prefill_block_static",
@@ -70,7 +71,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         L.echo_above_words.argtypes = [i32, i64]
         L.echo_index_scores.restype = i32
         L.echo_index_scores.argtypes = [i32, _vp, i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
-                                        ctypes.POINTER(EchoCacheStruct), _vp, _vp]
+                                        ctypes.POINTER(EchoCacheStruct), i32, _vp, _vp]
         L.echo_early_fetch.restype = i32
         L.echo_early_fetch.argtypes = [i32, _vp, i64, _vp, i32, ctypes.POINTER(EchoCacheStruct), _vp, _vp]
         L.echo_topk_select.restype = i32
@@ -140,14 +141,14 @@ def above_words(B: int, n_tokens: int) -> int:
 
 
 def index_scores(tok_off, n_tokens, q8, wfold, k8, ks, scores, theta_hat, hist, status, above=None,
-                 cache=None, stream=None):
+                 cache=None, stream=None, ctas=0):
     """echo_index_scores; cache: a LayerCache whose residents `above` leaves out (and whose free bits
     are snapshotted for early_fetch)."""
     B = q8.shape[0]
     _check("echo_index_scores", load().echo_index_scores(
         B, _ptr(tok_off), int(n_tokens), _ptr(q8), _ptr(wfold), _ptr(k8), _ptr(ks), _ptr(scores),
         _ptr(theta_hat), _ptr(hist), _ptr(above), ctypes.byref(cache.struct) if cache is not None else None,
-        _ptr(status), _stream(stream)))
+        int(ctas), _ptr(status), _stream(stream)))
 
 
 def early_fetch(tok_off, n_tokens, above, early_cap, cache, status, stream=None):
@@ -249,9 +250,34 @@ class LayerCache:
         s.row_bytes, s.C, s.reserved = self.row_bytes, C, 0
         self.struct = s
 
+    def view(self, b0: int, b1: int) -> "CacheView":
+        """The tables of requests [b0, b1) as a cache of b1 - b0 requests (shared storage)."""
+        return CacheView(self, b0, b1)
+
     def reset(self):
         self.tok2slot.fill_(-1)
         self.slot2tok.fill_(-1)
         self.freebits.fill_(-1)
         self.miss_cnt.zero_()
         self.early_cnt.zero_()
+
+
+class CacheView:
+    """Requests [b0, b1) of a LayerCache: per-request arrays offset to b0, tok2slot and the host
+    pool shared (token rows are global).  Holds the parent so its storage stays alive."""
+
+    def __init__(self, parent: LayerCache, b0: int, b1: int):
+        self.parent, self.b0, self.b1 = parent, int(b0), int(b1)
+        C, words = parent.C, parent.C // 32
+        s = EchoCacheStruct()
+        s.tok2slot = _ptr(parent.tok2slot)
+        s.slot2tok = _ptr(parent.slot2tok[b0 * C:])
+        s.freebits = _ptr(parent.freebits[b0 * words:])
+        s.miss_tok, s.miss_slot = _ptr(parent.miss_tok[b0 * C:]), _ptr(parent.miss_slot[b0 * C:])
+        s.miss_cnt = _ptr(parent.miss_cnt[b0:])
+        s.early_tok, s.early_slot = _ptr(parent.early_tok[b0 * C:]), _ptr(parent.early_slot[b0 * C:])
+        s.early_cnt = _ptr(parent.early_cnt[b0:])
+        s.free_snap = _ptr(parent.free_snap[b0 * words:])
+        s.host_kv, s.dev_kv = parent.host_alias, _ptr(parent.dev_kv[b0 * C:])
+        s.row_bytes, s.C, s.reserved = parent.row_bytes, C, 0
+        self.struct = s

@@ -55,12 +55,36 @@ constexpr int kPer = 4;        // selection entries per thread per chunk
 constexpr int kEarlyWordsStep = 1;
 constexpr int kEarlyWordsFetch = 2;
 
+constexpr int kES = 4096;  // early (token, slot) pairs kept in shared memory for the table phases
+
+// Shared memory of the cache-step kernel, in 32-bit words.
+__host__ __device__ constexpr size_t cache_step_smem_words(int C) {
+    return 3 * static_cast<size_t>(C / 32) + 1 + 2 * static_cast<size_t>(kES);
+}
+
+// Binary search of v in the ascending a[0, n); -1 when absent.
+__device__ __forceinline__ int find_sorted(const int32_t* a, int n, int32_t v) {
+    int lo = 0, hi = n - 1;
+    while (lo <= hi) {
+        const int mid = (lo + hi) >> 1;
+        const int32_t x = a[mid];
+        if (x == v) return mid;
+        if (x < v)
+            lo = mid + 1;
+        else
+            hi = mid - 1;
+    }
+    return -1;
+}
+
 __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restrict__ tok_off, int64_t n_tokens,
                                                          const int32_t* __restrict__ sel, int m,
                                                          const uint32_t* __restrict__ above, int early_cap,
                                                          CacheArgs c, int32_t* __restrict__ sel_slot, int32_t* status,
                                                          uint32_t* stats) {
-    extern __shared__ uint32_t keep[];  // keep [words]: a selected token lives in the slot; then wpre, fbs
+    // keep [words]: a selected token lives in the slot | wpre [words + 1] | fbs [words] (free bits)
+    // | es_tok [kES] | es_slot [kES] (the early pairs, both ascending)
+    extern __shared__ uint32_t keep[];
     __shared__ uint32_t scan[40];
     __shared__ uint32_t s_flags, s_early_used;
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -78,13 +102,18 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
     int32_t* eslot = c.early_slot + static_cast<int64_t>(b) * C;
     uint32_t* wpre = keep + words;
     uint32_t* fbs = wpre + words + 1;
+    int32_t* es_tok = reinterpret_cast<int32_t*>(fbs + words);
+    int32_t* es_slot = es_tok + kES;
     constexpr int kChunk = kCT * kPer;
     const int chunks = (m + kChunk - 1) / kChunk;
     const bool early = above != nullptr && early_cap != 0 && n > 0;
 
-    // Loads that depend on nothing else go out together: this thread's
-    // selection entries (kPer consecutive ones, so its misses have consecutive
-    // ranks), the free-bit words, and its first above-threshold words.
+    // Global latency is what this kernel costs (it runs while the early rows
+    // stream over the host link), so the loads go out in two rounds and every
+    // later phase works from registers and shared memory.  Round 1: this
+    // thread's selection entries (kPer consecutive ones, so its misses have
+    // consecutive ranks) and the one after them, the slot owners and free-bit
+    // words, the first above-threshold words.
     int32_t s[kPer], j[kPer];
     auto load_sel = [&](int c0) {
 #pragma unroll
@@ -94,6 +123,15 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
         }
     };
     load_sel(0);
+    int32_t after0 = (kPer * tid + kPer < m) ? sl[kPer * tid + kPer] : -1;
+    constexpr int kPre = 4;  // 32-slot words per warp held in registers
+    const bool pre = words <= kPre * (kCT / 32);
+    int32_t own[kPre];
+#pragma unroll
+    for (int r = 0; r < kPre; ++r) {
+        const int w = warp + r * (kCT / 32);
+        own[r] = (pre && w < words) ? s2t[w * 32 + lane] : -1;
+    }
     const uint32_t* ab = early ? above + 4 * (base / 128 + b) : nullptr;
     const int nw = static_cast<int>((n + 31) >> 5);
     const uint32_t tail_mask = (n & 31) ? (1u << (n & 31)) - 1u : ~0u;
@@ -107,6 +145,11 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
         s_flags = 0;
         s_early_used = 0;
     }
+    // Round 2: the slots of the selected tokens as the step found them.
+    if (chunks == 1) {
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) j[q] = (s[q] >= 0 && s[q] < n) ? t2s[s[q]] : -1;
+    }
     __syncthreads();
 
     // 0. the early set (the tokens echo_early_fetch copied) becomes resident
@@ -117,7 +160,7 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
         const uint32_t found = early_assign<kCT, kEarlyWordsStep>(
             ab, nw, tail_mask, limit, 0u, limit, wpre, fbs, words, scan, v, [&](uint32_t r, int tok, int slot) {
                 // the marked tokens are not resident (the score kernel filtered them against these
-                // tables), so the tables are only written here, never read: no load on this path
+                // tables), so the tables are only written here, never read
                 if (slot < 0) {
                     set_status(status, ECHO_ST_BADDATA);
                     return;
@@ -126,35 +169,48 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
                 eslot[r] = slot;
                 t2s[tok] = slot;
                 s2t[slot] = tok;
+                if (r < static_cast<uint32_t>(kES)) {
+                    es_tok[r] = tok;
+                    es_slot[r] = slot;
+                }
             });
         E = min(found, limit);
         __syncthreads();  // every walk over fbs is done before its bits change
         take_lowest_free<kCT>(fbs, words, E, wpre);
         __syncthreads();
     }
+    // With every early pair in shared memory, the values read before the early
+    // phase are corrected from there; otherwise the tables are read again
+    // (this block's own writes, visible after the barrier).
+    const bool es_ok = E <= static_cast<uint32_t>(kES);
 
     // 1a. slots that hold a selected token are kept; the selection must be
     // ascending with -1 padding last
-    auto resident_slots = [&](int c0) -> uint32_t {
-        const int inext = c0 + kPer * tid + kPer;
-        const int32_t after = (inext < m) ? sl[inext] : -1;
+    for (int ch = 0; ch < chunks; ++ch) {
+        const int c0 = ch * kChunk;
+        int32_t after = after0;
+        if (chunks > 1) {
+            load_sel(c0);
+            const int inext = c0 + kPer * tid + kPer;
+            after = (inext < m) ? sl[inext] : -1;
+        }
         uint32_t flags = 0;
 #pragma unroll
         for (int q = 0; q < kPer; ++q) {
             const int32_t nxt = (q + 1 < kPer) ? s[q + 1] : after;
             if (s[q] >= 0 && s[q] < n) {
                 if (nxt >= 0 && nxt <= s[q]) flags |= ECHO_ST_BADDATA;
-                j[q] = t2s[s[q]];
+                if (chunks > 1 || !es_ok) {
+                    j[q] = t2s[s[q]];
+                } else if (E > 0 && j[q] < 0) {
+                    const int e = find_sorted(es_tok, static_cast<int>(E), s[q]);
+                    if (e >= 0) j[q] = es_slot[e];
+                }
             } else {
                 j[q] = -1;
                 if (s[q] >= 0 || nxt >= 0) flags |= ECHO_ST_BADDATA;
             }
         }
-        return flags;
-    };
-    for (int ch = 0; ch < chunks; ++ch) {
-        if (ch > 0) load_sel(ch * kChunk);
-        const uint32_t flags = resident_slots(ch * kChunk);
         if (flags) atomicOr(&s_flags, flags);
 #pragma unroll
         for (int q = 0; q < kPer; ++q)
@@ -163,10 +219,9 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
     __syncthreads();
 
     // 1b. every other occupied slot is freed (bytes stay, nothing is written
-    // back), one warp per 32-slot word
-    for (int w = warp; w < words; w += kCT / 32) {
+    // back), one warp per 32-slot word; the new free-bit words stay in shared memory
+    auto free_word = [&](int w, int32_t st) {
         const int slot = w * 32 + lane;
-        const int32_t st = s2t[slot];
         const bool kept = (keep[w] >> lane) & 1u;
         const bool freeing = st >= 0 && !kept;
         if (freeing) {
@@ -175,11 +230,26 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
         }
         const unsigned fm = __ballot_sync(0xffffffffu, freeing);
         if (lane == 0) fbs[w] |= fm;
+    };
+    if (pre && es_ok) {
+#pragma unroll
+        for (int r = 0; r < kPre; ++r) {
+            const int w = warp + r * (kCT / 32);
+            if (w >= words) continue;
+            int32_t st = own[r];
+            if (st < 0 && E > 0) {  // a slot the early set took this step
+                const int e = find_sorted(es_slot, static_cast<int>(E), w * 32 + lane);
+                if (e >= 0) st = es_tok[e];
+            }
+            free_word(w, st);
+        }
+    } else {
+        for (int w = warp; w < words; w += kCT / 32) free_word(w, s2t[w * 32 + lane]);
     }
     // early fetches of this step that the selection kept (their slot is kept)
     uint32_t used = 0;
     for (uint32_t e = tid; e < E; e += kCT) {
-        const int32_t es = eslot[e];
+        const int32_t es = es_ok ? es_slot[e] : eslot[e];
         if (es >= 0 && es < C && ((keep[es >> 5] >> (es & 31)) & 1u)) ++used;
     }
     if (used) atomicAdd(&s_early_used, used);
@@ -451,7 +521,7 @@ namespace echo {
 int enqueue_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
                        const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,
                        int32_t* status, uint32_t* stats, cudaStream_t stream, cudaStream_t copy_stream) {
-    const size_t smem = (3 * static_cast<size_t>(cache->C / 32) + 1) * sizeof(uint32_t);
+    const size_t smem = cache_step_smem_words(cache->C) * sizeof(uint32_t);
     ECHO_CUDA_OK(prefer_max_shared(cache_step_kernel));
     ECHO_CUDA_OK(cudaFuncSetAttribute(cache_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(smem)));

@@ -494,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 static int launch_scores(const ScoreArgs& args, const uint8_t* q8, const uint8_t* k8, const float* ks,
-                  const int32_t* tok2slot, int64_t key_rows, int64_t tiles_ub, cudaStream_t stream) {
+                  const int32_t* tok2slot, int64_t key_rows, int64_t tiles_ub, int ctas, cudaStream_t stream) {
     CUtensorMap kmap, qmap, smap, rmap;
     int rc = encode_tmap_bytes_2d(&kmap, k8, ECHO_DIM, static_cast<uint64_t>(key_rows), ECHO_DIM, kTileM);
     if (rc) return rc;
@@ -508,7 +508,8 @@ static int launch_scores(const ScoreArgs& args, const uint8_t* q8, const uint8_t
     if (rc) return rc;
     const int sms = sm_count();
     if (sms <= 0) return ECHO_ECUDA;
-    const int grid = static_cast<int>(tiles_ub < sms ? tiles_ub : sms);
+    const int most = (ctas > 0 && ctas < sms) ? ctas : sms;
+    const int grid = static_cast<int>(tiles_ub < most ? tiles_ub : most);
     const size_t smem = smem_bytes(args.B);
     ECHO_CUDA_OK(prefer_max_shared(score_kernel));
     ECHO_CUDA_OK(cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -534,7 +535,7 @@ static int launch_scores(const ScoreArgs& args, const uint8_t* q8, const uint8_t
 extern "C" int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens, const uint8_t* q8,
                                  const float* wfold, const uint8_t* k8, const float* ks, float* scores,
                                  const float* theta_hat, uint32_t* hist, uint32_t* above, const echo_cache* cache,
-                                 int32_t* status, echo_stream_t stream) {
+                                 int ctas, int32_t* status, echo_stream_t stream) {
     using namespace echo;
     if (B <= 0 || n_tokens < 0) return ECHO_EINVAL;
     if (B > ECHO_MAX_REQUESTS) return ECHO_EUNSUPPORTED;
@@ -554,7 +555,7 @@ extern "C" int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens
                    cache ? 1 : 0, status, cache ? cache->freebits : nullptr,
                    cache ? cache->free_snap : nullptr,
                    cache ? static_cast<int64_t>(B) * (cache->C / 32) : 0};
-    return launch_scores(args, q8, k8, ks, cache ? cache->tok2slot : nullptr, n_tokens, n_tokens / kTileM + B,
+    return launch_scores(args, q8, k8, ks, cache ? cache->tok2slot : nullptr, n_tokens, n_tokens / kTileM + B, ctas,
                          stream);
 }
 
@@ -572,7 +573,7 @@ extern "C" int echo_prefill_scores(int R, int64_t row0, int64_t n_keys, const ui
     ScoreArgs args{R, nullptr, n_keys, row0, W, 0, wfold, scores, theta_hat, hist, nullptr, 0, status, nullptr,
                    nullptr, 0};
     const int64_t tiles_ub = static_cast<int64_t>(R) * ((row0 + R + kTileM - 1) / kTileM);
-    return launch_scores(args, q8, k8, ks, nullptr, n_keys, tiles_ub, stream);
+    return launch_scores(args, q8, k8, ks, nullptr, n_keys, tiles_ub, 0, stream);
 }
 
 extern "C" size_t echo_above_words(int B, int64_t n_tokens) {

@@ -92,6 +92,10 @@ template <int NT>
 __device__ void take_lowest_free(uint32_t* fbs, int words, uint32_t take, const uint32_t* wpre) {
     for (int w = threadIdx.x; w < words; w += NT) {
         if (wpre[w] >= take) continue;
+        if (wpre[w + 1] <= take) {  // every free slot of the word is taken
+            fbs[w] = 0u;
+            continue;
+        }
         uint32_t f = fbs[w];
         uint32_t k = take - wpre[w];
         uint32_t taken = 0;

@@ -28,7 +28,7 @@ from . import _lib as L
 class DecodeLayer:
     def __init__(self, tok_off, k8: torch.Tensor, ks: torch.Tensor, k: int, C: int,
                  host_pool: torch.Tensor, alpha: float = 0.5, predictor: bool = True,
-                 early_cap: int = -1, device="cuda"):
+                 early_cap: int = -1, groups: int | None = None, device="cuda"):
         tok_off = torch.as_tensor(tok_off, dtype=torch.int64)
         self.B = int(tok_off.numel() - 1)
         self.n_tokens = int(k8.shape[0])
@@ -44,7 +44,16 @@ class DecodeLayer:
         self.sel_idx = torch.full((self.B, self.k), -1, **i32)
         self.sel_slot = torch.full((self.B, self.k), -1, **i32)
         self.kth = torch.zeros((self.B,), **f32)
-        self.above = torch.zeros(max(L.above_words(self.B, self.n_tokens), 1), **i32)
+        # Requests are scored in groups (contiguous request ranges): the early fetch of group g
+        # streams over the host link while group g+1 is scored, so the link starts sooner.
+        if groups is None:
+            groups = 2 if (self.predictor and self.B >= 2) else 1
+        groups = max(1, min(int(groups), self.B))
+        bounds = [self.B * g // groups for g in range(groups + 1)]
+        self.groups = [(bounds[g], bounds[g + 1]) for g in range(groups) if bounds[g + 1] > bounds[g]]
+        # each group's above-threshold words: the groups' word ranges may overlap
+        self.above_g = [torch.zeros(max(L.above_words(b1 - b0, self.n_tokens), 1), **i32)
+                        for b0, b1 in self.groups]
         self.q8 = torch.zeros((self.B, L.HEADS, L.DIM), dtype=torch.uint8, device=device)
         self.qscale = torch.zeros((self.B, L.HEADS), **f32)
         self.wfold = torch.zeros((self.B, L.HEADS), **f32)
@@ -53,7 +62,13 @@ class DecodeLayer:
         self.q_in = torch.zeros((self.B, L.HEADS, L.DIM), **f32)
         self.w_in = torch.zeros((self.B, L.HEADS), **f32)
         self.cache = L.LayerCache(self.B, self.n_tokens, self.C, host_pool, device=device)
-        self.side = torch.cuda.Stream(device=device)
+        self.views = [self.cache.view(b0, b1) for b0, b1 in self.groups]
+        self.sides = [torch.cuda.Stream(device=device) for _ in self.groups]
+        self.side = self.sides[0]
+        # scoring streams of the groups after the first (the first uses the step's stream);
+        # low priority, so the early fetch of the group before is placed first
+        lo, _ = torch.cuda.Stream.priority_range()
+        self.gstreams = [torch.cuda.Stream(device=device, priority=lo) for _ in self.groups[1:]]
 
     def reset(self):
         self.cache.reset()
@@ -69,25 +84,51 @@ class DecodeLayer:
         q = self.q_in if q is None else q
         w = self.w_in if w is None else w
         main = torch.cuda.current_stream() if stream is None else stream
-        above = self.above if self.predictor else None
         L.quantize_q(q, w, self.q8, self.qscale, self.wfold, self.status, hist=self.hist, stream=main)
-        L.index_scores(self.tok_off, self.n_tokens, self.q8, self.wfold, self.k8, self.ks, self.scores,
-                       self.theta, self.hist, self.status, above=above,
-                       cache=self.cache if self.predictor else None, stream=main)
-        if self.predictor:
-            # the early rows stream over the host link on `main` while top-k and
-            # the table update run on the side stream
-            self.side.wait_stream(main)
-            L.early_fetch(self.tok_off, self.n_tokens, self.above, self.early_cap, self.cache, self.status,
-                          stream=main)
-            work = self.side
-        else:
-            work = main
-        L.topk_select(self.tok_off, self.n_tokens, self.scores, self.k, self.hist, self.theta, self.alpha,
-                      self.sel_idx, self.kth, self.status, stats=self.stats, stream=work)
-        L.cache_step(self.tok_off, self.n_tokens, self.sel_idx, self.cache, self.sel_slot, self.status,
-                     stats=self.stats, stream=work, copy_stream=main, above=above, early_cap=self.early_cap)
+        if not self.predictor:
+            L.index_scores(self.tok_off, self.n_tokens, self.q8, self.wfold, self.k8, self.ks, self.scores,
+                           self.theta, self.hist, self.status, stream=main)
+            L.topk_select(self.tok_off, self.n_tokens, self.scores, self.k, self.hist, self.theta, self.alpha,
+                          self.sel_idx, self.kth, self.status, stats=self.stats, stream=main)
+            L.cache_step(self.tok_off, self.n_tokens, self.sel_idx, self.cache, self.sel_slot, self.status,
+                         stats=self.stats, stream=main, copy_stream=main)
+            return
+        sms = torch.cuda.get_device_properties(main.device).multi_processor_count
+        streams, scored = [], None
+        for g, (b0, b1) in enumerate(self.groups):
+            s = main if g == 0 else self.gstreams[g - 1]
+            if scored is not None:
+                s.wait_event(scored)           # after the previous group's scores
+            # while a group's early fetch holds its SMs, the next group's score kernel leaves them
+            ctas = 0 if g == 0 else sms - L.EARLY_FETCH_BLOCKS
+            L.index_scores(self.tok_off[b0:b1 + 1], self.n_tokens, self.q8[b0:b1], self.wfold[b0:b1], self.k8,
+                           self.ks, self.scores, self.theta[b0:b1], self.hist[b0:b1], self.status,
+                           above=self.above_g[g], cache=self.views[g], stream=s, ctas=ctas)
+            scored = torch.cuda.Event()
+            scored.record(s)
+            streams.append(s)
+            # the group's early rows stream over the host link on `s` (programmatic dependent of its
+            # score kernel) while the next group is scored
+            L.early_fetch(self.tok_off[b0:b1 + 1], self.n_tokens, self.above_g[g], self.early_cap, self.views[g],
+                          self.status, stream=s)
+        # top-k and the table update of every group on the groups' side streams once all scores are
+        # done (a top-k started earlier would take SMs the next score kernel counts on); the late
+        # misses of a group follow its early fetch on its stream
+        for g, (b0, b1) in enumerate(self.groups):
+            side, s = self.sides[g], streams[g]
+            side.wait_event(scored)
+            off = self.tok_off[b0:b1 + 1]
+            L.topk_select(off, self.n_tokens, self.scores, self.k, self.hist[b0:b1], self.theta[b0:b1],
+                          self.alpha, self.sel_idx[b0:b1], self.kth[b0:b1], self.status, stats=self.stats,
+                          stream=side)
+            L.cache_step(off, self.n_tokens, self.sel_idx[b0:b1], self.views[g], self.sel_slot[b0:b1], self.status,
+                         stats=self.stats, stream=side, copy_stream=s, above=self.above_g[g],
+                         early_cap=self.early_cap)
+        for gs in self.gstreams:
+            main.wait_stream(gs)
 
     def kernel_launches_per_step(self) -> int:
-        # quantize + score (+ early fetch) + top-k + cache step + late recall
-        return 2 + (1 if self.predictor else 0) + 1 + 2
+        # quantize, then per group: score (+ early fetch) + top-k + cache step + late recall
+        if not self.predictor:
+            return 5
+        return 1 + 5 * len(self.groups)

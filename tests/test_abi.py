@@ -51,9 +51,11 @@ def test_host_checks_reject_bad_arguments(L):
     from sparse_attention_kv_echo_gb300 import lib
     v = ctypes.c_void_p
     dummy = v(0x1000)
-    # index_scores(B, tok_off, n_tokens, q8, wfold, k8, ks, scores, theta, hist, above, cache, status, stream)
+    # index_scores(B, tok_off, n_tokens, q8, wfold, k8, ks, scores, theta, hist, above, cache, ctas, status,
+    #              stream)
     def scores_call(B=1, n=10, q8=dummy, k8=dummy, above=None, cache=None):
-        return L.echo_index_scores(B, dummy, n, q8, dummy, k8, dummy, dummy, None, None, above, cache, dummy, None)
+        return L.echo_index_scores(B, dummy, n, q8, dummy, k8, dummy, dummy, None, None, above, cache, 0, dummy,
+                                   None)
     assert scores_call(B=0) == lib.ECHO_EINVAL
     assert scores_call(B=lib.MAX_REQUESTS + 1) == lib.ECHO_EUNSUPPORTED
     assert scores_call(q8=None) == lib.ECHO_EINVAL                     # missing q8
