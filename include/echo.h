@@ -179,9 +179,10 @@ int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens, const uin
  * not resident), in ascending order, at most min(early_cap, free slots) of
  * them (early_cap < 0: no cap but the free slots); they take the lowest free
  * slots in ascending order (free as in cache->free_snap).  This call copies
- * their rows host_kv[tok_off[b] + t] -> dev_kv[b*C + slot] and writes nothing
- * else: the tables learn the early set in echo_cache_step (given the same
- * above and early_cap), which may therefore run concurrently with this copy.
+ * their rows host_kv[tok_off[b] + t] -> dev_kv[b*C + slot] and lists them in
+ * early_tok / early_slot (ranks 0 .. E-1); it touches no table: the tables
+ * learn the early set in echo_cache_step (given the same above and
+ * early_cap), which may therefore run concurrently with this copy.
  * Enqueue it on the stream of echo_index_scores right after it: it is
  * launched as a programmatic dependent of the score kernel.  It reads neither
  * the scores nor the threshold, so echo_topk_select may run on another stream
@@ -219,8 +220,8 @@ int echo_topk_select(int B, const int64_t* tok_off, int64_t n_tokens, const floa
  * (ascending request-local tokens, -1 padded):
  *   0. with above (may be NULL: no early fetch this step), the early set of
  *      echo_early_fetch (same above and early_cap) becomes resident in the
- *      slots that call copied it to; early_tok / early_slot / early_cnt list
- *      it (early_cnt = 0 without above);
+ *      slots that call copied it to, and early_cnt[b] = its size E (0
+ *      without above);
  *   1. every resident token that is not selected is freed (both table
  *      entries -1, its free bit set); its bytes stay, nothing is written back;
  *   2. the selected tokens that are not resident (the misses), in ascending
