@@ -53,6 +53,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-budget-s", type=float, default=10.0,
                    help="seconds of oracle work for the CPU baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--groups", type=int, default=None,
+                   help="request groups of the decode step (default: the layer's choice)")
     return p.parse_args(argv)
 
 
@@ -225,7 +227,7 @@ def run_ours(args):
     qsrc = wl.QueryStream(w, 0, device=dev)
     q_all = torch.stack([qsrc.next() for _ in range(w.steps)])
     S = q_all.shape[0]
-    lay = DecodeLayer(off, k8, ks, w.k, w.C, host, device=dev)
+    lay = DecodeLayer(off, k8, ks, w.k, w.C, host, device=dev, groups=args.groups)
     main = torch.cuda.Stream()
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 

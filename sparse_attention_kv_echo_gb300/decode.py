@@ -100,7 +100,8 @@ class DecodeLayer:
             if scored is not None:
                 s.wait_event(scored)           # after the previous group's scores
             # while a group's early fetch holds its SMs, the next group's score kernel leaves them
-            ctas = 0 if g == 0 else sms - L.EARLY_FETCH_BLOCKS
+            # (every earlier group's early fetch may still be copying)
+            ctas = 0 if g == 0 else max(sms - L.EARLY_FETCH_BLOCKS * g, sms // 4)
             L.index_scores(self.tok_off[b0:b1 + 1], self.n_tokens, self.q8[b0:b1], self.wfold[b0:b1], self.k8,
                            self.ks, self.scores, self.theta[b0:b1], self.hist[b0:b1], self.status,
                            above=self.above_g[g], cache=self.views[g], stream=s, ctas=ctas)
