@@ -27,6 +27,7 @@
 #include "echo_common.cuh"
 #include "echo_internal.h"
 #include "echo_slots.cuh"
+#include "echo_cachestep.cuh"
 
 namespace echo {
 namespace {
@@ -78,275 +79,25 @@ __device__ __forceinline__ int find_sorted(const int32_t* a, int n, int32_t v) {
 }
 
 // ---------------------------------------------------------------- cache step, look-up form
-// The early fetch already copied the early set's rows and wrote its lists; this
-// kernel needs only the selected tokens among it.  A selected token s that is
-// not resident is early iff its above-threshold bit is set and its rank r among
-// the marked tokens (a prefix of popcounts over the above words) is below E; its
-// slot is then the r-th free slot of the step's starting free bits.  So the
-// early set is never walked here: one scan over the above words, one over the
-// free bits, O(1) work per selected token.  Used when C <= kLookupMaxSlots.
+// (echo_cachestep.cuh): the early set is found by rank look-ups, not walked.
+// Used when C <= kLookupMaxSlots.
 constexpr int kAWC = 8192;                 // above words per chunk held in shared memory
 constexpr int kLookupMaxSlots = 1 << 17;   // 4 x 4096 words + the chunk fit shared memory
-
-__host__ __device__ constexpr size_t lookup_smem_words(int C) {
-    return 4 * static_cast<size_t>(C / 32) + 1 + 2 * static_cast<size_t>(kAWC) + 1;
-}
 
 __global__ void __launch_bounds__(kCT)
     cache_step_lookup_kernel(const int64_t* __restrict__ tok_off, int64_t n_tokens, const int32_t* __restrict__ sel,
                              int m, const uint32_t* __restrict__ above, int early_cap, CacheArgs c,
                              int32_t* __restrict__ sel_slot, int32_t* status, uint32_t* stats) {
-    // keep [words] | wpre [words + 1] | fbs [words] | etaken [words] | aw [kAWC] | apre [kAWC + 1]
-    extern __shared__ uint32_t keep[];
+    extern __shared__ uint32_t smem[];
     __shared__ uint32_t scan[40];
-    __shared__ uint32_t s_flags, s_early_used;
-    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    int64_t base, n;
-    if (!request_range(tok_off, n_tokens, b, &base, &n) && tid == 0) set_status(status, ECHO_ST_BADDATA);
-    const int C = c.C, words = C / 32;
-    int32_t* t2s = c.tok2slot + base;
-    int32_t* s2t = c.slot2tok + static_cast<int64_t>(b) * C;
-    uint32_t* fb = c.freebits + static_cast<int64_t>(b) * words;
-    const int32_t* sl = sel + static_cast<int64_t>(b) * m;
-    int32_t* out = sel_slot + static_cast<int64_t>(b) * m;
-    int32_t* mtok = c.miss_tok + static_cast<int64_t>(b) * C;
-    int32_t* mslot = c.miss_slot + static_cast<int64_t>(b) * C;
-    uint32_t* wpre = keep + words;
-    uint32_t* fbs = wpre + words + 1;
-    uint32_t* etaken = fbs + words;
-    uint32_t* aw = etaken + words;
-    uint32_t* apre = aw + kAWC;
-    constexpr int kChunk = kCT * kPer;
-    const int chunks = (m + kChunk - 1) / kChunk;
-    const bool early = above != nullptr && early_cap != 0 && n > 0;
-    const uint32_t* ab = early ? above + 4 * (base / 128 + b) : nullptr;
-    const int nw = early ? static_cast<int>((n + 31) >> 5) : 0;
-    const uint32_t tail_mask = (n & 31) ? (1u << (n & 31)) - 1u : ~0u;
-    auto above_word = [&](int w) -> uint32_t {
-        const uint32_t x = __ldcg(ab + w);
-        return (w == nw - 1) ? (x & tail_mask) : x;
-    };
-
-    // Round 1 of loads: selection entries (kPer consecutive ones per thread)
-    // and the one after them, slot owners, free bits, the first above words.
-    int32_t s[kPer], j[kPer];
-    auto load_sel = [&](int c0) {
-#pragma unroll
-        for (int q = 0; q < kPer; ++q) {
-            const int i = c0 + kPer * tid + q;
-            s[q] = (i < m) ? sl[i] : -1;
-        }
-    };
-    load_sel(0);
-    const int32_t after0 = (kPer * tid + kPer < m) ? sl[kPer * tid + kPer] : -1;
-    constexpr int kPre = 4;  // 32-slot words per warp held in registers
-    const bool pre = words <= kPre * (kCT / 32);
-    int32_t own[kPre];
-#pragma unroll
-    for (int r = 0; r < kPre; ++r) {
-        const int w = warp + r * (kCT / 32);
-        own[r] = (pre && w < words) ? s2t[w * 32 + lane] : -1;
-    }
-    for (int w = tid; w < words; w += kCT) {
-        fbs[w] = fb[w];
-        keep[w] = 0u;
-        etaken[w] = 0u;
-    }
-    for (int w = tid; w < min(nw, kAWC); w += kCT) aw[w] = above_word(w);
-    if (tid == 0) {
-        s_flags = 0;
-        s_early_used = 0;
-    }
-    // Round 2: the slots of the selected tokens as the step found them.
-    if (chunks == 1) {
-#pragma unroll
-        for (int q = 0; q < kPer; ++q) j[q] = (s[q] >= 0 && s[q] < n) ? t2s[s[q]] : -1;
-    }
-    __syncthreads();
-
-    // The early set: the marked tokens of rank < limit took the lowest free
-    // slots of the starting free bits (wpre/fbs, untouched until the lookups end).
-    uint32_t limit = 0, A = 0, used = 0;
-    if (early) {
-        const uint32_t F0 = free_prefix<kCT>(fbs, words, scan, wpre, fbs);
-        limit = (early_cap < 0) ? F0 : min(F0, static_cast<uint32_t>(early_cap));
-    }
-    auto lookup = [&](int32_t sv, int32_t jv, int k0) -> int32_t {
-        if (sv < 0 || sv >= n || jv >= 0) return jv;
-        const int w = sv >> 5;
-        if (w < k0 || w >= k0 + kAWC) return jv;
-        const uint32_t word = aw[w - k0];
-        const int bit = sv & 31;
-        if (!((word >> bit) & 1u)) return jv;
-        const uint32_t r = apre[w - k0] + __popc(word & ((1u << bit) - 1u));
-        if (r >= limit) return jv;
-        FreeWalk walk(wpre, fbs, words, r);
-        const int slot = walk.next();
-        if (slot < 0) {
-            set_status(status, ECHO_ST_BADDATA);
-            return jv;
-        }
-        t2s[sv] = slot;
-        s2t[slot] = sv;
-        atomicOr(&etaken[slot >> 5], 1u << (slot & 31));
-        ++used;
-        return slot;
-    };
-    for (int k0 = 0; k0 < nw; k0 += kAWC) {
-        const int len = min(kAWC, nw - k0);
-        if (k0 > 0) {
-            __syncthreads();  // the previous chunk's look-ups are done
-            for (int w = tid; w < len; w += kCT) aw[w] = above_word(k0 + w);
-            __syncthreads();
-        }
-        // prefix of the chunk's popcounts: each thread sums `per` consecutive words
-        const int per = (len + kCT - 1) / kCT;
-        uint32_t local = 0;
-        for (int i = 0; i < per; ++i) {
-            const int w = tid * per + i;
-            if (w < len) local += __popc(aw[w]);
-        }
-        uint32_t tot;
-        uint32_t run = A + block_exclusive_scan<kCT>(local, scan, &tot);
-        for (int i = 0; i < per; ++i) {
-            const int w = tid * per + i;
-            if (w < len) {
-                apre[w] = run;
-                run += __popc(aw[w]);
-            }
-        }
-        A += tot;
-        __syncthreads();
-        if (chunks == 1) {
-#pragma unroll
-            for (int q = 0; q < kPer; ++q) j[q] = lookup(s[q], j[q], k0);
-        } else {
-            for (int ch = 0; ch < chunks; ++ch) {
-                load_sel(ch * kChunk);
-#pragma unroll
-                for (int q = 0; q < kPer; ++q) lookup(s[q], (s[q] >= 0 && s[q] < n) ? t2s[s[q]] : -1, k0);
-            }
-        }
-    }
-    const uint32_t E = min(A, limit);
-    if (used) atomicAdd(&s_early_used, used);
-    __syncthreads();
-    // the selected early tokens keep their slots; the rest of the early set is
-    // free again by the end of the step, as its slots were at the start
-    for (int w = tid; w < words; w += kCT) fbs[w] &= ~etaken[w];
-    __syncthreads();
-
-    // 1a. slots that hold a selected token are kept; the selection must be
-    // ascending with -1 padding last
-    for (int ch = 0; ch < chunks; ++ch) {
-        const int c0 = ch * kChunk;
-        int32_t after = after0;
-        if (chunks > 1) {
-            load_sel(c0);
-            const int inext = c0 + kPer * tid + kPer;
-            after = (inext < m) ? sl[inext] : -1;
-        }
-        uint32_t flags = 0;
-#pragma unroll
-        for (int q = 0; q < kPer; ++q) {
-            const int32_t nxt = (q + 1 < kPer) ? s[q + 1] : after;
-            if (s[q] >= 0 && s[q] < n) {
-                if (nxt >= 0 && nxt <= s[q]) flags |= ECHO_ST_BADDATA;
-                if (chunks > 1) j[q] = t2s[s[q]];  // the early look-ups above already wrote theirs
-            } else {
-                j[q] = -1;
-                if (s[q] >= 0 || nxt >= 0) flags |= ECHO_ST_BADDATA;
-            }
-        }
-        if (flags) atomicOr(&s_flags, flags);
-#pragma unroll
-        for (int q = 0; q < kPer; ++q)
-            if (j[q] >= 0 && j[q] < C) atomicOr(&keep[j[q] >> 5], 1u << (j[q] & 31));
-    }
-    __syncthreads();
-
-    // 1b. every other slot occupied at the start of the step is freed (bytes
-    // stay, nothing is written back), one warp per 32-slot word
-    auto free_word = [&](int w, int32_t st) {
-        const int slot = w * 32 + lane;
-        const bool kept = (keep[w] >> lane) & 1u;
-        const bool freeing = st >= 0 && !kept;
-        if (freeing) {
-            s2t[slot] = -1;
-            if (st < n) t2s[st] = -1;
-        }
-        const unsigned fm = __ballot_sync(0xffffffffu, freeing);
-        if (lane == 0) fbs[w] |= fm;
-    };
-    if (pre) {
-#pragma unroll
-        for (int r = 0; r < kPre; ++r) {
-            const int w = warp + r * (kCT / 32);
-            if (w < words) free_word(w, own[r]);
-        }
-    } else {
-        for (int w = warp; w < words; w += kCT / 32) free_word(w, s2t[w * 32 + lane]);
-    }
-    __syncthreads();
-
-    // 2. free-slot prefix over the new free-bit words
-    const uint32_t F = free_prefix<kCT>(fbs, words, scan, wpre, fbs);
-
-    // 3. the misses, in ascending token order, take the lowest free slots; the
-    // slot of every selected entry is written on the way
-    uint32_t found = 0;
-    for (int ch = 0; ch < chunks; ++ch) {
-        const int c0 = ch * kChunk;
-        if (chunks > 1) {  // the registers hold the last chunk only: reload
-            load_sel(c0);
-#pragma unroll
-            for (int q = 0; q < kPer; ++q) j[q] = (s[q] >= 0 && s[q] < n) ? t2s[s[q]] : -1;
-        }
-        uint32_t missing = 0;
-#pragma unroll
-        for (int q = 0; q < kPer; ++q)
-            if (s[q] >= 0 && s[q] < n && j[q] < 0) missing |= 1u << q;
-        uint32_t tot;
-        uint32_t rank = found + block_exclusive_scan<kCT>(__popc(missing), scan, &tot);
-        FreeWalk walk(wpre, fbs, words, rank < F ? rank : 0u);
-#pragma unroll
-        for (int q = 0; q < kPer; ++q) {
-            const int i = c0 + kPer * tid + q;
-            if (i >= m) break;
-            int32_t slot = j[q];
-            if (missing & (1u << q)) {
-                slot = (rank < F) ? walk.next() : -1;
-                if (slot >= 0) {
-                    if (rank < static_cast<uint32_t>(C)) {
-                        mtok[rank] = s[q];
-                        mslot[rank] = slot;
-                    }
-                    t2s[s[q]] = slot;
-                    s2t[slot] = s[q];
-                }
-                ++rank;
-            } else if (s[q] < 0 || s[q] >= n) {
-                slot = -1;
-            }
-            out[i] = slot;
-        }
-        found += tot;
-    }
-    const uint32_t got = min(found, F);
-    __syncthreads();  // every walk over fbs is done before its bits change
-    take_lowest_free<kCT>(fbs, words, got, wpre);
-    __syncthreads();
-    for (int w = tid; w < words; w += kCT) fb[w] = fbs[w];
-    if (tid == 0) {
-        c.miss_cnt[b] = static_cast<int32_t>(got);
-        c.early_cnt[b] = static_cast<int32_t>(E);
-        if (stats && got) atomicAdd(stats + ECHO_STAT_MISSES, got);
-        if (stats && E) atomicAdd(stats + ECHO_STAT_EARLY, E);
-        if (stats && s_early_used) atomicAdd(stats + ECHO_STAT_EARLY_USED, s_early_used);
-        uint32_t flags = s_flags;
-        if (found > F) flags |= ECHO_ST_NOSLOT;
-        if (flags) set_status(status, static_cast<int>(flags));
-    }
+    __shared__ uint32_t flags[2];
+    CacheStepLookup<kCT, kAWC> cs;
+    cs.init(tok_off, n_tokens, blockIdx.x, sel, m, sel_slot, above, early_cap, c, status, stats, smem, scan, flags);
+    cs.load_selection();  // first in the first round of loads: the slot loads depend on it
+    cs.prologue_issue();
+    cs.load_slots();      // in flight while the prologue stores and scans
+    cs.prologue_finish();
+    cs.finish();
 }
 
 __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restrict__ tok_off, int64_t n_tokens,
@@ -803,7 +554,7 @@ int enqueue_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const in
                        const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,
                        int32_t* status, uint32_t* stats, cudaStream_t stream, cudaStream_t copy_stream) {
     if (cache->C <= kLookupMaxSlots) {
-        const size_t smem = lookup_smem_words(cache->C) * sizeof(uint32_t);
+        const size_t smem = cache_lookup_smem_words(cache->C, kAWC) * sizeof(uint32_t);
         ECHO_CUDA_OK(prefer_max_shared(cache_step_lookup_kernel));
         ECHO_CUDA_OK(cudaFuncSetAttribute(cache_step_lookup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           static_cast<int>(smem)));

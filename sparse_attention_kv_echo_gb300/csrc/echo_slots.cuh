@@ -55,6 +55,25 @@ __device__ uint32_t free_prefix(const uint32_t* fb, int words, uint32_t* scan, u
 
 // Walks the free slots of a request in ascending order from free rank r
 // (r < wpre[words]): next() returns the slot of rank r, r + 1, ...
+// Position of the k-th (0-based) set bit of f; k < popc(f).  Five halving
+// steps on popcounts instead of clearing k bits one by one.
+__device__ __forceinline__ int nth_set_bit(uint32_t f, uint32_t k) {
+    int base = 0;
+#pragma unroll
+    for (int width = 16; width > 0; width >>= 1) {
+        const uint32_t low = f & ((1u << width) - 1u);
+        const uint32_t c = static_cast<uint32_t>(__popc(low));
+        if (k >= c) {
+            k -= c;
+            f >>= width;
+            base += width;
+        } else {
+            f = low;
+        }
+    }
+    return base;
+}
+
 struct FreeWalk {
     const uint32_t* fbs;
     int words, w;
@@ -71,7 +90,13 @@ struct FreeWalk {
         }
         w = lo;
         f = fbs[lo];
-        for (uint32_t i = r - wpre[lo]; i > 0 && f; --i) f &= f - 1;
+        const uint32_t k = r - wpre[lo];
+        if (k < static_cast<uint32_t>(__popc(f))) {
+            const int bit = nth_set_bit(f, k);  // the walk starts at the k-th free slot of the word
+            f &= ~((1u << bit) - 1u);
+        } else {
+            f = 0u;
+        }
     }
     // -1 once the free slots run out (a caller that keeps r < wpre[words] never sees it)
     __device__ int next() {
@@ -96,16 +121,11 @@ __device__ void take_lowest_free(uint32_t* fbs, int words, uint32_t take, const 
             fbs[w] = 0u;
             continue;
         }
-        uint32_t f = fbs[w];
-        uint32_t k = take - wpre[w];
-        uint32_t taken = 0;
-        while (f && k) {
-            const uint32_t low = f & (0u - f);
-            taken |= low;
-            f ^= low;
-            --k;
-        }
-        fbs[w] &= ~taken;
+        // the boundary word: its lowest take - wpre[w] free slots are taken, the
+        // rest (from its (take - wpre[w])-th free bit on) stay free
+        const uint32_t f = fbs[w];
+        const int bit = nth_set_bit(f, take - wpre[w]);
+        fbs[w] = f & ~((1u << bit) - 1u);
     }
 }
 
