@@ -55,6 +55,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--groups", type=int, default=None,
                    help="request groups of the decode step (default: the layer's choice)")
+    p.add_argument("--first-share", type=float, default=None,
+                   help="share of the requests in the first of two groups (default: the layer's choice)")
     return p.parse_args(argv)
 
 
@@ -227,7 +229,8 @@ def run_ours(args):
     qsrc = wl.QueryStream(w, 0, device=dev)
     q_all = torch.stack([qsrc.next() for _ in range(w.steps)])
     S = q_all.shape[0]
-    lay = DecodeLayer(off, k8, ks, w.k, w.C, host, device=dev, groups=args.groups)
+    kw = {} if args.first_share is None else {"first_share": args.first_share}
+    lay = DecodeLayer(off, k8, ks, w.k, w.C, host, device=dev, groups=args.groups, **kw)
     main = torch.cuda.Stream()
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 

@@ -28,7 +28,7 @@ from . import _lib as L
 class DecodeLayer:
     def __init__(self, tok_off, k8: torch.Tensor, ks: torch.Tensor, k: int, C: int,
                  host_pool: torch.Tensor, alpha: float = 0.5, predictor: bool = True,
-                 early_cap: int = -1, groups: int | None = None, device="cuda"):
+                 early_cap: int = -1, groups: int | None = None, first_share: float = 0.5, device="cuda"):
         tok_off = torch.as_tensor(tok_off, dtype=torch.int64)
         self.B = int(tok_off.numel() - 1)
         self.n_tokens = int(k8.shape[0])
@@ -50,6 +50,8 @@ class DecodeLayer:
             groups = 2 if (self.predictor and self.B >= 2) else 1
         groups = max(1, min(int(groups), self.B))
         bounds = [self.B * g // groups for g in range(groups + 1)]
+        if groups == 2:  # the second group's scores gate top-k; a smaller second group starts it sooner
+            bounds[1] = min(self.B - 1, max(1, round(self.B * first_share)))
         self.groups = [(bounds[g], bounds[g + 1]) for g in range(groups) if bounds[g + 1] > bounds[g]]
         # each group's above-threshold words: the groups' word ranges may overlap
         self.above_g = [torch.zeros(max(L.above_words(b1 - b0, self.n_tokens), 1), **i32)
