@@ -411,6 +411,8 @@ def run_ours(args):
                    "scoring_topk_frac_of_8tbs": round(scoring_topk_gbs / 8000.0, 4),
                    "misses_per_step": round(misses_per_step, 1), "early_per_step": round(early_per_step, 1),
                    "early_used_per_step": round(float(stats[L.STAT_EARLY_USED]) / args.steps, 1),
+                   "topk_boundary_bin_max": int(stats[L.STAT_BOUNDARY_MAX]),
+                   "topk_boundary_fallbacks": int(stats[L.STAT_TOPK_FALLBACK]),
                    "recall_rows_per_step_kernel_pass": round(statistics.mean(recall_rows), 1),
                    "early_fetch_gbs": round(recall_gbs, 1), "h2d_copy_gbs": round(h2d_gbs, 1),
                    "recall_frac_of_h2d": round(recall_gbs / h2d_gbs, 4) if h2d_gbs else None,

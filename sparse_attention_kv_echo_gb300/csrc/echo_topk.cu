@@ -7,21 +7,26 @@
 // predicted threshold (panel "Prefill: one-round histogram").
 //
 // One thread-block cluster of kCS CTAs (1024 threads each) per request; CTA r
-// of the cluster owns the r-th contiguous slice of the request's tokens.
+// of the cluster owns the r-th contiguous slice of the request's tokens and
+// reads its scores from global memory once, into shared memory (slices of up
+// to kSliceMax tokens).
 //   1. boundary bin: from the 256-bin histogram of the shifted scores (made by
 //      the score kernel, or rebuilt here), the bin b* where the count from the
 //      top reaches k.  Shifting is monotone, so every token in a bin above b*
 //      outranks every token at or below it.
-//   2. every CTA scans its slice once and appends the tokens of bin b* to the
-//      leader CTA's shared memory through distributed shared memory (one
-//      atomic per warp); the leader runs a radix select (four 8-bit digits of
-//      the order key) for K*, the key of the k-th score, and a second one on
-//      ~index to resolve equal keys towards the lower index.  When bin b*
-//      does not fit in shared memory the leader runs the same selects as
-//      passes over the scores in global memory.
-//   3. every CTA counts its selected tokens; a cluster-wide prefix of those
-//      counts (read over DSMEM) places each slice, and one ordered pass per
-//      slice writes the indices in ascending order with block-wide scans.
+//   2. every CTA counts its slice's tokens above b* and lists its tokens of
+//      b* (order key, index) in its own shared memory; one cluster barrier
+//      publishes the counts and the lists.
+//   3. every CTA gathers the whole boundary bin over distributed shared
+//      memory and runs the same radix select on it: K*, the key of the k-th
+//      score, then ~index among keys equal to K* for the lower-index tie rule.
+//      Redundant selection replaces a broadcast barrier.  When the bin does
+//      not fit, the selects run as passes over the scores in global memory.
+//   4. a CTA's place in the output is the count of selected tokens in the
+//      slices before it (their counts above b*, plus their boundary-bin
+//      entries at or above the cut), so one ordered pass per slice writes the
+//      indices in ascending order with block-wide scans, with no further
+//      exchange.
 // A good prediction puts the k-th score near 0 after the shift, where the
 // exponent bins are narrow, so the boundary bin holds few tokens.
 #include <cooperative_groups.h>
@@ -35,27 +40,44 @@ namespace echo {
 namespace {
 
 constexpr int kTT = 1024;
-constexpr int kCS = 8;           // CTAs per request (one cluster)
-constexpr int kCandMax = 12288;  // boundary-bin entries the leader keeps in shared memory
+constexpr int kCS = 8;            // CTAs per request (one cluster)
+constexpr int kCandMax = 12288;   // boundary-bin entries of a request a CTA gathers
+constexpr int kCandLocal = 4096;  // boundary-bin entries of one slice
+constexpr int kSliceMax = 16384;  // scores of its slice a CTA keeps in shared memory
 
 struct TopkShared {
     uint32_t hist[256];
-    uint32_t hist_acc[256];      // leader: cluster-wide rebuild of the histogram
+    uint32_t hist_acc[256];        // leader: cluster-wide rebuild of the histogram
     uint32_t scan[40];
-    uint32_t cand_key[kCandMax];
+    uint32_t cand_key[kCandMax];   // the request's boundary bin, slices in rank order
     uint32_t cand_idx[kCandMax];
-    uint32_t cnt;                // leader: boundary-bin entries appended
-    uint32_t chk_above;          // leader: tokens above b*, summed over the cluster
-    uint32_t chk_eq;             // leader: tokens in b*, summed over the cluster
+    uint32_t loc_key[kCandLocal];  // this slice's boundary-bin entries
+    uint32_t loc_idx[kCandLocal];
+    uint32_t r_above[kCS];         // per slice: tokens above b*
+    uint32_t r_cnt[kCS];           // per slice: boundary-bin entries
+    uint32_t cnt;                  // this slice: boundary-bin entries
+    uint32_t n_above;              // this slice: tokens above b*
+    uint32_t red[3];               // radix select: min, max and count of the elements
+    uint32_t taken[2];             // boundary-bin entries taken: before this slice, in all
     uint32_t digit;
     uint32_t above;
     uint32_t minkey;
     uint32_t flag;
-    uint32_t K;                  // leader -> all: key of the k-th score
-    uint32_t idx_cut;            // leader -> all: last index taken among keys == K
-    uint32_t selected;           // this CTA's number of selected tokens
 };
 
+__host__ __device__ constexpr size_t topk_cache_offset() { return (sizeof(TopkShared) + 15) / 16 * 16; }
+constexpr size_t kTopkSmem = topk_cache_offset() + sizeof(float) * kSliceMax;
+static_assert(kTopkSmem <= 227u * 1024u, "top-k shared memory");
+
+// Split cluster barrier: arrive says this CTA is done reading the others'
+// shared memory; wait (before exit) lets no CTA leave while another may still
+// read its shared memory.
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 // Warp 0: the largest digit d with (count of digits >= d) >= target, and the
 // count strictly above d.  target >= 1 and total >= target.
 __device__ void find_digit(const uint32_t* h, uint32_t target, uint32_t* out_digit, uint32_t* out_above) {
@@ -98,7 +120,9 @@ __device__ void find_digit(const uint32_t* h, uint32_t target, uint32_t* out_dig
     }
 }
 
-// Elements seen by a radix select.
+// Elements seen by a radix select.  for_each(f) calls f(v, ok) on every lane of
+// a warp the same number of times, so f may use warp-collective operations;
+// ok is false on lanes that hold no element.
 struct SmemCands {
     const uint32_t* key;
     const uint32_t* idx;
@@ -107,11 +131,18 @@ struct SmemCands {
     uint32_t eq_key;
     template <class F>
     __device__ __forceinline__ void for_each(F f) const {
-        for (uint32_t i = threadIdx.x; i < cnt; i += kTT) {
-            if (!by_index)
-                f(key[i]);
-            else if (key[i] == eq_key)
-                f(~idx[i]);
+        for (uint32_t i0 = threadIdx.x & ~31u; i0 < cnt; i0 += kTT) {
+            const uint32_t i = i0 + (threadIdx.x & 31u);
+            bool ok = i < cnt;
+            uint32_t v = 0;
+            if (ok) {
+                v = key[i];
+                if (by_index) {
+                    ok = v == eq_key;
+                    v = ~idx[i];
+                }
+            }
+            f(v, ok);
         }
     }
 };
@@ -125,29 +156,70 @@ struct GlobalCands {
     uint32_t eq_key;
     template <class F>
     __device__ __forceinline__ void for_each(F f) const {
-        for (int64_t s = threadIdx.x; s < n; s += kTT) {
-            const float x = sc[s];
-            if (shifted_bin(x, shift) != bstar) continue;
-            const uint32_t key = order_key(x);
-            if (!by_index)
-                f(key);
-            else if (key == eq_key)
-                f(~static_cast<uint32_t>(s));
+        for (int64_t s0 = threadIdx.x & ~31; s0 < n; s0 += kTT) {
+            const int64_t s = s0 + (threadIdx.x & 31);
+            bool ok = s < n;
+            uint32_t v = 0;
+            if (ok) {
+                const float x = sc[s];
+                v = order_key(x);
+                ok = shifted_bin(x, shift) == bstar;
+                if (by_index) {
+                    ok = ok && v == eq_key;
+                    v = ~static_cast<uint32_t>(s);
+                }
+            }
+            f(v, ok);
         }
     }
 };
 
 // The r-th largest value (1-based) among the elements (block-wide); *rem = r
 // minus the number of elements strictly larger (>= 1), *eq = number equal to it.
+// The leading bits that every element shares are skipped (a boundary bin's
+// keys share their sign and most of their exponent), and lanes adding to the
+// same digit add once per warp.
 template <class Src>
 __device__ uint32_t radix_select(const Src& src, uint32_t r, TopkShared& sh, uint32_t* rem, uint32_t* eq) {
-    uint32_t prefix = 0, mask = 0;
+    const unsigned lane = threadIdx.x & 31u;
+    if (threadIdx.x == 0) {
+        sh.red[0] = 0xFFFFFFFFu;
+        sh.red[1] = 0u;
+        sh.red[2] = 0u;
+    }
+    __syncthreads();
+    src.for_each([&](uint32_t v, bool ok) {
+        const unsigned m = __ballot_sync(0xffffffffu, ok);
+        if (m == 0) return;
+        const uint32_t lo = __reduce_min_sync(0xffffffffu, ok ? v : 0xFFFFFFFFu);
+        const uint32_t hi = __reduce_max_sync(0xffffffffu, ok ? v : 0u);
+        if (lane == 0) {
+            atomicMin(&sh.red[0], lo);
+            atomicMax(&sh.red[1], hi);
+            atomicAdd(&sh.red[2], static_cast<uint32_t>(__popc(m)));
+        }
+    });
+    __syncthreads();
+    const uint32_t vmin = sh.red[0], vmax = sh.red[1], total = sh.red[2];
+    if (vmin == vmax) {
+        __syncthreads();  // everyone has read red before a later select resets it
+        *rem = r;
+        *eq = total;
+        return vmin;
+    }
+    int shift = (31 - __clz(vmin ^ vmax)) & ~7;
+    uint32_t mask = (shift >= 24) ? 0u : ~((1u << (shift + 8)) - 1u);
+    uint32_t prefix = vmin & mask;
     uint32_t last_count = 0;
-    for (int shift = 24; shift >= 0; shift -= 8) {
+    for (; shift >= 0; shift -= 8) {
         for (int i = threadIdx.x; i < 256; i += kTT) sh.hist[i] = 0u;
         __syncthreads();
-        src.for_each([&](uint32_t v) {
-            if ((v & mask) == prefix) atomicAdd(&sh.hist[(v >> shift) & 255u], 1u);
+        src.for_each([&](uint32_t v, bool ok) {
+            ok = ok && (v & mask) == prefix;
+            const uint32_t d = (v >> shift) & 255u;
+            const unsigned peers = __match_any_sync(0xffffffffu, ok ? d : 0x100u);
+            if (ok && lane == static_cast<unsigned>(__ffs(peers) - 1))
+                atomicAdd(&sh.hist[d], static_cast<uint32_t>(__popc(peers)));
         });
         __syncthreads();
         if (threadIdx.x < 32) find_digit(sh.hist, r, &sh.digit, &sh.above);
@@ -256,15 +328,37 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTT, 1)
         return;
     }
 
-    // this CTA's slice of the request
+    // this CTA's slice of the request; its scores are staged in shared memory
+    // when they fit (xs[i] is the score of token s_lo + i), the histogram row
+    // is fetched alongside
     const int64_t s_lo = n * rank / kCS, s_hi = n * (rank + 1) / kCS;
+    const int64_t len = s_hi - s_lo;
+    const uint32_t hist_mine = (hist && tid < 256) ? hist[static_cast<int64_t>(b) * 256 + tid] : 0u;
+    float* const cache = reinterpret_cast<float*>(smem_raw + topk_cache_offset());
+    const bool cached = len <= kSliceMax;
+    if (cached) {
+        for (int64_t i0 = 0; i0 < len; i0 += 4 * kTT) {
+            float v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t i = i0 + j * kTT + tid;
+                v[j] = i < len ? sc[s_lo + i] : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t i = i0 + j * kTT + tid;
+                if (i < len) cache[i] = v[j];
+            }
+        }
+    }
+    const float* const xs = cached ? cache : sc + s_lo;
 
-    // ---- 1-2. boundary bin, its tokens gathered in the leader
+    // ---- 1-2. boundary bin; each slice lists its boundary-bin tokens in its own shared memory
     bool have = hist != nullptr;
     uint32_t bstar = 0, above = 0;
     for (int attempt = 0; attempt < 2; ++attempt) {
         if (have) {
-            for (int i = tid; i < 256; i += kTT) sh.hist[i] = hist[static_cast<int64_t>(b) * 256 + i];
+            if (tid < 256) sh.hist[tid] = hist_mine;
         } else {
             // rebuild: slice histograms summed into the leader over DSMEM
             if (leader)
@@ -274,7 +368,7 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTT, 1)
             for (int64_t s0 = s_lo; s0 < s_hi; s0 += kTT) {
                 const int64_t s = s0 + tid;
                 const bool v = s < s_hi;
-                const uint32_t bin = v ? shifted_bin(sc[s], shift) : 256u;
+                const uint32_t bin = v ? shifted_bin(xs[s - s_lo], shift) : 256u;
                 const unsigned grp = __match_any_sync(0xffffffffu, bin);
                 if (v && (tid & 31) == __ffs(grp) - 1) atomicAdd(&sh.hist[bin], __popc(grp));
             }
@@ -286,123 +380,164 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTT, 1)
         }
         __syncthreads();
         if (tid < 32) find_digit(sh.hist, static_cast<uint32_t>(k), &sh.digit, &sh.above);
-        if (leader && tid == 0) {
+        if (tid == 0) {
             sh.cnt = 0;
-            sh.chk_above = 0;
-            sh.chk_eq = 0;
+            sh.n_above = 0;
         }
         __syncthreads();
         bstar = sh.digit;
         above = sh.above;
         const uint32_t eq_total = sh.hist[bstar];
-        cluster.sync();  // the leader's counters are reset before anyone appends
-        uint32_t my_above = 0, my_eq = 0;
+        uint32_t my_above = 0;
         for (int64_t s0 = s_lo; s0 < s_hi; s0 += kTT) {
             const int64_t s = s0 + tid;
             const bool v = s < s_hi;
-            const float x = v ? sc[s] : 0.f;
+            const float x = v ? xs[s - s_lo] : 0.f;
             const uint32_t bin = shifted_bin(x, shift);
             my_above += v && bin > bstar;
             const bool in = v && bin == bstar;
-            my_eq += in;
             const unsigned m = __ballot_sync(0xffffffffu, in);
-            if (in) {
-                const int leader_lane = __ffs(m) - 1;
-                uint32_t basepos = 0;
-                if ((tid & 31) == leader_lane) basepos = atomicAdd(&lsh.cnt, __popc(m));
-                basepos = __shfl_sync(m, basepos, leader_lane);
-                const uint32_t pos = basepos + __popc(m & ((1u << (tid & 31)) - 1u));
-                if (pos < kCandMax) {
-                    lsh.cand_key[pos] = order_key(x);
-                    lsh.cand_idx[pos] = static_cast<uint32_t>(s);
+            if (m) {
+                const int first = __ffs(m) - 1;
+                uint32_t base = 0;
+                if ((tid & 31) == first) base = atomicAdd(&sh.cnt, static_cast<uint32_t>(__popc(m)));
+                base = __shfl_sync(0xffffffffu, base, first);
+                const uint32_t pos = base + __popc(m & ((1u << (tid & 31)) - 1u));
+                if (in && pos < kCandLocal) {
+                    sh.loc_key[pos] = order_key(x);
+                    sh.loc_idx[pos] = static_cast<uint32_t>(s);
                 }
             }
         }
-        // warp-reduce the checks before the remote atomics
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            my_above += __shfl_xor_sync(0xffffffffu, my_above, o);
-            my_eq += __shfl_xor_sync(0xffffffffu, my_eq, o);
+        my_above = __reduce_add_sync(0xffffffffu, my_above);
+        if ((tid & 31) == 0 && my_above) atomicAdd(&sh.n_above, my_above);
+        cluster.sync();  // every slice's counts and list are complete
+        if (tid < kCS) {
+            sh.r_above[tid] = *cluster.map_shared_rank(&sh.n_above, tid);
+            sh.r_cnt[tid] = *cluster.map_shared_rank(&sh.cnt, tid);
         }
-        if ((tid & 31) == 0) {
-            if (my_above) atomicAdd(&lsh.chk_above, my_above);
-            if (my_eq) atomicAdd(&lsh.chk_eq, my_eq);
+        __syncthreads();
+        uint32_t sum_above = 0, sum_cnt = 0;
+        for (int r = 0; r < kCS; ++r) {
+            sum_above += sh.r_above[r];
+            sum_cnt += sh.r_cnt[r];
         }
-        cluster.sync();
-        const bool consistent = lsh.chk_above == above && lsh.chk_eq == eq_total;
-        cluster.sync();  // everyone has read the leader's checks before they may be reset
-        if (consistent) break;
+        if (sum_above == above && sum_cnt == eq_total) break;
         // The histogram given does not describe these scores: rebuild it here.
         if (leader && tid == 0) set_status(status, ECHO_ST_BADDATA);
         have = false;
+        cluster.sync();  // every slice has read the counts before they are reset
     }
 
-    // ---- 3. K*, the key of the k-th score, and the index cut among equal keys (leader)
-    if (leader) {
-        const uint32_t need = static_cast<uint32_t>(k) - above;  // >= 1
-        const uint32_t cnt = sh.cnt;
-        if (tid == 0 && stats) {
-            atomicMax(stats + ECHO_STAT_BOUNDARY_MAX, cnt);
-            if (cnt > kCandMax) atomicAdd(stats + ECHO_STAT_TOPK_FALLBACK, 1u);
+    // ---- 3. the boundary bin gathered (slices in rank order), K* and the index cut
+    uint32_t above_before = 0, pre = 0, total_cnt = 0, above_all = 0;
+    bool fits = true;
+    for (int r = 0; r < kCS; ++r) {
+        const uint32_t a = sh.r_above[r], c = sh.r_cnt[r];
+        if (r < rank) {
+            above_before += a;
+            pre += c;
         }
-        uint32_t rem = 0, eqn = 0, K = 0, idx_cut = 0xFFFFFFFFu;
-        if (cnt <= kCandMax) {
-            SmemCands src{sh.cand_key, sh.cand_idx, cnt, false, 0};
-            K = radix_select(src, need, sh, &rem, &eqn);
-            if (rem < eqn) {
-                SmemCands src2{sh.cand_key, sh.cand_idx, cnt, true, K};
-                uint32_t r2, e2;
-                idx_cut = ~radix_select(src2, rem, sh, &r2, &e2);
-            }
-        } else {
-            GlobalCands src{sc, n, shift, bstar, false, 0};
-            K = radix_select(src, need, sh, &rem, &eqn);
-            if (rem < eqn) {
-                GlobalCands src2{sc, n, shift, bstar, true, K};
-                uint32_t r2, e2;
-                idx_cut = ~radix_select(src2, rem, sh, &r2, &e2);
-            }
-        }
-        if (tid == 0) {
-            sh.K = K;
-            sh.idx_cut = idx_cut;
-        }
+        above_all += a;
+        total_cnt += c;
+        fits = fits && c <= static_cast<uint32_t>(kCandLocal);
     }
-    cluster.sync();
-    const uint32_t K = lsh.K, idx_cut = lsh.idx_cut;
-
-    // ---- 4. ordered compaction: count, cluster prefix, write
-    uint32_t mine = 0;
-    bool nan = false;
-    for (int64_t s = s_lo + tid; s < s_hi; s += kTT) {
-        const float x = sc[s];
-        nan |= isnan(x);
-        mine += takes(x, shift, bstar, K, idx_cut, s);
-    }
+    fits = fits && total_cnt <= static_cast<uint32_t>(kCandMax);
+    if (fits) {
+        for (uint32_t g0 = 0; g0 < total_cnt; g0 += 2 * kTT) {
+            uint32_t kv[2] = {0u, 0u}, iv[2] = {0u, 0u};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+            for (int j = 0; j < 2; ++j) {
+                const uint32_t g = g0 + j * kTT + tid;
+                if (g < total_cnt) {
+                    int r = 0;
+                    uint32_t base = 0;
+                    while (r < kCS - 1 && g >= base + sh.r_cnt[r]) base += sh.r_cnt[r++];
+                    kv[j] = *cluster.map_shared_rank(&sh.loc_key[g - base], r);
+                    iv[j] = *cluster.map_shared_rank(&sh.loc_idx[g - base], r);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const uint32_t g = g0 + j * kTT + tid;
+                if (g < total_cnt) {
+                    sh.cand_key[g] = kv[j];
+                    sh.cand_idx[g] = iv[j];
+                }
+            }
+        }
+    }
     if (tid == 0) {
-        sh.selected = 0;
-        sh.flag = 0;
+        sh.taken[0] = 0;
+        sh.taken[1] = 0;
+    }
+    cluster_arrive_release();  // done reading the other slices' shared memory
+    __syncthreads();
+    if (leader && tid == 0 && stats) {
+        atomicMax(stats + ECHO_STAT_BOUNDARY_MAX, total_cnt);
+        if (!fits) atomicAdd(stats + ECHO_STAT_TOPK_FALLBACK, 1u);
+    }
+    const uint32_t need = static_cast<uint32_t>(k) - above;  // >= 1
+    uint32_t rem = 0, eqn = 0, K = 0, idx_cut = 0xFFFFFFFFu;
+    if (fits) {
+        SmemCands src{sh.cand_key, sh.cand_idx, total_cnt, false, 0};
+        K = radix_select(src, need, sh, &rem, &eqn);
+        if (rem < eqn) {
+            SmemCands src2{sh.cand_key, sh.cand_idx, total_cnt, true, K};
+            uint32_t r2, e2;
+            idx_cut = ~radix_select(src2, rem, sh, &r2, &e2);
+        }
+    } else {
+        GlobalCands src{sc, n, shift, bstar, false, 0};
+        K = radix_select(src, need, sh, &rem, &eqn);
+        if (rem < eqn) {
+            GlobalCands src2{sc, n, shift, bstar, true, K};
+            uint32_t r2, e2;
+            idx_cut = ~radix_select(src2, rem, sh, &r2, &e2);
+        }
+    }
+
+    // ---- 4. this slice's place: the selected tokens of the slices before it
+    uint32_t t_before = 0, t_all = 0;
+    if (fits) {
+        for (uint32_t i = tid; i < total_cnt; i += kTT) {
+            const uint32_t key = sh.cand_key[i];
+            const bool t = key > K || (key == K && sh.cand_idx[i] <= idx_cut);
+            t_all += t;
+            t_before += t && i < pre;
+        }
+    } else {
+        const int64_t lim = leader ? n : s_lo;
+        for (int64_t s = tid; s < lim; s += kTT) {
+            const float x = sc[s];
+            if (shifted_bin(x, shift) != bstar) continue;
+            const uint32_t key = order_key(x);
+            const bool t = key > K || (key == K && static_cast<uint32_t>(s) <= idx_cut);
+            t_all += t;
+            t_before += t && s < s_lo;
+        }
+    }
+    t_before = __reduce_add_sync(0xffffffffu, t_before);
+    t_all = __reduce_add_sync(0xffffffffu, t_all);
+    if ((tid & 31) == 0) {
+        if (t_before) atomicAdd(&sh.taken[0], t_before);
+        if (t_all) atomicAdd(&sh.taken[1], t_all);
     }
     __syncthreads();
-    if ((tid & 31) == 0 && mine) atomicAdd(&sh.selected, mine);
-    if (nan) sh.flag = 1;
-    cluster.sync();
-    uint32_t offset = 0, total = 0;
-    for (int r = 0; r < kCS; ++r) {
-        const uint32_t c = cluster.map_shared_rank(&sh, r)->selected;
-        if (r < rank) offset += c;
-        total += c;
-    }
-    uint32_t written = offset;
+    const uint32_t total = above_all + sh.taken[1];
+    uint32_t written = above_before + sh.taken[0];
+    bool nan = false;
     for (int64_t c0 = s_lo; c0 < s_hi; c0 += 4 * kTT) {
         const int64_t s0 = c0 + 4 * tid;
         uint32_t f = 0;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int64_t s = s0 + j;
-            if (s < s_hi && takes(sc[s], shift, bstar, K, idx_cut, s)) f |= 1u << j;
+            if (s < s_hi) {
+                const float x = xs[s - s_lo];
+                nan |= isnan(x);
+                if (takes(x, shift, bstar, K, idx_cut, s)) f |= 1u << j;
+            }
         }
         uint32_t tot;
         uint32_t pos = written + block_exclusive_scan<kTT>(__popc(f), sh.scan, &tot);
@@ -423,8 +558,8 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTT, 1)
             if (theta_upd) theta_upd[b] = ema_update(th_old, kth, alpha);
         }
     }
-    if (tid == 0 && sh.flag) set_status(status, ECHO_ST_NAN);
-    cluster.sync();  // no CTA leaves while another may still read its shared memory
+    if (__any_sync(0xffffffffu, nan) && (tid & 31) == 0) set_status(status, ECHO_ST_NAN);
+    cluster_wait_acquire();  // no CTA leaves while another may still read its shared memory
 }
 
 }  // namespace
@@ -435,7 +570,7 @@ namespace echo {
 int launch_topk(int B, const int64_t* tok_off, int64_t n_tokens, int64_t row0, int64_t W, const float* scores, int k,
                 const uint32_t* hist, float* theta_hat, float alpha, int32_t* sel_idx, float* kth, int32_t* status,
                 uint32_t* stats, cudaStream_t stream) {
-    const size_t smem = sizeof(TopkShared);
+    const size_t smem = kTopkSmem;
     ECHO_CUDA_OK(prefer_max_shared(topk_kernel));
     ECHO_CUDA_OK(cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(smem)));

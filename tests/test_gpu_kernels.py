@@ -196,6 +196,9 @@ def test_topk_crafted(hist):
         np.array([-0.0, 0.0, -0.0] * 500, np.float32),                # signed zeros tie
         (rng.standard_normal(70000) * 30 + 140).astype(np.float32),   # boundary bin overflows smem
         -np.abs(rng.standard_normal(4097)).astype(np.float32),        # negative scores
+        (rng.standard_normal(140000) * 1e4).astype(np.float32),       # slices too long for shared memory
+        np.concatenate([rng.random(35000) * 1e-3,                     # the boundary bin in one slice,
+                        0.6 + 0.3 * rng.random(5000)]).astype(np.float32),  # more than a slice lists
     ]
     k = 256
     sel, kth, th_new, st, stats, th = _topk_gpu(cases, k, hist=hist)
