@@ -209,6 +209,8 @@ int echo_early_fetch(int B, const int64_t* tok_off, int64_t n_tokens, const uint
  *   histogram or the prediction; they only decide how much work it takes (a
  *   histogram that does not describe the scores is rebuilt and flagged
  *   ECHO_ST_BADDATA).
+ * The kernel lets a programmatic dependent launch (echo_cache_step) start as
+ * soon as it begins; it writes sel_idx, kth and theta_hat only.
  */
 int echo_topk_select(int B, const int64_t* tok_off, int64_t n_tokens, const float* scores, int k,
                      const uint32_t* hist, float* theta_hat, float alpha, int32_t* sel_idx,
@@ -229,7 +231,12 @@ int echo_topk_select(int B, const int64_t* tok_off, int64_t n_tokens, const floa
  *   3. sel_slot [B,m] = slot of each selected token (-1 for padding);
  *   4. the miss rows are copied host_kv[tok_off[b] + t] -> dev_kv[b*C + slot],
  *      on copy_stream (which may equal stream; an event orders it after 0-3).
- * Needs m <= C.
+ * Needs m <= C.  Steps 0-3 are launched as a programmatic dependent of the
+ * kernel before them on `stream`: while that kernel still runs (if it lets
+ * dependents start early, as echo_topk_select and echo_index_scores do) they
+ * may read slot2tok and freebits, which none of this library's kernels but
+ * this step writes; sel and above are read only after that kernel has
+ * completed.
  */
 int echo_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
                     const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,

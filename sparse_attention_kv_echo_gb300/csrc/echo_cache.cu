@@ -93,10 +93,13 @@ __global__ void __launch_bounds__(kCT)
     __shared__ uint32_t flags[2];
     CacheStepLookup<kCT, kAWC> cs;
     cs.init(tok_off, n_tokens, blockIdx.x, sel, m, sel_slot, above, early_cap, c, status, stats, smem, scan, flags);
-    cs.load_selection();  // first in the first round of loads: the slot loads depend on it
-    cs.prologue_issue();
-    cs.load_slots();      // in flight while the prologue stores and scans
+    cs.prologue_issue();  // the tables only: they may be read before the kernel before this one ends
     cs.prologue_finish();
+    pdl_wait();           // the selection and the above words come from the kernels before this one
+    cs.load_selection();
+    cs.load_above();
+    cs.load_slots();
+    cs.above_finish();    // while the slot loads are in flight
     cs.finish();
 }
 
@@ -111,6 +114,7 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
     __shared__ uint32_t scan[40];
     __shared__ uint32_t s_flags, s_early_used;
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_wait();  // launched as a programmatic dependent: everything below may depend on the kernel before
     int64_t base, n;
     if (!request_range(tok_off, n_tokens, b, &base, &n) && tid == 0) set_status(status, ECHO_ST_BADDATA);
     const int C = c.C, words = C / 32;
@@ -553,22 +557,40 @@ namespace echo {
 int enqueue_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
                        const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,
                        int32_t* status, uint32_t* stats, cudaStream_t stream, cudaStream_t copy_stream) {
-    if (cache->C <= kLookupMaxSlots) {
-        const size_t smem = cache_lookup_smem_words(cache->C, kAWC) * sizeof(uint32_t);
+    const bool lookup = cache->C <= kLookupMaxSlots;
+    const size_t smem =
+        (lookup ? cache_lookup_smem_words(cache->C, kAWC) : cache_step_smem_words(cache->C)) * sizeof(uint32_t);
+    if (lookup) {
         ECHO_CUDA_OK(prefer_max_shared(cache_step_lookup_kernel));
         ECHO_CUDA_OK(cudaFuncSetAttribute(cache_step_lookup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           static_cast<int>(smem)));
-        cache_step_lookup_kernel<<<B, kCT, smem, stream>>>(tok_off, n_tokens, sel, m, above, early_cap,
-                                                           cache_args(*cache), sel_slot, status, stats);
     } else {
-        const size_t smem = cache_step_smem_words(cache->C) * sizeof(uint32_t);
         ECHO_CUDA_OK(prefer_max_shared(cache_step_kernel));
         ECHO_CUDA_OK(cudaFuncSetAttribute(cache_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           static_cast<int>(smem)));
-        cache_step_kernel<<<B, kCT, smem, stream>>>(tok_off, n_tokens, sel, m, above, early_cap,
-                                                    cache_args(*cache), sel_slot, status, stats);
     }
-    ECHO_CUDA_OK(cudaGetLastError());
+    // Programmatic dependent launch: once the kernel before it on `stream`
+    // lets dependents start (top-k does at its start), the look-up form reads
+    // the cache's own tables and takes the free-slot prefix while that kernel
+    // still runs; it waits (griddepcontrol.wait) before anything else.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(B);
+    cfg.blockDim = dim3(kCT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const CacheArgs ca = cache_args(*cache);
+    if (lookup) {
+        ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, cache_step_lookup_kernel, tok_off, n_tokens, sel, m, above, early_cap,
+                                        ca, sel_slot, status, stats));
+    } else {
+        ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, cache_step_kernel, tok_off, n_tokens, sel, m, above, early_cap, ca,
+                                        sel_slot, status, stats));
+    }
     const int rc = stream_wait(copy_stream, stream);
     if (rc) return rc;
     ECHO_CUDA_OK(launch_recall(B, tok_off, n_tokens, cache->C, cache->miss_tok, cache->miss_slot, cache->miss_cnt,

@@ -14,8 +14,13 @@
 // starting free bits.  The early set is never walked: one scan over the above
 // words, one over the free bits, O(1) work per selected token.
 //
-// Two parts: prologue() needs no selection (table, free-bit and above-word
-// loads, their prefixes); finish() reads the selection and does the rest.
+// Order of the parts: prologue_issue() and prologue_finish() read only the
+// cache's own tables (slot owners, free bits: the free-slot prefix and the
+// early limit), so a kernel may run them before it waits for the kernel that
+// writes the selection; then load_selection() and load_above() (one round of
+// loads), load_slots() (the selected tokens' slots, a second round),
+// above_finish() (the rank prefix over the above words, while the slots are
+// in flight) and finish().
 #pragma once
 
 #include "echo_common.cuh"
@@ -155,8 +160,8 @@ struct CacheStepLookup {
         A += tot;
     }
 
-    // Part 1a: issue the loads that need no selection, one word of each
-    // table per thread, into registers.
+    // Part 1a: issue the table loads, one word of each table per thread,
+    // into registers.
     __device__ void prologue_issue() {
         const int tid = static_cast<int>(threadIdx.x), lane = tid & 31, warp = tid >> 5;
 #pragma unroll
@@ -165,12 +170,10 @@ struct CacheStepLookup {
             own[r] = (pre && w < words) ? s2t[w * 32 + lane] : -1;
         }
         pf_fb = (tid < words) ? fb[tid] : 0u;
-        pf_aw = (tid < min(nw, AWC)) ? above_word(tid) : 0u;
     }
 
-    // Part 1b: the rest of the free bits and of the first chunk of above
-    // words into shared memory, then the starting free-slot prefix, the early
-    // limit and the chunk's rank prefix.
+    // Part 1b: the rest of the free bits into shared memory, then the
+    // starting free-slot prefix and the early limit.
     __device__ void prologue_finish() {
         const int tid = static_cast<int>(threadIdx.x);
         for (int w = tid; w < words; w += NT) {
@@ -178,7 +181,6 @@ struct CacheStepLookup {
             keep[w] = 0u;
             etaken[w] = 0u;
         }
-        for (int w = tid; w < min(nw, AWC); w += NT) aw[w] = (w == tid) ? pf_aw : above_word(w);
         if (tid == 0) {
             *s_flags = range_ok ? 0u : static_cast<uint32_t>(ECHO_ST_BADDATA);
             *s_used = 0;
@@ -187,14 +189,21 @@ struct CacheStepLookup {
         if (early) {
             const uint32_t F0 = free_prefix<NT>(fbs, words, scan, wpre, fbs);
             limit = (early_cap < 0) ? F0 : min(F0, static_cast<uint32_t>(early_cap));
+        }
+    }
+
+    // The first chunk of above words, one per thread, into registers.
+    __device__ void load_above() { pf_aw = (threadIdx.x < min(nw, AWC)) ? above_word(threadIdx.x) : 0u; }
+
+    // The first chunk of above words into shared memory and its rank prefix.
+    __device__ void above_finish() {
+        const int tid = static_cast<int>(threadIdx.x);
+        if (early) {
+            for (int w = tid; w < min(nw, AWC); w += NT) aw[w] = (w == tid) ? pf_aw : above_word(w);
+            __syncthreads();
             above_prefix(min(nw, AWC));
         }
         __syncthreads();
-    }
-
-    __device__ void prologue() {
-        prologue_issue();
-        prologue_finish();
     }
 
     // A selected token s with slot jv (-1: not resident): its early slot if it
@@ -221,8 +230,7 @@ struct CacheStepLookup {
         return slot;
     }
 
-    // Part 2: everything that needs the selection; load_selection() and
-    // load_slots() have run (before prologue_finish()).
+    // Part 2: everything else; every part above has run.
     __device__ void finish() {
         const int tid = static_cast<int>(threadIdx.x), lane = tid & 31, warp = tid >> 5;
         constexpr int kChunk = NT * kCsPer;

@@ -263,6 +263,7 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTT, 1)
     topk_kernel(TopkSegs segs, const float* __restrict__ scores, int k, const uint32_t* __restrict__ hist,
                 float* theta_hat, float alpha, int32_t* __restrict__ sel, float* kth_out, int32_t* status,
                 uint32_t* stats) {
+    pdl_launch_dependents();  // a programmatic dependent (the cache step) may start its table prologue
     extern __shared__ uint8_t smem_raw[];
     TopkShared& sh = *reinterpret_cast<TopkShared*>(smem_raw);
     cg::cluster_group cluster = cg::this_cluster();
