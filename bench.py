@@ -203,6 +203,14 @@ def cpu_inputs(w, k8, ks, wt, host, q_all):
 
 
 # ----------------------------------------------------------------------------- our arm
+def park(stream):
+    """Holds the GPU (~10 ms spin kernel, before the first timed event) while the host
+    enqueues the timed steps, so no step's events time a pause of the Python loop."""
+    import torch
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(20_000_000)
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -245,15 +253,22 @@ def run_ours(args):
     torch.cuda.synchronize()
     lay.reset()
     torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=main):
-        lay.step(stream=main)
+    # one graph per query of the stream: the quantiser reads that query in HBM directly
+    graphs = []
+    for i in range(S):
+        gi = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gi, stream=main):
+            lay.step(q_all[i], stream=main)
+        graphs.append(gi)
+    torch.cuda.synchronize()
+    for i in range(S):  # untimed: every graph launched once (its first launch uploads it)
+        with torch.cuda.stream(main):
+            graphs[i].replay()
     torch.cuda.synchronize()
 
     def replay(t):
         with torch.cuda.stream(main):
-            lay.q_in.copy_(q_all[t % S])
-            g.replay()
+            graphs[t % S].replay()
 
     # ---------------- timed region: graph replays, L2 flushed before each step
     props = torch.cuda.get_device_properties(local)
@@ -272,6 +287,7 @@ def run_ours(args):
     stats0 = lay.stats.clone()
     sampler.start()
     torch.cuda.synchronize()
+    park(main)
     for i in range(args.steps):
         with torch.cuda.stream(main):
             flush.zero_()
@@ -370,17 +386,20 @@ def run_ours(args):
     w_host = wt.cpu().pin_memory()
     slot_host = torch.empty_like(lay.sel_slot, device="cpu").pin_memory()
     kth_host = torch.empty_like(lay.kth, device="cpu").pin_memory()
+    # one graph per query buffer: copies in, the step, copies out (DecodeLayer.capture_host_step)
+    host_graphs = [lay.capture_host_step(q_host[i], w_host, slot_host, kth_host, stream=main) for i in range(S)]
+    for i in range(S):  # untimed warm-up: every graph launched once (its first launch uploads it)
+        with torch.cuda.stream(main):
+            host_graphs[i].replay()
+    torch.cuda.synchronize()
     e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     e_ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    park(main)
     for i in range(args.steps):
         with torch.cuda.stream(main):
             flush.zero_()
             e_starts[i].record(main)
-            lay.q_in.copy_(q_host[i % S], non_blocking=True)
-            lay.w_in.copy_(w_host, non_blocking=True)
-            g.replay()
-            slot_host.copy_(lay.sel_slot, non_blocking=True)
-            kth_host.copy_(lay.kth, non_blocking=True)
+            host_graphs[i % S].replay()
             e_ends[i].record(main)
     torch.cuda.synchronize()
     e2e_s = sum(s.elapsed_time(e) for s, e in zip(e_starts, e_ends)) / 1e3
@@ -411,7 +430,7 @@ def run_ours(args):
                    "scoring_topk_frac_of_8tbs": round(scoring_topk_gbs / 8000.0, 4),
                    "misses_per_step": round(misses_per_step, 1), "early_per_step": round(early_per_step, 1),
                    "early_used_per_step": round(float(stats[L.STAT_EARLY_USED]) / args.steps, 1),
-                   "topk_boundary_bin_max": int(stats[L.STAT_BOUNDARY_MAX]),
+                   "topk_boundary_bin_max": int(lay.stats[L.STAT_BOUNDARY_MAX].item()),
                    "topk_boundary_fallbacks": int(stats[L.STAT_TOPK_FALLBACK]),
                    "recall_rows_per_step_kernel_pass": round(statistics.mean(recall_rows), 1),
                    "early_fetch_gbs": round(recall_gbs, 1), "h2d_copy_gbs": round(h2d_gbs, 1),

@@ -133,6 +133,9 @@ typedef struct echo_cache {
  * wfold[b,h] = w[b,h] * scale (fp32).
  *   q [B,64,128] f32 (16-byte aligned), w [B,64] f32
  *   -> q8 [B,64,128] u8, qscale [B,64] f32, wfold [B,64] f32 (16-byte aligned).
+ *   q and w may be device memory or pinned host memory given by its device
+ *   alias (echo_host_device_alias); the kernel reads each element once, so a
+ *   step's inputs need no separate host-to-device copy.
  *   hist [B,256] u32 (may be NULL) is set to zero, ready for echo_index_scores.
  * NaN/Inf in q or w -> ECHO_ST_NAN.
  */

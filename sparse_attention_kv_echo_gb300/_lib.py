@@ -126,13 +126,36 @@ def host_device_alias(host_tensor: torch.Tensor) -> int:
     return out.value
 
 
+class _CudaArray:
+    def __init__(self, iface):
+        self.__cuda_array_interface__ = iface
+
+
+_TYPESTR = {torch.int32: "<i4", torch.float32: "<f4", torch.uint8: "|u1", torch.int64: "<i8"}
+
+
+def host_alias_tensor(host: torch.Tensor, device) -> torch.Tensor:
+    """A CUDA tensor over the device alias of a pinned, contiguous host tensor (kernels
+    read and write the host memory directly).  The caller keeps `host` alive."""
+    if host.device.type != "cpu" or not host.is_pinned() or not host.is_contiguous():
+        raise ValueError("host_alias_tensor needs a pinned, contiguous CPU tensor")
+    iface = {"shape": tuple(host.shape), "typestr": _TYPESTR[host.dtype],
+             "data": (host_device_alias(host), False), "version": 2, "strides": None}
+    with torch.cuda.device(device):
+        return torch.as_tensor(_CudaArray(iface), device=device)
+
+
 def sm_count() -> int:
     return load().echo_device_sm_count()
 
 
 def quantize_q(q, w, q8, qscale, wfold, status, hist=None, stream=None):
+    """echo_quantize_q; q and w may be pinned host tensors, read by the kernel through their
+    device alias."""
     B = q.shape[0]
-    _check("echo_quantize_q", load().echo_quantize_q(B, _ptr(q), _ptr(w), _ptr(q8), _ptr(qscale),
+    qp = host_device_alias(q) if q.device.type == "cpu" else _ptr(q)
+    wp = host_device_alias(w) if w.device.type == "cpu" else _ptr(w)
+    _check("echo_quantize_q", load().echo_quantize_q(B, qp, wp, _ptr(q8), _ptr(qscale),
                                                     _ptr(wfold), _ptr(hist), _ptr(status), _stream(stream)))
 
 

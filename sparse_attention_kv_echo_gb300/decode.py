@@ -15,6 +15,9 @@ quantised query) and issues the calls of a step:
                           recall joins the step's stream after both.
 Every buffer keeps its address and size, so ``step`` can be captured into a
 CUDA graph and replayed; ``q_in``/``w_in`` are the inputs a graph reads.
+``capture_host_step`` captures the step together with its host I/O (inputs
+from pinned host buffers, selection slots and k-th scores back to pinned host
+buffers), so one graph launch carries a whole step end to end.
 """
 from __future__ import annotations
 
@@ -78,11 +81,16 @@ class DecodeLayer:
         self.status.zero_()
         self.stats.zero_()
 
-    def step(self, q: torch.Tensor | None = None, w: torch.Tensor | None = None, stream=None):
-        """Enqueue one decode step (q [B,64,128] f32, w [B,64] f32; defaults q_in / w_in).
+    def step(self, q: torch.Tensor | None = None, w: torch.Tensor | None = None, stream=None, out_host=None):
+        """Enqueue one decode step (q [B,64,128] f32, w [B,64] f32; defaults q_in / w_in; pinned
+        host tensors are read by the quantiser directly).
 
         stream: the step's stream (default: current).  Everything, the row copies
-        included, is ordered before whatever is enqueued on `stream` next."""
+        included, is ordered before whatever is enqueued on `stream` next.
+        out_host: optional (slot [B,k] int32, kth [B] f32) CUDA tensors over pinned host
+        memory (_lib.host_alias_tensor): each request group's slots and k-th scores are
+        written there by a kernel as soon as its cache step is done, while the late misses
+        are still being recalled."""
         q = self.q_in if q is None else q
         w = self.w_in if w is None else w
         main = torch.cuda.current_stream() if stream is None else stream
@@ -94,6 +102,9 @@ class DecodeLayer:
                           self.sel_idx, self.kth, self.status, stats=self.stats, stream=main)
             L.cache_step(self.tok_off, self.n_tokens, self.sel_idx, self.cache, self.sel_slot, self.status,
                          stats=self.stats, stream=main, copy_stream=main)
+            if out_host is not None:
+                with torch.cuda.stream(main):
+                    self._write_out(out_host, 0, self.B)
             return
         sms = torch.cuda.get_device_properties(main.device).multi_processor_count
         streams, scored = [], None
@@ -127,8 +138,43 @@ class DecodeLayer:
             L.cache_step(off, self.n_tokens, self.sel_idx[b0:b1], self.views[g], self.sel_slot[b0:b1], self.status,
                          stats=self.stats, stream=side, copy_stream=s, above=self.above_g[g],
                          early_cap=self.early_cap)
+            if out_host is not None:
+                with torch.cuda.stream(side):
+                    self._write_out(out_host, b0, b1)
         for gs in self.gstreams:
             main.wait_stream(gs)
+        if out_host is not None:
+            for side in self.sides:
+                main.wait_stream(side)
+
+    def _write_out(self, out_host, b0, b1):
+        # elementwise kernels, not copy-engine transfers: their stores go straight to the
+        # host memory behind the alias, with no copy-engine launch in the graph
+        torch.bitwise_or(self.sel_slot[b0:b1], 0, out=out_host[0][b0:b1])
+        torch.mul(self.kth[b0:b1], 1.0, out=out_host[1][b0:b1])
+
+    def capture_host_step(self, q_host: torch.Tensor, w_host: torch.Tensor, slot_host: torch.Tensor,
+                          kth_host: torch.Tensor, stream=None) -> torch.cuda.CUDAGraph:
+        """A CUDA graph of one step with its host I/O: the quantiser reads q_host [B,64,128]
+        f32 and w_host [B,64] f32 (pinned) directly, the step runs, and sel_slot / kth are
+        copied out to slot_host [B,k] int32 / kth_host [B] f32 (pinned) per request group
+        as soon as they are final.  The buffers are bound to the graph: refill
+        q_host/w_host before a replay, read the outputs after it."""
+        for t, like in ((q_host, self.q_in), (w_host, self.w_in), (slot_host, self.sel_slot), (kth_host, self.kth)):
+            if t.device.type != "cpu" or not t.is_pinned() or t.shape != like.shape or t.dtype != like.dtype:
+                raise ValueError("host I/O buffers must be pinned CPU tensors shaped like q_in, w_in, "
+                                 "sel_slot and kth")
+        cap = torch.cuda.Stream(device=self.q_in.device) if stream is None else stream
+        cap.wait_stream(torch.cuda.current_stream(self.q_in.device))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            # the graph reads and writes these buffers through their aliases: keep them alive
+            self._host_io = getattr(self, "_host_io", []) + [(q_host, w_host, slot_host, kth_host)]
+            out = (L.host_alias_tensor(slot_host, self.q_in.device), L.host_alias_tensor(kth_host, self.q_in.device))
+            with torch.cuda.graph(g, stream=cap):
+                self.step(q_host, w_host, stream=cap, out_host=out)
+        torch.cuda.current_stream(self.q_in.device).wait_stream(cap)
+        return g
 
     def kernel_launches_per_step(self) -> int:
         # quantize, then per group: score (+ early fetch) + top-k + cache step + late recall

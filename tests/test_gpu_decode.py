@@ -119,3 +119,41 @@ def test_graph_replay_equals_eager():
         for name in ("tok2slot", "slot2tok", "freebits", "dev_kv"):
             assert torch.equal(getattr(eager.cache, name), getattr(graph.cache, name)), (t, name)
         assert eager.status.item() == 0 and graph.status.item() == 0
+
+
+def test_host_io_graph_equals_eager():
+    """A step captured with its host I/O (pinned inputs in, slots and k-th scores out)
+    gives the same outputs and tables as eager steps."""
+    w = wl.scaled(wl.WORKLOADS["batch"], "hostio", B=2, lengths=(12000, 7000), k=512, C=1024)
+    dev = "cuda"
+    off = wl.tok_offsets(w.lengths)
+    k8, ks = wl.make_keys(w, 0)
+    wt = wl.make_weights(w, 0)
+    host = wl.make_host_pool(w, 0, pin=True)
+    eager = DecodeLayer(off, k8.to(dev), ks.to(dev), w.k, w.C, host)
+    hio = DecodeLayer(off, k8.to(dev), ks.to(dev), w.k, w.C, host)
+    qs = wl.QueryStream(w, 0)
+    queries = [qs.next() for _ in range(5)]
+    q_host = torch.empty_like(hio.q_in, device="cpu").pin_memory()
+    w_host = wt.clone().pin_memory()
+    slot_host = torch.empty_like(hio.sel_slot, device="cpu").pin_memory()
+    kth_host = torch.empty_like(hio.kth, device="cpu").pin_memory()
+    for lay in (eager, hio):
+        lay.q_in.copy_(queries[0].to(dev))
+        lay.w_in.copy_(wt.to(dev))
+        lay.step()
+    torch.cuda.synchronize()
+    g = hio.capture_host_step(q_host, w_host, slot_host, kth_host)
+    for t in range(1, 5):
+        eager.q_in.copy_(queries[t].to(dev))
+        eager.step()
+        q_host.copy_(queries[t])
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(slot_host, eager.sel_slot.cpu()), t
+        assert torch.equal(kth_host, eager.kth.cpu()), t
+        for name in ("tok2slot", "slot2tok", "freebits", "dev_kv"):
+            assert torch.equal(getattr(eager.cache, name), getattr(hio.cache, name)), (t, name)
+        assert eager.status.item() == 0 and hio.status.item() == 0
+    with pytest.raises(ValueError):
+        hio.capture_host_step(q_host.to(dev), w_host, slot_host, kth_host)
