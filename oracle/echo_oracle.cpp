@@ -354,31 +354,47 @@ int orc_early_fetch(int64_t n, int C, const float* scores, float theta, int cap,
 
 // ---- [EXPL "One layer, one step: free -> allocate -> recall"] -------------
 // sel [m] is the step's selection in ascending token order, -1 padded.
+// early_tok [n_early] are the tokens this step's early fetch made resident
+// (orc_early_fetch's output; may be NULL when n_early = 0).
 // 1. Free every resident token that is not selected: both table entries go
 //    to -1; the KV bytes stay where they are and nothing is written back to
-//    the host, which holds every token.
+//    the host, which holds every token.  The slot of an early token of this
+//    step is held until step 2 is done (READING: the early copy into that
+//    slot may still be in flight during the step, so no miss of the same
+//    step is placed there; the slot is free again for the next step).
 // 2. The selected tokens that are not resident are the misses; in ascending
 //    token order each takes the lowest free slot, in ascending order.
-// 3. sel_slot[i] = slot of sel[i] (-1 for padding).
-// Outputs: miss_tok / miss_slot [*nmiss], *nfreed.  Capacity: the number of
-// selected tokens must not exceed C (return 2, state untouched).
+// 3. The held slots are free.
+// 4. sel_slot[i] = slot of sel[i] (-1 for padding).
+// Outputs: miss_tok / miss_slot [*nmiss], *nfreed (held slots included).
+// Capacity: selected tokens plus held slots must not exceed C (return 2,
+// state untouched).
 int orc_cache_step(int64_t n, int C, int32_t* tok2slot, int32_t* slot2tok, const int32_t* sel,
-                   int m, int32_t* sel_slot, int32_t* miss_tok, int32_t* miss_slot,
-                   int32_t* nmiss, int32_t* nfreed) {
+                   int m, const int32_t* early_tok, int32_t n_early, int32_t* sel_slot,
+                   int32_t* miss_tok, int32_t* miss_slot, int32_t* nmiss, int32_t* nfreed) {
     if (!cache_consistent(n, C, tok2slot, slot2tok)) return ORC_EINVAL;
+    if (n_early < 0 || (n_early > 0 && !early_tok)) return ORC_EINVAL;
     std::set<int32_t> selected;
     for (int i = 0; i < m; ++i) {
         if (sel[i] < 0) continue;
         if (sel[i] >= n) return ORC_EINVAL;
         selected.insert(sel[i]);
     }
-    if ((int64_t)selected.size() > C) return ORC_ECAPACITY;
+    const std::set<int32_t> early(early_tok, early_tok + n_early);
+    int64_t held_count = 0;
+    for (int32_t e : early)
+        if (!selected.count(e)) ++held_count;
+    if ((int64_t)selected.size() + held_count > C) return ORC_ECAPACITY;
     Cache c = load_cache(n, C, tok2slot, slot2tok);
-    // 1. free
+    // 1. free (early slots held)
     int32_t freed = 0;
+    std::vector<int32_t> held;
     for (auto it = c.resident.begin(); it != c.resident.end();) {
         if (!selected.count(it->first)) {
-            c.free_slots.insert(it->second);
+            if (early.count(it->first))
+                held.push_back(it->second);
+            else
+                c.free_slots.insert(it->second);
             it = c.resident.erase(it);
             ++freed;
         } else {
@@ -396,6 +412,8 @@ int orc_cache_step(int64_t n, int C, int32_t* tok2slot, int32_t* slot2tok, const
         miss_slot[got] = slot;
         ++got;
     }
+    // 3. the held slots are free again
+    for (int32_t slot : held) c.free_slots.insert(slot);
     // 3. slot of every selected entry
     for (int i = 0; i < m; ++i) sel_slot[i] = (sel[i] < 0) ? -1 : c.resident.at(sel[i]);
     *nmiss = got;
@@ -434,6 +452,15 @@ int orc_prefill_rows(const float* scores, int64_t W, int R, int64_t row0, int k,
             if (sel[(int64_t)r * k + i] >= 0) union_mask[sel[(int64_t)r * k + i]] = 1;
     }
     return ORC_OK;
+}
+
+// The early set of a decode step with selection width k is capped at C - k
+// on top of the caller's cap (cap < 0: no cap of its own) (READING: with the
+// early slots held through the miss placement, selected tokens plus held
+// slots stay within C only if the early set leaves room for k misses).
+int orc_early_cap_for(int cap, int C, int k) {
+    const int room = C - k;
+    return (cap < 0 || cap > room) ? room : cap;
 }
 
 // ---- one whole decode step of one layer, for the CPU baseline ------------
@@ -475,7 +502,8 @@ int orc_decode_step(int B, const int64_t* tok_off, const float* q, const float* 
         std::vector<int32_t> et((size_t)C), es((size_t)C);
         int32_t ne = 0;
         if (predictor) {
-            rc = orc_early_fetch(n, C, sf.data(), theta[b], cap, t2s, s2t, et.data(), es.data(), &ne);
+            rc = orc_early_fetch(n, C, sf.data(), theta[b], orc_early_cap_for(cap, C, k), t2s, s2t, et.data(),
+                                 es.data(), &ne);
             if (rc) { rcs[(size_t)b] = rc; return; }
             orc_recall(hrows, row_bytes, et.data(), es.data(), ne, drows);
         }
@@ -484,8 +512,8 @@ int orc_decode_step(int B, const int64_t* tok_off, const float* q, const float* 
         theta[b] = ema(theta[b], kth[b], alpha);
         std::vector<int32_t> mt((size_t)k), ms((size_t)k);
         int32_t nm = 0, nf = 0;
-        rc = orc_cache_step(n, C, t2s, s2t, sel_idx + (int64_t)b * k, k, sel_slot + (int64_t)b * k,
-                            mt.data(), ms.data(), &nm, &nf);
+        rc = orc_cache_step(n, C, t2s, s2t, sel_idx + (int64_t)b * k, k, et.data(), ne,
+                            sel_slot + (int64_t)b * k, mt.data(), ms.data(), &nm, &nf);
         if (rc) { rcs[(size_t)b] = rc; return; }
         orc_recall(hrows, row_bytes, mt.data(), ms.data(), nm, drows);
         nmiss[b] = nm;

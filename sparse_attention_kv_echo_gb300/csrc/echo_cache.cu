@@ -32,7 +32,9 @@
 namespace echo {
 namespace {
 
-constexpr int kCT = 1024;
+constexpr int kCT = 1024;  // threads of the walking cache step
+constexpr int kLT = 1024;  // threads of the look-up cache step (at ~64 registers a block fills an SM's
+                           // register file: no copy block, whose loads wait on the host link, shares it)
 
 
 __device__ __forceinline__ bool request_range(const int64_t* tok_off, int64_t n_tokens, int b, int64_t* base,
@@ -84,14 +86,15 @@ __device__ __forceinline__ int find_sorted(const int32_t* a, int n, int32_t v) {
 constexpr int kAWC = 8192;                 // above words per chunk held in shared memory
 constexpr int kLookupMaxSlots = 1 << 17;   // 4 x 4096 words + the chunk fit shared memory
 
-__global__ void __launch_bounds__(kCT)
+__global__ void __launch_bounds__(kLT)
     cache_step_lookup_kernel(const int64_t* __restrict__ tok_off, int64_t n_tokens, const int32_t* __restrict__ sel,
                              int m, const uint32_t* __restrict__ above, int early_cap, CacheArgs c,
                              int32_t* __restrict__ sel_slot, int32_t* status, uint32_t* stats) {
+    pdl_launch_dependents();  // the late recall's blocks may be scheduled now; they wait for this kernel
     extern __shared__ uint32_t smem[];
     __shared__ uint32_t scan[40];
     __shared__ uint32_t flags[2];
-    CacheStepLookup<kCT, kAWC> cs;
+    CacheStepLookup<kLT, kAWC> cs;
     cs.init(tok_off, n_tokens, blockIdx.x, sel, m, sel_slot, above, early_cap, c, status, stats, smem, scan, flags);
     cs.prologue_issue();  // the tables only: they may be read before the kernel before this one ends
     cs.prologue_finish();
@@ -114,6 +117,7 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
     __shared__ uint32_t scan[40];
     __shared__ uint32_t s_flags, s_early_used;
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_launch_dependents();  // the late recall's blocks may be scheduled now; they wait for this kernel
     pdl_wait();  // launched as a programmatic dependent: everything below may depend on the kernel before
     int64_t base, n;
     if (!request_range(tok_off, n_tokens, b, &base, &n) && tid == 0) set_status(status, ECHO_ST_BADDATA);
@@ -179,23 +183,22 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
     }
     __syncthreads();
 
-    // 0. the early set (the tokens echo_early_fetch copied) becomes resident
+    // 0. the early set (the tokens echo_early_fetch copied) and its slots; the
+    // slots leave the free bits, the tables learn only the selected early tokens
+    // (1a), and the slots of the others are held until the misses are placed
+    // (their early copies may still be in flight) and free again after the step
     uint32_t E = 0;
     if (early) {
         const uint32_t F = free_prefix<kCT>(fbs, words, scan, wpre, fbs);
         const uint32_t limit = (early_cap < 0) ? F : min(F, static_cast<uint32_t>(early_cap));
         const uint32_t found = early_assign<kCT, kEarlyWordsStep>(
             ab, nw, tail_mask, limit, 0u, limit, wpre, fbs, words, scan, v, [&](uint32_t r, int tok, int slot) {
-                // the marked tokens are not resident (the score kernel filtered them against these
-                // tables), so the tables are only written here, never read
                 if (slot < 0) {
                     set_status(status, ECHO_ST_BADDATA);
                     return;
                 }
                 etok[r] = tok;
                 eslot[r] = slot;
-                t2s[tok] = slot;
-                s2t[slot] = tok;
                 if (r < static_cast<uint32_t>(kES)) {
                     es_tok[r] = tok;
                     es_slot[r] = slot;
@@ -206,10 +209,12 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
         take_lowest_free<kCT>(fbs, words, E, wpre);
         __syncthreads();
     }
-    // With every early pair in shared memory, the values read before the early
-    // phase are corrected from there; otherwise the tables are read again
-    // (this block's own writes, visible after the barrier).
+    // the early pairs are looked up in shared memory when they all fit, else in
+    // the early lists just written (this block's own writes)
     const bool es_ok = E <= static_cast<uint32_t>(kES);
+    const int32_t* e_tok = es_ok ? es_tok : etok;
+    const int32_t* e_slot = es_ok ? es_slot : eslot;
+    uint32_t used = 0;
 
     // 1a. slots that hold a selected token are kept; the selection must be
     // ascending with -1 padding last
@@ -227,11 +232,15 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
             const int32_t nxt = (q + 1 < kPer) ? s[q + 1] : after;
             if (s[q] >= 0 && s[q] < n) {
                 if (nxt >= 0 && nxt <= s[q]) flags |= ECHO_ST_BADDATA;
-                if (chunks > 1 || !es_ok) {
-                    j[q] = t2s[s[q]];
-                } else if (E > 0 && j[q] < 0) {
-                    const int e = find_sorted(es_tok, static_cast<int>(E), s[q]);
-                    if (e >= 0) j[q] = es_slot[e];
+                if (chunks > 1) j[q] = t2s[s[q]];
+                if (j[q] < 0 && E > 0) {  // a selected early token becomes resident in its slot
+                    const int e = find_sorted(e_tok, static_cast<int>(E), s[q]);
+                    if (e >= 0) {
+                        j[q] = e_slot[e];
+                        t2s[s[q]] = j[q];
+                        s2t[j[q]] = s[q];
+                        ++used;
+                    }
                 }
             } else {
                 j[q] = -1;
@@ -258,26 +267,15 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
         const unsigned fm = __ballot_sync(0xffffffffu, freeing);
         if (lane == 0) fbs[w] |= fm;
     };
-    if (pre && es_ok) {
+    // (the owners read at the start: early slots were free then, so none of them is freed here)
+    if (pre) {
 #pragma unroll
         for (int r = 0; r < kPre; ++r) {
             const int w = warp + r * (kCT / 32);
-            if (w >= words) continue;
-            int32_t st = own[r];
-            if (st < 0 && E > 0) {  // a slot the early set took this step
-                const int e = find_sorted(es_slot, static_cast<int>(E), w * 32 + lane);
-                if (e >= 0) st = es_tok[e];
-            }
-            free_word(w, st);
+            if (w < words) free_word(w, own[r]);
         }
     } else {
         for (int w = warp; w < words; w += kCT / 32) free_word(w, s2t[w * 32 + lane]);
-    }
-    // early fetches of this step that the selection kept (their slot is kept)
-    uint32_t used = 0;
-    for (uint32_t e = tid; e < E; e += kCT) {
-        const int32_t es = es_ok ? es_slot[e] : eslot[e];
-        if (es >= 0 && es < C && ((keep[es >> 5] >> (es & 31)) & 1u)) ++used;
     }
     if (used) atomicAdd(&s_early_used, used);
     __syncthreads();
@@ -328,6 +326,12 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
     const uint32_t got = min(found, F);
     __syncthreads();  // every walk over fbs is done before its bits change
     take_lowest_free<kCT>(fbs, words, got, wpre);
+    __syncthreads();
+    // the held early slots (not kept by a selected token) are free again
+    for (uint32_t e = tid; e < E; e += kCT) {
+        const int32_t es = e_slot[e];
+        if (es >= 0 && es < C && !((keep[es >> 5] >> (es & 31)) & 1u)) atomicOr(&fbs[es >> 5], 1u << (es & 31));
+    }
     __syncthreads();
     for (int w = tid; w < words; w += kCT) fb[w] = fbs[w];
     if (tid == 0) {
@@ -380,6 +384,7 @@ __global__ void __launch_bounds__(kRecallThreads)
     __shared__ uint32_t scan[kRecallThreads / 32 + 1];
     const int lane = threadIdx.x & 31;
     const int warps = blockDim.x >> 5;
+    pdl_wait();  // the lists and counts come from the cache step (when launched as its dependent)
     uint32_t run = 0;
     for (int b0 = 0; b0 < B; b0 += kRecallThreads) {
         const int b = b0 + static_cast<int>(threadIdx.x);
@@ -529,7 +534,7 @@ __global__ void __launch_bounds__(kRecallThreads)
 
 cudaError_t launch_recall(int B, const int64_t* tok_off, int64_t n_tokens, int C, const int32_t* tok_list,
                           const int32_t* slot_list, const int32_t* cnt, const void* host_kv, void* dev_kv,
-                          int64_t row_bytes, int32_t* status, cudaStream_t s) {
+                          int64_t row_bytes, int32_t* status, cudaStream_t s, bool programmatic) {
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
     // A few large blocks: the host link, not the SMs, bounds the copy (32 x 16
@@ -544,10 +549,21 @@ cudaError_t launch_recall(int B, const int64_t* tok_off, int64_t n_tokens, int C
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(recall_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    recall_kernel<<<blocks, kRecallThreads, smem, s>>>(B, tok_off, n_tokens, C, tok_list, slot_list, cnt,
-                                                      static_cast<const uint8_t*>(host_kv),
-                                                      static_cast<uint8_t*>(dev_kv), row_bytes, status);
-    return cudaGetLastError();
+    // programmatic: the blocks may be scheduled while the kernel before them on
+    // `s` runs (the cache step lets them at its start); they wait for it first
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(kRecallThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = programmatic ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, recall_kernel, B, tok_off, n_tokens, C, tok_list, slot_list, cnt,
+                              static_cast<const uint8_t*>(host_kv), static_cast<uint8_t*>(dev_kv), row_bytes,
+                              status);
 }
 
 }  // namespace echo
@@ -575,7 +591,7 @@ int enqueue_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const in
     // still runs; it waits (griddepcontrol.wait) before anything else.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(B);
-    cfg.blockDim = dim3(kCT);
+    cfg.blockDim = dim3(lookup ? kLT : kCT);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -594,7 +610,8 @@ int enqueue_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const in
     const int rc = stream_wait(copy_stream, stream);
     if (rc) return rc;
     ECHO_CUDA_OK(launch_recall(B, tok_off, n_tokens, cache->C, cache->miss_tok, cache->miss_slot, cache->miss_cnt,
-                               cache->host_kv, cache->dev_kv, cache->row_bytes, status, copy_stream));
+                               cache->host_kv, cache->dev_kv, cache->row_bytes, status, copy_stream,
+                               copy_stream == stream));
     return ECHO_OK;
 }
 

@@ -29,12 +29,11 @@
 namespace echo {
 
 constexpr int kCsPer = 4;   // selection entries per thread per chunk
-constexpr int kCsPre = 4;   // 32-slot words per warp held in registers
 
 // Shared memory in 32-bit words: keep [words] | wpre [words + 1] | fbs [words]
-// | etaken [words] | aw [awc] | apre [awc + 1].
+// | etaken [words] | held [words] | aw [awc] | apre [awc + 1].
 __host__ __device__ constexpr size_t cache_lookup_smem_words(int C, int awc) {
-    return 4 * static_cast<size_t>(C / 32) + 1 + 2 * static_cast<size_t>(awc) + 1;
+    return 5 * static_cast<size_t>(C / 32) + 1 + 2 * static_cast<size_t>(awc) + 1;
 }
 
 template <int NT, int AWC>
@@ -56,13 +55,15 @@ struct CacheStepLookup {
     int32_t *t2s, *s2t, *mtok, *mslot;
     uint32_t* fb;
     // shared memory
-    uint32_t *keep, *wpre, *fbs, *etaken, *aw, *apre, *scan;
+    uint32_t *keep, *wpre, *fbs, *etaken, *held, *aw, *apre, *scan;
     uint32_t *s_flags, *s_used;
     // registers
-    int32_t s[kCsPer], j[kCsPer], own[kCsPre];
+    static constexpr int kPreW = 4096 / NT;                  // 32-slot words per warp held in registers
+    static constexpr int kAwPre = (NT >= 1024) ? 1 : 1024 / NT;  // above words per thread in the first round
+    int32_t s[kCsPer], j[kCsPer], own[kPreW];
     int64_t triv_n;           // >= 0: the selection is tokens 0 .. triv_n - 1 (not read from memory)
     int32_t after0;
-    uint32_t pf_fb, pf_aw;
+    uint32_t pf_fb, pf_aw[kAwPre];
     uint32_t limit, A;
 
     // smem: cache_lookup_smem_words(C, AWC) words; scan: 40 words; flags: 2 words.
@@ -92,12 +93,13 @@ struct CacheStepLookup {
         ab = early ? above + 4 * (base / 128 + b) : nullptr;
         nw = early ? static_cast<int>((n + 31) >> 5) : 0;
         tail_mask = (n & 31) ? (1u << (n & 31)) - 1u : ~0u;
-        pre = words <= kCsPre * (NT / 32);
+        pre = words <= kPreW * (NT / 32);
         keep = smem;
         wpre = keep + words;
         fbs = wpre + words + 1;
         etaken = fbs + words;
-        aw = etaken + words;
+        held = etaken + words;
+        aw = held + words;
         apre = aw + AWC;
         scan = scan_;
         s_flags = flags;
@@ -165,7 +167,7 @@ struct CacheStepLookup {
     __device__ void prologue_issue() {
         const int tid = static_cast<int>(threadIdx.x), lane = tid & 31, warp = tid >> 5;
 #pragma unroll
-        for (int r = 0; r < kCsPre; ++r) {
+        for (int r = 0; r < kPreW; ++r) {
             const int w = warp + r * (NT / 32);
             own[r] = (pre && w < words) ? s2t[w * 32 + lane] : -1;
         }
@@ -193,13 +195,23 @@ struct CacheStepLookup {
     }
 
     // The first chunk of above words, one per thread, into registers.
-    __device__ void load_above() { pf_aw = (threadIdx.x < min(nw, AWC)) ? above_word(threadIdx.x) : 0u; }
+    __device__ void load_above() {
+#pragma unroll
+        for (int i = 0; i < kAwPre; ++i) {
+            const int w = static_cast<int>(threadIdx.x) + i * NT;
+            pf_aw[i] = (w < min(nw, AWC)) ? above_word(w) : 0u;
+        }
+    }
 
     // The first chunk of above words into shared memory and its rank prefix.
     __device__ void above_finish() {
         const int tid = static_cast<int>(threadIdx.x);
         if (early) {
-            for (int w = tid; w < min(nw, AWC); w += NT) aw[w] = (w == tid) ? pf_aw : above_word(w);
+            const int lim = min(nw, AWC);
+#pragma unroll
+            for (int i = 0; i < kAwPre; ++i)
+                if (tid + i * NT < lim) aw[tid + i * NT] = pf_aw[i];
+            for (int w = tid + kAwPre * NT; w < lim; w += NT) aw[w] = above_word(w);
             __syncthreads();
             above_prefix(min(nw, AWC));
         }
@@ -260,10 +272,15 @@ struct CacheStepLookup {
         }
         const uint32_t E = min(A, limit);
         if (used) atomicAdd(s_used, used);
+        // the early set's slots (the lowest E free slots at the start) leave the free
+        // bits; the selected early tokens keep theirs, the others are held until the
+        // misses are placed (their early copies may still be in flight) and are free
+        // again after the step
+        for (int w = tid; w < words; w += NT) held[w] = fbs[w];
+        __syncthreads();  // every look-up walk over fbs is done before its bits change
+        take_lowest_free<NT>(fbs, words, E, wpre);
         __syncthreads();
-        // the selected early tokens keep their slots; the rest of the early set is
-        // free again by the end of the step, as its slots were at the start
-        for (int w = tid; w < words; w += NT) fbs[w] &= ~etaken[w];
+        for (int w = tid; w < words; w += NT) held[w] &= ~(fbs[w] | etaken[w]);
         __syncthreads();
 
         // 1a. slots that hold a selected token are kept; the selection must be
@@ -309,7 +326,7 @@ struct CacheStepLookup {
         };
         if (pre) {
 #pragma unroll
-            for (int r = 0; r < kCsPre; ++r) {
+            for (int r = 0; r < kPreW; ++r) {
                 const int w = warp + r * (NT / 32);
                 if (w < words) free_word(w, own[r]);
             }
@@ -365,7 +382,7 @@ struct CacheStepLookup {
         __syncthreads();  // every walk over fbs is done before its bits change
         take_lowest_free<NT>(fbs, words, got, wpre);
         __syncthreads();
-        for (int w = tid; w < words; w += NT) fb[w] = fbs[w];
+        for (int w = tid; w < words; w += NT) fb[w] = fbs[w] | held[w];
         if (tid == 0) {
             c.miss_cnt[b] = static_cast<int32_t>(got);
             c.early_cnt[b] = static_cast<int32_t>(E);

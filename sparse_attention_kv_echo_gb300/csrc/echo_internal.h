@@ -38,7 +38,7 @@ cudaError_t launch_quantize(int B, const float* q, const float* w, uint8_t* q8, 
                             uint32_t* hist_to_zero, int32_t* status, cudaStream_t s);
 cudaError_t launch_recall(int B, const int64_t* tok_off, int64_t n_tokens, int C, const int32_t* tok_list,
                           const int32_t* slot_list, const int32_t* cnt, const void* host_kv, void* dev_kv,
-                          int64_t row_bytes, int32_t* status, cudaStream_t s);
+                          int64_t row_bytes, int32_t* status, cudaStream_t s, bool programmatic);
 
 // Ask for the largest shared-memory carveout.  An SM reconfigures its
 // L1/shared split only when it drains, so a block of a kernel that needs little

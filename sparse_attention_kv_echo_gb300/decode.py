@@ -36,7 +36,12 @@ class DecodeLayer:
         self.B = int(tok_off.numel() - 1)
         self.n_tokens = int(k8.shape[0])
         self.k, self.C, self.alpha = int(k), int(C), float(alpha)
-        self.predictor, self.early_cap = bool(predictor), int(early_cap)
+        self.predictor = bool(predictor)
+        # the early set is capped at C - k on top of the caller's cap: the cache step holds the
+        # slots of unselected early tokens while it places the misses, so selected tokens plus
+        # held slots stay within C
+        room = self.C - self.k
+        self.early_cap = room if (early_cap < 0 or early_cap > room) else int(early_cap)
         self.tok_off = tok_off.to(device)
         self.k8, self.ks = k8, ks
         f32 = dict(dtype=torch.float32, device=device)
@@ -107,7 +112,7 @@ class DecodeLayer:
                     self._write_out(out_host, 0, self.B)
             return
         sms = torch.cuda.get_device_properties(main.device).multi_processor_count
-        streams, scored = [], None
+        scored = None
         for g, (b0, b1) in enumerate(self.groups):
             s = main if g == 0 else self.gstreams[g - 1]
             if scored is not None:
@@ -120,32 +125,31 @@ class DecodeLayer:
                            above=self.above_g[g], cache=self.views[g], stream=s, ctas=ctas)
             scored = torch.cuda.Event()
             scored.record(s)
-            streams.append(s)
             # the group's early rows stream over the host link on `s` (programmatic dependent of its
             # score kernel) while the next group is scored
             L.early_fetch(self.tok_off[b0:b1 + 1], self.n_tokens, self.above_g[g], self.early_cap, self.views[g],
                           self.status, stream=s)
         # top-k and the table update of every group on the groups' side streams once all scores are
         # done (a top-k started earlier would take SMs the next score kernel counts on); the late
-        # misses of a group follow its early fetch on its stream
+        # misses of a group follow its cache step on the side stream (a miss never takes a slot the
+        # early fetch is still writing), so they share the host link with the early rows
         for g, (b0, b1) in enumerate(self.groups):
-            side, s = self.sides[g], streams[g]
+            side = self.sides[g]
             side.wait_event(scored)
             off = self.tok_off[b0:b1 + 1]
             L.topk_select(off, self.n_tokens, self.scores, self.k, self.hist[b0:b1], self.theta[b0:b1],
                           self.alpha, self.sel_idx[b0:b1], self.kth[b0:b1], self.status, stats=self.stats,
                           stream=side)
             L.cache_step(off, self.n_tokens, self.sel_idx[b0:b1], self.views[g], self.sel_slot[b0:b1], self.status,
-                         stats=self.stats, stream=side, copy_stream=s, above=self.above_g[g],
+                         stats=self.stats, stream=side, copy_stream=side, above=self.above_g[g],
                          early_cap=self.early_cap)
             if out_host is not None:
                 with torch.cuda.stream(side):
                     self._write_out(out_host, b0, b1)
         for gs in self.gstreams:
             main.wait_stream(gs)
-        if out_host is not None:
-            for side in self.sides:
-                main.wait_stream(side)
+        for side in self.sides:
+            main.wait_stream(side)
 
     def _write_out(self, out_host, b0, b1):
         # elementwise kernels, not copy-engine transfers: their stores go straight to the

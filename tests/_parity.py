@@ -111,8 +111,11 @@ def run_decode(w: wl.Workload, steps: int, predictor: bool, cap: int = -1, score
             assert np.array_equal(gh[b], orc.hist256(sc, theta_before[b])), (t, b, "hist")
             t2s = o.t2s[lo:hi]
             s2t = o.s2t[b * w.C:(b + 1) * w.C]
+            et = None
             if predictor:
-                et, es = orc.early_fetch(sc, theta_before[b], cap, t2s, s2t)
+                # the layer's cap: the caller's, capped at C - k (the oracle's rule, pinned on the CPU)
+                assert lay.early_cap == orc.early_cap_for(cap, w.C, w.k)
+                et, es = orc.early_fetch(sc, theta_before[b], lay.early_cap, t2s, s2t)
                 assert g_ecnt[b] == et.size, (t, b, "early count", g_ecnt[b], et.size)
                 assert np.array_equal(g_etok[b * w.C:b * w.C + et.size], et), (t, b, "early tok")
                 assert np.array_equal(g_eslot[b * w.C:b * w.C + et.size], es), (t, b, "early slot")
@@ -123,7 +126,7 @@ def run_decode(w: wl.Workload, steps: int, predictor: bool, cap: int = -1, score
             o.theta[b] = orc.ema(theta_before[b], kth, 0.5)
             assert g_theta[b] == o.theta[b] or (np.isinf(o.theta[b]) and np.isinf(g_theta[b])), \
                 (t, b, "theta", g_theta[b], o.theta[b])
-            sel_slot, mt, ms, _ = orc.cache_step(idx, t2s, s2t)
+            sel_slot, mt, ms, _ = orc.cache_step(idx, t2s, s2t, early_tok=et)
             assert np.array_equal(g_slot[b], sel_slot), (t, b, "sel_slot")
             assert g_mcnt[b] == mt.size, (t, b, "miss count", g_mcnt[b], mt.size)
             assert np.array_equal(g_mtok[b * w.C:b * w.C + mt.size], mt), (t, b, "miss tok")

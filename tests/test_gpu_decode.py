@@ -62,6 +62,14 @@ def test_early_set_larger_than_one_staging_round():
     assert max(rep["early"]) > 4096, rep["early"]
 
 
+def test_walking_cache_step_with_large_early_sets():
+    """C above the look-up form's limit (2^17 slots): the cache step walks the early set, which a
+    query redraw makes larger than the 4096 pairs it keeps in shared memory."""
+    w = wl.scaled(wl.WORKLOADS["skewed"], "walk", B=1, lengths=(200000,), k=6144, C=140000)
+    rep = run_decode(w, 10, predictor=True, score_sample=1024)
+    assert max(rep["early"]) > 4096, rep["early"]
+
+
 def test_batch_workload_full_size():
     """8 x 32768, k=2048, C=4096: every table/selection bit-exact, scores sampled."""
     w = wl.WORKLOADS["batch"]

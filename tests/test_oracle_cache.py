@@ -21,11 +21,12 @@ def test_golden_walkthrough(orc):
     t2s = np.full(g["N"], -1, np.int32)
     s2t = np.full(g["C"], -1, np.int32)
     for st in g["steps"]:
+        et = None
         if "early" in st:
             e = st["early"]
             et, es = orc.early_fetch(np.array(e["scores"], np.float32), e["theta"], e["cap"], t2s, s2t)
             assert list(et) == e["early_tok"] and list(es) == e["early_slot"], st["why"]
-        sel_slot, mt, ms, nf = orc.cache_step(np.array(st["sel"], np.int32), t2s, s2t)
+        sel_slot, mt, ms, nf = orc.cache_step(np.array(st["sel"], np.int32), t2s, s2t, early_tok=et)
         assert list(sel_slot) == st["sel_slot"], st["why"]
         assert list(mt) == st["miss_tok"] and list(ms) == st["miss_slot"], st["why"]
         assert nf == st["nfreed"], st["why"]
@@ -94,6 +95,24 @@ def test_capacity_error_leaves_state(orc):
     with pytest.raises(orc.OracleError):
         orc.cache_step(np.array([1, 2, 3], np.int32), t2s, s2t)
     assert np.all(t2s == -1) and np.all(s2t == -1)
+
+
+def test_held_early_slots_count_against_capacity(orc):
+    """Selected tokens plus the held slots of unselected early tokens must fit in C; the early cap
+    C - k of a decode step guarantees it (the early set leaves room for k misses)."""
+    t2s = np.full(10, -1, np.int32)
+    s2t = np.full(3, -1, np.int32)
+    et, es = orc.early_fetch(np.array([0, 0, 0, 0, 0, 0, 0, 2.0, 2.0, 0], np.float32), 1.0, -1, t2s, s2t)
+    assert list(et) == [7, 8] and list(es) == [0, 1]
+    before = (t2s.copy(), s2t.copy())
+    with pytest.raises(orc.OracleError):                     # 2 selected + 2 held > 3
+        orc.cache_step(np.array([1, 2], np.int32), t2s, s2t, early_tok=et)
+    assert np.array_equal(t2s, before[0]) and np.array_equal(s2t, before[1])
+    sel_slot, mt, ms, nf = orc.cache_step(np.array([2, 7], np.int32), t2s, s2t, early_tok=et)
+    assert list(sel_slot) == [2, 0] and list(mt) == [2] and list(ms) == [2] and nf == 1
+    assert list(s2t) == [7, -1, 2]                           # slot 1 (held for 8) is free again
+    assert [orc.early_cap_for(c, 4096, 2048) for c in (-1, 0, 100, 2048, 5000)] == [2048, 0, 100, 2048, 2048]
+    assert orc.early_cap_for(-1, 64, 64) == 0
 
 
 def test_early_fetch_strict_and_inf(orc):
