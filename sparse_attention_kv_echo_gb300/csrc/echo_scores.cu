@@ -231,7 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // do not depend on it); the q8 of every request after the first (which
         // the MMA warp loads) come after that wait.
         if (ntiles > 0 && lane == 0) {
-            const uint64_t pol = policy_evict_first();
+            // keys and scales stream through L2 once; the slot table stays in L2 for the
+            // cache step, which looks up the selected tokens' slots in it (a miss to HBM
+            // waits behind the host-link traffic of the early fetch)
+            const uint64_t pol = policy_evict_first(), pol_keep = policy_evict_last();
             const uint32_t prefill = ntiles < static_cast<uint32_t>(kStages) ? ntiles : kStages;
             const uint32_t side_tx = kSideBytes * (a.has_res ? 2u : 1u);
             int kb = find_request(tstart, B, t_begin);   // request of the next key load
@@ -256,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d_hint(smem_addr(keys + s * kKeyBytes), &kmap, full, 0, static_cast<int32_t>(tok0), pol);
                 mbar_arrive_expect_tx(sfull, side_tx);
                 tma_load_1d_hint(smem_addr(&ctl->ks[ss][0]), &smap, sfull, x0, pol);
-                if (a.has_res) tma_load_1d_hint(smem_addr(&ctl->res[ss][0]), &rmap, sfull, x0, pol);
+                if (a.has_res) tma_load_1d_hint(smem_addr(&ctl->res[ss][0]), &rmap, sfull, x0, pol_keep);
                 return true;
             };
             for (; issued < prefill; ++issued)
