@@ -189,9 +189,8 @@ int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens, const uin
  * Enqueue it on the stream of echo_index_scores right after it: it is
  * launched as a programmatic dependent of the score kernel.  It reads neither
  * the scores nor the threshold, so echo_topk_select may run on another stream
- * meanwhile; the late-miss recall of echo_cache_step must be ordered after it
- * (its copy_stream = this stream), since a slot fetched early and then freed
- * may be handed to a miss.
+ * meanwhile.  The cache step never hands a slot of this set to a miss of the
+ * same step, so its late recall need not wait for this copy.
  */
 int echo_early_fetch(int B, const int64_t* tok_off, int64_t n_tokens, const uint32_t* above, int early_cap,
                      const echo_cache* cache, int32_t* status, echo_stream_t stream);
@@ -228,13 +227,18 @@ int echo_topk_select(int B, const int64_t* tok_off, int64_t n_tokens, const floa
  *      slots that call copied it to, and early_cnt[b] = its size E (0
  *      without above);
  *   1. every resident token that is not selected is freed (both table
- *      entries -1, its free bit set); its bytes stay, nothing is written back;
+ *      entries -1); its bytes stay, nothing is written back.  Its free bit is
+ *      set, except for an early token: its slot is held until step 2 is done
+ *      (its early copy may still be in flight) and is free after the step;
  *   2. the selected tokens that are not resident (the misses), in ascending
  *      order, take the lowest free slots in ascending order;
  *   3. sel_slot [B,m] = slot of each selected token (-1 for padding);
  *   4. the miss rows are copied host_kv[tok_off[b] + t] -> dev_kv[b*C + slot],
- *      on copy_stream (which may equal stream; an event orders it after 0-3).
- * Needs m <= C.  Steps 0-3 are launched as a programmatic dependent of the
+ *      on copy_stream (which may equal stream: then as a programmatic
+ *      dependent of steps 0-3; else an event orders it after them).
+ * Needs m <= C, and m + (unselected early tokens) <= C, which an early_cap
+ * of at most C - m guarantees (else a miss may find no slot:
+ * ECHO_ST_NOSLOT).  Steps 0-3 are launched as a programmatic dependent of the
  * kernel before them on `stream`: while that kernel still runs (if it lets
  * dependents start early, as echo_topk_select and echo_index_scores do) they
  * may read slot2tok and freebits, which none of this library's kernels but
@@ -244,6 +248,30 @@ int echo_topk_select(int B, const int64_t* tok_off, int64_t n_tokens, const floa
 int echo_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
                     const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,
                     int32_t* status, uint32_t* stats, echo_stream_t stream, echo_stream_t copy_stream);
+
+/*
+ * The two calls above with the cache step's look-up done by top-k:
+ * echo_topk_select_cached is echo_topk_select (m = k) that also writes, for
+ * every selected entry, sel_slot[b,i] = the slot the token holds at the
+ * start of the cache step (step 0 of echo_cache_step: its resident slot, or
+ * for a token of the early set, given above and early_cap as there, the
+ * slot echo_early_fetch copied it to, which this call enters into tok2slot
+ * and slot2tok), -1 for a miss or padding, and early_cnt[b] = E.  The
+ * request's free bits must be as echo_early_fetch saw them (nothing between
+ * the two calls changes them).  Needs C <= 32768 (ECHO_EUNSUPPORTED
+ * otherwise) and reads the free bits and tables of `cache`.
+ * echo_cache_step_resolved then does steps 1-4 of echo_cache_step with those
+ * slots (sel_slot in/out, early_cnt in), launched the same way; needs
+ * C <= 131072.  Together they give exactly the tables, slots, lists and rows
+ * of echo_topk_select followed by echo_cache_step.
+ */
+int echo_topk_select_cached(int B, const int64_t* tok_off, int64_t n_tokens, const float* scores, int k,
+                            const uint32_t* hist, float* theta_hat, float alpha, int32_t* sel_idx, float* kth,
+                            const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,
+                            int32_t* status, uint32_t* stats, echo_stream_t stream);
+int echo_cache_step_resolved(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
+                             const echo_cache* cache, int32_t* sel_slot, int32_t* status, uint32_t* stats,
+                             echo_stream_t stream, echo_stream_t copy_stream);
 
 /*
  * Chunked prefill [EXPL panel "Prefill: one-round histogram"; AE section

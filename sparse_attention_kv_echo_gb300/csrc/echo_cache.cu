@@ -89,13 +89,14 @@ constexpr int kLookupMaxSlots = 1 << 17;   // 4 x 4096 words + the chunk fit sha
 __global__ void __launch_bounds__(kLT)
     cache_step_lookup_kernel(const int64_t* __restrict__ tok_off, int64_t n_tokens, const int32_t* __restrict__ sel,
                              int m, const uint32_t* __restrict__ above, int early_cap, CacheArgs c,
-                             int32_t* __restrict__ sel_slot, int32_t* status, uint32_t* stats) {
+                             int32_t* sel_slot, int32_t* status, uint32_t* stats, bool resolved) {
     pdl_launch_dependents();  // the late recall's blocks may be scheduled now; they wait for this kernel
     extern __shared__ uint32_t smem[];
     __shared__ uint32_t scan[40];
     __shared__ uint32_t flags[2];
     CacheStepLookup<kLT, kAWC> cs;
-    cs.init(tok_off, n_tokens, blockIdx.x, sel, m, sel_slot, above, early_cap, c, status, stats, smem, scan, flags);
+    cs.init(tok_off, n_tokens, blockIdx.x, sel, m, sel_slot, above, early_cap, c, status, stats, smem, scan, flags,
+            resolved ? sel_slot : nullptr);
     cs.prologue_issue();  // the tables only: they may be read before the kernel before this one ends
     cs.prologue_finish();
     pdl_wait();           // the selection and the above words come from the kernels before this one
@@ -572,8 +573,10 @@ namespace echo {
 
 int enqueue_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
                        const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,
-                       int32_t* status, uint32_t* stats, cudaStream_t stream, cudaStream_t copy_stream) {
+                       int32_t* status, uint32_t* stats, cudaStream_t stream, cudaStream_t copy_stream,
+                       bool resolved) {
     const bool lookup = cache->C <= kLookupMaxSlots;
+    if (resolved && !lookup) return ECHO_EUNSUPPORTED;
     const size_t smem =
         (lookup ? cache_lookup_smem_words(cache->C, kAWC) : cache_step_smem_words(cache->C)) * sizeof(uint32_t);
     if (lookup) {
@@ -601,8 +604,9 @@ int enqueue_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const in
     cfg.numAttrs = 1;
     const CacheArgs ca = cache_args(*cache);
     if (lookup) {
-        ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, cache_step_lookup_kernel, tok_off, n_tokens, sel, m, above, early_cap,
-                                        ca, sel_slot, status, stats));
+        ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, cache_step_lookup_kernel, tok_off, n_tokens, sel, m,
+                                        resolved ? nullptr : above, early_cap, ca, sel_slot, status, stats,
+                                        resolved));
     } else {
         ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, cache_step_kernel, tok_off, n_tokens, sel, m, above, early_cap, ca,
                                         sel_slot, status, stats));
@@ -637,7 +641,19 @@ extern "C" int echo_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, 
     const int rc = check_cache_step_args(B, n_tokens, sel, m, cache, sel_slot);
     if (rc) return rc;
     return enqueue_cache_step(B, tok_off, n_tokens, sel, m, above, early_cap, cache, sel_slot, status, stats, stream,
-                              copy_stream);
+                              copy_stream, false);
+}
+
+extern "C" int echo_cache_step_resolved(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
+                                        const echo_cache* cache, int32_t* sel_slot, int32_t* status, uint32_t* stats,
+                                        echo_stream_t stream, echo_stream_t copy_stream) {
+    using namespace echo;
+    if (!tok_off || !status) return ECHO_EINVAL;
+    const int rc = check_cache_step_args(B, n_tokens, sel, m, cache, sel_slot);
+    if (rc) return rc;
+    if (cache->C > kLookupMaxSlots) return ECHO_EUNSUPPORTED;
+    return enqueue_cache_step(B, tok_off, n_tokens, sel, m, nullptr, 0, cache, sel_slot, status, stats, stream,
+                              copy_stream, true);
 }
 
 extern "C" int echo_early_fetch(int B, const int64_t* tok_off, int64_t n_tokens, const uint32_t* above,

@@ -14,6 +14,11 @@
 // starting free bits.  The early set is never walked: one scan over the above
 // words, one over the free bits, O(1) work per selected token.
 //
+// Resolved form: top-k already looked up every selected token's slot
+// (resident or early, -1 for a miss; echo_topk_select_cached) and the early
+// set's size; the step reads those instead of the above words and the tables,
+// and does the rest.
+//
 // Order of the parts: prologue_issue() and prologue_finish() read only the
 // cache's own tables (slot owners, free bits: the free-slot prefix and the
 // early limit), so a kernel may run them before it waits for the kernel that
@@ -31,9 +36,9 @@ namespace echo {
 constexpr int kCsPer = 4;   // selection entries per thread per chunk
 
 // Shared memory in 32-bit words: keep [words] | wpre [words + 1] | fbs [words]
-// | etaken [words] | held [words] | aw [awc] | apre [awc + 1].
+// | held [words] | aw [awc] | apre [awc + 1].
 __host__ __device__ constexpr size_t cache_lookup_smem_words(int C, int awc) {
-    return 5 * static_cast<size_t>(C / 32) + 1 + 2 * static_cast<size_t>(awc) + 1;
+    return 4 * static_cast<size_t>(C / 32) + 1 + 2 * static_cast<size_t>(awc) + 1;
 }
 
 template <int NT, int AWC>
@@ -55,7 +60,10 @@ struct CacheStepLookup {
     int32_t *t2s, *s2t, *mtok, *mslot;
     uint32_t* fb;
     // shared memory
-    uint32_t *keep, *wpre, *fbs, *etaken, *held, *aw, *apre, *scan;
+    uint32_t *keep, *wpre, *fbs, *held, *aw, *apre, *scan;
+    const int32_t* pre_slot;  // resolved form: the selection's slots as top-k looked them up
+    bool resolved;
+    int32_t E_pre;            // resolved form: the early set's size
     uint32_t *s_flags, *s_used;
     // registers
     static constexpr int kPreW = 4096 / NT;                  // 32-slot words per warp held in registers
@@ -64,12 +72,13 @@ struct CacheStepLookup {
     int64_t triv_n;           // >= 0: the selection is tokens 0 .. triv_n - 1 (not read from memory)
     int32_t after0;
     uint32_t pf_fb, pf_aw[kAwPre];
-    uint32_t limit, A;
+    uint32_t limit, A, F0;
 
     // smem: cache_lookup_smem_words(C, AWC) words; scan: 40 words; flags: 2 words.
     __device__ void init(const int64_t* tok_off, int64_t n_tokens, int b_, const int32_t* sel, int m_,
                          int32_t* sel_slot, const uint32_t* above, int cap, const CacheArgs& args, int32_t* st,
-                         uint32_t* sts, uint32_t* smem, uint32_t* scan_, uint32_t* flags) {
+                         uint32_t* sts, uint32_t* smem, uint32_t* scan_, uint32_t* flags,
+                         const int32_t* pre_slot_ = nullptr) {
         c = args;
         b = b_;
         m = m_;
@@ -89,7 +98,10 @@ struct CacheStepLookup {
         sl = sel + static_cast<int64_t>(b) * m;
         out = sel_slot + static_cast<int64_t>(b) * m;
         chunks = (m + NT * kCsPer - 1) / (NT * kCsPer);
-        early = above != nullptr && early_cap != 0 && n > 0;
+        pre_slot = pre_slot_ ? pre_slot_ + static_cast<int64_t>(b) * m : nullptr;
+        resolved = pre_slot_ != nullptr;
+        E_pre = 0;
+        early = !resolved && above != nullptr && early_cap != 0 && n > 0;
         ab = early ? above + 4 * (base / 128 + b) : nullptr;
         nw = early ? static_cast<int>((n + 31) >> 5) : 0;
         tail_mask = (n & 31) ? (1u << (n & 31)) - 1u : ~0u;
@@ -97,8 +109,7 @@ struct CacheStepLookup {
         keep = smem;
         wpre = keep + words;
         fbs = wpre + words + 1;
-        etaken = fbs + words;
-        held = etaken + words;
+        held = fbs + words;
         aw = held + words;
         apre = aw + AWC;
         scan = scan_;
@@ -106,6 +117,7 @@ struct CacheStepLookup {
         s_used = flags + 1;
         limit = 0;
         A = 0;
+        F0 = 0;
         triv_n = -1;
     }
 
@@ -132,9 +144,17 @@ struct CacheStepLookup {
     __device__ void load_selection() {
         load_sel(0);
         after0 = sel_at(kCsPer * static_cast<int>(threadIdx.x) + kCsPer);
+        if (resolved) {  // the slots top-k looked up, loaded with the selection
+#pragma unroll
+            for (int q = 0; q < kCsPer; ++q) {
+                const int i = kCsPer * static_cast<int>(threadIdx.x) + q;
+                j[q] = (i < m) ? pre_slot[i] : -1;
+            }
+            E_pre = c.early_cnt[b];
+        }
     }
     __device__ void load_slots() {
-        if (chunks == 1) {
+        if (chunks == 1 && !resolved) {
 #pragma unroll
             for (int q = 0; q < kCsPer; ++q) j[q] = (s[q] >= 0 && s[q] < n) ? t2s[s[q]] : -1;
         }
@@ -181,15 +201,14 @@ struct CacheStepLookup {
         for (int w = tid; w < words; w += NT) {
             fbs[w] = (w == tid) ? pf_fb : fb[w];
             keep[w] = 0u;
-            etaken[w] = 0u;
         }
         if (tid == 0) {
             *s_flags = range_ok ? 0u : static_cast<uint32_t>(ECHO_ST_BADDATA);
             *s_used = 0;
         }
         __syncthreads();
-        if (early) {
-            const uint32_t F0 = free_prefix<NT>(fbs, words, scan, wpre, fbs);
+        if (early || resolved) {
+            F0 = free_prefix<NT>(fbs, words, scan, wpre, fbs);
             limit = (early_cap < 0) ? F0 : min(F0, static_cast<uint32_t>(early_cap));
         }
     }
@@ -237,7 +256,6 @@ struct CacheStepLookup {
         }
         t2s[sv] = slot;
         s2t[slot] = sv;
-        atomicOr(&etaken[slot >> 5], 1u << (slot & 31));
         ++*used;
         return slot;
     }
@@ -270,17 +288,18 @@ struct CacheStepLookup {
                 }
             }
         }
-        const uint32_t E = min(A, limit);
+        const uint32_t E = resolved ? min(static_cast<uint32_t>(max(E_pre, 0)), F0) : min(A, limit);
         if (used) atomicAdd(s_used, used);
         // the early set's slots (the lowest E free slots at the start) leave the free
         // bits; the selected early tokens keep theirs, the others are held until the
         // misses are placed (their early copies may still be in flight) and are free
-        // again after the step
+        // again after the step (held: the early set's slots; the kept ones are
+        // dropped from it at the end)
         for (int w = tid; w < words; w += NT) held[w] = fbs[w];
         __syncthreads();  // every look-up walk over fbs is done before its bits change
         take_lowest_free<NT>(fbs, words, E, wpre);
         __syncthreads();
-        for (int w = tid; w < words; w += NT) held[w] &= ~(fbs[w] | etaken[w]);
+        for (int w = tid; w < words; w += NT) held[w] &= ~fbs[w];
         __syncthreads();
 
         // 1a. slots that hold a selected token are kept; the selection must be
@@ -382,13 +401,15 @@ struct CacheStepLookup {
         __syncthreads();  // every walk over fbs is done before its bits change
         take_lowest_free<NT>(fbs, words, got, wpre);
         __syncthreads();
-        for (int w = tid; w < words; w += NT) fb[w] = fbs[w] | held[w];
+        for (int w = tid; w < words; w += NT) fb[w] = fbs[w] | (held[w] & ~keep[w]);
         if (tid == 0) {
             c.miss_cnt[b] = static_cast<int32_t>(got);
-            c.early_cnt[b] = static_cast<int32_t>(E);
             if (stats && got) atomicAdd(stats + ECHO_STAT_MISSES, got);
-            if (stats && E) atomicAdd(stats + ECHO_STAT_EARLY, E);
-            if (stats && *s_used) atomicAdd(stats + ECHO_STAT_EARLY_USED, *s_used);
+            if (!resolved) {  // (the resolved form's top-k counted the early set)
+                c.early_cnt[b] = static_cast<int32_t>(E);
+                if (stats && E) atomicAdd(stats + ECHO_STAT_EARLY, E);
+                if (stats && *s_used) atomicAdd(stats + ECHO_STAT_EARLY_USED, *s_used);
+            }
             uint32_t flags = *s_flags;
             if (found > F) flags |= ECHO_ST_NOSLOT;
             if (flags) set_status(status, static_cast<int>(flags));

@@ -78,8 +78,13 @@ struct FreeWalk {
     const uint32_t* fbs;
     int words, w;
     uint32_t f;
-    __device__ FreeWalk(const uint32_t* wpre, const uint32_t* fbs_, int words_, uint32_t r)
-        : fbs(fbs_), words(words_) {
+    __device__ FreeWalk() {}
+    __device__ FreeWalk(const uint32_t* wpre, const uint32_t* fbs_, int words_, uint32_t r) {
+        init(wpre, fbs_, words_, r);
+    }
+    __device__ void init(const uint32_t* wpre, const uint32_t* fbs_, int words_, uint32_t r) {
+        fbs = fbs_;
+        words = words_;
         int lo = 0, hi = words - 1;  // largest w with wpre[w] <= r
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;

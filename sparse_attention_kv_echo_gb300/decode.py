@@ -31,12 +31,16 @@ from . import _lib as L
 class DecodeLayer:
     def __init__(self, tok_off, k8: torch.Tensor, ks: torch.Tensor, k: int, C: int,
                  host_pool: torch.Tensor, alpha: float = 0.5, predictor: bool = True,
-                 early_cap: int = -1, groups: int | None = None, first_share: float = 0.5, device="cuda"):
+                 early_cap: int = -1, groups: int | None = None, first_share: float = 0.5,
+                 resolved: bool = True, device="cuda"):
         tok_off = torch.as_tensor(tok_off, dtype=torch.int64)
         self.B = int(tok_off.numel() - 1)
         self.n_tokens = int(k8.shape[0])
         self.k, self.C, self.alpha = int(k), int(C), float(alpha)
         self.predictor = bool(predictor)
+        # top-k looks up the selected tokens' slots itself (the cache step then frees and places
+        # the misses) when the request's free bits fit its shared memory
+        self.resolved = bool(resolved) and self.C <= L.TOPK_CACHED_MAX_SLOTS
         # the early set is capped at C - k on top of the caller's cap: the cache step holds the
         # slots of unselected early tokens while it places the misses, so selected tokens plus
         # held slots stay within C
@@ -137,12 +141,21 @@ class DecodeLayer:
             side = self.sides[g]
             side.wait_event(scored)
             off = self.tok_off[b0:b1 + 1]
-            L.topk_select(off, self.n_tokens, self.scores, self.k, self.hist[b0:b1], self.theta[b0:b1],
-                          self.alpha, self.sel_idx[b0:b1], self.kth[b0:b1], self.status, stats=self.stats,
-                          stream=side)
-            L.cache_step(off, self.n_tokens, self.sel_idx[b0:b1], self.views[g], self.sel_slot[b0:b1], self.status,
-                         stats=self.stats, stream=side, copy_stream=side, above=self.above_g[g],
-                         early_cap=self.early_cap)
+            if self.resolved:
+                # top-k looks up every selected token's slot (resident or early) on its slices
+                L.topk_select_cached(off, self.n_tokens, self.scores, self.k, self.hist[b0:b1], self.theta[b0:b1],
+                                     self.alpha, self.sel_idx[b0:b1], self.kth[b0:b1], self.views[g],
+                                     self.sel_slot[b0:b1], self.status, stats=self.stats, stream=side,
+                                     above=self.above_g[g], early_cap=self.early_cap)
+                L.cache_step_resolved(off, self.n_tokens, self.sel_idx[b0:b1], self.views[g], self.sel_slot[b0:b1],
+                                      self.status, stats=self.stats, stream=side, copy_stream=side)
+            else:
+                L.topk_select(off, self.n_tokens, self.scores, self.k, self.hist[b0:b1], self.theta[b0:b1],
+                              self.alpha, self.sel_idx[b0:b1], self.kth[b0:b1], self.status, stats=self.stats,
+                              stream=side)
+                L.cache_step(off, self.n_tokens, self.sel_idx[b0:b1], self.views[g], self.sel_slot[b0:b1],
+                             self.status, stats=self.stats, stream=side, copy_stream=side, above=self.above_g[g],
+                             early_cap=self.early_cap)
             if out_host is not None:
                 with torch.cuda.stream(side):
                     self._write_out(out_host, b0, b1)

@@ -63,7 +63,7 @@ def check_scores(layer_inputs, q, w, gpu_scores, sample=None, rng=None):
 
 
 def run_decode(w: wl.Workload, steps: int, predictor: bool, cap: int = -1, score_sample=None,
-               check_every_score_step=True, keys_device="cpu", layer: int = 0):
+               check_every_score_step=True, keys_device="cpu", layer: int = 0, resolved: bool = True):
     """Runs `steps` decode steps of one layer on the GPU and checks each against the oracle."""
     dev = "cuda"
     off = wl.tok_offsets(w.lengths)
@@ -73,7 +73,8 @@ def run_decode(w: wl.Workload, steps: int, predictor: bool, cap: int = -1, score
     wt = wl.make_weights(w, layer, device=keys_device).cpu()
     host = wl.make_host_pool(w, layer, device=keys_device, pin=True)
     host_before = host.clone()
-    lay = DecodeLayer(off, k8c.to(dev), ksc.to(dev), w.k, w.C, host, predictor=predictor, early_cap=cap)
+    lay = DecodeLayer(off, k8c.to(dev), ksc.to(dev), w.k, w.C, host, predictor=predictor, early_cap=cap,
+                      resolved=resolved)
     o = OracleLayer(w.B, w.total_tokens, w.C)
     qsrc = wl.QueryStream(w, layer, device=keys_device)
     rng = np.random.default_rng(7)

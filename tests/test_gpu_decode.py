@@ -26,6 +26,19 @@ def test_tiny_workload_all_steps():
     assert rep["misses"][0] == w.k                     # first step: everything misses
 
 
+def test_tiny_workload_table_look_up_in_the_cache_step():
+    """The decode step with the look-up in the cache step (echo_topk_select + echo_cache_step)
+    instead of in top-k."""
+    w = wl.WORKLOADS["tiny"]
+    rep = run_decode(w, w.steps, predictor=True, resolved=False)
+    assert sum(rep["early"]) > 0
+
+
+def test_batch_workload_table_look_up_in_the_cache_step():
+    w = wl.WORKLOADS["batch"]
+    run_decode(w, 4, predictor=True, score_sample=256, check_every_score_step=False, resolved=False)
+
+
 def test_tiny_predictor_off():
     w = wl.WORKLOADS["tiny"]
     rep = run_decode(w, 6, predictor=False)
