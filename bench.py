@@ -57,6 +57,8 @@ def parse_args(argv=None):
                    help="request groups of the decode step (default: the layer's choice)")
     p.add_argument("--lookup-in", choices=["topk", "cache-step"], default="topk",
                    help="where the selected tokens' slots are looked up (top-k's slices or the cache step)")
+    p.add_argument("--hold-early", action="store_true",
+                   help="the held-slot variant of the cache step (the late recall need not wait for the early copy)")
     p.add_argument("--first-share", type=float, default=None,
                    help="share of the requests in the first of two groups (default: the layer's choice)")
     return p.parse_args(argv)
@@ -241,6 +243,7 @@ def run_ours(args):
     S = q_all.shape[0]
     kw = {} if args.first_share is None else {"first_share": args.first_share}
     kw["resolved"] = args.lookup_in == "topk"
+    kw["hold_early"] = bool(args.hold_early)
     lay = DecodeLayer(off, k8, ks, w.k, w.C, host, device=dev, groups=args.groups, **kw)
     main = torch.cuda.Stream()
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -416,7 +419,8 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8-e4m3 MMA, fp32 accumulate/epilogue, int32 tables",
         "data": "synthetic (seeded; shapes of the evaluation workloads)",
         "config": dict(workload_config(w), request_groups=len(lay.groups),
-                       slot_lookup="top-k" if lay.resolved else "cache step"),
+                       slot_lookup="top-k" if lay.resolved else "cache step",
+                       early_slots="held through the miss placement" if lay.hold_early else "free for misses"),
         "roofline": {"kernel": "score_kernel (echo_index_scores)", "bound": "hbm", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"hbm_gbs, {peak_kind}", "algorithmic_bytes": score_bytes,

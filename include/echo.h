@@ -78,6 +78,9 @@ typedef struct CUstream_st* echo_stream_t; /* a cudaStream_t; NULL = legacy defa
 #define ECHO_STAT_EARLY_USED 4      /* early-fetched tokens that top-k then selected */
 #define ECHO_STATS_N 8
 
+/* echo_cache_step flags */
+#define ECHO_CACHE_HOLD_EARLY 1     /* hold the unselected early tokens' slots until the misses are placed */
+
 #define ECHO_HEADS 64           /* index heads */
 #define ECHO_DIM 128            /* index head dimension (bytes per E4M3 key row) */
 #define ECHO_MAX_REQUESTS 4096  /* requests per call */
@@ -189,8 +192,10 @@ int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens, const uin
  * Enqueue it on the stream of echo_index_scores right after it: it is
  * launched as a programmatic dependent of the score kernel.  It reads neither
  * the scores nor the threshold, so echo_topk_select may run on another stream
- * meanwhile.  The cache step never hands a slot of this set to a miss of the
- * same step, so its late recall need not wait for this copy.
+ * meanwhile.  The late-miss recall of echo_cache_step must be ordered after
+ * it (its copy_stream = this stream), since a slot fetched early and then
+ * freed may be handed to a miss, unless the cache step holds those slots
+ * (ECHO_CACHE_HOLD_EARLY).
  */
 int echo_early_fetch(int B, const int64_t* tok_off, int64_t n_tokens, const uint32_t* above, int early_cap,
                      const echo_cache* cache, int32_t* status, echo_stream_t stream);
@@ -227,18 +232,21 @@ int echo_topk_select(int B, const int64_t* tok_off, int64_t n_tokens, const floa
  *      slots that call copied it to, and early_cnt[b] = its size E (0
  *      without above);
  *   1. every resident token that is not selected is freed (both table
- *      entries -1); its bytes stay, nothing is written back.  Its free bit is
- *      set, except for an early token: its slot is held until step 2 is done
- *      (its early copy may still be in flight) and is free after the step;
+ *      entries -1, its free bit set); its bytes stay, nothing is written
+ *      back.  With flags & ECHO_CACHE_HOLD_EARLY, the slot of an early token
+ *      of this step is held until step 2 is done instead (its early copy may
+ *      still be in flight) and is free after the step;
  *   2. the selected tokens that are not resident (the misses), in ascending
  *      order, take the lowest free slots in ascending order;
  *   3. sel_slot [B,m] = slot of each selected token (-1 for padding);
  *   4. the miss rows are copied host_kv[tok_off[b] + t] -> dev_kv[b*C + slot],
  *      on copy_stream (which may equal stream: then as a programmatic
  *      dependent of steps 0-3; else an event orders it after them).
- * Needs m <= C, and m + (unselected early tokens) <= C, which an early_cap
- * of at most C - m guarantees (else a miss may find no slot:
- * ECHO_ST_NOSLOT).  Steps 0-3 are launched as a programmatic dependent of the
+ * Needs m <= C; holding, also m + (unselected early tokens) <= C, which an
+ * early_cap of at most C - m guarantees (else a miss may find no slot:
+ * ECHO_ST_NOSLOT).  Holding, the recall may run before echo_early_fetch's
+ * copy ends.  flags: 0 or ECHO_CACHE_HOLD_EARLY (other bits: ECHO_EINVAL).
+ * Steps 0-3 are launched as a programmatic dependent of the
  * kernel before them on `stream`: while that kernel still runs (if it lets
  * dependents start early, as echo_topk_select and echo_index_scores do) they
  * may read slot2tok and freebits, which none of this library's kernels but
@@ -247,7 +255,8 @@ int echo_topk_select(int B, const int64_t* tok_off, int64_t n_tokens, const floa
  */
 int echo_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
                     const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,
-                    int32_t* status, uint32_t* stats, echo_stream_t stream, echo_stream_t copy_stream);
+                    int32_t* status, uint32_t* stats, echo_stream_t stream, echo_stream_t copy_stream,
+                    int flags);
 
 /*
  * The two calls above with the cache step's look-up done by top-k:
@@ -261,7 +270,7 @@ int echo_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32
  * the two calls changes them).  Needs C <= 32768 (ECHO_EUNSUPPORTED
  * otherwise) and reads the free bits and tables of `cache`.
  * echo_cache_step_resolved then does steps 1-4 of echo_cache_step with those
- * slots (sel_slot in/out, early_cnt in), launched the same way; needs
+ * slots (sel_slot in/out, early_cnt in, the same flags), launched the same way; needs
  * C <= 131072.  Together they give exactly the tables, slots, lists and rows
  * of echo_topk_select followed by echo_cache_step.
  */
@@ -271,7 +280,7 @@ int echo_topk_select_cached(int B, const int64_t* tok_off, int64_t n_tokens, con
                             int32_t* status, uint32_t* stats, echo_stream_t stream);
 int echo_cache_step_resolved(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
                              const echo_cache* cache, int32_t* sel_slot, int32_t* status, uint32_t* stats,
-                             echo_stream_t stream, echo_stream_t copy_stream);
+                             echo_stream_t stream, echo_stream_t copy_stream, int flags);
 
 /*
  * Chunked prefill [EXPL panel "Prefill: one-round histogram"; AE section

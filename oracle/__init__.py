@@ -77,8 +77,8 @@ def lib():
                                           ctypes.c_int, c_i32p, c_i32p, c_i32p, c_i32p, c_i32p]
             L.orc_cache_step.restype = ctypes.c_int
             L.orc_cache_step.argtypes = [ctypes.c_int64, ctypes.c_int, c_i32p, c_i32p, c_i32p,
-                                         ctypes.c_int, c_i32p, ctypes.c_int32, c_i32p, c_i32p, c_i32p,
-                                         c_i32p, c_i32p]
+                                         ctypes.c_int, c_i32p, ctypes.c_int32, ctypes.c_int, c_i32p, c_i32p,
+                                         c_i32p, c_i32p, c_i32p]
             L.orc_early_cap_for.restype = ctypes.c_int
             L.orc_early_cap_for.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
             L.orc_recall.restype = None
@@ -213,14 +213,15 @@ def early_fetch(scores_f32, theta: float, cap: int, tok2slot, slot2tok):
 
 
 def early_cap_for(cap: int, C: int, k: int) -> int:
-    """The early-set cap of a decode step with selection width k (C - k on top of cap)."""
+    """The early-set cap of the held-slot variant of a decode step with selection width k
+    (C - k on top of cap)."""
     return int(lib().orc_early_cap_for(int(cap), int(C), int(k)))
 
 
-def cache_step(sel, tok2slot, slot2tok, early_tok=None):
+def cache_step(sel, tok2slot, slot2tok, early_tok=None, hold_early=False):
     """Updates the tables in place; early_tok: the tokens this step's early fetch made
-    resident (their slots are held through the miss placement).
-    -> (sel_slot, miss_tok, miss_slot, nfreed)."""
+    resident; hold_early: the held-slot variant (their slots are held through the miss
+    placement).  -> (sel_slot, miss_tok, miss_slot, nfreed)."""
     sel = _c(sel, np.int32).reshape(-1)
     et = _c(np.zeros(0, np.int32) if early_tok is None else early_tok, np.int32).reshape(-1)
     assert tok2slot.dtype == np.int32 and slot2tok.dtype == np.int32
@@ -232,7 +233,7 @@ def cache_step(sel, tok2slot, slot2tok, early_tok=None):
     nf = ctypes.c_int32()
     rc = lib().orc_cache_step(n, C, _p(tok2slot, ctypes.c_int32), _p(slot2tok, ctypes.c_int32),
                               _p(sel, ctypes.c_int32), m, _p(et, ctypes.c_int32) if et.size else None,
-                              et.size, _p(sel_slot, ctypes.c_int32),
+                              et.size, int(bool(hold_early)), _p(sel_slot, ctypes.c_int32),
                               _p(mt, ctypes.c_int32), _p(ms, ctypes.c_int32), ctypes.byref(nm),
                               ctypes.byref(nf))
     _check(rc, "cache_step")

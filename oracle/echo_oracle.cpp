@@ -358,10 +358,12 @@ int orc_early_fetch(int64_t n, int C, const float* scores, float theta, int cap,
 // (orc_early_fetch's output; may be NULL when n_early = 0).
 // 1. Free every resident token that is not selected: both table entries go
 //    to -1; the KV bytes stay where they are and nothing is written back to
-//    the host, which holds every token.  The slot of an early token of this
-//    step is held until step 2 is done (READING: the early copy into that
-//    slot may still be in flight during the step, so no miss of the same
-//    step is placed there; the slot is free again for the next step).
+//    the host, which holds every token.  With hold_early, the slot of an
+//    early token of this step is held until step 2 is done (a variant, not
+//    the contract reading: the early copy into that slot may still be in
+//    flight during the step, so no miss of the same step is placed there;
+//    the slot is free again for the next step).  Without it the early tokens
+//    are residents like any other.
 // 2. The selected tokens that are not resident are the misses; in ascending
 //    token order each takes the lowest free slot, in ascending order.
 // 3. The held slots are free.
@@ -370,7 +372,7 @@ int orc_early_fetch(int64_t n, int C, const float* scores, float theta, int cap,
 // Capacity: selected tokens plus held slots must not exceed C (return 2,
 // state untouched).
 int orc_cache_step(int64_t n, int C, int32_t* tok2slot, int32_t* slot2tok, const int32_t* sel,
-                   int m, const int32_t* early_tok, int32_t n_early, int32_t* sel_slot,
+                   int m, const int32_t* early_tok, int32_t n_early, int hold_early, int32_t* sel_slot,
                    int32_t* miss_tok, int32_t* miss_slot, int32_t* nmiss, int32_t* nfreed) {
     if (!cache_consistent(n, C, tok2slot, slot2tok)) return ORC_EINVAL;
     if (n_early < 0 || (n_early > 0 && !early_tok)) return ORC_EINVAL;
@@ -380,7 +382,8 @@ int orc_cache_step(int64_t n, int C, int32_t* tok2slot, int32_t* slot2tok, const
         if (sel[i] >= n) return ORC_EINVAL;
         selected.insert(sel[i]);
     }
-    const std::set<int32_t> early(early_tok, early_tok + n_early);
+    std::set<int32_t> early;
+    if (hold_early) early.insert(early_tok, early_tok + n_early);
     int64_t held_count = 0;
     for (int32_t e : early)
         if (!selected.count(e)) ++held_count;
@@ -454,10 +457,9 @@ int orc_prefill_rows(const float* scores, int64_t W, int R, int64_t row0, int k,
     return ORC_OK;
 }
 
-// The early set of a decode step with selection width k is capped at C - k
-// on top of the caller's cap (cap < 0: no cap of its own) (READING: with the
-// early slots held through the miss placement, selected tokens plus held
-// slots stay within C only if the early set leaves room for k misses).
+// The early-set cap of the held-slot variant of a decode step with selection
+// width k: C - k on top of the caller's cap (cap < 0: no cap of its own), so
+// that selected tokens plus held slots stay within C.
 int orc_early_cap_for(int cap, int C, int k) {
     const int room = C - k;
     return (cap < 0 || cap > room) ? room : cap;
@@ -502,8 +504,7 @@ int orc_decode_step(int B, const int64_t* tok_off, const float* q, const float* 
         std::vector<int32_t> et((size_t)C), es((size_t)C);
         int32_t ne = 0;
         if (predictor) {
-            rc = orc_early_fetch(n, C, sf.data(), theta[b], orc_early_cap_for(cap, C, k), t2s, s2t, et.data(),
-                                 es.data(), &ne);
+            rc = orc_early_fetch(n, C, sf.data(), theta[b], cap, t2s, s2t, et.data(), es.data(), &ne);
             if (rc) { rcs[(size_t)b] = rc; return; }
             orc_recall(hrows, row_bytes, et.data(), es.data(), ne, drows);
         }
@@ -512,7 +513,7 @@ int orc_decode_step(int B, const int64_t* tok_off, const float* q, const float* 
         theta[b] = ema(theta[b], kth[b], alpha);
         std::vector<int32_t> mt((size_t)k), ms((size_t)k);
         int32_t nm = 0, nf = 0;
-        rc = orc_cache_step(n, C, t2s, s2t, sel_idx + (int64_t)b * k, k, et.data(), ne,
+        rc = orc_cache_step(n, C, t2s, s2t, sel_idx + (int64_t)b * k, k, et.data(), ne, 0,
                             sel_slot + (int64_t)b * k, mt.data(), ms.data(), &nm, &nf);
         if (rc) { rcs[(size_t)b] = rc; return; }
         orc_recall(hrows, row_bytes, mt.data(), ms.data(), nm, drows);

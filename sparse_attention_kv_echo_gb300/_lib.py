@@ -21,6 +21,7 @@ ST_TIMEOUT, ST_NAN, ST_NOSLOT, ST_BADDATA = 0x1, 0x2, 0x4, 0x8
 STAT_TOPK_FALLBACK, STAT_BOUNDARY_MAX, STAT_EARLY, STAT_MISSES, STAT_EARLY_USED = 0, 1, 2, 3, 4
 STATS_N = 8
 HEADS, DIM, MAX_REQUESTS = 64, 128, 4096
+CACHE_HOLD_EARLY = 1            # echo_cache_step flag
 TOPK_CACHED_MAX_SLOTS = 32768  # C limit of echo_topk_select_cached
 EARLY_FETCH_BLOCKS = 32      # CTAs of the early-fetch and late-recall kernels
 
@@ -79,13 +80,13 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         L.echo_topk_select.argtypes = [i32, _vp, i64, _vp, i32, _vp, _vp, f32, _vp, _vp, _vp, _vp, _vp]
         L.echo_cache_step.restype = i32
         L.echo_cache_step.argtypes = [i32, _vp, i64, _vp, i32, _vp, i32, ctypes.POINTER(EchoCacheStruct), _vp,
-                                      _vp, _vp, _vp, _vp]
+                                      _vp, _vp, _vp, _vp, i32]
         L.echo_topk_select_cached.restype = i32
         L.echo_topk_select_cached.argtypes = [i32, _vp, i64, _vp, i32, _vp, _vp, f32, _vp, _vp, _vp, i32,
                                               ctypes.POINTER(EchoCacheStruct), _vp, _vp, _vp, _vp]
         L.echo_cache_step_resolved.restype = i32
         L.echo_cache_step_resolved.argtypes = [i32, _vp, i64, _vp, i32, ctypes.POINTER(EchoCacheStruct), _vp, _vp,
-                                               _vp, _vp, _vp]
+                                               _vp, _vp, _vp, i32]
         L.echo_prefill_scores.restype = i32
         L.echo_prefill_scores.argtypes = [i32, i64, i64, _vp, _vp, _vp, _vp, _vp, i64, _vp, _vp, _vp, _vp]
         L.echo_prefill_workspace_size.restype = ctypes.c_size_t
@@ -198,15 +199,17 @@ def topk_select(tok_off, n_tokens, scores, k, hist, theta_hat, alpha, sel_idx, k
 
 
 def cache_step(tok_off, n_tokens, sel, cache, sel_slot, status, stats=None, stream=None, copy_stream=None,
-               above=None, early_cap=-1):
-    """echo_cache_step; above/early_cap: the early set of this step (as given to early_fetch)."""
+               above=None, early_cap=-1, hold_early=False):
+    """echo_cache_step; above/early_cap: the early set of this step (as given to early_fetch);
+    hold_early: ECHO_CACHE_HOLD_EARLY."""
     B = tok_off.shape[0] - 1
     m = sel.shape[-1]
     st = _stream(stream)
     cst = _stream(copy_stream) if copy_stream is not None else st
     _check("echo_cache_step", load().echo_cache_step(
         B, _ptr(tok_off), int(n_tokens), _ptr(sel), int(m), _ptr(above), int(early_cap),
-        ctypes.byref(cache.struct), _ptr(sel_slot), _ptr(status), _ptr(stats), st, cst))
+        ctypes.byref(cache.struct), _ptr(sel_slot), _ptr(status), _ptr(stats), st, cst,
+        CACHE_HOLD_EARLY if hold_early else 0))
 
 
 def topk_select_cached(tok_off, n_tokens, scores, k, hist, theta_hat, alpha, sel_idx, kth, cache, sel_slot,
@@ -220,7 +223,8 @@ def topk_select_cached(tok_off, n_tokens, scores, k, hist, theta_hat, alpha, sel
         _ptr(status), _ptr(stats), _stream(stream)))
 
 
-def cache_step_resolved(tok_off, n_tokens, sel, cache, sel_slot, status, stats=None, stream=None, copy_stream=None):
+def cache_step_resolved(tok_off, n_tokens, sel, cache, sel_slot, status, stats=None, stream=None, copy_stream=None,
+                        hold_early=False):
     """echo_cache_step_resolved: the cache step after topk_select_cached (sel_slot in/out)."""
     B = tok_off.shape[0] - 1
     m = sel.shape[-1]
@@ -228,7 +232,7 @@ def cache_step_resolved(tok_off, n_tokens, sel, cache, sel_slot, status, stats=N
     cst = _stream(copy_stream) if copy_stream is not None else st
     _check("echo_cache_step_resolved", load().echo_cache_step_resolved(
         B, _ptr(tok_off), int(n_tokens), _ptr(sel), int(m), ctypes.byref(cache.struct), _ptr(sel_slot),
-        _ptr(status), _ptr(stats), st, cst))
+        _ptr(status), _ptr(stats), st, cst, CACHE_HOLD_EARLY if hold_early else 0))
 
 
 def prefill_scores(R, row0, n_keys, q8, wfold, k8, ks, scores, W, theta_hat, hist, status, stream=None):

@@ -89,14 +89,15 @@ constexpr int kLookupMaxSlots = 1 << 17;   // 4 x 4096 words + the chunk fit sha
 __global__ void __launch_bounds__(kLT)
     cache_step_lookup_kernel(const int64_t* __restrict__ tok_off, int64_t n_tokens, const int32_t* __restrict__ sel,
                              int m, const uint32_t* __restrict__ above, int early_cap, CacheArgs c,
-                             int32_t* sel_slot, int32_t* status, uint32_t* stats, bool resolved) {
+                             int32_t* sel_slot, int32_t* status, uint32_t* stats, bool resolved,
+                             bool hold_early) {
     pdl_launch_dependents();  // the late recall's blocks may be scheduled now; they wait for this kernel
     extern __shared__ uint32_t smem[];
     __shared__ uint32_t scan[40];
     __shared__ uint32_t flags[2];
     CacheStepLookup<kLT, kAWC> cs;
     cs.init(tok_off, n_tokens, blockIdx.x, sel, m, sel_slot, above, early_cap, c, status, stats, smem, scan, flags,
-            resolved ? sel_slot : nullptr);
+            resolved ? sel_slot : nullptr, hold_early);
     cs.prologue_issue();  // the tables only: they may be read before the kernel before this one ends
     cs.prologue_finish();
     pdl_wait();           // the selection and the above words come from the kernels before this one
@@ -111,7 +112,7 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
                                                          const int32_t* __restrict__ sel, int m,
                                                          const uint32_t* __restrict__ above, int early_cap,
                                                          CacheArgs c, int32_t* __restrict__ sel_slot, int32_t* status,
-                                                         uint32_t* stats) {
+                                                         uint32_t* stats, bool hold_early) {
     // keep [words]: a selected token lives in the slot | wpre [words + 1] | fbs [words] (free bits)
     // | es_tok [kES] | es_slot [kES] (the early pairs, both ascending)
     extern __shared__ uint32_t keep[];
@@ -280,6 +281,13 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
     }
     if (used) atomicAdd(&s_early_used, used);
     __syncthreads();
+    if (!hold_early) {  // the unselected early tokens' slots are free for the misses
+        for (uint32_t e = tid; e < E; e += kCT) {
+            const int32_t es = e_slot[e];
+            if (es >= 0 && es < C && !((keep[es >> 5] >> (es & 31)) & 1u)) atomicOr(&fbs[es >> 5], 1u << (es & 31));
+        }
+        __syncthreads();
+    }
 
     // 2. free-slot prefix over the new free-bit words
     const uint32_t F = free_prefix<kCT>(fbs, words, scan, wpre, fbs);
@@ -329,7 +337,7 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
     take_lowest_free<kCT>(fbs, words, got, wpre);
     __syncthreads();
     // the held early slots (not kept by a selected token) are free again
-    for (uint32_t e = tid; e < E; e += kCT) {
+    for (uint32_t e = tid; e < (hold_early ? E : 0u); e += kCT) {
         const int32_t es = e_slot[e];
         if (es >= 0 && es < C && !((keep[es >> 5] >> (es & 31)) & 1u)) atomicOr(&fbs[es >> 5], 1u << (es & 31));
     }
@@ -574,7 +582,7 @@ namespace echo {
 int enqueue_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
                        const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,
                        int32_t* status, uint32_t* stats, cudaStream_t stream, cudaStream_t copy_stream,
-                       bool resolved) {
+                       bool resolved, bool hold_early) {
     const bool lookup = cache->C <= kLookupMaxSlots;
     if (resolved && !lookup) return ECHO_EUNSUPPORTED;
     const size_t smem =
@@ -606,10 +614,10 @@ int enqueue_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const in
     if (lookup) {
         ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, cache_step_lookup_kernel, tok_off, n_tokens, sel, m,
                                         resolved ? nullptr : above, early_cap, ca, sel_slot, status, stats,
-                                        resolved));
+                                        resolved, hold_early));
     } else {
         ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, cache_step_kernel, tok_off, n_tokens, sel, m, above, early_cap, ca,
-                                        sel_slot, status, stats));
+                                        sel_slot, status, stats, hold_early));
     }
     const int rc = stream_wait(copy_stream, stream);
     if (rc) return rc;
@@ -635,25 +643,26 @@ int check_cache_step_args(int B, int64_t n_tokens, const int32_t* sel, int m, co
 
 extern "C" int echo_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
                                const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,
-                               int32_t* status, uint32_t* stats, echo_stream_t stream, echo_stream_t copy_stream) {
+                               int32_t* status, uint32_t* stats, echo_stream_t stream, echo_stream_t copy_stream,
+                               int flags) {
     using namespace echo;
-    if (!tok_off || !status) return ECHO_EINVAL;
+    if (!tok_off || !status || (flags & ~ECHO_CACHE_HOLD_EARLY)) return ECHO_EINVAL;
     const int rc = check_cache_step_args(B, n_tokens, sel, m, cache, sel_slot);
     if (rc) return rc;
     return enqueue_cache_step(B, tok_off, n_tokens, sel, m, above, early_cap, cache, sel_slot, status, stats, stream,
-                              copy_stream, false);
+                              copy_stream, false, (flags & ECHO_CACHE_HOLD_EARLY) != 0);
 }
 
 extern "C" int echo_cache_step_resolved(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
                                         const echo_cache* cache, int32_t* sel_slot, int32_t* status, uint32_t* stats,
-                                        echo_stream_t stream, echo_stream_t copy_stream) {
+                                        echo_stream_t stream, echo_stream_t copy_stream, int flags) {
     using namespace echo;
-    if (!tok_off || !status) return ECHO_EINVAL;
+    if (!tok_off || !status || (flags & ~ECHO_CACHE_HOLD_EARLY)) return ECHO_EINVAL;
     const int rc = check_cache_step_args(B, n_tokens, sel, m, cache, sel_slot);
     if (rc) return rc;
     if (cache->C > kLookupMaxSlots) return ECHO_EUNSUPPORTED;
     return enqueue_cache_step(B, tok_off, n_tokens, sel, m, nullptr, 0, cache, sel_slot, status, stats, stream,
-                              copy_stream, true);
+                              copy_stream, true, (flags & ECHO_CACHE_HOLD_EARLY) != 0);
 }
 
 extern "C" int echo_early_fetch(int B, const int64_t* tok_off, int64_t n_tokens, const uint32_t* above,

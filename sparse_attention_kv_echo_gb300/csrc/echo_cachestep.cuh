@@ -63,6 +63,7 @@ struct CacheStepLookup {
     uint32_t *keep, *wpre, *fbs, *held, *aw, *apre, *scan;
     const int32_t* pre_slot;  // resolved form: the selection's slots as top-k looked them up
     bool resolved;
+    bool hold;                // the unselected early tokens' slots are held until the misses are placed
     int32_t E_pre;            // resolved form: the early set's size
     uint32_t *s_flags, *s_used;
     // registers
@@ -78,7 +79,7 @@ struct CacheStepLookup {
     __device__ void init(const int64_t* tok_off, int64_t n_tokens, int b_, const int32_t* sel, int m_,
                          int32_t* sel_slot, const uint32_t* above, int cap, const CacheArgs& args, int32_t* st,
                          uint32_t* sts, uint32_t* smem, uint32_t* scan_, uint32_t* flags,
-                         const int32_t* pre_slot_ = nullptr) {
+                         const int32_t* pre_slot_, bool hold_early) {
         c = args;
         b = b_;
         m = m_;
@@ -100,6 +101,7 @@ struct CacheStepLookup {
         chunks = (m + NT * kCsPer - 1) / (NT * kCsPer);
         pre_slot = pre_slot_ ? pre_slot_ + static_cast<int64_t>(b) * m : nullptr;
         resolved = pre_slot_ != nullptr;
+        hold = hold_early;
         E_pre = 0;
         early = !resolved && above != nullptr && early_cap != 0 && n > 0;
         ab = early ? above + 4 * (base / 128 + b) : nullptr;
@@ -291,10 +293,9 @@ struct CacheStepLookup {
         const uint32_t E = resolved ? min(static_cast<uint32_t>(max(E_pre, 0)), F0) : min(A, limit);
         if (used) atomicAdd(s_used, used);
         // the early set's slots (the lowest E free slots at the start) leave the free
-        // bits; the selected early tokens keep theirs, the others are held until the
-        // misses are placed (their early copies may still be in flight) and are free
-        // again after the step (held: the early set's slots; the kept ones are
-        // dropped from it at the end)
+        // bits (held: the early set's slots); the selected early tokens keep theirs,
+        // the others are free again before the misses are placed, or, holding, after
+        // (their early copies may still be in flight)
         for (int w = tid; w < words; w += NT) held[w] = fbs[w];
         __syncthreads();  // every look-up walk over fbs is done before its bits change
         take_lowest_free<NT>(fbs, words, E, wpre);
@@ -353,6 +354,14 @@ struct CacheStepLookup {
             for (int w = warp; w < words; w += NT / 32) free_word(w, s2t[w * 32 + lane]);
         }
         __syncthreads();
+
+        if (!hold) {  // the unselected early tokens' slots are free for the misses
+            for (int w = tid; w < words; w += NT) {
+                fbs[w] |= held[w] & ~keep[w];
+                held[w] = 0u;
+            }
+            __syncthreads();
+        }
 
         // 2. free-slot prefix over the new free-bit words
         const uint32_t F = free_prefix<NT>(fbs, words, scan, wpre, fbs);

@@ -61,7 +61,7 @@ int check_cache_step_args(int B, int64_t n_tokens, const int32_t* sel, int m, co
 int enqueue_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
                        const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,
                        int32_t* status, uint32_t* stats, cudaStream_t stream, cudaStream_t copy_stream,
-                       bool resolved);
+                       bool resolved, bool hold_early);
 
 }  // namespace echo
 

@@ -32,7 +32,7 @@ class DecodeLayer:
     def __init__(self, tok_off, k8: torch.Tensor, ks: torch.Tensor, k: int, C: int,
                  host_pool: torch.Tensor, alpha: float = 0.5, predictor: bool = True,
                  early_cap: int = -1, groups: int | None = None, first_share: float = 0.5,
-                 resolved: bool = True, device="cuda"):
+                 resolved: bool = True, hold_early: bool = False, device="cuda"):
         tok_off = torch.as_tensor(tok_off, dtype=torch.int64)
         self.B = int(tok_off.numel() - 1)
         self.n_tokens = int(k8.shape[0])
@@ -41,11 +41,14 @@ class DecodeLayer:
         # top-k looks up the selected tokens' slots itself (the cache step then frees and places
         # the misses) when the request's free bits fit its shared memory
         self.resolved = bool(resolved) and self.C <= L.TOPK_CACHED_MAX_SLOTS
-        # the early set is capped at C - k on top of the caller's cap: the cache step holds the
-        # slots of unselected early tokens while it places the misses, so selected tokens plus
-        # held slots stay within C
+        # hold_early: the cache step holds the slots of unselected early tokens until the misses
+        # are placed, so the late recall need not wait for the early copy; the early set is then
+        # capped at C - k on top of the caller's cap (selected tokens plus held slots within C)
+        self.hold_early = bool(hold_early)
         room = self.C - self.k
-        self.early_cap = room if (early_cap < 0 or early_cap > room) else int(early_cap)
+        if self.hold_early and (early_cap < 0 or early_cap > room):
+            early_cap = room
+        self.early_cap = int(early_cap)
         self.tok_off = tok_off.to(device)
         self.k8, self.ks = k8, ks
         f32 = dict(dtype=torch.float32, device=device)
@@ -116,7 +119,7 @@ class DecodeLayer:
                     self._write_out(out_host, 0, self.B)
             return
         sms = torch.cuda.get_device_properties(main.device).multi_processor_count
-        scored = None
+        scored, gstream = None, []
         for g, (b0, b1) in enumerate(self.groups):
             s = main if g == 0 else self.gstreams[g - 1]
             if scored is not None:
@@ -129,16 +132,18 @@ class DecodeLayer:
                            above=self.above_g[g], cache=self.views[g], stream=s, ctas=ctas)
             scored = torch.cuda.Event()
             scored.record(s)
+            gstream.append(s)
             # the group's early rows stream over the host link on `s` (programmatic dependent of its
             # score kernel) while the next group is scored
             L.early_fetch(self.tok_off[b0:b1 + 1], self.n_tokens, self.above_g[g], self.early_cap, self.views[g],
                           self.status, stream=s)
         # top-k and the table update of every group on the groups' side streams once all scores are
         # done (a top-k started earlier would take SMs the next score kernel counts on); the late
-        # misses of a group follow its cache step on the side stream (a miss never takes a slot the
-        # early fetch is still writing), so they share the host link with the early rows
+        # misses of a group follow its early fetch on the group's stream (a slot fetched early and
+        # then freed may go to a miss), or, holding those slots, its cache step on the side stream
         for g, (b0, b1) in enumerate(self.groups):
             side = self.sides[g]
+            copy = side if self.hold_early else gstream[g]
             side.wait_event(scored)
             off = self.tok_off[b0:b1 + 1]
             if self.resolved:
@@ -148,14 +153,15 @@ class DecodeLayer:
                                      self.sel_slot[b0:b1], self.status, stats=self.stats, stream=side,
                                      above=self.above_g[g], early_cap=self.early_cap)
                 L.cache_step_resolved(off, self.n_tokens, self.sel_idx[b0:b1], self.views[g], self.sel_slot[b0:b1],
-                                      self.status, stats=self.stats, stream=side, copy_stream=side)
+                                      self.status, stats=self.stats, stream=side, copy_stream=copy,
+                                      hold_early=self.hold_early)
             else:
                 L.topk_select(off, self.n_tokens, self.scores, self.k, self.hist[b0:b1], self.theta[b0:b1],
                               self.alpha, self.sel_idx[b0:b1], self.kth[b0:b1], self.status, stats=self.stats,
                               stream=side)
                 L.cache_step(off, self.n_tokens, self.sel_idx[b0:b1], self.views[g], self.sel_slot[b0:b1],
-                             self.status, stats=self.stats, stream=side, copy_stream=side, above=self.above_g[g],
-                             early_cap=self.early_cap)
+                             self.status, stats=self.stats, stream=side, copy_stream=copy, above=self.above_g[g],
+                             early_cap=self.early_cap, hold_early=self.hold_early)
             if out_host is not None:
                 with torch.cuda.stream(side):
                     self._write_out(out_host, b0, b1)

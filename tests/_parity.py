@@ -63,7 +63,8 @@ def check_scores(layer_inputs, q, w, gpu_scores, sample=None, rng=None):
 
 
 def run_decode(w: wl.Workload, steps: int, predictor: bool, cap: int = -1, score_sample=None,
-               check_every_score_step=True, keys_device="cpu", layer: int = 0, resolved: bool = True):
+               check_every_score_step=True, keys_device="cpu", layer: int = 0, resolved: bool = True,
+               hold_early: bool = False):
     """Runs `steps` decode steps of one layer on the GPU and checks each against the oracle."""
     dev = "cuda"
     off = wl.tok_offsets(w.lengths)
@@ -74,7 +75,7 @@ def run_decode(w: wl.Workload, steps: int, predictor: bool, cap: int = -1, score
     host = wl.make_host_pool(w, layer, device=keys_device, pin=True)
     host_before = host.clone()
     lay = DecodeLayer(off, k8c.to(dev), ksc.to(dev), w.k, w.C, host, predictor=predictor, early_cap=cap,
-                      resolved=resolved)
+                      resolved=resolved, hold_early=hold_early)
     o = OracleLayer(w.B, w.total_tokens, w.C)
     qsrc = wl.QueryStream(w, layer, device=keys_device)
     rng = np.random.default_rng(7)
@@ -114,8 +115,8 @@ def run_decode(w: wl.Workload, steps: int, predictor: bool, cap: int = -1, score
             s2t = o.s2t[b * w.C:(b + 1) * w.C]
             et = None
             if predictor:
-                # the layer's cap: the caller's, capped at C - k (the oracle's rule, pinned on the CPU)
-                assert lay.early_cap == orc.early_cap_for(cap, w.C, w.k)
+                # the layer's cap: the caller's (holding: capped at C - k, the oracle's rule)
+                assert lay.early_cap == (orc.early_cap_for(cap, w.C, w.k) if hold_early else cap)
                 et, es = orc.early_fetch(sc, theta_before[b], lay.early_cap, t2s, s2t)
                 assert g_ecnt[b] == et.size, (t, b, "early count", g_ecnt[b], et.size)
                 assert np.array_equal(g_etok[b * w.C:b * w.C + et.size], et), (t, b, "early tok")
@@ -127,7 +128,7 @@ def run_decode(w: wl.Workload, steps: int, predictor: bool, cap: int = -1, score
             o.theta[b] = orc.ema(theta_before[b], kth, 0.5)
             assert g_theta[b] == o.theta[b] or (np.isinf(o.theta[b]) and np.isinf(g_theta[b])), \
                 (t, b, "theta", g_theta[b], o.theta[b])
-            sel_slot, mt, ms, _ = orc.cache_step(idx, t2s, s2t, early_tok=et)
+            sel_slot, mt, ms, _ = orc.cache_step(idx, t2s, s2t, early_tok=et, hold_early=hold_early)
             assert np.array_equal(g_slot[b], sel_slot), (t, b, "sel_slot")
             assert g_mcnt[b] == mt.size, (t, b, "miss count", g_mcnt[b], mt.size)
             assert np.array_equal(g_mtok[b * w.C:b * w.C + mt.size], mt), (t, b, "miss tok")

@@ -105,13 +105,28 @@ def test_cache_checks(L):
     dummy = v(0x1000)
     # k (m) larger than C
     assert L.echo_cache_step(1, dummy, 100, dummy, 65, None, 0, ctypes.byref(s), dummy, dummy, None, None,
-                             None) == lib.ECHO_ECAPACITY
+                             None, 0) == lib.ECHO_ECAPACITY
     s.C = 48   # not a multiple of 32
     assert L.echo_cache_step(1, dummy, 100, dummy, 16, None, 0, ctypes.byref(s), dummy, dummy, None, None,
-                             None) == lib.ECHO_ECAPACITY
+                             None, 0) == lib.ECHO_ECAPACITY
     s.C, s.row_bytes = 64, 1000  # row not a multiple of 16 bytes
     assert L.echo_cache_step(1, dummy, 100, dummy, 16, None, 0, ctypes.byref(s), dummy, dummy, None, None,
-                             None) == lib.ECHO_EUNSUPPORTED
+                             None, 0) == lib.ECHO_EUNSUPPORTED
     s.row_bytes, s.dev_kv = 1152, None
     assert L.echo_cache_step(1, dummy, 100, dummy, 16, None, 0, ctypes.byref(s), dummy, dummy, None, None,
-                             None) == lib.ECHO_EINVAL
+                             None, 0) == lib.ECHO_EINVAL
+    s.dev_kv = 0x2000
+    # unknown flag bits
+    assert L.echo_cache_step(1, dummy, 100, dummy, 16, None, 0, ctypes.byref(s), dummy, dummy, None, None,
+                             None, 2) == lib.ECHO_EINVAL
+    assert L.echo_cache_step_resolved(1, dummy, 100, dummy, 16, ctypes.byref(s), dummy, dummy, None, None,
+                                      None, 4) == lib.ECHO_EINVAL
+    # the resolved form: k larger than C; the cached top-k: C above its shared-memory limit
+    assert L.echo_cache_step_resolved(1, dummy, 100, dummy, 65, ctypes.byref(s), dummy, dummy, None, None,
+                                      None, 0) == lib.ECHO_ECAPACITY
+    s.C = 65536
+    assert L.echo_topk_select_cached(1, dummy, 100, dummy, 16, None, None, 0.5, dummy, dummy, None, -1,
+                                     ctypes.byref(s), dummy, dummy, None, None) == lib.ECHO_EUNSUPPORTED
+    s.C = 64
+    assert L.echo_topk_select_cached(1, dummy, 100, dummy, 16, None, None, 0.5, dummy, dummy, None, -1,
+                                     ctypes.byref(s), None, dummy, None, None) == lib.ECHO_EINVAL   # no sel_slot

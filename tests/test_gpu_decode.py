@@ -39,6 +39,21 @@ def test_batch_workload_table_look_up_in_the_cache_step():
     run_decode(w, 4, predictor=True, score_sample=256, check_every_score_step=False, resolved=False)
 
 
+def test_tiny_workload_held_early_slots():
+    """The held-slot variant (ECHO_CACHE_HOLD_EARLY): misses never take this step's early slots, the
+    late recall runs right after the cache step."""
+    w = wl.WORKLOADS["tiny"]
+    rep = run_decode(w, w.steps, predictor=True, hold_early=True)
+    assert sum(rep["early"]) > 0
+
+
+def test_batch_workload_held_early_slots_both_look_ups():
+    w = wl.WORKLOADS["batch"]
+    run_decode(w, 4, predictor=True, score_sample=256, check_every_score_step=False, hold_early=True)
+    run_decode(w, 4, predictor=True, score_sample=256, check_every_score_step=False, hold_early=True,
+               resolved=False)
+
+
 def test_tiny_predictor_off():
     w = wl.WORKLOADS["tiny"]
     rep = run_decode(w, 6, predictor=False)

@@ -26,7 +26,8 @@ def test_golden_walkthrough(orc):
             e = st["early"]
             et, es = orc.early_fetch(np.array(e["scores"], np.float32), e["theta"], e["cap"], t2s, s2t)
             assert list(et) == e["early_tok"] and list(es) == e["early_slot"], st["why"]
-        sel_slot, mt, ms, nf = orc.cache_step(np.array(st["sel"], np.int32), t2s, s2t, early_tok=et)
+        sel_slot, mt, ms, nf = orc.cache_step(np.array(st["sel"], np.int32), t2s, s2t, early_tok=et,
+                                              hold_early=st.get("hold_early", False))
         assert list(sel_slot) == st["sel_slot"], st["why"]
         assert list(mt) == st["miss_tok"] and list(ms) == st["miss_slot"], st["why"]
         assert nf == st["nfreed"], st["why"]
@@ -98,19 +99,25 @@ def test_capacity_error_leaves_state(orc):
 
 
 def test_held_early_slots_count_against_capacity(orc):
-    """Selected tokens plus the held slots of unselected early tokens must fit in C; the early cap
-    C - k of a decode step guarantees it (the early set leaves room for k misses)."""
+    """Held-slot variant: selected tokens plus the held slots of unselected early tokens must fit
+    in C; the early cap C - k of a decode step guarantees it (the early set leaves room for k
+    misses).  Under the contract reading the same step fits: the miss reuses a freed early slot."""
     t2s = np.full(10, -1, np.int32)
     s2t = np.full(3, -1, np.int32)
     et, es = orc.early_fetch(np.array([0, 0, 0, 0, 0, 0, 0, 2.0, 2.0, 0], np.float32), 1.0, -1, t2s, s2t)
     assert list(et) == [7, 8] and list(es) == [0, 1]
     before = (t2s.copy(), s2t.copy())
     with pytest.raises(orc.OracleError):                     # 2 selected + 2 held > 3
-        orc.cache_step(np.array([1, 2], np.int32), t2s, s2t, early_tok=et)
+        orc.cache_step(np.array([1, 2], np.int32), t2s, s2t, early_tok=et, hold_early=True)
     assert np.array_equal(t2s, before[0]) and np.array_equal(s2t, before[1])
-    sel_slot, mt, ms, nf = orc.cache_step(np.array([2, 7], np.int32), t2s, s2t, early_tok=et)
+    t2s_c, s2t_c = t2s.copy(), s2t.copy()
+    sel_slot, mt, ms, nf = orc.cache_step(np.array([2, 7], np.int32), t2s, s2t, early_tok=et, hold_early=True)
     assert list(sel_slot) == [2, 0] and list(mt) == [2] and list(ms) == [2] and nf == 1
     assert list(s2t) == [7, -1, 2]                           # slot 1 (held for 8) is free again
+    # contract reading: 8 is freed at once and the miss 2 takes the lowest free slot, 1
+    sel_slot, mt, ms, nf = orc.cache_step(np.array([2, 7], np.int32), t2s_c, s2t_c, early_tok=et)
+    assert list(sel_slot) == [1, 0] and list(mt) == [2] and list(ms) == [1] and nf == 1
+    assert list(s2t_c) == [7, 2, -1]
     assert [orc.early_cap_for(c, 4096, 2048) for c in (-1, 0, 100, 2048, 5000)] == [2048, 0, 100, 2048, 2048]
     assert orc.early_cap_for(-1, 64, 64) == 0
 
