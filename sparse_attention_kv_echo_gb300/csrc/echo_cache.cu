@@ -86,18 +86,18 @@ __device__ __forceinline__ int find_sorted(const int32_t* a, int n, int32_t v) {
 constexpr int kAWC = 8192;                 // above words per chunk held in shared memory
 constexpr int kLookupMaxSlots = 1 << 17;   // 4 x 4096 words + the chunk fit shared memory
 
+template <bool kResolved>
 __global__ void __launch_bounds__(kLT)
     cache_step_lookup_kernel(const int64_t* __restrict__ tok_off, int64_t n_tokens, const int32_t* __restrict__ sel,
                              int m, const uint32_t* __restrict__ above, int early_cap, CacheArgs c,
-                             int32_t* sel_slot, int32_t* status, uint32_t* stats, bool resolved,
-                             bool hold_early) {
+                             int32_t* sel_slot, int32_t* status, uint32_t* stats, bool hold_early) {
     pdl_launch_dependents();  // the late recall's blocks may be scheduled now; they wait for this kernel
     extern __shared__ uint32_t smem[];
     __shared__ uint32_t scan[40];
     __shared__ uint32_t flags[2];
-    CacheStepLookup<kLT, kAWC> cs;
+    CacheStepLookup<kLT, kAWC, kResolved> cs;
     cs.init(tok_off, n_tokens, blockIdx.x, sel, m, sel_slot, above, early_cap, c, status, stats, smem, scan, flags,
-            resolved ? sel_slot : nullptr, hold_early);
+            hold_early);
     cs.prologue_issue();  // the tables only: they may be read before the kernel before this one ends
     cs.prologue_finish();
     pdl_wait();           // the selection and the above words come from the kernels before this one
@@ -587,9 +587,10 @@ int enqueue_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const in
     if (resolved && !lookup) return ECHO_EUNSUPPORTED;
     const size_t smem =
         (lookup ? cache_lookup_smem_words(cache->C, kAWC) : cache_step_smem_words(cache->C)) * sizeof(uint32_t);
+    auto lookup_kernel = resolved ? cache_step_lookup_kernel<true> : cache_step_lookup_kernel<false>;
     if (lookup) {
-        ECHO_CUDA_OK(prefer_max_shared(cache_step_lookup_kernel));
-        ECHO_CUDA_OK(cudaFuncSetAttribute(cache_step_lookup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        ECHO_CUDA_OK(prefer_max_shared(lookup_kernel));
+        ECHO_CUDA_OK(cudaFuncSetAttribute(lookup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           static_cast<int>(smem)));
     } else {
         ECHO_CUDA_OK(prefer_max_shared(cache_step_kernel));
@@ -612,9 +613,8 @@ int enqueue_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const in
     cfg.numAttrs = 1;
     const CacheArgs ca = cache_args(*cache);
     if (lookup) {
-        ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, cache_step_lookup_kernel, tok_off, n_tokens, sel, m,
-                                        resolved ? nullptr : above, early_cap, ca, sel_slot, status, stats,
-                                        resolved, hold_early));
+        ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, lookup_kernel, tok_off, n_tokens, sel, m, resolved ? nullptr : above,
+                                        early_cap, ca, sel_slot, status, stats, hold_early));
     } else {
         ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, cache_step_kernel, tok_off, n_tokens, sel, m, above, early_cap, ca,
                                         sel_slot, status, stats, hold_early));

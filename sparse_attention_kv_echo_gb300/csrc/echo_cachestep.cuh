@@ -41,8 +41,9 @@ __host__ __device__ constexpr size_t cache_lookup_smem_words(int C, int awc) {
     return 4 * static_cast<size_t>(C / 32) + 1 + 2 * static_cast<size_t>(awc) + 1;
 }
 
-template <int NT, int AWC>
+template <int NT, int AWC, bool kResolved>
 struct CacheStepLookup {
+    static constexpr bool resolved = kResolved;  // each form is its own kernel: less code to fetch
     // arguments
     CacheArgs c;
     const int32_t* sl;        // this request's selection [m]
@@ -62,7 +63,6 @@ struct CacheStepLookup {
     // shared memory
     uint32_t *keep, *wpre, *fbs, *held, *aw, *apre, *scan;
     const int32_t* pre_slot;  // resolved form: the selection's slots as top-k looked them up
-    bool resolved;
     bool hold;                // the unselected early tokens' slots are held until the misses are placed
     int32_t E_pre;            // resolved form: the early set's size
     uint32_t *s_flags, *s_used;
@@ -79,7 +79,7 @@ struct CacheStepLookup {
     __device__ void init(const int64_t* tok_off, int64_t n_tokens, int b_, const int32_t* sel, int m_,
                          int32_t* sel_slot, const uint32_t* above, int cap, const CacheArgs& args, int32_t* st,
                          uint32_t* sts, uint32_t* smem, uint32_t* scan_, uint32_t* flags,
-                         const int32_t* pre_slot_, bool hold_early) {
+                         bool hold_early) {
         c = args;
         b = b_;
         m = m_;
@@ -99,8 +99,7 @@ struct CacheStepLookup {
         sl = sel + static_cast<int64_t>(b) * m;
         out = sel_slot + static_cast<int64_t>(b) * m;
         chunks = (m + NT * kCsPer - 1) / (NT * kCsPer);
-        pre_slot = pre_slot_ ? pre_slot_ + static_cast<int64_t>(b) * m : nullptr;
-        resolved = pre_slot_ != nullptr;
+        pre_slot = resolved ? sel_slot + static_cast<int64_t>(b) * m : nullptr;
         hold = hold_early;
         E_pre = 0;
         early = !resolved && above != nullptr && early_cap != 0 && n > 0;
@@ -146,7 +145,7 @@ struct CacheStepLookup {
     __device__ void load_selection() {
         load_sel(0);
         after0 = sel_at(kCsPer * static_cast<int>(threadIdx.x) + kCsPer);
-        if (resolved) {  // the slots top-k looked up, loaded with the selection
+        if constexpr (kResolved) {  // the slots top-k looked up, loaded with the selection
 #pragma unroll
             for (int q = 0; q < kCsPer; ++q) {
                 const int i = kCsPer * static_cast<int>(threadIdx.x) + q;
@@ -156,7 +155,7 @@ struct CacheStepLookup {
         }
     }
     __device__ void load_slots() {
-        if (chunks == 1 && !resolved) {
+        if (!kResolved && chunks == 1) {
 #pragma unroll
             for (int q = 0; q < kCsPer; ++q) j[q] = (s[q] >= 0 && s[q] < n) ? t2s[s[q]] : -1;
         }
@@ -269,7 +268,7 @@ struct CacheStepLookup {
         const int C = c.C;
         // the selected tokens of the early set take their slots
         uint32_t used = 0;
-        for (int k0 = 0; k0 < nw; k0 += AWC) {
+        for (int k0 = 0; !kResolved && k0 < nw; k0 += AWC) {
             if (k0 > 0) {
                 const int len = min(AWC, nw - k0);
                 __syncthreads();  // the previous chunk's look-ups are done
@@ -414,7 +413,7 @@ struct CacheStepLookup {
         if (tid == 0) {
             c.miss_cnt[b] = static_cast<int32_t>(got);
             if (stats && got) atomicAdd(stats + ECHO_STAT_MISSES, got);
-            if (!resolved) {  // (the resolved form's top-k counted the early set)
+            if constexpr (!kResolved) {  // (the resolved form's top-k counted the early set)
                 c.early_cnt[b] = static_cast<int32_t>(E);
                 if (stats && E) atomicAdd(stats + ECHO_STAT_EARLY, E);
                 if (stats && *s_used) atomicAdd(stats + ECHO_STAT_EARLY_USED, *s_used);
