@@ -52,6 +52,12 @@ def lib():
             c_u8p = ctypes.POINTER(ctypes.c_uint8)
             c_f32p = ctypes.POINTER(ctypes.c_float)
             c_f64p = ctypes.POINTER(ctypes.c_double)
+            c_u16p = ctypes.POINTER(ctypes.c_uint16)
+            L.orc_bf16_value.restype = ctypes.c_double
+            L.orc_bf16_value.argtypes = [ctypes.c_uint16]
+            L.orc_mla_decode.restype = ctypes.c_int
+            L.orc_mla_decode.argtypes = [c_u16p, ctypes.c_int, c_u16p, ctypes.c_int64, c_i32p, ctypes.c_int,
+                                         ctypes.c_double, c_f64p, c_f64p, c_f64p]
             L.orc_e4m3_decode.restype = ctypes.c_double
             L.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
             L.orc_e4m3_encode.restype = ctypes.c_uint8
@@ -295,3 +301,26 @@ def decode_step(tok_off, q, w, k8, ks, k, alpha, predictor, cap, theta, C, tok2s
         _p(sc, ctypes.c_float) if sc is not None else None, int(nthreads))
     _check(rc, "decode_step")
     return dict(sel_idx=sel_idx, sel_slot=sel_slot, kth=kth, nmiss=nmiss, scores=sc)
+
+
+def bf16_value(bits: int) -> float:
+    return float(lib().orc_bf16_value(int(bits)))
+
+
+def mla_decode(q_bits, kv_bits, slots, scale: float):
+    """Sparse MLA decode attention of one request (fp64).  q_bits [H,576] and kv_bits
+    [rows,576] are bf16 bit patterns (uint16); slots [k] int32 (-1: padding).
+    -> (out [H,512] f64, lse [H] f64, mass [H,512] f64)."""
+    q = _c(q_bits, np.uint16)
+    kv = _c(kv_bits, np.uint16)
+    sl = _c(slots, np.int32).reshape(-1)
+    H = q.shape[0]
+    assert q.shape[1] == 576 and kv.shape[1] == 576
+    out = np.empty((H, 512), np.float64)
+    lse = np.empty(H, np.float64)
+    mass = np.empty((H, 512), np.float64)
+    rc = lib().orc_mla_decode(_p(q, ctypes.c_uint16), H, _p(kv, ctypes.c_uint16), kv.shape[0],
+                              _p(sl, ctypes.c_int32), sl.size, float(scale), _p(out, ctypes.c_double),
+                              _p(lse, ctypes.c_double), _p(mass, ctypes.c_double))
+    _check(rc, "mla_decode")
+    return out, lse, mass

@@ -36,6 +36,7 @@
  */
 #include <algorithm>
 #include <cmath>
+#include <limits>
 #include <cstdint>
 #include <cstring>
 #include <map>
@@ -431,6 +432,68 @@ void orc_recall(const uint8_t* host_rows, int64_t row_bytes, const int32_t* tok,
     for (int32_t i = 0; i < count; ++i)
         std::memcpy(dev_rows + (int64_t)slot[i] * row_bytes, host_rows + (int64_t)tok[i] * row_bytes,
                     (size_t)row_bytes);
+}
+
+// ---- sparse MLA decode attention over the selected slots ------------------
+// The consumer of the cache (survey NEXT-1; EXPL section 2 names the sparse
+// attention over the k selected tokens but gives no formula).  READING: MLA
+// in its absorbed form, one latent KV row of 576 bf16 per token (512 latent
+// + 64 rotary dims) shared by every query head; for head h over the valid
+// slots t (slot >= 0):
+//   s_t = scale * sum_{d<576} q[h,d] * kv[slot_t, d]
+//   out[h, :] = sum_t softmax(s)_t * kv[slot_t, 0:512],  lse[h] = log sum_t exp(s_t)
+// in fp64 (bf16 values are exact in fp64); no valid slot: out = 0,
+// lse = -inf.  mass[h, d] = sum_t softmax(s)_t * |kv[slot_t, d]| (may be
+// NULL) sizes the rounding a reordered or lower-precision sum may make.
+double orc_bf16_value(uint16_t b) {
+    const uint32_t u = (uint32_t)b << 16;
+    float f;
+    std::memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+int orc_mla_decode(const uint16_t* q, int H, const uint16_t* kv, int64_t rows, const int32_t* slots, int k,
+                   double scale, double* out, double* lse, double* mass) {
+    const int DQK = 576, DV = 512;
+    if (H <= 0 || k < 0 || rows < 0) return ORC_EINVAL;
+    for (int i = 0; i < k; ++i)
+        if (slots[i] >= rows) return ORC_EINVAL;
+    std::vector<double> sc((size_t)k);
+    for (int h = 0; h < H; ++h) {
+        double mx = -std::numeric_limits<double>::infinity();
+        for (int i = 0; i < k; ++i) {
+            if (slots[i] < 0) continue;
+            double acc = 0.0;
+            for (int d = 0; d < DQK; ++d)
+                acc += orc_bf16_value(q[(int64_t)h * DQK + d]) * orc_bf16_value(kv[(int64_t)slots[i] * DQK + d]);
+            sc[(size_t)i] = scale * acc;
+            mx = std::max(mx, sc[(size_t)i]);
+        }
+        double* o = out + (int64_t)h * DV;
+        double* ms = mass ? mass + (int64_t)h * DV : nullptr;
+        for (int d = 0; d < DV; ++d) {
+            o[d] = 0.0;
+            if (ms) ms[d] = 0.0;
+        }
+        if (!(mx > -std::numeric_limits<double>::infinity())) {
+            lse[h] = -std::numeric_limits<double>::infinity();
+            continue;
+        }
+        double sum = 0.0;
+        for (int i = 0; i < k; ++i)
+            if (slots[i] >= 0) sum += std::exp(sc[(size_t)i] - mx);
+        for (int i = 0; i < k; ++i) {
+            if (slots[i] < 0) continue;
+            const double p = std::exp(sc[(size_t)i] - mx) / sum;
+            for (int d = 0; d < DV; ++d) {
+                const double v = orc_bf16_value(kv[(int64_t)slots[i] * DQK + d]);
+                o[d] += p * v;
+                if (ms) ms[d] += p * std::fabs(v);
+            }
+        }
+        lse[h] = mx + std::log(sum);
+    }
+    return ORC_OK;
 }
 
 // ---- [EXPL "Prefill: one-round histogram"] chunked-prefill block ----------
