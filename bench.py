@@ -361,6 +361,40 @@ def run_ours(args):
         early_rows.append(int(lay.cache.early_cnt.sum().item()))
         recall_ms.append(max(0.0, ev["c1"].elapsed_time(ev["r1"])))
         recall_rows.append(int(lay.cache.miss_cnt.sum().item()))
+    # ---------------- consumer: sparse MLA decode attention over the slots the step gave
+    # the selected tokens (the cache's rows), timed alone with events, L2 flushed
+    gq = torch.Generator(device=dev).manual_seed(7)
+    q_mla = torch.randn((lay.B, L.MLA_HEADS, L.MLA_DQK), generator=gq, device=dev).to(torch.bfloat16)
+    o_mla = torch.empty((lay.B, L.MLA_HEADS, L.MLA_DV), dtype=torch.float32, device=dev)
+    lse_mla = torch.empty((lay.B, L.MLA_HEADS), dtype=torch.float32, device=dev)
+    ws_mla = torch.empty(L.mla_workspace_size(lay.B, lay.k), dtype=torch.uint8, device=dev)
+    mla_ms = []
+    for r in range(reps + 3):
+        with torch.cuda.stream(main):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(main)
+            L.mla_decode(q_mla, lay.sel_slot, lay.cache.dev_kv, lay.C, 1.0 / math.sqrt(192.0), o_mla, lse_mla,
+                         ws_mla, lay.status, stream=main)
+            b.record(main)
+        torch.cuda.synchronize()
+        if r >= 3:
+            mla_ms.append(a.elapsed_time(b))
+    n_sel = int((lay.sel_slot >= 0).sum().item())
+    mla_flops = 2.0 * L.MLA_HEADS * n_sel * (L.MLA_DQK + L.MLA_DV)
+    mla_bytes = n_sel * lay.cache.row_bytes + q_mla.numel() * 2 + o_mla.numel() * 4 + lse_mla.numel() * 4
+    t_mla = statistics.mean(mla_ms) / 1e3
+    mla_detail = {"kernels": "mla_split_kernel + mla_combine_kernel (echo_mla_decode)", "heads": L.MLA_HEADS,
+                  "selected_rows": n_sel, "us": round(1e6 * t_mla, 2),
+                  "tflops": round(mla_flops / t_mla / 1e12, 2), "gbs": round(mla_bytes / t_mla / 1e9, 1),
+                  "algorithmic_flops": mla_flops, "algorithmic_bytes": mla_bytes}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            bf16_peak = float(json.load(f)["bf16_tflops"])
+        mla_detail["tensor_frac_of_measured_bf16"] = round(mla_detail["tflops"] / bf16_peak, 4)
+    except Exception:
+        pass
+    mla_detail["hbm_frac_of_peak"] = round(mla_detail["gbs"] / measured_peaks()[0], 4)
     misses_per_step = float(stats[L.STAT_MISSES]) / args.steps
     early_per_step = float(stats[L.STAT_EARLY]) / args.steps
     kern_us = {n: 1e3 * statistics.mean(v) for n, v in kt.items()}
@@ -443,7 +477,8 @@ def run_ours(args):
                    "recall_rows_per_step_kernel_pass": round(statistics.mean(recall_rows), 1),
                    "early_fetch_gbs": round(recall_gbs, 1), "h2d_copy_gbs": round(h2d_gbs, 1),
                    "recall_frac_of_h2d": round(recall_gbs / h2d_gbs, 4) if h2d_gbs else None,
-                   "step_ms_min": round(min(step_ms), 4), "step_ms_median": round(statistics.median(step_ms), 4)},
+                   "step_ms_min": round(min(step_ms), 4), "step_ms_median": round(statistics.median(step_ms), 4),
+                   "mla_decode": mla_detail},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n, secs, threads = oracle_steps(w, cpu_inputs(w, k8, ks, wt, host, q_all), max_steps=args.steps,

@@ -355,6 +355,31 @@ int echo_prefill_block_static(int R, int64_t row0, int64_t n_keys, const float* 
                               const echo_cache* cache, int32_t* sel_slot, int32_t* status, uint32_t* stats,
                               echo_stream_t stream, echo_stream_t copy_stream);
 
+/*
+ * Sparse MLA decode attention over the selected slots [EXPL section 2: a
+ * decode step attends over the k selected tokens only; the formula is
+ * DeepSeek-V3.2's sparse MLA in its absorbed form, the pages give none]:
+ * per request b and head h, over the entries i with sel_slot[b,i] >= 0,
+ *   s_i = scale * sum_{d<576} q[b,h,d] * kv[b*C + sel_slot[b,i], d],
+ *   out[b,h,:] = sum_i softmax(s)_i * kv[b*C + sel_slot[b,i], 0:512],
+ *   lse[b,h] = log sum_i exp(s_i)   (out = 0, lse = -inf with no valid slot).
+ *   q [B,128,576] bf16 (as uint16 bits), dev_kv [B*C,576] bf16 rows (the
+ *   cache's rows, 1152 bytes each), both 16-byte aligned; sel_slot [B,k];
+ *   out [B,128,512] f32 (16-byte aligned), lse [B,128] f32.
+ *   ws: echo_mla_workspace_size(B, k) bytes of device memory (16-byte
+ *   aligned), the splits' partial results.
+ * Scores are fp32 sums of bf16 products (tensor cores); the softmax weights
+ * enter the value sum rounded to bf16.
+ */
+#define ECHO_MLA_HEADS 128
+#define ECHO_MLA_DQK 576
+#define ECHO_MLA_DV 512
+#define ECHO_MLA_SPLIT 256   /* selection entries per split */
+size_t echo_mla_workspace_size(int B, int k);
+int echo_mla_decode(int B, int k, const uint16_t* q, const int32_t* sel_slot, const void* dev_kv, int64_t C,
+                    float scale, float* out, float* lse, void* ws, size_t ws_bytes, int32_t* status,
+                    echo_stream_t stream);
+
 /* Device-accessible address of a pinned host buffer (for echo_cache.host_kv).
  * Returns ECHO_ECUDA when the pointer is not pinned/mapped host memory. */
 int echo_host_device_alias(const void* host_ptr, const void** device_ptr);

@@ -1,0 +1,84 @@
+"""GPU parity of the sparse MLA decode attention over the selected slots against
+the oracle (fp64): ragged selections with padding, a split boundary and a
+ragged last tile, an empty request, the full k = 2048 selection."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from sparse_attention_kv_echo_gb300 import _lib as L
+
+pytestmark = pytest.mark.gpu
+dev = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    L.load(build_if_missing=True)
+
+
+def _bits(t):
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _run(B, C, k, valid_frac, seed, scale=1.0 / math.sqrt(192.0), empty=()):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((B, L.MLA_HEADS, L.MLA_DQK), generator=g).to(torch.bfloat16)
+    kv = torch.randn((B * C, L.MLA_DQK), generator=g).to(torch.bfloat16)
+    rng = np.random.default_rng(seed)
+    sel = np.full((B, k), -1, np.int32)
+    for b in range(B):
+        if b in empty:
+            continue
+        m = max(1, int(k * valid_frac))
+        pos = np.sort(rng.choice(k, m, replace=False))
+        sel[b, pos] = rng.choice(C, m, replace=False)
+    out = torch.empty((B, L.MLA_HEADS, L.MLA_DV), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, L.MLA_HEADS), dtype=torch.float32, device=dev)
+    ws = torch.empty(L.mla_workspace_size(B, k), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    L.mla_decode(q.to(dev), torch.from_numpy(sel).to(dev), kv.to(dev), C, scale, out, lse, ws, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return q, kv, sel, out.cpu().numpy(), lse.cpu().numpy(), scale
+
+
+def _check(q, kv, sel, out, lse, scale, C, orc):
+    kvb = _bits(kv)
+    qb = _bits(q)
+    for b in range(sel.shape[0]):
+        ref, ref_lse, mass = orc.mla_decode(qb[b], kvb[b * C:(b + 1) * C], sel[b], scale)
+        tol = 5e-3 * mass + 1e-5
+        bad = np.abs(out[b] - ref) > tol
+        assert not bad.any(), (b, np.argwhere(bad)[:5], out[b][bad][:5], ref[bad][:5])
+        fin = np.isfinite(ref_lse)
+        assert np.array_equal(fin, np.isfinite(lse[b]))
+        assert np.all(np.abs(lse[b][fin] - ref_lse[fin]) <= 3e-3 * np.maximum(1.0, np.abs(ref_lse[fin])))
+
+
+def test_one_tile(orc):
+    B, C, k = 1, 64, 16            # one split of one tile
+    r = _run(B, C, k, 1.0, 3)
+    _check(*r, C, orc)
+
+
+def test_ragged_selection_two_splits(orc):
+    B, C, k = 3, 700, 300          # splits of 256 + 44 (a ragged last tile), padding, one empty request
+    r = _run(B, C, k, 0.8, 0, empty=(1,))
+    _check(*r, C, orc)
+    out = r[3]
+    assert np.all(out[1] == 0) and np.all(np.isneginf(r[4][1]))
+
+
+def test_full_selection_batch(orc):
+    B, C, k = 2, 4096, 2048        # the decode workload's k and slots
+    r = _run(B, C, k, 1.0, 1)
+    _check(*r, C, orc)
+
+
+def test_peaked_scores(orc):
+    # a large scale makes the softmax nearly one-hot: the running max moves between tiles
+    B, C, k = 1, 512, 256
+    r = _run(B, C, k, 1.0, 2, scale=0.5)
+    _check(*r, C, orc)
