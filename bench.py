@@ -59,6 +59,9 @@ def parse_args(argv=None):
                    help="where the selected tokens' slots are looked up (top-k's slices or the cache step)")
     p.add_argument("--hold-early", action="store_true",
                    help="the held-slot variant of the cache step (the late recall need not wait for the early copy)")
+    p.add_argument("--part", choices=["step", "mla"], default="step",
+                   help="step: the decode step (default); mla: the sparse MLA attention over the selected "
+                        "slots alone, at the step's batch, k and GPU slots")
     p.add_argument("--first-share", type=float, default=None,
                    help="share of the requests in the first of two groups (default: the layer's choice)")
     return p.parse_args(argv)
@@ -367,7 +370,6 @@ def run_ours(args):
     q_mla = torch.randn((lay.B, L.MLA_HEADS, L.MLA_DQK), generator=gq, device=dev).to(torch.bfloat16)
     o_mla = torch.empty((lay.B, L.MLA_HEADS, L.MLA_DV), dtype=torch.float32, device=dev)
     lse_mla = torch.empty((lay.B, L.MLA_HEADS), dtype=torch.float32, device=dev)
-    ws_mla = torch.empty(L.mla_workspace_size(lay.B, lay.k), dtype=torch.uint8, device=dev)
     mla_ms = []
     for r in range(reps + 3):
         with torch.cuda.stream(main):
@@ -375,7 +377,7 @@ def run_ours(args):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(main)
             L.mla_decode(q_mla, lay.sel_slot, lay.cache.dev_kv, lay.C, 1.0 / math.sqrt(192.0), o_mla, lse_mla,
-                         ws_mla, lay.status, stream=main)
+                         lay.status, stream=main)
             b.record(main)
         torch.cuda.synchronize()
         if r >= 3:
@@ -384,7 +386,7 @@ def run_ours(args):
     mla_flops = 2.0 * L.MLA_HEADS * n_sel * (L.MLA_DQK + L.MLA_DV)
     mla_bytes = n_sel * lay.cache.row_bytes + q_mla.numel() * 2 + o_mla.numel() * 4 + lse_mla.numel() * 4
     t_mla = statistics.mean(mla_ms) / 1e3
-    mla_detail = {"kernels": "mla_split_kernel + mla_combine_kernel (echo_mla_decode)", "heads": L.MLA_HEADS,
+    mla_detail = {"kernels": "mla_split_kernel (echo_mla_decode)", "heads": L.MLA_HEADS,
                   "selected_rows": n_sel, "us": round(1e6 * t_mla, 2),
                   "tflops": round(mla_flops / t_mla / 1e12, 2), "gbs": round(mla_bytes / t_mla / 1e9, 1),
                   "algorithmic_flops": mla_flops, "algorithmic_bytes": mla_bytes}
@@ -522,10 +524,79 @@ def run_reference(args):
     }), flush=True)
 
 
+# ----------------------------------------------------------------------------- consumer alone
+MLA_METRIC = "sparse MLA decode attention over the selected slots: requests/s (128 heads, k selected rows)"
+
+
+def run_mla(args):
+    """The sparse MLA decode attention alone: 8 requests, k = 2048 selected slots
+    each (distinct, random) out of 4096 GPU slots of 576-dim bf16 rows, 128 heads."""
+    import numpy as np
+    import torch
+    from sparse_attention_kv_echo_gb300 import _lib as L
+    from sparse_attention_kv_echo_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    L.load(build_if_missing=True)
+    w = wl.WORKLOADS["batch"]
+    B, k, C = w.B, w.k, w.C
+    g = torch.Generator(device=dev).manual_seed(11 + rank)
+    q = torch.randn((B, L.MLA_HEADS, L.MLA_DQK), generator=g, device=dev).to(torch.bfloat16)
+    kv = torch.randn((B * C, L.MLA_DQK), generator=g, device=dev).to(torch.bfloat16)
+    rng = np.random.default_rng(11 + rank)
+    sel = torch.from_numpy(np.stack([rng.permutation(C)[:k] for _ in range(B)]).astype(np.int32)).to(dev)
+    out = torch.empty((B, L.MLA_HEADS, L.MLA_DV), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, L.MLA_HEADS), dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    main = torch.cuda.Stream()
+    scale = 1.0 / math.sqrt(192.0)
+
+    def call():
+        L.mla_decode(q, sel, kv, C, scale, out, lse, st, stream=main)
+
+    for _ in range(args.warmup):
+        with torch.cuda.stream(main):
+            flush.zero_()
+            call()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    park(main)
+    for i in range(args.steps):
+        with torch.cuda.stream(main):
+            flush.zero_()
+            starts[i].record(main)
+            call()
+            ends[i].record(main)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    t = statistics.mean(ms) / 1e3
+    flops = 2.0 * L.MLA_HEADS * B * k * (L.MLA_DQK + L.MLA_DV)
+    nbytes = B * k * L.MLA_DQK * 2 + q.numel() * 2 + out.numel() * 4 + lse.numel() * 4
+    peak, kind = measured_peaks()
+    print(json.dumps({
+        "metric": MLA_METRIC, "value": round(B / t, 1), "unit": "requests/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t, 5), "higher_is_better": True,
+        "dtype": "bf16 MMA, fp32 accumulate/softmax", "data": "synthetic (seeded)",
+        "config": {"workload": f"{B} requests x {k} selected of {C} GPU slots, 576-dim bf16 rows, 128 heads",
+                   "l2": "flushed by a 256 MB write before every timed call"},
+        "roofline": {"kernel": "mla_split_kernel", "bound": "hbm",
+                     "achieved": round(nbytes / t / 1e9, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(nbytes / t / 1e9 / peak, 4), "algorithmic_bytes": nbytes,
+                     "peak_source": f"hbm_gbs, {kind}"},
+        "tflops": round(flops / t / 1e12, 2), "us_min": round(1e3 * min(ms), 2), "status": int(st.item()),
+    }), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.part == "mla":
+        run_mla(args)
     else:
         run_ours(args)
 

@@ -366,19 +366,23 @@ int echo_prefill_block_static(int R, int64_t row0, int64_t n_keys, const float* 
  *   q [B,128,576] bf16 (as uint16 bits), dev_kv [B*C,576] bf16 rows (the
  *   cache's rows, 1152 bytes each), both 16-byte aligned; sel_slot [B,k];
  *   out [B,128,512] f32 (16-byte aligned), lse [B,128] f32.
- *   ws: echo_mla_workspace_size(B, k) bytes of device memory (16-byte
- *   aligned), the splits' partial results.
+ *   k <= ECHO_MLA_MAX_K.  No workspace: the selection is cut into at most
+ *   ECHO_MLA_MAX_SPLITS splits (one thread-block cluster per request and
+ *   output half) that combine on chip.
+ *   A device-side wait that gives up sets ECHO_ST_TIMEOUT in *status.
+ *   Errors: ECHO_EINVAL (sizes, NULL or misaligned pointers),
+ *   ECHO_EUNSUPPORTED (B > ECHO_MAX_REQUESTS or k > ECHO_MLA_MAX_K),
+ *   ECHO_ECUDA (launch).
  * Scores are fp32 sums of bf16 products (tensor cores); the softmax weights
  * enter the value sum rounded to bf16.
  */
 #define ECHO_MLA_HEADS 128
 #define ECHO_MLA_DQK 576
 #define ECHO_MLA_DV 512
-#define ECHO_MLA_SPLIT 256   /* selection entries per split */
-size_t echo_mla_workspace_size(int B, int k);
+#define ECHO_MLA_MAX_SPLITS 8
+#define ECHO_MLA_MAX_K 8192
 int echo_mla_decode(int B, int k, const uint16_t* q, const int32_t* sel_slot, const void* dev_kv, int64_t C,
-                    float scale, float* out, float* lse, void* ws, size_t ws_bytes, int32_t* status,
-                    echo_stream_t stream);
+                    float scale, float* out, float* lse, int32_t* status, echo_stream_t stream);
 
 /* Device-accessible address of a pinned host buffer (for echo_cache.host_kv).
  * Returns ECHO_ECUDA when the pointer is not pinned/mapped host memory. */

@@ -26,8 +26,7 @@ TOPK_CACHED_MAX_SLOTS = 32768  # C limit of echo_topk_select_cached
 EARLY_FETCH_BLOCKS = 32      # CTAs of the early-fetch and late-recall kernels
 
 EXPORTS = ("echo_above_words", "echo_cache_step", "echo_cache_step_resolved", "echo_device_sm_count",
-           "echo_early_fetch", "echo_host_device_alias", "echo_index_scores", "echo_mla_decode",
-           "echo_mla_workspace_size", "echo_prefill_block",
+           "echo_early_fetch", "echo_host_device_alias", "echo_index_scores", "echo_mla_decode", "echo_prefill_block",
            "echo_prefill_block_static", "echo_prefill_scores", "echo_prefill_workspace_size", "echo_quantize_q",
            "echo_topk_select", "echo_topk_select_cached")
 
@@ -82,10 +81,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         L.echo_cache_step.restype = i32
         L.echo_cache_step.argtypes = [i32, _vp, i64, _vp, i32, _vp, i32, ctypes.POINTER(EchoCacheStruct), _vp,
                                       _vp, _vp, _vp, _vp, i32]
-        L.echo_mla_workspace_size.restype = ctypes.c_size_t
-        L.echo_mla_workspace_size.argtypes = [i32, i32]
         L.echo_mla_decode.restype = i32
-        L.echo_mla_decode.argtypes = [i32, i32, _vp, _vp, _vp, i64, f32, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]
+        L.echo_mla_decode.argtypes = [i32, i32, _vp, _vp, _vp, i64, f32, _vp, _vp, _vp, _vp]
         L.echo_topk_select_cached.restype = i32
         L.echo_topk_select_cached.argtypes = [i32, _vp, i64, _vp, i32, _vp, _vp, f32, _vp, _vp, _vp, i32,
                                               ctypes.POINTER(EchoCacheStruct), _vp, _vp, _vp, _vp]
@@ -240,20 +237,16 @@ def cache_step_resolved(tok_off, n_tokens, sel, cache, sel_slot, status, stats=N
         _ptr(status), _ptr(stats), st, cst, CACHE_HOLD_EARLY if hold_early else 0))
 
 
-MLA_HEADS, MLA_DQK, MLA_DV = 128, 576, 512
+MLA_HEADS, MLA_DQK, MLA_DV, MLA_MAX_K = 128, 576, 512, 8192
 
 
-def mla_workspace_size(B: int, k: int) -> int:
-    return int(load().echo_mla_workspace_size(int(B), int(k)))
-
-
-def mla_decode(q, sel_slot, dev_kv, C, scale, out, lse, ws, status, stream=None):
+def mla_decode(q, sel_slot, dev_kv, C, scale, out, lse, status, stream=None):
     """echo_mla_decode: q [B,128,576] bf16, sel_slot [B,k] int32, dev_kv [B*C,576] bf16 (the
-    cache's rows) -> out [B,128,512] f32, lse [B,128] f32; ws: uint8 device workspace."""
+    cache's rows) -> out [B,128,512] f32, lse [B,128] f32."""
     B, k = sel_slot.shape
     _check("echo_mla_decode", load().echo_mla_decode(
         int(B), int(k), _ptr(q), _ptr(sel_slot), _ptr(dev_kv), int(C), float(scale), _ptr(out), _ptr(lse),
-        _ptr(ws), ws.numel() * ws.element_size(), _ptr(status), _stream(stream)))
+        _ptr(status), _stream(stream)))
 
 
 def prefill_scores(R, row0, n_keys, q8, wfold, k8, ks, scores, W, theta_hat, hist, status, stream=None):

@@ -9,19 +9,29 @@
 //   s_t = scale * q[h] . kv[slot_t]   (576 dims),   out[h] = softmax(s) . kv[slot_t][0:512].
 //
 // CTA (request b, output half, split of the selection) takes the 128 heads and
-// the split's tokens, 16 at a time:
-//   S = Q K^T   tcgen05.mma kind::f16 (bf16 in, fp32 in TMEM), M = 128 heads,
-//               N = 16 tokens, K = 576 in 36 steps; Q stays in shared memory
-//               (128-byte swizzle, K-major), the 16 gathered KV rows are B;
-//   softmax     one thread per head reads its S row from TMEM, keeps the
-//               running max and sum in fp32, writes its P row (bf16) to shared
-//               memory and rescales its O row in TMEM when the max grows;
-//   O += P V    M = 128 heads, N = 256 dims (the CTA's half), K = 16 tokens:
-//               P is A; the tile's value dims, transposed in shared memory into
-//               the same K-major swizzled layout (a row per dim), are B.
-// Every operand uses the one K-major 128-byte-swizzle layout.
-// Each split leaves its unnormalised O and its (max, sum) per head; a second
-// kernel combines the splits.
+// the split's tokens, 32 at a time, in a two-stage pipeline (the gather of the
+// next tile is in flight while this one is computed):
+//   S = Q K^T   tcgen05.mma kind::f16 (bf16 in, fp32 in TMEM, two S buffers),
+//               M = 128 heads, N = 32 tokens, K = 576 in 36 steps; Q stays in
+//               shared memory (128-byte swizzle, K-major), the gathered KV rows
+//               of the tile (same layout, a row per token) are B;
+//   softmax     one thread per head reads its S row from TMEM and keeps a
+//               running reference max and sum in fp32.  The reference moves
+//               only when a score exceeds it by more than 2^8 (P <= 256 in
+//               bf16, exact after the final division); O in TMEM is rescaled
+//               then.  The P row (bf16) goes to the tile's atoms of the other
+//               output half, which S no longer needs;
+//   O += P V    M = 128 heads, N = 256 dims (the CTA's half), K = 32 tokens in
+//               2 steps: P is A (K-major); V is the tile's value dims read in
+//               place as an MN-major B operand (dims contiguous in a 128-byte
+//               swizzled row, tokens across rows).
+// The splits of one (request, half) -- at most 8, sized on the host so the
+// grid runs in the fewest waves of resident clusters -- form one thread-block cluster and combine in distributed shared memory:
+// each CTA publishes its (reference max, sum) per head, scales its O rows by
+// 2^(m_j - M) / L and stages them in shared memory; CTA r of the cluster then
+// sums its share of the heads over the cluster and writes out and lse.  No
+// partial result goes to global memory.
+#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
 #include "echo_common.cuh"
@@ -34,17 +44,19 @@ constexpr int kHeads = ECHO_MLA_HEADS;      // 128
 constexpr int kDqk = ECHO_MLA_DQK;          // 576
 constexpr int kDv = ECHO_MLA_DV;            // 512
 constexpr int kRowBytes = kDqk * 2;         // 1152
-constexpr int kTok = 16;                    // tokens per tile
-constexpr int kSplit = ECHO_MLA_SPLIT;      // tokens per CTA
+constexpr int kTok = 32;                    // tokens per tile
+constexpr int kMaxSplits = ECHO_MLA_MAX_SPLITS;      // 8: CTAs of one cluster
+constexpr int kSplitMax = ECHO_MLA_MAX_K / ECHO_MLA_MAX_SPLITS;  // 1024: most tokens per split
 constexpr int kThreads = 128;               // one thread per head
 constexpr int kAtoms = kDqk / 64;           // 9 swizzle atoms of 64 bf16 along the 576 dims
 constexpr int kChunks = kRowBytes / 16;     // 72 16-byte pieces per row
 constexpr uint32_t kQBytes = kAtoms * kHeads * 128;   // Q: 9 x (128 rows x 128 B)
-constexpr uint32_t kKBytes = kAtoms * kTok * 128;     // tile: 9 x (16 rows x 128 B)
-constexpr uint32_t kPBytes = kHeads * 128;            // P: 128 rows x 128 B (first 32 B used)
-constexpr uint32_t kVBytes = 256 * 128;               // V^T of the half: 256 rows x 128 B (first 32 B used)
-constexpr uint32_t kTmemCols = 512;                   // S [0, 32) | O [32, 288)
-constexpr uint32_t kOCol = 32;
+constexpr uint32_t kAtomBytes = kTok * 128;           // one atom of a tile: 32 rows x 128 B
+constexpr uint32_t kKBytes = kAtoms * kAtomBytes;     // a tile: 9 atoms
+constexpr int kStages = 2;
+constexpr uint32_t kTmemCols = 512;                   // S0 [0, 32) | S1 [32, 64) | O [64, 320)
+constexpr uint32_t kOCol = 64;
+constexpr float kLazy = 8.f;                          // log2 headroom before the reference max moves
 constexpr uint64_t kMlaWaitNs = 100000000ull;         // 0.1 s: a tile's MMA takes microseconds
 
 struct MlaCtl {
@@ -52,9 +64,16 @@ struct MlaCtl {
     uint64_t pv_bar;     // PV MMA of the tile done
     uint32_t tmem;       // TMEM base address
     int abort;
+    uint32_t valid[kStages];  // tokens of the staged tile with a slot (bit t)
+    float m[kHeads];          // this split's reference max (log2 units) per head
+    float l[kHeads];          // this split's sum per head
+    int32_t slot[kSplitMax];  // the split's slots
 };
-constexpr uint32_t kSmem = kQBytes + kKBytes + kPBytes + kVBytes + 1024 /* control */ + 1024 /* alignment */;
+constexpr uint32_t kCtlBytes = (sizeof(MlaCtl) + 1023u) & ~1023u;
+constexpr uint32_t kSmem = kQBytes + kStages * kKBytes + kCtlBytes + 1024 /* alignment */;
 static_assert(kSmem <= 227u * 1024u, "MLA shared memory");
+static_assert(kHeads * 128 == 4 * kAtomBytes, "P fills the 4 atoms of the other output half");
+static_assert(kHeads * 256 * 4 <= kQBytes, "the scaled O rows fit where Q was");
 
 // Instruction descriptor of kind::f16 with bf16 A and B (both K-major), fp32
 // accumulator, shape M x N: D format [4,6) = 1 (f32), A / B format [7,10) /
@@ -63,7 +82,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 constexpr uint32_t kIdescS = idesc_bf16_f32(128, kTok);
-constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256);
+constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256) | (1u << 16);  // B (V) MN-major
+
+// Shared-memory descriptor of an MN-major operand in the 128-byte swizzle: 64
+// MN elements contiguous in a 128-byte row, K across rows (8-row groups 1024
+// bytes apart: stride byte offset), successive 64-element MN groups lbo bytes
+// apart (leading byte offset).  Same version and swizzle fields as the K-major one.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr, uint32_t lbo) {
+    return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
 
 // Bounded wait on an mbarrier phase (this kernel's own limit).
 __device__ __forceinline__ bool mla_wait(uint32_t bar, uint32_t parity, const volatile int* abort) {
@@ -122,6 +151,14 @@ __device__ __forceinline__ void tmem_st_x32(uint32_t taddr, const float (&r)[32]
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 2^x by the hardware's approximate base-2 exponential (ex2.approx.ftz): the
+// softmax weights are rounded to bf16 right after, far coarser than its error.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -133,35 +170,70 @@ __device__ __forceinline__ uint32_t sw_offset(int r, int c, uint32_t atom_bytes)
            (static_cast<uint32_t>((c & 7) ^ (r & 7)) << 4);
 }
 
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src))
+// 16-byte asynchronous copy global -> shared; src_bytes 0 writes zeros without reading.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes = 16u) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)),
+                 "r"(src_bytes)
                  : "memory");
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
 }
 
+// The gather of tile `it` of the split into stage buffer sT: 4 threads per row,
+// 18 pieces each; rows without a slot are zero-filled (their scores are masked
+// and their V rows must be finite).  Warp 0 also records the tile's valid mask.
+// sl: the split's slots in shared memory, from token t0 - t_lo on; n: tokens left.
+__device__ __forceinline__ void gather_tile(uint32_t sT, const int32_t* sl, int n, const uint8_t* kv, int64_t C,
+                                            int tid, uint32_t* valid) {
+    const int r = tid >> 2;
+    const int32_t slot = (r < n) ? sl[r] : -1;
+    const bool ok = slot >= 0 && slot < C;
+    const uint8_t* row = kv + (ok ? static_cast<int64_t>(slot) * kRowBytes : 0);
+#pragma unroll 6
+    for (int c = tid & 3; c < kChunks; c += 4) cp_async_16(sT + sw_offset(r, c, kAtomBytes), row + 16 * c, ok ? 16u : 0u);
+    cp_async_commit();
+    if (tid < 32) {
+        const int32_t sj = (tid < n) ? sl[tid] : -1;
+        const uint32_t m = __ballot_sync(0xffffffffu, sj >= 0 && sj < C);
+        if (tid == 0) *valid = m;
+    }
+}
+
+// Byte offset of float4 c (0..63) of staged O row h: the 16-byte pieces of a row
+// are permuted by h so a warp writing one piece of 32 rows spreads over the banks.
+__device__ __forceinline__ uint32_t ostage_offset(int h, int c) {
+    return static_cast<uint32_t>(h) * 1024u + (static_cast<uint32_t>(c ^ (h & 7)) << 4);
+}
+
+// Grid: B x 2 halves x splits CTAs, split index fastest; cluster = the splits
+// of one (request, half).
 __global__ void __launch_bounds__(kThreads, 1)
-    mla_split_kernel(int k, const uint16_t* __restrict__ q, const int32_t* __restrict__ sel_slot,
-                     const uint8_t* __restrict__ dev_kv, int64_t C, float scale_log2, float* __restrict__ opart,
-                     float* __restrict__ mpart, float* __restrict__ lpart, int splits, int32_t* status) {
+    mla_split_kernel(int k, int split_tokens, const uint16_t* __restrict__ q, const int32_t* __restrict__ sel_slot,
+                     const uint8_t* __restrict__ dev_kv, int64_t C, float scale_log2, float* __restrict__ out,
+                     float* __restrict__ lse, int32_t* status) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* const gbase = smem_raw + (base - raw);
-    // Q [9 atoms x 128 rows] | tile [9 atoms x 16 rows] | P [128 rows] | V^T [256 rows] | control
-    const uint32_t sQ = base, sK = sQ + kQBytes, sP = sK + kKBytes, sV = sP + kPBytes;
-    uint8_t* const gK = gbase + kQBytes;
-    uint8_t* const gP = gK + kKBytes;
-    uint8_t* const gV = gP + kPBytes;
-    MlaCtl* ctl = reinterpret_cast<MlaCtl*>(gV + kVBytes);
+    // Q [9 atoms x 128 rows] (later: the scaled O rows) | tile stage 0 | tile stage 1 | control
+    const uint32_t sQ = base, sT0 = sQ + kQBytes;
+    uint8_t* const gT0 = gbase + kQBytes;
+    MlaCtl* ctl = reinterpret_cast<MlaCtl*>(gT0 + kStages * kKBytes);
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int split = blockIdx.x % splits;
+    const int splits = static_cast<int>(cluster.num_blocks());
+    const int split = static_cast<int>(cluster.block_rank());
     const int half = (blockIdx.x / splits) & 1;
     const int b = blockIdx.x / (2 * splits);
-    const int t_lo = split * kSplit, t_hi = min(k, t_lo + kSplit);
-    const int32_t* sl = sel_slot + static_cast<int64_t>(b) * k;
+    const int t_lo = split * split_tokens, t_hi = min(k, t_lo + split_tokens);
+    const int n_tok = max(0, t_hi - t_lo);
     const uint8_t* kv = dev_kv + static_cast<int64_t>(b) * C * kRowBytes;
+    // P of a tile lives in the 4 atoms of the other output half (128 rows x 128 B)
+    const uint32_t p_off = static_cast<uint32_t>(4 * (1 - half)) * kAtomBytes;
+    const uint32_t v_off = static_cast<uint32_t>(4 * half) * kAtomBytes;
 
     if (tid == 0) {
         mbar_init(smem_addr(&ctl->s_bar), 1);
@@ -173,11 +245,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_addr(&ctl->tmem), kTmemCols);
         tmem_relinquish();
     }
-    // Q of the request: row h = head h, 72 pieces
+    // Q of the request (row h = head h), piece-major so a warp reads contiguous bytes
     {
-        const uint8_t* qrow = reinterpret_cast<const uint8_t*>(q) + (static_cast<int64_t>(b) * kHeads + tid) * kRowBytes;
-        for (int c = 0; c < kChunks; ++c) cp_async_16(sQ + sw_offset(tid, c, kHeads * 128u), qrow + 16 * c);
+        const uint8_t* qb = reinterpret_cast<const uint8_t*>(q) + static_cast<int64_t>(b) * kHeads * kRowBytes;
+#pragma unroll 8
+        for (int g = tid; g < kHeads * kChunks; g += kThreads) {
+            const int h = g / kChunks, c = g - h * kChunks;
+            cp_async_16(sQ + sw_offset(h, c, kHeads * 128u), qb + static_cast<int64_t>(h) * kRowBytes + 16 * c);
+        }
+        cp_async_commit();
     }
+    // the split's slots (one read of the selection)
+    {
+        const int32_t* sl = sel_slot + static_cast<int64_t>(b) * k + t_lo;
+        for (int i = tid; i < n_tok; i += kThreads) ctl->slot[i] = sl[i];
+    }
+    __syncthreads();
+    const int tiles = (n_tok + kTok - 1) / kTok;
+    if (tiles > 0) gather_tile(sT0, ctl->slot, n_tok, kv, C, tid, &ctl->valid[0]);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -187,58 +272,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool failed = false;
     uint32_t pending = 0, phase = 0;  // the barrier and phase a timed-out wait was on
 
-    float m = -INFINITY, l = 0.f;  // this thread's head: running max (of log2-scaled scores) and sum
-    const int tiles = (t_hi - t_lo + kTok - 1) / kTok;
+    float m = -INFINITY, l = 0.f;  // this thread's head: reference max (log2-scaled scores) and sum
     for (int it = 0; it < tiles; ++it) {
-        const int t0 = t_lo + it * kTok;
-        // ---- gather the tile's KV rows (8 threads per row, 9 pieces each); rows
-        // without a slot are zero (their scores are masked in the softmax)
-        {
-            const int r = tid >> 3;
-            const int i = t0 + r;
-            const int32_t slot = (i < t_hi) ? sl[i] : -1;
-            if (slot >= 0 && slot < C) {
-                const uint8_t* row = kv + static_cast<int64_t>(slot) * kRowBytes;
-                for (int c = tid & 7; c < kChunks; c += 8) cp_async_16(sK + sw_offset(r, c, kTok * 128u), row + 16 * c);
-            } else {
-                for (int c = tid & 7; c < kChunks; c += 8)
-                    *reinterpret_cast<uint4*>(gK + sw_offset(r, c, kTok * 128u)) = make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
+        const int st = it & 1;
+        const uint32_t sT = sT0 + static_cast<uint32_t>(st) * kKBytes;
+        uint8_t* const gT = gT0 + st * kKBytes;
+        // ---- tile `it` (and Q) landed
         cp_async_wait_all();
-        __syncthreads();
-        // ---- V^T of this half: row n = value dim 256 * half + n, its 16 tokens in
-        // the first 32 bytes (two 16-byte pieces, swizzled like every operand)
-        {
-#pragma unroll
-            for (int jn = 0; jn < 2; ++jn) {
-                const int n = 2 * tid + jn;
-                const int d = 256 * half + n;
-                uint32_t w[8];
-#pragma unroll
-                for (int t = 0; t < kTok; t += 2) {
-                    const uint16_t* r0 = reinterpret_cast<const uint16_t*>(gK + sw_offset(t, d >> 3, kTok * 128u));
-                    const uint16_t* r1 = reinterpret_cast<const uint16_t*>(gK + sw_offset(t + 1, d >> 3, kTok * 128u));
-                    w[t >> 1] = static_cast<uint32_t>(r0[d & 7]) | (static_cast<uint32_t>(r1[d & 7]) << 16);
-                }
-                uint8_t* vrow = gV + n * 128;
-                *reinterpret_cast<uint4*>(vrow + (((0 ^ (n & 7)) & 7) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-                *reinterpret_cast<uint4*>(vrow + (((1 ^ (n & 7)) & 7) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
-            }
-        }
         fence_proxy_async_smem();
         __syncthreads();
-        // ---- S = Q K^T
+        // ---- S = Q K^T into S buffer st
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll 4
             for (int kk = 0; kk < kAtoms * 4; ++kk) {
                 const uint32_t a = static_cast<uint32_t>(kk >> 2), off = static_cast<uint32_t>(kk & 3) * 32u;
-                mma_bf16(tmem, sw128_kmajor_desc(sQ + a * kHeads * 128u + off),
-                         sw128_kmajor_desc(sK + a * kTok * 128u + off), kIdescS, kk > 0 ? 1u : 0u);
+                mma_bf16(tmem + static_cast<uint32_t>(st) * kTok, sw128_kmajor_desc(sQ + a * kHeads * 128u + off),
+                         sw128_kmajor_desc(sT + a * kAtomBytes + off), kIdescS, kk > 0 ? 1u : 0u);
             }
             mma_commit(smem_addr(&ctl->s_bar));
         }
+        // ---- the previous tile's PV done: its stage buffer takes the next gather
+        if (it > 0) {
+            if (__syncthreads_or(!mla_wait(smem_addr(&ctl->pv_bar), (it - 1) & 1, abort))) {
+                failed = true;
+                pending = smem_addr(&ctl->pv_bar);
+                phase = (it - 1) & 1;
+                break;
+            }
+        }
+        if (it + 1 < tiles)
+            gather_tile(sT0 + static_cast<uint32_t>(st ^ 1) * kKBytes, ctl->slot + (it + 1) * kTok,
+                        n_tok - (it + 1) * kTok, kv, C, tid, &ctl->valid[st ^ 1]);
         if (__syncthreads_or(!mla_wait(smem_addr(&ctl->s_bar), it & 1, abort))) {  // block-uniform
             failed = true;
             pending = smem_addr(&ctl->s_bar);
@@ -246,44 +311,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
         }
         tc_fence_after();
-        // ---- online softmax of this head's row; P row to shared memory
+        // ---- softmax of this head's row against the reference max; P row to shared memory
         {
-            float s[16];
-            {
-                uint32_t u[16];
-                tmem_ld_x16(tmem + lane_base, u);
-                tmem_wait_ld();
+            float s[kTok];
+            tmem_ld_x32(tmem + lane_base + static_cast<uint32_t>(st) * kTok, s);
+            const uint32_t vm = ctl->valid[st];
 #pragma unroll
-                for (int t = 0; t < 16; ++t) s[t] = __uint_as_float(u[t]);
-            }
-            float mx = m;
+            for (int t = 0; t < kTok; ++t) s[t] = ((vm >> t) & 1u) ? s[t] : -INFINITY;
+            // tile max of the raw scores (a tree: short dependency chains); scale > 0
+            float mx[kTok / 2];
 #pragma unroll
-            for (int t = 0; t < kTok; ++t) {
-                const bool v = t0 + t < t_hi && sl[t0 + t] >= 0 && sl[t0 + t] < C;
-                s[t] = v ? s[t] * scale_log2 : -INFINITY;
-                mx = fmaxf(mx, s[t]);
+            for (int t = 0; t < kTok / 2; ++t) mx[t] = fmaxf(s[2 * t], s[2 * t + 1]);
+#pragma unroll
+            for (int w = kTok / 4; w >= 1; w >>= 1)
+#pragma unroll
+                for (int t = 0; t < w; ++t) mx[t] = fmaxf(mx[t], mx[t + w]);
+            const float tmx = mx[0] * scale_log2;
+            const bool need = tmx > m + kLazy;  // also m = -inf with a valid token
+            // tcgen05.ld / st are warp-collective: the whole warp rescales when any head moves
+            const bool warp_moves = __any_sync(0xffffffffu, need);
+            float corr = 1.f;
+            if (warp_moves && tmx > m) {
+                corr = ex2_approx(m - tmx);  // 0 when m = -inf
+                m = tmx;
             }
-            const float corr = (mx == -INFINITY) ? 1.f : exp2f(m - mx);
-            float sum = 0.f;
-            uint32_t packed[8];
+            // p = 2^(s * scale_log2 - m); with m = -inf every score is -inf and p = 0
+            const float neg_m = (m == -INFINITY) ? 0.f : -m;
+            float part[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t packed[kTok / 2];
 #pragma unroll
             for (int t = 0; t < kTok; t += 2) {
-                const float p0 = (mx == -INFINITY) ? 0.f : exp2f(s[t] - mx);
-                const float p1 = (mx == -INFINITY) ? 0.f : exp2f(s[t + 1] - mx);
+                const float p0 = ex2_approx(fmaf(s[t], scale_log2, neg_m));
+                const float p1 = ex2_approx(fmaf(s[t + 1], scale_log2, neg_m));
                 const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-                sum += __low2float(pb) + __high2float(pb);  // the sum of the values the MMA uses
+                part[(t >> 1) & 3] += __low2float(pb) + __high2float(pb);  // the values the MMA uses
                 packed[t >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
             }
+            const float sum = (part[0] + part[1]) + (part[2] + part[3]);
             l = l * corr + sum;
-            m = mx;
-            uint8_t* prow = gP + tid * 128;
-            *reinterpret_cast<uint4*>(prow + (((0 ^ (tid & 7)) & 7) << 4)) =
-                make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            *reinterpret_cast<uint4*>(prow + (((1 ^ (tid & 7)) & 7) << 4)) =
-                make_uint4(packed[4], packed[5], packed[6], packed[7]);
-            // O holds earlier tiles: bring it to the new max.  tcgen05.ld / st are
-            // warp-collective, so the whole warp rescales when any of its heads must.
-            if (it > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+            uint8_t* prow = gT + p_off + tid * 128;
+#pragma unroll
+            for (int c = 0; c < kTok / 8; ++c)
+                *reinterpret_cast<uint4*>(prow + ((c ^ (tid & 7)) << 4)) =
+                    make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+            if (it > 0 && warp_moves) {  // O holds earlier tiles (their PV is done): bring it to the new reference
 #pragma unroll 1
                 for (int c = 0; c < 256; c += 32) {
                     float o[32];
@@ -297,119 +368,200 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         fence_proxy_async_smem();
         __syncthreads();
-        // ---- O += P V (this CTA's 256 dims), one K step of 16 tokens
+        // ---- O += P V (this CTA's 256 dims), two K steps of 16 tokens
         if (tid == 0) {
             tc_fence_after();
-            mma_bf16(tmem + kOCol, sw128_kmajor_desc(sP), sw128_kmajor_desc(sV), kIdescPV, it > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < kTok / 16; ++kk)
+                mma_bf16(tmem + kOCol, sw128_kmajor_desc(sT + p_off + kk * 32u),
+                         sw128_mnmajor_desc(sT + v_off + kk * 2048u, kAtomBytes), kIdescPV,
+                         (it > 0 || kk > 0) ? 1u : 0u);
             mma_commit(smem_addr(&ctl->pv_bar));
         }
-        // the tile, P and V^T are free again once the PV MMA is done
-        if (__syncthreads_or(!mla_wait(smem_addr(&ctl->pv_bar), it & 1, abort))) {
+    }
+    if (!failed && tiles > 0) {
+        if (__syncthreads_or(!mla_wait(smem_addr(&ctl->pv_bar), (tiles - 1) & 1, abort))) {
             failed = true;
             pending = smem_addr(&ctl->pv_bar);
-            phase = it & 1;
-            break;
+            phase = (tiles - 1) & 1;
         }
-        tc_fence_after();
     }
+    tc_fence_after();
     cp_async_wait_all();
     if (failed) {  // every thread took this branch; give the late MMA one more bounded wait
         if (tid == 0) {
             set_status(status, ECHO_ST_TIMEOUT);
             mla_wait(pending, phase, abort);
-            *abort = 1;
         }
+        m = -INFINITY;  // this split then adds nothing
+        l = 0.f;
     }
-    __syncthreads();
-    // ---- the split's unnormalised O, max and sum of each head
-    if (!*abort) {
-        float* orow = opart + ((static_cast<int64_t>(b) * splits + split) * kHeads + tid) * kDv + half * 256;
+    // ---- combine over the cluster.  Every CTA passes the same three cluster
+    // barriers whatever happened above.
+    ctl->m[tid] = m;
+    ctl->l[tid] = l;
+    cluster.sync();  // (1) every split's (m, l) is published
+    float mj[kMaxSplits], lj[kMaxSplits];
+#pragma unroll
+    for (int j = 0; j < kMaxSplits; ++j) {  // all loads in flight at once
+        mj[j] = (j < splits) ? cluster.map_shared_rank(ctl->m, j)[tid] : -INFINITY;
+        lj[j] = (j < splits) ? cluster.map_shared_rank(ctl->l, j)[tid] : 0.f;
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kMaxSplits; ++j) M = fmaxf(M, mj[j]);
+    float L = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxSplits; ++j)
+        if (M > -INFINITY && mj[j] > -INFINITY) L += lj[j] * exp2f(mj[j] - M);
+    const float f = (M > -INFINITY && L > 0.f && m > -INFINITY) ? exp2f(m - M) / L : 0.f;
+    // this head's O row, scaled, staged where Q was (the MMAs are done with Q)
+    {
+        const bool have_o = !failed && tiles > 0;
 #pragma unroll 1
         for (int c = 0; c < 256; c += 32) {
             float o[32];
-            tmem_ld_x32(tmem + lane_base + kOCol + c, o);
+            if (have_o) {
+                tmem_ld_x32(tmem + lane_base + kOCol + c, o);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) o[j] = 0.f;
+            }
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4*>(orow + c + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
-        }
-        if (half == 0) {
-            mpart[(static_cast<int64_t>(b) * splits + split) * kHeads + tid] = m;
-            lpart[(static_cast<int64_t>(b) * splits + split) * kHeads + tid] = l;
+                *reinterpret_cast<float4*>(gbase + ostage_offset(tid, (c + j) >> 2)) =
+                    make_float4(o[j] * f, o[j + 1] * f, o[j + 2] * f, o[j + 3] * f);
         }
     }
+    cluster.sync();  // (2) every split's scaled O is staged
+    // CTA `split` sums heads [h0, h1) over the cluster: one float4 of a head row per thread and pass
+    {
+        const int per = (kHeads + splits - 1) / splits;
+        const int h0 = split * per, h1 = min(kHeads, h0 + per);
+        for (int g = tid; g < (h1 - h0) * 64; g += kThreads) {
+            const int h = h0 + (g >> 6), c = g & 63;
+            float4 v[kMaxSplits];
+#pragma unroll
+            for (int j = 0; j < kMaxSplits; ++j)  // all loads in flight at once
+                v[j] = (j < splits) ? *reinterpret_cast<const float4*>(cluster.map_shared_rank(
+                                          reinterpret_cast<float*>(gbase + ostage_offset(h, c)), j))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 acc = v[0];
+#pragma unroll
+            for (int j = 1; j < kMaxSplits; ++j) {
+                acc.x += v[j].x;
+                acc.y += v[j].y;
+                acc.z += v[j].z;
+                acc.w += v[j].w;
+            }
+            *reinterpret_cast<float4*>(out + (static_cast<int64_t>(b) * kHeads + h) * kDv + half * 256 + 4 * c) = acc;
+        }
+        if (half == 0 && tid >= h0 && tid < h1)  // this thread's head is in the share: its lse
+            lse[static_cast<int64_t>(b) * kHeads + tid] =
+                (M > -INFINITY && L > 0.f) ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+    }
+    cluster.sync();  // (3) no CTA leaves while another reads its shared memory
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-// The splits of one (request, head): out = sum_j 2^(m_j - M) O_j / L with
-// L = sum_j 2^(m_j - M) l_j (scores in log2 units), lse = ln(2) (M + log2 L).
-__global__ void __launch_bounds__(128)
-    mla_combine_kernel(int splits, const float* __restrict__ opart, const float* __restrict__ mpart,
-                       const float* __restrict__ lpart, float* __restrict__ out, float* __restrict__ lse) {
-    const int bh = blockIdx.x, b = bh / kHeads, h = bh % kHeads;
-    float M = -INFINITY;
-    for (int j = 0; j < splits; ++j) M = fmaxf(M, mpart[(static_cast<int64_t>(b) * splits + j) * kHeads + h]);
-    float L = 0.f;
-    for (int j = 0; j < splits; ++j) {
-        const int64_t e = (static_cast<int64_t>(b) * splits + j) * kHeads + h;
-        if (mpart[e] > -INFINITY) L += lpart[e] * exp2f(mpart[e] - M);
-    }
-    for (int d = threadIdx.x; d < kDv; d += blockDim.x) {
-        float acc = 0.f;
-        for (int j = 0; j < splits; ++j) {
-            const int64_t e = (static_cast<int64_t>(b) * splits + j) * kHeads + h;
-            if (mpart[e] > -INFINITY) acc += exp2f(mpart[e] - M) * opart[e * kDv + d];
-        }
-        out[static_cast<int64_t>(bh) * kDv + d] = (L > 0.f) ? acc / L : 0.f;
-    }
-    if (threadIdx.x == 0) lse[bh] = (L > 0.f) ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
-}
-
 }  // namespace
 
-int mla_splits(int k) { return (k + kSplit - 1) / kSplit; }
+// How many clusters of `size` CTAs of this kernel the device holds at once
+// (queried once per device and size).
+int max_active_clusters(int size) {
+    static int cache[64][kMaxSplits + 1];
+    static bool init = false;
+    if (!init) {
+        for (auto& row : cache)
+            for (int& v : row) v = -1;
+        init = true;
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    int& v = cache[dev][size];
+    if (v < 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(size));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(size);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, mla_split_kernel, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 0;
+        }
+        v = n;
+    }
+    return v;
+}
 
-size_t mla_workspace_bytes(int B, int k) {
-    const size_t parts = static_cast<size_t>(B) * mla_splits(k) * kHeads;
-    return parts * (kDv + 2) * sizeof(float) + 256;
+// Splits of the selection for B requests: the cluster size (at most 8) whose
+// grid of B x 2 clusters finishes soonest -- waves of resident clusters times
+// the tiles of a split plus about two tiles of fixed work (Q, combine).
+void mla_plan(int B, int k, int* split_tokens, int* splits) {
+    long best = -1;
+    for (int size = kMaxSplits; size >= 1; --size) {
+        int per = (k + size - 1) / size;
+        per = (per + kTok - 1) / kTok * kTok;
+        if (per > kSplitMax) break;
+        const int n = (k + per - 1) / per;
+        const int active = max_active_clusters(n);
+        if (active <= 0) continue;
+        const long waves = (2L * B + active - 1) / active;
+        const long cost = waves * (per / kTok + 2);
+        if (best < 0 || cost < best) {
+            best = cost;
+            *split_tokens = per;
+            *splits = n;
+        }
+    }
+    if (best < 0) {  // no residency figure: 8 splits
+        *split_tokens = ((k + kMaxSplits - 1) / kMaxSplits + kTok - 1) / kTok * kTok;
+        *splits = (k + *split_tokens - 1) / *split_tokens;
+    }
 }
 
 int launch_mla(int B, int k, const uint16_t* q, const int32_t* sel_slot, const void* dev_kv, int64_t C, float scale,
-               float* out, float* lse, void* ws, int32_t* status, cudaStream_t stream) {
-    const int splits = mla_splits(k);
-    const size_t parts = static_cast<size_t>(B) * splits * kHeads;
-    float* opart = static_cast<float*>(ws);
-    float* mpart = opart + parts * kDv;
-    float* lpart = mpart + parts;
+               float* out, float* lse, int32_t* status, cudaStream_t stream) {
     ECHO_CUDA_OK(prefer_max_shared(mla_split_kernel));
     ECHO_CUDA_OK(cudaFuncSetAttribute(mla_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(kSmem)));
+    int split_tokens = 0, splits = 0;
+    mla_plan(B, k, &split_tokens, &splits);
     const float scale_log2 = scale * 1.4426950408889634f;
-    mla_split_kernel<<<B * 2 * splits, kThreads, kSmem, stream>>>(k, q, sel_slot, static_cast<const uint8_t*>(dev_kv),
-                                                                  C, scale_log2, opart, mpart, lpart, splits, status);
-    ECHO_CUDA_OK(cudaGetLastError());
-    mla_combine_kernel<<<B * kHeads, 128, 0, stream>>>(splits, opart, mpart, lpart, out, lse);
-    ECHO_CUDA_OK(cudaGetLastError());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(B * 2 * splits));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, mla_split_kernel, k, split_tokens, q, sel_slot,
+                                    static_cast<const uint8_t*>(dev_kv), C, scale_log2, out, lse, status));
     return ECHO_OK;
 }
 
 }  // namespace echo
 
-extern "C" size_t echo_mla_workspace_size(int B, int k) {
-    if (B <= 0 || k <= 0) return 0;
-    return echo::mla_workspace_bytes(B, k);
-}
-
 extern "C" int echo_mla_decode(int B, int k, const uint16_t* q, const int32_t* sel_slot, const void* dev_kv, int64_t C,
-                               float scale, float* out, float* lse, void* ws, size_t ws_bytes, int32_t* status,
-                               echo_stream_t stream) {
+                               float scale, float* out, float* lse, int32_t* status, echo_stream_t stream) {
     using namespace echo;
     if (B <= 0 || k <= 0 || C <= 0) return ECHO_EINVAL;
-    if (B > ECHO_MAX_REQUESTS) return ECHO_EUNSUPPORTED;
-    if (!q || !sel_slot || !dev_kv || !out || !lse || !ws || !status) return ECHO_EINVAL;
-    if (!is_aligned(q, 16) || !is_aligned(dev_kv, 16) || !is_aligned(out, 16) || !is_aligned(ws, 16))
-        return ECHO_EINVAL;
-    if (ws_bytes < mla_workspace_bytes(B, k)) return ECHO_ECAPACITY;
-    return launch_mla(B, k, q, sel_slot, dev_kv, C, scale, out, lse, ws, status, static_cast<cudaStream_t>(stream));
+    if (B > ECHO_MAX_REQUESTS || k > ECHO_MLA_MAX_K) return ECHO_EUNSUPPORTED;
+    if (!q || !sel_slot || !dev_kv || !out || !lse || !status) return ECHO_EINVAL;
+    if (!is_aligned(q, 16) || !is_aligned(dev_kv, 16) || !is_aligned(out, 16)) return ECHO_EINVAL;
+    return launch_mla(B, k, q, sel_slot, dev_kv, C, scale, out, lse, status, static_cast<cudaStream_t>(stream));
 }

@@ -36,9 +36,8 @@ def _run(B, C, k, valid_frac, seed, scale=1.0 / math.sqrt(192.0), empty=()):
         sel[b, pos] = rng.choice(C, m, replace=False)
     out = torch.empty((B, L.MLA_HEADS, L.MLA_DV), dtype=torch.float32, device=dev)
     lse = torch.empty((B, L.MLA_HEADS), dtype=torch.float32, device=dev)
-    ws = torch.empty(L.mla_workspace_size(B, k), dtype=torch.uint8, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
-    L.mla_decode(q.to(dev), torch.from_numpy(sel).to(dev), kv.to(dev), C, scale, out, lse, ws, st)
+    L.mla_decode(q.to(dev), torch.from_numpy(sel).to(dev), kv.to(dev), C, scale, out, lse, st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     return q, kv, sel, out.cpu().numpy(), lse.cpu().numpy(), scale
@@ -75,6 +74,31 @@ def test_full_selection_batch(orc):
     B, C, k = 2, 4096, 2048        # the decode workload's k and slots
     r = _run(B, C, k, 1.0, 1)
     _check(*r, C, orc)
+
+
+def test_long_selection_wide_splits(orc):
+    # k = 3000: splits of at least 384 tokens (12 tiles), the last one ragged
+    B, C, k = 1, 4096, 3000
+    r = _run(B, C, k, 0.9, 4)
+    _check(*r, C, orc)
+
+
+def test_odd_split_count(orc):
+    # k = 700: a split count that does not divide the 128 heads evenly over the cluster
+    B, C, k = 2, 1024, 700
+    r = _run(B, C, k, 1.0, 5)
+    _check(*r, C, orc)
+
+
+def test_rejects_oversized_selection():
+    q = torch.zeros((1, L.MLA_HEADS, L.MLA_DQK), dtype=torch.bfloat16, device=dev)
+    kv = torch.zeros((64, L.MLA_DQK), dtype=torch.bfloat16, device=dev)
+    sel = torch.zeros((1, L.MLA_MAX_K + 1), dtype=torch.int32, device=dev)
+    out = torch.empty((1, L.MLA_HEADS, L.MLA_DV), dtype=torch.float32, device=dev)
+    lse = torch.empty((1, L.MLA_HEADS), dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    with pytest.raises(L.EchoError):
+        L.mla_decode(q, sel, kv, 64, 1.0, out, lse, st)
 
 
 def test_peaked_scores(orc):
