@@ -12,7 +12,10 @@ quantised query) and issues the calls of a step:
     echo_topk_select   -> exact top-k indices, k-th score, EMA threshold, and
     echo_cache_step    -> early set into the tables, free / allocate, slot of
                           every selection run on a side stream; the late-miss
-                          recall joins the step's stream after both.
+                          recall joins the step's stream after both;
+    echo_mla_decode    -> (attention=True) sparse MLA attention of each request
+                          group over its selected slots, as soon as the group's
+                          rows are in the cache.
 Every buffer keeps its address and size, so ``step`` can be captured into a
 CUDA graph and replayed; ``q_in``/``w_in`` are the inputs a graph reads.
 ``capture_host_step`` captures the step together with its host I/O (inputs
@@ -32,7 +35,8 @@ class DecodeLayer:
     def __init__(self, tok_off, k8: torch.Tensor, ks: torch.Tensor, k: int, C: int,
                  host_pool: torch.Tensor, alpha: float = 0.5, predictor: bool = True,
                  early_cap: int = -1, groups: int | None = None, first_share: float = 0.5,
-                 resolved: bool = True, hold_early: bool = False, device="cuda"):
+                 resolved: bool = True, hold_early: bool = False, attention: bool = False,
+                 mla_scale: float = 1.0 / math.sqrt(192.0), device="cuda"):
         tok_off = torch.as_tensor(tok_off, dtype=torch.int64)
         self.B = int(tok_off.numel() - 1)
         self.n_tokens = int(k8.shape[0])
@@ -79,6 +83,14 @@ class DecodeLayer:
         self.q_in = torch.zeros((self.B, L.HEADS, L.DIM), **f32)
         self.w_in = torch.zeros((self.B, L.HEADS), **f32)
         self.cache = L.LayerCache(self.B, self.n_tokens, self.C, host_pool, device=device)
+        # sparse MLA attention over the selected slots (the cache rows are its 576-dim KV rows)
+        self.attention, self.mla_scale = bool(attention), float(mla_scale)
+        if self.attention:
+            if self.cache.row_bytes != 2 * L.MLA_DQK:
+                raise ValueError("attention needs 576-dim bf16 cache rows")
+            self.mla_q = torch.zeros((self.B, L.MLA_HEADS, L.MLA_DQK), dtype=torch.bfloat16, device=device)
+            self.attn_out = torch.zeros((self.B, L.MLA_HEADS, L.MLA_DV), **f32)
+            self.attn_lse = torch.zeros((self.B, L.MLA_HEADS), **f32)
         self.views = [self.cache.view(b0, b1) for b0, b1 in self.groups]
         self.sides = [torch.cuda.Stream(device=device) for _ in self.groups]
         self.side = self.sides[0]
@@ -93,7 +105,8 @@ class DecodeLayer:
         self.status.zero_()
         self.stats.zero_()
 
-    def step(self, q: torch.Tensor | None = None, w: torch.Tensor | None = None, stream=None, out_host=None):
+    def step(self, q: torch.Tensor | None = None, w: torch.Tensor | None = None, stream=None, out_host=None,
+             mla_q: torch.Tensor | None = None):
         """Enqueue one decode step (q [B,64,128] f32, w [B,64] f32; defaults q_in / w_in; pinned
         host tensors are read by the quantiser directly).
 
@@ -102,8 +115,12 @@ class DecodeLayer:
         out_host: optional (slot [B,k] int32, kth [B] f32) CUDA tensors over pinned host
         memory (_lib.host_alias_tensor): each request group's slots and k-th scores are
         written there by a kernel as soon as its cache step is done, while the late misses
-        are still being recalled."""
+        are still being recalled.
+        mla_q: with attention=True, the step's MLA queries [B,128,576] bf16 (default
+        self.mla_q); attn_out / attn_lse receive the attention of every request."""
         q = self.q_in if q is None else q
+        if self.attention:
+            mla_q = self.mla_q if mla_q is None else mla_q
         w = self.w_in if w is None else w
         main = torch.cuda.current_stream() if stream is None else stream
         L.quantize_q(q, w, self.q8, self.qscale, self.wfold, self.status, hist=self.hist, stream=main)
@@ -117,6 +134,8 @@ class DecodeLayer:
             if out_host is not None:
                 with torch.cuda.stream(main):
                     self._write_out(out_host, 0, self.B)
+            if self.attention:
+                self._attend(mla_q, 0, self.B, main)
             return
         sms = torch.cuda.get_device_properties(main.device).multi_processor_count
         scored, gstream = None, []
@@ -165,10 +184,20 @@ class DecodeLayer:
             if out_host is not None:
                 with torch.cuda.stream(side):
                     self._write_out(out_host, b0, b1)
+            if self.attention:
+                # after the group's late recall (on `copy`) and its early rows (on its scoring stream)
+                if copy is not gstream[g]:
+                    copy.wait_stream(gstream[g])
+                self._attend(mla_q, b0, b1, copy)
         for gs in self.gstreams:
             main.wait_stream(gs)
         for side in self.sides:
             main.wait_stream(side)
+
+    def _attend(self, mla_q, b0, b1, stream):
+        C = self.C
+        L.mla_decode(mla_q[b0:b1], self.sel_slot[b0:b1], self.cache.dev_kv[b0 * C:b1 * C], C, self.mla_scale,
+                     self.attn_out[b0:b1], self.attn_lse[b0:b1], self.status, stream=stream)
 
     def _write_out(self, out_host, b0, b1):
         # elementwise kernels, not copy-engine transfers: their stores go straight to the
@@ -201,6 +230,7 @@ class DecodeLayer:
 
     def kernel_launches_per_step(self) -> int:
         # quantize, then per group: score (+ early fetch) + top-k + cache step + late recall
+        att = 1 if self.attention else 0
         if not self.predictor:
-            return 5
-        return 1 + 5 * len(self.groups)
+            return 5 + att
+        return 1 + (5 + att) * len(self.groups)

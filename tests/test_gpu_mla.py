@@ -106,3 +106,52 @@ def test_peaked_scores(orc):
     B, C, k = 1, 512, 256
     r = _run(B, C, k, 1.0, 2, scale=0.5)
     _check(*r, C, orc)
+
+
+@pytest.mark.parametrize("hold_early", [False, True])
+def test_attention_in_the_decode_graph(orc, hold_early):
+    # the decode step with attention=True, captured in one CUDA graph: each request group's
+    # attention runs over its selected slots once its rows are in the cache.  Expected values:
+    # the oracle's top-k on the step's fp32 scores, then the oracle attention over those
+    # tokens' rows of the host pool (slot placement does not enter)
+    from sparse_attention_kv_echo_gb300 import DecodeLayer
+    from sparse_attention_kv_echo_gb300 import workloads as wl
+    w = wl.scaled(wl.WORKLOADS["batch"], "attn", B=4, lengths=(3000, 5000, 700, 4096), k=512, C=1024)
+    off = wl.tok_offsets(w.lengths)
+    k8, ks = wl.make_keys(w, 0)
+    wt = wl.make_weights(w, 0)
+    host = wl.make_host_pool(w, 0, pin=True)
+    lay = DecodeLayer(off, k8.to(dev), ks.to(dev), w.k, w.C, host, attention=True, hold_early=hold_early,
+                      device=dev)
+    assert len(lay.groups) == 2
+    qs = wl.QueryStream(w, 0)
+    g = torch.Generator().manual_seed(9)
+    mq = [torch.randn((w.B, L.MLA_HEADS, L.MLA_DQK), generator=g).to(torch.bfloat16) for _ in range(3)]
+    qq = [qs.next() for _ in range(3)]
+    main = torch.cuda.Stream()
+    with torch.cuda.stream(main):
+        lay.w_in.copy_(wt.to(dev))
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=main):
+        lay.step(stream=main)
+    torch.cuda.synchronize()
+    lay.reset()
+    hb = _bits(host)
+    for t in range(3):
+        with torch.cuda.stream(main):
+            lay.q_in.copy_(qq[t].to(dev))
+            lay.mla_q.copy_(mq[t].to(dev))
+            graph.replay()
+        torch.cuda.synchronize()
+        assert int(lay.status.item()) == 0
+        scores = lay.scores.cpu().numpy()
+        out = lay.attn_out.cpu().numpy()
+        lse = lay.attn_lse.cpu().numpy()
+        qb = _bits(mq[t])
+        for b in range(w.B):
+            idx, _ = orc.topk(scores[off[b]:off[b + 1]], w.k)
+            assert np.array_equal(idx, lay.sel_idx[b].cpu().numpy())
+            ref, ref_lse, mass = orc.mla_decode(qb[b], hb[off[b]:off[b + 1]], idx, lay.mla_scale)
+            assert np.all(np.abs(out[b] - ref) <= 5e-3 * mass + 1e-5), (t, b)
+            assert np.all(np.abs(lse[b] - ref_lse) <= 3e-3 * np.maximum(1.0, np.abs(ref_lse)))
