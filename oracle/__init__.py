@@ -93,6 +93,10 @@ def lib():
             L.orc_prefill_rows.argtypes = [c_f32p, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
                                            ctypes.c_int, ctypes.c_float, c_i32p, c_f32p, c_u32p,
                                            c_u8p]
+            L.orc_append_tokens.restype = ctypes.c_int
+            L.orc_append_tokens.argtypes = [ctypes.c_int, c_i64p, c_i64p, c_f32p, ctypes.c_int, c_u8p,
+                                            ctypes.c_int64, c_u8p, c_f32p, c_u8p, ctypes.c_int, c_i32p, c_i32p,
+                                            c_u8p, c_i32p]
             L.orc_decode_step.restype = ctypes.c_int
             L.orc_decode_step.argtypes = [
                 ctypes.c_int, c_i64p, c_f32p, c_f32p, ctypes.c_int, ctypes.c_int, c_u8p, c_f32p,
@@ -254,6 +258,28 @@ def recall(host_rows, tok, slot, dev_rows):
     slot = _c(slot, np.int32)
     lib().orc_recall(_p(host_rows, ctypes.c_uint8), host_rows.shape[1], _p(tok, ctypes.c_int32),
                      _p(slot, ctypes.c_int32), tok.size, _p(dev_rows, ctypes.c_uint8))
+
+
+def append_tokens(tok_off, tok_end, k_new, kv_new, k8, ks, host_rows, C, tok2slot, slot2tok, dev_rows):
+    """One new token per request (survey NEXT-2 reading).  tok_off [B+1] int64 (regions),
+    tok_end [B] int64 (updated), k_new [B,D] f32, kv_new [B,row_bytes] u8; k8 [n,D] u8, ks [n]
+    f32, host_rows [n,row_bytes] u8, tok2slot [n] / slot2tok [B*C] int32, dev_rows
+    [B*C,row_bytes] u8 are updated in place.  -> full [B] int32 (1: region had no room)."""
+    tok_off = _c(tok_off, np.int64)
+    k_new = _c(k_new, np.float32)
+    kv_new = _c(kv_new, np.uint8)
+    for a, dt in ((tok_end, np.int64), (k8, np.uint8), (ks, np.float32), (host_rows, np.uint8),
+                  (tok2slot, np.int32), (slot2tok, np.int32), (dev_rows, np.uint8)):
+        assert a.dtype == dt and a.flags.c_contiguous
+    B, D = k_new.shape
+    full = np.zeros(B, np.int32)
+    rc = lib().orc_append_tokens(B, _p(tok_off, ctypes.c_int64), _p(tok_end, ctypes.c_int64),
+                                 _p(k_new, ctypes.c_float), D, _p(kv_new, ctypes.c_uint8), kv_new.shape[1],
+                                 _p(k8, ctypes.c_uint8), _p(ks, ctypes.c_float), _p(host_rows, ctypes.c_uint8),
+                                 int(C), _p(tok2slot, ctypes.c_int32), _p(slot2tok, ctypes.c_int32),
+                                 _p(dev_rows, ctypes.c_uint8), _p(full, ctypes.c_int32))
+    _check(rc, "append_tokens")
+    return full
 
 
 def prefill_rows(scores_rows, row0: int, k: int, theta: float):

@@ -434,6 +434,67 @@ void orc_recall(const uint8_t* host_rows, int64_t row_bytes, const int32_t* tok,
                     (size_t)row_bytes);
 }
 
+// ---- append: one new token per request (survey NEXT-2) ---------------------
+// EXPL section 2 ("One layer, one step"): the host holds every token, which is
+// why eviction needs no write-back; the pages give no append mechanics.
+// READING: request b's rows live in its region [tok_off[b], tok_off[b+1]) and
+// tok_end[b] is its current end.  For each request with pos = tok_end[b]:
+//   - no room (pos == tok_off[b+1]): nothing changes, full[b] = 1;
+//   - the indexer key [IDX, FP8 keys with one fp32 scale per token]:
+//     amax = max_d |k[d]|, ks = amax / 448 rounded in fp32, and
+//     k8[d] = E4M3 round-to-nearest-even (saturating) of k[d] / ks rounded in
+//     fp32 (both divisions in the precision the GPU takes them, since they
+//     decide integer codes); amax = 0 gives ks = 0 and all-zero codes;
+//   - the KV row goes to host row pos;
+//   - the lowest free slot of the request, if any, takes the token (tok2slot,
+//     slot2tok) and its device row gets the KV row; with none free the token
+//     is host-only and will be recalled when selected;
+//   - tok_end[b] = pos + 1.
+// A non-finite key component returns 3 with nothing changed.
+int orc_append_tokens(int B, const int64_t* tok_off, int64_t* tok_end, const float* k_new, int D,
+                      const uint8_t* kv_new, int64_t row_bytes, uint8_t* k8, float* ks, uint8_t* host_rows, int C,
+                      int32_t* tok2slot, int32_t* slot2tok, uint8_t* dev_rows, int32_t* full) {
+    if (B < 0 || D <= 0 || C < 0 || row_bytes <= 0) return ORC_EINVAL;
+    for (int b = 0; b < B; ++b) {
+        if (tok_off[b] < 0 || tok_off[b + 1] < tok_off[b]) return ORC_EINVAL;
+        if (tok_end[b] < tok_off[b] || tok_end[b] > tok_off[b + 1]) return ORC_EINVAL;
+        for (int d = 0; d < D; ++d)
+            if (!finite_f(k_new[(int64_t)b * D + d])) return ORC_ENAN;
+    }
+    for (int b = 0; b < B; ++b) {
+        full[b] = 0;
+        const int64_t pos = tok_end[b];
+        if (pos == tok_off[b + 1]) {
+            full[b] = 1;
+            continue;
+        }
+        const float* k = k_new + (int64_t)b * D;
+        float amax = 0.0f;
+        for (int d = 0; d < D; ++d) amax = std::max(amax, std::fabs(k[d]));
+        const float scale = amax / 448.0f;
+        ks[pos] = scale;
+        for (int d = 0; d < D; ++d) {
+            if (amax == 0.0f) {
+                k8[pos * D + d] = 0;
+            } else {
+                const float x = k[d] / scale;
+                k8[pos * D + d] = e4m3_round((double)x);
+            }
+        }
+        std::memcpy(host_rows + pos * row_bytes, kv_new + (int64_t)b * row_bytes, (size_t)row_bytes);
+        for (int slot = 0; slot < C; ++slot) {
+            if (slot2tok[(int64_t)b * C + slot] != -1) continue;
+            slot2tok[(int64_t)b * C + slot] = (int32_t)(pos - tok_off[b]);
+            tok2slot[pos] = slot;
+            std::memcpy(dev_rows + ((int64_t)b * C + slot) * row_bytes, kv_new + (int64_t)b * row_bytes,
+                        (size_t)row_bytes);
+            break;
+        }
+        tok_end[b] = pos + 1;
+    }
+    return ORC_OK;
+}
+
 // ---- sparse MLA decode attention over the selected slots ------------------
 // The consumer of the cache (survey NEXT-1; EXPL section 2 names the sparse
 // attention over the k selected tokens but gives no formula).  READING: MLA
