@@ -69,6 +69,7 @@ typedef struct CUstream_st* echo_stream_t; /* a cudaStream_t; NULL = legacy defa
 #define ECHO_ST_NAN 0x2         /* NaN/Inf in q or w, or a NaN score */
 #define ECHO_ST_NOSLOT 0x4      /* a miss found no free slot (cannot happen when k <= C) */
 #define ECHO_ST_BADDATA 0x8     /* tok_off/tables/selection/histogram inconsistent with the sizes given */
+#define ECHO_ST_FULL 0x10       /* echo_append_tokens: a request's region had no room (nothing written) */
 
 /* stats counters (uint32 each) */
 #define ECHO_STAT_TOPK_FALLBACK 0   /* top-k boundary bins too large for shared memory */
@@ -81,6 +82,16 @@ typedef struct CUstream_st* echo_stream_t; /* a cudaStream_t; NULL = legacy defa
 /* echo_cache_step flags */
 #define ECHO_CACHE_HOLD_EARLY 1     /* hold the unselected early tokens' slots until the misses are placed */
 
+/*
+ * Requests.  tok_off [B+1] (int64, device) gives request b its region of rows
+ * [tok_off[b], tok_off[b+1]) in every per-token array (keys, scales, scores,
+ * tok2slot, host pool).  tok_end [B] (int64, device, optional: NULL = every
+ * region full) gives the request's current end, tok_off[b] <= tok_end[b] <=
+ * tok_off[b+1]: a context that grows by echo_append_tokens inside its region.
+ * Tokens in [tok_end[b], tok_off[b+1]) are not part of the request; every call
+ * of one step must see the same tok_end.  Inconsistent bounds give an empty
+ * request and ECHO_ST_BADDATA.
+ */
 #define ECHO_HEADS 64           /* index heads */
 #define ECHO_DIM 128            /* index head dimension (bytes per E4M3 key row) */
 #define ECHO_MAX_REQUESTS 4096  /* requests per call */
@@ -173,7 +184,7 @@ int echo_quantize_q(int B, const float* q, const float* w, uint8_t* q8, float* q
  *   waits for an SM.
  */
 size_t echo_above_words(int B, int64_t n_tokens);
-int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens, const uint8_t* q8,
+int echo_index_scores(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens, const uint8_t* q8,
                       const float* wfold, const uint8_t* k8, const float* ks, float* scores,
                       const float* theta_hat, uint32_t* hist, uint32_t* above,
                       const echo_cache* cache, int ctas, int32_t* status, echo_stream_t stream);
@@ -197,7 +208,8 @@ int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens, const uin
  * freed may be handed to a miss, unless the cache step holds those slots
  * (ECHO_CACHE_HOLD_EARLY).
  */
-int echo_early_fetch(int B, const int64_t* tok_off, int64_t n_tokens, const uint32_t* above, int early_cap,
+int echo_early_fetch(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens, const uint32_t* above,
+                     int early_cap,
                      const echo_cache* cache, int32_t* status, echo_stream_t stream);
 
 /*
@@ -219,7 +231,8 @@ int echo_early_fetch(int B, const int64_t* tok_off, int64_t n_tokens, const uint
  * The kernel lets a programmatic dependent launch (echo_cache_step) start as
  * soon as it begins; it writes sel_idx, kth and theta_hat only.
  */
-int echo_topk_select(int B, const int64_t* tok_off, int64_t n_tokens, const float* scores, int k,
+int echo_topk_select(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens, const float* scores,
+                     int k,
                      const uint32_t* hist, float* theta_hat, float alpha, int32_t* sel_idx,
                      float* kth, int32_t* status, uint32_t* stats, echo_stream_t stream);
 
@@ -253,7 +266,8 @@ int echo_topk_select(int B, const int64_t* tok_off, int64_t n_tokens, const floa
  * this step writes; sel and above are read only after that kernel has
  * completed.
  */
-int echo_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
+int echo_cache_step(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens, const int32_t* sel,
+                    int m,
                     const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,
                     int32_t* status, uint32_t* stats, echo_stream_t stream, echo_stream_t copy_stream,
                     int flags);
@@ -274,11 +288,13 @@ int echo_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32
  * C <= 131072.  Together they give exactly the tables, slots, lists and rows
  * of echo_topk_select followed by echo_cache_step.
  */
-int echo_topk_select_cached(int B, const int64_t* tok_off, int64_t n_tokens, const float* scores, int k,
+int echo_topk_select_cached(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens,
+                            const float* scores, int k,
                             const uint32_t* hist, float* theta_hat, float alpha, int32_t* sel_idx, float* kth,
                             const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,
                             int32_t* status, uint32_t* stats, echo_stream_t stream);
-int echo_cache_step_resolved(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
+int echo_cache_step_resolved(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens,
+                             const int32_t* sel, int m,
                              const echo_cache* cache, int32_t* sel_slot, int32_t* status, uint32_t* stats,
                              echo_stream_t stream, echo_stream_t copy_stream, int flags);
 
@@ -383,6 +399,32 @@ int echo_prefill_block_static(int R, int64_t row0, int64_t n_keys, const float* 
 #define ECHO_MLA_MAX_K 8192
 int echo_mla_decode(int B, int k, const uint16_t* q, const int32_t* sel_slot, const void* dev_kv, int64_t C,
                     float scale, float* out, float* lse, int32_t* status, echo_stream_t stream);
+
+/*
+ * Append one new token to each request: the offload write path [EXPL section
+ * 2, "One layer, one step": the host holds every token, hence no write-back
+ * on eviction; the pages give no append mechanics -- reading below].
+ * For request b with pos = tok_end[b]:
+ *   pos == tok_off[b+1] (region full): nothing is written, ECHO_ST_FULL;
+ *   ks[pos] = amax / 448 (fp32), amax = max_d |k_new[b,d]|;
+ *   k8[pos,d] = E4M3 round-to-nearest-even, saturating, of k_new[b,d] / ks[pos]
+ *               (fp32 quotient); amax = 0 gives ks = 0 and zero codes;
+ *   host pool row pos = kv_new[b] (row_bytes, through cache->host_kv);
+ *   the request's lowest free slot s, if any, takes the token: freebits bit
+ *   cleared, tok2slot[pos] = s, slot2tok[b*C+s] = pos - tok_off[b], device
+ *   row b*C+s = kv_new[b]; with no free slot the token is host-only;
+ *   tok_end[b] = pos + 1.
+ * A non-finite key component sets ECHO_ST_NAN and leaves that request as it
+ * was.  Args: tok_off [B+1] / tok_end [B] int64 device (tok_end updated),
+ * k_new [B,128] f32 device, kv_new [B,row_bytes] device (16-byte aligned),
+ * k8 [n_tokens,128] u8 and ks [n_tokens] f32 device, cache as above.
+ * Enqueue between steps, on the step's stream (every call of the next step
+ * must see the new tok_end).  Errors: ECHO_EINVAL (sizes, NULL or misaligned
+ * pointers), ECHO_EUNSUPPORTED, cache errors as echo_cache_step.
+ */
+int echo_append_tokens(int B, const int64_t* tok_off, int64_t* tok_end, int64_t n_tokens, const float* k_new,
+                       const void* kv_new, uint8_t* k8, float* ks, const echo_cache* cache, int32_t* status,
+                       echo_stream_t stream);
 
 /* Device-accessible address of a pinned host buffer (for echo_cache.host_kv).
  * Returns ECHO_ECUDA when the pointer is not pinned/mapped host memory. */

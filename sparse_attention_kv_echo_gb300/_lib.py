@@ -17,7 +17,7 @@ from . import build as _build
 
 ECHO_OK, ECHO_EINVAL, ECHO_ECAPACITY, ECHO_EUNSUPPORTED, ECHO_ECUDA, ECHO_ETOOLARGE = 0, -1, -2, -3, -4, -5
 PREFILL_STATIC_SCRATCH_BYTES = 32 << 20
-ST_TIMEOUT, ST_NAN, ST_NOSLOT, ST_BADDATA = 0x1, 0x2, 0x4, 0x8
+ST_TIMEOUT, ST_NAN, ST_NOSLOT, ST_BADDATA, ST_FULL = 0x1, 0x2, 0x4, 0x8, 0x10
 STAT_TOPK_FALLBACK, STAT_BOUNDARY_MAX, STAT_EARLY, STAT_MISSES, STAT_EARLY_USED = 0, 1, 2, 3, 4
 STATS_N = 8
 HEADS, DIM, MAX_REQUESTS = 64, 128, 4096
@@ -25,7 +25,7 @@ CACHE_HOLD_EARLY = 1            # echo_cache_step flag
 TOPK_CACHED_MAX_SLOTS = 32768  # C limit of echo_topk_select_cached
 EARLY_FETCH_BLOCKS = 32      # CTAs of the early-fetch and late-recall kernels
 
-EXPORTS = ("echo_above_words", "echo_cache_step", "echo_cache_step_resolved", "echo_device_sm_count",
+EXPORTS = ("echo_above_words", "echo_append_tokens", "echo_cache_step", "echo_cache_step_resolved", "echo_device_sm_count",
            "echo_early_fetch", "echo_host_device_alias", "echo_index_scores", "echo_mla_decode", "echo_prefill_block",
            "echo_prefill_block_static", "echo_prefill_scores", "echo_prefill_workspace_size", "echo_quantize_q",
            "echo_topk_select", "echo_topk_select_cached")
@@ -72,22 +72,25 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         L.echo_above_words.restype = ctypes.c_size_t
         L.echo_above_words.argtypes = [i32, i64]
         L.echo_index_scores.restype = i32
-        L.echo_index_scores.argtypes = [i32, _vp, i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+        L.echo_index_scores.argtypes = [i32, _vp, _vp, i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                         ctypes.POINTER(EchoCacheStruct), i32, _vp, _vp]
         L.echo_early_fetch.restype = i32
-        L.echo_early_fetch.argtypes = [i32, _vp, i64, _vp, i32, ctypes.POINTER(EchoCacheStruct), _vp, _vp]
+        L.echo_early_fetch.argtypes = [i32, _vp, _vp, i64, _vp, i32, ctypes.POINTER(EchoCacheStruct), _vp, _vp]
         L.echo_topk_select.restype = i32
-        L.echo_topk_select.argtypes = [i32, _vp, i64, _vp, i32, _vp, _vp, f32, _vp, _vp, _vp, _vp, _vp]
+        L.echo_topk_select.argtypes = [i32, _vp, _vp, i64, _vp, i32, _vp, _vp, f32, _vp, _vp, _vp, _vp, _vp]
         L.echo_cache_step.restype = i32
-        L.echo_cache_step.argtypes = [i32, _vp, i64, _vp, i32, _vp, i32, ctypes.POINTER(EchoCacheStruct), _vp,
+        L.echo_cache_step.argtypes = [i32, _vp, _vp, i64, _vp, i32, _vp, i32, ctypes.POINTER(EchoCacheStruct), _vp,
                                       _vp, _vp, _vp, _vp, i32]
         L.echo_mla_decode.restype = i32
         L.echo_mla_decode.argtypes = [i32, i32, _vp, _vp, _vp, i64, f32, _vp, _vp, _vp, _vp]
+        L.echo_append_tokens.restype = i32
+        L.echo_append_tokens.argtypes = [i32, _vp, _vp, i64, _vp, _vp, _vp, _vp, ctypes.POINTER(EchoCacheStruct),
+                                         _vp, _vp]
         L.echo_topk_select_cached.restype = i32
-        L.echo_topk_select_cached.argtypes = [i32, _vp, i64, _vp, i32, _vp, _vp, f32, _vp, _vp, _vp, i32,
+        L.echo_topk_select_cached.argtypes = [i32, _vp, _vp, i64, _vp, i32, _vp, _vp, f32, _vp, _vp, _vp, i32,
                                               ctypes.POINTER(EchoCacheStruct), _vp, _vp, _vp, _vp]
         L.echo_cache_step_resolved.restype = i32
-        L.echo_cache_step_resolved.argtypes = [i32, _vp, i64, _vp, i32, ctypes.POINTER(EchoCacheStruct), _vp, _vp,
+        L.echo_cache_step_resolved.argtypes = [i32, _vp, _vp, i64, _vp, i32, ctypes.POINTER(EchoCacheStruct), _vp, _vp,
                                                _vp, _vp, _vp, i32]
         L.echo_prefill_scores.restype = i32
         L.echo_prefill_scores.argtypes = [i32, i64, i64, _vp, _vp, _vp, _vp, _vp, i64, _vp, _vp, _vp, _vp]
@@ -174,34 +177,34 @@ def above_words(B: int, n_tokens: int) -> int:
 
 
 def index_scores(tok_off, n_tokens, q8, wfold, k8, ks, scores, theta_hat, hist, status, above=None,
-                 cache=None, stream=None, ctas=0):
+                 cache=None, stream=None, ctas=0, tok_end=None):
     """echo_index_scores; cache: a LayerCache whose residents `above` leaves out (and whose free bits
-    are snapshotted for early_fetch)."""
+    are snapshotted for early_fetch); tok_end: the requests' current ends (None: full regions)."""
     B = q8.shape[0]
     _check("echo_index_scores", load().echo_index_scores(
-        B, _ptr(tok_off), int(n_tokens), _ptr(q8), _ptr(wfold), _ptr(k8), _ptr(ks), _ptr(scores),
+        B, _ptr(tok_off), _ptr(tok_end), int(n_tokens), _ptr(q8), _ptr(wfold), _ptr(k8), _ptr(ks), _ptr(scores),
         _ptr(theta_hat), _ptr(hist), _ptr(above), ctypes.byref(cache.struct) if cache is not None else None,
         int(ctas), _ptr(status), _stream(stream)))
 
 
-def early_fetch(tok_off, n_tokens, above, early_cap, cache, status, stream=None):
+def early_fetch(tok_off, n_tokens, above, early_cap, cache, status, stream=None, tok_end=None):
     """echo_early_fetch: copy the rows of the early set (the tables learn it in cache_step)."""
     B = tok_off.shape[0] - 1
     _check("echo_early_fetch", load().echo_early_fetch(
-        B, _ptr(tok_off), int(n_tokens), _ptr(above), int(early_cap), ctypes.byref(cache.struct), _ptr(status),
+        B, _ptr(tok_off), _ptr(tok_end), int(n_tokens), _ptr(above), int(early_cap), ctypes.byref(cache.struct), _ptr(status),
         _stream(stream)))
 
 
 def topk_select(tok_off, n_tokens, scores, k, hist, theta_hat, alpha, sel_idx, kth, status, stats=None,
-                stream=None):
+                stream=None, tok_end=None):
     B = tok_off.shape[0] - 1
     _check("echo_topk_select", load().echo_topk_select(
-        B, _ptr(tok_off), int(n_tokens), _ptr(scores), int(k), _ptr(hist), _ptr(theta_hat), float(alpha),
+        B, _ptr(tok_off), _ptr(tok_end), int(n_tokens), _ptr(scores), int(k), _ptr(hist), _ptr(theta_hat), float(alpha),
         _ptr(sel_idx), _ptr(kth), _ptr(status), _ptr(stats), _stream(stream)))
 
 
 def cache_step(tok_off, n_tokens, sel, cache, sel_slot, status, stats=None, stream=None, copy_stream=None,
-               above=None, early_cap=-1, hold_early=False):
+               above=None, early_cap=-1, hold_early=False, tok_end=None):
     """echo_cache_step; above/early_cap: the early set of this step (as given to early_fetch);
     hold_early: ECHO_CACHE_HOLD_EARLY."""
     B = tok_off.shape[0] - 1
@@ -209,32 +212,42 @@ def cache_step(tok_off, n_tokens, sel, cache, sel_slot, status, stats=None, stre
     st = _stream(stream)
     cst = _stream(copy_stream) if copy_stream is not None else st
     _check("echo_cache_step", load().echo_cache_step(
-        B, _ptr(tok_off), int(n_tokens), _ptr(sel), int(m), _ptr(above), int(early_cap),
+        B, _ptr(tok_off), _ptr(tok_end), int(n_tokens), _ptr(sel), int(m), _ptr(above), int(early_cap),
         ctypes.byref(cache.struct), _ptr(sel_slot), _ptr(status), _ptr(stats), st, cst,
         CACHE_HOLD_EARLY if hold_early else 0))
 
 
 def topk_select_cached(tok_off, n_tokens, scores, k, hist, theta_hat, alpha, sel_idx, kth, cache, sel_slot,
-                       status, stats=None, stream=None, above=None, early_cap=-1):
+                       status, stats=None, stream=None, above=None, early_cap=-1, tok_end=None):
     """echo_topk_select_cached: top-k plus each selected token's slot at the cache step's start
     (resident or early; -1: a miss); finish with cache_step_resolved."""
     B = tok_off.shape[0] - 1
     _check("echo_topk_select_cached", load().echo_topk_select_cached(
-        B, _ptr(tok_off), int(n_tokens), _ptr(scores), int(k), _ptr(hist), _ptr(theta_hat), float(alpha),
+        B, _ptr(tok_off), _ptr(tok_end), int(n_tokens), _ptr(scores), int(k), _ptr(hist), _ptr(theta_hat), float(alpha),
         _ptr(sel_idx), _ptr(kth), _ptr(above), int(early_cap), ctypes.byref(cache.struct), _ptr(sel_slot),
         _ptr(status), _ptr(stats), _stream(stream)))
 
 
 def cache_step_resolved(tok_off, n_tokens, sel, cache, sel_slot, status, stats=None, stream=None, copy_stream=None,
-                        hold_early=False):
+                        hold_early=False, tok_end=None):
     """echo_cache_step_resolved: the cache step after topk_select_cached (sel_slot in/out)."""
     B = tok_off.shape[0] - 1
     m = sel.shape[-1]
     st = _stream(stream)
     cst = _stream(copy_stream) if copy_stream is not None else st
     _check("echo_cache_step_resolved", load().echo_cache_step_resolved(
-        B, _ptr(tok_off), int(n_tokens), _ptr(sel), int(m), ctypes.byref(cache.struct), _ptr(sel_slot),
+        B, _ptr(tok_off), _ptr(tok_end), int(n_tokens), _ptr(sel), int(m), ctypes.byref(cache.struct), _ptr(sel_slot),
         _ptr(status), _ptr(stats), st, cst, CACHE_HOLD_EARLY if hold_early else 0))
+
+
+def append_tokens(tok_off, tok_end, n_tokens, k_new, kv_new, k8, ks, cache, status, stream=None):
+    """echo_append_tokens: one new token per request (k_new [B,128] f32, kv_new [B,576] bf16, device)
+    into its region at tok_end[b] (updated): E4M3 key + scale, host-pool row, and the lowest free
+    cache slot when one is free."""
+    B = tok_off.shape[0] - 1
+    _check("echo_append_tokens", load().echo_append_tokens(
+        B, _ptr(tok_off), _ptr(tok_end), int(n_tokens), _ptr(k_new), _ptr(kv_new), _ptr(k8), _ptr(ks),
+        ctypes.byref(cache.struct), _ptr(status), _stream(stream)))
 
 
 MLA_HEADS, MLA_DQK, MLA_DV, MLA_MAX_K = 128, 576, 512, 8192

@@ -37,17 +37,13 @@ constexpr int kLT = 1024;  // threads of the look-up cache step (at ~64 register
                            // register file: no copy block, whose loads wait on the host link, shares it)
 
 
-__device__ __forceinline__ bool request_range(const int64_t* tok_off, int64_t n_tokens, int b, int64_t* base,
-                                              int64_t* n) {
-    const int64_t lo = tok_off[b], hi = tok_off[b + 1];
-    if (lo < 0 || hi < lo || hi > n_tokens) {
-        *base = 0;
-        *n = 0;
-        return false;
-    }
+__device__ __forceinline__ bool request_range(const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens, int b,
+                                              int64_t* base, int64_t* n) {
+    int64_t lo, hi;
+    const bool ok = seg_bounds(tok_off, tok_end, n_tokens, b, &lo, &hi);
     *base = lo;
     *n = hi - lo;
-    return true;
+    return ok;
 }
 
 constexpr int kPer = 4;        // selection entries per thread per chunk
@@ -88,7 +84,7 @@ constexpr int kLookupMaxSlots = 1 << 17;   // 4 x 4096 words + the chunk fit sha
 
 template <bool kResolved>
 __global__ void __launch_bounds__(kLT)
-    cache_step_lookup_kernel(const int64_t* __restrict__ tok_off, int64_t n_tokens, const int32_t* __restrict__ sel,
+    cache_step_lookup_kernel(const int64_t* __restrict__ tok_off, const int64_t* __restrict__ tok_end, int64_t n_tokens, const int32_t* __restrict__ sel,
                              int m, const uint32_t* __restrict__ above, int early_cap, CacheArgs c,
                              int32_t* sel_slot, int32_t* status, uint32_t* stats, bool hold_early) {
     pdl_launch_dependents();  // the late recall's blocks may be scheduled now; they wait for this kernel
@@ -96,7 +92,7 @@ __global__ void __launch_bounds__(kLT)
     __shared__ uint32_t scan[40];
     __shared__ uint32_t flags[2];
     CacheStepLookup<kLT, kAWC, kResolved> cs;
-    cs.init(tok_off, n_tokens, blockIdx.x, sel, m, sel_slot, above, early_cap, c, status, stats, smem, scan, flags,
+    cs.init(tok_off, tok_end, n_tokens, blockIdx.x, sel, m, sel_slot, above, early_cap, c, status, stats, smem, scan, flags,
             hold_early);
     cs.prologue_issue();  // the tables only: they may be read before the kernel before this one ends
     cs.prologue_finish();
@@ -108,7 +104,8 @@ __global__ void __launch_bounds__(kLT)
     cs.finish();
 }
 
-__global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restrict__ tok_off, int64_t n_tokens,
+__global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restrict__ tok_off,
+                                                         const int64_t* __restrict__ tok_end, int64_t n_tokens,
                                                          const int32_t* __restrict__ sel, int m,
                                                          const uint32_t* __restrict__ above, int early_cap,
                                                          CacheArgs c, int32_t* __restrict__ sel_slot, int32_t* status,
@@ -122,7 +119,7 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
     pdl_launch_dependents();  // the late recall's blocks may be scheduled now; they wait for this kernel
     pdl_wait();  // launched as a programmatic dependent: everything below may depend on the kernel before
     int64_t base, n;
-    if (!request_range(tok_off, n_tokens, b, &base, &n) && tid == 0) set_status(status, ECHO_ST_BADDATA);
+    if (!request_range(tok_off, tok_end, n_tokens, b, &base, &n) && tid == 0) set_status(status, ECHO_ST_BADDATA);
     const int C = c.C, words = C / 32;
     int32_t* t2s = c.tok2slot + base;
     int32_t* s2t = c.slot2tok + static_cast<int64_t>(b) * C;
@@ -385,7 +382,8 @@ __device__ __forceinline__ void copy_rows(const int4* const (&src)[kRows], int4*
 // Rows of all requests form one list (request b's rows at pre[b] .. pre[b+1]);
 // warp w of the grid copies rows w*2, w*2+1, then strides by the grid's warps.
 __global__ void __launch_bounds__(kRecallThreads)
-    recall_kernel(int B, const int64_t* __restrict__ tok_off, int64_t n_tokens, int C,
+    recall_kernel(int B, const int64_t* __restrict__ tok_off, const int64_t* __restrict__ tok_end, int64_t n_tokens,
+                  int C,
                   const int32_t* __restrict__ tok_list, const int32_t* __restrict__ slot_list,
                   const int32_t* __restrict__ cnt, const uint8_t* host, uint8_t* __restrict__ dev, int64_t row_bytes,
                   int32_t* status) {
@@ -429,7 +427,7 @@ __global__ void __launch_bounds__(kRecallThreads)
                 }
                 const int b = lo;
                 int64_t base, n;
-                const bool range_ok = request_range(tok_off, n_tokens, b, &base, &n);
+                const bool range_ok = request_range(tok_off, tok_end, n_tokens, b, &base, &n);
                 const int64_t e = static_cast<int64_t>(b) * C + (i - pre[b]);
                 const int32_t tok = tok_list[e];
                 const int32_t slot = slot_list[e];
@@ -452,7 +450,7 @@ __global__ void __launch_bounds__(kRecallThreads)
 // are not touched), stages (token, slot) pairs in shared memory, and copies
 // the staged rows whose index is g (mod G), g its place in the request's group.
 __global__ void __launch_bounds__(kRecallThreads)
-    early_fetch_kernel(int B, const int64_t* __restrict__ tok_off, int64_t n_tokens,
+    early_fetch_kernel(int B, const int64_t* __restrict__ tok_off, const int64_t* __restrict__ tok_end, int64_t n_tokens,
                        const uint32_t* __restrict__ above, int cap, const uint32_t* __restrict__ snap, int C,
                        int32_t* __restrict__ early_tok, int32_t* __restrict__ early_slot, const uint8_t* host,
                        uint8_t* __restrict__ dev, int64_t row_bytes, int32_t* status) {
@@ -473,10 +471,10 @@ __global__ void __launch_bounds__(kRecallThreads)
     // before waiting for it
     int b = static_cast<int>(blockIdx.x) / G;
     int64_t base = 0, n = 0;
-    bool range_ok = b < B && request_range(tok_off, n_tokens, b, &base, &n);
+    bool range_ok = b < B && request_range(tok_off, tok_end, n_tokens, b, &base, &n);
     pdl_wait();  // the above-threshold words and the snapshot come from the score kernel
     for (; b < B && static_cast<int>(blockIdx.x) < groups * G; b += groups) {
-        if (b != static_cast<int>(blockIdx.x) / G) range_ok = request_range(tok_off, n_tokens, b, &base, &n);
+        if (b != static_cast<int>(blockIdx.x) / G) range_ok = request_range(tok_off, tok_end, n_tokens, b, &base, &n);
         if (!range_ok) {
             if (threadIdx.x == 0) set_status(status, ECHO_ST_BADDATA);
             continue;
@@ -541,7 +539,7 @@ __global__ void __launch_bounds__(kRecallThreads)
 
 }  // namespace
 
-cudaError_t launch_recall(int B, const int64_t* tok_off, int64_t n_tokens, int C, const int32_t* tok_list,
+cudaError_t launch_recall(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens, int C, const int32_t* tok_list,
                           const int32_t* slot_list, const int32_t* cnt, const void* host_kv, void* dev_kv,
                           int64_t row_bytes, int32_t* status, cudaStream_t s, bool programmatic) {
     const int sms = sm_count();
@@ -570,7 +568,7 @@ cudaError_t launch_recall(int B, const int64_t* tok_off, int64_t n_tokens, int C
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = programmatic ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, recall_kernel, B, tok_off, n_tokens, C, tok_list, slot_list, cnt,
+    return cudaLaunchKernelEx(&cfg, recall_kernel, B, tok_off, tok_end, n_tokens, C, tok_list, slot_list, cnt,
                               static_cast<const uint8_t*>(host_kv), static_cast<uint8_t*>(dev_kv), row_bytes,
                               status);
 }
@@ -579,7 +577,8 @@ cudaError_t launch_recall(int B, const int64_t* tok_off, int64_t n_tokens, int C
 
 namespace echo {
 
-int enqueue_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
+int enqueue_cache_step(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens, const int32_t* sel,
+                       int m,
                        const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,
                        int32_t* status, uint32_t* stats, cudaStream_t stream, cudaStream_t copy_stream,
                        bool resolved, bool hold_early) {
@@ -613,15 +612,15 @@ int enqueue_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const in
     cfg.numAttrs = 1;
     const CacheArgs ca = cache_args(*cache);
     if (lookup) {
-        ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, lookup_kernel, tok_off, n_tokens, sel, m, resolved ? nullptr : above,
+        ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, lookup_kernel, tok_off, tok_end, n_tokens, sel, m, resolved ? nullptr : above,
                                         early_cap, ca, sel_slot, status, stats, hold_early));
     } else {
-        ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, cache_step_kernel, tok_off, n_tokens, sel, m, above, early_cap, ca,
+        ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, cache_step_kernel, tok_off, tok_end, n_tokens, sel, m, above, early_cap, ca,
                                         sel_slot, status, stats, hold_early));
     }
     const int rc = stream_wait(copy_stream, stream);
     if (rc) return rc;
-    ECHO_CUDA_OK(launch_recall(B, tok_off, n_tokens, cache->C, cache->miss_tok, cache->miss_slot, cache->miss_cnt,
+    ECHO_CUDA_OK(launch_recall(B, tok_off, tok_end, n_tokens, cache->C, cache->miss_tok, cache->miss_slot, cache->miss_cnt,
                                cache->host_kv, cache->dev_kv, cache->row_bytes, status, copy_stream,
                                copy_stream == stream));
     return ECHO_OK;
@@ -641,7 +640,8 @@ int check_cache_step_args(int B, int64_t n_tokens, const int32_t* sel, int m, co
 
 }  // namespace echo
 
-extern "C" int echo_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
+extern "C" int echo_cache_step(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens,
+                               const int32_t* sel, int m,
                                const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,
                                int32_t* status, uint32_t* stats, echo_stream_t stream, echo_stream_t copy_stream,
                                int flags) {
@@ -649,11 +649,12 @@ extern "C" int echo_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, 
     if (!tok_off || !status || (flags & ~ECHO_CACHE_HOLD_EARLY)) return ECHO_EINVAL;
     const int rc = check_cache_step_args(B, n_tokens, sel, m, cache, sel_slot);
     if (rc) return rc;
-    return enqueue_cache_step(B, tok_off, n_tokens, sel, m, above, early_cap, cache, sel_slot, status, stats, stream,
+    return enqueue_cache_step(B, tok_off, tok_end, n_tokens, sel, m, above, early_cap, cache, sel_slot, status, stats, stream,
                               copy_stream, false, (flags & ECHO_CACHE_HOLD_EARLY) != 0);
 }
 
-extern "C" int echo_cache_step_resolved(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
+extern "C" int echo_cache_step_resolved(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens,
+                                        const int32_t* sel, int m,
                                         const echo_cache* cache, int32_t* sel_slot, int32_t* status, uint32_t* stats,
                                         echo_stream_t stream, echo_stream_t copy_stream, int flags) {
     using namespace echo;
@@ -661,11 +662,12 @@ extern "C" int echo_cache_step_resolved(int B, const int64_t* tok_off, int64_t n
     const int rc = check_cache_step_args(B, n_tokens, sel, m, cache, sel_slot);
     if (rc) return rc;
     if (cache->C > kLookupMaxSlots) return ECHO_EUNSUPPORTED;
-    return enqueue_cache_step(B, tok_off, n_tokens, sel, m, nullptr, 0, cache, sel_slot, status, stats, stream,
+    return enqueue_cache_step(B, tok_off, tok_end, n_tokens, sel, m, nullptr, 0, cache, sel_slot, status, stats, stream,
                               copy_stream, true, (flags & ECHO_CACHE_HOLD_EARLY) != 0);
 }
 
-extern "C" int echo_early_fetch(int B, const int64_t* tok_off, int64_t n_tokens, const uint32_t* above,
+extern "C" int echo_early_fetch(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens,
+                                const uint32_t* above,
                                 int early_cap, const echo_cache* cache, int32_t* status, echo_stream_t stream) {
     using namespace echo;
     if (B <= 0 || n_tokens < 0) return ECHO_EINVAL;
@@ -697,7 +699,7 @@ extern "C" int echo_early_fetch(int B, const int64_t* tok_off, int64_t n_tokens,
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, early_fetch_kernel, B, tok_off, n_tokens, above, early_cap,
+    ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, early_fetch_kernel, B, tok_off, tok_end, n_tokens, above, early_cap,
                                     static_cast<const uint32_t*>(cache->free_snap), static_cast<int>(cache->C),
                                     cache->early_tok, cache->early_slot,
                                     static_cast<const uint8_t*>(cache->host_kv), static_cast<uint8_t*>(cache->dev_kv),

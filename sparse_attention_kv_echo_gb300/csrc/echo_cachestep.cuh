@@ -76,7 +76,7 @@ struct CacheStepLookup {
     uint32_t limit, A, F0;
 
     // smem: cache_lookup_smem_words(C, AWC) words; scan: 40 words; flags: 2 words.
-    __device__ void init(const int64_t* tok_off, int64_t n_tokens, int b_, const int32_t* sel, int m_,
+    __device__ void init(const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens, int b_, const int32_t* sel, int m_,
                          int32_t* sel_slot, const uint32_t* above, int cap, const CacheArgs& args, int32_t* st,
                          uint32_t* sts, uint32_t* smem, uint32_t* scan_, uint32_t* flags,
                          bool hold_early) {
@@ -86,10 +86,10 @@ struct CacheStepLookup {
         status = st;
         stats = sts;
         early_cap = cap;
-        const int64_t lo = tok_off[b], hi = tok_off[b + 1];
-        range_ok = !(lo < 0 || hi < lo || hi > n_tokens);
-        base = range_ok ? lo : 0;
-        n = range_ok ? hi - lo : 0;
+        int64_t lo, hi;
+        range_ok = seg_bounds(tok_off, tok_end, n_tokens, b, &lo, &hi);
+        base = lo;
+        n = hi - lo;
         words = c.C / 32;
         t2s = c.tok2slot + base;
         s2t = c.slot2tok + static_cast<int64_t>(b) * c.C;

@@ -26,6 +26,24 @@ __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Request b's tokens [lo, hi): rows lo.. of every per-token array.  The
+// request's region is [tok_off[b], tok_off[b+1]); tok_end (optional) holds its
+// current end (a context that grows inside its region), else the region is
+// full.  False, with an empty range at 0, when inconsistent with n_tokens.
+__device__ __forceinline__ bool seg_bounds(const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens, int b,
+                                           int64_t* lo, int64_t* hi) {
+    const int64_t l = tok_off[b], r = tok_off[b + 1];
+    const int64_t h = tok_end ? tok_end[b] : r;
+    if (l < 0 || r < l || r > n_tokens || h < l || h > r) {
+        *lo = 0;
+        *hi = 0;
+        return false;
+    }
+    *lo = l;
+    *hi = h;
+    return true;
+}
+
 __device__ __forceinline__ void set_status(int32_t* status, int bits) {
     if (status) atomicOr(reinterpret_cast<int*>(status), bits);
 }

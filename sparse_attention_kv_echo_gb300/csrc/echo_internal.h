@@ -36,7 +36,7 @@ int check_cache(const echo_cache* c, int B, int m);
 // Launchers shared across translation units.
 cudaError_t launch_quantize(int B, const float* q, const float* w, uint8_t* q8, float* qscale, float* wfold,
                             uint32_t* hist_to_zero, int32_t* status, cudaStream_t s);
-cudaError_t launch_recall(int B, const int64_t* tok_off, int64_t n_tokens, int C, const int32_t* tok_list,
+cudaError_t launch_recall(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens, int C, const int32_t* tok_list,
                           const int32_t* slot_list, const int32_t* cnt, const void* host_kv, void* dev_kv,
                           int64_t row_bytes, int32_t* status, cudaStream_t s, bool programmatic);
 
@@ -53,12 +53,13 @@ cudaError_t prefer_max_shared(Kernel kernel) {
 constexpr int kMaxSlots = 1 << 19;   // slots per request: per-slot-word tables fit shared memory
 
 // Enqueue helpers shared by the decode calls and the prefill block call.
-int launch_topk(int B, const int64_t* tok_off, int64_t n_tokens, int64_t row0, int64_t W, const float* scores, int k,
+int launch_topk(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens, int64_t row0, int64_t W, const float* scores, int k,
                 const uint32_t* hist, float* theta_hat, float alpha, int32_t* sel_idx, float* kth, int32_t* status,
                 uint32_t* stats, cudaStream_t stream);
 int check_cache_step_args(int B, int64_t n_tokens, const int32_t* sel, int m, const echo_cache* cache,
                           const int32_t* sel_slot);
-int enqueue_cache_step(int B, const int64_t* tok_off, int64_t n_tokens, const int32_t* sel, int m,
+int enqueue_cache_step(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens, const int32_t* sel,
+                       int m,
                        const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,
                        int32_t* status, uint32_t* stats, cudaStream_t stream, cudaStream_t copy_stream,
                        bool resolved, bool hold_early);

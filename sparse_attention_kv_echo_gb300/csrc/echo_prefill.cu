@@ -144,7 +144,7 @@ extern "C" int echo_prefill_block(int R, int64_t row0, int64_t n_keys, const flo
     if (launch_quantize(R, q, w, p.q8, p.qscale, p.wfold, hist, status, stream) != cudaSuccess) return ECHO_ECUDA;
     int rc = echo_prefill_scores(R, row0, n_keys, p.q8, p.wfold, k8, ks, scores, W, theta_hat, hist, status, stream);
     if (rc) return rc;
-    rc = launch_topk(R, nullptr, 0, row0, W, scores, k, hist, theta_hat, alpha, sel_idx, kth, status, stats, stream);
+    rc = launch_topk(R, nullptr, nullptr, 0, row0, W, scores, k, hist, theta_hat, alpha, sel_idx, kth, status, stats, stream);
     if (rc) return rc;
     const int64_t n = row0 + R;
     ECHO_CUDA_OK(cudaMemsetAsync(p.mark, 0, static_cast<size_t>(n), stream));
@@ -164,7 +164,7 @@ extern "C" int echo_prefill_block(int R, int64_t row0, int64_t n_keys, const flo
     // the previous block's recall reads the miss lists this step rewrites
     rc = stream_wait(stream, copy_stream);
     if (rc) return rc;
-    return enqueue_cache_step(1, p.tok_off2, n_keys, union_list, static_cast<int>(W), nullptr, 0, cache, sel_slot,
+    return enqueue_cache_step(1, p.tok_off2, nullptr, n_keys, union_list, static_cast<int>(W), nullptr, 0, cache, sel_slot,
                               status, stats, stream, copy_stream, false, false);
 }
 

@@ -46,12 +46,13 @@ constexpr int kSidePitch = 160;                        // 640-byte smem rows (12
 constexpr uint32_t kSideBytes = kSideBox * 4;
 constexpr uint32_t kIdesc = idesc_e4m3_f32(kTileM, ECHO_HEADS);
 
-// Segments: decode requests (CSR tok_off: keys and scores at rows
-// [tok_off[b], tok_off[b+1])) or prefill rows (W > 0: row b at position
+// Segments: decode requests (keys and scores at rows [tok_off[b], end) with
+// end = tok_end[b] when given, else tok_off[b+1]) or prefill rows (W > 0: row b at position
 // row0 + b sees keys [0, row0 + b] and writes its scores at b * W).
 struct ScoreArgs {
     int B;
     const int64_t* tok_off;
+    const int64_t* tok_end;    // optional current ends (growing contexts)
     int64_t n_tokens;
     int64_t row0;
     int64_t W;
@@ -121,8 +122,8 @@ __device__ __forceinline__ Seg segment(const ScoreArgs& a, int b, bool* bad) {
         }
         return Seg{0, len, static_cast<int64_t>(b) * a.W};
     }
-    const int64_t lo = a.tok_off[b], hi = a.tok_off[b + 1];
-    if (lo < 0 || hi < lo || hi > a.n_tokens) {
+    int64_t lo, hi;
+    if (!seg_bounds(a.tok_off, a.tok_end, a.n_tokens, b, &lo, &hi)) {
         *bad = true;
         return Seg{0, 0, 0};
     }
@@ -535,7 +536,8 @@ static int launch_scores(const ScoreArgs& args, const uint8_t* q8, const uint8_t
 
 }  // namespace echo
 
-extern "C" int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens, const uint8_t* q8,
+extern "C" int echo_index_scores(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens,
+                                 const uint8_t* q8,
                                  const float* wfold, const uint8_t* k8, const float* ks, float* scores,
                                  const float* theta_hat, uint32_t* hist, uint32_t* above, const echo_cache* cache,
                                  int ctas, int32_t* status, echo_stream_t stream) {
@@ -554,7 +556,7 @@ extern "C" int echo_index_scores(int B, const int64_t* tok_off, int64_t n_tokens
         if (!cache->free_snap || !is_aligned(cache->tok2slot, 16)) return ECHO_EINVAL;
     }
     if (n_tokens == 0) return ECHO_OK;
-    ScoreArgs args{B, tok_off, n_tokens, 0, 0, 1, wfold, scores, theta_hat, hist, above,
+    ScoreArgs args{B, tok_off, tok_end, n_tokens, 0, 0, 1, wfold, scores, theta_hat, hist, above,
                    cache ? 1 : 0, status, cache ? cache->freebits : nullptr,
                    cache ? cache->free_snap : nullptr,
                    cache ? static_cast<int64_t>(B) * (cache->C / 32) : 0};
@@ -573,7 +575,7 @@ extern "C" int echo_prefill_scores(int R, int64_t row0, int64_t n_keys, const ui
     if (n_keys >= (1ll << 31) || static_cast<int64_t>(R) * W >= (1ll << 40)) return ECHO_EUNSUPPORTED;
     if (!is_aligned(q8, 16) || !is_aligned(wfold, 16) || !is_aligned(k8, 16) || !is_aligned(ks, 16))
         return ECHO_EINVAL;
-    ScoreArgs args{R, nullptr, n_keys, row0, W, 0, wfold, scores, theta_hat, hist, nullptr, 0, status, nullptr,
+    ScoreArgs args{R, nullptr, nullptr, n_keys, row0, W, 0, wfold, scores, theta_hat, hist, nullptr, 0, status, nullptr,
                    nullptr, 0};
     const int64_t tiles_ub = static_cast<int64_t>(R) * ((row0 + R + kTileM - 1) / kTileM);
     return launch_scores(args, q8, k8, ks, nullptr, n_keys, tiles_ub, 0, stream);

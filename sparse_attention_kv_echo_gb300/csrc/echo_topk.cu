@@ -272,6 +272,7 @@ __device__ __forceinline__ bool takes(float x, float shift, uint32_t bstar, uint
 // threshold is one scalar for every row and is not updated here.
 struct TopkSegs {
     const int64_t* tok_off;
+    const int64_t* tok_end;  // optional current ends (growing contexts)
     int64_t n_tokens;
     int64_t row0;
     int64_t W;
@@ -522,13 +523,10 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTT, 1)
             n = 0;
         }
     } else {
-        lo = segs.tok_off[b];
-        const int64_t hi = segs.tok_off[b + 1];
+        int64_t hi;
+        if (!seg_bounds(segs.tok_off, segs.tok_end, segs.n_tokens, b, &lo, &hi) && leader && tid == 0)
+            set_status(status, ECHO_ST_BADDATA);
         n = hi - lo;
-        if (lo < 0 || hi < lo || hi > segs.n_tokens) {
-            if (leader && tid == 0) set_status(status, ECHO_ST_BADDATA);
-            n = 0;
-        }
     }
     const float* sc = scores + (n > 0 ? lo : 0);
     int32_t* out = sel + static_cast<int64_t>(b) * k;
@@ -660,11 +658,12 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTT, 1)
     const bool leader = rank == 0;
     TopkShared& lsh = *cluster.map_shared_rank(&sh, 0);
     const int b = blockIdx.x / kCS, tid = threadIdx.x;
-    int64_t lo = segs.tok_off[b], n = segs.tok_off[b + 1] - lo;
-    if (lo < 0 || n < 0 || lo + n > segs.n_tokens) {
-        if (leader && tid == 0) set_status(status, ECHO_ST_BADDATA);
-        lo = 0;
-        n = 0;
+    int64_t lo, n;
+    {
+        int64_t hi;
+        if (!seg_bounds(segs.tok_off, segs.tok_end, segs.n_tokens, b, &lo, &hi) && leader && tid == 0)
+            set_status(status, ECHO_ST_BADDATA);
+        n = hi - lo;
     }
     const float* sc = scores + lo;
     int32_t* out = sel + static_cast<int64_t>(b) * k;
@@ -893,14 +892,14 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTT, 1)
 
 namespace echo {
 
-int launch_topk(int B, const int64_t* tok_off, int64_t n_tokens, int64_t row0, int64_t W, const float* scores, int k,
+int launch_topk(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens, int64_t row0, int64_t W, const float* scores, int k,
                 const uint32_t* hist, float* theta_hat, float alpha, int32_t* sel_idx, float* kth, int32_t* status,
                 uint32_t* stats, cudaStream_t stream) {
     const size_t smem = kTopkSmem;
     ECHO_CUDA_OK(prefer_max_shared(topk_kernel));
     ECHO_CUDA_OK(cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(smem)));
-    TopkSegs segs{tok_off, n_tokens, row0, W};
+    TopkSegs segs{tok_off, tok_end, n_tokens, row0, W};
     topk_kernel<<<B * kCS, kTT, smem, stream>>>(segs, scores, k, hist, theta_hat, alpha, sel_idx, kth, status, stats);
     ECHO_CUDA_OK(cudaGetLastError());
     return ECHO_OK;
@@ -908,7 +907,8 @@ int launch_topk(int B, const int64_t* tok_off, int64_t n_tokens, int64_t row0, i
 
 }  // namespace echo
 
-extern "C" int echo_topk_select(int B, const int64_t* tok_off, int64_t n_tokens, const float* scores, int k,
+extern "C" int echo_topk_select(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens,
+                                const float* scores, int k,
                                 const uint32_t* hist, float* theta_hat, float alpha, int32_t* sel_idx, float* kth,
                                 int32_t* status, uint32_t* stats, echo_stream_t stream) {
     using namespace echo;
@@ -916,13 +916,13 @@ extern "C" int echo_topk_select(int B, const int64_t* tok_off, int64_t n_tokens,
     if (B > ECHO_MAX_REQUESTS) return ECHO_EUNSUPPORTED;
     if (!tok_off || !sel_idx || !kth || !status || (n_tokens > 0 && !scores)) return ECHO_EINVAL;
     if (n_tokens >= (1ll << 31)) return ECHO_EUNSUPPORTED;
-    return launch_topk(B, tok_off, n_tokens, 0, 0, scores, k, hist, theta_hat, alpha, sel_idx, kth, status, stats,
+    return launch_topk(B, tok_off, tok_end, n_tokens, 0, 0, scores, k, hist, theta_hat, alpha, sel_idx, kth, status, stats,
                        stream);
 }
 
 namespace echo {
 
-int launch_topk_cached(int B, const int64_t* tok_off, int64_t n_tokens, const float* scores, int k,
+int launch_topk_cached(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens, const float* scores, int k,
                        const uint32_t* hist, float* theta_hat, float alpha, int32_t* sel_idx, float* kth,
                        const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,
                        int32_t* status, uint32_t* stats, cudaStream_t stream) {
@@ -930,7 +930,7 @@ int launch_topk_cached(int B, const int64_t* tok_off, int64_t n_tokens, const fl
     ECHO_CUDA_OK(prefer_max_shared(topk_cached_kernel));
     ECHO_CUDA_OK(cudaFuncSetAttribute(topk_cached_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(smem)));
-    TopkSegs segs{tok_off, n_tokens, 0, 0};
+    TopkSegs segs{tok_off, tok_end, n_tokens, 0, 0};
     TopkCache tc{above, early_cap, cache->tok2slot, cache->slot2tok, cache->freebits, cache->early_cnt, sel_slot,
                  static_cast<int>(cache->C)};
     topk_cached_kernel<<<B * kCS, kTT, smem, stream>>>(segs, scores, k, hist, theta_hat, alpha, sel_idx, kth, tc,
@@ -941,7 +941,8 @@ int launch_topk_cached(int B, const int64_t* tok_off, int64_t n_tokens, const fl
 
 }  // namespace echo
 
-extern "C" int echo_topk_select_cached(int B, const int64_t* tok_off, int64_t n_tokens, const float* scores, int k,
+extern "C" int echo_topk_select_cached(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens,
+                                       const float* scores, int k,
                                        const uint32_t* hist, float* theta_hat, float alpha, int32_t* sel_idx,
                                        float* kth, const uint32_t* above, int early_cap, const echo_cache* cache,
                                        int32_t* sel_slot, int32_t* status, uint32_t* stats, echo_stream_t stream) {
@@ -953,6 +954,6 @@ extern "C" int echo_topk_select_cached(int B, const int64_t* tok_off, int64_t n_
     const int rc = check_cache(cache, B, k);
     if (rc) return rc;
     if (cache->C / 32 > kFbWordsMax) return ECHO_EUNSUPPORTED;
-    return launch_topk_cached(B, tok_off, n_tokens, scores, k, hist, theta_hat, alpha, sel_idx, kth, above, early_cap,
+    return launch_topk_cached(B, tok_off, tok_end, n_tokens, scores, k, hist, theta_hat, alpha, sel_idx, kth, above, early_cap,
                               cache, sel_slot, status, stats, static_cast<cudaStream_t>(stream));
 }

@@ -36,7 +36,7 @@ class DecodeLayer:
                  host_pool: torch.Tensor, alpha: float = 0.5, predictor: bool = True,
                  early_cap: int = -1, groups: int | None = None, first_share: float = 0.5,
                  resolved: bool = True, hold_early: bool = False, attention: bool = False,
-                 mla_scale: float = 1.0 / math.sqrt(192.0), device="cuda"):
+                 mla_scale: float = 1.0 / math.sqrt(192.0), tok_end=None, device="cuda"):
         tok_off = torch.as_tensor(tok_off, dtype=torch.int64)
         self.B = int(tok_off.numel() - 1)
         self.n_tokens = int(k8.shape[0])
@@ -54,6 +54,9 @@ class DecodeLayer:
             early_cap = room
         self.early_cap = int(early_cap)
         self.tok_off = tok_off.to(device)
+        # growing contexts: request b's region is [tok_off[b], tok_off[b+1]) and tok_end[b] its current end
+        # (append() adds a token); None: every region is full
+        self.tok_end = None if tok_end is None else torch.as_tensor(tok_end, dtype=torch.int64).to(device)
         self.k8, self.ks = k8, ks
         f32 = dict(dtype=torch.float32, device=device)
         i32 = dict(dtype=torch.int32, device=device)
@@ -126,11 +129,11 @@ class DecodeLayer:
         L.quantize_q(q, w, self.q8, self.qscale, self.wfold, self.status, hist=self.hist, stream=main)
         if not self.predictor:
             L.index_scores(self.tok_off, self.n_tokens, self.q8, self.wfold, self.k8, self.ks, self.scores,
-                           self.theta, self.hist, self.status, stream=main)
+                           self.theta, self.hist, self.status, stream=main, tok_end=self.tok_end)
             L.topk_select(self.tok_off, self.n_tokens, self.scores, self.k, self.hist, self.theta, self.alpha,
-                          self.sel_idx, self.kth, self.status, stats=self.stats, stream=main)
+                          self.sel_idx, self.kth, self.status, stats=self.stats, stream=main, tok_end=self.tok_end)
             L.cache_step(self.tok_off, self.n_tokens, self.sel_idx, self.cache, self.sel_slot, self.status,
-                         stats=self.stats, stream=main, copy_stream=main)
+                         stats=self.stats, stream=main, copy_stream=main, tok_end=self.tok_end)
             if out_host is not None:
                 with torch.cuda.stream(main):
                     self._write_out(out_host, 0, self.B)
@@ -139,6 +142,7 @@ class DecodeLayer:
             return
         sms = torch.cuda.get_device_properties(main.device).multi_processor_count
         scored, gstream = None, []
+        end = (lambda b0, b1: None) if self.tok_end is None else (lambda b0, b1: self.tok_end[b0:b1])
         for g, (b0, b1) in enumerate(self.groups):
             s = main if g == 0 else self.gstreams[g - 1]
             if scored is not None:
@@ -148,14 +152,14 @@ class DecodeLayer:
             ctas = 0 if g == 0 else max(sms - L.EARLY_FETCH_BLOCKS * g, sms // 4)
             L.index_scores(self.tok_off[b0:b1 + 1], self.n_tokens, self.q8[b0:b1], self.wfold[b0:b1], self.k8,
                            self.ks, self.scores, self.theta[b0:b1], self.hist[b0:b1], self.status,
-                           above=self.above_g[g], cache=self.views[g], stream=s, ctas=ctas)
+                           above=self.above_g[g], cache=self.views[g], stream=s, ctas=ctas, tok_end=end(b0, b1))
             scored = torch.cuda.Event()
             scored.record(s)
             gstream.append(s)
             # the group's early rows stream over the host link on `s` (programmatic dependent of its
             # score kernel) while the next group is scored
             L.early_fetch(self.tok_off[b0:b1 + 1], self.n_tokens, self.above_g[g], self.early_cap, self.views[g],
-                          self.status, stream=s)
+                          self.status, stream=s, tok_end=end(b0, b1))
         # top-k and the table update of every group on the groups' side streams once all scores are
         # done (a top-k started earlier would take SMs the next score kernel counts on); the late
         # misses of a group follow its early fetch on the group's stream (a slot fetched early and
@@ -170,17 +174,17 @@ class DecodeLayer:
                 L.topk_select_cached(off, self.n_tokens, self.scores, self.k, self.hist[b0:b1], self.theta[b0:b1],
                                      self.alpha, self.sel_idx[b0:b1], self.kth[b0:b1], self.views[g],
                                      self.sel_slot[b0:b1], self.status, stats=self.stats, stream=side,
-                                     above=self.above_g[g], early_cap=self.early_cap)
+                                     above=self.above_g[g], early_cap=self.early_cap, tok_end=end(b0, b1))
                 L.cache_step_resolved(off, self.n_tokens, self.sel_idx[b0:b1], self.views[g], self.sel_slot[b0:b1],
                                       self.status, stats=self.stats, stream=side, copy_stream=copy,
-                                      hold_early=self.hold_early)
+                                      hold_early=self.hold_early, tok_end=end(b0, b1))
             else:
                 L.topk_select(off, self.n_tokens, self.scores, self.k, self.hist[b0:b1], self.theta[b0:b1],
                               self.alpha, self.sel_idx[b0:b1], self.kth[b0:b1], self.status, stats=self.stats,
-                              stream=side)
+                              stream=side, tok_end=end(b0, b1))
                 L.cache_step(off, self.n_tokens, self.sel_idx[b0:b1], self.views[g], self.sel_slot[b0:b1],
                              self.status, stats=self.stats, stream=side, copy_stream=copy, above=self.above_g[g],
-                             early_cap=self.early_cap, hold_early=self.hold_early)
+                             early_cap=self.early_cap, hold_early=self.hold_early, tok_end=end(b0, b1))
             if out_host is not None:
                 with torch.cuda.stream(side):
                     self._write_out(out_host, b0, b1)
@@ -193,6 +197,16 @@ class DecodeLayer:
             main.wait_stream(gs)
         for side in self.sides:
             main.wait_stream(side)
+
+    def append(self, k_new: torch.Tensor, kv_new: torch.Tensor, stream=None):
+        """Enqueue the append of one new token per request (k_new [B,128] f32, kv_new [B,576] bf16,
+        device): its E4M3 key and scale at tok_end[b], its row in the host pool and, when a slot is
+        free, in the cache; tok_end advances (a full region sets ECHO_ST_FULL).  Needs tok_end."""
+        if self.tok_end is None:
+            raise ValueError("append needs growing contexts (tok_end)")
+        main = torch.cuda.current_stream() if stream is None else stream
+        L.append_tokens(self.tok_off, self.tok_end, self.n_tokens, k_new, kv_new, self.k8, self.ks, self.cache,
+                        self.status, stream=main)
 
     def _attend(self, mla_q, b0, b1, stream):
         C = self.C

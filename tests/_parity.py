@@ -153,3 +153,85 @@ def run_decode(w: wl.Workload, steps: int, predictor: bool, cap: int = -1, score
     report["fallbacks"] = int(lay.stats[L.STAT_TOPK_FALLBACK].item())
     assert torch.equal(host.view(torch.int16), host_before.view(torch.int16))  # no write-back
     return report
+
+
+def run_decode_growing(w: wl.Workload, steps: int, room: int, hold_early: bool = False, seed: int = 5):
+    """Decode steps on growing contexts: request b's region holds its w.lengths[b] tokens plus `room`
+    free rows; after each step one new token per request is appended (GPU: echo_append_tokens; the
+    oracle: its own append on its own copies of the keys, the host pool and the tables).  Every step
+    is checked as in run_decode over each request's current tokens, and every append bit-exactly."""
+    dev = "cuda"
+    lens = np.asarray(w.lengths, np.int64)
+    off = np.concatenate([[0], np.cumsum(lens + room)]).astype(np.int64)
+    n = int(off[-1])
+    end = off[:-1] + lens
+    big = wl.scaled(w, w.name + "_room", lengths=tuple(int(x) for x in lens + room))
+    k8c, ksc = wl.make_keys(big, 0)
+    wt = wl.make_weights(big, 0).cpu()
+    host = wl.make_host_pool(big, 0, pin=True)
+    # the rows after each request's end are not tokens yet
+    k8 = k8c.numpy().copy()
+    ks = ksc.numpy().copy()
+    for b in range(w.B):
+        k8[end[b]:off[b + 1]] = 0
+        ks[end[b]:off[b + 1]] = 0
+        host[end[b]:off[b + 1]] = 0
+    lay = DecodeLayer(off, torch.from_numpy(k8).to(dev), torch.from_numpy(ks).to(dev), w.k, w.C, host,
+                      hold_early=hold_early, tok_end=torch.from_numpy(end), device=dev)
+    o = OracleLayer(w.B, n, w.C)
+    o_end = end.copy()
+    o_host = host.view(torch.uint8).numpy().copy()
+    o_dev = np.zeros((w.B * w.C, o_host.shape[1]), np.uint8)
+    qsrc = wl.QueryStream(big, 0)
+    rng = np.random.default_rng(seed)
+    for t in range(steps):
+        q = qsrc.next().cpu()
+        theta_before = o.theta.copy()
+        lay.step(q.to(dev), wt.to(dev))
+        torch.cuda.synchronize()
+        assert int(lay.status.item()) == 0, f"status {int(lay.status.item()):#x} at step {t}"
+        gs = lay.scores.cpu().numpy()
+        g_sel, g_slot, g_kth = lay.sel_idx.cpu().numpy(), lay.sel_slot.cpu().numpy(), lay.kth.cpu().numpy()
+        q8, qs, _ = orc.quantize_q(q.numpy(), wt.numpy())
+        for b in range(w.B):
+            lo, hi = int(off[b]), int(o_end[b])
+            tok = np.arange(lo, hi, dtype=np.int64)
+            ref, ab = orc.scores(q8[b], qs[b], wt.numpy()[b], k8, ks, tok=tok)
+            bad, _ = score_tolerance_ok(gs[lo:hi], ref, ab)
+            assert bad.size == 0, (t, b, "scores")
+            sc = gs[lo:hi]
+            t2s = o.t2s[lo:hi]
+            s2t = o.s2t[b * w.C:(b + 1) * w.C]
+            et, _ = orc.early_fetch(sc, theta_before[b], lay.early_cap, t2s, s2t)
+            idx, kth = orc.topk(sc, w.k)
+            assert np.array_equal(g_sel[b], idx), (t, b, "topk")
+            assert g_kth[b] == np.float32(kth), (t, b, "kth")
+            o.theta[b] = orc.ema(theta_before[b], kth, 0.5)
+            sel_slot, mt, ms, _ = orc.cache_step(idx, t2s, s2t, early_tok=et, hold_early=hold_early)
+            assert np.array_equal(g_slot[b], sel_slot), (t, b, "sel_slot")
+            orc.recall(o_host[lo:hi], mt, ms, o_dev[b * w.C:(b + 1) * w.C])
+            valid = idx >= 0
+            o_dev[b * w.C + sel_slot[valid]] = o_host[lo + idx[valid]]
+        assert np.array_equal(lay.cache.tok2slot.cpu().numpy(), o.t2s), (t, "tok2slot")
+        assert np.array_equal(lay.cache.slot2tok.cpu().numpy(), o.s2t), (t, "slot2tok")
+        # every selected token's device row is its host row
+        g_dev = lay.cache.dev_kv.view(torch.uint8).cpu().numpy().reshape(w.B * w.C, -1)
+        for b in range(w.B):
+            v = g_slot[b] >= 0
+            assert np.array_equal(g_dev[b * w.C + g_slot[b][v]], o_host[off[b] + g_sel[b][v]]), (t, b, "rows")
+        # ---- append one token per request
+        k_new = rng.standard_normal((w.B, L.DIM), dtype=np.float32)
+        kv_new = rng.integers(-2**15, 2**15, (w.B, o_host.shape[1] // 2), dtype=np.int16)
+        lay.append(torch.from_numpy(k_new).to(dev), torch.from_numpy(kv_new).to(dev))
+        torch.cuda.synchronize()
+        full = orc.append_tokens(off, o_end, k_new, kv_new.view(np.uint8), k8, ks, o_host, w.C, o.t2s, o.s2t,
+                                 o_dev)
+        want = L.ST_FULL if full.any() else 0
+        assert int(lay.status.item()) == want, (t, "append status")
+        lay.status.zero_()
+        assert np.array_equal(lay.tok_end.cpu().numpy(), o_end), (t, "tok_end")
+        assert np.array_equal(lay.k8.cpu().numpy(), k8) and np.array_equal(lay.ks.cpu().numpy(), ks), (t, "keys")
+        assert np.array_equal(host.view(torch.uint8).numpy(), o_host), (t, "host pool")
+        assert np.array_equal(lay.cache.tok2slot.cpu().numpy(), o.t2s), (t, "append tok2slot")
+        assert np.array_equal(lay.cache.slot2tok.cpu().numpy(), o.s2t), (t, "append slot2tok")
+    return o_end - end

@@ -51,10 +51,10 @@ def test_host_checks_reject_bad_arguments(L):
     from sparse_attention_kv_echo_gb300 import lib
     v = ctypes.c_void_p
     dummy = v(0x1000)
-    # index_scores(B, tok_off, n_tokens, q8, wfold, k8, ks, scores, theta, hist, above, cache, ctas, status,
-    #              stream)
+    # index_scores(B, tok_off, tok_end, n_tokens, q8, wfold, k8, ks, scores, theta, hist, above, cache, ctas,
+    #              status, stream)
     def scores_call(B=1, n=10, q8=dummy, k8=dummy, above=None, cache=None):
-        return L.echo_index_scores(B, dummy, n, q8, dummy, k8, dummy, dummy, None, None, above, cache, 0, dummy,
+        return L.echo_index_scores(B, dummy, None, n, q8, dummy, k8, dummy, dummy, None, None, above, cache, 0, dummy,
                                    None)
     assert scores_call(B=0) == lib.ECHO_EINVAL
     assert scores_call(B=lib.MAX_REQUESTS + 1) == lib.ECHO_EUNSUPPORTED
@@ -72,23 +72,23 @@ def test_host_checks_reject_bad_arguments(L):
     assert scores_call(above=None, cache=cache) == lib.ECHO_EINVAL
     c.free_snap = None
     assert scores_call(above=dummy, cache=cache) == lib.ECHO_EINVAL
-    # early_fetch(B, tok_off, n_tokens, above, early_cap, cache, status, stream)
-    assert L.echo_early_fetch(1, dummy, 10, dummy, -1, cache, dummy, None) == lib.ECHO_EINVAL   # no snapshot
+    # early_fetch(B, tok_off, tok_end, n_tokens, above, early_cap, cache, status, stream)
+    assert L.echo_early_fetch(1, dummy, None, 10, dummy, -1, cache, dummy, None) == lib.ECHO_EINVAL   # no snapshot
     c.free_snap = 0x1000
-    assert L.echo_early_fetch(1, dummy, 10, None, -1, cache, dummy, None) == lib.ECHO_EINVAL    # no above words
-    assert L.echo_early_fetch(1, dummy, 10, dummy, -1, None, dummy, None) == lib.ECHO_EINVAL    # no cache
-    assert L.echo_early_fetch(0, dummy, 10, dummy, -1, cache, dummy, None) == lib.ECHO_EINVAL
-    assert L.echo_early_fetch(1, dummy, 0, dummy, -1, cache, dummy, None) == lib.ECHO_OK        # nothing to do
-    assert L.echo_early_fetch(1, dummy, 10, dummy, 0, cache, dummy, None) == lib.ECHO_OK        # cap 0: nothing
+    assert L.echo_early_fetch(1, dummy, None, 10, None, -1, cache, dummy, None) == lib.ECHO_EINVAL    # no above words
+    assert L.echo_early_fetch(1, dummy, None, 10, dummy, -1, None, dummy, None) == lib.ECHO_EINVAL    # no cache
+    assert L.echo_early_fetch(0, dummy, None, 10, dummy, -1, cache, dummy, None) == lib.ECHO_EINVAL
+    assert L.echo_early_fetch(1, dummy, None, 0, dummy, -1, cache, dummy, None) == lib.ECHO_OK        # nothing to do
+    assert L.echo_early_fetch(1, dummy, None, 10, dummy, 0, cache, dummy, None) == lib.ECHO_OK        # cap 0: nothing
     c.C = 48                                                           # not a multiple of 32
-    assert L.echo_early_fetch(1, dummy, 10, dummy, -1, cache, dummy, None) == lib.ECHO_ECAPACITY
+    assert L.echo_early_fetch(1, dummy, None, 10, dummy, -1, cache, dummy, None) == lib.ECHO_ECAPACITY
     assert scores_call(above=dummy, cache=cache) == lib.ECHO_ECAPACITY
     # the bitmask size: four words per 128-token tile of each request, at most
     assert lib.above_words(8, 32768) == 4 * (256 + 8)
     assert lib.above_words(0, 10) == 0
-    assert L.echo_topk_select(1, dummy, 10, dummy, 0, None, None, 0.5, dummy, dummy, dummy, None,
+    assert L.echo_topk_select(1, dummy, None, 10, dummy, 0, None, None, 0.5, dummy, dummy, dummy, None,
                               None) == lib.ECHO_EINVAL
-    assert L.echo_topk_select(-3, dummy, 10, dummy, 4, None, None, 0.5, dummy, dummy, dummy, None,
+    assert L.echo_topk_select(-3, dummy, None, 10, dummy, 4, None, None, 0.5, dummy, dummy, dummy, None,
                               None) == lib.ECHO_EINVAL
     assert L.echo_quantize_q(-1, dummy, dummy, dummy, dummy, dummy, None, dummy, None) == lib.ECHO_EINVAL
     assert L.echo_quantize_q(1, dummy, dummy, dummy, dummy, v(0x1004), None, dummy, None) == lib.ECHO_EINVAL
@@ -104,29 +104,43 @@ def test_cache_checks(L):
     s.row_bytes, s.C = 1152, 64
     dummy = v(0x1000)
     # k (m) larger than C
-    assert L.echo_cache_step(1, dummy, 100, dummy, 65, None, 0, ctypes.byref(s), dummy, dummy, None, None,
+    assert L.echo_cache_step(1, dummy, None, 100, dummy, 65, None, 0, ctypes.byref(s), dummy, dummy, None, None,
                              None, 0) == lib.ECHO_ECAPACITY
     s.C = 48   # not a multiple of 32
-    assert L.echo_cache_step(1, dummy, 100, dummy, 16, None, 0, ctypes.byref(s), dummy, dummy, None, None,
+    assert L.echo_cache_step(1, dummy, None, 100, dummy, 16, None, 0, ctypes.byref(s), dummy, dummy, None, None,
                              None, 0) == lib.ECHO_ECAPACITY
     s.C, s.row_bytes = 64, 1000  # row not a multiple of 16 bytes
-    assert L.echo_cache_step(1, dummy, 100, dummy, 16, None, 0, ctypes.byref(s), dummy, dummy, None, None,
+    assert L.echo_cache_step(1, dummy, None, 100, dummy, 16, None, 0, ctypes.byref(s), dummy, dummy, None, None,
                              None, 0) == lib.ECHO_EUNSUPPORTED
     s.row_bytes, s.dev_kv = 1152, None
-    assert L.echo_cache_step(1, dummy, 100, dummy, 16, None, 0, ctypes.byref(s), dummy, dummy, None, None,
+    assert L.echo_cache_step(1, dummy, None, 100, dummy, 16, None, 0, ctypes.byref(s), dummy, dummy, None, None,
                              None, 0) == lib.ECHO_EINVAL
     s.dev_kv = 0x2000
     # unknown flag bits
-    assert L.echo_cache_step(1, dummy, 100, dummy, 16, None, 0, ctypes.byref(s), dummy, dummy, None, None,
+    assert L.echo_cache_step(1, dummy, None, 100, dummy, 16, None, 0, ctypes.byref(s), dummy, dummy, None, None,
                              None, 2) == lib.ECHO_EINVAL
-    assert L.echo_cache_step_resolved(1, dummy, 100, dummy, 16, ctypes.byref(s), dummy, dummy, None, None,
+    assert L.echo_cache_step_resolved(1, dummy, None, 100, dummy, 16, ctypes.byref(s), dummy, dummy, None, None,
                                       None, 4) == lib.ECHO_EINVAL
     # the resolved form: k larger than C; the cached top-k: C above its shared-memory limit
-    assert L.echo_cache_step_resolved(1, dummy, 100, dummy, 65, ctypes.byref(s), dummy, dummy, None, None,
+    assert L.echo_cache_step_resolved(1, dummy, None, 100, dummy, 65, ctypes.byref(s), dummy, dummy, None, None,
                                       None, 0) == lib.ECHO_ECAPACITY
     s.C = 65536
-    assert L.echo_topk_select_cached(1, dummy, 100, dummy, 16, None, None, 0.5, dummy, dummy, None, -1,
+    assert L.echo_topk_select_cached(1, dummy, None, 100, dummy, 16, None, None, 0.5, dummy, dummy, None, -1,
                                      ctypes.byref(s), dummy, dummy, None, None) == lib.ECHO_EUNSUPPORTED
     s.C = 64
-    assert L.echo_topk_select_cached(1, dummy, 100, dummy, 16, None, None, 0.5, dummy, dummy, None, -1,
+    assert L.echo_topk_select_cached(1, dummy, None, 100, dummy, 16, None, None, 0.5, dummy, dummy, None, -1,
                                      ctypes.byref(s), None, dummy, None, None) == lib.ECHO_EINVAL   # no sel_slot
+
+
+
+def test_append_argument_checks(L):
+    """echo_append_tokens(B, tok_off, tok_end, n_tokens, k_new, kv_new, k8, ks, cache, status, stream):
+    argument errors return before anything is enqueued (no GPU needed)."""
+    from sparse_attention_kv_echo_gb300 import lib
+    d = ctypes.c_void_p(0x1000)
+    assert L.echo_append_tokens(0, d, d, 10, d, d, d, d, None, d, None) == lib.ECHO_EINVAL
+    assert L.echo_append_tokens(1, d, d, 0, d, d, d, d, None, d, None) == lib.ECHO_EINVAL
+    assert L.echo_append_tokens(1, None, d, 10, d, d, d, d, None, d, None) == lib.ECHO_EINVAL
+    assert L.echo_append_tokens(1, d, None, 10, d, d, d, d, None, d, None) == lib.ECHO_EINVAL
+    assert L.echo_append_tokens(1, d, d, 10, d, d, d, d, None, d, None) == lib.ECHO_EINVAL   # no cache
+    assert L.echo_append_tokens(lib.MAX_REQUESTS + 1, d, d, 10, d, d, d, d, None, d, None) == lib.ECHO_EUNSUPPORTED
