@@ -59,9 +59,10 @@ def parse_args(argv=None):
                    help="where the selected tokens' slots are looked up (top-k's slices or the cache step)")
     p.add_argument("--hold-early", action="store_true",
                    help="the held-slot variant of the cache step (the late recall need not wait for the early copy)")
-    p.add_argument("--part", choices=["step", "mla"], default="step",
+    p.add_argument("--part", choices=["step", "mla", "append"], default="step",
                    help="step: the decode step (default); mla: the sparse MLA attention over the selected "
-                        "slots alone, at the step's batch, k and GPU slots")
+                        "slots alone, at the step's batch, k and GPU slots; append: the append of one new "
+                        "token per request (key, host-pool row, cache slot) at the step's batch")
     p.add_argument("--first-share", type=float, default=None,
                    help="share of the requests in the first of two groups (default: the layer's choice)")
     return p.parse_args(argv)
@@ -591,10 +592,77 @@ def run_mla(args):
     }), flush=True)
 
 
+APPEND_METRIC = "appends/s: one new token per request (E4M3 key + scale, host-pool row, cache slot)"
+
+
+def run_append(args):
+    """echo_append_tokens alone: 8 requests of 32768 tokens in regions with room for every timed
+    call, 4096 GPU slots each with free slots, 576-dim bf16 rows into the pinned host pool."""
+    import numpy as np
+    import torch
+    from sparse_attention_kv_echo_gb300 import _lib as L
+    from sparse_attention_kv_echo_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    L.load(build_if_missing=True)
+    w = wl.WORKLOADS["batch"]
+    B, C, n0 = w.B, w.C, w.lengths[0]
+    room = args.warmup + args.steps
+    off = torch.arange(B + 1, dtype=torch.int64, device=dev) * (n0 + room)
+    end = off[:-1] + n0
+    n = int(off[-1].item())
+    k8 = torch.zeros((n, L.DIM), dtype=torch.uint8, device=dev)
+    ks = torch.zeros(n, dtype=torch.float32, device=dev)
+    host = torch.empty((n, 576), dtype=torch.bfloat16).pin_memory()
+    cache = L.LayerCache(B, n, C, host, device=dev)
+    g = torch.Generator(device=dev).manual_seed(13 + rank)
+    k_new = torch.randn((room, B, L.DIM), generator=g, device=dev)
+    kv_new = torch.randn((room, B, 576), generator=g, device=dev).to(torch.bfloat16)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    main = torch.cuda.Stream()
+    for i in range(args.warmup):
+        with torch.cuda.stream(main):
+            flush.zero_()
+            L.append_tokens(off, end, n, k_new[i], kv_new[i], k8, ks, cache, st, stream=main)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    park(main)
+    for i in range(args.steps):
+        with torch.cuda.stream(main):
+            flush.zero_()
+            starts[i].record(main)
+            L.append_tokens(off, end, n, k_new[args.warmup + i], kv_new[args.warmup + i], k8, ks, cache, st,
+                            stream=main)
+            ends[i].record(main)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and torch.equal(end, off[:-1] + n0 + room)
+    ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    t = statistics.mean(ms) / 1e3
+    # per appended token: key in (512 B) and codes + scale out (132 B), row in (1152 B) and out to the
+    # cache (1152 B) and over the host link (1152 B), ~12 B of tables
+    per_tok = 512 + 132 + 1152 * 3 + 12
+    print(json.dumps({
+        "metric": APPEND_METRIC, "value": round(B / t, 1), "unit": "appends/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t, 5), "higher_is_better": True,
+        "dtype": "fp32 key -> E4M3, bf16 rows", "data": "synthetic (seeded)",
+        "config": {"workload": f"{B} requests x {n0} tokens (+{room} rows of room), {C} GPU slots each",
+                   "l2": "flushed by a 256 MB write before every timed call"},
+        "roofline": {"kernel": "append_kernel", "bound": "latency", "achieved_us": round(1e6 * t, 2),
+                     "bytes_per_call": B * per_tok, "gbs": round(B * per_tok / t / 1e9, 2)},
+        "us_min": round(1e3 * min(ms), 2), "status": int(st.item()),
+    }), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.part == "append":
+        run_append(args)
     elif args.part == "mla":
         run_mla(args)
     else:
