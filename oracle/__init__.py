@@ -93,6 +93,9 @@ def lib():
             L.orc_prefill_rows.argtypes = [c_f32p, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
                                            ctypes.c_int, ctypes.c_float, c_i32p, c_f32p, c_u32p,
                                            c_u8p]
+            L.orc_early_from_selection.restype = ctypes.c_int
+            L.orc_early_from_selection.argtypes = [ctypes.c_int64, ctypes.c_int, c_i32p, ctypes.c_int,
+                                                   ctypes.c_int, c_i32p, c_i32p, c_i32p, c_i32p, c_i32p]
             L.orc_append_tokens.restype = ctypes.c_int
             L.orc_append_tokens.argtypes = [ctypes.c_int, c_i64p, c_i64p, c_f32p, ctypes.c_int, c_u8p,
                                             ctypes.c_int64, c_u8p, c_f32p, c_u8p, ctypes.c_int, c_i32p, c_i32p,
@@ -219,6 +222,24 @@ def early_fetch(scores_f32, theta: float, cap: int, tok2slot, slot2tok):
                                _p(tok2slot, ctypes.c_int32), _p(slot2tok, ctypes.c_int32),
                                _p(et, ctypes.c_int32), _p(es, ctypes.c_int32), ctypes.byref(cnt))
     _check(rc, "early_fetch")
+    return et[:cnt.value].copy(), es[:cnt.value].copy()
+
+
+def early_from_selection(prev_sel, n: int, cap: int, tok2slot, slot2tok):
+    """Cross-layer early fetch (survey NEXT-4 reading): the previous layer's selection prev_sel
+    [m] (-1 padded) minus this layer's residents, ascending, <= min(cap, free).  Updates
+    tok2slot [n] / slot2tok [C] (numpy int32, in place); -> (early_tok, early_slot)."""
+    sel = _c(prev_sel, np.int32).reshape(-1)
+    assert tok2slot.dtype == np.int32 and slot2tok.dtype == np.int32
+    assert tok2slot.flags.c_contiguous and slot2tok.flags.c_contiguous and tok2slot.size == n
+    C = slot2tok.size
+    et = np.empty(max(C, 1), np.int32)
+    es = np.empty(max(C, 1), np.int32)
+    cnt = ctypes.c_int32()
+    rc = lib().orc_early_from_selection(int(n), C, _p(sel, ctypes.c_int32), sel.size, int(cap),
+                                        _p(tok2slot, ctypes.c_int32), _p(slot2tok, ctypes.c_int32),
+                                        _p(et, ctypes.c_int32), _p(es, ctypes.c_int32), ctypes.byref(cnt))
+    _check(rc, "early_from_selection")
     return et[:cnt.value].copy(), es[:cnt.value].copy()
 
 

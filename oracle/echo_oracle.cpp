@@ -353,6 +353,41 @@ int orc_early_fetch(int64_t n, int C, const float* scores, float theta, int cap,
     return ORC_OK;
 }
 
+// ---- cross-layer early fetch (survey NEXT-4) -------------------------------
+// Blog page "ECHO KV Cache Offloading ... Guide", section "Intra-Query
+// Prefetching: Layer-to-Layer Pipeline": the tokens that layer l selects are
+// mostly selected by layers l+1 and l+2 too, so the ones not yet resident for
+// layer l+1 are fetched as soon as layer l's selection is known.  READING: the
+// early set of layer l+1 is then layer l's selection (prev_sel [m], -1
+// padded, entries >= n ignored) minus layer l+1's residents, taken exactly as
+// the threshold early fetch takes its marked tokens: ascending token order,
+// at most min(cap, F) (F = free slots of layer l+1 at that moment), lowest
+// free slots ascending, resident at once.  Outputs as orc_early_fetch.
+int orc_early_from_selection(int64_t n, int C, const int32_t* prev_sel, int m, int cap, int32_t* tok2slot,
+                             int32_t* slot2tok, int32_t* early_tok, int32_t* early_slot, int32_t* count) {
+    if (!cache_consistent(n, C, tok2slot, slot2tok) || m < 0) return ORC_EINVAL;
+    std::set<int32_t> marked;
+    for (int i = 0; i < m; ++i)
+        if (prev_sel[i] >= 0 && prev_sel[i] < n) marked.insert(prev_sel[i]);
+    Cache c = load_cache(n, C, tok2slot, slot2tok);
+    const int64_t F = (int64_t)c.free_slots.size();
+    const int64_t limit = (cap < 0) ? F : std::min<int64_t>(cap, F);
+    int32_t got = 0;
+    for (int32_t s : marked) {  // ascending
+        if (got >= limit) break;
+        if (c.resident.count(s)) continue;
+        const int32_t slot = *c.free_slots.begin();
+        c.free_slots.erase(c.free_slots.begin());
+        c.resident[s] = slot;
+        early_tok[got] = s;
+        early_slot[got] = slot;
+        ++got;
+    }
+    *count = got;
+    store_cache(c, n, C, tok2slot, slot2tok);
+    return ORC_OK;
+}
+
 // ---- [EXPL "One layer, one step: free -> allocate -> recall"] -------------
 // sel [m] is the step's selection in ascending token order, -1 padded.
 // early_tok [n_early] are the tokens this step's early fetch made resident

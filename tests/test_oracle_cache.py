@@ -182,3 +182,51 @@ def test_decode_step_pipeline(orc):
             for s, j in zip(idx, out["sel_slot"][b]):
                 assert np.array_equal(dev[b * w.C + j], host_u8[off[b] + s])
         assert np.all(np.isfinite(theta))
+
+
+def test_cross_layer_early_set_pins(orc):
+    # layer l selected {1, 3, 4, 6}; layer l+1 holds token 3 in slot 0 and token 5 in slot 2:
+    # the early set is {1, 4, 6} (3 is resident), ascending, on the free slots 1, 3, 4
+    n, C = 8, 32
+    t2s = np.full(n, -1, np.int32)
+    s2t = np.full(C, -1, np.int32)
+    t2s[3], s2t[0] = 0, 3
+    t2s[5], s2t[2] = 2, 5
+    prev = np.array([1, 3, 4, 6, -1, -1], np.int32)
+    et, es = orc.early_from_selection(prev, n, -1, t2s, s2t)
+    assert et.tolist() == [1, 4, 6] and es.tolist() == [1, 3, 4]
+    assert t2s.tolist() == [-1, 1, -1, 0, 3, 2, 4, -1]
+    # a cap of 2 takes the two lowest tokens; with 2 free slots only, the free slots bound it
+    t2s = np.full(n, -1, np.int32)
+    s2t = np.full(C, -1, np.int32)
+    et, es = orc.early_from_selection(prev, n, 2, t2s, s2t)
+    assert et.tolist() == [1, 3] and es.tolist() == [0, 1]
+    t2s = np.full(n, -1, np.int32)
+    t2s[7] = 0
+    s2t = np.full(C, -1, np.int32)
+    s2t[0] = 7
+    s2t[1] = 100   # a slot held by a token beyond the request
+    with pytest.raises(Exception):
+        orc.early_from_selection(prev, n, -1, t2s, s2t)  # inconsistent tables are refused
+
+
+def test_cross_layer_equals_threshold_fetch_on_indicator_scores(orc):
+    # the cross-layer early set is the threshold early fetch whose marked tokens are the previous
+    # selection: both take the same tokens and slots on random tables
+    rng = np.random.default_rng(4)
+    for trial in range(20):
+        n, C = 300, 64
+        t2s = np.full(n, -1, np.int32)
+        s2t = np.full(C, -1, np.int32)
+        res = rng.choice(n, 20, replace=False)
+        slots = rng.choice(C, 20, replace=False)
+        t2s[res], s2t[slots] = slots, res
+        prev = np.sort(rng.choice(n, 40, replace=False)).astype(np.int32)
+        cap = int(rng.integers(-1, 50))
+        ind = np.zeros(n, np.float32)
+        ind[prev] = 1.0
+        a2s, a_s2t = t2s.copy(), s2t.copy()
+        et, es = orc.early_from_selection(np.concatenate([prev, [-1, -1]]), n, cap, t2s, s2t)
+        et2, es2 = orc.early_fetch(ind, 0.5, cap, a2s, a_s2t)
+        assert np.array_equal(et, et2) and np.array_equal(es, es2)
+        assert np.array_equal(t2s, a2s) and np.array_equal(s2t, a_s2t)
