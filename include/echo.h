@@ -401,6 +401,24 @@ int echo_mla_decode(int B, int k, const uint16_t* q, const int32_t* sel_slot, co
                     float scale, float* out, float* lse, int32_t* status, echo_stream_t stream);
 
 /*
+ * Cross-layer early set [blog page "ECHO KV Cache Offloading ... Guide",
+ * section "Intra-Query Prefetching: Layer-to-Layer Pipeline": layers l+1 and
+ * l+2 select mostly what layer l selected; reading: layer l+1's early set is
+ * layer l's selection minus layer l+1's residents].  Writes, for this layer's
+ * cache, the two inputs of its early set: `above` (echo_above_words(B,
+ * n_tokens) words, the layout echo_index_scores writes; bit set = selected by
+ * prev_sel [B,m] (-1 padded, request-local) and not resident) and
+ * cache->free_snap (this layer's free bits now).  Then call echo_early_fetch
+ * with the same `above` at once (it streams the rows while this layer has not
+ * scored yet), echo_index_scores of this layer with above = NULL and cache =
+ * NULL (no threshold bits, no new snapshot), and this layer's top-k / cache
+ * step with the same `above`.  The tables must not change between this call
+ * and this layer's cache step.  Errors as echo_early_fetch.
+ */
+int echo_seed_early(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens, const int32_t* prev_sel,
+                    int m, uint32_t* above, const echo_cache* cache, int32_t* status, echo_stream_t stream);
+
+/*
  * Append one new token to each request: the offload write path [EXPL section
  * 2, "One layer, one step": the host holds every token, hence no write-back
  * on eviction; the pages give no append mechanics -- reading below].

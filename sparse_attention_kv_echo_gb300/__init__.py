@@ -5,4 +5,4 @@ zero-copy recall from a pinned host pool.  The compute lives in ``libecho.so``
 (CUDA for sm_103a, C ABI in ``include/echo.h``); this package binds it.
 """
 from . import _lib as lib  # noqa: F401
-from .decode import DecodeLayer  # noqa: F401
+from .decode import DecodeLayer, DecodeStack  # noqa: F401

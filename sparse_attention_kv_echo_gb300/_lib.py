@@ -27,7 +27,7 @@ EARLY_FETCH_BLOCKS = 32      # CTAs of the early-fetch and late-recall kernels
 
 EXPORTS = ("echo_above_words", "echo_append_tokens", "echo_cache_step", "echo_cache_step_resolved", "echo_device_sm_count",
            "echo_early_fetch", "echo_host_device_alias", "echo_index_scores", "echo_mla_decode", "echo_prefill_block",
-           "echo_prefill_block_static", "echo_prefill_scores", "echo_prefill_workspace_size", "echo_quantize_q",
+           "echo_prefill_block_static", "echo_prefill_scores", "echo_prefill_workspace_size", "echo_quantize_q", "echo_seed_early",
            "echo_topk_select", "echo_topk_select_cached")
 
 _vp = ctypes.c_void_p
@@ -83,6 +83,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
                                       _vp, _vp, _vp, _vp, i32]
         L.echo_mla_decode.restype = i32
         L.echo_mla_decode.argtypes = [i32, i32, _vp, _vp, _vp, i64, f32, _vp, _vp, _vp, _vp]
+        L.echo_seed_early.restype = i32
+        L.echo_seed_early.argtypes = [i32, _vp, _vp, i64, _vp, i32, _vp, ctypes.POINTER(EchoCacheStruct), _vp, _vp]
         L.echo_append_tokens.restype = i32
         L.echo_append_tokens.argtypes = [i32, _vp, _vp, i64, _vp, _vp, _vp, _vp, ctypes.POINTER(EchoCacheStruct),
                                          _vp, _vp]
@@ -238,6 +240,15 @@ def cache_step_resolved(tok_off, n_tokens, sel, cache, sel_slot, status, stats=N
     _check("echo_cache_step_resolved", load().echo_cache_step_resolved(
         B, _ptr(tok_off), _ptr(tok_end), int(n_tokens), _ptr(sel), int(m), ctypes.byref(cache.struct), _ptr(sel_slot),
         _ptr(status), _ptr(stats), st, cst, CACHE_HOLD_EARLY if hold_early else 0))
+
+
+def seed_early(tok_off, n_tokens, prev_sel, above, cache, status, stream=None, tok_end=None):
+    """echo_seed_early: this layer's early set from the previous layer's selection prev_sel [B,m]
+    (above words + cache free-bit snapshot); follow with early_fetch on the same above words."""
+    B = tok_off.shape[0] - 1
+    _check("echo_seed_early", load().echo_seed_early(
+        B, _ptr(tok_off), _ptr(tok_end), int(n_tokens), _ptr(prev_sel), int(prev_sel.shape[-1]), _ptr(above),
+        ctypes.byref(cache.struct), _ptr(status), _stream(stream)))
 
 
 def append_tokens(tok_off, tok_end, n_tokens, k_new, kv_new, k8, ks, cache, status, stream=None):

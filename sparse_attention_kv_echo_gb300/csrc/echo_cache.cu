@@ -537,6 +537,35 @@ __global__ void __launch_bounds__(kRecallThreads)
     }
 }
 
+// Cross-layer seed of the early set: one block per request marks, in the
+// above-threshold word layout the score kernel writes (the request's words
+// from 4 * (floor(first row / 128) + b); bit j of word w = request-local token
+// 32 w + j), the tokens the previous layer selected that are not resident in
+// this layer, and snapshots this layer's free bits -- the two inputs the early
+// fetch, the cached top-k and the cache step read.
+constexpr int kSeedThreads = 256;
+__global__ void __launch_bounds__(kSeedThreads)
+    seed_kernel(const int64_t* __restrict__ tok_off, const int64_t* __restrict__ tok_end, int64_t n_tokens,
+                const int32_t* __restrict__ prev_sel, int m, uint32_t* __restrict__ above,
+                const int32_t* __restrict__ tok2slot, const uint32_t* __restrict__ freebits,
+                uint32_t* __restrict__ free_snap, int C, int32_t* status) {
+    const int b = blockIdx.x, tid = threadIdx.x;
+    int64_t base, n;
+    if (!request_range(tok_off, tok_end, n_tokens, b, &base, &n) && tid == 0) set_status(status, ECHO_ST_BADDATA);
+    uint32_t* ab = above + 4 * (base / 128 + b);
+    const int nw = static_cast<int>((n + 31) >> 5);
+    for (int w = tid; w < nw; w += kSeedThreads) ab[w] = 0u;
+    const int words = C / 32;
+    for (int w = tid; w < words; w += kSeedThreads)
+        free_snap[static_cast<int64_t>(b) * words + w] = freebits[static_cast<int64_t>(b) * words + w];
+    __syncthreads();
+    const int32_t* ps = prev_sel + static_cast<int64_t>(b) * m;
+    for (int i = tid; i < m; i += kSeedThreads) {
+        const int32_t t = ps[i];
+        if (t >= 0 && t < n && tok2slot[base + t] < 0) atomicOr(ab + (t >> 5), 1u << (t & 31));
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_recall(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens, int C, const int32_t* tok_list,
@@ -704,5 +733,23 @@ extern "C" int echo_early_fetch(int B, const int64_t* tok_off, const int64_t* to
                                     cache->early_tok, cache->early_slot,
                                     static_cast<const uint8_t*>(cache->host_kv), static_cast<uint8_t*>(cache->dev_kv),
                                     cache->row_bytes, status));
+    return ECHO_OK;
+}
+
+extern "C" int echo_seed_early(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens,
+                               const int32_t* prev_sel, int m, uint32_t* above, const echo_cache* cache,
+                               int32_t* status, echo_stream_t stream) {
+    using namespace echo;
+    if (B <= 0 || n_tokens < 0 || m < 0) return ECHO_EINVAL;
+    if (B > ECHO_MAX_REQUESTS) return ECHO_EUNSUPPORTED;
+    if (!tok_off || !prev_sel || !above || !status) return ECHO_EINVAL;
+    const int rc = check_cache(cache, B, 0);
+    if (rc) return rc;
+    if (!cache->free_snap) return ECHO_EINVAL;
+    if (n_tokens >= (1ll << 31)) return ECHO_EUNSUPPORTED;
+    seed_kernel<<<B, kSeedThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        tok_off, tok_end, n_tokens, prev_sel, m, above, cache->tok2slot, cache->freebits, cache->free_snap, cache->C,
+        status);
+    ECHO_CUDA_OK(cudaGetLastError());
     return ECHO_OK;
 }

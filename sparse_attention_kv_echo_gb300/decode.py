@@ -36,7 +36,8 @@ class DecodeLayer:
                  host_pool: torch.Tensor, alpha: float = 0.5, predictor: bool = True,
                  early_cap: int = -1, groups: int | None = None, first_share: float = 0.5,
                  resolved: bool = True, hold_early: bool = False, attention: bool = False,
-                 mla_scale: float = 1.0 / math.sqrt(192.0), tok_end=None, device="cuda"):
+                 mla_scale: float = 1.0 / math.sqrt(192.0), tok_end=None, cross_layer: bool = False,
+                 device="cuda"):
         tok_off = torch.as_tensor(tok_off, dtype=torch.int64)
         self.B = int(tok_off.numel() - 1)
         self.n_tokens = int(k8.shape[0])
@@ -68,6 +69,11 @@ class DecodeLayer:
         self.kth = torch.zeros((self.B,), **f32)
         # Requests are scored in groups (contiguous request ranges): the early fetch of group g
         # streams over the host link while group g+1 is scored, so the link starts sooner.
+        # cross_layer: this layer's early set comes from the previous layer's selection (seed_from),
+        # fetched before this layer scores; one request group
+        self.cross_layer = bool(cross_layer) and self.predictor
+        if self.cross_layer:
+            groups = 1
         if groups is None:
             groups = 2 if (self.predictor and self.B >= 2) else 1
         groups = max(1, min(int(groups), self.B))
@@ -101,6 +107,11 @@ class DecodeLayer:
         # low priority, so the early fetch of the group before is placed first
         lo, _ = torch.cuda.Stream.priority_range()
         self.gstreams = [torch.cuda.Stream(device=device, priority=lo) for _ in self.groups[1:]]
+        self.selected_evs = []     # after each group's top-k in the last enqueued step
+        if self.cross_layer:
+            self.above_seed = torch.zeros(max(L.above_words(self.B, self.n_tokens), 1), **i32)
+            self.xfer = torch.cuda.Stream(device=device)
+            self.seed_ev = None
 
     def reset(self):
         self.cache.reset()
@@ -108,8 +119,65 @@ class DecodeLayer:
         self.status.zero_()
         self.stats.zero_()
 
+    def seed_from(self, prev: "DecodeLayer"):
+        """Cross-layer early fetch of this layer from the previous layer's selection (enqueue after
+        prev.step and before this layer's step(seeded=True)): on this layer's transfer stream, after
+        prev's top-k, the seed kernel marks prev's selected tokens that are not resident here and
+        snapshots the free bits, and the early fetch streams their rows into this layer's cache
+        while this layer has not scored yet.  The caller orders the transfer stream after this
+        layer's previous step (DecodeStack forks it from the step's stream)."""
+        if not self.cross_layer:
+            raise ValueError("seed_from needs cross_layer=True")
+        x = self.xfer
+        for ev in prev.selected_evs:
+            x.wait_event(ev)
+        L.seed_early(self.tok_off, self.n_tokens, prev.sel_idx, self.above_seed, self.cache, self.status, stream=x,
+                     tok_end=self.tok_end)
+        self.seed_ev = torch.cuda.Event()
+        self.seed_ev.record(x)
+        L.early_fetch(self.tok_off, self.n_tokens, self.above_seed, self.early_cap, self.cache, self.status,
+                      stream=x, tok_end=self.tok_end)
+
+    def _step_seeded(self, q, w, main, out_host, mla_q):
+        # scores without threshold bits or snapshot; top-k and the cache step take the seeded set
+        L.quantize_q(q, w, self.q8, self.qscale, self.wfold, self.status, hist=self.hist, stream=main)
+        L.index_scores(self.tok_off, self.n_tokens, self.q8, self.wfold, self.k8, self.ks, self.scores, self.theta,
+                       self.hist, self.status, stream=main, tok_end=self.tok_end)
+        side = self.sides[0]
+        side.wait_stream(main)
+        if self.seed_ev is not None:
+            side.wait_event(self.seed_ev)
+        copy = side if self.hold_early else self.xfer
+        if self.resolved:
+            L.topk_select_cached(self.tok_off, self.n_tokens, self.scores, self.k, self.hist, self.theta, self.alpha,
+                                 self.sel_idx, self.kth, self.cache, self.sel_slot, self.status, stats=self.stats,
+                                 stream=side, above=self.above_seed, early_cap=self.early_cap, tok_end=self.tok_end)
+        else:
+            L.topk_select(self.tok_off, self.n_tokens, self.scores, self.k, self.hist, self.theta, self.alpha,
+                          self.sel_idx, self.kth, self.status, stats=self.stats, stream=side, tok_end=self.tok_end)
+        ev = torch.cuda.Event()
+        ev.record(side)
+        self.selected_evs = [ev]
+        if self.resolved:
+            L.cache_step_resolved(self.tok_off, self.n_tokens, self.sel_idx, self.cache, self.sel_slot, self.status,
+                                  stats=self.stats, stream=side, copy_stream=copy, hold_early=self.hold_early,
+                                  tok_end=self.tok_end)
+        else:
+            L.cache_step(self.tok_off, self.n_tokens, self.sel_idx, self.cache, self.sel_slot, self.status,
+                         stats=self.stats, stream=side, copy_stream=copy, above=self.above_seed,
+                         early_cap=self.early_cap, hold_early=self.hold_early, tok_end=self.tok_end)
+        if out_host is not None:
+            with torch.cuda.stream(side):
+                self._write_out(out_host, 0, self.B)
+        if self.attention:
+            copy.wait_stream(self.xfer)
+            copy.wait_stream(side)
+            self._attend(mla_q, 0, self.B, copy)
+        main.wait_stream(side)
+        main.wait_stream(self.xfer)
+
     def step(self, q: torch.Tensor | None = None, w: torch.Tensor | None = None, stream=None, out_host=None,
-             mla_q: torch.Tensor | None = None):
+             mla_q: torch.Tensor | None = None, seeded: bool = False):
         """Enqueue one decode step (q [B,64,128] f32, w [B,64] f32; defaults q_in / w_in; pinned
         host tensors are read by the quantiser directly).
 
@@ -120,12 +188,18 @@ class DecodeLayer:
         written there by a kernel as soon as its cache step is done, while the late misses
         are still being recalled.
         mla_q: with attention=True, the step's MLA queries [B,128,576] bf16 (default
-        self.mla_q); attn_out / attn_lse receive the attention of every request."""
+        self.mla_q); attn_out / attn_lse receive the attention of every request.
+        seeded: (cross_layer) the early set is the one seed_from enqueued for this step."""
         q = self.q_in if q is None else q
         if self.attention:
             mla_q = self.mla_q if mla_q is None else mla_q
         w = self.w_in if w is None else w
         main = torch.cuda.current_stream() if stream is None else stream
+        if seeded:
+            if not self.cross_layer:
+                raise ValueError("seeded steps need cross_layer=True")
+            self._step_seeded(q, w, main, out_host, mla_q)
+            return
         L.quantize_q(q, w, self.q8, self.qscale, self.wfold, self.status, hist=self.hist, stream=main)
         if not self.predictor:
             L.index_scores(self.tok_off, self.n_tokens, self.q8, self.wfold, self.k8, self.ks, self.scores,
@@ -164,6 +238,7 @@ class DecodeLayer:
         # done (a top-k started earlier would take SMs the next score kernel counts on); the late
         # misses of a group follow its early fetch on the group's stream (a slot fetched early and
         # then freed may go to a miss), or, holding those slots, its cache step on the side stream
+        self.selected_evs = []
         for g, (b0, b1) in enumerate(self.groups):
             side = self.sides[g]
             copy = side if self.hold_early else gstream[g]
@@ -175,6 +250,9 @@ class DecodeLayer:
                                      self.alpha, self.sel_idx[b0:b1], self.kth[b0:b1], self.views[g],
                                      self.sel_slot[b0:b1], self.status, stats=self.stats, stream=side,
                                      above=self.above_g[g], early_cap=self.early_cap, tok_end=end(b0, b1))
+                ev = torch.cuda.Event()
+                ev.record(side)
+                self.selected_evs.append(ev)
                 L.cache_step_resolved(off, self.n_tokens, self.sel_idx[b0:b1], self.views[g], self.sel_slot[b0:b1],
                                       self.status, stats=self.stats, stream=side, copy_stream=copy,
                                       hold_early=self.hold_early, tok_end=end(b0, b1))
@@ -182,6 +260,9 @@ class DecodeLayer:
                 L.topk_select(off, self.n_tokens, self.scores, self.k, self.hist[b0:b1], self.theta[b0:b1],
                               self.alpha, self.sel_idx[b0:b1], self.kth[b0:b1], self.status, stats=self.stats,
                               stream=side, tok_end=end(b0, b1))
+                ev = torch.cuda.Event()
+                ev.record(side)
+                self.selected_evs.append(ev)
                 L.cache_step(off, self.n_tokens, self.sel_idx[b0:b1], self.views[g], self.sel_slot[b0:b1],
                              self.status, stats=self.stats, stream=side, copy_stream=copy, above=self.above_g[g],
                              early_cap=self.early_cap, hold_early=self.hold_early, tok_end=end(b0, b1))
@@ -247,4 +328,33 @@ class DecodeLayer:
         att = 1 if self.attention else 0
         if not self.predictor:
             return 5 + att
+        if self.cross_layer:  # quantize, score, top-k, cache step, recall + seed, early fetch (seeded steps)
+            return 7 + att
         return 1 + (5 + att) * len(self.groups)
+
+
+class DecodeStack:
+    """Several layers of one decode step, in order.  cross_layer: every layer after the first
+    takes its early set from the layer before (DecodeLayer.seed_from): its rows stream while the
+    earlier layers finish and it scores.  The first layer keeps the threshold predictor."""
+
+    def __init__(self, layers: list[DecodeLayer], cross_layer: bool = False):
+        self.layers = layers
+        self.cross_layer = bool(cross_layer)
+        if self.cross_layer and not all(l.cross_layer for l in layers[1:]):
+            raise ValueError("layers after the first need cross_layer=True")
+
+    def step(self, qs, ws, stream=None):
+        """qs / ws: per layer the step's query [B,64,128] and weights [B,64] (f32)."""
+        main = torch.cuda.current_stream() if stream is None else stream
+        if self.cross_layer:  # the transfer streams follow everything before this step
+            for lay in self.layers[1:]:
+                lay.xfer.wait_stream(main)
+        for i, lay in enumerate(self.layers):
+            seeded = self.cross_layer and i > 0
+            if seeded:
+                lay.seed_from(self.layers[i - 1])
+            lay.step(qs[i], ws[i], stream=main, seeded=seeded)
+
+    def kernel_launches_per_step(self) -> int:
+        return sum(l.kernel_launches_per_step() for l in self.layers)

@@ -235,3 +235,95 @@ def run_decode_growing(w: wl.Workload, steps: int, room: int, hold_early: bool =
         assert np.array_equal(lay.cache.tok2slot.cpu().numpy(), o.t2s), (t, "append tok2slot")
         assert np.array_equal(lay.cache.slot2tok.cpu().numpy(), o.s2t), (t, "append slot2tok")
     return o_end - end
+
+
+def run_stack(w: wl.Workload, steps: int, n_layers: int, cross_layer: bool, hold_early: bool = False,
+              graph: bool = True):
+    """A DecodeStack of n_layers layers (each its own keys, weights, queries, host pool and cache),
+    optionally captured as one CUDA graph; every step of every layer is checked against the oracle:
+    layer 0's early set by the threshold predictor, the others' (cross_layer) from the previous
+    layer's selection.  Returns the per-layer early counts and misses per step."""
+    from sparse_attention_kv_echo_gb300 import DecodeStack
+    dev = "cuda"
+    off = wl.tok_offsets(w.lengths)
+    lays, inputs, qsrcs, hosts, orcs = [], [], [], [], []
+    for l in range(n_layers):
+        k8c, ksc = wl.make_keys(w, l)
+        wt = wl.make_weights(w, l)
+        host = wl.make_host_pool(w, l, pin=True)
+        lays.append(DecodeLayer(off, k8c.to(dev), ksc.to(dev), w.k, w.C, host, hold_early=hold_early,
+                                cross_layer=cross_layer and l > 0, device=dev))
+        inputs.append((k8c.numpy(), ksc.numpy(), wt.numpy()))
+        qsrcs.append(wl.QueryStream(w, l))
+        hosts.append(host.view(torch.uint8).numpy())
+        orcs.append(OracleLayer(w.B, w.total_tokens, w.C))
+    stack = DecodeStack(lays, cross_layer=cross_layer)
+    main = torch.cuda.Stream()
+    for l, lay in enumerate(lays):
+        with torch.cuda.stream(main):
+            lay.w_in.copy_(torch.from_numpy(inputs[l][2]).to(dev))
+    torch.cuda.synchronize()
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=main):
+            stack.step([lay.q_in for lay in lays], [lay.w_in for lay in lays], stream=main)
+        torch.cuda.synchronize()
+        for lay in lays:
+            lay.reset()
+        torch.cuda.synchronize()
+    rng = np.random.default_rng(11)
+    report = dict(early=[[] for _ in lays], misses=[[] for _ in lays])
+    for t in range(steps):
+        qs = [qsrcs[l].next().cpu() for l in range(n_layers)]
+        with torch.cuda.stream(main):
+            for l, lay in enumerate(lays):
+                lay.q_in.copy_(qs[l].to(dev))
+            if graph:
+                g.replay()
+            else:
+                stack.step([lay.q_in for lay in lays], [lay.w_in for lay in lays], stream=main)
+        torch.cuda.synchronize()
+        prev_sel = None   # the oracle's own selection of the layer before
+        for l, lay in enumerate(lays):
+            assert int(lay.status.item()) == 0, (t, l, "status")
+            o = orcs[l]
+            k8, ks, wt = inputs[l]
+            gs = lay.scores.cpu().numpy()
+            check_scores((off, k8, ks), qs[l].numpy(), wt, gs, sample=64, rng=rng)
+            g_sel, g_slot = lay.sel_idx.cpu().numpy(), lay.sel_slot.cpu().numpy()
+            g_ecnt = lay.cache.early_cnt.cpu().numpy()
+            g_etok, g_eslot = lay.cache.early_tok.cpu().numpy(), lay.cache.early_slot.cpu().numpy()
+            g_mcnt = lay.cache.miss_cnt.cpu().numpy()
+            theta_before = o.theta.copy()
+            misses = 0
+            o_sel = []
+            for b in range(w.B):
+                lo, hi = int(off[b]), int(off[b + 1])
+                sc = gs[lo:hi]
+                t2s = o.t2s[lo:hi]
+                s2t = o.s2t[b * w.C:(b + 1) * w.C]
+                if cross_layer and l > 0:
+                    et, es = orc.early_from_selection(prev_sel[b], hi - lo, lay.early_cap, t2s, s2t)
+                else:
+                    et, es = orc.early_fetch(sc, theta_before[b], lay.early_cap, t2s, s2t)
+                assert g_ecnt[b] == et.size, (t, l, b, "early count", g_ecnt[b], et.size)
+                assert np.array_equal(g_etok[b * w.C:b * w.C + et.size], et), (t, l, b, "early tok")
+                assert np.array_equal(g_eslot[b * w.C:b * w.C + et.size], es), (t, l, b, "early slot")
+                idx, kth = orc.topk(sc, w.k)
+                assert np.array_equal(g_sel[b], idx), (t, l, b, "topk")
+                o_sel.append(idx)
+                o.theta[b] = orc.ema(theta_before[b], kth, 0.5)
+                sel_slot, mt, ms, _ = orc.cache_step(idx, t2s, s2t, early_tok=et, hold_early=hold_early)
+                assert np.array_equal(g_slot[b], sel_slot), (t, l, b, "sel_slot")
+                assert g_mcnt[b] == mt.size, (t, l, b, "miss count")
+                misses += mt.size
+                report["early"][l].append(int(et.size))
+            report["misses"][l].append(misses)
+            assert np.array_equal(lay.cache.tok2slot.cpu().numpy(), o.t2s), (t, l, "tok2slot")
+            assert np.array_equal(lay.cache.slot2tok.cpu().numpy(), o.s2t), (t, l, "slot2tok")
+            g_dev = lay.cache.dev_kv.view(torch.uint8).cpu().numpy().reshape(w.B * w.C, -1)
+            for b in range(w.B):
+                v = g_slot[b] >= 0
+                assert np.array_equal(g_dev[b * w.C + g_slot[b][v]], hosts[l][off[b] + g_sel[b][v]]), (t, l, b)
+            prev_sel = o_sel
+    return report

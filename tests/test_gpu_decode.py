@@ -193,3 +193,19 @@ def test_host_io_graph_equals_eager():
         assert eager.status.item() == 0 and hio.status.item() == 0
     with pytest.raises(ValueError):
         hio.capture_host_step(q_host.to(dev), w_host, slot_host, kth_host)
+
+
+@pytest.mark.parametrize("hold_early", [False, True])
+def test_cross_layer_stack_in_one_graph(hold_early):
+    # three layers in one CUDA graph; layers 1 and 2 fetch early what the layer before selected
+    from tests._parity import run_stack
+    w = wl.scaled(wl.WORKLOADS["tiny"], "xlayer", B=2, lengths=(3000, 5000), k=256, C=1024)
+    rep = run_stack(w, steps=4, n_layers=3, cross_layer=True, hold_early=hold_early)
+    # the seeded layers fetch early every selected token of the layer before that is not resident
+    assert all(e > 0 for e in rep["early"][1][:2]) and all(e > 0 for e in rep["early"][2][:2])
+
+
+def test_threshold_stack_eager():
+    from tests._parity import run_stack
+    w = wl.scaled(wl.WORKLOADS["tiny"], "stack", B=2, lengths=(3000, 1200), k=256, C=1024)
+    run_stack(w, steps=3, n_layers=2, cross_layer=False, graph=False)
