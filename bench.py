@@ -59,10 +59,12 @@ def parse_args(argv=None):
                    help="where the selected tokens' slots are looked up (top-k's slices or the cache step)")
     p.add_argument("--hold-early", action="store_true",
                    help="the held-slot variant of the cache step (the late recall need not wait for the early copy)")
-    p.add_argument("--part", choices=["step", "mla", "append"], default="step",
+    p.add_argument("--part", choices=["step", "mla", "append", "layers"], default="step",
                    help="step: the decode step (default); mla: the sparse MLA attention over the selected "
                         "slots alone, at the step's batch, k and GPU slots; append: the append of one new "
-                        "token per request (key, host-pool row, cache slot) at the step's batch")
+                        "token per request (key, host-pool row, cache slot) at the step's batch; layers: "
+                        "a 4-layer step on layer-correlated inputs, threshold predictor against the "
+                        "cross-layer early fetch")
     p.add_argument("--first-share", type=float, default=None,
                    help="share of the requests in the first of two groups (default: the layer's choice)")
     return p.parse_args(argv)
@@ -657,10 +659,118 @@ def run_append(args):
     }), flush=True)
 
 
+LAYERS_METRIC = "decode steps/s, 4 layers (indexer+top-k+recall each), cross-layer early fetch"
+
+
+def run_layers(args):
+    """A 4-layer decode step (8 requests x 32768 tokens per layer, k = 2048, 4096 slots per request
+    and layer; keys and queries correlated 0.9 from layer to layer) as one CUDA graph, timed with
+    the threshold predictor on every layer and with layers 1-3 seeded from the layer before."""
+    import numpy as np
+    import torch
+    from sparse_attention_kv_echo_gb300 import DecodeLayer, DecodeStack
+    from sparse_attention_kv_echo_gb300 import _lib as L
+    from sparse_attention_kv_echo_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    L.load(build_if_missing=True)
+    w = wl.WORKLOADS["layers"]
+    off = wl.tok_offsets(w.lengths)
+    keys = [wl.make_keys(w, l, device=dev) for l in range(w.L)]
+    wts = [wl.make_weights(w, l, device=dev) for l in range(w.L)]
+    hosts = [wl.make_host_pool(w, l, device=dev, pin=True) for l in range(w.L)]
+    S = 16
+    qsrc = [wl.QueryStream(w, l, device=dev) for l in range(w.L)]
+    q_all = [torch.stack([qsrc[l].next() for _ in range(S)]) for l in range(w.L)]
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    main = torch.cuda.Stream()
+    # the rest of a transformer layer between two indexers, emulated by a spin of ~40 us (the page's
+    # 40-80 us window between an early layer's indexing and a later layer's attention)
+    gap_cycles = 80000
+
+    def spin(stream):
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(gap_cycles)
+
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        a.record(main)
+        spin(main)
+        b.record(main)
+    torch.cuda.synchronize()
+    gap_us = 1e3 * a.elapsed_time(b)
+
+    out = {}
+    for mode, gap in (("threshold", False), ("cross", False), ("threshold_gap", True), ("cross_gap", True)):
+        cross = mode.startswith("cross")
+        lays = [DecodeLayer(off, keys[l][0], keys[l][1], w.k, w.C, hosts[l], cross_layer=cross and l > 0, device=dev)
+                for l in range(w.L)]
+        stack = DecodeStack(lays, cross_layer=cross)
+        with torch.cuda.stream(main):
+            for l, lay in enumerate(lays):
+                lay.w_in.copy_(wts[l])
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=main):
+            stack.step([lay.q_in for lay in lays], [lay.w_in for lay in lays], stream=main,
+                       between=spin if gap else None)
+        torch.cuda.synchronize()
+        for lay in lays:
+            lay.reset()
+
+        def load_q(t):
+            for l, lay in enumerate(lays):
+                lay.q_in.copy_(q_all[l][t % S])
+
+        for t in range(args.warmup):
+            with torch.cuda.stream(main):
+                load_q(t)
+                g.replay()
+        torch.cuda.synchronize()
+        stats0 = [lay.stats.clone() for lay in lays]
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        park(main)
+        for i in range(args.steps):
+            with torch.cuda.stream(main):
+                load_q(args.warmup + i)
+                flush.zero_()
+                starts[i].record(main)
+                g.replay()
+                ends[i].record(main)
+        torch.cuda.synchronize()
+        ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+        st = [(lay.stats - s0).cpu().numpy().astype(np.int64) for lay, s0 in zip(lays, stats0)]
+        out[mode] = dict(
+            steps_s=round(args.steps / (sum(ms) / 1e3), 1), ms_per_step=round(statistics.mean(ms), 4),
+            early_per_layer=[round(float(x[L.STAT_EARLY]) / args.steps, 1) for x in st],
+            early_used_per_layer=[round(float(x[L.STAT_EARLY_USED]) / args.steps, 1) for x in st],
+            late_misses_per_layer=[round(float(x[L.STAT_MISSES]) / args.steps, 1) for x in st],
+            status=int(sum(int(lay.status.item()) for lay in lays)), launches=stack.kernel_launches_per_step())
+        del g, stack, lays
+        torch.cuda.synchronize()
+    print(json.dumps({
+        "metric": LAYERS_METRIC, "value": out["cross"]["steps_s"], "unit": "steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": out["cross"]["ms_per_step"],
+        "higher_is_better": True, "dtype": "fp8-e4m3 MMA, fp32 accumulate, int32 tables",
+        "data": "synthetic (seeded; layers correlated 0.9)",
+        "config": {"workload": f"{w.B} requests x {w.lengths[0]} tokens x {w.L} layers, k={w.k}, "
+                               f"{w.C} GPU slots/request/layer, keys and queries correlated 0.9 layer to layer",
+                   "l2": "flushed by a 256 MB write before every timed step", "cuda_graph": True},
+        "threshold": out["threshold"], "cross_layer": out["cross"],
+        "with_layer_gap": {"gap": f"{gap_us:.1f} us spin between layers ({gap_cycles} cycles)",
+                           "threshold": out["threshold_gap"], "cross_layer": out["cross_gap"]},
+    }), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.part == "layers":
+        run_layers(args)
     elif args.part == "append":
         run_append(args)
     elif args.part == "mla":

@@ -344,8 +344,10 @@ class DecodeStack:
         if self.cross_layer and not all(l.cross_layer for l in layers[1:]):
             raise ValueError("layers after the first need cross_layer=True")
 
-    def step(self, qs, ws, stream=None):
-        """qs / ws: per layer the step's query [B,64,128] and weights [B,64] (f32)."""
+    def step(self, qs, ws, stream=None, between=None):
+        """qs / ws: per layer the step's query [B,64,128] and weights [B,64] (f32).
+        between(stream): optional work enqueued on the step's stream after each layer but the last
+        (the rest of a transformer layer -- attention, MLP -- that separates two indexers)."""
         main = torch.cuda.current_stream() if stream is None else stream
         if self.cross_layer:  # the transfer streams follow everything before this step
             for lay in self.layers[1:]:
@@ -355,6 +357,8 @@ class DecodeStack:
             if seeded:
                 lay.seed_from(self.layers[i - 1])
             lay.step(qs[i], ws[i], stream=main, seeded=seeded)
+            if between is not None and i + 1 < len(self.layers):
+                between(main)
 
     def kernel_launches_per_step(self) -> int:
         return sum(l.kernel_launches_per_step() for l in self.layers)

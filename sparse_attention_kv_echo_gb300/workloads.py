@@ -14,6 +14,10 @@ Workloads (all seeded, seed 0 unless stated):
   prefill  1 x 102400-token prompt, 2048-row query blocks, k=2048 per row, 260000 slots
   skewed   64 requests, lengths log-uniform in [4096, 262144], 2 layers, k=2048,
            2560 slots/request, queries re-drawn every 8 steps, 96 steps
+  layers   8 x 32768, 4 layers whose keys and queries are correlated layer to layer
+           (rho = 0.9: layer l = rho * layer l-1 + sqrt(1 - rho^2) * fresh N(0,1)),
+           k=2048, 4096 slots/request/layer, 64 steps -- the shape the cross-layer
+           prefetch assumes (consecutive layers select mostly the same tokens)
 Queries q ~ N(0,1) [64,128] fp32 drift as q_t = 0.9 q_{t-1} + 0.44 eps_t; head
 weights w ~ U(0,1); host KV rows are 576 bf16 values ~ N(0,1) (1152 bytes).
 """
@@ -46,6 +50,7 @@ class Workload:
     predictor: bool = True
     prefill_block: int = 0      # > 0: chunked prefill with this many rows per block
     seed: int = 0
+    layer_rho: float = 0.0      # > 0: keys, queries and weights correlated from layer to layer
 
     @property
     def total_tokens(self) -> int:
@@ -61,6 +66,7 @@ def _skewed_lengths(B: int, seed: int) -> tuple:
 WORKLOADS = {
     "tiny": Workload("tiny", 1, 1, (8192,), 256, 1024, 16),
     "batch": Workload("batch", 8, 1, (32768,) * 8, 2048, 4096, 64),
+    "layers": Workload("layers", 8, 4, (32768,) * 8, 2048, 4096, 64, layer_rho=0.995),
     "v32": Workload("v32", 32, 4, (131072,) * 32, 2048, 8192, 128, hot_frac=0.05, hot_offset=2.0),
     "prefill": Workload("prefill", 1, 1, (102400,), 2048, 260000, 50, prefill_block=2048),
     "skewed": Workload("skewed", 64, 2, _skewed_lengths(64, 0), 2048, 2560, 96, drift="redraw8"),
@@ -96,8 +102,11 @@ def make_keys(w: Workload, layer: int, device="cpu"):
     rows = []
     scales = []
     for b, n in enumerate(w.lengths):
-        g = _gen(device, w.seed, 10_000 + 1000 * layer + b)
-        kf = torch.randn((n, D), generator=g, device=device, dtype=torch.float32)
+        if w.layer_rho > 0:
+            kf = _correlated((n, D), w, layer, 10_000 + b, device)
+        else:
+            g = _gen(device, w.seed, 10_000 + 1000 * layer + b)
+            kf = torch.randn((n, D), generator=g, device=device, dtype=torch.float32)
         if w.hot_frac > 0:
             nh = int(round(w.hot_frac * n))
             perm = torch.randperm(n, generator=g, device=device)[:nh]
@@ -111,9 +120,19 @@ def make_keys(w: Workload, layer: int, device="cpu"):
     return torch.cat(rows, 0).contiguous(), torch.cat(scales, 0).contiguous()
 
 
+def _correlated(shape, w: Workload, layer: int, sub: int, device) -> torch.Tensor:
+    """N(0,1) draws of `layer` that correlate rho with the same draws of layer - 1."""
+    x = torch.randn(shape, generator=_gen(device, w.seed, sub), device=device, dtype=torch.float32)
+    c = math.sqrt(1.0 - w.layer_rho ** 2)
+    for j in range(1, layer + 1):
+        z = torch.randn(shape, generator=_gen(device, w.seed, sub + 1000 * j), device=device, dtype=torch.float32)
+        x = w.layer_rho * x + c * z
+    return x
+
+
 def make_weights(w: Workload, layer: int, device="cpu") -> torch.Tensor:
-    """Per-head weights w ~ U(0,1), [B, 64] fp32."""
-    g = _gen(device, w.seed, 20_000 + layer)
+    """Per-head weights w ~ U(0,1), [B, 64] fp32 (the same for every layer when layer_rho > 0)."""
+    g = _gen(device, w.seed, 20_000 + (0 if w.layer_rho > 0 else layer))
     return torch.rand((w.B, H), generator=g, device=device, dtype=torch.float32)
 
 
@@ -126,10 +145,16 @@ class QueryStream:
         self.device = device
         self.t = 0
         self.q = torch.randn((w.B, H, D), generator=self.g, device=device, dtype=torch.float32)
+        # correlated layers: this layer's query = rho * the layer before's + sqrt(1 - rho^2) * its own
+        self.prev = None
+        if w.layer_rho > 0 and layer > 0:
+            self.prev = QueryStream(w, layer - 1, device)
 
     def next(self) -> torch.Tensor:
         """The query of the current step; advances the stream."""
         out = self.q.clone()
+        if self.prev is not None:
+            out = self.w.layer_rho * self.prev.next() + math.sqrt(1.0 - self.w.layer_rho ** 2) * out
         self.t += 1
         eps = torch.randn(self.q.shape, generator=self.g, device=self.device, dtype=torch.float32)
         if self.w.drift == "redraw8" and self.t % 8 == 0:
