@@ -226,7 +226,7 @@ def early_fetch(scores_f32, theta: float, cap: int, tok2slot, slot2tok):
 
 
 def early_from_selection(prev_sel, n: int, cap: int, tok2slot, slot2tok):
-    """Cross-layer early fetch (survey NEXT-4 reading): the previous layer's selection prev_sel
+    """Cross-layer early fetch (the layer-to-layer prefetch, as read here): the previous layer's selection prev_sel
     [m] (-1 padded) minus this layer's residents, ascending, <= min(cap, free).  Updates
     tok2slot [n] / slot2tok [C] (numpy int32, in place); -> (early_tok, early_slot)."""
     sel = _c(prev_sel, np.int32).reshape(-1)
@@ -282,7 +282,7 @@ def recall(host_rows, tok, slot, dev_rows):
 
 
 def append_tokens(tok_off, tok_end, k_new, kv_new, k8, ks, host_rows, C, tok2slot, slot2tok, dev_rows):
-    """One new token per request (survey NEXT-2 reading).  tok_off [B+1] int64 (regions),
+    """One new token per request (the offload write path, as read here).  tok_off [B+1] int64 (regions),
     tok_end [B] int64 (updated), k_new [B,D] f32, kv_new [B,row_bytes] u8; k8 [n,D] u8, ks [n]
     f32, host_rows [n,row_bytes] u8, tok2slot [n] / slot2tok [B*C] int32, dev_rows
     [B*C,row_bytes] u8 are updated in place.  -> full [B] int32 (1: region had no room)."""

@@ -353,7 +353,7 @@ int orc_early_fetch(int64_t n, int C, const float* scores, float theta, int cap,
     return ORC_OK;
 }
 
-// ---- cross-layer early fetch (survey NEXT-4) -------------------------------
+// ---- cross-layer early fetch ----------------------------------------------
 // Blog page "ECHO KV Cache Offloading ... Guide", section "Intra-Query
 // Prefetching: Layer-to-Layer Pipeline": the tokens that layer l selects are
 // mostly selected by layers l+1 and l+2 too, so the ones not yet resident for
@@ -469,7 +469,7 @@ void orc_recall(const uint8_t* host_rows, int64_t row_bytes, const int32_t* tok,
                     (size_t)row_bytes);
 }
 
-// ---- append: one new token per request (survey NEXT-2) ---------------------
+// ---- append: one new token per request ------------------------------------
 // EXPL section 2 ("One layer, one step"): the host holds every token, which is
 // why eviction needs no write-back; the pages give no append mechanics.
 // READING: request b's rows live in its region [tok_off[b], tok_off[b+1]) and
@@ -531,7 +531,7 @@ int orc_append_tokens(int B, const int64_t* tok_off, int64_t* tok_end, const flo
 }
 
 // ---- sparse MLA decode attention over the selected slots ------------------
-// The consumer of the cache (survey NEXT-1; EXPL section 2 names the sparse
+// The consumer of the cache (EXPL section 2 names the sparse
 // attention over the k selected tokens but gives no formula).  READING: MLA
 // in its absorbed form, one latent KV row of 576 bf16 per token (512 latent
 // + 64 rotary dims) shared by every query head; for head h over the valid
