@@ -401,7 +401,7 @@ int echo_mla_decode(int B, int k, const uint16_t* q, const int32_t* sel_slot, co
                     float scale, float* out, float* lse, int32_t* status, echo_stream_t stream);
 
 /*
- * Cross-layer early set [blog page "ECHO KV Cache Offloading ... Guide",
+ * Cross-layer early set [page "ECHO Guide: KV Offloading for Native Sparse Attention",
  * section "Intra-Query Prefetching: Layer-to-Layer Pipeline": layers l+1 and
  * l+2 select mostly what layer l selected; reading: layer l+1's early set is
  * layer l's selection minus layer l+1's residents].  Writes, for this layer's

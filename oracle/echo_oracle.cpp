@@ -354,7 +354,7 @@ int orc_early_fetch(int64_t n, int C, const float* scores, float theta, int cap,
 }
 
 // ---- cross-layer early fetch ----------------------------------------------
-// Blog page "ECHO KV Cache Offloading ... Guide", section "Intra-Query
+// Page "ECHO Guide: KV Offloading for Native Sparse Attention", section "Intra-Query
 // Prefetching: Layer-to-Layer Pipeline": the tokens that layer l selects are
 // mostly selected by layers l+1 and l+2 too, so the ones not yet resident for
 // layer l+1 are fetched as soon as layer l's selection is known.  READING: the
