@@ -419,6 +419,33 @@ int echo_seed_early(int B, const int64_t* tok_off, const int64_t* tok_end, int64
                     int m, uint32_t* above, const echo_cache* cache, int32_t* status, echo_stream_t stream);
 
 /*
+ * Shared per-worker pool [AE "Baselines under evaluation" and the decode
+ * server's NSA_DEV_CACHE_SIZE: one device pool of slots per layer for the
+ * worker's requests].  The pool is an echo_cache of one request spanning all
+ * n_tokens rows (tok_off = {0, n_tokens}, token ids global, C = pool slots);
+ * the early fetch, cache step and recall run on it unchanged.  Reading: the
+ * requests' early sets and misses take the pool's lowest free slots in
+ * (request, token) order.  A step: echo_index_scores per request with
+ * `above_req` and cache = NULL; echo_pool_above; echo_early_fetch(1,
+ * {0, n_tokens}, ..., above_pool, cap, pool); echo_topk_select per request;
+ * echo_pool_select; echo_cache_step(1, {0, n_tokens}, ..., sel_pool, B*k,
+ * above_pool, cap, pool, slot_pool, ...); echo_pool_slots.
+ *   echo_pool_above: above_pool [echo_above_words(1, n_tokens)] = the marks of
+ *     above_req [echo_above_words(B, n_tokens)] at global positions, tokens
+ *     resident in the pool left out; pool->free_snap = pool->freebits.
+ *   echo_pool_select: sel [B,k] (request-local, ascending, -1 padded) ->
+ *     sel_pool [B*k] (global ids tok_off[b] + sel, ascending, -1 padding last).
+ *   echo_pool_slots: slot_pool [B*k] (the pool step's sel_slot of sel_pool) ->
+ *     sel_slot [B,k] aligned with sel.
+ * Errors: ECHO_EINVAL (sizes, NULL pointers), ECHO_EUNSUPPORTED, cache errors.
+ */
+int echo_pool_above(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens, const uint32_t* above_req,
+                    const echo_cache* pool, uint32_t* above_pool, int32_t* status, echo_stream_t stream);
+int echo_pool_select(int B, const int64_t* tok_off, const int32_t* sel, int k, int32_t* sel_pool, echo_stream_t stream);
+int echo_pool_slots(int B, const int32_t* sel, int k, const int32_t* slot_pool, int32_t* sel_slot,
+                    echo_stream_t stream);
+
+/*
  * Append one new token to each request: the offload write path [EXPL section
  * 2, "One layer, one step": the host holds every token, hence no write-back
  * on eviction; the pages give no append mechanics -- reading below].

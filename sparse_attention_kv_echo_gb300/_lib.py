@@ -26,7 +26,8 @@ TOPK_CACHED_MAX_SLOTS = 32768  # C limit of echo_topk_select_cached
 EARLY_FETCH_BLOCKS = 32      # CTAs of the early-fetch and late-recall kernels
 
 EXPORTS = ("echo_above_words", "echo_append_tokens", "echo_cache_step", "echo_cache_step_resolved", "echo_device_sm_count",
-           "echo_early_fetch", "echo_host_device_alias", "echo_index_scores", "echo_mla_decode", "echo_prefill_block",
+           "echo_early_fetch", "echo_host_device_alias", "echo_index_scores", "echo_mla_decode", "echo_pool_above", "echo_pool_select",
+           "echo_pool_slots", "echo_prefill_block",
            "echo_prefill_block_static", "echo_prefill_scores", "echo_prefill_workspace_size", "echo_quantize_q", "echo_seed_early",
            "echo_topk_select", "echo_topk_select_cached")
 
@@ -83,6 +84,12 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
                                       _vp, _vp, _vp, _vp, i32]
         L.echo_mla_decode.restype = i32
         L.echo_mla_decode.argtypes = [i32, i32, _vp, _vp, _vp, i64, f32, _vp, _vp, _vp, _vp]
+        L.echo_pool_above.restype = i32
+        L.echo_pool_above.argtypes = [i32, _vp, _vp, i64, _vp, ctypes.POINTER(EchoCacheStruct), _vp, _vp, _vp]
+        L.echo_pool_select.restype = i32
+        L.echo_pool_select.argtypes = [i32, _vp, _vp, i32, _vp, _vp]
+        L.echo_pool_slots.restype = i32
+        L.echo_pool_slots.argtypes = [i32, _vp, i32, _vp, _vp, _vp]
         L.echo_seed_early.restype = i32
         L.echo_seed_early.argtypes = [i32, _vp, _vp, i64, _vp, i32, _vp, ctypes.POINTER(EchoCacheStruct), _vp, _vp]
         L.echo_append_tokens.restype = i32
@@ -240,6 +247,29 @@ def cache_step_resolved(tok_off, n_tokens, sel, cache, sel_slot, status, stats=N
     _check("echo_cache_step_resolved", load().echo_cache_step_resolved(
         B, _ptr(tok_off), _ptr(tok_end), int(n_tokens), _ptr(sel), int(m), ctypes.byref(cache.struct), _ptr(sel_slot),
         _ptr(status), _ptr(stats), st, cst, CACHE_HOLD_EARLY if hold_early else 0))
+
+
+def pool_above(tok_off, n_tokens, above_req, pool, above_pool, status, stream=None, tok_end=None):
+    """echo_pool_above: per-request above words -> the shared pool's global marks (residents left
+    out) and the pool's free-bit snapshot."""
+    B = tok_off.shape[0] - 1
+    _check("echo_pool_above", load().echo_pool_above(
+        B, _ptr(tok_off), _ptr(tok_end), int(n_tokens), _ptr(above_req), ctypes.byref(pool.struct),
+        _ptr(above_pool), _ptr(status), _stream(stream)))
+
+
+def pool_select(tok_off, sel, sel_pool, stream=None):
+    """echo_pool_select: sel [B,k] (request-local) -> sel_pool [B*k] (global, ascending, padding last)."""
+    B, k = sel.shape
+    _check("echo_pool_select", load().echo_pool_select(B, _ptr(tok_off), _ptr(sel), int(k), _ptr(sel_pool),
+                                                       _stream(stream)))
+
+
+def pool_slots(sel, slot_pool, sel_slot, stream=None):
+    """echo_pool_slots: the pool step's slots of sel_pool -> sel_slot [B,k] aligned with sel."""
+    B, k = sel.shape
+    _check("echo_pool_slots", load().echo_pool_slots(B, _ptr(sel), int(k), _ptr(slot_pool), _ptr(sel_slot),
+                                                     _stream(stream)))
 
 
 def seed_early(tok_off, n_tokens, prev_sel, above, cache, status, stream=None, tok_end=None):

@@ -37,7 +37,7 @@ class DecodeLayer:
                  early_cap: int = -1, groups: int | None = None, first_share: float = 0.5,
                  resolved: bool = True, hold_early: bool = False, attention: bool = False,
                  mla_scale: float = 1.0 / math.sqrt(192.0), tok_end=None, cross_layer: bool = False,
-                 device="cuda"):
+                 pool_slots: int = 0, device="cuda"):
         tok_off = torch.as_tensor(tok_off, dtype=torch.int64)
         self.B = int(tok_off.numel() - 1)
         self.n_tokens = int(k8.shape[0])
@@ -50,7 +50,8 @@ class DecodeLayer:
         # are placed, so the late recall need not wait for the early copy; the early set is then
         # capped at C - k on top of the caller's cap (selected tokens plus held slots within C)
         self.hold_early = bool(hold_early)
-        room = self.C - self.k
+        # (shared pool: the batch's selections and the held slots share the pool)
+        room = (int(pool_slots) - self.B * self.k) if pool_slots else (self.C - self.k)
         if self.hold_early and (early_cap < 0 or early_cap > room):
             early_cap = room
         self.early_cap = int(early_cap)
@@ -72,7 +73,12 @@ class DecodeLayer:
         # cross_layer: this layer's early set comes from the previous layer's selection (seed_from),
         # fetched before this layer scores; one request group
         self.cross_layer = bool(cross_layer) and self.predictor
-        if self.cross_layer:
+        # pool_slots > 0: one cache pool of that many slots shared by every request (the worker's
+        # device cache) instead of C slots per request; one request group
+        self.pool_slots = int(pool_slots)
+        if self.pool_slots and (cross_layer or attention):
+            raise ValueError("the shared pool goes with neither cross_layer nor attention")
+        if self.cross_layer or self.pool_slots:
             groups = 1
         if groups is None:
             groups = 2 if (self.predictor and self.B >= 2) else 1
@@ -91,7 +97,17 @@ class DecodeLayer:
         self.stats = torch.zeros(L.STATS_N, **i32)
         self.q_in = torch.zeros((self.B, L.HEADS, L.DIM), **f32)
         self.w_in = torch.zeros((self.B, L.HEADS), **f32)
-        self.cache = L.LayerCache(self.B, self.n_tokens, self.C, host_pool, device=device)
+        if self.pool_slots:
+            # the pool is the cache of one request spanning every row: token ids are global
+            self.cache = L.LayerCache(1, self.n_tokens, self.pool_slots, host_pool, device=device)
+            self.tok_off_pool = torch.tensor([0, self.n_tokens], dtype=torch.int64, device=device)
+            self.above_req = torch.zeros(max(L.above_words(self.B, self.n_tokens), 1), **i32)
+            self.above_pool = torch.zeros(max(L.above_words(1, self.n_tokens), 1), **i32)
+            self.sel_pool = torch.full((1, self.B * self.k), -1, **i32)
+            self.slot_pool = torch.full((1, self.B * self.k), -1, **i32)
+            self.resolved = False
+        else:
+            self.cache = L.LayerCache(self.B, self.n_tokens, self.C, host_pool, device=device)
         # sparse MLA attention over the selected slots (the cache rows are its 576-dim KV rows)
         self.attention, self.mla_scale = bool(attention), float(mla_scale)
         if self.attention:
@@ -100,7 +116,7 @@ class DecodeLayer:
             self.mla_q = torch.zeros((self.B, L.MLA_HEADS, L.MLA_DQK), dtype=torch.bfloat16, device=device)
             self.attn_out = torch.zeros((self.B, L.MLA_HEADS, L.MLA_DV), **f32)
             self.attn_lse = torch.zeros((self.B, L.MLA_HEADS), **f32)
-        self.views = [self.cache.view(b0, b1) for b0, b1 in self.groups]
+        self.views = [] if self.pool_slots else [self.cache.view(b0, b1) for b0, b1 in self.groups]
         self.sides = [torch.cuda.Stream(device=device) for _ in self.groups]
         self.side = self.sides[0]
         # scoring streams of the groups after the first (the first uses the step's stream);
@@ -137,6 +153,34 @@ class DecodeLayer:
         self.seed_ev.record(x)
         L.early_fetch(self.tok_off, self.n_tokens, self.above_seed, self.early_cap, self.cache, self.status,
                       stream=x, tok_end=self.tok_end)
+
+    def _step_pool(self, q, w, main, out_host):
+        # per-request scores and marks; the early fetch, top-k's slots and the cache step on the pool
+        n, end = self.n_tokens, self.tok_end
+        L.quantize_q(q, w, self.q8, self.qscale, self.wfold, self.status, hist=self.hist, stream=main)
+        L.index_scores(self.tok_off, n, self.q8, self.wfold, self.k8, self.ks, self.scores, self.theta, self.hist,
+                       self.status, above=self.above_req if self.predictor else None, stream=main, tok_end=end)
+        if self.predictor:
+            L.pool_above(self.tok_off, n, self.above_req, self.cache, self.above_pool, self.status, stream=main,
+                         tok_end=end)
+            L.early_fetch(self.tok_off_pool, n, self.above_pool, self.early_cap, self.cache, self.status, stream=main)
+        side = self.sides[0]
+        side.wait_stream(main)
+        copy = side if self.hold_early else main
+        L.topk_select(self.tok_off, n, self.scores, self.k, self.hist, self.theta, self.alpha, self.sel_idx, self.kth,
+                      self.status, stats=self.stats, stream=side, tok_end=end)
+        ev = torch.cuda.Event()
+        ev.record(side)
+        self.selected_evs = [ev]
+        L.pool_select(self.tok_off, self.sel_idx, self.sel_pool, stream=side)
+        L.cache_step(self.tok_off_pool, n, self.sel_pool, self.cache, self.slot_pool, self.status, stats=self.stats,
+                     stream=side, copy_stream=copy, above=self.above_pool if self.predictor else None,
+                     early_cap=self.early_cap if self.predictor else 0, hold_early=self.hold_early)
+        L.pool_slots(self.sel_idx, self.slot_pool, self.sel_slot, stream=side)
+        if out_host is not None:
+            with torch.cuda.stream(side):
+                self._write_out(out_host, 0, self.B)
+        main.wait_stream(side)
 
     def _step_seeded(self, q, w, main, out_host, mla_q):
         # scores without threshold bits or snapshot; top-k and the cache step take the seeded set
@@ -195,6 +239,9 @@ class DecodeLayer:
             mla_q = self.mla_q if mla_q is None else mla_q
         w = self.w_in if w is None else w
         main = torch.cuda.current_stream() if stream is None else stream
+        if self.pool_slots:
+            self._step_pool(q, w, main, out_host)
+            return
         if seeded:
             if not self.cross_layer:
                 raise ValueError("seeded steps need cross_layer=True")
@@ -326,6 +373,8 @@ class DecodeLayer:
     def kernel_launches_per_step(self) -> int:
         # quantize, then per group: score (+ early fetch) + top-k + cache step + late recall
         att = 1 if self.attention else 0
+        if self.pool_slots:  # quantize, score, top-k, select, cache step, recall, slots (+ marks, early fetch)
+            return 7 + (2 if self.predictor else 0)
         if not self.predictor:
             return 5 + att
         if self.cross_layer:  # quantize, score, top-k, cache step, recall + seed, early fetch (seeded steps)

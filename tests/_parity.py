@@ -327,3 +327,90 @@ def run_stack(w: wl.Workload, steps: int, n_layers: int, cross_layer: bool, hold
                 assert np.array_equal(g_dev[b * w.C + g_slot[b][v]], hosts[l][off[b] + g_sel[b][v]]), (t, l, b)
             prev_sel = o_sel
     return report
+
+
+def run_pool(w: wl.Workload, steps: int, pool: int, hold_early: bool = False, predictor: bool = True,
+             graph: bool = True, cap: int = -1):
+    """Decode steps with one cache pool of `pool` slots shared by the batch's requests, checked
+    against the oracle's own pool (a cache of one request over every row, token ids global): the
+    early set (the requests' marked, non-resident tokens in (request, token) order), top-k per
+    request, the pool step on the batch's selection in (request, token) order, tables, rows."""
+    dev = "cuda"
+    off = wl.tok_offsets(w.lengths)
+    n = w.total_tokens
+    k8c, ksc = wl.make_keys(w, 0)
+    wt = wl.make_weights(w, 0)
+    host = wl.make_host_pool(w, 0, pin=True)
+    lay = DecodeLayer(off, k8c.to(dev), ksc.to(dev), w.k, w.C, host, predictor=predictor, hold_early=hold_early,
+                      early_cap=cap, pool_slots=pool, device=dev)
+    k8, ks, wn = k8c.numpy(), ksc.numpy(), wt.numpy()
+    hb = host.view(torch.uint8).numpy()
+    t2s = np.full(n, -1, np.int32)
+    s2t = np.full(pool, -1, np.int32)
+    theta = np.full(w.B, np.inf, np.float32)
+    qsrc = wl.QueryStream(w, 0)
+    main = torch.cuda.Stream()
+    with torch.cuda.stream(main):
+        lay.w_in.copy_(wt.to(dev))
+    torch.cuda.synchronize()
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=main):
+            lay.step(stream=main)
+        torch.cuda.synchronize()
+        lay.reset()
+        torch.cuda.synchronize()
+    rng = np.random.default_rng(3)
+    report = dict(early=[], misses=[])
+    for t in range(steps):
+        q = qsrc.next().cpu()
+        with torch.cuda.stream(main):
+            lay.q_in.copy_(q.to(dev))
+            if graph:
+                g.replay()
+            else:
+                lay.step(stream=main)
+        torch.cuda.synchronize()
+        assert int(lay.status.item()) == 0, (t, "status")
+        gs = lay.scores.cpu().numpy()
+        check_scores((off, k8, ks), q.numpy(), wn, gs, sample=64, rng=rng)
+        # the early set: every request's tokens above its threshold, not in the pool, in global order
+        marked = []
+        for b in range(w.B):
+            lo, hi = int(off[b]), int(off[b + 1])
+            if predictor and np.isfinite(theta[b]):
+                s = np.nonzero(gs[lo:hi] > theta[b])[0] + lo
+                marked.extend(int(x) for x in s if t2s[x] < 0)
+        et, es = orc.early_from_selection(np.array(marked, np.int32), n, lay.early_cap, t2s, s2t)
+        if predictor:
+            g_cnt = int(lay.cache.early_cnt.cpu().numpy()[0])
+            assert g_cnt == et.size, (t, "early count", g_cnt, et.size)
+            assert np.array_equal(lay.cache.early_tok.cpu().numpy()[:g_cnt], et), (t, "early tok")
+            assert np.array_equal(lay.cache.early_slot.cpu().numpy()[:g_cnt], es), (t, "early slot")
+        g_sel, g_slot = lay.sel_idx.cpu().numpy(), lay.sel_slot.cpu().numpy()
+        glob, counts = [], []
+        for b in range(w.B):
+            lo, hi = int(off[b]), int(off[b + 1])
+            idx, kth = orc.topk(gs[lo:hi], w.k)
+            assert np.array_equal(g_sel[b], idx), (t, b, "topk")
+            theta[b] = orc.ema(theta[b], kth, 0.5)
+            v = idx[idx >= 0]
+            glob.extend(int(x) + lo for x in v)
+            counts.append(v.size)
+        sel_g = np.full(w.B * w.k, -1, np.int32)
+        sel_g[:len(glob)] = glob
+        sl_g, mt, ms, _ = orc.cache_step(sel_g, t2s, s2t, early_tok=et, hold_early=hold_early)
+        pos = 0
+        for b in range(w.B):
+            want = np.full(w.k, -1, np.int32)
+            want[:counts[b]] = sl_g[pos:pos + counts[b]]
+            pos += counts[b]
+            assert np.array_equal(g_slot[b], want), (t, b, "sel_slot")
+        assert np.array_equal(lay.cache.tok2slot.cpu().numpy(), t2s), (t, "pool tok2slot")
+        assert np.array_equal(lay.cache.slot2tok.cpu().numpy(), s2t), (t, "pool slot2tok")
+        g_dev = lay.cache.dev_kv.view(torch.uint8).cpu().numpy()
+        valid = sel_g >= 0
+        assert np.array_equal(g_dev[sl_g[valid]], hb[sel_g[valid]]), (t, "rows")
+        report["early"].append(int(et.size))
+        report["misses"].append(int(mt.size))
+    return report

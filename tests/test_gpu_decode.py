@@ -209,3 +209,21 @@ def test_threshold_stack_eager():
     from tests._parity import run_stack
     w = wl.scaled(wl.WORKLOADS["tiny"], "stack", B=2, lengths=(3000, 1200), k=256, C=1024)
     run_stack(w, steps=3, n_layers=2, cross_layer=False, graph=False)
+
+
+@pytest.mark.parametrize("hold_early", [False, True])
+def test_shared_pool_in_one_graph(hold_early):
+    # one pool of slots shared by the batch's requests; the pool smaller than B x C would be
+    from tests._parity import run_pool
+    w = wl.scaled(wl.WORKLOADS["batch"], "pool", B=3, lengths=(9000, 2000, 6000), k=512, C=1024)
+    rep = run_pool(w, steps=5, pool=2048, hold_early=hold_early)
+    assert sum(rep["early"]) > 0 and sum(rep["misses"]) > 0
+
+
+def test_shared_pool_large_predictor_off_and_cap():
+    # a pool above 2^17 slots (the walking cache step), predictor off; then a capped early set
+    from tests._parity import run_pool
+    w = wl.scaled(wl.WORKLOADS["batch"], "pool_big", B=2, lengths=(70000, 65000), k=2048, C=4096)
+    run_pool(w, steps=3, pool=140032, predictor=False, graph=False)
+    w2 = wl.scaled(wl.WORKLOADS["batch"], "pool_cap", B=2, lengths=(8000, 5000), k=256, C=1024)
+    run_pool(w2, steps=4, pool=1024, cap=100)
