@@ -59,12 +59,13 @@ def parse_args(argv=None):
                    help="where the selected tokens' slots are looked up (top-k's slices or the cache step)")
     p.add_argument("--hold-early", action="store_true",
                    help="the held-slot variant of the cache step (the late recall need not wait for the early copy)")
-    p.add_argument("--part", choices=["step", "mla", "append", "layers"], default="step",
+    p.add_argument("--part", choices=["step", "mla", "append", "layers", "pool"], default="step",
                    help="step: the decode step (default); mla: the sparse MLA attention over the selected "
                         "slots alone, at the step's batch, k and GPU slots; append: the append of one new "
                         "token per request (key, host-pool row, cache slot) at the step's batch; layers: "
                         "a 4-layer step on layer-correlated inputs, threshold predictor against the "
-                        "cross-layer early fetch")
+                        "cross-layer early fetch; pool: the decode step with one cache pool shared by the "
+                        "batch (B x C slots, and 260000) against per-request slot ranges")
     p.add_argument("--first-share", type=float, default=None,
                    help="share of the requests in the first of two groups (default: the layer's choice)")
     return p.parse_args(argv)
@@ -765,10 +766,86 @@ def run_layers(args):
     }), flush=True)
 
 
+POOL_METRIC = "decode steps/s (indexer+top-k+recall per layer), one cache pool shared by the batch"
+
+
+def run_pool(args):
+    """The decode step of the batch workload (8 x 32768 tokens, k = 2048) with its cache as one pool
+    shared by the requests -- 8 x 4096 slots (the per-request capacity in total) and the decode
+    server's 260000 -- against the per-request slot ranges (4096 each), each as one CUDA graph per
+    query, L2 flushed before every timed step."""
+    import numpy as np
+    import torch
+    from sparse_attention_kv_echo_gb300 import DecodeLayer
+    from sparse_attention_kv_echo_gb300 import _lib as L
+    from sparse_attention_kv_echo_gb300 import workloads as wl
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    L.load(build_if_missing=True)
+    w = wl.WORKLOADS["batch"]
+    off = wl.tok_offsets(w.lengths)
+    k8, ks = wl.make_keys(w, 0, device=dev)
+    wt = wl.make_weights(w, 0, device=dev)
+    host = wl.make_host_pool(w, 0, device=dev, pin=True)
+    S = 16
+    qsrc = wl.QueryStream(w, 0, device=dev)
+    q_all = torch.stack([qsrc.next() for _ in range(S)])
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    main = torch.cuda.Stream()
+    out = {}
+    for name, pool in (("per_request", 0), ("pool_32768", w.B * w.C), ("pool_260000", 260000)):
+        lay = DecodeLayer(off, k8, ks, w.k, w.C, host, pool_slots=pool, groups=1 if pool else None, device=dev)
+        with torch.cuda.stream(main):
+            lay.w_in.copy_(wt)
+        torch.cuda.synchronize()
+        graphs = []
+        for i in range(S):
+            gi = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gi, stream=main):
+                lay.step(q_all[i], stream=main)
+            graphs.append(gi)
+        torch.cuda.synchronize()
+        lay.reset()
+        for i in range(max(S, args.warmup)):
+            with torch.cuda.stream(main):
+                graphs[i % S].replay()
+        torch.cuda.synchronize()
+        stats0 = lay.stats.clone()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        park(main)
+        for i in range(args.steps):
+            with torch.cuda.stream(main):
+                flush.zero_()
+                starts[i].record(main)
+                graphs[i % S].replay()
+                ends[i].record(main)
+        torch.cuda.synchronize()
+        ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+        st = (lay.stats - stats0).cpu().numpy().astype(np.int64)
+        out[name] = dict(steps_s=round(args.steps / (sum(ms) / 1e3), 1), ms_per_step=round(statistics.mean(ms), 4),
+                         early_per_step=round(float(st[L.STAT_EARLY]) / args.steps, 1),
+                         late_misses_per_step=round(float(st[L.STAT_MISSES]) / args.steps, 1),
+                         status=int(lay.status.item()), launches=lay.kernel_launches_per_step())
+        del graphs, lay
+        torch.cuda.synchronize()
+    print(json.dumps({
+        "metric": POOL_METRIC, "value": out["pool_32768"]["steps_s"], "unit": "steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": out["pool_32768"]["ms_per_step"],
+        "higher_is_better": True, "dtype": "fp8-e4m3 MMA, fp32 accumulate, int32 tables", "data": "synthetic (seeded)",
+        "config": dict(workload_config(w), l2="flushed by a 256 MB write before every timed step"),
+        "per_request_slots": out["per_request"], "pool_32768": out["pool_32768"], "pool_260000": out["pool_260000"],
+    }), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.part == "pool":
+        run_pool(args)
     elif args.part == "layers":
         run_layers(args)
     elif args.part == "append":

@@ -24,6 +24,7 @@ namespace echo {
 namespace {
 
 constexpr int kPT = 256;
+constexpr int kPer = 4;  // selection entries per thread of the mapping kernel
 
 __global__ void __launch_bounds__(kPT)
     pool_above_kernel(int B, const int64_t* __restrict__ tok_off, const int64_t* __restrict__ tok_end, int64_t n_tokens,
@@ -84,8 +85,10 @@ __device__ __forceinline__ void pool_offsets(int B, const int32_t* sel, int k, i
     __syncthreads();
 }
 
-// One block: sel [B, k] (request-local) -> sel_pool [B * k] (global, ascending,
-// padding last); or, with to_req, slot_pool [B * k] -> sel_slot [B, k].
+// sel [B, k] (request-local) -> sel_pool [B * k] (global, ascending, padding
+// last); or, with to_req, slot_pool [B * k] -> sel_slot [B, k].  Every block
+// scans the requests' counts (B binary searches), then maps its kPT * kPer
+// entries.
 __global__ void __launch_bounds__(kPT)
     pool_map_kernel(int B, const int64_t* __restrict__ tok_off, const int32_t* __restrict__ sel, int k, bool to_req,
                     int32_t* __restrict__ pool_list, int32_t* __restrict__ sel_slot) {
@@ -93,7 +96,9 @@ __global__ void __launch_bounds__(kPT)
     __shared__ uint32_t scan[kPT / 32 + 1];
     pool_offsets(B, sel, k, s_off, scan);
     const int64_t total = static_cast<int64_t>(B) * k;
-    for (int64_t i = threadIdx.x; i < total; i += kPT) {
+    const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kPT * kPer;
+    const int64_t i1 = min(total, i0 + static_cast<int64_t>(kPT) * kPer);
+    for (int64_t i = i0 + threadIdx.x; i < i1; i += kPT) {
         const int b = static_cast<int>(i / k), j = static_cast<int>(i - static_cast<int64_t>(b) * k);
         const int cnt = s_off[b + 1] - s_off[b];
         if (!to_req) {
@@ -133,8 +138,9 @@ extern "C" int echo_pool_select(int B, const int64_t* tok_off, const int32_t* se
     if (B <= 0 || k <= 0) return ECHO_EINVAL;
     if (B > ECHO_MAX_REQUESTS) return ECHO_EUNSUPPORTED;
     if (!tok_off || !sel || !sel_pool) return ECHO_EINVAL;
-    pool_map_kernel<<<1, kPT, (B + 1) * sizeof(int32_t), static_cast<cudaStream_t>(stream)>>>(B, tok_off, sel, k, false,
-                                                                                              sel_pool, nullptr);
+    const int blocks = static_cast<int>((static_cast<int64_t>(B) * k + kPT * kPer - 1) / (kPT * kPer));
+    pool_map_kernel<<<blocks, kPT, (B + 1) * sizeof(int32_t), static_cast<cudaStream_t>(stream)>>>(
+        B, tok_off, sel, k, false, sel_pool, nullptr);
     ECHO_CUDA_OK(cudaGetLastError());
     return ECHO_OK;
 }
@@ -145,7 +151,8 @@ extern "C" int echo_pool_slots(int B, const int32_t* sel, int k, const int32_t* 
     if (B <= 0 || k <= 0) return ECHO_EINVAL;
     if (B > ECHO_MAX_REQUESTS) return ECHO_EUNSUPPORTED;
     if (!sel || !slot_pool || !sel_slot) return ECHO_EINVAL;
-    pool_map_kernel<<<1, kPT, (B + 1) * sizeof(int32_t), static_cast<cudaStream_t>(stream)>>>(
+    const int blocks = static_cast<int>((static_cast<int64_t>(B) * k + kPT * kPer - 1) / (kPT * kPer));
+    pool_map_kernel<<<blocks, kPT, (B + 1) * sizeof(int32_t), static_cast<cudaStream_t>(stream)>>>(
         B, nullptr, sel, k, true, const_cast<int32_t*>(slot_pool), sel_slot);
     ECHO_CUDA_OK(cudaGetLastError());
     return ECHO_OK;
