@@ -332,6 +332,10 @@ class DecodeLayer:
         free, in the cache; tok_end advances (a full region sets ECHO_ST_FULL).  Needs tok_end."""
         if self.tok_end is None:
             raise ValueError("append needs growing contexts (tok_end)")
+        if self.pool_slots:
+            # echo_append_tokens places each request in its own slot range; a shared pool would
+            # need one allocation across the requests
+            raise ValueError("append goes with per-request slot ranges, not the shared pool")
         main = torch.cuda.current_stream() if stream is None else stream
         L.append_tokens(self.tok_off, self.tok_end, self.n_tokens, k_new, kv_new, self.k8, self.ks, self.cache,
                         self.status, stream=main)

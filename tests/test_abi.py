@@ -144,3 +144,24 @@ def test_append_argument_checks(L):
     assert L.echo_append_tokens(1, d, None, 10, d, d, d, d, None, d, None) == lib.ECHO_EINVAL
     assert L.echo_append_tokens(1, d, d, 10, d, d, d, d, None, d, None) == lib.ECHO_EINVAL   # no cache
     assert L.echo_append_tokens(lib.MAX_REQUESTS + 1, d, d, 10, d, d, d, d, None, d, None) == lib.ECHO_EUNSUPPORTED
+
+
+def test_pool_argument_checks(L):
+    """echo_pool_above / echo_pool_select / echo_pool_slots refuse bad arguments before any launch."""
+    from sparse_attention_kv_echo_gb300 import lib
+    d = ctypes.c_void_p(0x1000)
+    assert L.echo_pool_above(0, d, None, 10, d, None, d, d, None) == lib.ECHO_EINVAL
+    assert L.echo_pool_above(1, d, None, 10, d, None, d, d, None) == lib.ECHO_EINVAL      # no pool
+    assert L.echo_pool_select(1, None, d, 8, d, None) == lib.ECHO_EINVAL
+    assert L.echo_pool_select(1, d, d, 0, d, None) == lib.ECHO_EINVAL
+    assert L.echo_pool_slots(lib.MAX_REQUESTS + 1, d, 8, d, d, None) == lib.ECHO_EUNSUPPORTED
+    assert L.echo_seed_early(1, d, None, 10, None, 8, d, None, d, None) == lib.ECHO_EINVAL
+
+
+def test_pool_layer_refuses_append():
+    import torch
+    from sparse_attention_kv_echo_gb300 import DecodeLayer
+    lay = DecodeLayer.__new__(DecodeLayer)
+    lay.tok_end, lay.pool_slots = torch.zeros(1, dtype=torch.int64), 64
+    with pytest.raises(ValueError):
+        lay.append(torch.zeros((1, 128)), torch.zeros((1, 576)))
