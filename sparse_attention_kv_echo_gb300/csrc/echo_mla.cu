@@ -9,12 +9,17 @@
 //   s_t = scale * q[h] . kv[slot_t]   (576 dims),   out[h] = softmax(s) . kv[slot_t][0:512].
 //
 // CTA (request b, output half, split of the selection) takes the 128 heads and
-// the split's tokens, 32 at a time, in a two-stage pipeline (the gather of the
-// next tile is in flight while this one is computed):
+// the split's tokens, 32 at a time, through a four-stage ring of gathered tiles
+// (three tiles in flight while one is computed).  Warps 0-3 (thread = head =
+// TMEM lane) gather the tiles and run the softmax; warp 4 issues every MMA, so
+// the next tile's S runs on the tensor pipe while this tile's softmax runs;
+// mbarriers carry the hand-offs (tile landed, S done, P written, P.V done):
 //   S = Q K^T   tcgen05.mma kind::f16 (bf16 in, fp32 in TMEM, two S buffers),
-//               M = 128 heads, N = 32 tokens, K = 576 in 36 steps; Q stays in
-//               shared memory (128-byte swizzle, K-major), the gathered KV rows
-//               of the tile (same layout, a row per token) are B;
+//               M = 128 heads, N = 32 tokens, K = 576 in 36 steps; Q is the A
+//               operand from TMEM for its first 384 dims (two bf16 per column,
+//               lane = head) and from shared memory for the last 192 (128-byte
+//               swizzle, K-major), which keeps shared memory for the ring; the
+//               gathered KV rows of the tile (same layout, a row per token) are B;
 //   softmax     one thread per head reads its S row from TMEM and keeps a
 //               running reference max and sum in fp32.  The reference moves
 //               only when a score exceeds it by more than 2^8 (P <= 256 in
@@ -47,21 +52,27 @@ constexpr int kRowBytes = kDqk * 2;         // 1152
 constexpr int kTok = 32;                    // tokens per tile
 constexpr int kMaxSplits = ECHO_MLA_MAX_SPLITS;      // 8: CTAs of one cluster
 constexpr int kSplitMax = ECHO_MLA_MAX_K / ECHO_MLA_MAX_SPLITS;  // 1024: most tokens per split
-constexpr int kThreads = 128;               // one thread per head
+constexpr int kThreads = 160;               // warps 0-3: one thread per head; warp 4: the MMAs
+constexpr int kHeadThreads = 128;
 constexpr int kAtoms = kDqk / 64;           // 9 swizzle atoms of 64 bf16 along the 576 dims
 constexpr int kChunks = kRowBytes / 16;     // 72 16-byte pieces per row
-constexpr uint32_t kQBytes = kAtoms * kHeads * 128;   // Q: 9 x (128 rows x 128 B)
+constexpr int kQTmemAtoms = 6;              // Q atoms 0..5 in TMEM (192 columns), 6..8 in shared memory
+constexpr uint32_t kQBytes = (kAtoms - kQTmemAtoms) * kHeads * 128;   // Q in shared memory: 3 x (128 rows x 128 B)
 constexpr uint32_t kAtomBytes = kTok * 128;           // one atom of a tile: 32 rows x 128 B
 constexpr uint32_t kKBytes = kAtoms * kAtomBytes;     // a tile: 9 atoms
-constexpr int kStages = 2;
-constexpr uint32_t kTmemCols = 512;                   // S0 [0, 32) | S1 [32, 64) | O [64, 320)
-constexpr uint32_t kOCol = 64;
+constexpr int kStages = 4;
+constexpr uint32_t kTmemCols = 512;                   // Q [0, 192) | S0 [192, 224) | S1 [224, 256) | O [256, 512)
+constexpr uint32_t kSCol = kQTmemAtoms * 32;
+constexpr uint32_t kOCol = kSCol + 2 * kTok;
+static_assert(kOCol + 256 <= kTmemCols, "TMEM columns");
 constexpr float kLazy = 8.f;                          // log2 headroom before the reference max moves
 constexpr uint64_t kMlaWaitNs = 100000000ull;         // 0.1 s: a tile's MMA takes microseconds
 
 struct MlaCtl {
-    uint64_t s_bar;      // S MMA of the tile done
-    uint64_t pv_bar;     // PV MMA of the tile done
+    uint64_t tile_full[4];  // a stage's tile landed (one arrival per head thread's copies)
+    uint64_t s_full[2];     // S of a tile done (per S buffer)
+    uint64_t p_full[2];     // P of a tile written, O rescaled (one arrival per head thread)
+    uint64_t pv_done[2];    // P.V of a tile done
     uint32_t tmem;       // TMEM base address
     int abort;
     uint32_t valid[kStages];  // tokens of the staged tile with a slot (bit t)
@@ -73,7 +84,7 @@ constexpr uint32_t kCtlBytes = (sizeof(MlaCtl) + 1023u) & ~1023u;
 constexpr uint32_t kSmem = kQBytes + kStages * kKBytes + kCtlBytes + 1024 /* alignment */;
 static_assert(kSmem <= 227u * 1024u, "MLA shared memory");
 static_assert(kHeads * 128 == 4 * kAtomBytes, "P fills the 4 atoms of the other output half");
-static_assert(kHeads * 256 * 4 <= kQBytes, "the scaled O rows fit where Q was");
+static_assert(kHeads * 256 * 4 <= kQBytes + (kStages - 1) * kKBytes, "the scaled O rows fit where Q and the ring were");
 
 // Instruction descriptor of kind::f16 with bf16 A and B (both K-major), fp32
 // accumulator, shape M x N: D format [4,6) = 1 (f32), A / B format [7,10) /
@@ -114,6 +125,37 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+
+// D[tmem] (+)= A[tmem] x B[smem desc]^T: A (M x K) in TMEM, row m in lane m,
+// two 16-bit elements per 32-bit column (the lower K index in the low half).
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_x32u(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0],"
+        " {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16,"
+        " %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+// Arrive on bar once this thread's earlier cp.async copies have landed (the
+// arrival is one of the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 
 __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, float (&r)[32]) {
     uint32_t u[32];
@@ -177,9 +219,6 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint3
                  : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
-}
 
 // The gather of tile `it` of the split into stage buffer sT: 4 threads per row,
 // 18 pieces each; rows without a slot are zero-filled (their scores are masked
@@ -193,7 +232,6 @@ __device__ __forceinline__ void gather_tile(uint32_t sT, const int32_t* sl, int 
     const uint8_t* row = kv + (ok ? static_cast<int64_t>(slot) * kRowBytes : 0);
 #pragma unroll 6
     for (int c = tid & 3; c < kChunks; c += 4) cp_async_16(sT + sw_offset(r, c, kAtomBytes), row + 16 * c, ok ? 16u : 0u);
-    cp_async_commit();
     if (tid < 32) {
         const int32_t sj = (tid < n) ? sl[tid] : -1;
         const uint32_t m = __ballot_sync(0xffffffffu, sj >= 0 && sj < C);
@@ -219,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* const gbase = smem_raw + (base - raw);
-    // Q [9 atoms x 128 rows] (later: the scaled O rows) | tile stage 0 | tile stage 1 | control
+    // Q atoms 6..8 [3 x 128 rows] | tile stages 0..3 (later, from the start: the scaled O rows) | control
     const uint32_t sQ = base, sT0 = sQ + kQBytes;
     uint8_t* const gT0 = gbase + kQBytes;
     MlaCtl* ctl = reinterpret_cast<MlaCtl*>(gT0 + kStages * kKBytes);
@@ -236,8 +274,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t v_off = static_cast<uint32_t>(4 * half) * kAtomBytes;
 
     if (tid == 0) {
-        mbar_init(smem_addr(&ctl->s_bar), 1);
-        mbar_init(smem_addr(&ctl->pv_bar), 1);
+        for (int i = 0; i < kStages; ++i) mbar_init(smem_addr(&ctl->tile_full[i]), kHeadThreads);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_addr(&ctl->s_full[i]), 1);
+            mbar_init(smem_addr(&ctl->p_full[i]), kHeadThreads);
+            mbar_init(smem_addr(&ctl->pv_done[i]), 1);
+        }
         ctl->abort = 0;
         fence_barrier_init();
     }
@@ -245,13 +287,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_addr(&ctl->tmem), kTmemCols);
         tmem_relinquish();
     }
-    // Q of the request (row h = head h), piece-major so a warp reads contiguous bytes
+    // Q atoms 6..8 of the request (row h = head h) into shared memory, piece-major
     {
         const uint8_t* qb = reinterpret_cast<const uint8_t*>(q) + static_cast<int64_t>(b) * kHeads * kRowBytes;
+        constexpr int kQc = kChunks - 8 * kQTmemAtoms;  // 24 pieces per row
 #pragma unroll 8
-        for (int g = tid; g < kHeads * kChunks; g += kThreads) {
-            const int h = g / kChunks, c = g - h * kChunks;
-            cp_async_16(sQ + sw_offset(h, c, kHeads * 128u), qb + static_cast<int64_t>(h) * kRowBytes + 16 * c);
+        for (int g = tid; g < kHeads * kQc; g += kThreads) {
+            const int h = g / kQc, c = g - h * kQc;
+            cp_async_16(sQ + sw_offset(h, c, kHeads * 128u),
+                        qb + static_cast<int64_t>(h) * kRowBytes + 16 * (8 * kQTmemAtoms + c));
         }
         cp_async_commit();
     }
@@ -260,152 +304,193 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t* sl = sel_slot + static_cast<int64_t>(b) * k + t_lo;
         for (int i = tid; i < n_tok; i += kThreads) ctl->slot[i] = sl[i];
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");  // Q's pieces landed
+    fence_proxy_async_smem();
     __syncthreads();
     const int tiles = (n_tok + kTok - 1) / kTok;
-    if (tiles > 0) gather_tile(sT0, ctl->slot, n_tok, kv, C, tid, &ctl->valid[0]);
+    const bool head = tid < kHeadThreads;
+    if (head)
+        for (int t = 0; t < min(tiles, kStages - 1); ++t) {  // the first three tiles of the ring
+            gather_tile(sT0 + static_cast<uint32_t>(t) * kKBytes, ctl->slot + t * kTok, n_tok - t * kTok, kv, C, tid,
+                        &ctl->valid[t]);
+            cp_async_arrive_noinc(smem_addr(&ctl->tile_full[t]));
+        }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctl->tmem;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;  // this warp's TMEM lanes
-    volatile int* abort = &ctl->abort;
-    bool failed = false;
-    uint32_t pending = 0, phase = 0;  // the barrier and phase a timed-out wait was on
-
-    float m = -INFINITY, l = 0.f;  // this thread's head: reference max (log2-scaled scores) and sum
-    for (int it = 0; it < tiles; ++it) {
-        const int st = it & 1;
-        const uint32_t sT = sT0 + static_cast<uint32_t>(st) * kKBytes;
-        uint8_t* const gT = gT0 + st * kKBytes;
-        // ---- tile `it` (and Q) landed
-        cp_async_wait_all();
-        fence_proxy_async_smem();
-        __syncthreads();
-        // ---- S = Q K^T into S buffer st
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll 4
-            for (int kk = 0; kk < kAtoms * 4; ++kk) {
-                const uint32_t a = static_cast<uint32_t>(kk >> 2), off = static_cast<uint32_t>(kk & 3) * 32u;
-                mma_bf16(tmem + static_cast<uint32_t>(st) * kTok, sw128_kmajor_desc(sQ + a * kHeads * 128u + off),
-                         sw128_kmajor_desc(sT + a * kAtomBytes + off), kIdescS, kk > 0 ? 1u : 0u);
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;  // a head warp's TMEM lanes
+    // Q atoms 0..5 into TMEM: each head thread its row, 32 columns (64 bf16) per store
+    if (head) {
+        const uint4* qrow = reinterpret_cast<const uint4*>(q + (static_cast<int64_t>(b) * kHeads + tid) * kDqk);
+#pragma unroll 1
+        for (int a = 0; a < kQTmemAtoms; ++a) {
+            uint32_t u[32];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint4 v = __ldg(qrow + 8 * a + j);
+                u[4 * j] = v.x;
+                u[4 * j + 1] = v.y;
+                u[4 * j + 2] = v.z;
+                u[4 * j + 3] = v.w;
             }
-            mma_commit(smem_addr(&ctl->s_bar));
+            tmem_st_x32u(tmem + lane_base + 32u * a, u);
         }
-        // ---- the previous tile's PV done: its stage buffer takes the next gather
-        if (it > 0) {
-            if (__syncthreads_or(!mla_wait(smem_addr(&ctl->pv_bar), (it - 1) & 1, abort))) {
-                failed = true;
-                pending = smem_addr(&ctl->pv_bar);
-                phase = (it - 1) & 1;
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    volatile int* abort = &ctl->abort;
+    float m = -INFINITY, l = 0.f;  // a head thread's head: reference max (log2-scaled scores) and sum
+
+    if (tid == kHeadThreads) {
+        // ---- warp 4, lane 0: S(it) as soon as tile it lands, then P.V(it - 1) once P(it - 1) is written
+        for (int it = 0; it <= tiles && !*abort; ++it) {
+            if (it < tiles) {
+                const int st = it % kStages;
+                const uint32_t sT = sT0 + static_cast<uint32_t>(st) * kKBytes;
+                const uint32_t sCol = kSCol + static_cast<uint32_t>(it & 1) * kTok;
+                if (!mla_wait(smem_addr(&ctl->tile_full[st]), static_cast<uint32_t>(it / kStages) & 1u, abort)) {
+                    *abort = 1;
+                    break;
+                }
+                fence_proxy_async_smem();  // the head threads' copies, seen by the MMAs
+                tc_fence_after();
+#pragma unroll 4
+                for (int kk = 0; kk < kQTmemAtoms * 4; ++kk) {
+                    const uint32_t a = static_cast<uint32_t>(kk >> 2), off = static_cast<uint32_t>(kk & 3) * 32u;
+                    mma_bf16_ta(tmem + sCol, tmem + 8u * kk, sw128_kmajor_desc(sT + a * kAtomBytes + off), kIdescS,
+                                kk > 0 ? 1u : 0u);
+                }
+#pragma unroll 4
+                for (int kk = kQTmemAtoms * 4; kk < kAtoms * 4; ++kk) {
+                    const uint32_t a = static_cast<uint32_t>(kk >> 2), off = static_cast<uint32_t>(kk & 3) * 32u;
+                    mma_bf16(tmem + sCol, sw128_kmajor_desc(sQ + (a - kQTmemAtoms) * kHeads * 128u + off),
+                             sw128_kmajor_desc(sT + a * kAtomBytes + off), kIdescS, 1u);
+                }
+                mma_commit(smem_addr(&ctl->s_full[it & 1]));
+            }
+            if (it > 0) {
+                const int pt = it - 1;
+                if (!mla_wait(smem_addr(&ctl->p_full[pt & 1]), static_cast<uint32_t>(pt >> 1) & 1u, abort)) {
+                    *abort = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t pT = sT0 + static_cast<uint32_t>(pt % kStages) * kKBytes;
+#pragma unroll
+                for (int kk = 0; kk < kTok / 16; ++kk)
+                    mma_bf16(tmem + kOCol, sw128_kmajor_desc(pT + p_off + kk * 32u),
+                             sw128_mnmajor_desc(pT + v_off + kk * 2048u, kAtomBytes), kIdescPV,
+                             (pt > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(smem_addr(&ctl->pv_done[pt & 1]));
+            }
+        }
+    } else if (head) {
+        // ---- warps 0-3: softmax of tile it, P into the tile's dead atoms, then the gather of tile it + 3
+        for (int it = 0; it < tiles; ++it) {
+            const int st = it % kStages;
+            uint8_t* const gT = gT0 + st * kKBytes;
+            const uint32_t sCol = kSCol + static_cast<uint32_t>(it & 1) * kTok;
+            if (!mla_wait(smem_addr(&ctl->s_full[it & 1]), static_cast<uint32_t>(it >> 1) & 1u, abort)) {
+                *abort = 1;
                 break;
             }
-        }
-        if (it + 1 < tiles)
-            gather_tile(sT0 + static_cast<uint32_t>(st ^ 1) * kKBytes, ctl->slot + (it + 1) * kTok,
-                        n_tok - (it + 1) * kTok, kv, C, tid, &ctl->valid[st ^ 1]);
-        if (__syncthreads_or(!mla_wait(smem_addr(&ctl->s_bar), it & 1, abort))) {  // block-uniform
-            failed = true;
-            pending = smem_addr(&ctl->s_bar);
-            phase = it & 1;
-            break;
-        }
-        tc_fence_after();
-        // ---- softmax of this head's row against the reference max; P row to shared memory
-        {
-            float s[kTok];
-            tmem_ld_x32(tmem + lane_base + static_cast<uint32_t>(st) * kTok, s);
-            const uint32_t vm = ctl->valid[st];
-#pragma unroll
-            for (int t = 0; t < kTok; ++t) s[t] = ((vm >> t) & 1u) ? s[t] : -INFINITY;
-            // tile max of the raw scores (a tree: short dependency chains); scale > 0
-            float mx[kTok / 2];
-#pragma unroll
-            for (int t = 0; t < kTok / 2; ++t) mx[t] = fmaxf(s[2 * t], s[2 * t + 1]);
-#pragma unroll
-            for (int w = kTok / 4; w >= 1; w >>= 1)
-#pragma unroll
-                for (int t = 0; t < w; ++t) mx[t] = fmaxf(mx[t], mx[t + w]);
-            const float tmx = mx[0] * scale_log2;
-            const bool need = tmx > m + kLazy;  // also m = -inf with a valid token
-            // tcgen05.ld / st are warp-collective: the whole warp rescales when any head moves
-            const bool warp_moves = __any_sync(0xffffffffu, need);
-            float corr = 1.f;
-            if (warp_moves && tmx > m) {
-                corr = ex2_approx(m - tmx);  // 0 when m = -inf
-                m = tmx;
+            // P.V(it - 1) done: O may be rescaled and tile it - 1's stage takes tile it + 3
+            if (it > 0 && !mla_wait(smem_addr(&ctl->pv_done[(it - 1) & 1]), static_cast<uint32_t>((it - 1) >> 1) & 1u,
+                                    abort)) {
+                *abort = 1;
+                break;
             }
-            // p = 2^(s * scale_log2 - m); with m = -inf every score is -inf and p = 0
-            const float neg_m = (m == -INFINITY) ? 0.f : -m;
-            float part[4] = {0.f, 0.f, 0.f, 0.f};
-            uint32_t packed[kTok / 2];
+            tc_fence_after();
+            {
+                float s[kTok];
+                tmem_ld_x32(tmem + lane_base + sCol, s);
+                const uint32_t vm = ctl->valid[st];
 #pragma unroll
-            for (int t = 0; t < kTok; t += 2) {
-                const float p0 = ex2_approx(fmaf(s[t], scale_log2, neg_m));
-                const float p1 = ex2_approx(fmaf(s[t + 1], scale_log2, neg_m));
-                const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
-                part[(t >> 1) & 3] += __low2float(pb) + __high2float(pb);  // the values the MMA uses
-                packed[t >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
-            }
-            const float sum = (part[0] + part[1]) + (part[2] + part[3]);
-            l = l * corr + sum;
-            uint8_t* prow = gT + p_off + tid * 128;
+                for (int t = 0; t < kTok; ++t) s[t] = ((vm >> t) & 1u) ? s[t] : -INFINITY;
+                float mx[kTok / 2];
 #pragma unroll
-            for (int c = 0; c < kTok / 8; ++c)
-                *reinterpret_cast<uint4*>(prow + ((c ^ (tid & 7)) << 4)) =
-                    make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
-            if (it > 0 && warp_moves) {  // O holds earlier tiles (their PV is done): bring it to the new reference
+                for (int t = 0; t < kTok / 2; ++t) mx[t] = fmaxf(s[2 * t], s[2 * t + 1]);
+#pragma unroll
+                for (int w = kTok / 4; w >= 1; w >>= 1)
+#pragma unroll
+                    for (int t = 0; t < w; ++t) mx[t] = fmaxf(mx[t], mx[t + w]);
+                const float tmx = mx[0] * scale_log2;
+                const bool need = tmx > m + kLazy;  // also m = -inf with a valid token
+                // tcgen05.ld / st are warp-collective: the whole warp rescales when any head moves
+                const bool warp_moves = __any_sync(0xffffffffu, need);
+                float corr = 1.f;
+                if (warp_moves && tmx > m) {
+                    corr = ex2_approx(m - tmx);  // 0 when m = -inf
+                    m = tmx;
+                }
+                const float neg_m = (m == -INFINITY) ? 0.f : -m;
+                float part[4] = {0.f, 0.f, 0.f, 0.f};
+                uint32_t packed[kTok / 2];
+#pragma unroll
+                for (int t = 0; t < kTok; t += 2) {
+                    const float p0 = ex2_approx(fmaf(s[t], scale_log2, neg_m));
+                    const float p1 = ex2_approx(fmaf(s[t + 1], scale_log2, neg_m));
+                    const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+                    part[(t >> 1) & 3] += __low2float(pb) + __high2float(pb);  // the values the MMA uses
+                    packed[t >> 1] = *reinterpret_cast<const uint32_t*>(&pb);
+                }
+                l = l * corr + ((part[0] + part[1]) + (part[2] + part[3]));
+                uint8_t* prow = gT + p_off + tid * 128;
+#pragma unroll
+                for (int c = 0; c < kTok / 8; ++c)
+                    *reinterpret_cast<uint4*>(prow + ((c ^ (tid & 7)) << 4)) =
+                        make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+                if (it > 0 && warp_moves) {  // O holds earlier tiles: bring it to the new reference
 #pragma unroll 1
-                for (int c = 0; c < 256; c += 32) {
-                    float o[32];
-                    tmem_ld_x32(tmem + lane_base + kOCol + c, o);
+                    for (int c = 0; c < 256; c += 32) {
+                        float o[32];
+                        tmem_ld_x32(tmem + lane_base + kOCol + c, o);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) o[j] *= corr;
-                    tmem_st_x32(tmem + lane_base + kOCol + c, o);
+                        for (int j = 0; j < 32; ++j) o[j] *= corr;
+                        tmem_st_x32(tmem + lane_base + kOCol + c, o);
+                    }
                 }
             }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(smem_addr(&ctl->p_full[it & 1]));
+            if (it + kStages - 1 < tiles) {  // tile it + 3 into the stage tile it - 1 had
+                const int t = it + kStages - 1, ts = t % kStages;
+                gather_tile(sT0 + static_cast<uint32_t>(ts) * kKBytes, ctl->slot + t * kTok, n_tok - t * kTok, kv, C,
+                            tid, &ctl->valid[ts]);
+                cp_async_arrive_noinc(smem_addr(&ctl->tile_full[ts]));
+            }
         }
-        tc_fence_before();
-        fence_proxy_async_smem();
-        __syncthreads();
-        // ---- O += P V (this CTA's 256 dims), two K steps of 16 tokens
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < kTok / 16; ++kk)
-                mma_bf16(tmem + kOCol, sw128_kmajor_desc(sT + p_off + kk * 32u),
-                         sw128_mnmajor_desc(sT + v_off + kk * 2048u, kAtomBytes), kIdescPV,
-                         (it > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(smem_addr(&ctl->pv_bar));
-        }
+        // the last P.V done
+        if (!*abort && tiles > 0 &&
+            !mla_wait(smem_addr(&ctl->pv_done[(tiles - 1) & 1]), static_cast<uint32_t>((tiles - 1) >> 1) & 1u, abort))
+            *abort = 1;
     }
-    if (!failed && tiles > 0) {
-        if (__syncthreads_or(!mla_wait(smem_addr(&ctl->pv_bar), (tiles - 1) & 1, abort))) {
-            failed = true;
-            pending = smem_addr(&ctl->pv_bar);
-            phase = (tiles - 1) & 1;
-        }
-    }
+    __syncthreads();
     tc_fence_after();
-    cp_async_wait_all();
-    if (failed) {  // every thread took this branch; give the late MMA one more bounded wait
-        if (tid == 0) {
-            set_status(status, ECHO_ST_TIMEOUT);
-            mla_wait(pending, phase, abort);
-        }
+    const bool failed = *abort != 0;
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    if (failed) {  // every thread sees it
+        if (tid == 0) set_status(status, ECHO_ST_TIMEOUT);
         m = -INFINITY;  // this split then adds nothing
         l = 0.f;
     }
     // ---- combine over the cluster.  Every CTA passes the same three cluster
     // barriers whatever happened above.
-    ctl->m[tid] = m;
-    ctl->l[tid] = l;
+    const int hh = head ? tid : 0;  // warp 4 takes no head
+    if (head) {
+        ctl->m[tid] = m;
+        ctl->l[tid] = l;
+    }
     cluster.sync();  // (1) every split's (m, l) is published
     float mj[kMaxSplits], lj[kMaxSplits];
 #pragma unroll
     for (int j = 0; j < kMaxSplits; ++j) {  // all loads in flight at once
-        mj[j] = (j < splits) ? cluster.map_shared_rank(ctl->m, j)[tid] : -INFINITY;
-        lj[j] = (j < splits) ? cluster.map_shared_rank(ctl->l, j)[tid] : 0.f;
+        mj[j] = (j < splits) ? cluster.map_shared_rank(ctl->m, j)[hh] : -INFINITY;
+        lj[j] = (j < splits) ? cluster.map_shared_rank(ctl->l, j)[hh] : 0.f;
     }
     float M = -INFINITY;
 #pragma unroll
@@ -415,8 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < kMaxSplits; ++j)
         if (M > -INFINITY && mj[j] > -INFINITY) L += lj[j] * exp2f(mj[j] - M);
     const float f = (M > -INFINITY && L > 0.f && m > -INFINITY) ? exp2f(m - M) / L : 0.f;
-    // this head's O row, scaled, staged where Q was (the MMAs are done with Q)
-    {
+    // this head's O row, scaled, staged at the start of shared memory (the MMAs are done with it)
+    if (head) {
         const bool have_o = !failed && tiles > 0;
 #pragma unroll 1
         for (int c = 0; c < 256; c += 32) {
