@@ -155,3 +155,37 @@ def test_attention_in_the_decode_graph(orc, hold_early):
             ref, ref_lse, mass = orc.mla_decode(qb[b], hb[off[b]:off[b + 1]], idx, lay.mla_scale)
             assert np.all(np.abs(out[b] - ref) <= 5e-3 * mass + 1e-5), (t, b)
             assert np.all(np.abs(lse[b] - ref_lse) <= 3e-3 * np.maximum(1.0, np.abs(ref_lse)))
+
+
+@pytest.mark.parametrize("k", [1, 31, 33])
+def test_tiny_selections(orc, k):
+    # one tile, or fewer tiles than the gather ring keeps in flight, or a ragged second tile
+    B, C = 2, 64
+    r = _run(B, C, k, 1.0, 10 + k)
+    _check(*r, C, orc)
+
+
+def test_maximum_selection_wraps_the_ring(orc):
+    # k = 8192: 8 splits of 1024 tokens, 32 tiles each -- the four-stage ring wraps eight times
+    B, C, k = 1, 9000, 8192
+    r = _run(B, C, k, 0.97, 21)
+    _check(*r, C, orc)
+
+
+def test_only_the_last_entry_valid(orc):
+    B, C, k = 1, 512, 300
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn((B, L.MLA_HEADS, L.MLA_DQK), generator=g).to(torch.bfloat16)
+    kv = torch.randn((B * C, L.MLA_DQK), generator=g).to(torch.bfloat16)
+    sel = np.full((B, k), -1, np.int32)
+    sel[0, k - 1] = 77
+    out = torch.empty((B, L.MLA_HEADS, L.MLA_DV), dtype=torch.float32, device=dev)
+    lse = torch.empty((B, L.MLA_HEADS), dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    L.mla_decode(q.to(dev), torch.from_numpy(sel).to(dev), kv.to(dev), C, 0.1, out, lse, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    # one valid token: every head's output is that token's first 512 values, lse its score
+    row = kv[77, :L.MLA_DV].float().numpy()
+    assert np.allclose(out.cpu().numpy()[0], row[None, :], atol=1e-6, rtol=0)
+    _check(q, kv, sel, out.cpu().numpy(), lse.cpu().numpy(), 0.1, C, orc)
