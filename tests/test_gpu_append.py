@@ -105,3 +105,13 @@ def test_decode_on_growing_contexts(hold_early):
     w = wl.scaled(wl.WORKLOADS["tiny"], "grow", B=3, lengths=(3000, 200, 5000), k=256, C=1024)
     grown = run_decode_growing(w, steps=4, room=3, hold_early=hold_early)
     assert grown.tolist() == [3, 3, 3]
+
+
+def test_context_growing_from_empty():
+    # request 0 starts with no token (its first append lands on its region's first row); request 1
+    # is shorter than k; three decode steps with appends in between, checked step by step
+    from sparse_attention_kv_echo_gb300 import workloads as wl
+    from tests._parity import run_decode_growing
+    w = wl.scaled(wl.WORKLOADS["tiny"], "grow0", B=2, lengths=(0, 180), k=256, C=1024)
+    grown = run_decode_growing(w, steps=3, room=5)
+    assert grown.tolist() == [3, 3]

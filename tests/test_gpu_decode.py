@@ -227,3 +227,10 @@ def test_shared_pool_large_predictor_off_and_cap():
     run_pool(w, steps=3, pool=140032, predictor=False, graph=False)
     w2 = wl.scaled(wl.WORKLOADS["batch"], "pool_cap", B=2, lengths=(8000, 5000), k=256, C=1024)
     run_pool(w2, steps=4, pool=1024, cap=100)
+
+
+def test_shared_pool_ragged_batch():
+    # an empty request, one shorter than k, and long ones sharing one pool
+    from tests._parity import run_pool
+    w = wl.scaled(wl.WORKLOADS["batch"], "pool_ragged", B=4, lengths=(7000, 0, 150, 3000), k=256, C=1024)
+    run_pool(w, steps=4, pool=1024)
