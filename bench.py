@@ -59,13 +59,14 @@ def parse_args(argv=None):
                    help="where the selected tokens' slots are looked up (top-k's slices or the cache step)")
     p.add_argument("--hold-early", action="store_true",
                    help="the held-slot variant of the cache step (the late recall need not wait for the early copy)")
-    p.add_argument("--part", choices=["step", "mla", "append", "layers", "pool"], default="step",
+    p.add_argument("--part", choices=["step", "mla", "append", "layers", "pool", "prefill"], default="step",
                    help="step: the decode step (default); mla: the sparse MLA attention over the selected "
                         "slots alone, at the step's batch, k and GPU slots; append: the append of one new "
                         "token per request (key, host-pool row, cache slot) at the step's batch; layers: "
                         "a 4-layer step on layer-correlated inputs, threshold predictor against the "
                         "cross-layer early fetch; pool: the decode step with one cache pool shared by the "
-                        "batch (B x C slots, and 260000) against per-request slot ranges")
+                        "batch (B x C slots, and 260000) against per-request slot ranges; prefill: the "
+                        "chunked prefill of a 102400-token prompt in 2048-row blocks")
     p.add_argument("--first-share", type=float, default=None,
                    help="share of the requests in the first of two groups (default: the layer's choice)")
     return p.parse_args(argv)
@@ -840,10 +841,81 @@ def run_pool(args):
     }), flush=True)
 
 
+PREFILL_METRIC = "chunked prefill, prompt tokens/s (scores, per-row one-round histogram top-k, union, recall)"
+
+
+def run_prefill(args):
+    """The chunked prefill of one 102400-token prompt: 50 blocks of 2048 query rows, k = 2048 per
+    row, a 260000-slot cache; one timed step = the whole prompt (every block enqueued, block i's
+    recall on the copy stream under block i+1's scores), from a fresh cache and threshold."""
+    import torch
+    from sparse_attention_kv_echo_gb300 import _lib as L
+    from sparse_attention_kv_echo_gb300 import workloads as wl
+    from sparse_attention_kv_echo_gb300.prefill import PrefillRunner
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    L.load(build_if_missing=True)
+    w = wl.WORKLOADS["prefill"]
+    k8, ks = wl.make_keys(w, 0, device=dev)
+    host = wl.make_host_pool(w, 0, device=dev, pin=True)
+    pr = PrefillRunner(k8, ks, w.k, w.C, host, w.prefill_block)
+    nb = pr.blocks()
+    qs = [wl.make_prefill_queries(w, i, device=dev) for i in range(nb)]
+    main = torch.cuda.Stream()
+
+    def prompt():
+        with torch.cuda.stream(main):
+            pr.cache.reset()
+            pr.theta.fill_(math.inf)
+            for i in range(nb):
+                pr.block(i, qs[i][0], qs[i][1], stream=main)
+            pr.wait_recall(main)
+
+    for _ in range(max(1, args.warmup)):
+        prompt()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(main):
+            a.record(main)
+        prompt()
+        with torch.cuda.stream(main):
+            b.record(main)
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    t = statistics.mean(ms) / 1e3
+    n = w.total_tokens
+    # scoring work of the prompt: every row p sees p + 1 keys, 64 heads x 128 dims (2 FLOP per MAC)
+    flops = 2.0 * 64 * 128 * n * (n + 1) / 2
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            fp8_peak = 2.0 * float(json.load(f)["bf16_tflops"])   # measured bf16 x the nominal fp8/bf16 ratio
+        kind = "measured bf16 x 2 (nominal fp8 / bf16)"
+    except Exception:
+        fp8_peak, kind = 2.0 * 1900.0, "fallback bf16 x 2"
+    tf = flops / t / 1e12
+    print(json.dumps({
+        "metric": PREFILL_METRIC, "value": round(n / t, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * t, 3), "higher_is_better": True,
+        "dtype": "fp8-e4m3 MMA, fp32 accumulate, int32 tables", "data": "synthetic (seeded)",
+        "config": {"workload": f"1 prompt x {n} tokens, {w.prefill_block}-row blocks ({nb}), k={w.k} per row, "
+                               f"{w.C} GPU slots", "step": "the whole prompt"},
+        "roofline": {"kernel": "the prefill's scoring (all kernels of the prompt, an upper bound)",
+                     "bound": "tensor", "achieved": round(tf, 1), "peak": round(fp8_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(tf / fp8_peak, 4), "algorithmic_flops": flops, "peak_source": kind},
+        "status": int(pr.status.item()), "ms_min": round(min(ms), 3),
+    }), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         run_reference(args)
+    elif args.part == "prefill":
+        run_prefill(args)
     elif args.part == "pool":
         run_pool(args)
     elif args.part == "layers":
