@@ -37,8 +37,11 @@ def _check_rows_scores(rows, row0, gs, q, wt, k8, ks):
         assert bad.size == 0, (r, bad[:5])
 
 
-def _run(w, full_rows=True, row_sample=8, blocks=None, keys_device="cpu"):
+def _run(w, full_rows=True, row_sample=8, blocks=None, keys_device="cpu", same_keys=False):
     k8c, ksc = wl.make_keys(w, 0, device=keys_device)
+    if same_keys:  # every token carries the first token's key and scale
+        k8c = k8c[:1].expand_as(k8c).contiguous()
+        ksc = ksc[:1].expand_as(ksc).contiguous()
     k8, ks = k8c.cpu().numpy(), ksc.cpu().numpy()
     host = wl.make_host_pool(w, 0, device=keys_device, pin=True)
     host_gpu = host.to(dev)
@@ -110,6 +113,17 @@ def test_prefill_rows_fewer_than_k():
     # early rows see fewer than k tokens and select all of them
     w = wl.scaled(wl.WORKLOADS["prefill"], "pf_tiny", lengths=(700,), prefill_block=256, k=300, C=704)
     _run(w, full_rows=True)
+
+
+def test_prefill_all_keys_equal():
+    """Every key the same, so every score of a row ties: each row selects its lowest
+    k positions (ties go to the lower index), the union is [0, k), and rows longer
+    than 6144 tokens -- a boundary bin too large for the shared-memory list --
+    select from global memory."""
+    w = wl.scaled(wl.WORKLOADS["prefill"], "pf_ties", lengths=(8192,), prefill_block=2048, k=256, C=8192)
+    pr = _run(w, full_rows=True, row_sample=4, same_keys=True)
+    sel = pr.sel_idx[:2048].cpu().numpy()
+    assert np.array_equal(sel[-1], np.arange(256, dtype=np.int32))
 
 
 def test_prefill_full_size_sampled():
