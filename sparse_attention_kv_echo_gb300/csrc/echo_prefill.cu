@@ -11,7 +11,8 @@
 //   score_kernel         prefill mode: row r at position row0 + r scores keys
 //                        [0, row0 + r] (causal, itself included) into scores[r*W + s],
 //                        with the per-row histogram shifted by the block's threshold
-//   topk_kernel          one 8-CTA cluster per row: exact top-k of the row
+//   row_topk_kernel      one CTA per row: exact top-k of the row, its boundary
+//                        bin taken from the row's histogram
 //   union_mark_kernel    marks every token some row selected
 //   union_compact_kernel ascending list of the marked tokens (the block's
 //                        selection for the cache), its bit words, and the
