@@ -397,10 +397,13 @@ class DecodeStack:
         if self.cross_layer and not all(l.cross_layer for l in layers[1:]):
             raise ValueError("layers after the first need cross_layer=True")
 
-    def step(self, qs, ws, stream=None, between=None):
-        """qs / ws: per layer the step's query [B,64,128] and weights [B,64] (f32).
+    def step(self, qs, ws, stream=None, between=None, out_host=None):
+        """qs / ws: per layer the step's query [B,64,128] and weights [B,64] (f32; pinned host
+        tensors are read by the quantisers directly).
         between(stream): optional work enqueued on the step's stream after each layer but the last
-        (the rest of a transformer layer -- attention, MLP -- that separates two indexers)."""
+        (the rest of a transformer layer -- attention, MLP -- that separates two indexers).
+        out_host: optional per layer (slot [B,k] int32, kth [B] f32) CUDA tensors over pinned host
+        memory, written as each layer's request groups finish (DecodeLayer.step)."""
         main = torch.cuda.current_stream() if stream is None else stream
         if self.cross_layer:  # the transfer streams follow everything before this step
             for lay in self.layers[1:]:
@@ -409,9 +412,37 @@ class DecodeStack:
             seeded = self.cross_layer and i > 0
             if seeded:
                 lay.seed_from(self.layers[i - 1])
-            lay.step(qs[i], ws[i], stream=main, seeded=seeded)
+            lay.step(qs[i], ws[i], stream=main, seeded=seeded, out_host=None if out_host is None else out_host[i])
             if between is not None and i + 1 < len(self.layers):
                 between(main)
+
+    def capture_host_step(self, q_host: torch.Tensor, w_host: torch.Tensor, slot_host: torch.Tensor,
+                          kth_host: torch.Tensor, stream=None) -> torch.cuda.CUDAGraph:
+        """A CUDA graph of one step of every layer with its host I/O: layer l's quantiser reads
+        q_host[l] [B,64,128] f32 and w_host[l] [B,64] f32 (pinned) directly, and its slots and k-th
+        scores go to slot_host[l] [B,k] int32 / kth_host[l] [B] f32 (pinned) as soon as each request
+        group's are final.  The buffers are bound to the graph: refill the inputs before a replay,
+        read the outputs after it."""
+        lays = self.layers
+        n = len(lays)
+        for t, like in ((q_host, lays[0].q_in), (w_host, lays[0].w_in), (slot_host, lays[0].sel_slot),
+                        (kth_host, lays[0].kth)):
+            if (t.device.type != "cpu" or not t.is_pinned() or not t.is_contiguous()
+                    or tuple(t.shape) != (n,) + tuple(like.shape) or t.dtype != like.dtype):
+                raise ValueError("host I/O buffers must be pinned, contiguous CPU tensors shaped like "
+                                 "[layers] + q_in, w_in, sel_slot and kth")
+        dev = lays[0].q_in.device
+        cap = torch.cuda.Stream(device=dev) if stream is None else stream
+        cap.wait_stream(torch.cuda.current_stream(dev))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            # the graph reads and writes these buffers through their aliases: keep them alive
+            self._host_io = getattr(self, "_host_io", []) + [(q_host, w_host, slot_host, kth_host)]
+            outs = [(L.host_alias_tensor(slot_host[i], dev), L.host_alias_tensor(kth_host[i], dev)) for i in range(n)]
+            with torch.cuda.graph(g, stream=cap):
+                self.step([q_host[i] for i in range(n)], [w_host[i] for i in range(n)], stream=cap, out_host=outs)
+        torch.cuda.current_stream(dev).wait_stream(cap)
+        return g
 
     def kernel_launches_per_step(self) -> int:
         return sum(l.kernel_launches_per_step() for l in self.layers)

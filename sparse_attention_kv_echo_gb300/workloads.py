@@ -93,19 +93,22 @@ def tok_offsets(lengths) -> np.ndarray:
     return off
 
 
-def make_keys(w: Workload, layer: int, device="cpu"):
+def make_keys(w: Workload, layer: int, device="cpu", requests=None):
     """E4M3 index keys [sum N, 128] (uint8) and per-token fp32 scales [sum N] of one layer.
 
     Each key row ~ N(0,1) (plus hot_offset on a hot subset of hot_frac of each
     request's tokens, drawn uniformly without replacement), then stored as
-    E4M3 bytes with scale amax/448 per token."""
+    E4M3 bytes with scale amax/448 per token.  requests: only these requests'
+    rows, concatenated in the order given (each request has its own generator,
+    so its bytes are the same as in the full set)."""
     rows = []
     scales = []
-    for b, n in enumerate(w.lengths):
+    for b in (range(w.B) if requests is None else requests):
+        n = w.lengths[b]
+        g = _gen(device, w.seed, 10_000 + 1000 * layer + b)
         if w.layer_rho > 0:
             kf = _correlated((n, D), w, layer, 10_000 + b, device)
         else:
-            g = _gen(device, w.seed, 10_000 + 1000 * layer + b)
             kf = torch.randn((n, D), generator=g, device=device, dtype=torch.float32)
         if w.hot_frac > 0:
             nh = int(round(w.hot_frac * n))
@@ -164,17 +167,41 @@ class QueryStream:
         return out
 
 
-def make_host_pool(w: Workload, layer: int, device="cpu", pin: bool = False) -> torch.Tensor:
+def pinned_empty(shape, dtype) -> torch.Tensor:
+    """An uninitialised host tensor whose pages are locked and mapped for the GPU
+    (cudaHostRegister), sized exactly: torch's pinned allocator rounds every
+    block up to a power of two, which for a multi-GB host pool nearly doubles
+    the locked memory.  The bytes belong to a numpy buffer that the tensor's
+    storage keeps alive (views included); the registration is dropped just
+    before that buffer is freed."""
+    import weakref
+    nbytes = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+    if nbytes == 0:
+        return torch.empty(shape, dtype=dtype, pin_memory=True)
+    buf = np.empty(nbytes, np.uint8)
+    rt = torch.cuda.cudart()
+    rc = rt.cudaHostRegister(buf.ctypes.data, nbytes, 3)   # portable | mapped
+    if int(rc) != 0:
+        raise RuntimeError(f"cudaHostRegister failed ({int(rc)})")
+    weakref.finalize(buf, rt.cudaHostUnregister, buf.ctypes.data)
+    return torch.from_numpy(buf).view(dtype).view(shape)
+
+
+def make_host_pool(w: Workload, layer: int, device="cpu", pin: bool = False, rows: int | None = None) -> torch.Tensor:
     """Host KV pool [sum N, 576] bf16 ~ N(0,1) of one layer (pinned when pin=True).
 
-    With device='cuda' the values are drawn on the GPU and copied to host memory."""
+    With device='cuda' the values are drawn on the GPU and copied to host memory.
+    rows: only the first `rows` rows, a multiple of the 65536-row draw (the same
+    values as in the whole pool: the draws are made in that order)."""
     g = _gen(device, w.seed, 40_000 + layer)
-    n = w.total_tokens
+    chunk = 1 << 16
+    n = w.total_tokens if rows is None else int(rows)
+    if n != w.total_tokens and n % chunk:
+        raise ValueError("a partial host pool takes a multiple of 65536 rows")
     if pin:
-        out = torch.empty((n, KV_DIM), dtype=torch.bfloat16, pin_memory=True)
+        out = pinned_empty((n, KV_DIM), torch.bfloat16)
     else:
         out = torch.empty((n, KV_DIM), dtype=torch.bfloat16)
-    chunk = 1 << 16
     for r0 in range(0, n, chunk):
         r1 = min(n, r0 + chunk)
         out[r0:r1].copy_(torch.randn((r1 - r0, KV_DIM), generator=g, device=device,
