@@ -439,6 +439,7 @@ def run_ours(args):
     side = lay.side
     above_all = torch.zeros(max(L.above_words(lay.B, lay.n_tokens), 1), dtype=torch.int32, device=dev)
     fb0 = int(lay.stats[L.STAT_TOPK_FALLBACK].item())
+    cm0 = int(lay.stats[L.STAT_CAND_MISS].item())
     for r in range(reps + 2):
         t = (args.warmup + args.steps + r) % S
         with torch.cuda.stream(main):
@@ -450,10 +451,10 @@ def run_ours(args):
                   for k in ("q0", "q1", "s1", "e1", "t0", "t1", "c1", "r1")}
             ev["q0"].record(main)
             L.quantize_q(q_all[t, 0], lay.w_in, lay.q8, lay.qscale, lay.wfold, lay.status, hist=lay.hist,
-                         stream=main)
+                         stream=main, cand_cnt=None if lay.cands is None else lay.cands.cnt)
             ev["q1"].record(main)
             L.index_scores(lay.tok_off, lay.n_tokens, lay.q8, lay.wfold, lay.k8, lay.ks, lay.scores, lay.theta,
-                           lay.hist, lay.status, above=above_all, cache=lay.cache, stream=main)
+                           lay.hist, lay.status, above=above_all, cache=lay.cache, stream=main, cands=lay.cands)
             ev["s1"].record(main)
             side.wait_stream(main)
             # as in the step: early rows on `main`, top-k and the tables on `side`
@@ -461,15 +462,13 @@ def run_ours(args):
             ev["e1"].record(main)
             ev["t0"].record(side)
             if lay.resolved:
-                L.topk_select_cached(lay.tok_off, lay.n_tokens, lay.scores, lay.k, lay.hist, lay.theta, lay.alpha,
-                                     lay.sel_idx, lay.kth, lay.cache, lay.sel_slot, lay.status, stats=lay.stats,
-                                     stream=side, above=above_all, early_cap=lay.early_cap)
+                lay._select(lay.tok_off, 0, lay.B, lay.cands, side, cache=lay.cache, above=above_all,
+                            early_cap=lay.early_cap)
                 ev["t1"].record(side)
                 L.cache_step_resolved(lay.tok_off, lay.n_tokens, lay.sel_idx, lay.cache, lay.sel_slot, lay.status,
                                       stream=side, copy_stream=main)
             else:
-                L.topk_select(lay.tok_off, lay.n_tokens, lay.scores, lay.k, lay.hist, lay.theta, lay.alpha,
-                              lay.sel_idx, lay.kth, lay.status, stats=lay.stats, stream=side)
+                lay._select(lay.tok_off, 0, lay.B, lay.cands, side)
                 ev["t1"].record(side)
                 L.cache_step(lay.tok_off, lay.n_tokens, lay.sel_idx, lay.cache, lay.sel_slot, lay.status,
                              stream=side, copy_stream=main, above=above_all, early_cap=lay.early_cap)
@@ -487,6 +486,7 @@ def run_ours(args):
         recall_ms.append(max(0.0, ev["c1"].elapsed_time(ev["r1"])))
         recall_rows.append(int(lay.cache.miss_cnt.sum().item()))
     pass_fallbacks = int(lay.stats[L.STAT_TOPK_FALLBACK].item()) - fb0
+    pass_cand_miss = int(lay.stats[L.STAT_CAND_MISS].item()) - cm0
     status |= int(lay.status.item())
     kern_us = {n: 1e3 * statistics.mean(v) for n, v in kt.items()}
     t_score = statistics.mean(kt["scores"]) / 1e3
@@ -537,6 +537,9 @@ def run_ours(args):
                    "topk_boundary_bin_max": boundary_max,
                    "topk_boundary_fallbacks_timed": int(stats[L.STAT_TOPK_FALLBACK]),
                    "topk_boundary_fallbacks_kernel_pass": pass_fallbacks,
+                   "topk_candidate_lists": lay.cands is not None,
+                   "topk_list_misses_timed": int(stats[L.STAT_CAND_MISS]),
+                   "topk_list_misses_kernel_pass": pass_cand_miss,
                    "recall_rows_per_layer_kernel_pass": round(statistics.mean(recall_rows), 1),
                    "early_fetch_gbs": round(recall_gbs, 1), "h2d_probes_gbs": probes,
                    "recall_frac_of_h2d": round(recall_gbs / link_peak, 4) if link_peak else None,
@@ -692,6 +695,7 @@ def run_kernels(args):
     theta, kth = torch.full((B,), math.inf, **f32), torch.zeros(B, **f32)
     sel = torch.full((B, w.k), -1, **i32)
     status, stats = torch.zeros(1, **i32), torch.zeros(L.STATS_N, **i32)
+    cands = L.Cands(B, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     main = torch.cuda.Stream()
     qs = [qsrc.next() for _ in range(args.warmup + args.steps)]
@@ -699,13 +703,14 @@ def run_kernels(args):
     for i, q in enumerate(qs):
         with torch.cuda.stream(main):
             ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-            L.quantize_q(q, wt, q8, qscale, wfold, status, hist=hist, stream=main)
+            L.quantize_q(q, wt, q8, qscale, wfold, status, hist=hist, stream=main, cand_cnt=cands.cnt)
             flush.zero_()
             ev[0].record(main)
-            L.index_scores(tok_off, n, q8, wfold, k8, ks, scores, theta, hist, status, stream=main)
+            L.index_scores(tok_off, n, q8, wfold, k8, ks, scores, theta, hist, status, stream=main, cands=cands)
             ev[1].record(main)
             ev[2].record(main)
-            L.topk_select(tok_off, n, scores, w.k, hist, theta, 0.5, sel, kth, status, stats=stats, stream=main)
+            L.topk_select_cands(tok_off, n, scores, w.k, hist, theta, 0.5, cands, sel, kth, status, stats=stats,
+                                stream=main)
             ev[3].record(main)
         torch.cuda.synchronize()
         if i >= args.warmup:
@@ -729,7 +734,9 @@ def run_kernels(args):
         "score_us": round(1e6 * ts, 2), "topk_us": round(1e6 * tt, 2),
         "scoring_topk_gbs": round(both, 1), "scoring_topk_frac_of_8tbs": round(both / 8000.0, 4),
         "scoring_topk_frac_of_measured": round(both / peak, 4),
-        "topk_boundary_fallbacks": int(stats[L.STAT_TOPK_FALLBACK].item()), "status": int(status.item()),
+        "topk_boundary_fallbacks": int(stats[L.STAT_TOPK_FALLBACK].item()),
+        "topk_list_misses": int(stats[L.STAT_CAND_MISS].item()),
+        "list_entries_last_call": [int(x) for x in cands.cnt.cpu().tolist()[:4]], "status": int(status.item()),
     }), flush=True)
 
 

@@ -77,6 +77,7 @@ typedef struct CUstream_st* echo_stream_t; /* a cudaStream_t; NULL = legacy defa
 #define ECHO_STAT_EARLY 2           /* tokens fetched early (above the prediction) */
 #define ECHO_STAT_MISSES 3          /* tokens recalled after top-k */
 #define ECHO_STAT_EARLY_USED 4      /* early-fetched tokens that top-k then selected */
+#define ECHO_STAT_CAND_MISS 5       /* top-k given candidate lists that selected from all the scores */
 #define ECHO_STATS_N 8
 
 /* echo_cache_step flags */
@@ -150,11 +151,13 @@ typedef struct echo_cache {
  *   q and w may be device memory or pinned host memory given by its device
  *   alias (echo_host_device_alias); the kernel reads each element once, so a
  *   step's inputs need no separate host-to-device copy.
- *   hist [B,256] u32 (may be NULL) is set to zero, ready for echo_index_scores.
+ *   hist [B,256] u32 (may be NULL) is set to zero, ready for echo_index_scores;
+ *   cand_cnt [B] int32 (may be NULL; the cnt of an echo_cands) is set to zero,
+ *   ready for echo_index_scores_cands.
  * NaN/Inf in q or w -> ECHO_ST_NAN.
  */
 int echo_quantize_q(int B, const float* q, const float* w, uint8_t* q8, float* qscale,
-                    float* wfold, uint32_t* hist, int32_t* status, echo_stream_t stream);
+                    float* wfold, uint32_t* hist, int32_t* cand_cnt, int32_t* status, echo_stream_t stream);
 
 /*
  * Indexer score of every token [IDX] and the 256-bin histogram of the
@@ -299,6 +302,68 @@ int echo_cache_step_resolved(int B, const int64_t* tok_off, const int64_t* tok_e
                              echo_stream_t stream, echo_stream_t copy_stream, int flags);
 
 /*
+ * Decode top-k over candidate lists [EXPL section 2 "The top-k dependency":
+ * an exact top-k after the scores; what the lists change is only how much of
+ * the scores top-k reads].  The score kernel appends, per request, every
+ * token whose score has order key >= cut[b] to the request's list; when a
+ * request's list holds at least k and at most cap tokens it contains every
+ * token of the top-k (the k-th score is then >= the cut), and top-k selects
+ * among those alone; otherwise it selects from all the scores as
+ * echo_topk_select does.  Top-k sets cut[b] for the next step: the score of
+ * rank 4k of this step (from the list, or the lower edge of a histogram bin
+ * when the list cannot tell), a guess that only decides which path the next
+ * step takes.  Selections, k-th scores, thresholds, slots and tables are the
+ * same as without lists.
+ *   key [B*cap] u32   order keys of the candidates' scores (request b: [b*cap, (b+1)*cap))
+ *   idx [B*cap] int32 request-local token of each candidate, in no particular order
+ *   cnt [B]     int32 candidates found; may exceed cap (the list then holds only
+ *                     cap of them and top-k reads all the scores); cleared by
+ *                     echo_quantize_q before every score call
+ *   cut [B]     u32   0xFFFFFFFF = no list (the initial value); written by top-k
+ *   cap               entries per request, > 0
+ */
+typedef struct echo_cands {
+    uint32_t* key;
+    int32_t* idx;
+    int32_t* cnt;
+    uint32_t* cut;
+    int32_t cap;
+    int32_t reserved;
+} echo_cands;
+
+/*
+ * echo_index_scores that also fills the candidate lists: cands->cnt must hold
+ * zeros on entry (echo_quantize_q clears it); cands->cut is read.  A NaN score
+ * sets ECHO_ST_NAN here (top-k over a list reads only the list).  All other
+ * arguments and outputs as echo_index_scores.
+ */
+int echo_index_scores_cands(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens,
+                            const uint8_t* q8, const float* wfold, const uint8_t* k8, const float* ks,
+                            float* scores, const float* theta_hat, uint32_t* hist, uint32_t* above,
+                            const echo_cache* cache, const echo_cands* cands, int ctas, int32_t* status,
+                            echo_stream_t stream);
+
+/*
+ * Top-k from candidate lists, one thread block per request: echo_topk_select
+ * (cache NULL; sel_slot, above and early_cap unused) or
+ * echo_topk_select_cached (cache given: sel_slot, early_cnt and the early
+ * set's table entries as described there, C <= 32768), with the lists the
+ * score call filled (cands may be NULL: every request selects from all its
+ * scores).  scores, hist and theta_hat as for those calls; hist may be NULL.
+ * Selecting from all the scores, the boundary bin's entries are gathered into
+ * shared memory (up to 16384 of them; past that the bin is selected by passes
+ * over the scores, counted in ECHO_STAT_TOPK_FALLBACK).  A request that had a
+ * list (cut < 0xFFFFFFFF) but selected from all its scores is counted in
+ * ECHO_STAT_CAND_MISS.  Lets a programmatic dependent launch start as soon as
+ * it begins, like echo_topk_select.
+ */
+int echo_topk_select_cands(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens,
+                           const float* scores, int k, const uint32_t* hist, float* theta_hat, float alpha,
+                           const echo_cands* cands, int32_t* sel_idx, float* kth, const uint32_t* above,
+                           int early_cap, const echo_cache* cache, int32_t* sel_slot, int32_t* status,
+                           uint32_t* stats, echo_stream_t stream);
+
+/*
  * Chunked prefill [EXPL panel "Prefill: one-round histogram"; AE section
  * "Fused Prefetch Kernels (ECHO only)", inter-query prefetch].
  *
@@ -357,11 +422,17 @@ int echo_prefill_block(int R, int64_t row0, int64_t n_keys, const float* q, cons
  *     larger than the array return ECHO_ETOOLARGE and enqueue nothing; a
  *     2048-row block of a 102400-token prompt needs about 18 MB.
  *   - The first call on each device looks up the array's device address with
- *     that device current; make that first call before any stream capture.
+ *     that device current (again after the device's context is replaced, e.g.
+ *     by cudaDeviceReset); make that first call before any stream capture: a
+ *     lookup that would happen while `stream` is capturing returns
+ *     ECHO_EINVAL and enqueues nothing.
  *   - All calls on a device share the one array and it keeps the previous
  *     call's contents; the block clears what must start at zero itself.
  *     Calls whose work overlaps on the GPU (other streams, other threads)
- *     race on the array: order them on one stream or serialise them.
+ *     race on the array: order them on one stream or serialise them.  A call
+ *     on the stream and copy stream of the previous call is ordered after that
+ *     call's recall (still running on the copy stream) before it rewrites
+ *     anything the recall reads.
  */
 #define ECHO_PREFILL_STATIC_SCRATCH_BYTES (32u << 20)
 int echo_prefill_block_static(int R, int64_t row0, int64_t n_keys, const float* q, const float* w,
@@ -370,6 +441,20 @@ int echo_prefill_block_static(int R, int64_t row0, int64_t n_keys, const float* 
                               int32_t* union_list, int32_t* union_count, uint32_t* union_bits,
                               const echo_cache* cache, int32_t* sel_slot, int32_t* status, uint32_t* stats,
                               echo_stream_t stream, echo_stream_t copy_stream);
+
+/*
+ * Failure-path knob, for tests (the pages have no counterpart).  Every wait
+ * inside a kernel gives up after a limit (2 s) and reports ECHO_ST_TIMEOUT
+ * instead of hanging; this call sets the limit of one of them -- the score
+ * kernel's wait for an accumulator in its epilogue -- on the current device:
+ * ns >= 0 the new limit (0: give up unless the accumulator is ready at the
+ * first look), ns < 0 back to 2 s.  A score call that gives up sets
+ * ECHO_ST_TIMEOUT, its outputs are invalid, and its kernel still drains its
+ * copies and MMAs before it frees tensor memory and exits, so the next call
+ * runs normally.  The waits that drain are never shortened.  Synchronous
+ * (a copy to device memory); not for use while a score call is in flight.
+ */
+int echo_debug_set_wait_limit(int64_t ns);
 
 /*
  * Sparse MLA decode attention over the selected slots [EXPL section 2: a

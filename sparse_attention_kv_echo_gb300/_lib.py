@@ -18,18 +18,20 @@ from . import build as _build
 ECHO_OK, ECHO_EINVAL, ECHO_ECAPACITY, ECHO_EUNSUPPORTED, ECHO_ECUDA, ECHO_ETOOLARGE = 0, -1, -2, -3, -4, -5
 PREFILL_STATIC_SCRATCH_BYTES = 32 << 20
 ST_TIMEOUT, ST_NAN, ST_NOSLOT, ST_BADDATA, ST_FULL = 0x1, 0x2, 0x4, 0x8, 0x10
-STAT_TOPK_FALLBACK, STAT_BOUNDARY_MAX, STAT_EARLY, STAT_MISSES, STAT_EARLY_USED = 0, 1, 2, 3, 4
+STAT_TOPK_FALLBACK, STAT_BOUNDARY_MAX, STAT_EARLY, STAT_MISSES, STAT_EARLY_USED, STAT_CAND_MISS = 0, 1, 2, 3, 4, 5
 STATS_N = 8
 HEADS, DIM, MAX_REQUESTS = 64, 128, 4096
 CACHE_HOLD_EARLY = 1            # echo_cache_step flag
-TOPK_CACHED_MAX_SLOTS = 32768  # C limit of echo_topk_select_cached
+TOPK_CACHED_MAX_SLOTS = 32768  # C limit of echo_topk_select_cached and of the cached form of echo_topk_select_cands
+CAND_CAP = 16384             # candidate-list entries per request top-k keeps in shared memory
 EARLY_FETCH_BLOCKS = 32      # CTAs of the early-fetch and late-recall kernels
 
-EXPORTS = ("echo_above_words", "echo_append_tokens", "echo_cache_step", "echo_cache_step_resolved", "echo_device_sm_count",
-           "echo_early_fetch", "echo_host_device_alias", "echo_index_scores", "echo_mla_decode", "echo_pool_above", "echo_pool_select",
+EXPORTS = ("echo_above_words", "echo_append_tokens", "echo_cache_step", "echo_cache_step_resolved",
+           "echo_debug_set_wait_limit", "echo_device_sm_count",
+           "echo_early_fetch", "echo_host_device_alias", "echo_index_scores", "echo_index_scores_cands", "echo_mla_decode", "echo_pool_above", "echo_pool_select",
            "echo_pool_slots", "echo_prefill_block",
            "echo_prefill_block_static", "echo_prefill_scores", "echo_prefill_workspace_size", "echo_quantize_q", "echo_seed_early",
-           "echo_topk_select", "echo_topk_select_cached")
+           "echo_topk_select", "echo_topk_select_cached", "echo_topk_select_cands")
 
 _vp = ctypes.c_void_p
 
@@ -39,6 +41,11 @@ class EchoCacheStruct(ctypes.Structure):
                 ("miss_slot", _vp), ("miss_cnt", _vp), ("early_tok", _vp), ("early_slot", _vp),
                 ("early_cnt", _vp), ("free_snap", _vp), ("host_kv", _vp), ("dev_kv", _vp), ("row_bytes", ctypes.c_int64),
                 ("C", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+class EchoCandsStruct(ctypes.Structure):
+    _fields_ = [("key", _vp), ("idx", _vp), ("cnt", _vp), ("cut", _vp), ("cap", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class EchoError(RuntimeError):
@@ -69,12 +76,20 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         L = ctypes.CDLL(_build.LIB)
         i32, i64, f32 = ctypes.c_int, ctypes.c_int64, ctypes.c_float
         L.echo_quantize_q.restype = i32
-        L.echo_quantize_q.argtypes = [i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+        L.echo_quantize_q.argtypes = [i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
         L.echo_above_words.restype = ctypes.c_size_t
         L.echo_above_words.argtypes = [i32, i64]
         L.echo_index_scores.restype = i32
         L.echo_index_scores.argtypes = [i32, _vp, _vp, i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                         ctypes.POINTER(EchoCacheStruct), i32, _vp, _vp]
+        L.echo_index_scores_cands.restype = i32
+        L.echo_index_scores_cands.argtypes = [i32, _vp, _vp, i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                              ctypes.POINTER(EchoCacheStruct), ctypes.POINTER(EchoCandsStruct),
+                                              i32, _vp, _vp]
+        L.echo_topk_select_cands.restype = i32
+        L.echo_topk_select_cands.argtypes = [i32, _vp, _vp, i64, _vp, i32, _vp, _vp, f32,
+                                             ctypes.POINTER(EchoCandsStruct), _vp, _vp, _vp, i32,
+                                             ctypes.POINTER(EchoCacheStruct), _vp, _vp, _vp, _vp]
         L.echo_early_fetch.restype = i32
         L.echo_early_fetch.argtypes = [i32, _vp, _vp, i64, _vp, i32, ctypes.POINTER(EchoCacheStruct), _vp, _vp]
         L.echo_topk_select.restype = i32
@@ -115,6 +130,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
                                                 _vp, _vp, _vp]
         L.echo_host_device_alias.restype = i32
         L.echo_host_device_alias.argtypes = [_vp, ctypes.POINTER(_vp)]
+        L.echo_debug_set_wait_limit.restype = i32
+        L.echo_debug_set_wait_limit.argtypes = [i64]
         L.echo_device_sm_count.restype = i32
         L.echo_device_sm_count.argtypes = []
         _lib = L
@@ -167,18 +184,25 @@ def host_alias_tensor(host: torch.Tensor, device) -> torch.Tensor:
         return torch.as_tensor(_CudaArray(iface), device=device)
 
 
+def debug_set_wait_limit(ns: int) -> None:
+    """echo_debug_set_wait_limit: the give-up limit of the score epilogue's accumulator wait
+    (tests of the timeout path; ns < 0 restores the default)."""
+    _check("echo_debug_set_wait_limit", load().echo_debug_set_wait_limit(int(ns)))
+
+
 def sm_count() -> int:
     return load().echo_device_sm_count()
 
 
-def quantize_q(q, w, q8, qscale, wfold, status, hist=None, stream=None):
+def quantize_q(q, w, q8, qscale, wfold, status, hist=None, stream=None, cand_cnt=None):
     """echo_quantize_q; q and w may be pinned host tensors, read by the kernel through their
-    device alias."""
+    device alias; cand_cnt: the counts of a Cands (cleared with the histogram)."""
     B = q.shape[0]
     qp = host_device_alias(q) if q.device.type == "cpu" else _ptr(q)
     wp = host_device_alias(w) if w.device.type == "cpu" else _ptr(w)
     _check("echo_quantize_q", load().echo_quantize_q(B, qp, wp, _ptr(q8), _ptr(qscale),
-                                                    _ptr(wfold), _ptr(hist), _ptr(status), _stream(stream)))
+                                                    _ptr(wfold), _ptr(hist), _ptr(cand_cnt), _ptr(status),
+                                                    _stream(stream)))
 
 
 def above_words(B: int, n_tokens: int) -> int:
@@ -186,14 +210,34 @@ def above_words(B: int, n_tokens: int) -> int:
 
 
 def index_scores(tok_off, n_tokens, q8, wfold, k8, ks, scores, theta_hat, hist, status, above=None,
-                 cache=None, stream=None, ctas=0, tok_end=None):
+                 cache=None, stream=None, ctas=0, tok_end=None, cands=None):
     """echo_index_scores; cache: a LayerCache whose residents `above` leaves out (and whose free bits
-    are snapshotted for early_fetch); tok_end: the requests' current ends (None: full regions)."""
+    are snapshotted for early_fetch); tok_end: the requests' current ends (None: full regions);
+    cands: a Cands (or a view of one) to fill: echo_index_scores_cands."""
     B = q8.shape[0]
+    cs = ctypes.byref(cache.struct) if cache is not None else None
+    if cands is not None:
+        _check("echo_index_scores_cands", load().echo_index_scores_cands(
+            B, _ptr(tok_off), _ptr(tok_end), int(n_tokens), _ptr(q8), _ptr(wfold), _ptr(k8), _ptr(ks), _ptr(scores),
+            _ptr(theta_hat), _ptr(hist), _ptr(above), cs, ctypes.byref(cands.struct), int(ctas), _ptr(status),
+            _stream(stream)))
+        return
     _check("echo_index_scores", load().echo_index_scores(
         B, _ptr(tok_off), _ptr(tok_end), int(n_tokens), _ptr(q8), _ptr(wfold), _ptr(k8), _ptr(ks), _ptr(scores),
-        _ptr(theta_hat), _ptr(hist), _ptr(above), ctypes.byref(cache.struct) if cache is not None else None,
-        int(ctas), _ptr(status), _stream(stream)))
+        _ptr(theta_hat), _ptr(hist), _ptr(above), cs, int(ctas), _ptr(status), _stream(stream)))
+
+
+def topk_select_cands(tok_off, n_tokens, scores, k, hist, theta_hat, alpha, cands, sel_idx, kth, status, stats=None,
+                      stream=None, cache=None, sel_slot=None, above=None, early_cap=-1, tok_end=None):
+    """echo_topk_select_cands: top-k from the candidate lists of `cands` (None: from all the
+    scores), one block per request; with cache (and sel_slot) the cached form (slots of the
+    selected tokens as echo_topk_select_cached gives them)."""
+    B = tok_off.shape[0] - 1
+    _check("echo_topk_select_cands", load().echo_topk_select_cands(
+        B, _ptr(tok_off), _ptr(tok_end), int(n_tokens), _ptr(scores), int(k), _ptr(hist), _ptr(theta_hat),
+        float(alpha), ctypes.byref(cands.struct) if cands is not None else None, _ptr(sel_idx), _ptr(kth),
+        _ptr(above), int(early_cap), ctypes.byref(cache.struct) if cache is not None else None, _ptr(sel_slot),
+        _ptr(status), _ptr(stats), _stream(stream)))
 
 
 def early_fetch(tok_off, n_tokens, above, early_cap, cache, status, stream=None, tok_end=None):
@@ -336,6 +380,46 @@ def prefill_block_static(R, row0, n_keys, q, w, k8, ks, k, theta_hat, alpha, sco
         float(alpha), _ptr(scores), int(W), _ptr(hist), _ptr(sel_idx), _ptr(kth), _ptr(union_list),
         _ptr(union_count), _ptr(union_bits), ctypes.byref(cache.struct) if cache is not None else None,
         _ptr(sel_slot), _ptr(status), _ptr(stats), st, cst))
+
+
+class Cands:
+    """Candidate lists of decode top-k for B requests (torch-owned, int32 storage): key / idx
+    [B*cap], cnt [B] (cleared by quantize_q when passed as cand_cnt), cut [B] (all ones = no
+    list yet; top-k writes the next step's)."""
+
+    def __init__(self, B: int, cap: int = CAND_CAP, device="cuda"):
+        i32 = dict(dtype=torch.int32, device=device)
+        self.B, self.cap, self.b0 = int(B), int(cap), 0
+        self.key = torch.zeros(max(self.B * self.cap, 1), **i32)
+        self.idx = torch.zeros(max(self.B * self.cap, 1), **i32)
+        self.cnt = torch.zeros(max(self.B, 1), **i32)
+        self.cut = torch.full((max(self.B, 1),), -1, **i32)
+        self.struct = self._struct(0)
+
+    def _struct(self, b0: int) -> EchoCandsStruct:
+        # b0: absolute first request in the storage of the lists this object was made from
+        root = getattr(self, "_parent", self)
+        s = EchoCandsStruct()
+        s.key, s.idx = _ptr(root.key[b0 * self.cap:]), _ptr(root.idx[b0 * self.cap:])
+        s.cnt, s.cut = _ptr(root.cnt[b0:]), _ptr(root.cut[b0:])
+        s.cap, s.reserved = self.cap, 0
+        return s
+
+    def view(self, b0: int, b1: int) -> "Cands":
+        """The lists of requests [b0, b1) of this object (shared storage)."""
+        root = getattr(self, "_parent", self)
+        a0, a1 = self.b0 + int(b0), self.b0 + int(b1)
+        v = Cands.__new__(Cands)
+        v._parent = root
+        v.B, v.cap, v.b0 = a1 - a0, self.cap, a0
+        v.key, v.idx = root.key, root.idx
+        v.cnt, v.cut = root.cnt[a0:a1], root.cut[a0:a1]
+        v.struct = v._struct(a0)
+        return v
+
+    def reset(self):
+        self.cnt.zero_()
+        self.cut.fill_(-1)
 
 
 class LayerCache:

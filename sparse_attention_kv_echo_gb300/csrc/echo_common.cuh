@@ -111,15 +111,23 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 }
 
 // Wait for the phase of the given parity.  Returns false when *abort becomes
-// non-zero (abort may be NULL) or after kWaitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort) {
+// non-zero (abort may be NULL) or after limit_ns (0: unless the phase is
+// complete at the first look).
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity, const volatile int* abort,
+                                                uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (limit_ns == 0) return false;
     const uint64_t t0 = global_ns();
     for (;;) {
         if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (abort && *abort) return false;
-        if (global_ns() - t0 > kWaitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
+}
+
+// The same with the library's limit, kWaitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort) {
+    return mbar_wait_limit(bar, parity, abort, kWaitNs);
 }
 
 // ---------------------------------------------------------------- TMA

@@ -35,7 +35,7 @@ int check_cache(const echo_cache* c, int B, int m);
 
 // Launchers shared across translation units.
 cudaError_t launch_quantize(int B, const float* q, const float* w, uint8_t* q8, float* qscale, float* wfold,
-                            uint32_t* hist_to_zero, int32_t* status, cudaStream_t s);
+                            uint32_t* hist_to_zero, int32_t* cand_cnt_to_zero, int32_t* status, cudaStream_t s);
 cudaError_t launch_recall(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens, int C, const int32_t* tok_list,
                           const int32_t* slot_list, const int32_t* cnt, const void* host_kv, void* dev_kv,
                           int64_t row_bytes, int32_t* status, cudaStream_t s, bool programmatic);

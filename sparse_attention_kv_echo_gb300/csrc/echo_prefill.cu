@@ -97,10 +97,17 @@ size_t prefill_ws_bytes(int R, int64_t W) {
            round_up(static_cast<size_t>(W), 256) + 256;
 }
 
+// tok_off2 | q8 | qscale | wfold | mark.  The request range the recall reads
+// sits at the same place whatever R and W are, so the blocks before a call's
+// wait on the copy stream never write where an earlier call's recall (of a
+// prompt with another W, sharing the workspace) still reads.
 PrefillWs carve(void* ws, int R, int64_t W) {
+    (void)W;
     uint8_t* p = static_cast<uint8_t*>(ws);
     const size_t r = static_cast<size_t>(R);
     PrefillWs o;
+    o.tok_off2 = reinterpret_cast<int64_t*>(p);
+    p += 256;
     o.q8 = p;
     p += round_up(r * ECHO_HEADS * ECHO_DIM, 256);
     o.qscale = reinterpret_cast<float*>(p);
@@ -108,8 +115,6 @@ PrefillWs carve(void* ws, int R, int64_t W) {
     o.wfold = reinterpret_cast<float*>(p);
     p += round_up(r * ECHO_HEADS * 4, 256);
     o.mark = p;
-    p += round_up(static_cast<size_t>(W), 256);
-    o.tok_off2 = reinterpret_cast<int64_t*>(p);
     return o;
 }
 
@@ -142,7 +147,7 @@ extern "C" int echo_prefill_block(int R, int64_t row0, int64_t n_keys, const flo
         if (rc) return rc;
     }
     const PrefillWs p = carve(ws, R, W);
-    if (launch_quantize(R, q, w, p.q8, p.qscale, p.wfold, hist, status, stream) != cudaSuccess) return ECHO_ECUDA;
+    if (launch_quantize(R, q, w, p.q8, p.qscale, p.wfold, hist, nullptr, status, stream) != cudaSuccess) return ECHO_ECUDA;
     int rc = echo_prefill_scores(R, row0, n_keys, p.q8, p.wfold, k8, ks, scores, W, theta_hat, hist, status, stream);
     if (rc) return rc;
     rc = launch_topk(R, nullptr, nullptr, 0, row0, W, scores, k, hist, theta_hat, alpha, sel_idx, kth, status, stats, stream);
@@ -158,13 +163,18 @@ extern "C" int echo_prefill_block(int R, int64_t row0, int64_t n_keys, const flo
     ECHO_CUDA_OK(prefer_max_shared(union_compact_kernel));
     union_mark_kernel<<<static_cast<int>(grid), 256, 0, stream>>>(sel_idx, total, p.mark, n);
     ECHO_CUDA_OK(cudaGetLastError());
+    if (cache) {
+        // the previous block's recall, still running on copy_stream, reads the request range
+        // (workspace tok_off2, which union_compact_kernel writes next) and the miss lists (which
+        // the cache step rewrites): both wait for it.  Only the tiny union kernels follow the
+        // wait; the quantiser, the scores and top-k above overlap that recall.
+        rc = stream_wait(stream, copy_stream);
+        if (rc) return rc;
+    }
     union_compact_kernel<<<1, kPT, 0, stream>>>(p.mark, n, W, union_list, union_bits, union_count, p.tok_off2,
                                                 n_keys, kth, R, theta_hat, alpha);
     ECHO_CUDA_OK(cudaGetLastError());
     if (!cache) return ECHO_OK;
-    // the previous block's recall reads the miss lists this step rewrites
-    rc = stream_wait(stream, copy_stream);
-    if (rc) return rc;
     return enqueue_cache_step(1, p.tok_off2, nullptr, n_keys, union_list, static_cast<int>(W), nullptr, 0, cache, sel_slot,
                               status, stats, stream, copy_stream, false, false);
 }
@@ -190,21 +200,50 @@ static __device__ __align__(256) uint8_t g_prefill_scratch[ECHO_PREFILL_STATIC_S
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
 void* g_scratch_addr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};   // the context the address belongs to
 
-// Device address of the scratch array on the current device, looked up once
-// per device (with that device current) and remembered.
-int static_scratch(void** out) {
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+// The current context, through the runtime's driver entry point (no libcuda link).
+CUcontext current_context() {
+    static CtxGetCurrentFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    }
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
+
+// Device address of the scratch array on the current device, looked up with
+// that device current and remembered per device; looked up again when the
+// device's context is a new one (after cudaDeviceReset the library image, and
+// the array with it, is loaded anew).  A lookup is not made while `stream` is
+// being captured into a graph: ECHO_EINVAL then.
+int static_scratch(cudaStream_t stream, void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return ECHO_ECUDA;
     if (dev < 0 || dev >= kMaxDevices) return ECHO_EUNSUPPORTED;
+    const CUcontext ctx = current_context();
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_addr[dev]) {
+    if (!g_scratch_addr[dev] || g_scratch_ctx[dev] != ctx) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+            cudaGetLastError();
+            return ECHO_ECUDA;
+        }
+        if (cs != cudaStreamCaptureStatusNone) return ECHO_EINVAL;
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_prefill_scratch) != cudaSuccess || !p) {
             cudaGetLastError();
             return ECHO_ECUDA;
         }
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_addr[dev];
     return ECHO_OK;
@@ -223,7 +262,7 @@ extern "C" int echo_prefill_block_static(int R, int64_t row0, int64_t n_keys, co
     if (R <= 0 || W <= 0) return ECHO_EINVAL;
     if (prefill_ws_bytes(R, W) > static_cast<size_t>(ECHO_PREFILL_STATIC_SCRATCH_BYTES)) return ECHO_ETOOLARGE;
     void* scratch = nullptr;
-    const int rc = static_scratch(&scratch);
+    const int rc = static_scratch(static_cast<cudaStream_t>(stream), &scratch);
     if (rc) return rc;
     // Everything the block needs zeroed (the union marks) it clears itself on
     // the stream; the rest of the scratch is written before it is read.

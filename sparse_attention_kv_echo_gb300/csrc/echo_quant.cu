@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) quantize_kernel(int B, co
                                                                        float* __restrict__ qscale,
                                                                        float* __restrict__ wfold,
                                                                        uint32_t* __restrict__ hist,
+                                                                       int32_t* __restrict__ cand_cnt,
                                                                        int32_t* status) {
     pdl_launch_dependents();  // the score kernel may start its prologue and key loads
     const int lane = threadIdx.x & 31;
@@ -44,6 +45,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) quantize_kernel(int B, co
 #pragma unroll
         for (int i = 0; i < 8; ++i) h[lane + 32 * i] = 0u;
     }
+    if (cand_cnt && (gw % ECHO_HEADS) == 0 && lane == 0) cand_cnt[gw / ECHO_HEADS] = 0;
     const float4 v = reinterpret_cast<const float4*>(q + static_cast<size_t>(gw) * ECHO_DIM)[lane];
     const float wv = w[gw];
     bool bad = !(isfinite(v.x) && isfinite(v.y) && isfinite(v.z) && isfinite(v.w));
@@ -70,25 +72,27 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) quantize_kernel(int B, co
 }  // namespace
 
 cudaError_t launch_quantize(int B, const float* q, const float* w, uint8_t* q8, float* qscale, float* wfold,
-                            uint32_t* hist_to_zero, int32_t* status, cudaStream_t s) {
+                            uint32_t* hist_to_zero, int32_t* cand_cnt_to_zero, int32_t* status, cudaStream_t s) {
     const int rows = B * ECHO_HEADS;
     const int blocks = (rows + kWarpsPerBlock - 1) / kWarpsPerBlock;
     const cudaError_t e = prefer_max_shared(quantize_kernel);
     if (e != cudaSuccess) return e;
-    quantize_kernel<<<blocks, kWarpsPerBlock * 32, 0, s>>>(B, q, w, q8, qscale, wfold, hist_to_zero, status);
+    quantize_kernel<<<blocks, kWarpsPerBlock * 32, 0, s>>>(B, q, w, q8, qscale, wfold, hist_to_zero,
+                                                            cand_cnt_to_zero, status);
     return cudaGetLastError();
 }
 
 }  // namespace echo
 
 extern "C" int echo_quantize_q(int B, const float* q, const float* w, uint8_t* q8, float* qscale, float* wfold,
-                               uint32_t* hist, int32_t* status, echo_stream_t stream) {
+                               uint32_t* hist, int32_t* cand_cnt, int32_t* status, echo_stream_t stream) {
     if (B < 0 || B > ECHO_MAX_REQUESTS) return B < 0 ? ECHO_EINVAL : ECHO_EUNSUPPORTED;
     if (B == 0) return ECHO_OK;
     if (!q || !w || !q8 || !qscale || !wfold) return ECHO_EINVAL;
     if (!echo::is_aligned(q, 16) || !echo::is_aligned(q8, 16) || !echo::is_aligned(w, 4) ||
-        !echo::is_aligned(wfold, 16) || !echo::is_aligned(qscale, 4) || !echo::is_aligned(hist, 4))
+        !echo::is_aligned(wfold, 16) || !echo::is_aligned(qscale, 4) || !echo::is_aligned(hist, 4) ||
+        !echo::is_aligned(cand_cnt, 4))
         return ECHO_EINVAL;
-    return echo::launch_quantize(B, q, w, q8, qscale, wfold, hist, status, stream) == cudaSuccess ? ECHO_OK
+    return echo::launch_quantize(B, q, w, q8, qscale, wfold, hist, cand_cnt, status, stream) == cudaSuccess ? ECHO_OK
                                                                                                  : ECHO_ECUDA;
 }

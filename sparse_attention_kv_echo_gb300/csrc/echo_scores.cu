@@ -19,6 +19,10 @@
 //               tcgen05.ld of its 64 head sums, ReLU, weighted sum, times the
 //               token scale, store, and a warp-private histogram in shared
 //               memory flushed with global atomics when the request changes.
+//               With candidate lists, the tokens whose score key reaches the
+//               request's cut go to a warp-private buffer in shared memory
+//               that is appended to the request's list 32 entries at a time
+//               (one atomic per 32 candidates).
 // Tiles of all requests form one list; CTA c takes a contiguous share of it.
 // The scan of the keys is the HBM-bound part: 132 bytes per token (128 key
 // bytes + 4 scale bytes) against 16384 FP8 MAC-flops.
@@ -67,7 +71,21 @@ struct ScoreArgs {
     const uint32_t* freebits;  // copied to free_snap (fb_words words) for the early fetch
     uint32_t* free_snap;
     int64_t fb_words;
+    // candidate lists (cand_key null: none): tokens with order key >= cand_cut[b]
+    uint32_t* cand_key;
+    int32_t* cand_idx;
+    int32_t* cand_cnt;
+    const uint32_t* cand_cut;
+    int cand_cap;
 };
+
+constexpr uint32_t kNoCut = 0xFFFFFFFFu;   // a request without a candidate list
+
+// Give-up limit of the epilogue's wait for an accumulator (echo_debug_set_wait_limit):
+// the other waits, and every wait that drains copies or MMAs before TMEM is
+// freed, keep kWaitNs.
+__device__ uint64_t g_epilogue_wait_ns = kWaitNs;
+constexpr int kCandBuf = 64;               // per epilogue warp: < 32 waiting + one tile's 32
 
 struct __align__(128) ScoreCtl {
     float ks[kSideStages][kSidePitch];    // per-token key scales of each side stage's tile
@@ -85,6 +103,8 @@ struct __align__(128) ScoreCtl {
     int abort;
     uint32_t scan[16];
     uint32_t hist[kEpiWarps][256];
+    uint32_t cbuf_key[kEpiWarps][kCandBuf];   // candidates waiting to be appended
+    uint32_t cbuf_idx[kEpiWarps][kCandBuf];
 };
 
 // keys | q8 x 2 | ScoreCtl | tstart[B+1] | seg_lo[B] | seg_len[B]  (int32)
@@ -368,11 +388,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         pdl_wait();                            // wfold and the cleared histogram come from the quantiser
+        const uint64_t acc_wait_ns = g_epilogue_wait_ns;
         const int ew = warp - 2;               // 0..7
         const int group = ew >> 2;             // tiles with local index = group (mod 2)
         const int quarter = warp & 3;          // TMEM lanes this warp may access
         const int row = quarter * 32 + lane;   // token row within the tile
         uint32_t* whist = ctl->hist[ew];
+        uint32_t* cbk = ctl->cbuf_key[ew];
+        uint32_t* cbi = ctl->cbuf_idx[ew];
+        uint32_t nbuf = 0, cut = kNoCut;
+        // append the first cnt waiting candidates to request bb's list (one atomic for the
+        // warp), keep the rest at the front of the buffer
+        auto cand_flush = [&](int bb, uint32_t cnt) {
+            __syncwarp();
+            uint32_t base = 0;
+            if (lane == 0) base = static_cast<uint32_t>(atomicAdd(a.cand_cnt + bb, static_cast<int>(cnt)));
+            base = __shfl_sync(0xffffffffu, base, 0);
+            const uint32_t cap = static_cast<uint32_t>(a.cand_cap);
+            const uint32_t ul = static_cast<uint32_t>(lane);
+            if (ul < cnt && base + ul < cap) {
+                const int64_t o = static_cast<int64_t>(bb) * cap + base + ul;
+                a.cand_key[o] = cbk[ul];
+                a.cand_idx[o] = static_cast<int32_t>(cbi[ul]);
+            }
+            const uint32_t rest = nbuf - cnt;
+            uint32_t k2 = 0, i2 = 0;
+            if (ul < rest) {
+                k2 = cbk[cnt + ul];
+                i2 = cbi[cnt + ul];
+            }
+            __syncwarp();
+            if (ul < rest) {
+                cbk[ul] = k2;
+                cbi[ul] = i2;
+            }
+            __syncwarp();
+            nbuf = rest;
+        };
         int b = (ntiles > 0) ? find_request(tstart, B, t_begin) : 0;
         int cur_b = -1;
         float wv[ECHO_HEADS];
@@ -397,7 +449,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     __syncwarp();
                 }
+                if (cur_b >= 0 && nbuf) cand_flush(cur_b, nbuf);
                 cur_b = b;
+                cut = a.cand_key ? a.cand_cut[b] : kNoCut;
                 const float4* wp = reinterpret_cast<const float4*>(a.wfold + static_cast<size_t>(b) * ECHO_HEADS);
 #pragma unroll
                 for (int i = 0; i < ECHO_HEADS / 4; ++i) {
@@ -423,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t tok = static_cast<int64_t>(t - tstart[b]) * kTileM + row;
             const bool valid = tok < nb;
             const uint32_t acc = it % kAccBufs;
-            if (!mbar_wait(smem_addr(&ctl->accfull[acc]), (it / kAccBufs) & 1, abort)) {
+            if (!mbar_wait_limit(smem_addr(&ctl->accfull[acc]), (it / kAccBufs) & 1, abort, acc_wait_ns)) {
                 ok = false;
                 break;
             }
@@ -460,6 +514,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float score = __fmul_rn(__fadd_rn(__fadd_rn(s0, s1), __fadd_rn(s2, s3)), ksv);
             const unsigned vm = __ballot_sync(0xffffffffu, valid);
+            if (cut != kNoCut) {
+                // candidates of the request's top-k: score key at or above the cut
+                const uint32_t key = order_key(score);
+                const bool cnd = valid && key >= cut;
+                const unsigned cm = __ballot_sync(0xffffffffu, cnd);
+                if (cm) {
+                    if (cnd) {
+                        const uint32_t p = nbuf + __popc(cm & ((1u << lane) - 1u));
+                        cbk[p] = key;
+                        cbi[p] = static_cast<uint32_t>(tok);
+                    }
+                    nbuf += __popc(cm);
+                    if (nbuf >= 32) cand_flush(b, 32);
+                }
+            }
+            if (a.cand_key && __any_sync(0xffffffffu, valid && isnan(score)) && lane == 0)
+                set_status(a.status, ECHO_ST_NAN);
             if (a.above) {
                 // tokens above the predicted threshold: one word per 32 rows of the tile
                 const unsigned am = __ballot_sync(0xffffffffu, valid && theta_ok && score > theta && !resident);
@@ -478,6 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             set_status(a.status, ECHO_ST_TIMEOUT);
             *abort = 1;
         }
+        if (cur_b >= 0 && nbuf) cand_flush(cur_b, nbuf);
         if (cur_b >= 0 && a.hist) {
             __syncwarp();
 #pragma unroll
@@ -536,12 +608,12 @@ static int launch_scores(const ScoreArgs& args, const uint8_t* q8, const uint8_t
 
 }  // namespace echo
 
-extern "C" int echo_index_scores(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens,
-                                 const uint8_t* q8,
-                                 const float* wfold, const uint8_t* k8, const float* ks, float* scores,
-                                 const float* theta_hat, uint32_t* hist, uint32_t* above, const echo_cache* cache,
-                                 int ctas, int32_t* status, echo_stream_t stream) {
-    using namespace echo;
+namespace echo {
+
+static int index_scores(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens, const uint8_t* q8,
+                        const float* wfold, const uint8_t* k8, const float* ks, float* scores,
+                        const float* theta_hat, uint32_t* hist, uint32_t* above, const echo_cache* cache,
+                        const echo_cands* cands, int ctas, int32_t* status, cudaStream_t stream) {
     if (B <= 0 || n_tokens < 0) return ECHO_EINVAL;
     if (B > ECHO_MAX_REQUESTS) return ECHO_EUNSUPPORTED;
     if (!tok_off || !q8 || !wfold || !status) return ECHO_EINVAL;
@@ -555,13 +627,40 @@ extern "C" int echo_index_scores(int B, const int64_t* tok_off, const int64_t* t
         if (rc) return rc;
         if (!cache->free_snap || !is_aligned(cache->tok2slot, 16)) return ECHO_EINVAL;
     }
+    if (cands && (!cands->key || !cands->idx || !cands->cnt || !cands->cut || cands->cap <= 0 ||
+                  !is_aligned(cands->key, 4) || !is_aligned(cands->idx, 4) || !is_aligned(cands->cnt, 4) ||
+                  !is_aligned(cands->cut, 4)))
+        return ECHO_EINVAL;
     if (n_tokens == 0) return ECHO_OK;
     ScoreArgs args{B, tok_off, tok_end, n_tokens, 0, 0, 1, wfold, scores, theta_hat, hist, above,
                    cache ? 1 : 0, status, cache ? cache->freebits : nullptr,
                    cache ? cache->free_snap : nullptr,
-                   cache ? static_cast<int64_t>(B) * (cache->C / 32) : 0};
+                   cache ? static_cast<int64_t>(B) * (cache->C / 32) : 0,
+                   cands ? cands->key : nullptr, cands ? cands->idx : nullptr, cands ? cands->cnt : nullptr,
+                   cands ? cands->cut : nullptr, cands ? cands->cap : 0};
     return launch_scores(args, q8, k8, ks, cache ? cache->tok2slot : nullptr, n_tokens, n_tokens / kTileM + B, ctas,
                          stream);
+}
+
+}  // namespace echo
+
+extern "C" int echo_index_scores(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens,
+                                 const uint8_t* q8,
+                                 const float* wfold, const uint8_t* k8, const float* ks, float* scores,
+                                 const float* theta_hat, uint32_t* hist, uint32_t* above, const echo_cache* cache,
+                                 int ctas, int32_t* status, echo_stream_t stream) {
+    return echo::index_scores(B, tok_off, tok_end, n_tokens, q8, wfold, k8, ks, scores, theta_hat, hist, above, cache,
+                              nullptr, ctas, status, stream);
+}
+
+extern "C" int echo_index_scores_cands(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens,
+                                       const uint8_t* q8, const float* wfold, const uint8_t* k8, const float* ks,
+                                       float* scores, const float* theta_hat, uint32_t* hist, uint32_t* above,
+                                       const echo_cache* cache, const echo_cands* cands, int ctas, int32_t* status,
+                                       echo_stream_t stream) {
+    if (!cands) return ECHO_EINVAL;
+    return echo::index_scores(B, tok_off, tok_end, n_tokens, q8, wfold, k8, ks, scores, theta_hat, hist, above, cache,
+                              cands, ctas, status, stream);
 }
 
 extern "C" int echo_prefill_scores(int R, int64_t row0, int64_t n_keys, const uint8_t* q8, const float* wfold,
@@ -576,7 +675,7 @@ extern "C" int echo_prefill_scores(int R, int64_t row0, int64_t n_keys, const ui
     if (!is_aligned(q8, 16) || !is_aligned(wfold, 16) || !is_aligned(k8, 16) || !is_aligned(ks, 16))
         return ECHO_EINVAL;
     ScoreArgs args{R, nullptr, nullptr, n_keys, row0, W, 0, wfold, scores, theta_hat, hist, nullptr, 0, status, nullptr,
-                   nullptr, 0};
+                   nullptr, 0, nullptr, nullptr, nullptr, nullptr, 0};
     const int64_t tiles_ub = static_cast<int64_t>(R) * ((row0 + R + kTileM - 1) / kTileM);
     return launch_scores(args, q8, k8, ks, nullptr, n_keys, tiles_ub, 0, stream);
 }
@@ -584,4 +683,13 @@ extern "C" int echo_prefill_scores(int R, int64_t row0, int64_t n_keys, const ui
 extern "C" size_t echo_above_words(int B, int64_t n_tokens) {
     if (B <= 0 || n_tokens < 0) return 0;
     return 4 * static_cast<size_t>(n_tokens / 128 + B);
+}
+
+extern "C" int echo_debug_set_wait_limit(int64_t ns) {
+    const uint64_t v = ns < 0 ? echo::kWaitNs : static_cast<uint64_t>(ns);
+    if (cudaMemcpyToSymbol(echo::g_epilogue_wait_ns, &v, sizeof(v)) != cudaSuccess) {
+        cudaGetLastError();
+        return ECHO_ECUDA;
+    }
+    return ECHO_OK;
 }

@@ -5,7 +5,8 @@ histogram, threshold state, selection, the GPU cache and its lists, the
 quantised query) and issues the calls of a step:
     echo_quantize_q    -> E4M3 query, folded head weights, cleared histogram
     echo_index_scores  -> scores, shifted-score histogram, above-threshold bits,
-                          free-bit snapshot
+                          free-bit snapshot, and (cands=True, the default) each
+                          request's candidate list for top-k
     echo_early_fetch   -> rows of the tokens above the predicted threshold,
                           copied from the host pool on the step's stream
                           (programmatic dependent of the score kernel) while
@@ -37,7 +38,7 @@ class DecodeLayer:
                  early_cap: int = -1, groups: int | None = None, first_share: float = 0.5,
                  resolved: bool = True, hold_early: bool = False, attention: bool = False,
                  mla_scale: float = 1.0 / math.sqrt(192.0), tok_end=None, cross_layer: bool = False,
-                 pool_slots: int = 0, device="cuda"):
+                 pool_slots: int = 0, cands: bool = True, cand_cap: int = L.CAND_CAP, device="cuda"):
         tok_off = torch.as_tensor(tok_off, dtype=torch.int64)
         self.B = int(tok_off.numel() - 1)
         self.n_tokens = int(k8.shape[0])
@@ -117,6 +118,11 @@ class DecodeLayer:
             self.attn_out = torch.zeros((self.B, L.MLA_HEADS, L.MLA_DV), **f32)
             self.attn_lse = torch.zeros((self.B, L.MLA_HEADS), **f32)
         self.views = [] if self.pool_slots else [self.cache.view(b0, b1) for b0, b1 in self.groups]
+        # candidate lists: the score kernel lists each request's tokens above a cut that top-k sets
+        # for the next step, and top-k selects among them when they hold the top-k
+        self.cands = L.Cands(self.B, cand_cap, device=device) if cands else None
+        self.cands_g = ([self.cands.view(b0, b1) for b0, b1 in self.groups] if self.cands is not None
+                        else [None] * len(self.groups))
         self.sides = [torch.cuda.Stream(device=device) for _ in self.groups]
         self.side = self.sides[0]
         # scoring streams of the groups after the first (the first uses the step's stream);
@@ -131,6 +137,8 @@ class DecodeLayer:
 
     def reset(self):
         self.cache.reset()
+        if self.cands is not None:
+            self.cands.reset()
         self.theta.fill_(math.inf)
         self.status.zero_()
         self.stats.zero_()
@@ -154,12 +162,34 @@ class DecodeLayer:
         L.early_fetch(self.tok_off, self.n_tokens, self.above_seed, self.early_cap, self.cache, self.status,
                       stream=x, tok_end=self.tok_end)
 
+    def _quantize(self, q, w, stream):
+        L.quantize_q(q, w, self.q8, self.qscale, self.wfold, self.status, hist=self.hist, stream=stream,
+                     cand_cnt=None if self.cands is None else self.cands.cnt)
+
+    def _select(self, off, b0, b1, cands, stream, cache=None, above=None, early_cap=-1, end=None):
+        """Top-k of requests [b0, b1) on `stream` (off: their tok_off); with cache the cached form,
+        which also writes sel_slot."""
+        sl = slice(b0, b1)
+        if self.cands is not None:
+            L.topk_select_cands(off, self.n_tokens, self.scores, self.k, self.hist[sl], self.theta[sl], self.alpha,
+                                cands, self.sel_idx[sl], self.kth[sl], self.status, stats=self.stats, stream=stream,
+                                cache=cache, sel_slot=None if cache is None else self.sel_slot[sl], above=above,
+                                early_cap=early_cap, tok_end=end)
+        elif cache is not None:
+            L.topk_select_cached(off, self.n_tokens, self.scores, self.k, self.hist[sl], self.theta[sl], self.alpha,
+                                 self.sel_idx[sl], self.kth[sl], cache, self.sel_slot[sl], self.status,
+                                 stats=self.stats, stream=stream, above=above, early_cap=early_cap, tok_end=end)
+        else:
+            L.topk_select(off, self.n_tokens, self.scores, self.k, self.hist[sl], self.theta[sl], self.alpha,
+                          self.sel_idx[sl], self.kth[sl], self.status, stats=self.stats, stream=stream, tok_end=end)
+
     def _step_pool(self, q, w, main, out_host):
         # per-request scores and marks; the early fetch, top-k's slots and the cache step on the pool
         n, end = self.n_tokens, self.tok_end
-        L.quantize_q(q, w, self.q8, self.qscale, self.wfold, self.status, hist=self.hist, stream=main)
+        self._quantize(q, w, main)
         L.index_scores(self.tok_off, n, self.q8, self.wfold, self.k8, self.ks, self.scores, self.theta, self.hist,
-                       self.status, above=self.above_req if self.predictor else None, stream=main, tok_end=end)
+                       self.status, above=self.above_req if self.predictor else None, stream=main, tok_end=end,
+                       cands=self.cands)
         if self.predictor:
             L.pool_above(self.tok_off, n, self.above_req, self.cache, self.above_pool, self.status, stream=main,
                          tok_end=end)
@@ -167,8 +197,7 @@ class DecodeLayer:
         side = self.sides[0]
         side.wait_stream(main)
         copy = side if self.hold_early else main
-        L.topk_select(self.tok_off, n, self.scores, self.k, self.hist, self.theta, self.alpha, self.sel_idx, self.kth,
-                      self.status, stats=self.stats, stream=side, tok_end=end)
+        self._select(self.tok_off, 0, self.B, self.cands, side, end=end)
         ev = torch.cuda.Event()
         ev.record(side)
         self.selected_evs = [ev]
@@ -184,21 +213,16 @@ class DecodeLayer:
 
     def _step_seeded(self, q, w, main, out_host, mla_q):
         # scores without threshold bits or snapshot; top-k and the cache step take the seeded set
-        L.quantize_q(q, w, self.q8, self.qscale, self.wfold, self.status, hist=self.hist, stream=main)
+        self._quantize(q, w, main)
         L.index_scores(self.tok_off, self.n_tokens, self.q8, self.wfold, self.k8, self.ks, self.scores, self.theta,
-                       self.hist, self.status, stream=main, tok_end=self.tok_end)
+                       self.hist, self.status, stream=main, tok_end=self.tok_end, cands=self.cands)
         side = self.sides[0]
         side.wait_stream(main)
         if self.seed_ev is not None:
             side.wait_event(self.seed_ev)
         copy = side if self.hold_early else self.xfer
-        if self.resolved:
-            L.topk_select_cached(self.tok_off, self.n_tokens, self.scores, self.k, self.hist, self.theta, self.alpha,
-                                 self.sel_idx, self.kth, self.cache, self.sel_slot, self.status, stats=self.stats,
-                                 stream=side, above=self.above_seed, early_cap=self.early_cap, tok_end=self.tok_end)
-        else:
-            L.topk_select(self.tok_off, self.n_tokens, self.scores, self.k, self.hist, self.theta, self.alpha,
-                          self.sel_idx, self.kth, self.status, stats=self.stats, stream=side, tok_end=self.tok_end)
+        self._select(self.tok_off, 0, self.B, self.cands, side, cache=self.cache if self.resolved else None,
+                     above=self.above_seed, early_cap=self.early_cap, end=self.tok_end)
         ev = torch.cuda.Event()
         ev.record(side)
         self.selected_evs = [ev]
@@ -247,12 +271,11 @@ class DecodeLayer:
                 raise ValueError("seeded steps need cross_layer=True")
             self._step_seeded(q, w, main, out_host, mla_q)
             return
-        L.quantize_q(q, w, self.q8, self.qscale, self.wfold, self.status, hist=self.hist, stream=main)
+        self._quantize(q, w, main)
         if not self.predictor:
             L.index_scores(self.tok_off, self.n_tokens, self.q8, self.wfold, self.k8, self.ks, self.scores,
-                           self.theta, self.hist, self.status, stream=main, tok_end=self.tok_end)
-            L.topk_select(self.tok_off, self.n_tokens, self.scores, self.k, self.hist, self.theta, self.alpha,
-                          self.sel_idx, self.kth, self.status, stats=self.stats, stream=main, tok_end=self.tok_end)
+                           self.theta, self.hist, self.status, stream=main, tok_end=self.tok_end, cands=self.cands)
+            self._select(self.tok_off, 0, self.B, self.cands, main, end=self.tok_end)
             L.cache_step(self.tok_off, self.n_tokens, self.sel_idx, self.cache, self.sel_slot, self.status,
                          stats=self.stats, stream=main, copy_stream=main, tok_end=self.tok_end)
             if out_host is not None:
@@ -273,7 +296,8 @@ class DecodeLayer:
             ctas = 0 if g == 0 else max(sms - L.EARLY_FETCH_BLOCKS * g, sms // 4)
             L.index_scores(self.tok_off[b0:b1 + 1], self.n_tokens, self.q8[b0:b1], self.wfold[b0:b1], self.k8,
                            self.ks, self.scores, self.theta[b0:b1], self.hist[b0:b1], self.status,
-                           above=self.above_g[g], cache=self.views[g], stream=s, ctas=ctas, tok_end=end(b0, b1))
+                           above=self.above_g[g], cache=self.views[g], stream=s, ctas=ctas, tok_end=end(b0, b1),
+                           cands=self.cands_g[g])
             scored = torch.cuda.Event()
             scored.record(s)
             gstream.append(s)
@@ -292,11 +316,9 @@ class DecodeLayer:
             side.wait_event(scored)
             off = self.tok_off[b0:b1 + 1]
             if self.resolved:
-                # top-k looks up every selected token's slot (resident or early) on its slices
-                L.topk_select_cached(off, self.n_tokens, self.scores, self.k, self.hist[b0:b1], self.theta[b0:b1],
-                                     self.alpha, self.sel_idx[b0:b1], self.kth[b0:b1], self.views[g],
-                                     self.sel_slot[b0:b1], self.status, stats=self.stats, stream=side,
-                                     above=self.above_g[g], early_cap=self.early_cap, tok_end=end(b0, b1))
+                # top-k looks up every selected token's slot (resident or early)
+                self._select(off, b0, b1, self.cands_g[g], side, cache=self.views[g], above=self.above_g[g],
+                             early_cap=self.early_cap, end=end(b0, b1))
                 ev = torch.cuda.Event()
                 ev.record(side)
                 self.selected_evs.append(ev)
@@ -304,9 +326,7 @@ class DecodeLayer:
                                       self.status, stats=self.stats, stream=side, copy_stream=copy,
                                       hold_early=self.hold_early, tok_end=end(b0, b1))
             else:
-                L.topk_select(off, self.n_tokens, self.scores, self.k, self.hist[b0:b1], self.theta[b0:b1],
-                              self.alpha, self.sel_idx[b0:b1], self.kth[b0:b1], self.status, stats=self.stats,
-                              stream=side, tok_end=end(b0, b1))
+                self._select(off, b0, b1, self.cands_g[g], side, end=end(b0, b1))
                 ev = torch.cuda.Event()
                 ev.record(side)
                 self.selected_evs.append(ev)

@@ -64,7 +64,7 @@ def check_scores(layer_inputs, q, w, gpu_scores, sample=None, rng=None):
 
 def run_decode(w: wl.Workload, steps: int, predictor: bool, cap: int = -1, score_sample=None,
                check_every_score_step=True, keys_device="cpu", layer: int = 0, resolved: bool = True,
-               hold_early: bool = False):
+               hold_early: bool = False, cands: bool = True):
     """Runs `steps` decode steps of one layer on the GPU and checks each against the oracle."""
     dev = "cuda"
     off = wl.tok_offsets(w.lengths)
@@ -75,7 +75,7 @@ def run_decode(w: wl.Workload, steps: int, predictor: bool, cap: int = -1, score
     host = wl.make_host_pool(w, layer, device=keys_device, pin=True)
     host_before = host.clone()
     lay = DecodeLayer(off, k8c.to(dev), ksc.to(dev), w.k, w.C, host, predictor=predictor, early_cap=cap,
-                      resolved=resolved, hold_early=hold_early)
+                      resolved=resolved, hold_early=hold_early, cands=cands)
     o = OracleLayer(w.B, w.total_tokens, w.C)
     qsrc = wl.QueryStream(w, layer, device=keys_device)
     rng = np.random.default_rng(7)
@@ -151,6 +151,7 @@ def run_decode(w: wl.Workload, steps: int, predictor: bool, cap: int = -1, score
         report["misses"].append(misses)
     report["boundary_max"] = int(lay.stats[L.STAT_BOUNDARY_MAX].item())
     report["fallbacks"] = int(lay.stats[L.STAT_TOPK_FALLBACK].item())
+    report["cand_miss"] = int(lay.stats[L.STAT_CAND_MISS].item())
     assert torch.equal(host.view(torch.int16), host_before.view(torch.int16))  # no write-back
     return report
 
@@ -238,25 +239,33 @@ def run_decode_growing(w: wl.Workload, steps: int, room: int, hold_early: bool =
 
 
 def run_stack(w: wl.Workload, steps: int, n_layers: int, cross_layer: bool, hold_early: bool = False,
-              graph: bool = True):
+              graph: bool = True, keys_device: str = "cpu", predictor: bool = True, score_steps=None,
+              score_sample: int = 64, threads: int = 1):
     """A DecodeStack of n_layers layers (each its own keys, weights, queries, host pool and cache),
     optionally captured as one CUDA graph; every step of every layer is checked against the oracle:
     layer 0's early set by the threshold predictor, the others' (cross_layer) from the previous
-    layer's selection.  Returns the per-layer early counts and misses per step."""
+    layer's selection.  Per step and layer: histograms, early lists, top-k, k-th scores, thresholds,
+    slots, miss lists, tables, free bits and the rows of every selected token, bit-exact; fp64
+    scores of score_sample tokens per request on the steps in score_steps (None: every step).
+    threads: the oracle's per-request work in parallel (its C calls release the interpreter).
+    Returns the per-layer early counts and misses per step."""
+    from concurrent.futures import ThreadPoolExecutor
+
     from sparse_attention_kv_echo_gb300 import DecodeStack
     dev = "cuda"
     off = wl.tok_offsets(w.lengths)
     lays, inputs, qsrcs, hosts, orcs = [], [], [], [], []
     for l in range(n_layers):
-        k8c, ksc = wl.make_keys(w, l)
-        wt = wl.make_weights(w, l)
-        host = wl.make_host_pool(w, l, pin=True)
+        k8c, ksc = wl.make_keys(w, l, device=keys_device)
+        wt = wl.make_weights(w, l, device=keys_device).cpu()
+        host = wl.make_host_pool(w, l, device=keys_device, pin=True)
         lays.append(DecodeLayer(off, k8c.to(dev), ksc.to(dev), w.k, w.C, host, hold_early=hold_early,
-                                cross_layer=cross_layer and l > 0, device=dev))
-        inputs.append((k8c.numpy(), ksc.numpy(), wt.numpy()))
-        qsrcs.append(wl.QueryStream(w, l))
-        hosts.append(host.view(torch.uint8).numpy())
+                                predictor=predictor, cross_layer=cross_layer and l > 0, device=dev))
+        inputs.append((k8c.cpu().numpy(), ksc.cpu().numpy(), wt.numpy()))
+        qsrcs.append(wl.QueryStream(w, l, device=keys_device))
+        hosts.append(host.to(dev))
         orcs.append(OracleLayer(w.B, w.total_tokens, w.C))
+        del k8c, ksc
     stack = DecodeStack(lays, cross_layer=cross_layer)
     main = torch.cuda.Stream()
     for l, lay in enumerate(lays):
@@ -273,6 +282,7 @@ def run_stack(w: wl.Workload, steps: int, n_layers: int, cross_layer: bool, hold
         torch.cuda.synchronize()
     rng = np.random.default_rng(11)
     report = dict(early=[[] for _ in lays], misses=[[] for _ in lays])
+    pool = ThreadPoolExecutor(max_workers=max(1, threads))
     for t in range(steps):
         qs = [qsrcs[l].next().cpu() for l in range(n_layers)]
         with torch.cuda.stream(main):
@@ -289,43 +299,69 @@ def run_stack(w: wl.Workload, steps: int, n_layers: int, cross_layer: bool, hold
             o = orcs[l]
             k8, ks, wt = inputs[l]
             gs = lay.scores.cpu().numpy()
-            check_scores((off, k8, ks), qs[l].numpy(), wt, gs, sample=64, rng=rng)
+            if score_steps is None or t in score_steps:
+                check_scores((off, k8, ks), qs[l].numpy(), wt, gs, sample=score_sample, rng=rng)
+            gh = lay.hist.cpu().numpy().view(np.uint32)
             g_sel, g_slot = lay.sel_idx.cpu().numpy(), lay.sel_slot.cpu().numpy()
+            g_kth = lay.kth.cpu().numpy()
+            g_theta = lay.theta.cpu().numpy()
             g_ecnt = lay.cache.early_cnt.cpu().numpy()
             g_etok, g_eslot = lay.cache.early_tok.cpu().numpy(), lay.cache.early_slot.cpu().numpy()
             g_mcnt = lay.cache.miss_cnt.cpu().numpy()
+            g_mtok, g_mslot = lay.cache.miss_tok.cpu().numpy(), lay.cache.miss_slot.cpu().numpy()
             theta_before = o.theta.copy()
-            misses = 0
-            o_sel = []
-            for b in range(w.B):
+
+            def one(b):
                 lo, hi = int(off[b]), int(off[b + 1])
                 sc = gs[lo:hi]
                 t2s = o.t2s[lo:hi]
                 s2t = o.s2t[b * w.C:(b + 1) * w.C]
+                assert np.array_equal(gh[b], orc.hist256(sc, theta_before[b])), (t, l, b, "hist")
+                et = None
                 if cross_layer and l > 0:
                     et, es = orc.early_from_selection(prev_sel[b], hi - lo, lay.early_cap, t2s, s2t)
-                else:
+                elif predictor:
                     et, es = orc.early_fetch(sc, theta_before[b], lay.early_cap, t2s, s2t)
-                assert g_ecnt[b] == et.size, (t, l, b, "early count", g_ecnt[b], et.size)
-                assert np.array_equal(g_etok[b * w.C:b * w.C + et.size], et), (t, l, b, "early tok")
-                assert np.array_equal(g_eslot[b * w.C:b * w.C + et.size], es), (t, l, b, "early slot")
+                if et is not None:
+                    assert g_ecnt[b] == et.size, (t, l, b, "early count", g_ecnt[b], et.size)
+                    assert np.array_equal(g_etok[b * w.C:b * w.C + et.size], et), (t, l, b, "early tok")
+                    assert np.array_equal(g_eslot[b * w.C:b * w.C + et.size], es), (t, l, b, "early slot")
                 idx, kth = orc.topk(sc, w.k)
                 assert np.array_equal(g_sel[b], idx), (t, l, b, "topk")
-                o_sel.append(idx)
+                assert g_kth[b] == np.float32(kth) or (math.isinf(kth) and math.isinf(g_kth[b])), (t, l, b, "kth")
                 o.theta[b] = orc.ema(theta_before[b], kth, 0.5)
+                assert g_theta[b] == o.theta[b] or (np.isinf(o.theta[b]) and np.isinf(g_theta[b])), \
+                    (t, l, b, "theta")
                 sel_slot, mt, ms, _ = orc.cache_step(idx, t2s, s2t, early_tok=et, hold_early=hold_early)
                 assert np.array_equal(g_slot[b], sel_slot), (t, l, b, "sel_slot")
                 assert g_mcnt[b] == mt.size, (t, l, b, "miss count")
-                misses += mt.size
-                report["early"][l].append(int(et.size))
-            report["misses"][l].append(misses)
-            assert np.array_equal(lay.cache.tok2slot.cpu().numpy(), o.t2s), (t, l, "tok2slot")
+                assert np.array_equal(g_mtok[b * w.C:b * w.C + mt.size], mt), (t, l, b, "miss tok")
+                assert np.array_equal(g_mslot[b * w.C:b * w.C + mt.size], ms), (t, l, b, "miss slot")
+                return idx, 0 if et is None else int(et.size), int(mt.size)
+
+            res = list(pool.map(one, range(w.B)))
+            o_sel = [r[0] for r in res]
+            for r in res:
+                report["early"][l].append(r[1])
+            report["misses"][l].append(sum(r[2] for r in res))
+            assert np.array_equal(lay.cache.tok2slot.cpu().numpy()[:w.total_tokens], o.t2s), (t, l, "tok2slot")
             assert np.array_equal(lay.cache.slot2tok.cpu().numpy(), o.s2t), (t, l, "slot2tok")
-            g_dev = lay.cache.dev_kv.view(torch.uint8).cpu().numpy().reshape(w.B * w.C, -1)
-            for b in range(w.B):
-                v = g_slot[b] >= 0
-                assert np.array_equal(g_dev[b * w.C + g_slot[b][v]], hosts[l][off[b] + g_sel[b][v]]), (t, l, b)
+            free = (o.s2t < 0).reshape(-1, 32)
+            want_fb = (free.astype(np.uint64) << np.arange(32, dtype=np.uint64)).sum(1).astype(np.uint32)
+            assert np.array_equal(lay.cache.freebits.cpu().numpy().view(np.uint32), want_fb), (t, l, "freebits")
+            # every selected token's device row is its host row (compared on the device)
+            sel_t = torch.from_numpy(g_sel).to(dev).long()
+            slot_t = torch.from_numpy(g_slot).to(dev).long()
+            valid = sel_t >= 0
+            bidx = torch.arange(w.B, device=dev)[:, None].expand_as(sel_t)
+            offs = torch.from_numpy(off[:-1]).to(dev)[:, None]
+            rows_dev = lay.cache.dev_kv[(bidx * w.C + slot_t)[valid]]
+            rows_host = hosts[l][(offs + sel_t)[valid]]
+            assert torch.equal(rows_dev.view(torch.int16), rows_host.view(torch.int16)), (t, l, "rows")
             prev_sel = o_sel
+    pool.shutdown()
+    report["cand_miss"] = [int(lay.stats[L.STAT_CAND_MISS].item()) for lay in lays]
+    report["fallbacks"] = [int(lay.stats[L.STAT_TOPK_FALLBACK].item()) for lay in lays]
     return report
 
 

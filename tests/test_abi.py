@@ -90,9 +90,52 @@ def test_host_checks_reject_bad_arguments(L):
                               None) == lib.ECHO_EINVAL
     assert L.echo_topk_select(-3, dummy, None, 10, dummy, 4, None, None, 0.5, dummy, dummy, dummy, None,
                               None) == lib.ECHO_EINVAL
-    assert L.echo_quantize_q(-1, dummy, dummy, dummy, dummy, dummy, None, dummy, None) == lib.ECHO_EINVAL
-    assert L.echo_quantize_q(1, dummy, dummy, dummy, dummy, v(0x1004), None, dummy, None) == lib.ECHO_EINVAL
-    assert L.echo_quantize_q(0, None, None, None, None, None, None, None, None) == lib.ECHO_OK
+    # quantize_q(B, q, w, q8, qscale, wfold, hist, cand_cnt, status, stream)
+    assert L.echo_quantize_q(-1, dummy, dummy, dummy, dummy, dummy, None, None, dummy, None) == lib.ECHO_EINVAL
+    assert L.echo_quantize_q(1, dummy, dummy, dummy, dummy, v(0x1004), None, None, dummy, None) == lib.ECHO_EINVAL
+    assert L.echo_quantize_q(1, dummy, dummy, dummy, dummy, dummy, None, v(0x1002), dummy, None) == lib.ECHO_EINVAL
+    assert L.echo_quantize_q(0, None, None, None, None, None, None, None, None, None) == lib.ECHO_OK
+
+
+def test_candidate_list_checks(L):
+    """echo_index_scores_cands needs complete lists; echo_topk_select_cands refuses bad sizes,
+    incomplete lists and a cache without sel_slot or above its shared-memory limit."""
+    from sparse_attention_kv_echo_gb300 import lib
+    v = ctypes.c_void_p
+    d = v(0x1000)
+    cl = lib.EchoCandsStruct()
+    cl.key, cl.idx, cl.cnt, cl.cut, cl.cap = 0x1000, 0x1000, 0x1000, 0x1000, 64
+    cands = ctypes.byref(cl)
+
+    def scores(c, n=10):
+        return L.echo_index_scores_cands(1, d, None, n, d, d, d, d, d, None, None, None, None, c, 0, d, None)
+    assert scores(None) == lib.ECHO_EINVAL
+    assert scores(cands, n=0) == lib.ECHO_OK
+    cl.cap = 0
+    assert scores(cands) == lib.ECHO_EINVAL
+    cl.cap, cl.cut = 64, None
+    assert scores(cands) == lib.ECHO_EINVAL
+    cl.cut = 0x1000
+
+    # topk_select_cands(B, tok_off, tok_end, n, scores, k, hist, theta, alpha, cands, sel, kth, above, cap,
+    #                   cache, sel_slot, status, stats, stream)
+    def topk(B=1, k=16, c=cands, cache=None, slot=None):
+        return L.echo_topk_select_cands(B, d, None, 100, d, k, None, None, 0.5, c, d, d, None, -1, cache, slot, d,
+                                        None, None)
+    assert topk(B=0) == lib.ECHO_EINVAL
+    assert topk(k=0) == lib.ECHO_EINVAL
+    assert topk(B=lib.MAX_REQUESTS + 1) == lib.ECHO_EUNSUPPORTED
+    cl.idx = None
+    assert topk() == lib.ECHO_EINVAL
+    cl.idx = 0x1000
+    s = lib.EchoCacheStruct()
+    for f, _ in lib.EchoCacheStruct._fields_[:12]:
+        setattr(s, f, 0x2000)
+    s.row_bytes, s.C = 1152, 64
+    assert topk(cache=ctypes.byref(s)) == lib.ECHO_EINVAL                    # no sel_slot
+    assert topk(k=65, cache=ctypes.byref(s), slot=d) == lib.ECHO_ECAPACITY   # k > C
+    s.C = 65536
+    assert topk(cache=ctypes.byref(s), slot=d) == lib.ECHO_EUNSUPPORTED      # free bits beyond shared memory
 
 
 def test_cache_checks(L):

@@ -4,8 +4,8 @@ Small prompt, every block, every row: causal scores within the fp64
 tolerance (sampled rows), per-row shifted histograms, exact per-row top-k
 and k-th scores, the union of a block's selections, the block threshold
 EMA, the cache step on the union (tables, slots) and the recalled bytes.
-Full-size prompt (102400 tokens in 2048-row blocks): sampled rows against
-the oracle, the rest through properties that hold at any size.
+The full-size prompt (102400 tokens in 2048-row blocks, every block) is in
+test_gpu_full.py.
 """
 import math
 
@@ -28,12 +28,12 @@ def _lib():
     L.load(build_if_missing=True)
 
 
-def _check_rows_scores(rows, row0, gs, q, wt, k8, ks):
+def _check_rows_scores(rows, row0, gs, q, wt, k8, ks, at=None):
     q8, qs, _ = orc.quantize_q(q, wt)
     for r in rows:
         p = row0 + r
         ref, ab = orc.scores(q8[r], qs[r], wt[r], k8, ks, tok=np.arange(p + 1, dtype=np.int64))
-        bad, _ = score_tolerance_ok(gs[r, :p + 1], ref, ab)
+        bad, _ = score_tolerance_ok(gs[r if at is None else at[int(r)], :p + 1], ref, ab)
         assert bad.size == 0, (r, bad[:5])
 
 
@@ -58,23 +58,29 @@ def _run(w, full_rows=True, row_sample=8, blocks=None, keys_device="cpu", same_k
         pr.wait_recall()
         torch.cuda.synchronize()
         assert int(pr.status.item()) == 0, f"status {int(pr.status.item()):#x} at block {i}"
-        gs = pr.scores[:R].cpu().numpy()
+        rows = np.arange(R) if full_rows else np.unique(np.concatenate(
+            [rng.choice(R, min(row_sample, R), replace=False), [R - 1]]))
+        # the scores of the rows checked (every row, or the sampled ones and the last), as rows of gs
+        if full_rows:
+            gs = pr.scores[:R].cpu().numpy()
+            at = {int(r): int(r) for r in rows}
+        else:
+            gs = pr.scores[torch.from_numpy(rows).to(dev)].cpu().numpy()
+            at = {int(r): j for j, r in enumerate(rows)}
         g_sel = pr.sel_idx[:R].cpu().numpy()
         g_kth = pr.kth[:R].cpu().numpy()
         g_hist = pr.hist[:R].cpu().numpy().view(np.uint32)
         g_list = pr.union_list.cpu().numpy()
         g_cnt = int(pr.union_count.item())
         g_theta = float(pr.theta.item())
-        rows = np.arange(R) if full_rows else np.unique(np.concatenate(
-            [rng.choice(R, min(row_sample, R), replace=False), [R - 1]]))
         _check_rows_scores(rows[:row_sample] if full_rows else rows, row0, gs, q.cpu().numpy(),
-                           wt.cpu().numpy(), k8, ks)
+                           wt.cpu().numpy(), k8, ks, at)
         for r in rows:
             p = row0 + r
-            idx, kt = orc.topk(gs[r, :p + 1], w.k)
+            idx, kt = orc.topk(gs[at[int(r)], :p + 1], w.k)
             assert np.array_equal(g_sel[r], idx), (i, r)
             assert g_kth[r] == np.float32(kt), (i, r)
-            assert np.array_equal(g_hist[r], orc.hist256(gs[r, :p + 1], theta)), (i, r)
+            assert np.array_equal(g_hist[r], orc.hist256(gs[at[int(r)], :p + 1], theta)), (i, r)
             assert np.all(g_sel[r][g_sel[r] >= 0] <= p)                     # causal
         # union: exactly the tokens some row selected, ascending, -1 padded
         sel_all = g_sel[g_sel >= 0]
@@ -87,7 +93,7 @@ def _run(w, full_rows=True, row_sample=8, blocks=None, keys_device="cpu", same_k
         assert np.array_equal(g_list[:g_cnt], want_union)
         assert np.all(g_list[g_cnt:] == -1)
         # block threshold: EMA of the last row's k-th score
-        _, kt_last = orc.topk(gs[R - 1, :row0 + R], w.k)
+        _, kt_last = orc.topk(gs[at[R - 1], :row0 + R], w.k)
         theta = np.float32(orc.ema(theta, kt_last, 0.5))
         assert g_theta == theta or (math.isinf(g_theta) and math.isinf(theta))
         # cache step on the union
@@ -126,7 +132,3 @@ def test_prefill_all_keys_equal():
     assert np.array_equal(sel[-1], np.arange(256, dtype=np.int32))
 
 
-def test_prefill_full_size_sampled():
-    """102400-token prompt, 2048-row blocks, k = 2048, C = 260000: first blocks, sampled rows."""
-    w = wl.WORKLOADS["prefill"]
-    _run(w, full_rows=False, row_sample=6, blocks=3, keys_device="cuda")
