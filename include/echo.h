@@ -78,10 +78,12 @@ typedef struct CUstream_st* echo_stream_t; /* a cudaStream_t; NULL = legacy defa
 #define ECHO_STAT_MISSES 3          /* tokens recalled after top-k */
 #define ECHO_STAT_EARLY_USED 4      /* early-fetched tokens that top-k then selected */
 #define ECHO_STAT_CAND_MISS 5       /* top-k given candidate lists that selected from all the scores */
+#define ECHO_STAT_REVIVED 6         /* lazy reuse: freed tokens selected again while their slot kept them */
 #define ECHO_STATS_N 8
 
 /* echo_cache_step flags */
 #define ECHO_CACHE_HOLD_EARLY 1     /* hold the unselected early tokens' slots until the misses are placed */
+#define ECHO_CACHE_LAZY 2           /* lazy-reuse eviction: a freed slot keeps its token until handed out */
 
 /*
  * Requests.  tok_off [B+1] (int64, device) gives request b its region of rows
@@ -261,7 +263,22 @@ int echo_topk_select(int B, const int64_t* tok_off, const int64_t* tok_end, int6
  * Needs m <= C; holding, also m + (unselected early tokens) <= C, which an
  * early_cap of at most C - m guarantees (else a miss may find no slot:
  * ECHO_ST_NOSLOT).  Holding, the recall may run before echo_early_fetch's
- * copy ends.  flags: 0 or ECHO_CACHE_HOLD_EARLY (other bits: ECHO_EINVAL).
+ * copy ends.  flags: 0, ECHO_CACHE_HOLD_EARLY or ECHO_CACHE_LAZY (other bits,
+ * or both: ECHO_EINVAL).
+ * Lazy-reuse eviction (ECHO_CACHE_LAZY; a variant -- the survey's reading of
+ * "freed slots keep their token until overwritten" -- not the contract): a
+ * token freed in step 1 keeps its bytes and both table entries (a ghost: its
+ * slot is free, the token still maps to it) until its slot is handed to
+ * another token, which drops it from the tables; every early token of step 0
+ * enters the tables in its slot (dropping the ghost there), a selected one
+ * stays resident, an unselected one becomes a ghost; in step 2 a selected
+ * ghost is a hit, resident again in its slot with no copy
+ * (ECHO_STAT_REVIVED); a miss that takes a ghost's slot drops the ghost.
+ * Ghosts map to their slots, so echo_index_scores leaves them out of the
+ * early set (their bytes are in the cache).  The tables keep every present
+ * token (resident or ghost) mutually inverse; freebits mark the slots no
+ * resident token holds.  Not with echo_cache_step_resolved or the held-slot
+ * form (ECHO_EUNSUPPORTED / ECHO_EINVAL); the look-up is the cache step's.
  * Steps 0-3 are launched as a programmatic dependent of the
  * kernel before them on `stream`: while that kernel still runs (if it lets
  * dependents start early, as echo_topk_select and echo_index_scores do) they
@@ -445,16 +462,16 @@ int echo_prefill_block_static(int R, int64_t row0, int64_t n_keys, const float* 
 /*
  * Failure-path knob, for tests (the pages have no counterpart).  Every wait
  * inside a kernel gives up after a limit (2 s) and reports ECHO_ST_TIMEOUT
- * instead of hanging; this call sets the limit of one of them -- the score
- * kernel's wait for an accumulator in its epilogue -- on the current device:
- * ns >= 0 the new limit (0: give up unless the accumulator is ready at the
- * first look), ns < 0 back to 2 s.  A score call that gives up sets
- * ECHO_ST_TIMEOUT, its outputs are invalid, and its kernel still drains its
- * copies and MMAs before it frees tensor memory and exits, so the next call
- * runs normally.  The waits that drain are never shortened.  Synchronous
- * (a copy to device memory); not for use while a score call is in flight.
+ * instead of hanging.  With limit_ns >= 0, the score kernel's epilogue (on the
+ * current device) first waits on a barrier that nothing arrives on, giving up
+ * after limit_ns: every score call then takes its timeout path -- it sets
+ * ECHO_ST_TIMEOUT, its outputs are invalid, and its kernel drains its copies
+ * and MMAs before it frees tensor memory and exits, so the next call runs
+ * normally.  limit_ns < 0 turns the wait off (the default).  The waits that
+ * drain are never shortened.  Synchronous (a copy to device memory); not for
+ * use while a score call is in flight.
  */
-int echo_debug_set_wait_limit(int64_t ns);
+int echo_debug_stall_epilogue(int64_t limit_ns);
 
 /*
  * Sparse MLA decode attention over the selected slots [EXPL section 2: a

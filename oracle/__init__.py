@@ -85,6 +85,13 @@ def lib():
             L.orc_cache_step.argtypes = [ctypes.c_int64, ctypes.c_int, c_i32p, c_i32p, c_i32p,
                                          ctypes.c_int, c_i32p, ctypes.c_int32, ctypes.c_int, c_i32p, c_i32p,
                                          c_i32p, c_i32p, c_i32p]
+            L.orc_lazy_early.restype = ctypes.c_int
+            L.orc_lazy_early.argtypes = [ctypes.c_int64, ctypes.c_int, c_f32p, ctypes.c_float, ctypes.c_int,
+                                         c_i32p, c_i32p, c_u8p, c_i32p, c_i32p, c_i32p]
+            L.orc_lazy_cache_step.restype = ctypes.c_int
+            L.orc_lazy_cache_step.argtypes = [ctypes.c_int64, ctypes.c_int, c_i32p, c_i32p, c_u8p, c_i32p,
+                                              ctypes.c_int, c_i32p, c_i32p, ctypes.c_int32, c_i32p, c_i32p,
+                                              c_i32p, c_i32p, c_i32p]
             L.orc_early_cap_for.restype = ctypes.c_int
             L.orc_early_cap_for.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
             L.orc_recall.restype = None
@@ -241,6 +248,47 @@ def early_from_selection(prev_sel, n: int, cap: int, tok2slot, slot2tok):
                                         _p(et, ctypes.c_int32), _p(es, ctypes.c_int32), ctypes.byref(cnt))
     _check(rc, "early_from_selection")
     return et[:cnt.value].copy(), es[:cnt.value].copy()
+
+
+def lazy_early(scores_f32, theta: float, cap: int, tok2slot, slot2tok, free):
+    """The early set under lazy-reuse eviction (nothing updated): tokens above theta that are
+    not present, ascending, <= min(cap, free slots), with the lowest free slots.  free: uint8
+    [C], 1 = the slot holds no resident token.  -> (early_tok, early_slot)."""
+    s = _c(scores_f32, np.float32).reshape(-1)
+    for a, dt in ((tok2slot, np.int32), (slot2tok, np.int32), (free, np.uint8)):
+        assert a.dtype == dt and a.flags.c_contiguous
+    n, C = s.size, slot2tok.size
+    et = np.empty(max(C, 1), np.int32)
+    es = np.empty(max(C, 1), np.int32)
+    cnt = ctypes.c_int32()
+    rc = lib().orc_lazy_early(n, C, _p(s, ctypes.c_float), float(theta), int(cap), _p(tok2slot, ctypes.c_int32),
+                              _p(slot2tok, ctypes.c_int32), _p(free, ctypes.c_uint8), _p(et, ctypes.c_int32),
+                              _p(es, ctypes.c_int32), ctypes.byref(cnt))
+    _check(rc, "lazy_early")
+    return et[:cnt.value].copy(), es[:cnt.value].copy()
+
+
+def lazy_cache_step(sel, tok2slot, slot2tok, free, early_tok=None, early_slot=None):
+    """The cache step under lazy-reuse eviction; updates tok2slot, slot2tok and free (uint8 [C])
+    in place.  -> (sel_slot, miss_tok, miss_slot, revived)."""
+    sel = _c(sel, np.int32).reshape(-1)
+    et = _c(np.zeros(0, np.int32) if early_tok is None else early_tok, np.int32).reshape(-1)
+    es = _c(np.zeros(0, np.int32) if early_slot is None else early_slot, np.int32).reshape(-1)
+    assert et.size == es.size
+    for a, dt in ((tok2slot, np.int32), (slot2tok, np.int32), (free, np.uint8)):
+        assert a.dtype == dt and a.flags.c_contiguous
+    n, C, m = tok2slot.size, slot2tok.size, sel.size
+    sel_slot = np.empty(max(m, 1), np.int32)
+    mt = np.empty(max(C, 1), np.int32)
+    ms = np.empty(max(C, 1), np.int32)
+    nm, nr = ctypes.c_int32(), ctypes.c_int32()
+    rc = lib().orc_lazy_cache_step(n, C, _p(tok2slot, ctypes.c_int32), _p(slot2tok, ctypes.c_int32),
+                                   _p(free, ctypes.c_uint8), _p(sel, ctypes.c_int32), m, _p(et, ctypes.c_int32),
+                                   _p(es, ctypes.c_int32), et.size, _p(sel_slot, ctypes.c_int32),
+                                   _p(mt, ctypes.c_int32), _p(ms, ctypes.c_int32), ctypes.byref(nm),
+                                   ctypes.byref(nr))
+    _check(rc, "lazy_cache_step")
+    return sel_slot[:m].copy(), mt[:nm.value].copy(), ms[:nm.value].copy(), nr.value
 
 
 def early_cap_for(cap: int, C: int, k: int) -> int:

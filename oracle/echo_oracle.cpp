@@ -461,6 +461,143 @@ int orc_cache_step(int64_t n, int C, int32_t* tok2slot, int32_t* slot2tok, const
     return ORC_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// ---- lazy-reuse eviction (a variant of the cache step) ---------------------
+// READING of the survey's alternative to "resident == selected after every
+// step": a slot freed at a step keeps its bytes and both table entries until
+// the slot is handed to another token.  Its token is then a ghost: present in
+// the cache, not resident.  A selected ghost is a hit: it is resident in its
+// slot again, with no copy.  Handing a slot to a token drops the ghost in it.
+// Slots are handed out as in the contract: lowest free slot first.
+// State: tok2slot / slot2tok are mutual inverses over the present tokens
+// (resident or ghost); free_[j] = 1 when slot j holds no resident token (a
+// ghost's slot is free).
+struct LazyCache {
+    std::map<int32_t, int32_t> present;  // token -> slot
+    std::map<int32_t, int32_t> owner;    // slot -> token
+    std::set<int32_t> free_slots;        // ascending
+};
+
+LazyCache load_lazy(int64_t n, int C, const int32_t* tok2slot, const int32_t* slot2tok, const uint8_t* free_) {
+    LazyCache c;
+    for (int64_t s = 0; s < n; ++s)
+        if (tok2slot[s] >= 0) c.present[(int32_t)s] = tok2slot[s];
+    for (int j = 0; j < C; ++j) {
+        if (slot2tok[j] >= 0) c.owner[j] = slot2tok[j];
+        if (free_[j]) c.free_slots.insert(j);
+    }
+    return c;
+}
+
+void store_lazy(const LazyCache& c, int64_t n, int C, int32_t* tok2slot, int32_t* slot2tok, uint8_t* free_) {
+    for (int64_t s = 0; s < n; ++s) tok2slot[s] = -1;
+    for (int j = 0; j < C; ++j) {
+        slot2tok[j] = -1;
+        free_[j] = 0;
+    }
+    for (const auto& kv : c.present) tok2slot[kv.first] = kv.second;
+    for (const auto& kv : c.owner) slot2tok[kv.first] = kv.second;
+    for (int32_t j : c.free_slots) free_[j] = 1;
+}
+
+// Hands slot j to token t: the ghost in j (if any) leaves the cache.
+void lazy_take(LazyCache& c, int32_t j, int32_t t) {
+    const auto o = c.owner.find(j);
+    if (o != c.owner.end()) c.present.erase(o->second);
+    c.owner[j] = t;
+    c.present[t] = j;
+    c.free_slots.erase(j);
+}
+
+}  // namespace
+
+extern "C" {
+
+// The early set under lazy reuse: tokens scoring strictly above theta that are
+// not present (a ghost's bytes are already in the cache), ascending, at most
+// min(cap, F) of them (F = free slots at the start, ghost slots included),
+// with the lowest free slots ascending.  Only reports the pairs; the cache
+// step takes them.
+int orc_lazy_early(int64_t n, int C, const float* scores, float theta, int cap, const int32_t* tok2slot,
+                   const int32_t* slot2tok, const uint8_t* free_, int32_t* early_tok, int32_t* early_slot,
+                   int32_t* count) {
+    if (!cache_consistent(n, C, tok2slot, slot2tok)) return ORC_EINVAL;
+    const LazyCache c = load_lazy(n, C, tok2slot, slot2tok, free_);
+    const int64_t F = (int64_t)c.free_slots.size();
+    const int64_t limit = (cap < 0) ? F : std::min<int64_t>(cap, F);
+    auto next = c.free_slots.begin();
+    int32_t got = 0;
+    for (int64_t s = 0; s < n && got < limit; ++s) {
+        if (!(scores[s] > theta)) continue;
+        if (c.present.count((int32_t)s)) continue;
+        early_tok[got] = (int32_t)s;
+        early_slot[got] = *next++;
+        ++got;
+    }
+    *count = got;
+    return ORC_OK;
+}
+
+// The cache step under lazy reuse.  sel [m] ascending, -1 padded; the early
+// pairs as orc_lazy_early gave them.
+//   0. each early token takes its slot (dropping the ghost there), resident.
+//   1. every resident token that is not selected becomes a ghost (its slot
+//      free, both table entries kept).
+//   2. every selected token still present is resident (a ghost is revived in
+//      its slot: its slot is no longer free).
+//   3. the misses (selected, not present), ascending, take the lowest free
+//      slots ascending, dropping the ghosts there.
+//   4. sel_slot[i] = slot of sel[i] (-1 for padding).
+// Outputs: miss_tok / miss_slot [*nmiss]; *nrevived = ghosts revived in step 2.
+// Capacity: the selection must fit C (return 2, state untouched).
+int orc_lazy_cache_step(int64_t n, int C, int32_t* tok2slot, int32_t* slot2tok, uint8_t* free_, const int32_t* sel,
+                        int m, const int32_t* early_tok, const int32_t* early_slot, int32_t n_early,
+                        int32_t* sel_slot, int32_t* miss_tok, int32_t* miss_slot, int32_t* nmiss,
+                        int32_t* nrevived) {
+    if (!cache_consistent(n, C, tok2slot, slot2tok)) return ORC_EINVAL;
+    if (n_early < 0 || (n_early > 0 && (!early_tok || !early_slot))) return ORC_EINVAL;
+    std::set<int32_t> selected;
+    for (int i = 0; i < m; ++i) {
+        if (sel[i] < 0) continue;
+        if (sel[i] >= n) return ORC_EINVAL;
+        selected.insert(sel[i]);
+    }
+    if ((int64_t)selected.size() > C) return ORC_ECAPACITY;
+    LazyCache c = load_lazy(n, C, tok2slot, slot2tok, free_);
+    for (int i = 0; i < n_early; ++i) {
+        if (!c.free_slots.count(early_slot[i]) || c.present.count(early_tok[i])) return ORC_EINVAL;
+        lazy_take(c, early_slot[i], early_tok[i]);
+    }
+    // 1. resident and unselected -> ghost
+    for (const auto& kv : c.present)
+        if (!c.free_slots.count(kv.second) && !selected.count(kv.first)) c.free_slots.insert(kv.second);
+    // 2. selected and present -> resident
+    int32_t revived = 0;
+    for (int32_t t : selected) {
+        const auto it = c.present.find(t);
+        if (it == c.present.end()) continue;
+        if (c.free_slots.erase(it->second)) ++revived;
+    }
+    // 3. the misses take the lowest free slots
+    int32_t got = 0;
+    for (int32_t t : selected) {
+        if (c.present.count(t)) continue;
+        const int32_t j = *c.free_slots.begin();
+        lazy_take(c, j, t);
+        miss_tok[got] = t;
+        miss_slot[got] = j;
+        ++got;
+    }
+    for (int i = 0; i < m; ++i) sel_slot[i] = (sel[i] < 0) ? -1 : c.present.at(sel[i]);
+    *nmiss = got;
+    *nrevived = revived;
+    store_lazy(c, n, C, tok2slot, slot2tok, free_);
+    return ORC_OK;
+}
+
 // ---- recall: the device copy of a row is the host row, byte for byte ------
 void orc_recall(const uint8_t* host_rows, int64_t row_bytes, const int32_t* tok,
                 const int32_t* slot, int32_t count, uint8_t* dev_rows) {

@@ -19,15 +19,16 @@ ECHO_OK, ECHO_EINVAL, ECHO_ECAPACITY, ECHO_EUNSUPPORTED, ECHO_ECUDA, ECHO_ETOOLA
 PREFILL_STATIC_SCRATCH_BYTES = 32 << 20
 ST_TIMEOUT, ST_NAN, ST_NOSLOT, ST_BADDATA, ST_FULL = 0x1, 0x2, 0x4, 0x8, 0x10
 STAT_TOPK_FALLBACK, STAT_BOUNDARY_MAX, STAT_EARLY, STAT_MISSES, STAT_EARLY_USED, STAT_CAND_MISS = 0, 1, 2, 3, 4, 5
+STAT_REVIVED = 6
 STATS_N = 8
 HEADS, DIM, MAX_REQUESTS = 64, 128, 4096
-CACHE_HOLD_EARLY = 1            # echo_cache_step flag
+CACHE_HOLD_EARLY, CACHE_LAZY = 1, 2   # echo_cache_step flags
 TOPK_CACHED_MAX_SLOTS = 32768  # C limit of echo_topk_select_cached and of the cached form of echo_topk_select_cands
 CAND_CAP = 16384             # candidate-list entries per request top-k keeps in shared memory
 EARLY_FETCH_BLOCKS = 32      # CTAs of the early-fetch and late-recall kernels
 
 EXPORTS = ("echo_above_words", "echo_append_tokens", "echo_cache_step", "echo_cache_step_resolved",
-           "echo_debug_set_wait_limit", "echo_device_sm_count",
+           "echo_debug_stall_epilogue", "echo_device_sm_count",
            "echo_early_fetch", "echo_host_device_alias", "echo_index_scores", "echo_index_scores_cands", "echo_mla_decode", "echo_pool_above", "echo_pool_select",
            "echo_pool_slots", "echo_prefill_block",
            "echo_prefill_block_static", "echo_prefill_scores", "echo_prefill_workspace_size", "echo_quantize_q", "echo_seed_early",
@@ -130,8 +131,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
                                                 _vp, _vp, _vp]
         L.echo_host_device_alias.restype = i32
         L.echo_host_device_alias.argtypes = [_vp, ctypes.POINTER(_vp)]
-        L.echo_debug_set_wait_limit.restype = i32
-        L.echo_debug_set_wait_limit.argtypes = [i64]
+        L.echo_debug_stall_epilogue.restype = i32
+        L.echo_debug_stall_epilogue.argtypes = [i64]
         L.echo_device_sm_count.restype = i32
         L.echo_device_sm_count.argtypes = []
         _lib = L
@@ -184,10 +185,10 @@ def host_alias_tensor(host: torch.Tensor, device) -> torch.Tensor:
         return torch.as_tensor(_CudaArray(iface), device=device)
 
 
-def debug_set_wait_limit(ns: int) -> None:
-    """echo_debug_set_wait_limit: the give-up limit of the score epilogue's accumulator wait
-    (tests of the timeout path; ns < 0 restores the default)."""
-    _check("echo_debug_set_wait_limit", load().echo_debug_set_wait_limit(int(ns)))
+def debug_stall_epilogue(limit_ns: int) -> None:
+    """echo_debug_stall_epilogue: >= 0, every score call first waits on a barrier nothing arrives
+    on and gives up after limit_ns (tests of the timeout path); < 0 turns that off."""
+    _check("echo_debug_stall_epilogue", load().echo_debug_stall_epilogue(int(limit_ns)))
 
 
 def sm_count() -> int:
@@ -257,9 +258,9 @@ def topk_select(tok_off, n_tokens, scores, k, hist, theta_hat, alpha, sel_idx, k
 
 
 def cache_step(tok_off, n_tokens, sel, cache, sel_slot, status, stats=None, stream=None, copy_stream=None,
-               above=None, early_cap=-1, hold_early=False, tok_end=None):
+               above=None, early_cap=-1, hold_early=False, tok_end=None, lazy=False):
     """echo_cache_step; above/early_cap: the early set of this step (as given to early_fetch);
-    hold_early: ECHO_CACHE_HOLD_EARLY."""
+    hold_early: ECHO_CACHE_HOLD_EARLY; lazy: ECHO_CACHE_LAZY (lazy-reuse eviction)."""
     B = tok_off.shape[0] - 1
     m = sel.shape[-1]
     st = _stream(stream)
@@ -267,7 +268,7 @@ def cache_step(tok_off, n_tokens, sel, cache, sel_slot, status, stats=None, stre
     _check("echo_cache_step", load().echo_cache_step(
         B, _ptr(tok_off), _ptr(tok_end), int(n_tokens), _ptr(sel), int(m), _ptr(above), int(early_cap),
         ctypes.byref(cache.struct), _ptr(sel_slot), _ptr(status), _ptr(stats), st, cst,
-        CACHE_HOLD_EARLY if hold_early else 0))
+        (CACHE_HOLD_EARLY if hold_early else 0) | (CACHE_LAZY if lazy else 0)))
 
 
 def topk_select_cached(tok_off, n_tokens, scores, k, hist, theta_hat, alpha, sel_idx, kth, cache, sel_slot,

@@ -109,12 +109,12 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
                                                          const int32_t* __restrict__ sel, int m,
                                                          const uint32_t* __restrict__ above, int early_cap,
                                                          CacheArgs c, int32_t* __restrict__ sel_slot, int32_t* status,
-                                                         uint32_t* stats, bool hold_early) {
+                                                         uint32_t* stats, bool hold_early, bool lazy) {
     // keep [words]: a selected token lives in the slot | wpre [words + 1] | fbs [words] (free bits)
     // | es_tok [kES] | es_slot [kES] (the early pairs, both ascending)
     extern __shared__ uint32_t keep[];
     __shared__ uint32_t scan[40];
-    __shared__ uint32_t s_flags, s_early_used;
+    __shared__ uint32_t s_flags, s_early_used, s_revived;
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_launch_dependents();  // the late recall's blocks may be scheduled now; they wait for this kernel
     pdl_wait();  // launched as a programmatic dependent: everything below may depend on the kernel before
@@ -174,6 +174,7 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
     if (tid == 0) {
         s_flags = 0;
         s_early_used = 0;
+        s_revived = 0;
     }
     // Round 2: the slots of the selected tokens as the step found them.
     if (chunks == 1) {
@@ -214,6 +215,19 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
     const int32_t* e_tok = es_ok ? es_tok : etok;
     const int32_t* e_slot = es_ok ? es_slot : eslot;
     uint32_t used = 0;
+    if (lazy) {
+        // lazy reuse: every early token enters the tables in its slot, and the ghost
+        // (a token freed earlier whose bytes and entries the slot kept) leaves them
+        for (uint32_t e = tid; e < E; e += kCT) {
+            const int32_t tok = e_tok[e], slot = e_slot[e];
+            if (tok < 0 || tok >= n || slot < 0 || slot >= C) continue;
+            const int32_t g = s2t[slot];
+            if (g >= 0 && g < n) t2s[g] = -1;
+            t2s[tok] = slot;
+            s2t[slot] = tok;
+        }
+        __syncthreads();
+    }
 
     // 1a. slots that hold a selected token are kept; the selection must be
     // ascending with -1 padding last
@@ -231,8 +245,10 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
             const int32_t nxt = (q + 1 < kPer) ? s[q + 1] : after;
             if (s[q] >= 0 && s[q] < n) {
                 if (nxt >= 0 && nxt <= s[q]) flags |= ECHO_ST_BADDATA;
-                if (chunks > 1) j[q] = t2s[s[q]];
-                if (j[q] < 0 && E > 0) {  // a selected early token becomes resident in its slot
+                if (chunks > 1 || lazy) j[q] = t2s[s[q]];
+                if (lazy) {
+                    if (j[q] >= 0 && E > 0 && find_sorted(e_tok, static_cast<int>(E), s[q]) >= 0) ++used;
+                } else if (j[q] < 0 && E > 0) {  // a selected early token becomes resident in its slot
                     const int e = find_sorted(e_tok, static_cast<int>(E), s[q]);
                     if (e >= 0) {
                         j[q] = e_slot[e];
@@ -259,7 +275,7 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
         const int slot = w * 32 + lane;
         const bool kept = (keep[w] >> lane) & 1u;
         const bool freeing = st >= 0 && !kept;
-        if (freeing) {
+        if (freeing && !lazy) {  // lazy reuse: the token stays in the tables as a ghost
             s2t[slot] = -1;
             if (st < n) t2s[st] = -1;
         }
@@ -278,6 +294,15 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
     }
     if (used) atomicAdd(&s_early_used, used);
     __syncthreads();
+    if (lazy) {  // a selected ghost is resident again in its slot: the slot is not free
+        uint32_t rev = 0;
+        for (int w = tid; w < words; w += kCT) {
+            rev += __popc(fbs[w] & keep[w]);
+            fbs[w] &= ~keep[w];
+        }
+        if (rev) atomicAdd(&s_revived, rev);
+        __syncthreads();
+    }
     if (!hold_early) {  // the unselected early tokens' slots are free for the misses
         for (uint32_t e = tid; e < E; e += kCT) {
             const int32_t es = e_slot[e];
@@ -318,6 +343,10 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
                         mtok[rank] = s[q];
                         mslot[rank] = slot;
                     }
+                    if (lazy) {  // the ghost in the slot leaves the tables
+                        const int32_t g = s2t[slot];
+                        if (g >= 0 && g < n) t2s[g] = -1;
+                    }
                     t2s[s[q]] = slot;
                     s2t[slot] = s[q];
                 }
@@ -346,6 +375,7 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
         if (stats && got) atomicAdd(stats + ECHO_STAT_MISSES, got);
         if (stats && E) atomicAdd(stats + ECHO_STAT_EARLY, E);
         if (stats && s_early_used) atomicAdd(stats + ECHO_STAT_EARLY_USED, s_early_used);
+        if (stats && s_revived) atomicAdd(stats + ECHO_STAT_REVIVED, s_revived);
         uint32_t flags = s_flags;
         if (found > F) flags |= ECHO_ST_NOSLOT;
         if (flags) set_status(status, static_cast<int>(flags));
@@ -354,7 +384,8 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
 
 constexpr int kRecallThreads = 512;
 constexpr int kRecallBlocks = 32;
-constexpr int kRows = 2;        // rows per warp in flight
+constexpr int kRows = 2;        // rows per warp in flight (4 measured: the host reads queue up and every
+                                // kernel of the step slowed about tenfold)
 constexpr int kStage = 4096;    // early (token, slot) pairs staged in shared memory per round
 
 // One warp copies kRows rows (those with ok[r]) of `chunks` 16-byte pieces.
@@ -610,8 +641,10 @@ int enqueue_cache_step(int B, const int64_t* tok_off, const int64_t* tok_end, in
                        int m,
                        const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,
                        int32_t* status, uint32_t* stats, cudaStream_t stream, cudaStream_t copy_stream,
-                       bool resolved, bool hold_early) {
-    const bool lookup = cache->C <= kLookupMaxSlots;
+                       bool resolved, bool hold_early, bool lazy) {
+    // lazy reuse walks the early set (every early token enters the tables)
+    const bool lookup = cache->C <= kLookupMaxSlots && !lazy;
+    if (lazy && (resolved || hold_early)) return ECHO_EUNSUPPORTED;
     if (resolved && !lookup) return ECHO_EUNSUPPORTED;
     const size_t smem =
         (lookup ? cache_lookup_smem_words(cache->C, kAWC) : cache_step_smem_words(cache->C)) * sizeof(uint32_t);
@@ -645,7 +678,7 @@ int enqueue_cache_step(int B, const int64_t* tok_off, const int64_t* tok_end, in
                                         early_cap, ca, sel_slot, status, stats, hold_early));
     } else {
         ECHO_CUDA_OK(cudaLaunchKernelEx(&cfg, cache_step_kernel, tok_off, tok_end, n_tokens, sel, m, above, early_cap, ca,
-                                        sel_slot, status, stats, hold_early));
+                                        sel_slot, status, stats, hold_early, lazy));
     }
     const int rc = stream_wait(copy_stream, stream);
     if (rc) return rc;
@@ -675,11 +708,12 @@ extern "C" int echo_cache_step(int B, const int64_t* tok_off, const int64_t* tok
                                int32_t* status, uint32_t* stats, echo_stream_t stream, echo_stream_t copy_stream,
                                int flags) {
     using namespace echo;
-    if (!tok_off || !status || (flags & ~ECHO_CACHE_HOLD_EARLY)) return ECHO_EINVAL;
+    if (!tok_off || !status || (flags & ~(ECHO_CACHE_HOLD_EARLY | ECHO_CACHE_LAZY))) return ECHO_EINVAL;
+    if ((flags & ECHO_CACHE_HOLD_EARLY) && (flags & ECHO_CACHE_LAZY)) return ECHO_EINVAL;
     const int rc = check_cache_step_args(B, n_tokens, sel, m, cache, sel_slot);
     if (rc) return rc;
     return enqueue_cache_step(B, tok_off, tok_end, n_tokens, sel, m, above, early_cap, cache, sel_slot, status, stats, stream,
-                              copy_stream, false, (flags & ECHO_CACHE_HOLD_EARLY) != 0);
+                              copy_stream, false, (flags & ECHO_CACHE_HOLD_EARLY) != 0, (flags & ECHO_CACHE_LAZY) != 0);
 }
 
 extern "C" int echo_cache_step_resolved(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens,
@@ -692,7 +726,7 @@ extern "C" int echo_cache_step_resolved(int B, const int64_t* tok_off, const int
     if (rc) return rc;
     if (cache->C > kLookupMaxSlots) return ECHO_EUNSUPPORTED;
     return enqueue_cache_step(B, tok_off, tok_end, n_tokens, sel, m, nullptr, 0, cache, sel_slot, status, stats, stream,
-                              copy_stream, true, (flags & ECHO_CACHE_HOLD_EARLY) != 0);
+                              copy_stream, true, (flags & ECHO_CACHE_HOLD_EARLY) != 0, false);
 }
 
 extern "C" int echo_early_fetch(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens,

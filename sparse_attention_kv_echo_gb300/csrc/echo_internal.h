@@ -62,7 +62,7 @@ int enqueue_cache_step(int B, const int64_t* tok_off, const int64_t* tok_end, in
                        int m,
                        const uint32_t* above, int early_cap, const echo_cache* cache, int32_t* sel_slot,
                        int32_t* status, uint32_t* stats, cudaStream_t stream, cudaStream_t copy_stream,
-                       bool resolved, bool hold_early);
+                       bool resolved, bool hold_early, bool lazy);
 
 }  // namespace echo
 

@@ -176,7 +176,7 @@ extern "C" int echo_prefill_block(int R, int64_t row0, int64_t n_keys, const flo
     ECHO_CUDA_OK(cudaGetLastError());
     if (!cache) return ECHO_OK;
     return enqueue_cache_step(1, p.tok_off2, nullptr, n_keys, union_list, static_cast<int>(W), nullptr, 0, cache, sel_slot,
-                              status, stats, stream, copy_stream, false, false);
+                              status, stats, stream, copy_stream, false, false, false);
 }
 
 // ---------------------------------------------------------------------------

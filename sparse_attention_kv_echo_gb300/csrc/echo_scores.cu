@@ -81,10 +81,12 @@ struct ScoreArgs {
 
 constexpr uint32_t kNoCut = 0xFFFFFFFFu;   // a request without a candidate list
 
-// Give-up limit of the epilogue's wait for an accumulator (echo_debug_set_wait_limit):
-// the other waits, and every wait that drains copies or MMAs before TMEM is
-// freed, keep kWaitNs.
-__device__ uint64_t g_epilogue_wait_ns = kWaitNs;
+// Failure-path test (echo_debug_stall_epilogue): >= 0, the epilogue first waits
+// on a barrier that nothing arrives on, giving up after this many ns, which
+// takes the kernel down its timeout path; < 0 (the default), no such wait.  The
+// other waits, and every wait that drains copies or MMAs before TMEM is freed,
+// keep kWaitNs.
+__device__ int64_t g_epilogue_stall_ns = -1;
 constexpr int kCandBuf = 64;               // per epilogue warp: < 32 waiting + one tile's 32
 
 struct __align__(128) ScoreCtl {
@@ -99,6 +101,7 @@ struct __align__(128) ScoreCtl {
     uint64_t accfull[kAccBufs];
     uint64_t accempty[kAccBufs];
     uint64_t done;
+    uint64_t never;                       // arrived on by nothing (failure-path test)
     uint32_t tmem_base;
     int abort;
     uint32_t scan[16];
@@ -215,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_addr(&ctl->accempty[i]), 4);
         }
         mbar_init(smem_addr(&ctl->done), 1);
+        mbar_init(smem_addr(&ctl->never), 1);
         ctl->abort = 0;
         fence_barrier_init();
     }
@@ -388,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         pdl_wait();                            // wfold and the cleared histogram come from the quantiser
-        const uint64_t acc_wait_ns = g_epilogue_wait_ns;
+        const int64_t stall_ns = g_epilogue_stall_ns;
         const int ew = warp - 2;               // 0..7
         const int group = ew >> 2;             // tiles with local index = group (mod 2)
         const int quarter = warp & 3;          // TMEM lanes this warp may access
@@ -432,8 +436,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool theta_ok = false;
         int64_t nb = 0, obase = 0, abase = 0;
         int side = 0;   // offset of the tile's first token in its side boxes
-        bool ok = true;
-        for (uint32_t it = group; it < ntiles; it += 2) {
+        // (failure-path test) a wait that can only run out
+        bool ok = stall_ns < 0 || mbar_wait_limit(smem_addr(&ctl->never), 0, abort, static_cast<uint64_t>(stall_ns));
+        for (uint32_t it = group; ok && it < ntiles; it += 2) {
             const uint32_t t = t_begin + it;
             while (t >= static_cast<uint32_t>(tstart[b + 1])) ++b;
             if (b != cur_b) {
@@ -477,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t tok = static_cast<int64_t>(t - tstart[b]) * kTileM + row;
             const bool valid = tok < nb;
             const uint32_t acc = it % kAccBufs;
-            if (!mbar_wait_limit(smem_addr(&ctl->accfull[acc]), (it / kAccBufs) & 1, abort, acc_wait_ns)) {
+            if (!mbar_wait(smem_addr(&ctl->accfull[acc]), (it / kAccBufs) & 1, abort)) {
                 ok = false;
                 break;
             }
@@ -685,9 +690,9 @@ extern "C" size_t echo_above_words(int B, int64_t n_tokens) {
     return 4 * static_cast<size_t>(n_tokens / 128 + B);
 }
 
-extern "C" int echo_debug_set_wait_limit(int64_t ns) {
-    const uint64_t v = ns < 0 ? echo::kWaitNs : static_cast<uint64_t>(ns);
-    if (cudaMemcpyToSymbol(echo::g_epilogue_wait_ns, &v, sizeof(v)) != cudaSuccess) {
+extern "C" int echo_debug_stall_epilogue(int64_t limit_ns) {
+    const int64_t v = limit_ns < 0 ? -1 : limit_ns;
+    if (cudaMemcpyToSymbol(echo::g_epilogue_stall_ns, &v, sizeof(v)) != cudaSuccess) {
         cudaGetLastError();
         return ECHO_ECUDA;
     }

@@ -38,7 +38,8 @@ class DecodeLayer:
                  early_cap: int = -1, groups: int | None = None, first_share: float = 0.5,
                  resolved: bool = True, hold_early: bool = False, attention: bool = False,
                  mla_scale: float = 1.0 / math.sqrt(192.0), tok_end=None, cross_layer: bool = False,
-                 pool_slots: int = 0, cands: bool = True, cand_cap: int = L.CAND_CAP, device="cuda"):
+                 pool_slots: int = 0, cands: bool = True, cand_cap: int = L.CAND_CAP, lazy: bool = False,
+                 device="cuda"):
         tok_off = torch.as_tensor(tok_off, dtype=torch.int64)
         self.B = int(tok_off.numel() - 1)
         self.n_tokens = int(k8.shape[0])
@@ -46,7 +47,12 @@ class DecodeLayer:
         self.predictor = bool(predictor)
         # top-k looks up the selected tokens' slots itself (the cache step then frees and places
         # the misses) when the request's free bits fit its shared memory
-        self.resolved = bool(resolved) and self.C <= L.TOPK_CACHED_MAX_SLOTS
+        # lazy: lazy-reuse eviction (a freed slot keeps its token until the slot is handed out); the
+        # cache step then does the slot look-up itself
+        self.lazy = bool(lazy)
+        if self.lazy and hold_early:
+            raise ValueError("lazy reuse goes with the contract's early slots, not the held-slot form")
+        self.resolved = bool(resolved) and self.C <= L.TOPK_CACHED_MAX_SLOTS and not self.lazy
         # hold_early: the cache step holds the slots of unselected early tokens until the misses
         # are placed, so the late recall need not wait for the early copy; the early set is then
         # capped at C - k on top of the caller's cap (selected tokens plus held slots within C)
@@ -204,7 +210,8 @@ class DecodeLayer:
         L.pool_select(self.tok_off, self.sel_idx, self.sel_pool, stream=side)
         L.cache_step(self.tok_off_pool, n, self.sel_pool, self.cache, self.slot_pool, self.status, stats=self.stats,
                      stream=side, copy_stream=copy, above=self.above_pool if self.predictor else None,
-                     early_cap=self.early_cap if self.predictor else 0, hold_early=self.hold_early)
+                     early_cap=self.early_cap if self.predictor else 0, hold_early=self.hold_early,
+                     lazy=self.lazy)
         L.pool_slots(self.sel_idx, self.slot_pool, self.sel_slot, stream=side)
         if out_host is not None:
             with torch.cuda.stream(side):
@@ -233,7 +240,7 @@ class DecodeLayer:
         else:
             L.cache_step(self.tok_off, self.n_tokens, self.sel_idx, self.cache, self.sel_slot, self.status,
                          stats=self.stats, stream=side, copy_stream=copy, above=self.above_seed,
-                         early_cap=self.early_cap, hold_early=self.hold_early, tok_end=self.tok_end)
+                         early_cap=self.early_cap, hold_early=self.hold_early, tok_end=self.tok_end, lazy=self.lazy)
         if out_host is not None:
             with torch.cuda.stream(side):
                 self._write_out(out_host, 0, self.B)
@@ -277,7 +284,7 @@ class DecodeLayer:
                            self.theta, self.hist, self.status, stream=main, tok_end=self.tok_end, cands=self.cands)
             self._select(self.tok_off, 0, self.B, self.cands, main, end=self.tok_end)
             L.cache_step(self.tok_off, self.n_tokens, self.sel_idx, self.cache, self.sel_slot, self.status,
-                         stats=self.stats, stream=main, copy_stream=main, tok_end=self.tok_end)
+                         stats=self.stats, stream=main, copy_stream=main, tok_end=self.tok_end, lazy=self.lazy)
             if out_host is not None:
                 with torch.cuda.stream(main):
                     self._write_out(out_host, 0, self.B)
@@ -332,7 +339,8 @@ class DecodeLayer:
                 self.selected_evs.append(ev)
                 L.cache_step(off, self.n_tokens, self.sel_idx[b0:b1], self.views[g], self.sel_slot[b0:b1],
                              self.status, stats=self.stats, stream=side, copy_stream=copy, above=self.above_g[g],
-                             early_cap=self.early_cap, hold_early=self.hold_early, tok_end=end(b0, b1))
+                             early_cap=self.early_cap, hold_early=self.hold_early, tok_end=end(b0, b1),
+                             lazy=self.lazy)
             if out_host is not None:
                 with torch.cuda.stream(side):
                     self._write_out(out_host, b0, b1)

@@ -64,7 +64,7 @@ def check_scores(layer_inputs, q, w, gpu_scores, sample=None, rng=None):
 
 def run_decode(w: wl.Workload, steps: int, predictor: bool, cap: int = -1, score_sample=None,
                check_every_score_step=True, keys_device="cpu", layer: int = 0, resolved: bool = True,
-               hold_early: bool = False, cands: bool = True):
+               hold_early: bool = False, cands: bool = True, lazy: bool = False):
     """Runs `steps` decode steps of one layer on the GPU and checks each against the oracle."""
     dev = "cuda"
     off = wl.tok_offsets(w.lengths)
@@ -75,12 +75,13 @@ def run_decode(w: wl.Workload, steps: int, predictor: bool, cap: int = -1, score
     host = wl.make_host_pool(w, layer, device=keys_device, pin=True)
     host_before = host.clone()
     lay = DecodeLayer(off, k8c.to(dev), ksc.to(dev), w.k, w.C, host, predictor=predictor, early_cap=cap,
-                      resolved=resolved, hold_early=hold_early, cands=cands)
+                      resolved=resolved, hold_early=hold_early, cands=cands, lazy=lazy)
     o = OracleLayer(w.B, w.total_tokens, w.C)
+    o_free = np.ones(w.B * w.C, np.uint8)   # lazy reuse: 1 = no resident token in the slot
     qsrc = wl.QueryStream(w, layer, device=keys_device)
     rng = np.random.default_rng(7)
     host_gpu = host.to(dev)
-    report = dict(worst_rel=0.0, misses=[], early=[], boundary_max=0)
+    report = dict(worst_rel=0.0, misses=[], early=[], boundary_max=0, revived=0)
     for t in range(steps):
         q = qsrc.next().cpu()
         theta_before = o.theta.copy()
@@ -113,11 +114,15 @@ def run_decode(w: wl.Workload, steps: int, predictor: bool, cap: int = -1, score
             assert np.array_equal(gh[b], orc.hist256(sc, theta_before[b])), (t, b, "hist")
             t2s = o.t2s[lo:hi]
             s2t = o.s2t[b * w.C:(b + 1) * w.C]
-            et = None
+            fr = o_free[b * w.C:(b + 1) * w.C]
+            et = es = None
             if predictor:
                 # the layer's cap: the caller's (holding: capped at C - k, the oracle's rule)
                 assert lay.early_cap == (orc.early_cap_for(cap, w.C, w.k) if hold_early else cap)
-                et, es = orc.early_fetch(sc, theta_before[b], lay.early_cap, t2s, s2t)
+                if lazy:
+                    et, es = orc.lazy_early(sc, theta_before[b], lay.early_cap, t2s, s2t, fr)
+                else:
+                    et, es = orc.early_fetch(sc, theta_before[b], lay.early_cap, t2s, s2t)
                 assert g_ecnt[b] == et.size, (t, b, "early count", g_ecnt[b], et.size)
                 assert np.array_equal(g_etok[b * w.C:b * w.C + et.size], et), (t, b, "early tok")
                 assert np.array_equal(g_eslot[b * w.C:b * w.C + et.size], es), (t, b, "early slot")
@@ -128,7 +133,11 @@ def run_decode(w: wl.Workload, steps: int, predictor: bool, cap: int = -1, score
             o.theta[b] = orc.ema(theta_before[b], kth, 0.5)
             assert g_theta[b] == o.theta[b] or (np.isinf(o.theta[b]) and np.isinf(g_theta[b])), \
                 (t, b, "theta", g_theta[b], o.theta[b])
-            sel_slot, mt, ms, _ = orc.cache_step(idx, t2s, s2t, early_tok=et, hold_early=hold_early)
+            if lazy:
+                sel_slot, mt, ms, rev = orc.lazy_cache_step(idx, t2s, s2t, fr, et, es)
+                report["revived"] += rev
+            else:
+                sel_slot, mt, ms, _ = orc.cache_step(idx, t2s, s2t, early_tok=et, hold_early=hold_early)
             assert np.array_equal(g_slot[b], sel_slot), (t, b, "sel_slot")
             assert g_mcnt[b] == mt.size, (t, b, "miss count", g_mcnt[b], mt.size)
             assert np.array_equal(g_mtok[b * w.C:b * w.C + mt.size], mt), (t, b, "miss tok")
@@ -136,7 +145,7 @@ def run_decode(w: wl.Workload, steps: int, predictor: bool, cap: int = -1, score
             misses += mt.size
         assert np.array_equal(g_t2s, o.t2s), (t, "tok2slot")
         assert np.array_equal(g_s2t, o.s2t), (t, "slot2tok")
-        free = (o.s2t < 0).reshape(-1, 32)
+        free = (o_free.astype(bool) if lazy else (o.s2t < 0)).reshape(-1, 32)
         want_fb = (free.astype(np.uint64) << np.arange(32, dtype=np.uint64)).sum(1).astype(np.uint32)
         assert np.array_equal(g_fb, want_fb), (t, "freebits")
         # recalled bytes: every selected token's device row equals its host row
@@ -148,10 +157,19 @@ def run_decode(w: wl.Workload, steps: int, predictor: bool, cap: int = -1, score
         rows_dev = lay.cache.dev_kv[(bidx * w.C + slot_t)[valid]]
         rows_host = host_gpu[(offs + sel_t)[valid]]
         assert torch.equal(rows_dev.view(torch.int16), rows_host.view(torch.int16)), (t, "recall bytes")
+        if lazy:  # every present token's bytes, ghosts' included, are its host row
+            for b in range(w.B):
+                lo, hi = int(off[b]), int(off[b + 1])
+                pres = np.nonzero(o.t2s[lo:hi] >= 0)[0]
+                sl_t = torch.from_numpy(b * w.C + o.t2s[lo:hi][pres]).long().to(dev)
+                tk_t = torch.from_numpy(lo + pres).long().to(dev)
+                assert torch.equal(lay.cache.dev_kv[sl_t].view(torch.int16), host_gpu[tk_t].view(torch.int16)), \
+                    (t, b, "present rows")
         report["misses"].append(misses)
     report["boundary_max"] = int(lay.stats[L.STAT_BOUNDARY_MAX].item())
     report["fallbacks"] = int(lay.stats[L.STAT_TOPK_FALLBACK].item())
     report["cand_miss"] = int(lay.stats[L.STAT_CAND_MISS].item())
+    report["revived_gpu"] = int(lay.stats[L.STAT_REVIVED].item())
     assert torch.equal(host.view(torch.int16), host_before.view(torch.int16))  # no write-back
     return report
 
@@ -366,7 +384,7 @@ def run_stack(w: wl.Workload, steps: int, n_layers: int, cross_layer: bool, hold
 
 
 def run_pool(w: wl.Workload, steps: int, pool: int, hold_early: bool = False, predictor: bool = True,
-             graph: bool = True, cap: int = -1):
+             graph: bool = True, cap: int = -1, lazy: bool = False):
     """Decode steps with one cache pool of `pool` slots shared by the batch's requests, checked
     against the oracle's own pool (a cache of one request over every row, token ids global): the
     early set (the requests' marked, non-resident tokens in (request, token) order), top-k per
@@ -378,11 +396,12 @@ def run_pool(w: wl.Workload, steps: int, pool: int, hold_early: bool = False, pr
     wt = wl.make_weights(w, 0)
     host = wl.make_host_pool(w, 0, pin=True)
     lay = DecodeLayer(off, k8c.to(dev), ksc.to(dev), w.k, w.C, host, predictor=predictor, hold_early=hold_early,
-                      early_cap=cap, pool_slots=pool, device=dev)
+                      early_cap=cap, pool_slots=pool, lazy=lazy, device=dev)
     k8, ks, wn = k8c.numpy(), ksc.numpy(), wt.numpy()
     hb = host.view(torch.uint8).numpy()
     t2s = np.full(n, -1, np.int32)
     s2t = np.full(pool, -1, np.int32)
+    fr = np.ones(pool, np.uint8)      # lazy reuse: 1 = no resident token in the slot
     theta = np.full(w.B, np.inf, np.float32)
     qsrc = wl.QueryStream(w, 0)
     main = torch.cuda.Stream()
@@ -397,7 +416,7 @@ def run_pool(w: wl.Workload, steps: int, pool: int, hold_early: bool = False, pr
         lay.reset()
         torch.cuda.synchronize()
     rng = np.random.default_rng(3)
-    report = dict(early=[], misses=[])
+    report = dict(early=[], misses=[], revived=0)
     for t in range(steps):
         q = qsrc.next().cpu()
         with torch.cuda.stream(main):
@@ -417,7 +436,12 @@ def run_pool(w: wl.Workload, steps: int, pool: int, hold_early: bool = False, pr
             if predictor and np.isfinite(theta[b]):
                 s = np.nonzero(gs[lo:hi] > theta[b])[0] + lo
                 marked.extend(int(x) for x in s if t2s[x] < 0)
-        et, es = orc.early_from_selection(np.array(marked, np.int32), n, lay.early_cap, t2s, s2t)
+        if lazy:   # the marked tokens, ascending, through the lazy early rule
+            ind = np.zeros(n, np.float32)
+            ind[np.array(marked, np.int64)] = 1.0
+            et, es = orc.lazy_early(ind, 0.5, lay.early_cap, t2s, s2t, fr)
+        else:
+            et, es = orc.early_from_selection(np.array(marked, np.int32), n, lay.early_cap, t2s, s2t)
         if predictor:
             g_cnt = int(lay.cache.early_cnt.cpu().numpy()[0])
             assert g_cnt == et.size, (t, "early count", g_cnt, et.size)
@@ -435,7 +459,11 @@ def run_pool(w: wl.Workload, steps: int, pool: int, hold_early: bool = False, pr
             counts.append(v.size)
         sel_g = np.full(w.B * w.k, -1, np.int32)
         sel_g[:len(glob)] = glob
-        sl_g, mt, ms, _ = orc.cache_step(sel_g, t2s, s2t, early_tok=et, hold_early=hold_early)
+        if lazy:
+            sl_g, mt, ms, rev = orc.lazy_cache_step(sel_g, t2s, s2t, fr, et, es)
+            report["revived"] += rev
+        else:
+            sl_g, mt, ms, _ = orc.cache_step(sel_g, t2s, s2t, early_tok=et, hold_early=hold_early)
         pos = 0
         for b in range(w.B):
             want = np.full(w.k, -1, np.int32)
@@ -447,6 +475,12 @@ def run_pool(w: wl.Workload, steps: int, pool: int, hold_early: bool = False, pr
         g_dev = lay.cache.dev_kv.view(torch.uint8).cpu().numpy()
         valid = sel_g >= 0
         assert np.array_equal(g_dev[sl_g[valid]], hb[sel_g[valid]]), (t, "rows")
+        if lazy:   # ghosts' bytes too, and the free bits
+            pres = np.nonzero(t2s >= 0)[0]
+            assert np.array_equal(g_dev[t2s[pres]], hb[pres]), (t, "present rows")
+            want_fb = (fr.astype(bool).reshape(-1, 32).astype(np.uint64) << np.arange(32, dtype=np.uint64)).sum(1)
+            assert np.array_equal(lay.cache.freebits.cpu().numpy().view(np.uint32), want_fb.astype(np.uint32)), \
+                (t, "pool freebits")
         report["early"].append(int(et.size))
         report["misses"].append(int(mt.size))
     return report

@@ -159,9 +159,13 @@ def test_cache_checks(L):
     assert L.echo_cache_step(1, dummy, None, 100, dummy, 16, None, 0, ctypes.byref(s), dummy, dummy, None, None,
                              None, 0) == lib.ECHO_EINVAL
     s.dev_kv = 0x2000
-    # unknown flag bits
+    # unknown flag bits; the held-slot form and lazy reuse together; lazy reuse in the resolved form
     assert L.echo_cache_step(1, dummy, None, 100, dummy, 16, None, 0, ctypes.byref(s), dummy, dummy, None, None,
-                             None, 2) == lib.ECHO_EINVAL
+                             None, 4) == lib.ECHO_EINVAL
+    assert L.echo_cache_step(1, dummy, None, 100, dummy, 16, None, 0, ctypes.byref(s), dummy, dummy, None, None,
+                             None, lib.CACHE_HOLD_EARLY | lib.CACHE_LAZY) == lib.ECHO_EINVAL
+    assert L.echo_cache_step_resolved(1, dummy, None, 100, dummy, 16, ctypes.byref(s), dummy, dummy, None, None,
+                                      None, lib.CACHE_LAZY) == lib.ECHO_EINVAL
     assert L.echo_cache_step_resolved(1, dummy, None, 100, dummy, 16, ctypes.byref(s), dummy, dummy, None, None,
                                       None, 4) == lib.ECHO_EINVAL
     # the resolved form: k larger than C; the cached top-k: C above its shared-memory limit

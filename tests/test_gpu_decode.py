@@ -102,7 +102,9 @@ def test_batch_workload_full_size():
     """8 x 32768, k=2048, C=4096: every table/selection bit-exact, scores sampled."""
     w = wl.WORKLOADS["batch"]
     rep = run_decode(w, 6, predictor=True, score_sample=1024)
-    assert rep["fallbacks"] >= 1            # the unshifted first step overflows the boundary bin
+    # the unshifted first step's boundary bin is larger than shared memory: a second round of
+    # bins resolves it without passes over the scores
+    assert rep["boundary_max"] > 16384 and rep["fallbacks"] == 0
 
 
 def test_hot_set_workload_one_layer():

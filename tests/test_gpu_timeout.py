@@ -1,12 +1,11 @@
 """A bounded wait that runs out, on the GPU, without a fault or a hang.
 
-The score kernel's epilogue waits for each accumulator the MMA warp fills.
-echo_debug_set_wait_limit(0) makes that one wait give up unless the
-accumulator is ready at its first look (which it is not: the MMA has to wait
-for the query's copy first).  The call must then report ECHO_ST_TIMEOUT in its
-status word, its kernel must drain its copies and MMAs and free its tensor
-memory, and with the limit restored the next call on the same context must
-run clean and match the oracle.
+echo_debug_stall_epilogue(limit) makes the score kernel's epilogue first wait
+on a barrier that nothing arrives on.  The wait must give up after the limit
+and the call report ECHO_ST_TIMEOUT in its status word, while the kernel's
+producer and MMA warps drain their copies and MMAs and the tensor memory is
+freed; with the stall off again the next call on the same context must run
+clean and match the oracle.
 """
 import math
 
@@ -47,17 +46,11 @@ def test_epilogue_wait_runs_out_then_the_next_call_is_clean():
     wt = wl.make_weights(w, 0)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     try:
-        L.debug_set_wait_limit(0)
-        timed_out = False
-        for _ in range(3):   # the first look at an accumulator precedes its MMA in practice
-            status.zero_()
-            _score(w, off, q.to(dev), wt.to(dev), k8, ks, status)
-            if int(status.item()) & L.ST_TIMEOUT:
-                timed_out = True
-                break
-        assert timed_out, f"status {int(status.item()):#x}"
+        L.debug_stall_epilogue(200_000)      # 0.2 ms
+        _score(w, off, q.to(dev), wt.to(dev), k8, ks, status)
+        assert int(status.item()) & L.ST_TIMEOUT, f"status {int(status.item()):#x}"
     finally:
-        L.debug_set_wait_limit(-1)
+        L.debug_stall_epilogue(-1)
     # the same context, the default limit: a clean call with correct scores
     status.zero_()
     scores = _score(w, off, q.to(dev), wt.to(dev), k8, ks, status)
