@@ -668,9 +668,11 @@ def run_kernels(args):
     """The score kernel and the top-k kernel alone on one layer of the DeepSeek-V3.2-shaped
     workload (32 requests x 131072 tokens, k = 2048, 5% hot keys): 554 MB of keys and scales
     per launch, so the launch's start-up and tail weigh little next to the read.  Predictor
-    on (theta from the previous call's top-k, so the histogram is shifted), no residency
-    filter: 132 B per token read (128 key bytes + the fp32 scale).  L2 flushed before each
-    call; the top-k reads the scores the score kernel just wrote (L2-resident)."""
+    on (theta from the previous call's top-k, so the histogram is shifted), and the score call
+    of the decode step: the layer's GPU cache (8192 slots per request) filters the above-
+    threshold marks, so the kernel reads 136 B per token (128 key bytes, the fp32 scale, the
+    4-byte slot entry) of which 132 are the method's.  L2 flushed before each call; the top-k
+    reads the scores the score kernel just wrote (L2-resident)."""
     import torch
     from sparse_attention_kv_echo_gb300 import _lib as L
     from sparse_attention_kv_echo_gb300 import workloads as wl
@@ -696,6 +698,9 @@ def run_kernels(args):
     sel = torch.full((B, w.k), -1, **i32)
     status, stats = torch.zeros(1, **i32), torch.zeros(L.STATS_N, **i32)
     cands = L.Cands(B, device=dev)
+    # the scores read only the cache's tables here: a one-row host pool stands in for the rows
+    cache = L.LayerCache(B, n, w.C, torch.empty((1, wl.KV_DIM), dtype=torch.bfloat16).pin_memory(), device=dev)
+    above = torch.zeros(max(L.above_words(B, n), 1), **i32)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     main = torch.cuda.Stream()
     qs = [qsrc.next() for _ in range(args.warmup + args.steps)]
@@ -706,7 +711,8 @@ def run_kernels(args):
             L.quantize_q(q, wt, q8, qscale, wfold, status, hist=hist, stream=main, cand_cnt=cands.cnt)
             flush.zero_()
             ev[0].record(main)
-            L.index_scores(tok_off, n, q8, wfold, k8, ks, scores, theta, hist, status, stream=main, cands=cands)
+            L.index_scores(tok_off, n, q8, wfold, k8, ks, scores, theta, hist, status, above=above, cache=cache,
+                           stream=main, cands=cands)
             ev[1].record(main)
             ev[2].record(main)
             L.topk_select_cands(tok_off, n, scores, w.k, hist, theta, 0.5, cands, sel, kth, status, stats=stats,
@@ -730,7 +736,8 @@ def run_kernels(args):
                    "l2": "flushed by a 256 MB write before every score call"},
         "roofline": {"kernel": "score_kernel (echo_index_scores)", "bound": "hbm", "achieved": round(gbs, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
-                     "algorithmic_bytes": score_bytes, "bytes_per_token": 132, "peak_source": f"hbm_gbs, {kind}"},
+                     "algorithmic_bytes": score_bytes, "bytes_per_token": 132, "peak_source": f"hbm_gbs, {kind}",
+                     "traffic": score_kernel_traffic(f"score_kernel_{w.name}.txt")},
         "score_us": round(1e6 * ts, 2), "topk_us": round(1e6 * tt, 2),
         "scoring_topk_gbs": round(both, 1), "scoring_topk_frac_of_8tbs": round(both / 8000.0, 4),
         "scoring_topk_frac_of_measured": round(both / peak, 4),
@@ -940,8 +947,10 @@ def run_pool(args):
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     main = torch.cuda.Stream()
     out = {}
-    for name, pool in (("per_request", 0), ("pool_32768", w.B * w.C), ("pool_260000", 260000)):
-        lay = DecodeLayer(off, k8, ks, w.k, w.C, host, pool_slots=pool, groups=1 if pool else None, device=dev)
+    for name, pool, lazy in (("per_request", 0, False), ("pool_32768", w.B * w.C, False), ("pool_260000", 260000, False),
+                             ("per_request_lazy", 0, True), ("pool_260000_lazy", 260000, True)):
+        lay = DecodeLayer(off, k8, ks, w.k, w.C, host, pool_slots=pool, groups=1 if pool else None, lazy=lazy,
+                          device=dev)
         with torch.cuda.stream(main):
             lay.w_in.copy_(wt)
         torch.cuda.synchronize()
@@ -973,6 +982,7 @@ def run_pool(args):
         out[name] = dict(steps_s=round(args.steps / (sum(ms) / 1e3), 1), ms_per_step=round(statistics.mean(ms), 4),
                          early_per_step=round(float(st[L.STAT_EARLY]) / args.steps, 1),
                          late_misses_per_step=round(float(st[L.STAT_MISSES]) / args.steps, 1),
+                         revived_per_step=round(float(st[L.STAT_REVIVED]) / args.steps, 1),
                          status=int(lay.status.item()), launches=lay.kernel_launches_per_step())
         del graphs, lay
         torch.cuda.synchronize()
@@ -982,6 +992,7 @@ def run_pool(args):
         "higher_is_better": True, "dtype": "fp8-e4m3 MMA, fp32 accumulate, int32 tables", "data": "synthetic (seeded)",
         "config": dict(workload_config(w), l2="flushed by a 256 MB write before every timed step"),
         "per_request_slots": out["per_request"], "pool_32768": out["pool_32768"], "pool_260000": out["pool_260000"],
+        "lazy_reuse": {"per_request_slots": out["per_request_lazy"], "pool_260000": out["pool_260000_lazy"]},
     }), flush=True)
 
 

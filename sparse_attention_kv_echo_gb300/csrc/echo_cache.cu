@@ -290,7 +290,31 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
             if (w < words) free_word(w, own[r]);
         }
     } else {
-        for (int w = warp; w < words; w += kCT / 32) free_word(w, s2t[w * 32 + lane]);
+        // C beyond the registers: only the slots that held a resident token at the start (free bit
+        // clear in freebits, which this kernel writes at its end only) and are not kept are read,
+        // their owners' loads issued together; lazy reuse keeps the entries and reads nothing
+        for (int w = tid; w < words; w += kCT) {
+            uint32_t occ = ~__ldcg(fb + w) & ~keep[w];
+            if (!occ) continue;
+            fbs[w] |= occ;
+            while (occ && !lazy) {
+                int32_t ps[8], po[8];
+                int cnt = 0;
+                while (occ && cnt < 8) {
+                    ps[cnt++] = w * 32 + (__ffs(occ) - 1);
+                    occ &= occ - 1;
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (i < cnt) po[i] = s2t[ps[i]];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (i < cnt) {
+                        s2t[ps[i]] = -1;
+                        if (po[i] >= 0 && po[i] < n) t2s[po[i]] = -1;
+                    }
+            }
+        }
     }
     if (used) atomicAdd(&s_early_used, used);
     __syncthreads();
