@@ -51,16 +51,12 @@ constexpr uint32_t kSideBytes = kSideBox * 4;
 constexpr uint32_t kIdesc = idesc_e4m3_f32(kTileM, ECHO_HEADS);
 
 // Segments: decode requests (keys and scores at rows [tok_off[b], end) with
-// end = tok_end[b] when given, else tok_off[b+1]) or prefill rows (W > 0: row b at position
-// row0 + b sees keys [0, row0 + b] and writes its scores at b * W).
+// end = tok_end[b] when given, else tok_off[b+1]).
 struct ScoreArgs {
     int B;
     const int64_t* tok_off;
     const int64_t* tok_end;    // optional current ends (growing contexts)
     int64_t n_tokens;
-    int64_t row0;
-    int64_t W;
-    int theta_stride;
     const float* wfold;
     float* scores;
     const float* theta_hat;
@@ -135,16 +131,8 @@ struct Seg {
     int64_t out;      // index of its first score
 };
 
-// Segment of request (row) b from the arguments; bad segments are empty.
+// Segment of request b from the arguments; bad segments are empty.
 __device__ __forceinline__ Seg segment(const ScoreArgs& a, int b, bool* bad) {
-    if (a.W > 0) {
-        const int64_t len = a.row0 + b + 1;
-        if (len > a.n_tokens || len > a.W) {
-            *bad = true;
-            return Seg{0, 0, 0};
-        }
-        return Seg{0, len, static_cast<int64_t>(b) * a.W};
-    }
     int64_t lo, hi;
     if (!seg_bounds(a.tok_off, a.tok_end, a.n_tokens, b, &lo, &hi)) {
         *bad = true;
@@ -157,7 +145,7 @@ __device__ __forceinline__ Seg segment(const ScoreArgs& a, int b, bool* bad) {
 __device__ __forceinline__ Seg cached_segment(const ScoreArgs& a, const int32_t* seg_lo, const int32_t* seg_len,
                                               int b) {
     const int64_t lo = seg_lo[b], len = seg_len[b];
-    return Seg{lo, len, a.W > 0 ? static_cast<int64_t>(b) * a.W : lo};
+    return Seg{lo, len, lo};
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -467,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     wv[4 * i + 3] = x.w;
                 }
                 const float th =
-                    a.theta_hat ? a.theta_hat[static_cast<int64_t>(b) * a.theta_stride] : __int_as_float(0x7f800000);
+                    a.theta_hat ? a.theta_hat[b] : __int_as_float(0x7f800000);
 
                 theta_ok = isfinite(th);
                 theta = th;
@@ -637,7 +625,7 @@ static int index_scores(int B, const int64_t* tok_off, const int64_t* tok_end, i
                   !is_aligned(cands->cut, 4)))
         return ECHO_EINVAL;
     if (n_tokens == 0) return ECHO_OK;
-    ScoreArgs args{B, tok_off, tok_end, n_tokens, 0, 0, 1, wfold, scores, theta_hat, hist, above,
+    ScoreArgs args{B, tok_off, tok_end, n_tokens, wfold, scores, theta_hat, hist, above,
                    cache ? 1 : 0, status, cache ? cache->freebits : nullptr,
                    cache ? cache->free_snap : nullptr,
                    cache ? static_cast<int64_t>(B) * (cache->C / 32) : 0,
@@ -666,23 +654,6 @@ extern "C" int echo_index_scores_cands(int B, const int64_t* tok_off, const int6
     if (!cands) return ECHO_EINVAL;
     return echo::index_scores(B, tok_off, tok_end, n_tokens, q8, wfold, k8, ks, scores, theta_hat, hist, above, cache,
                               cands, ctas, status, stream);
-}
-
-extern "C" int echo_prefill_scores(int R, int64_t row0, int64_t n_keys, const uint8_t* q8, const float* wfold,
-                                   const uint8_t* k8, const float* ks, float* scores, int64_t W,
-                                   const float* theta_hat, uint32_t* hist, int32_t* status, echo_stream_t stream) {
-    using namespace echo;
-    if (R <= 0 || row0 < 0 || n_keys <= 0) return ECHO_EINVAL;
-    if (R > ECHO_MAX_REQUESTS) return ECHO_EUNSUPPORTED;
-    if (!q8 || !wfold || !k8 || !ks || !scores || !status) return ECHO_EINVAL;
-    if (row0 + R > n_keys || W < row0 + R) return ECHO_EINVAL;
-    if (n_keys >= (1ll << 31) || static_cast<int64_t>(R) * W >= (1ll << 40)) return ECHO_EUNSUPPORTED;
-    if (!is_aligned(q8, 16) || !is_aligned(wfold, 16) || !is_aligned(k8, 16) || !is_aligned(ks, 16))
-        return ECHO_EINVAL;
-    ScoreArgs args{R, nullptr, nullptr, n_keys, row0, W, 0, wfold, scores, theta_hat, hist, nullptr, 0, status, nullptr,
-                   nullptr, 0, nullptr, nullptr, nullptr, nullptr, 0};
-    const int64_t tiles_ub = static_cast<int64_t>(R) * ((row0 + R + kTileM - 1) / kTileM);
-    return launch_scores(args, q8, k8, ks, nullptr, n_keys, tiles_ub, 0, stream);
 }
 
 extern "C" size_t echo_above_words(int B, int64_t n_tokens) {

@@ -5,7 +5,8 @@ histogram, threshold state, selection, the GPU cache and its lists, the
 quantised query) and issues the calls of a step:
     echo_quantize_q    -> E4M3 query, folded head weights, cleared histogram
     echo_index_scores  -> scores, shifted-score histogram, above-threshold bits,
-                          free-bit snapshot, and (cands=True, the default) each
+                          free-bit snapshot, and (cands; by default when the
+                          requests average 65536 tokens or more) each
                           request's candidate list for top-k
     echo_early_fetch   -> rows of the tokens above the predicted threshold,
                           copied from the host pool on the step's stream
@@ -38,7 +39,7 @@ class DecodeLayer:
                  early_cap: int = -1, groups: int | None = None, first_share: float = 0.5,
                  resolved: bool = True, hold_early: bool = False, attention: bool = False,
                  mla_scale: float = 1.0 / math.sqrt(192.0), tok_end=None, cross_layer: bool = False,
-                 pool_slots: int = 0, cands: bool = True, cand_cap: int = L.CAND_CAP, lazy: bool = False,
+                 pool_slots: int = 0, cands: bool | None = None, cand_cap: int = L.CAND_CAP, lazy: bool = False,
                  device="cuda"):
         tok_off = torch.as_tensor(tok_off, dtype=torch.int64)
         self.B = int(tok_off.numel() - 1)
@@ -88,7 +89,10 @@ class DecodeLayer:
         if self.cross_layer or self.pool_slots:
             groups = 1
         if groups is None:
-            groups = 2 if (self.predictor and self.B >= 2) else 1
+            # the early fetch of a group streams while the groups after it are scored: more groups
+            # start the host link sooner (32 x 131072: 1 group 389, 2 629, 3 693, 4 737, 8 387 steps/s;
+            # 8 x 32768: 2 groups best)
+            groups = (4 if self.B >= 16 else 2) if (self.predictor and self.B >= 2) else 1
         groups = max(1, min(int(groups), self.B))
         bounds = [self.B * g // groups for g in range(groups + 1)]
         if groups == 2:  # the second group's scores gate top-k; a smaller second group starts it sooner
@@ -126,6 +130,10 @@ class DecodeLayer:
         self.views = [] if self.pool_slots else [self.cache.view(b0, b1) for b0, b1 in self.groups]
         # candidate lists: the score kernel lists each request's tokens above a cut that top-k sets
         # for the next step, and top-k selects among them when they hold the top-k
+        # (default: lists when the requests average 65536 tokens or more -- at 32768 a list holds a
+        # quarter of a request, and the 8-CTA clusters select faster)
+        if cands is None:
+            cands = self.n_tokens >= 65536 * self.B
         self.cands = L.Cands(self.B, cand_cap, device=device) if cands else None
         self.cands_g = ([self.cands.view(b0, b1) for b0, b1 in self.groups] if self.cands is not None
                         else [None] * len(self.groups))
