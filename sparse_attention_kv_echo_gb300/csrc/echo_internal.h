@@ -56,6 +56,11 @@ constexpr int kMaxSlots = 1 << 19;   // slots per request: per-slot-word tables 
 int launch_topk(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens, int64_t row0, int64_t W, const float* scores, int k,
                 const uint32_t* hist, float* theta_hat, float alpha, int32_t* sel_idx, float* kth, int32_t* status,
                 uint32_t* stats, cudaStream_t stream);
+// Prefill rows' top-k (select_kernel, one block per row): row b of R at position row0 + b selects
+// among scores[b * W + s], s <= row0 + b; theta_hat[0] shifts the rows' histograms and is not updated.
+int launch_select_rows(int R, int64_t row0, int64_t W, const float* scores, int k, const uint32_t* hist,
+                       float* theta_hat, int32_t* sel_idx, float* kth, int32_t* status, uint32_t* stats,
+                       cudaStream_t stream);
 int check_cache_step_args(int B, int64_t n_tokens, const int32_t* sel, int m, const echo_cache* cache,
                           const int32_t* sel_slot);
 int enqueue_cache_step(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens, const int32_t* sel,

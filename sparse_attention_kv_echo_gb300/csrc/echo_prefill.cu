@@ -8,11 +8,14 @@
 //
 // echo_prefill_block enqueues, on `stream`:
 //   quantize_kernel      the block's R query rows (each row is its own "request")
-//   score_kernel         prefill mode: row r at position row0 + r scores keys
-//                        [0, row0 + r] (causal, itself included) into scores[r*W + s],
-//                        with the per-row histogram shifted by the block's threshold
-//   row_topk_kernel      one CTA per row: exact top-k of the row, its boundary
-//                        bin taken from the row's histogram
+//   prefill_score_kernel row r at position row0 + r scores keys [0, row0 + r]
+//                        (causal, itself included) into scores[r*W + s], 8 rows per
+//                        key tile, with the per-row histogram shifted by the block's
+//                        threshold (echo_prefill_scores.cu)
+//   select_kernel        one block per row: exact top-k of the row, its boundary
+//                        bin taken from the row's histogram, the row's scores read
+//                        once (the tokens above the bin into a bitmap, the bin's
+//                        entries into shared memory; echo_select.cu)
 //   union_mark_kernel    marks every token some row selected
 //   union_compact_kernel ascending list of the marked tokens (the block's
 //                        selection for the cache), its bit words, and the

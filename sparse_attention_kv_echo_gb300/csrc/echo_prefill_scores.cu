@@ -15,24 +15,29 @@
 // a key tile is read once per four rows and one MMA does the work of four.
 //
 // A unit is 8 consecutive rows: all of TMEM (512 columns) holds their 8 x 64
-// head sums for one 128-key tile, as 512 / N accumulators of N columns (N = 256:
-// two MMAs of four rows each; N = 128: four of two rows), so a key tile leaves
-// L2 once per 8 rows.
+// head sums for one 128-key tile, as two accumulators of 256 columns, so a key
+// tile leaves L2 once per 8 rows.  (N = 128 -- four MMAs of two rows -- measured
+// slower: an MMA of N <= 128 costs nearly as much as one of N = 256.)
 //
-// Design (one persistent CTA per SM, 320 threads, warp-specialised):
+// Design (one persistent CTA per SM, 576 threads, warp-specialised):
 //   warp 0      TMA producer: 128-key x 128-byte tiles into a 6-stage ring
 //               (128-byte swizzle); the unit's 512 q8 rows (64 KB, two boxes)
 //               into the q buffer when the unit changes.
 //   warp 1      TMEM owner (512 columns) and single-thread MMA issuer: per
-//               tile, one accumulator after the other, four K-steps each.
-//   warps 2-9   two epilogue groups of four warps; group e drains the
-//               accumulators a = e (mod 2) of every tile, i.e. four of the
-//               unit's rows.  Each thread owns one key: per row, tcgen05.ld of
-//               the row's 64 head sums (the next row's load in flight while
-//               this one is summed), ReLU, the weighted sum in packed f32x2
-//               FMAs, times the key scale, the causal mask, store, and a
-//               warp-private histogram per row flushed with global atomics
-//               when the unit changes.
+//               tile, two MMAs (rows 0-3 and 4-7 of the unit) of four K-steps.
+//   warps 2-17  sixteen epilogue warps, four per TMEM lane quarter; each owns
+//               two rows of the unit and, per thread, one key of the tile:
+//               tcgen05.ld of the rows' head sums 32 columns at a time, ReLU,
+//               the weighted sum in packed f32x2 FMAs over four chains, times
+//               the key scale, the causal mask, store, and a warp-private
+//               histogram per row (match.any groups, red.shared counts)
+//               flushed with global atomics when the unit changes.  An
+//               accumulator goes back to the MMA as soon as the eight warps
+//               that drain it have loaded their columns.
+// The epilogue is the bound, not the tensor pipe: per (key, row) it issues a
+// ReLU and half an FMA pair per head against the MMA's 256 FLOPs, so it gets
+// as many warps as 96 registers a thread allow (four per scheduler) to hide
+// the TMEM-load and FMA latencies.
 // The tiles of all units (ceil(keys of the unit's last row / 128) each) form
 // one list; CTA c takes a contiguous share.  The keys of the prompt's prefix
 // stay in L2 (at most 102400 x 132 B), so the kernel is bound by the tensor pipe
@@ -43,24 +48,24 @@
 namespace echo {
 namespace {
 
-#ifndef ECHO_PREFILL_N
-#define ECHO_PREFILL_N 256
-#endif
-constexpr int kN = ECHO_PREFILL_N;                     // the MMA's N: rows per MMA x 64 heads
-static_assert(kN == 128 || kN == 256, "N of the prefill MMA: 128 or 256");
+constexpr int kN = 256;                                // the MMA's N: 4 rows x 64 heads
 constexpr int kRows = 8;                               // rows per unit
-constexpr int kG = kN / ECHO_HEADS;                    // rows per MMA
-constexpr int kAcc = kRows / kG;                       // accumulators (MMAs per tile)
+constexpr int kG = kN / ECHO_HEADS;                    // rows per MMA (4)
+constexpr int kAcc = kRows / kG;                       // accumulators (MMAs per tile): 2
 constexpr int kTmemCols = kAcc * kN;                   // 512
 constexpr int kStages = 6;                             // key ring
 constexpr int kTileM = 128;                            // keys per tile (MMA M)
 constexpr int kKeyBytes = kTileM * ECHO_DIM;           // 16 KB
 constexpr int kQBytes = kRows * ECHO_HEADS * ECHO_DIM; // 64 KB: a unit's q8
 constexpr int kQBox = 256;                             // q8 rows per TMA box
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + kEpiWarps * 32;          // 320
-constexpr int kEpiRows = kRows / 2;                    // rows of a unit per epilogue group
+constexpr int kEpiWarps = 16;                          // four per TMEM lane quarter
+constexpr int kSlots = kEpiWarps / 4;                  // epilogue warps per lane quarter
+constexpr int kRPW = kRows / kSlots;                   // rows of a unit per epilogue warp (2)
+constexpr int kAccWarps = 4 * (kG / kRPW);             // epilogue warps that drain one accumulator (8)
+constexpr int kPieces = 2 * kRPW;                      // 32-column TMEM loads per warp and tile
+constexpr int kThreads = 64 + kEpiWarps * 32;
 constexpr uint32_t kIdesc = idesc_e4m3_f32(kTileM, kN);
+static_assert(kG % kRPW == 0, "a warp's rows sit in one accumulator");
 
 struct PfArgs {
     int R;                   // rows of the block
@@ -77,7 +82,7 @@ struct PfArgs {
 };
 
 struct __align__(128) PfCtl {
-    float wv[kEpiWarps][kEpiRows][ECHO_HEADS];   // each epilogue warp's copy of its rows' weights
+    float wv[kEpiWarps][kRPW][ECHO_HEADS];       // each epilogue warp's copy of its rows' weights
     uint64_t full[kStages];
     uint64_t empty[kStages];
     uint64_t qfull;
@@ -87,8 +92,8 @@ struct __align__(128) PfCtl {
     uint64_t done;
     uint32_t tmem_base;
     int abort;
-    uint32_t scan[16];
-    uint32_t hist[kEpiWarps][kEpiRows][256];     // per epilogue warp, per row
+    uint32_t scan[kThreads / 32 + 1];
+    uint32_t hist[kEpiWarps][kRPW][256];         // per epilogue warp, per row
 };
 
 // keys | q8 | PfCtl | tstart[units + 1] (int32)
@@ -116,9 +121,6 @@ __device__ __forceinline__ int find_unit(const int32_t* tstart, int U, uint32_t 
     return lo;
 }
 
-// Row of the unit (0..7) behind epilogue group e's l-th row: accumulator e + 2 * (l / kG), its row l % kG.
-__device__ __forceinline__ constexpr int acc_of(int e, int l) { return e + 2 * (l / kG); }
-__device__ __forceinline__ constexpr int unit_row(int e, int l) { return acc_of(e, l) * kG + l % kG; }
 
 // d = a * b + c on two fp32 lanes at once.
 __device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
@@ -152,29 +154,31 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t* r) {
         : "r"(taddr));
 }
 
-// 64 consecutive TMEM columns (one row's head sums) of this warp's 32 lanes.
-__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, uint32_t (&r)[64]) {
-    tmem_ld_x32(taddr, &r[0]);
-    tmem_ld_x32(taddr + 32, &r[32]);
+// Adds w[h] * max(0, x[h]) for 32 heads into kChains pair accumulators (FMA pair m of the piece
+// goes to p[m % kChains]), so that the dependent chains stay short.
+constexpr int kChains = 4;
+__device__ __forceinline__ void weighted_relu32(const uint32_t* r, const float* w, uint64_t* p) {
+    const float4* wp = reinterpret_cast<const float4*>(w);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {          // heads 4i .. 4i+3
+        const float4 w4 = wp[i];
+        const float x0 = fmaxf(__uint_as_float(r[4 * i + 0]), 0.f), x1 = fmaxf(__uint_as_float(r[4 * i + 1]), 0.f);
+        const float x2 = fmaxf(__uint_as_float(r[4 * i + 2]), 0.f), x3 = fmaxf(__uint_as_float(r[4 * i + 3]), 0.f);
+        p[(2 * i) % kChains] = ffma2(pack2(x0, x1), pack2(w4.x, w4.y), p[(2 * i) % kChains]);
+        p[(2 * i + 1) % kChains] = ffma2(pack2(x2, x3), pack2(w4.z, w4.w), p[(2 * i + 1) % kChains]);
+    }
 }
 
-// sum_h w[h] * max(0, x[h]): heads in four blocks of 16, each summed as (even, odd) pairs.
-__device__ __forceinline__ float weighted_relu(const uint32_t (&r)[64], const float* w) {
-    const float4* wp = reinterpret_cast<const float4*>(w);
-    uint64_t p[4] = {0ull, 0ull, 0ull, 0ull};
+// The row's sum of the kChains pair accumulators (a fixed tree).
+__device__ __forceinline__ float chains_sum(const uint64_t* p) {
+    float s[kChains];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {          // heads 4i .. 4i+3 of each block
+    for (int c = 0; c < kChains; ++c) s[c] = sum2(p[c]);
 #pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-            const float4 w4 = wp[blk * 4 + i];
-            const int h = blk * 16 + 4 * i;
-            const float x0 = fmaxf(__uint_as_float(r[h + 0]), 0.f), x1 = fmaxf(__uint_as_float(r[h + 1]), 0.f);
-            const float x2 = fmaxf(__uint_as_float(r[h + 2]), 0.f), x3 = fmaxf(__uint_as_float(r[h + 3]), 0.f);
-            p[blk] = ffma2(pack2(x0, x1), pack2(w4.x, w4.y), p[blk]);
-            p[blk] = ffma2(pack2(x2, x3), pack2(w4.z, w4.w), p[blk]);
-        }
-    }
-    return __fadd_rn(__fadd_rn(sum2(p[0]), sum2(p[1])), __fadd_rn(sum2(p[2]), sum2(p[3])));
+    for (int w = kChains / 2; w >= 1; w /= 2)
+#pragma unroll
+        for (int c = 0; c < w; ++c) s[c] = __fadd_rn(s[c], s[c + w]);
+    return s[0];
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -214,13 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_addr(&ctl->qempty), 1);
         for (int i = 0; i < kAcc; ++i) {
             mbar_init(smem_addr(&ctl->accfull[i]), 1);
-            mbar_init(smem_addr(&ctl->accempty[i]), 4);   // the group's four warps
+            mbar_init(smem_addr(&ctl->accempty[i]), kAccWarps);   // the warps that drain it
         }
         mbar_init(smem_addr(&ctl->done), 1);
         ctl->abort = 0;
         fence_barrier_init();
     }
-    for (int i = tid; i < kEpiWarps * kEpiRows * 256; i += kThreads) (&ctl->hist[0][0][0])[i] = 0u;
+    for (int i = tid; i < kEpiWarps * kRPW * 256; i += kThreads) (&ctl->hist[0][0][0])[i] = 0u;
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&kmap);
         prefetch_tmap(&qmap);
@@ -361,11 +365,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         pdl_wait();                            // wfold and the cleared histogram come from the quantiser
-        const int ew = warp - 2;               // 0..7
-        const int e = ew >> 2;                 // accumulators e, e + 2, ...
+        const int ew = warp - 2;               // 0 .. kEpiWarps-1
         const int quarter = warp & 3;          // TMEM lanes this warp may access
+        const int slot = ew >> 2;              // which of the quarter's warps
+        const int ur0 = slot * kRPW;           // the warp's first row of the unit
+        const int acc = ur0 / kG;              // the accumulator holding its rows
         const int row = quarter * 32 + lane;   // key within the tile
-        const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+        const uint32_t base_addr =
+            tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * kN + (ur0 % kG) * ECHO_HEADS;
         float (*wv)[ECHO_HEADS] = ctl->wv[ew];
         uint32_t (*whist)[256] = ctl->hist[ew];
         float shift = 0.f;
@@ -376,8 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto flush_hist = [&](int uu) {
             __syncwarp();
 #pragma unroll
-            for (int l = 0; l < kEpiRows; ++l) {
-                const int r = kRows * uu + unit_row(e, l);
+            for (int l = 0; l < kRPW; ++l) {
+                const int r = kRows * uu + ur0 + l;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const uint32_t v = whist[l][lane + 32 * j];
@@ -392,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int u = (ntiles > 0) ? find_unit(tstart, U, t_begin) : 0;
         int cur_u = -1;
         bool ok = true;
-        uint32_t rb[2][64];
+        uint32_t rb[32];
         for (uint32_t it = 0; ok && it < ntiles; ++it) {
             const uint32_t t = t_begin + it;
             while (t >= static_cast<uint32_t>(tstart[u + 1])) ++u;
@@ -401,8 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 cur_u = u;
                 __syncwarp();
 #pragma unroll
-                for (int l = 0; l < kEpiRows; ++l) {
-                    const int r = kRows * u + unit_row(e, l);
+                for (int l = 0; l < kRPW; ++l) {
+                    const int r = kRows * u + ur0 + l;
                     const bool in = r < a.R;
                     wv[l][lane] = in ? a.wfold[static_cast<size_t>(r) * ECHO_HEADS + lane] : 0.f;
                     wv[l][lane + 32] = in ? a.wfold[static_cast<size_t>(r) * ECHO_HEADS + lane + 32] : 0.f;
@@ -411,46 +418,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int64_t tok = static_cast<int64_t>(t - tstart[u]) * kTileM + row;
             const float ksv = tok < a.n_keys ? __ldg(a.ks + tok) : 0.f;
-            // rows in order; the next row's TMEM load is in flight while this one is summed
-            if (!mbar_wait(smem_addr(&ctl->accfull[acc_of(e, 0)]), it & 1, abort)) {
+            if (!mbar_wait(smem_addr(&ctl->accfull[acc]), it & 1, abort)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            tmem_ld_row(lane_addr + acc_of(e, 0) * kN, rb[0]);
+            // pieces of 32 head sums in order (row l = piece / 2, its heads 32 (piece % 2) ..)
+            uint64_t p[kChains];
 #pragma unroll
-            for (int l = 0; l < kEpiRows; ++l) {
-                const int acc = acc_of(e, l);
+            for (int c = 0; c < kChains; ++c) p[c] = 0ull;
+#pragma unroll
+            for (int pc = 0; pc < kPieces; ++pc) {
+                tmem_ld_x32(base_addr + pc * 32, rb);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 64; ++i) asm volatile("" : "+r"(rb[l & 1][i]));
-                if (l + 1 < kEpiRows && acc_of(e, l + 1) == acc) {
-                    tmem_ld_row(lane_addr + acc * kN + ((l + 1) % kG) * ECHO_HEADS, rb[(l + 1) & 1]);
-                } else {
-                    // this accumulator is read: hand it back (then wait for the group's next one)
+                for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(rb[i]));
+                if (pc + 1 == kPieces) {
+                    // every column this warp reads has arrived: hand the accumulator back
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_addr(&ctl->accempty[acc]));
-                    if (l + 1 < kEpiRows) {
-                        const int acc2 = acc_of(e, l + 1);
-                        if (!mbar_wait(smem_addr(&ctl->accfull[acc2]), it & 1, abort)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        tmem_ld_row(lane_addr + acc2 * kN + ((l + 1) % kG) * ECHO_HEADS, rb[(l + 1) & 1]);
-                    }
                 }
-                const int r = kRows * u + unit_row(e, l);
-                const float score = __fmul_rn(weighted_relu(rb[l & 1], wv[l]), ksv);
-                const bool valid = r < a.R && tok <= a.row0 + r;
-                const unsigned vm = __ballot_sync(0xffffffffu, valid);
-                if (valid) {
-                    a.scores[static_cast<int64_t>(r) * a.W + tok] = score;
-                    if (a.hist) {
-                        const uint32_t bin = shifted_bin(score, shift);
-                        const unsigned grp = __match_any_sync(vm, bin);
-                        if (lane == __ffs(grp) - 1) atomicAdd(&whist[l][bin], static_cast<uint32_t>(__popc(grp)));
+                const int l = pc >> 1, hh = pc & 1;
+                weighted_relu32(rb, &wv[l][hh * 32], p);
+                if (hh == 1) {
+                    const float sc = __fmul_rn(chains_sum(p), ksv);
+#pragma unroll
+                    for (int c = 0; c < kChains; ++c) p[c] = 0ull;
+                    const int r = kRows * u + ur0 + l;
+                    const bool valid = r < a.R && tok <= a.row0 + r;
+                    const unsigned vm = __ballot_sync(0xffffffffu, valid);
+                    if (valid) {
+                        a.scores[static_cast<int64_t>(r) * a.W + tok] = sc;
+                        if (a.hist) {
+                            const uint32_t bin = shifted_bin(sc, shift);
+                            const unsigned grp = __match_any_sync(vm, bin);
+                            if (lane == __ffs(grp) - 1) atomicAdd(&whist[l][bin], static_cast<uint32_t>(__popc(grp)));
+                        }
                     }
                 }
             }

@@ -104,6 +104,11 @@ struct SelArgs {
     int C;
     int32_t* status;
     uint32_t* stats;
+    // prefill rows (W > 0): row b at position row0 + b selects among scores[b * W + s],
+    // s <= row0 + b, its histogram shifted by the block's one threshold theta_hat[0],
+    // which the block's own EMA (not this kernel) updates
+    int64_t row0;
+    int64_t W;
 };
 
 // Warp 0: the key of the lower edge of the lowest histogram bin d with at most
@@ -167,15 +172,24 @@ __global__ void __launch_bounds__(kTT, 1) select_kernel(const SelArgs a) {
     uint32_t* const fbs = bm + kWinWords;
     uint32_t* const wpre = fbs + kFbMax;
     const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+    const bool rows = a.W > 0;
     int64_t lo, hi;
-    const bool range_ok = seg_bounds(a.tok_off, a.tok_end, a.n_tokens, b, &lo, &hi);
+    bool range_ok;
+    if (rows) {
+        lo = static_cast<int64_t>(b) * a.W;
+        hi = lo + a.row0 + b + 1;
+        range_ok = a.row0 + b + 1 <= a.W;
+        if (!range_ok) hi = lo;
+    } else {
+        range_ok = seg_bounds(a.tok_off, a.tok_end, a.n_tokens, b, &lo, &hi);
+    }
     const int64_t n = hi - lo;
     const float* sc = a.scores + lo;
     const uint32_t k = static_cast<uint32_t>(a.k);
     int32_t* out = a.sel + static_cast<int64_t>(b) * a.k;
     const bool cached = a.sel_slot != nullptr;
     int32_t* out_slot = cached ? a.sel_slot + static_cast<int64_t>(b) * a.k : nullptr;
-    const float th_old = a.theta_hat ? a.theta_hat[b] : __int_as_float(0x7f800000);
+    const float th_old = a.theta_hat ? a.theta_hat[rows ? 0 : b] : __int_as_float(0x7f800000);
     const float shift = isfinite(th_old) ? th_old : 0.f;
     const int words = cached ? a.C / 32 : 0;
     int32_t* t2s = cached ? a.tok2slot + lo : nullptr;
@@ -534,7 +548,7 @@ __global__ void __launch_bounds__(kTT, 1) select_kernel(const SelArgs a) {
         if (st) set_status(a.status, st);
         const float kth = key_to_float(K);
         a.kth[b] = kth;
-        if (a.theta_hat) a.theta_hat[b] = ema_update(th_old, kth, a.alpha);
+        if (a.theta_hat && !rows) a.theta_hat[b] = ema_update(th_old, kth, a.alpha);
         if (a.c_cut) a.c_cut[b] = (mode == kAll) ? kNoCut : sh.cut;
         if (cached) {
             const uint32_t E = ab ? min(run_ab, limit) : 0u;
@@ -546,6 +560,30 @@ __global__ void __launch_bounds__(kTT, 1) select_kernel(const SelArgs a) {
 }
 
 }  // namespace
+
+int launch_select_rows(int R, int64_t row0, int64_t W, const float* scores, int k, const uint32_t* hist,
+                       float* theta_hat, int32_t* sel_idx, float* kth, int32_t* status, uint32_t* stats,
+                       cudaStream_t stream) {
+    SelArgs a{};
+    a.scores = scores;
+    a.k = k;
+    a.hist = hist;
+    a.theta_hat = theta_hat;
+    a.sel = sel_idx;
+    a.kth = kth;
+    a.status = status;
+    a.stats = stats;
+    a.early_cap = 0;
+    a.row0 = row0;
+    a.W = W;
+    ECHO_CUDA_OK(prefer_max_shared(select_kernel));
+    ECHO_CUDA_OK(cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(kSelSmem)));
+    select_kernel<<<R, kTT, kSelSmem, stream>>>(a);
+    ECHO_CUDA_OK(cudaGetLastError());
+    return ECHO_OK;
+}
+
 }  // namespace echo
 
 extern "C" int echo_topk_select_cands(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n_tokens,

@@ -701,172 +701,6 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTT, 1)
     cluster_wait_acquire();  // no CTA leaves while another may still read its shared memory
 }
 
-// Prefill rows: one CTA (1024 threads) per row, no cluster -- the rows of a
-// block are many, so a CTA per row keeps the SMs full with two rows each.  Row
-// b (position row0 + b) selects among scores[b * W + s], s <= row0 + b:
-//   1. the boundary bin b* and the count above it from the row's histogram (the
-//      score kernel's; rebuilt here when none is given or it does not describe
-//      the row, the latter also flagged as bad data);
-//   2. one coalesced pass: the bin-b* entries (order key, index) into shared
-//      memory (past kCandMax the bin is selected from global memory), the
-//      count above b* checked against the histogram;
-//   3. the cut in bin b*: the (k - above)-th largest key, ties to the lower
-//      index (radix select on the key, then on the inverted index);
-//   4. the selected indices in ascending order, 4096 tokens per block scan.
-__global__ void __launch_bounds__(kTT)
-    row_topk_kernel(int64_t row0, int64_t W, const float* __restrict__ scores, int k, const uint32_t* __restrict__ hist,
-                    const float* theta_hat, int32_t* __restrict__ sel, float* kth_out, int32_t* status,
-                    uint32_t* stats) {
-    pdl_launch_dependents();
-    extern __shared__ uint8_t smem_raw[];
-    TopkShared& sh = *reinterpret_cast<TopkShared*>(smem_raw);
-    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
-    int64_t n = row0 + b + 1;
-    if (n > W) {
-        if (tid == 0) set_status(status, ECHO_ST_BADDATA);
-        n = 0;
-    }
-    const float* sc = scores + static_cast<int64_t>(b) * W;
-    int32_t* out = sel + static_cast<int64_t>(b) * k;
-    const float th = theta_hat ? theta_hat[0] : __int_as_float(0x7f800000);
-    const float shift = isfinite(th) ? th : 0.f;
-    if (n == 0) {
-        for (int i = tid; i < k; i += kTT) out[i] = -1;
-        if (tid == 0) kth_out[b] = __int_as_float(0xff800000);
-        return;
-    }
-    if (n <= k) {  // everything is selected
-        if (tid == 0) {
-            sh.minkey = 0xFFFFFFFFu;
-            sh.flag = 0;
-        }
-        __syncthreads();
-        uint32_t mk = 0xFFFFFFFFu;
-        bool nan = false;
-        for (int64_t s = tid; s < n; s += kTT) {
-            const float x = sc[s];
-            nan |= isnan(x);
-            mk = min(mk, order_key(x));
-        }
-        for (int i = tid; i < k; i += kTT) out[i] = (i < n) ? i : -1;
-        atomicMin(&sh.minkey, mk);
-        if (nan) sh.flag = 1;
-        __syncthreads();
-        if (tid == 0) {
-            kth_out[b] = key_to_float(sh.minkey);
-            if (sh.flag) set_status(status, ECHO_ST_NAN);
-        }
-        return;
-    }
-    // ---- 1-2. boundary bin, its entries, the count above it
-    bool have = hist != nullptr;
-    uint32_t bstar = 0, above = 0, cnt = 0;
-    for (int attempt = 0; attempt < 2; ++attempt) {
-        if (have) {
-            for (int i = tid; i < 256; i += kTT) sh.hist[i] = hist[static_cast<int64_t>(b) * 256 + i];
-        } else {
-            for (int i = tid; i < 256; i += kTT) sh.hist[i] = 0u;
-            __syncthreads();
-            for (int64_t s0 = tid & ~31; s0 < n; s0 += kTT) {
-                const int64_t s = s0 + lane;
-                const bool ok = s < n;
-                const uint32_t d = ok ? shifted_bin(sc[s], shift) : 0x100u;
-                const unsigned peers = __match_any_sync(0xffffffffu, d);
-                if (ok && lane == __ffs(peers) - 1) atomicAdd(&sh.hist[d], static_cast<uint32_t>(__popc(peers)));
-            }
-        }
-        __syncthreads();
-        if (tid < 32) find_digit(sh.hist, static_cast<uint32_t>(k), &sh.digit, &sh.above);
-        if (tid == 0) {
-            sh.cnt = 0;
-            sh.n_above = 0;
-        }
-        __syncthreads();
-        bstar = sh.digit;
-        above = sh.above;
-        const uint32_t eq_total = sh.hist[bstar];
-        uint32_t my_above = 0;
-        for (int64_t s0 = tid & ~31; s0 < n; s0 += kTT) {
-            const int64_t s = s0 + lane;
-            const bool ok = s < n;
-            const float x = ok ? sc[s] : 0.f;
-            const uint32_t bin = shifted_bin(x, shift);
-            my_above += (ok && bin > bstar) ? 1u : 0u;
-            const bool cand = ok && bin == bstar;
-            const unsigned m = __ballot_sync(0xffffffffu, cand);
-            if (m) {
-                const int first = __ffs(m) - 1;
-                uint32_t base = 0;
-                if (lane == first) base = atomicAdd(&sh.cnt, static_cast<uint32_t>(__popc(m)));
-                base = __shfl_sync(0xffffffffu, base, first);
-                const uint32_t pos = base + __popc(m & ((1u << lane) - 1u));
-                if (cand && pos < static_cast<uint32_t>(kCandMax)) {
-                    sh.cand_key[pos] = order_key(x);
-                    sh.cand_idx[pos] = static_cast<uint32_t>(s);
-                }
-            }
-        }
-        my_above = __reduce_add_sync(0xffffffffu, my_above);
-        if (lane == 0 && my_above) atomicAdd(&sh.n_above, my_above);
-        __syncthreads();
-        cnt = sh.cnt;
-        if (sh.n_above == above && cnt == eq_total) break;
-        // the histogram given does not describe this row: count it here
-        if (tid == 0) set_status(status, ECHO_ST_BADDATA);
-        have = false;
-        __syncthreads();  // every thread has read the counts before they are reset
-    }
-    const bool fits = cnt <= static_cast<uint32_t>(kCandMax);
-    if (tid == 0 && stats) {
-        atomicMax(stats + ECHO_STAT_BOUNDARY_MAX, cnt);
-        if (!fits) atomicAdd(stats + ECHO_STAT_TOPK_FALLBACK, 1u);
-    }
-    // ---- 3. the cut: the need-th largest key of bin b*, then the index among equal keys
-    const uint32_t need = static_cast<uint32_t>(k) - above;  // >= 1
-    uint32_t K, cut = 0xFFFFFFFFu;
-    if (fits) {
-        uint32_t rem, eq;
-        K = radix_select(SmemCands{sh.cand_key, sh.cand_idx, cnt, false, 0u}, need, sh, &rem, &eq);
-        if (rem < eq) {
-            uint32_t r2, e2;
-            cut = ~radix_select(SmemCands{sh.cand_key, sh.cand_idx, cnt, true, K}, rem, sh, &r2, &e2);
-        }
-    } else {
-        K = global_select(sc, n, shift, bstar, need, sh, &cut);
-    }
-    // ---- 4. ascending output, 4 consecutive tokens per thread
-    uint32_t written = 0;
-    bool nan = false;
-    for (int64_t c0 = 0; c0 < n; c0 += 4 * kTT) {
-        const int64_t s0 = c0 + 4 * tid;
-        uint32_t f = 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int64_t s = s0 + j;
-            if (s < n) {
-                const float x = sc[s];
-                nan |= isnan(x);
-                if (takes(x, shift, bstar, K, cut, s)) f |= 1u << j;
-            }
-        }
-        uint32_t tot;
-        uint32_t pos = written + block_exclusive_scan<kTT>(__popc(f), sh.scan, &tot);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (f & (1u << j)) {
-                if (pos < static_cast<uint32_t>(k)) out[pos] = static_cast<int32_t>(s0 + j);
-                ++pos;
-            }
-        written += tot;
-    }
-    for (int i = static_cast<int>(min(written, static_cast<uint32_t>(k))) + tid; i < k; i += kTT) out[i] = -1;
-    if (tid == 0) {
-        if (written != static_cast<uint32_t>(k)) set_status(status, ECHO_ST_BADDATA);
-        kth_out[b] = key_to_float(K);
-    }
-    if (__any_sync(0xffffffffu, nan) && lane == 0) set_status(status, ECHO_ST_NAN);
-}
-
 }  // namespace
 }  // namespace echo
 
@@ -879,14 +713,8 @@ int launch_topk(int B, const int64_t* tok_off, const int64_t* tok_end, int64_t n
     ECHO_CUDA_OK(prefer_max_shared(topk_kernel));
     ECHO_CUDA_OK(cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       static_cast<int>(smem)));
-    if (W > 0) {  // prefill rows: a CTA per row
-        const size_t rsmem = sizeof(TopkShared);
-        ECHO_CUDA_OK(cudaFuncSetAttribute(row_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          static_cast<int>(rsmem)));
-        row_topk_kernel<<<B, kTT, rsmem, stream>>>(row0, W, scores, k, hist, theta_hat, sel_idx, kth, status, stats);
-        ECHO_CUDA_OK(cudaGetLastError());
-        return ECHO_OK;
-    }
+    if (W > 0)  // prefill rows: one block per row, each row's scores read once
+        return launch_select_rows(B, row0, W, scores, k, hist, theta_hat, sel_idx, kth, status, stats, stream);
     TopkSegs segs{tok_off, tok_end, n_tokens, row0, W};
     topk_kernel<<<B * kCS, kTT, smem, stream>>>(segs, scores, k, hist, theta_hat, alpha, sel_idx, kth, status, stats);
     ECHO_CUDA_OK(cudaGetLastError());

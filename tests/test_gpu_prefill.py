@@ -123,12 +123,21 @@ def test_prefill_rows_fewer_than_k():
 
 def test_prefill_all_keys_equal():
     """Every key the same, so every score of a row ties: each row selects its lowest
-    k positions (ties go to the lower index), the union is [0, k), and rows longer
-    than 6144 tokens -- a boundary bin too large for the shared-memory list --
-    select from global memory."""
+    k positions (ties go to the lower index) and the union is [0, k)."""
     w = wl.scaled(wl.WORKLOADS["prefill"], "pf_ties", lengths=(8192,), prefill_block=2048, k=256, C=8192)
     pr = _run(w, full_rows=True, row_sample=4, same_keys=True)
     sel = pr.sel_idx[:2048].cpu().numpy()
     assert np.array_equal(sel[-1], np.arange(256, dtype=np.int32))
+
+
+def test_prefill_all_keys_equal_past_shared_memory():
+    """The same ties in rows longer than 16384 tokens: the boundary bin, then its second-round
+    sub-bin, overflow shared memory, and the row is selected by radix passes over its scores
+    (sampled rows of every block checked)."""
+    w = wl.scaled(wl.WORKLOADS["prefill"], "pf_ties2", lengths=(20000,), prefill_block=4096, k=256, C=20000)
+    pr = _run(w, full_rows=False, row_sample=3, same_keys=True)
+    sel = pr.sel_idx[:pr.R].cpu().numpy()
+    assert np.array_equal(sel[-1], np.arange(256, dtype=np.int32))
+    assert int(pr.stats[L.STAT_TOPK_FALLBACK].item()) > 0
 
 
