@@ -36,7 +36,7 @@ from . import _lib as L
 class DecodeLayer:
     def __init__(self, tok_off, k8: torch.Tensor, ks: torch.Tensor, k: int, C: int,
                  host_pool: torch.Tensor, alpha: float = 0.5, predictor: bool = True,
-                 early_cap: int = -1, groups: int | None = None, first_share: float = 0.5,
+                 early_cap: int = -1, groups: int | None = None, first_share: float | None = None,
                  resolved: bool = True, hold_early: bool = False, attention: bool = False,
                  mla_scale: float = 1.0 / math.sqrt(192.0), tok_end=None, cross_layer: bool = False,
                  pool_slots: int = 0, cands: bool | None = None, cand_cap: int = L.CAND_CAP, lazy: bool = False,
@@ -95,8 +95,11 @@ class DecodeLayer:
             groups = (4 if self.B >= 16 else 2) if (self.predictor and self.B >= 2) else 1
         groups = max(1, min(int(groups), self.B))
         bounds = [self.B * g // groups for g in range(groups + 1)]
-        if groups == 2:  # the second group's scores gate top-k; a smaller second group starts it sooner
-            bounds[1] = min(self.B - 1, max(1, round(self.B * first_share)))
+        if first_share is not None and groups >= 2:
+            # the first group's share of the requests (the rest split evenly): a smaller first group
+            # starts the host link sooner
+            f = min(self.B - (groups - 1), max(1, round(self.B * first_share)))
+            bounds = [0] + [f + (self.B - f) * g // (groups - 1) for g in range(groups)]
         self.groups = [(bounds[g], bounds[g + 1]) for g in range(groups) if bounds[g + 1] > bounds[g]]
         # each group's above-threshold words: the groups' word ranges may overlap
         self.above_g = [torch.zeros(max(L.above_words(b1 - b0, self.n_tokens), 1), **i32)

@@ -167,18 +167,39 @@ class QueryStream:
         return out
 
 
+def _huge_page_bytes() -> int:
+    """The transparent huge page size of this kernel (0 when it has none)."""
+    try:
+        with open("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size") as f:
+            return int(f.read().strip())
+    except (OSError, ValueError):
+        return 0
+
+
 def pinned_empty(shape, dtype) -> torch.Tensor:
     """An uninitialised host tensor whose pages are locked and mapped for the GPU
     (cudaHostRegister), sized exactly: torch's pinned allocator rounds every
     block up to a power of two, which for a multi-GB host pool nearly doubles
-    the locked memory.  The bytes belong to a numpy buffer that the tensor's
-    storage keeps alive (views included); the registration is dropped just
-    before that buffer is freed."""
+    the locked memory.  A buffer of at least one transparent huge page is a
+    private anonymous mapping advised for huge pages (aligned to their size), so
+    that the GPU's random row reads over the host link touch few page
+    translations; smaller ones are a numpy buffer.  The tensor's storage keeps
+    the bytes alive (views included); the registration is dropped just before
+    they are freed."""
+    import mmap
     import weakref
     nbytes = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
     if nbytes == 0:
         return torch.empty(shape, dtype=dtype, pin_memory=True)
-    buf = np.empty(nbytes, np.uint8)
+    hp = _huge_page_bytes()
+    if hp and nbytes >= hp and hasattr(mmap, "MADV_HUGEPAGE"):
+        region = mmap.mmap(-1, nbytes + hp, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+        whole = np.frombuffer(region, dtype=np.uint8)
+        off = (-whole.ctypes.data) % hp
+        region.madvise(mmap.MADV_HUGEPAGE, off, len(region) - off)
+        buf = whole[off:off + nbytes]
+    else:
+        buf = np.empty(nbytes, np.uint8)
     rt = torch.cuda.cudart()
     rc = rt.cudaHostRegister(buf.ctypes.data, nbytes, 3)   # portable | mapped
     if int(rc) != 0:

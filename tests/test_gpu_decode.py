@@ -227,6 +227,10 @@ def test_shared_pool_large_predictor_off_and_cap():
     from tests._parity import run_pool
     w = wl.scaled(wl.WORKLOADS["batch"], "pool_big", B=2, lengths=(70000, 65000), k=2048, C=4096)
     run_pool(w, steps=3, pool=140032, predictor=False, graph=False)
+    # more than 4096 selections (the walking step's wider per-thread chunks), predictor on
+    w3 = wl.scaled(wl.WORKLOADS["batch"], "pool_big3", B=3, lengths=(70000, 65000, 30000), k=2048, C=4096)
+    rep = run_pool(w3, steps=4, pool=140032)
+    assert sum(rep["early"]) > 0
     w2 = wl.scaled(wl.WORKLOADS["batch"], "pool_cap", B=2, lengths=(8000, 5000), k=256, C=1024)
     run_pool(w2, steps=4, pool=1024, cap=100)
 
