@@ -69,6 +69,8 @@ def parse_args(argv=None):
                    help="request groups of the decode step (default: the layer's choice)")
     p.add_argument("--lookup-in", choices=["topk", "cache-step"], default="topk",
                    help="where the selected tokens' slots are looked up (top-k's slices or the cache step)")
+    p.add_argument("--early-cap", type=int, default=-1,
+                   help="early-fetch cap per request and layer (-1: only the free slots cap it)")
     p.add_argument("--hold-early", action="store_true",
                    help="the held-slot variant of the cache step (the late recall need not wait for the early copy)")
     p.add_argument("--part", choices=["step", "mla", "append", "layers", "pool", "prefill", "kernels"], default="step",
@@ -338,6 +340,7 @@ def run_ours(args):
     kw = {} if args.first_share is None else {"first_share": args.first_share}
     kw["resolved"] = args.lookup_in == "topk"
     kw["hold_early"] = bool(args.hold_early)
+    kw["early_cap"] = int(args.early_cap)
     lays = [DecodeLayer(off, keys[l][0], keys[l][1], w.k, w.C, hosts[l], predictor=w.predictor, device=dev,
                         groups=args.groups, **kw) for l in range(w.L)]
     stack = DecodeStack(lays)
@@ -525,7 +528,8 @@ def run_ours(args):
         "config": dict(workload_config(w), request_groups=len(lays[0].groups),
                        state=f"cache primed by {P} decode steps from empty (untimed, before the warm-up)",
                        slot_lookup="top-k" if lays[0].resolved else "cache step",
-                       early_slots="held through the miss placement" if lays[0].hold_early else "free for misses"),
+                       early_slots="held through the miss placement" if lays[0].hold_early else "free for misses",
+                       early_cap=lays[0].early_cap),
         "roofline": {"kernel": "score_kernel (echo_index_scores), one layer of the batch per launch",
                      "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -558,6 +562,8 @@ def run_ours(args):
                    "early_fetch_alone_gbs": round(early_alone_gbs, 1),
                    "host_link_gbs_in_step": round(link_gbs, 1), "h2d_probes_gbs": probes,
                    "recall_frac_of_h2d": round(link_gbs / link_peak, 4) if link_peak else None,
+                   "host_pool_huge_page_share": [round(wl.huge_page_share(h), 3) for h in hosts],
+                   "step_ms": [round(x, 3) for x in step_ms],
                    "step_ms_min": round(min(step_ms), 4), "step_ms_median": round(statistics.median(step_ms), 4),
                    "e2e_ms_median": round(statistics.median(e2e_ms), 4)},
     }

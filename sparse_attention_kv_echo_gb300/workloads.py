@@ -208,6 +208,27 @@ def pinned_empty(shape, dtype) -> torch.Tensor:
     return torch.from_numpy(buf).view(dtype).view(shape)
 
 
+def huge_page_share(t: torch.Tensor) -> float:
+    """Share of a host tensor's bytes that sit on transparent huge pages (from /proc/self/smaps;
+    -1 when that cannot be read)."""
+    lo = t.data_ptr()
+    hi = lo + t.numel() * t.element_size()
+    try:
+        huge = 0
+        with open("/proc/self/smaps") as f:
+            start = end = None
+            for line in f:
+                head = line.split()
+                if "-" in head[0] and len(head) > 4 and not head[0].endswith(":"):
+                    a, b = head[0].split("-")
+                    start, end = int(a, 16), int(b, 16)
+                elif head[0] == "AnonHugePages:" and start is not None and start < hi and end > lo:
+                    huge += int(head[1]) * 1024
+        return min(1.0, huge / max(1, hi - lo))
+    except (OSError, ValueError, IndexError):
+        return -1.0
+
+
 def make_host_pool(w: Workload, layer: int, device="cpu", pin: bool = False, rows: int | None = None) -> torch.Tensor:
     """Host KV pool [sum N, 576] bf16 ~ N(0,1) of one layer (pinned when pin=True).
 
