@@ -170,10 +170,45 @@ class QueryStream:
 def _huge_page_bytes() -> int:
     """The transparent huge page size of this kernel (0 when it has none)."""
     try:
+        with open("/sys/kernel/mm/transparent_hugepage/enabled") as f:
+            if "[never]" in f.read():
+                return 0
         with open("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size") as f:
             return int(f.read().strip())
     except (OSError, ValueError):
         return 0
+
+
+def _madvise_collapse(addr: int, length: int) -> None:
+    import ctypes
+    if length <= 0:
+        return
+    try:
+        libc = ctypes.CDLL(None, use_errno=True)
+        libc.madvise.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int]
+        libc.madvise(ctypes.c_void_p(addr), ctypes.c_size_t(length), 25)   # MADV_COLLAPSE
+    except (OSError, AttributeError):
+        pass
+
+
+def _huge_mapping(nbytes: int, hp: int):
+    """A private anonymous mapping of nbytes, aligned to the huge page size hp and advised for
+    huge pages, its pages faulted in; returns (mapping, byte view)."""
+    import mmap
+    region = mmap.mmap(-1, nbytes + hp, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+    whole = np.frombuffer(region, dtype=np.uint8)
+    off = (-whole.ctypes.data) % hp
+    region.madvise(mmap.MADV_HUGEPAGE, off, len(region) - off)
+    buf = whole[off:off + nbytes]
+    # fault the pages in, then ask the kernel to collapse what did not come as huge pages
+    # (MADV_COLLAPSE, Linux 6.1+; a refusal leaves the small pages in place)
+    buf[::mmap.PAGESIZE] = 0
+    _madvise_collapse(buf.ctypes.data, nbytes - nbytes % hp)
+    # then keep the kernel's background collapsing away from these pages: once registered they
+    # cannot move, and repeated attempts on them only disturb the GPU's host reads
+    if hasattr(mmap, "MADV_NOHUGEPAGE"):
+        region.madvise(mmap.MADV_NOHUGEPAGE, off, len(region) - off)
+    return region, buf
 
 
 def pinned_empty(shape, dtype) -> torch.Tensor:
@@ -193,11 +228,17 @@ def pinned_empty(shape, dtype) -> torch.Tensor:
         return torch.empty(shape, dtype=dtype, pin_memory=True)
     hp = _huge_page_bytes()
     if hp and nbytes >= hp and hasattr(mmap, "MADV_HUGEPAGE"):
-        region = mmap.mmap(-1, nbytes + hp, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
-        whole = np.frombuffer(region, dtype=np.uint8)
-        off = (-whole.ctypes.data) % hp
-        region.madvise(mmap.MADV_HUGEPAGE, off, len(region) - off)
-        buf = whole[off:off + nbytes]
+        # After other work has fragmented memory a mapping may get only part of its huge pages;
+        # each try compacts memory further, so up to three tries, keeping the best
+        best, best_share = None, -1.0
+        for _ in range(3):
+            region, buf = _huge_mapping(nbytes, hp)
+            share = _huge_share_range(buf.ctypes.data, buf.ctypes.data + nbytes)
+            if share > best_share:
+                best, best_share = (region, buf), share
+            if share >= 1.0:
+                break
+        region, buf = best
     else:
         buf = np.empty(nbytes, np.uint8)
     rt = torch.cuda.cudart()
@@ -208,11 +249,9 @@ def pinned_empty(shape, dtype) -> torch.Tensor:
     return torch.from_numpy(buf).view(dtype).view(shape)
 
 
-def huge_page_share(t: torch.Tensor) -> float:
-    """Share of a host tensor's bytes that sit on transparent huge pages (from /proc/self/smaps;
-    -1 when that cannot be read)."""
-    lo = t.data_ptr()
-    hi = lo + t.numel() * t.element_size()
+def _huge_share_range(lo: int, hi: int) -> float:
+    """Share of the bytes [lo, hi) of this process that sit on transparent huge pages (from
+    /proc/self/smaps; -1 when that cannot be read)."""
     try:
         huge = 0
         with open("/proc/self/smaps") as f:
@@ -227,6 +266,12 @@ def huge_page_share(t: torch.Tensor) -> float:
         return min(1.0, huge / max(1, hi - lo))
     except (OSError, ValueError, IndexError):
         return -1.0
+
+
+def huge_page_share(t: torch.Tensor) -> float:
+    """Share of a host tensor's bytes that sit on transparent huge pages (-1: unknown)."""
+    lo = t.data_ptr()
+    return _huge_share_range(lo, lo + t.numel() * t.element_size())
 
 
 def make_host_pool(w: Workload, layer: int, device="cpu", pin: bool = False, rows: int | None = None) -> torch.Tensor:
