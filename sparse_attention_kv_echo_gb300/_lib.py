@@ -25,7 +25,7 @@ HEADS, DIM, MAX_REQUESTS = 64, 128, 4096
 CACHE_HOLD_EARLY, CACHE_LAZY = 1, 2   # echo_cache_step flags
 TOPK_CACHED_MAX_SLOTS = 32768  # C limit of echo_topk_select_cached and of the cached form of echo_topk_select_cands
 CAND_CAP = 16384             # candidate-list entries per request top-k keeps in shared memory
-EARLY_FETCH_BLOCKS = 32      # CTAs of the early-fetch and late-recall kernels
+EARLY_FETCH_BLOCKS = 24      # CTAs of the early-fetch and late-recall kernels
 
 EXPORTS = ("echo_above_words", "echo_append_tokens", "echo_cache_step", "echo_cache_step_resolved",
            "echo_debug_stall_epilogue", "echo_device_sm_count",

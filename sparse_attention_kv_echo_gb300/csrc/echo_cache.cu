@@ -407,7 +407,7 @@ __global__ void __launch_bounds__(kCT) cache_step_kernel(const int64_t* __restri
 }
 
 constexpr int kRecallThreads = 512;
-constexpr int kRecallBlocks = 32;
+constexpr int kRecallBlocks = 24;
 constexpr int kRows = 2;        // rows per warp in flight (4 measured: the host reads queue up and every
                                 // kernel of the step slowed about tenfold)
 constexpr int kStage = 4096;    // early (token, slot) pairs staged in shared memory per round
