@@ -628,8 +628,8 @@ cudaError_t launch_recall(int B, const int64_t* tok_off, const int64_t* tok_end,
                           int64_t row_bytes, int32_t* status, cudaStream_t s, bool programmatic) {
     const int sms = sm_count();
     if (sms <= 0) return cudaErrorInvalidDevice;
-    // A few large blocks: the host link, not the SMs, bounds the copy (32 x 16
-    // warps x 2 rows keep ~1.2 MB of host reads in flight).  Loads that wait on
+    // A few large blocks: the host link, not the SMs, bounds the copy (24 x 16
+    // warps x 2 rows keep ~0.9 MB of host reads in flight).  Loads that wait on
     // the host link slow every other kernel that shares an SM with them, so the
     // copy stays on few SMs, and a block this size (512 threads x ~50 registers)
     // cannot share an SM with a 1024-thread top-k CTA, which then runs elsewhere.
