@@ -146,6 +146,26 @@ def score_kernel_traffic(profile: str):
     return None
 
 
+def vmstat(keys=("pgmigrate_success", "compact_migrate_scanned", "compact_stall", "thp_fault_fallback",
+                  "thp_collapse_alloc_failed")) -> dict:
+    """The host kernel's page-migration and compaction counters (/proc/vmstat; {} when unreadable):
+    the GPU's reads of page-locked host memory slow down while the kernel moves pages."""
+    out = {}
+    try:
+        with open("/proc/vmstat") as f:
+            for line in f:
+                k, v = line.split()
+                if k in keys:
+                    out[k] = int(v)
+    except (OSError, ValueError):
+        pass
+    return out
+
+
+def vm_delta(a: dict, b: dict) -> dict:
+    return {k: b[k] - a[k] for k in a if k in b}
+
+
 class ClockSampler:
     """nvidia-smi sampling of the GPU's clocks and throttle reasons while running."""
 
@@ -413,7 +433,9 @@ def run_ours(args):
     stats0 = []      # the layers' counters as the timed steps start
     sampler = ClockSampler(bus)
     sampler.start()
+    vm0 = vmstat()
     step_ms = timed(lambda t: graphs[t % S].replay(), at_start=lambda: stats0.extend(lay.stats.clone() for lay in lays))
+    vm_timed = vm_delta(vm0, vmstat())
     clocks = sampler.stop()
     elapsed_s = sum(step_ms) / 1e3
     status = 0
@@ -435,7 +457,9 @@ def run_ours(args):
         with torch.cuda.stream(main):
             host_graphs[i].replay()
     reset()
+    vm1 = vmstat()
     e2e_ms = timed(lambda t: host_graphs[t % S].replay())
+    vm_e2e = vm_delta(vm1, vmstat())
     e2e_value, _ = combine_over_ranks(sum(e2e_ms) / 1e3, args.steps, world, reduce_max)
     h2d_bytes = q_host[0].numel() * 4 + w_host.numel() * 4
     d2h_bytes = slot_host.numel() * 4 + kth_host.numel() * 4
@@ -564,6 +588,7 @@ def run_ours(args):
                    "recall_frac_of_h2d": round(link_gbs / link_peak, 4) if link_peak else None,
                    "host_pool_huge_page_share": [round(wl.huge_page_share(h), 3) for h in hosts],
                    "step_ms": [round(x, 3) for x in step_ms],
+                   "host_vmstat_during_timed": vm_timed, "host_vmstat_during_e2e": vm_e2e,
                    "step_ms_min": round(min(step_ms), 4), "step_ms_median": round(statistics.median(step_ms), 4),
                    "e2e_ms_median": round(statistics.median(e2e_ms), 4)},
     }

@@ -228,17 +228,18 @@ def pinned_empty(shape, dtype) -> torch.Tensor:
         return torch.empty(shape, dtype=dtype, pin_memory=True)
     hp = _huge_page_bytes()
     if hp and nbytes >= hp and hasattr(mmap, "MADV_HUGEPAGE"):
-        # After other work has fragmented memory a mapping may get only part of its huge pages;
-        # each try compacts memory further, so up to three tries, keeping the best
-        best, best_share = None, -1.0
-        for _ in range(3):
+        # After other work has fragmented memory a mapping may get only part of its huge pages
+        # (and the GPU's host reads from the rest are slow and easily congested).  Each try
+        # compacts memory further; the earlier tries stay mapped until the end so that a new
+        # one cannot get their small pages back: up to six tries, keeping the best
+        tries = []
+        for _ in range(6):
             region, buf = _huge_mapping(nbytes, hp)
-            share = _huge_share_range(buf.ctypes.data, buf.ctypes.data + nbytes)
-            if share > best_share:
-                best, best_share = (region, buf), share
-            if share >= 1.0:
+            tries.append((_huge_share_range(buf.ctypes.data, buf.ctypes.data + nbytes), region, buf))
+            if tries[-1][0] >= 1.0:
                 break
-        region, buf = best
+        _, region, buf = max(tries, key=lambda t: t[0])
+        del tries
     else:
         buf = np.empty(nbytes, np.uint8)
     rt = torch.cuda.cudart()
