@@ -178,7 +178,10 @@ extern "C" int echo_prefill_block(int R, int64_t row0, int64_t n_keys, const flo
                                                 n_keys, kth, R, theta_hat, alpha);
     ECHO_CUDA_OK(cudaGetLastError());
     if (!cache) return ECHO_OK;
-    return enqueue_cache_step(1, p.tok_off2, nullptr, n_keys, union_list, static_cast<int>(W), nullptr, 0, cache, sel_slot,
+    // the union holds at most the n = row0 + R tokens the block's rows see, the rest of the list is
+    // padding: the cache step walks the first n entries and the padding's slots are set to -1 here
+    if (W > n) ECHO_CUDA_OK(cudaMemsetAsync(sel_slot + n, 0xFF, static_cast<size_t>(W - n) * sizeof(int32_t), stream));
+    return enqueue_cache_step(1, p.tok_off2, nullptr, n_keys, union_list, static_cast<int>(n), nullptr, 0, cache, sel_slot,
                               status, stats, stream, copy_stream, false, false, false);
 }
 
