@@ -69,6 +69,8 @@ def parse_args(argv=None):
                    help="request groups of the decode step (default: the layer's choice)")
     p.add_argument("--lookup-in", choices=["topk", "cache-step"], default="topk",
                    help="where the selected tokens' slots are looked up (top-k's slices or the cache step)")
+    p.add_argument("--e2e-first", action="store_true",
+                   help="time the end-to-end pass before the device-resident one")
     p.add_argument("--early-cap", type=int, default=-1,
                    help="early-fetch cap per request and layer (-1: only the free slots cap it)")
     p.add_argument("--hold-early", action="store_true",
@@ -429,41 +431,60 @@ def run_ours(args):
         torch.cuda.synchronize()
         return [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
-    # ---------------- timed region: graph replays, inputs resident in HBM
-    stats0 = []      # the layers' counters as the timed steps start
-    sampler = ClockSampler(bus)
-    sampler.start()
-    vm0 = vmstat()
-    step_ms = timed(lambda t: graphs[t % S].replay(), at_start=lambda: stats0.extend(lay.stats.clone() for lay in lays))
-    vm_timed = vm_delta(vm0, vmstat())
-    clocks = sampler.stop()
-    elapsed_s = sum(step_ms) / 1e3
-    status = 0
-    for lay in lays:
-        status |= int(lay.status.item())
-    stats = sum((lay.stats - s0).cpu().numpy().astype(np.int64) for lay, s0 in zip(lays, stats0))
-    boundary_max = max(int(lay.stats[L.STAT_BOUNDARY_MAX].item()) for lay in lays)
-    value, slowest = combine_over_ranks(elapsed_s, args.steps, world, reduce_max)
+    def device_pass():
+        reset()
+        # timed region: graph replays, inputs resident in HBM
+        stats0 = []      # the layers' counters as the timed steps start
+        sampler = ClockSampler(bus)
+        sampler.start()
+        vm0 = vmstat()
+        step_ms = timed(lambda t: graphs[t % S].replay(), at_start=lambda: stats0.extend(lay.stats.clone() for lay in lays))
+        vm_timed = vm_delta(vm0, vmstat())
+        clocks = sampler.stop()
+        elapsed_s = sum(step_ms) / 1e3
+        status = 0
+        for lay in lays:
+            status |= int(lay.status.item())
+        stats = sum((lay.stats - s0).cpu().numpy().astype(np.int64) for lay, s0 in zip(lays, stats0))
+        boundary_max = max(int(lay.stats[L.STAT_BOUNDARY_MAX].item()) for lay in lays)
+        value, slowest = combine_over_ranks(elapsed_s, args.steps, world, reduce_max)
 
-    # ---------------- end to end through the public API with host buffers
-    # one graph per step: each layer's quantiser reads the step's queries from pinned memory, each
-    # layer's slots and k-th scores are written to pinned memory (DecodeStack.capture_host_step)
-    q_host = q_all.cpu().pin_memory()
-    w_host = torch.stack(wts).cpu().pin_memory()
-    slot_host = torch.empty((nl,) + tuple(lays[0].sel_slot.shape), dtype=torch.int32).pin_memory()
-    kth_host = torch.empty((nl,) + tuple(lays[0].kth.shape), dtype=torch.float32).pin_memory()
-    host_graphs = [stack.capture_host_step(q_host[i], w_host, slot_host, kth_host, stream=main) for i in range(S)]
-    for i in range(S):
-        with torch.cuda.stream(main):
-            host_graphs[i].replay()
-    reset()
-    vm1 = vmstat()
-    e2e_ms = timed(lambda t: host_graphs[t % S].replay())
-    vm_e2e = vm_delta(vm1, vmstat())
-    e2e_value, _ = combine_over_ranks(sum(e2e_ms) / 1e3, args.steps, world, reduce_max)
-    h2d_bytes = q_host[0].numel() * 4 + w_host.numel() * 4
-    d2h_bytes = slot_host.numel() * 4 + kth_host.numel() * 4
-    del host_graphs
+        return dict(step_ms=step_ms, clocks=clocks, vm_timed=vm_timed, elapsed_s=elapsed_s, status=status,
+                    stats=stats, boundary_max=boundary_max, value=value, slowest=slowest)
+
+    def e2e_pass():
+        # end to end through the public API with host buffers
+        # one graph per step: each layer's quantiser reads the step's queries from pinned memory, each
+        # layer's slots and k-th scores are written to pinned memory (DecodeStack.capture_host_step)
+        q_host = q_all.cpu().pin_memory()
+        w_host = torch.stack(wts).cpu().pin_memory()
+        slot_host = torch.empty((nl,) + tuple(lays[0].sel_slot.shape), dtype=torch.int32).pin_memory()
+        kth_host = torch.empty((nl,) + tuple(lays[0].kth.shape), dtype=torch.float32).pin_memory()
+        host_graphs = [stack.capture_host_step(q_host[i], w_host, slot_host, kth_host, stream=main) for i in range(S)]
+        for i in range(S):
+            with torch.cuda.stream(main):
+                host_graphs[i].replay()
+        reset()
+        vm1 = vmstat()
+        e2e_ms = timed(lambda t: host_graphs[t % S].replay())
+        vm_e2e = vm_delta(vm1, vmstat())
+        e2e_value, _ = combine_over_ranks(sum(e2e_ms) / 1e3, args.steps, world, reduce_max)
+        h2d_bytes = q_host[0].numel() * 4 + w_host.numel() * 4
+        d2h_bytes = slot_host.numel() * 4 + kth_host.numel() * 4
+        del host_graphs
+        return dict(e2e_ms=e2e_ms, e2e_value=e2e_value, vm_e2e=vm_e2e, h2d_bytes=h2d_bytes, d2h_bytes=d2h_bytes)
+
+    # ---------------- the two timed passes (the end-to-end one first with --e2e-first)
+    if args.e2e_first:
+        r_e2e = e2e_pass()
+        r_dev = device_pass()
+    else:
+        r_dev = device_pass()
+        r_e2e = e2e_pass()
+    step_ms, clocks, vm_timed, elapsed_s, status = (r_dev[k] for k in ("step_ms", "clocks", "vm_timed", "elapsed_s", "status"))
+    stats, boundary_max, value, slowest = (r_dev[k] for k in ("stats", "boundary_max", "value", "slowest"))
+    e2e_ms, e2e_value, vm_e2e, h2d_bytes, d2h_bytes = (r_e2e[k] for k in ("e2e_ms", "e2e_value", "vm_e2e", "h2d_bytes", "d2h_bytes"))
+
 
     # ---------------- per-call pass on layer 0: each call timed alone with events (L2 flushed)
     lay = lays[0]
