@@ -265,8 +265,8 @@ int echo_topk_select(int B, const int64_t* tok_off, const int64_t* tok_end, int6
  * ECHO_ST_NOSLOT).  Holding, the recall may run before echo_early_fetch's
  * copy ends.  flags: 0, ECHO_CACHE_HOLD_EARLY or ECHO_CACHE_LAZY (other bits,
  * or both: ECHO_EINVAL).
- * Lazy-reuse eviction (ECHO_CACHE_LAZY; a variant -- the survey's reading of
- * "freed slots keep their token until overwritten" -- not the contract): a
+ * Lazy-reuse eviction (ECHO_CACHE_LAZY; a variant -- a reading of "freed slots
+ * keep their token until overwritten" -- not the contract): a
  * token freed in step 1 keeps its bytes and both table entries (a ghost: its
  * slot is free, the token still maps to it) until its slot is handed to
  * another token, which drops it from the tables; every early token of step 0

@@ -466,8 +466,8 @@ int orc_cache_step(int64_t n, int C, int32_t* tok2slot, int32_t* slot2tok, const
 namespace {
 
 // ---- lazy-reuse eviction (a variant of the cache step) ---------------------
-// READING of the survey's alternative to "resident == selected after every
-// step": a slot freed at a step keeps its bytes and both table entries until
+// READING of the alternative to "resident == selected after every step"
+// (freed slots keep their token until overwritten): a slot freed at a step keeps its bytes and both table entries until
 // the slot is handed to another token.  Its token is then a ghost: present in
 // the cache, not resident.  A selected ghost is a hit: it is resident in its
 // slot again, with no copy.  Handing a slot to a token drops the ghost in it.
